@@ -1,0 +1,257 @@
+/*
+ * dkv.h — C ABI of libdkv: differentiated KV compaction and mixed-precision
+ * paged decode attention for one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow "DiffKV: Differentiated Memory Management for Large
+ * Language Models with Parallel KV Compaction" (SOSP'25, arXiv 2412.03131).
+ * Section names below refer to that page:
+ *   [Bkg-Q]    Background — per-vector quantization Q = round((X - z)/s),
+ *              X^ = s*Q + z, applied to every key and value vector.
+ *   [Bkg-Attn] Background — the attention equation (softmax(q.k/sqrt(d)) v).
+ *   [Pol-P]    Compaction policy — prompt-phase logic (importance = mean
+ *              attention a token receives; GQA heads combined with max;
+ *              recent window W always high precision; thresholds a_h/N, a_l/N).
+ *   [Pol-G]    Compaction policy — generation-phase logic and algorithm flow
+ *              (candidate t_c, victim t_v, demote or prune).
+ *   [Mem-PC]   Memory management — parallel KV compaction (plan / coordinate,
+ *              parallel prefix sum).
+ *   [Mem-UP]   Memory management — unified pages (six segments).
+ *   [Mem-FL]   Memory management — circular free page list (start pointer
+ *              allocates, end pointer reclaims, both wrap).
+ *   [Mem-BT]   Memory management — bidirectional page table (high-precision
+ *              pages grow from the left, low-precision from the right).
+ *   [Mem-Fig6] Memory management — prompt-phase workflow, Figure 6.
+ *   [Mem-Gen]  Memory management — generation-phase workflow.
+ *   [Impl-Kern] System implementation — custom attention kernel (hi pages
+ *              first, then lo pages; key / value layouts; sequence split).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Return 0 on success, a negative DKV_ERR_* code otherwise.
+ *  - "host" pointers are read before the call returns and may be reused at
+ *    once. "device" pointers must stay valid until the work queued on
+ *    `stream` (a cudaStream_t passed as void*, NULL = legacy default stream)
+ *    completes. The caller owns every input and output buffer.
+ *  - All calls on one pool must be ordered on one stream (or synchronised by
+ *    the caller). compact_step, decode_attention and free_request never
+ *    synchronise the host; argument and request-state errors are detected on
+ *    the host and returned at once with nothing queued.
+ *  - Data-dependent failures (free list exhausted, page table full) are
+ *    detected on the device before anything is written: the whole call
+ *    becomes a no-op and the code latches in the pool's sticky status word.
+ *    While the sticky status is non-zero every later call is a device no-op;
+ *    dkv_pool_status reads it and dkv_pool_clear_error resets it.
+ *
+ * Unified page format  [Mem-UP]
+ * -----------------------------
+ * Two tiers, fixed bit widths: hi = K8V4 (8-bit key codes, 4-bit value
+ * codes), lo = K4V2 [Pol-P]. head_dim d = 128. A page holds T tokens of one
+ * tier; T is the largest multiple of g = 8/vbits (tokens sharing a value
+ * byte: 2 for hi, 4 for lo) whose six segments fit in page_bytes. For
+ * page_bytes = 4096: T_hi = 18, T_lo = 36. Segments, in order, each starting
+ * on a 16-byte boundary, slot t in [0, T):
+ *   1. K codes  T rows of d*kbits/8 bytes (128 B hi, 64 B lo).
+ *               8-bit: byte i = code of feature i.
+ *               4-bit: byte i bits 0-3 = feature 2i, bits 4-7 = feature 2i+1.
+ *   2. V codes  T/g rows of 128 bytes; row u holds slots u*g .. u*g+g-1.
+ *               A row is 32 little-endian 32-bit words; word w covers
+ *               features 4w..4w+3. For feature 4w+i, slot u*g+e:
+ *               4-bit (g=2): bits [16e + 4i, +4)
+ *               2-bit (g=4): bits [16(e&1) + 4i + 2(e>>1), +2)
+ *   3. K meta   T x {fp16 scale, fp16 zero} (4 bytes per slot).
+ *   4. V meta   same for values.
+ *   5. score    T x fp32 accumulated attention score S.
+ *   6. position T x int32 token position in the request.
+ * Codes [Bkg-Q], per token vector x (128 values, fp16 inputs widened to
+ * fp32), L = 2^bits - 1, all fp32 arithmetic correctly rounded, no fused
+ * contraction unless stated:
+ *   mn = min x, mx = max x; s = half(fdiv(fsub(mx, mn), L)); z = half(mn)
+ *   s == 0 -> every code 0; else inv = fdiv(1, s) and
+ *   code_i = clamp(rint_even(fmul(fsub(x_i, z), inv)), 0, L)
+ *   dequantised value = fma(s, code, z) (one rounding).
+ *   half() is IEEE binary16 round-to-nearest-even. Re-quantising a hi token to
+ *   lo applies the same steps to its dequantised hi values.
+ *
+ * Free list and page table  [Mem-FL] [Mem-BT]
+ * -------------------------------------------
+ * The free list is an int32 array of n_pages page IDs with two monotone
+ * 64-bit counters start and end; free = end - start, entry = list[c mod P].
+ * Initially list[i] = i, start = 0, end = n_pages. Allocation consumes from
+ * start, reclaim appends at end. One table row per (layer, request slot, KV
+ * head) of L_e = ceil(max_seq_len / T_hi) + 1 int32 entries: hi page k at
+ * entry k, lo page k at entry L_e-1-k, unused entries -1. Hi slot s lives on
+ * hi page s / T_hi at slot s % T_hi; lo slot s on lo page s / T_lo.
+ */
+#ifndef DKV_H
+#define DKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes ---------------------------------------------------- */
+#define DKV_OK               0
+#define DKV_ERR_ARG         -1  /* bad argument (NULL, out of range, bad config) */
+#define DKV_ERR_CUDA        -2  /* a CUDA runtime call failed */
+#define DKV_ERR_STATE       -3  /* request slot in the wrong state for the call */
+#define DKV_ERR_NO_PAGES    -4  /* free list holds fewer pages than the call needs */
+#define DKV_ERR_TABLE_FULL  -5  /* a head needs more pages than its grant / row */
+#define DKV_ERR_TIMEOUT     -6  /* a bounded device wait gave up */
+#define DKV_ERR_CHECK       -7  /* a device-side consistency check failed */
+#define DKV_ERR_UNSUPPORTED -8  /* configuration outside what the kernels support */
+
+/* ---- modes ------------------------------------------------------------ */
+#define DKV_PROMPT 0  /* compact a whole prompt            [Pol-P] [Mem-Fig6] */
+#define DKV_DECODE 1  /* append one token, compact one      [Pol-G] [Mem-Gen]  */
+
+/* ---- configuration ------------------------------------------------------ */
+typedef struct dkv_config {
+  int32_t n_layers;            /* layers sharing the page pool                 */
+  int32_t n_kv_heads;          /* Hkv                                          */
+  int32_t group_size;          /* G = query heads per KV head, 1..8            */
+  int32_t head_dim;            /* must be 128                                  */
+  int32_t page_bytes;          /* unified page size, multiple of 16, e.g. 4096 */
+  int32_t n_pages;             /* P, pages in the pool                         */
+  int32_t max_requests;        /* request slots 0..max_requests-1              */
+  int32_t max_seq_len;         /* longest request (prompt + generated)         */
+  int32_t tokens_per_hi_page;  /* 0 = largest that fits; else a multiple of 2  */
+  int32_t tokens_per_lo_page;  /* 0 = largest that fits; else a multiple of 4  */
+  int32_t lo_enabled;          /* 0: no K4V2 tier; survivors are stored hi     */
+  float   alpha_h;             /* hi threshold alpha_h / N                     */
+  float   alpha_l;             /* lo threshold alpha_l / N                     */
+  int32_t recent_window;       /* W: the last W tokens are always hi, >= 0     */
+  int32_t obs_window;          /* observation queries per prompt; must be 32   */
+  int32_t prompt_grant_slack;  /* extra pages in each head's all-hi grant, >=0 */
+  int32_t reclaim_in_decode;   /* 1: free a tier's emptied tail page in DECODE */
+} dkv_config;
+
+typedef struct dkv_pool dkv_pool;   /* opaque; owns every device structure */
+
+/* Pool geometry derived from the config (valid after dkv_pool_create). */
+typedef struct dkv_geometry {
+  int32_t t_hi, t_lo;              /* tokens per hi / lo page              */
+  int32_t table_len;               /* L_e                                  */
+  int32_t hi_off[6];               /* segment byte offsets, hi page        */
+  int32_t lo_off[6];               /* segment byte offsets, lo page        */
+  int32_t hi_used, lo_used;        /* bytes used by the six segments       */
+} dkv_geometry;
+
+/* Sticky status and pool-wide counters (host struct). */
+typedef struct dkv_status {
+  int32_t error;        /* first data-dependent error since the last clear, 0 if none */
+  int32_t error_info;   /* head or layer index associated with the error, -1 if none  */
+  int64_t list_start;   /* free-list allocation counter                                */
+  int64_t list_end;     /* free-list reclaim counter                                   */
+  int64_t free_pages;   /* list_end - list_start                                       */
+  int64_t hi_tokens;    /* stored hi tokens over all layers, requests and heads        */
+  int64_t lo_tokens;    /* stored lo tokens                                            */
+  int64_t hi_pages;     /* pages held as hi                                            */
+  int64_t lo_pages;     /* pages held as lo                                            */
+} dkv_status;
+
+/* Host snapshot of the device state; every pointer may be NULL to skip it.
+ * Sizes: pages  n_pages*page_bytes bytes; free_list n_pages int32;
+ *        table  n_layers*max_requests*n_kv_heads*table_len int32;
+ *        head_counts n_layers*max_requests*n_kv_heads*4 int32
+ *                    {hi tokens, lo tokens, hi pages, lo pages};
+ *        req_state   n_layers*max_requests*4 int32 {active, N0, N, updates};
+ *        pointers    2 int64 {start, end}. */
+typedef struct dkv_snapshot {
+  uint8_t* pages;
+  int32_t* free_list;
+  int32_t* table;
+  int32_t* head_counts;
+  int32_t* req_state;
+  int64_t* pointers;
+} dkv_snapshot;
+
+/* Create a pool on `cuda_device`: allocates the pages, the free list, page
+ * tables, counters, scratch and the status word, all on the device. The
+ * pool's memory is fixed for its lifetime. Errors: DKV_ERR_ARG for an invalid
+ * config, DKV_ERR_UNSUPPORTED (head_dim != 128, G outside 1..8,
+ * obs_window != 32), DKV_ERR_CUDA if an allocation fails (nothing leaks). */
+int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out);
+
+/* Synchronise the device, free everything the pool owns. NULL is a no-op. */
+int dkv_pool_destroy(dkv_pool* pool);
+
+/* Geometry of a created pool (host struct). */
+int dkv_pool_geometry(const dkv_pool* pool, dkv_geometry* out);
+
+/* One compaction step of one layer for n_req requests.
+ *
+ * PROMPT [Pol-P] [Mem-PC] [Mem-Fig6]: req_slots[i] (host, distinct, inactive
+ * in `layer`) gets a prompt of seq_lens[i] (host, 1..max_seq_len) tokens.
+ *   k, v    device fp16 [sum(seq_lens)][n_kv_heads][128], requests back to
+ *           back in call order.
+ *   q_obs   device fp16 [n_req][32][n_kv_heads*G][128]: the queries of the
+ *           last 32 prompt positions (row o is position seq_len-32+o; rows
+ *           with a negative position are ignored). Query head h belongs to KV
+ *           head h / G.
+ *   scores_in  NULL: the kernels score every token from q_obs (importance =
+ *           sum over observation queries at or after the token of the max
+ *           over the group's heads of softmax(q.k/sqrt(128)); divided by the
+ *           number of such queries). Non-NULL: device fp32
+ *           [sum(seq_lens)][n_kv_heads] scores given by the caller (q_obs is
+ *           then ignored and may be NULL).
+ *   scores_out NULL or device fp32 [sum(seq_lens)][n_kv_heads]: receives
+ *           the score S of every token (given or computed).
+ *   Each head is granted ceil(N0/T_hi)+slack pages by one prefix sum over
+ *   the heads (call order, then KV head) at the list start; hi tokens fill
+ *   the grant from the left, lo tokens from the right, the unused middle
+ *   pages are reclaimed at the list end by a second prefix sum.
+ *
+ * DECODE [Pol-G] [Mem-Gen]: every req_slots[i] must be active in `layer`.
+ *   k, v    device fp16 [n_req][n_kv_heads][128]: the new token of each
+ *           request (position N, N = the request's current length).
+ *   seq_lens, q_obs, scores_in, scores_out must be NULL.
+ *   Per head: append the new token hi; classify the window's oldest token
+ *   t_c; demote or prune one victim; new pages come from one prefix sum at
+ *   the list start, emptied tail pages (if reclaim_in_decode) go to the end.
+ *
+ * Errors: DKV_ERR_ARG, DKV_ERR_STATE (host, nothing queued); DKV_ERR_NO_PAGES,
+ * DKV_ERR_TABLE_FULL latch in the sticky status (device, call is a no-op). */
+int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req,
+                     const int32_t* req_slots, const int32_t* seq_lens,
+                     const void* k, const void* v, const void* q_obs,
+                     const float* scores_in, float* scores_out, void* stream);
+
+/* Decode attention of one layer over the mixed-precision pages [Impl-Kern]
+ * [Bkg-Attn]: for each request i and query head h,
+ *   out[i][h] = sum_j softmax_j(q[i][h] . k^_j / sqrt(128)) v^_j
+ * over every stored token j of KV head h / G (hi pages, then lo pages), with
+ * k^, v^ the dequantised codes. q: device fp16 [n_req][n_kv_heads*G][128];
+ * out: device fp32 [n_req][n_kv_heads*G][128]. If update_scores != 0, each
+ * stored token's score gains max over the group's heads of its softmax
+ * probability, and the request's update counter (used for the importance
+ * denominator in DECODE compaction) increases by one.
+ * Errors: DKV_ERR_ARG, DKV_ERR_STATE (slot inactive in `layer`). */
+int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
+                         const int32_t* req_slots, const void* q, float* out,
+                         int32_t update_scores, void* stream);
+
+/* Return every page of request `req_slot` in every layer to the list end
+ * (one prefix sum over (layer, KV head); within a head hi pages left to
+ * right, then lo pages from the outermost inward) and clear its rows
+ * [Mem-Gen]. Errors: DKV_ERR_ARG, DKV_ERR_STATE (slot active in no layer). */
+int dkv_free_request(dkv_pool* pool, int32_t req_slot, void* stream);
+
+/* Synchronise the pool's device work and read the sticky status and counters. */
+int dkv_pool_status(dkv_pool* pool, dkv_status* out);
+
+/* Synchronise, clear the sticky status and re-read the host's copy of the
+ * request state from the device. */
+int dkv_pool_clear_error(dkv_pool* pool);
+
+/* Synchronise and copy the device state into host buffers (see dkv_snapshot). */
+int dkv_pool_export(dkv_pool* pool, dkv_snapshot* out);
+
+/* Static description of an error code. */
+const char* dkv_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DKV_H */

@@ -1,0 +1,225 @@
+"""CPU oracle of differentiated KV compaction — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package. The product
+path (``differentiated_kv_cache_gb300``) never does, and the two share no code.
+
+The arithmetic lives in ``dkv_oracle.c`` (plain C, fp64 scores and attention,
+pinned fp32 codec and thresholds); this module compiles it with gcc and wraps
+it with ctypes and numpy.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dkv_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+TIER_PRUNE, TIER_LO, TIER_HI = 0, 1, 2
+ERR = dict(OK=0, ARG=-1, STATE=-3, NO_PAGES=-4, TABLE_FULL=-5, CHECK=-7)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (IEEE arithmetic, no contraction, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+                        "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Config(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("n_layers", "n_kv_heads", "group_size", "page_bytes",
+                                          "n_pages", "max_requests", "max_seq_len", "t_hi", "t_lo",
+                                          "lo_enabled")] + \
+               [("alpha_h", C.c_float), ("alpha_l", C.c_float)] + \
+               [(n, C.c_int32) for n in ("window", "grant_slack", "reclaim_in_decode")]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = C.CDLL(build())
+            P, I, I64 = C.c_void_p, C.c_int, C.c_int64
+            L.orc_half_to_float.argtypes = [C.c_uint16]; L.orc_half_to_float.restype = C.c_float
+            L.orc_float_to_half.argtypes = [C.c_float]; L.orc_float_to_half.restype = C.c_uint16
+            L.orc_quantize.argtypes = [P, I, I, P, P, P]; L.orc_quantize.restype = None
+            L.orc_dequant.argtypes = [C.c_uint16, C.c_uint16, I]; L.orc_dequant.restype = C.c_float
+            L.orc_pool_new.argtypes = [P]; L.orc_pool_new.restype = P
+            L.orc_pool_free.argtypes = [P]; L.orc_pool_free.restype = None
+            L.orc_geometry.argtypes = [P, P]; L.orc_geometry.restype = None
+            for f in ("orc_pages", "orc_list", "orc_pointers", "orc_table", "orc_head_counts",
+                      "orc_req_state"):
+                getattr(L, f).argtypes = [P]; getattr(L, f).restype = P
+            L.orc_unit_scores.argtypes = [I, I, P, I64, P, I64, I64, P]; L.orc_unit_scores.restype = None
+            L.orc_prompt_step.argtypes = [P, I, I, P, P, P, P, P, P, P]; L.orc_prompt_step.restype = I
+            L.orc_decode_step.argtypes = [P, I, I, P, P, P]; L.orc_decode_step.restype = I
+            L.orc_unit_attention.argtypes = [P, I, I, I, P, P, P]; L.orc_unit_attention.restype = I
+            L.orc_decode_attention.argtypes = [P, I, I, P, P, P, I]; L.orc_decode_attention.restype = I
+            L.orc_free_request.argtypes = [P, I]; L.orc_free_request.restype = I
+            _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float16)).view(np.uint16)
+
+
+# ---- codec ---------------------------------------------------------------
+def float_to_half_bits(x: float) -> int:
+    return int(lib().orc_float_to_half(C.c_float(x)))
+
+
+def half_bits_to_float(h: int) -> float:
+    return float(lib().orc_half_to_float(C.c_uint16(h)))
+
+
+def quantize(x: np.ndarray, bits: int):
+    """Quantize one fp32 vector: returns (codes uint8, scale fp16 bits, zero fp16 bits)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    codes = np.zeros(x.size, dtype=np.uint8)
+    s = C.c_uint16(); z = C.c_uint16()
+    lib().orc_quantize(_ptr(x), x.size, bits, _ptr(codes), C.byref(s), C.byref(z))
+    return codes, int(s.value), int(z.value)
+
+
+def dequant(scale_bits: int, zero_bits: int, codes: np.ndarray) -> np.ndarray:
+    L = lib()
+    return np.array([L.orc_dequant(scale_bits, zero_bits, int(c)) for c in codes], dtype=np.float32)
+
+
+def unit_scores(k_head: np.ndarray, q_group: np.ndarray) -> np.ndarray:
+    """fp64 prompt scores S of one KV head. k_head: fp16 [N0, 128]; q_group:
+    fp16 [32, G, 128] (row o = position N0-32+o)."""
+    k = _u16(k_head); q = _u16(q_group)
+    n0, G = k.shape[0], q.shape[1]
+    S = np.zeros(n0, dtype=np.float64)
+    lib().orc_unit_scores(n0, G, _ptr(k), 128, _ptr(q), G * 128, 128, _ptr(S))
+    return S
+
+
+# ---- pool -------------------------------------------------------------------
+class Pool:
+    """The oracle's pool: pages, free list, pointers, bidirectional table,
+    per-head counters and per-request state, as plain host arrays."""
+
+    def __init__(self, cfg: dict):
+        self.cfg = dict(cfg)
+        c = _Config(n_layers=cfg["n_layers"], n_kv_heads=cfg["n_kv_heads"], group_size=cfg["group_size"],
+                    page_bytes=cfg["page_bytes"], n_pages=cfg["n_pages"], max_requests=cfg["max_requests"],
+                    max_seq_len=cfg["max_seq_len"], t_hi=cfg.get("tokens_per_hi_page", 0),
+                    t_lo=cfg.get("tokens_per_lo_page", 0), lo_enabled=cfg["lo_enabled"],
+                    alpha_h=cfg["alpha_h"], alpha_l=cfg["alpha_l"], window=cfg["recent_window"],
+                    grant_slack=cfg["prompt_grant_slack"], reclaim_in_decode=cfg["reclaim_in_decode"])
+        self._h = lib().orc_pool_new(C.byref(c))
+        g = np.zeros(17, dtype=np.int32)
+        lib().orc_geometry(self._h, _ptr(g))
+        self.t_hi, self.t_lo, self.table_len = int(g[0]), int(g[1]), int(g[2])
+        self.hi_off, self.lo_off = g[3:9].copy(), g[9:15].copy()
+        self.hi_used, self.lo_used = int(g[15]), int(g[16])
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            lib().orc_pool_free(self._h)
+            self._h = None
+
+    def _view(self, fn, dtype, count):
+        addr = getattr(lib(), fn)(self._h)
+        return np.ctypeslib.as_array(C.cast(addr, C.POINTER(np.ctypeslib.as_ctypes_type(dtype))),
+                                     shape=(count,))
+
+    # live views of the state ----------------------------------------------------
+    @property
+    def pages(self):
+        c = self.cfg
+        return self._view("orc_pages", np.uint8, c["n_pages"] * c["page_bytes"]).reshape(c["n_pages"], c["page_bytes"])
+
+    @property
+    def free_list(self):
+        return self._view("orc_list", np.int32, self.cfg["n_pages"])
+
+    @property
+    def pointers(self):
+        return self._view("orc_pointers", np.int64, 2)
+
+    @property
+    def table(self):
+        c = self.cfg
+        n = c["n_layers"] * c["max_requests"] * c["n_kv_heads"]
+        return self._view("orc_table", np.int32, n * self.table_len).reshape(
+            c["n_layers"], c["max_requests"], c["n_kv_heads"], self.table_len)
+
+    @property
+    def head_counts(self):
+        c = self.cfg
+        n = c["n_layers"] * c["max_requests"] * c["n_kv_heads"]
+        return self._view("orc_head_counts", np.int32, n * 4).reshape(
+            c["n_layers"], c["max_requests"], c["n_kv_heads"], 4)
+
+    @property
+    def req_state(self):
+        c = self.cfg
+        return self._view("orc_req_state", np.int32, c["n_layers"] * c["max_requests"] * 4).reshape(
+            c["n_layers"], c["max_requests"], 4)
+
+    # operations -------------------------------------------------------------------
+    def prompt(self, layer, slots, lens, k, v, q_obs=None, scores_in=None, want_scores=False):
+        slots = np.ascontiguousarray(slots, dtype=np.int32)
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        ku, vu = _u16(k), _u16(v)
+        qu = None if q_obs is None else _u16(q_obs)
+        si = None if scores_in is None else np.ascontiguousarray(scores_in, dtype=np.float32)
+        so = np.zeros((int(lens.sum()), self.cfg["n_kv_heads"]), np.float32) if want_scores else None
+        rc = lib().orc_prompt_step(self._h, layer, len(slots), _ptr(slots), _ptr(lens), _ptr(ku),
+                                   _ptr(vu), _ptr(qu), _ptr(si), _ptr(so))
+        return (rc, so) if want_scores else rc
+
+    def decode(self, layer, slots, k, v):
+        slots = np.ascontiguousarray(slots, dtype=np.int32)
+        return lib().orc_decode_step(self._h, layer, len(slots), _ptr(slots), _ptr(_u16(k)), _ptr(_u16(v)))
+
+    def attention(self, layer, slots, q, update_scores=False):
+        slots = np.ascontiguousarray(slots, dtype=np.int32)
+        qu = _u16(q)
+        out = np.zeros(qu.shape, dtype=np.float64)
+        rc = lib().orc_decode_attention(self._h, layer, len(slots), _ptr(slots), _ptr(qu), _ptr(out),
+                                        int(bool(update_scores)))
+        return rc, out
+
+    def unit_attention(self, layer, slot, kvh, q_group):
+        """fp64 attention of one KV head (q_group fp16 [G, 128]); returns
+        (out [G,128] fp64, pmax over stored tokens (hi slots then lo slots))."""
+        qu = _u16(q_group)
+        cnt = self.head_counts[layer, slot, kvh]
+        n = int(cnt[0] + cnt[1])
+        out = np.zeros(qu.shape, np.float64)
+        pm = np.zeros(max(n, 1), np.float64)
+        lib().orc_unit_attention(self._h, layer, slot, kvh, _ptr(qu), _ptr(out), _ptr(pm))
+        return out, pm[:n]
+
+    def free_request(self, slot):
+        return lib().orc_free_request(self._h, int(slot))
+
+    def snapshot(self) -> dict:
+        return dict(pages=self.pages.copy(), free_list=self.free_list.copy(),
+                    pointers=self.pointers.copy(), table=self.table.copy(),
+                    head_counts=self.head_counts.copy(), req_state=self.req_state.copy())
