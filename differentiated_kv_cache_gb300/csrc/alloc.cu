@@ -1,0 +1,270 @@
+// alloc.cu — the coordination phase of parallel KV compaction (DiffKV,
+// memory management): page grants and reclaims by exclusive prefix sums over
+// all heads of a call against the circular free page list, and the updates of
+// the bidirectional page table. Each kernel here is one CTA of 1024 threads;
+// per-head work is spread over the threads and joined by block-wide scans.
+#include "dkv_kernels.cuh"
+
+namespace dkv {
+
+constexpr int kCoordThreads = 1024;
+
+// Copy the call's host arrays into the pool's device CallArgs and derive the
+// call's no-op flag from the sticky status.
+__global__ void k_setup(PoolView pv, CallArgs args) {
+  CallArgs* c = pv.call;
+  const int n = args.n_req;
+  for (int x = threadIdx.x; x < n; x += blockDim.x) {
+    c->slots[x] = args.slots[x];
+    c->lens[x] = args.lens[x];
+    c->tok0[x] = args.tok0[x];
+  }
+  if (threadIdx.x == 0) {
+    c->n_req = n;
+    c->tok0[n] = args.tok0[n];
+    pv.ctl->fail = pv.ctl->error != 0 ? 1 : 0;
+  }
+}
+
+// Exclusive scan of one int per thread over the whole block; returns the
+// thread's exclusive prefix and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, s);
+    if (lane >= s) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, s);
+      if (lane >= s) w += y;
+    }
+    if (lane < nw) s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int excl = x - v + (warp > 0 ? s_warp[warp - 1] : 0);
+  const int tot = s_warp[nw - 1];
+  __syncthreads();
+  *total = tot;
+  return excl;
+}
+
+__device__ __forceinline__ void latch_error(PoolView& pv, int code, int info) {
+  if (atomicCAS(&pv.ctl->error, 0, code) == 0) pv.ctl->error_info = info;
+  pv.ctl->fail = 1;
+}
+
+// ---------------------------------------------------------------------------
+// Prompt coordination (Figure 6): per head an all-hi grant of
+// ceil(N0/T_hi)+slack pages taken at the list start by one prefix sum; hi
+// pages from the left of the grant, lo pages from the right; the unused
+// middle pages appended at the list end by a second prefix sum; table rows,
+// counters and request state written. All checks precede every write.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCoordThreads) k_prompt_plan(PoolView pv, int layer, Scratch sc) {
+  if (pv.ctl->fail) return;
+  __shared__ int s_warp[32];
+  __shared__ int s_err, s_info;
+  const CallArgs* ca = pv.call;
+  const int n_units = ca->n_req * pv.hkv;
+  const int per = (n_units + kCoordThreads - 1) / kCoordThreads;
+  const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
+  if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
+  __syncthreads();
+  int my_g = 0, my_r = 0;
+  for (int u = u0; u < u1; u++) {
+    const int i = u / pv.hkv;
+    const int n0 = ca->lens[i];
+    const int nkb = (n0 + kKeyBlock - 1) / kKeyBlock;
+    int a = 0, b = 0;
+    for (int kb = 0; kb < nkb; kb++) {
+      const int2 c = sc.bcnt[(size_t)u * sc.nkb_cap + kb];
+      sc.bbase[(size_t)u * sc.nkb_cap + kb] = make_int2(a, b);
+      a += c.x;
+      b += c.y;
+    }
+    const int gh = (n0 + pv.hi.t - 1) / pv.hi.t + pv.slack;
+    const int nhp = (a + pv.hi.t - 1) / pv.hi.t, nlp = (b + pv.lo.t - 1) / pv.lo.t;
+    if (nhp + nlp > gh || nhp + nlp > pv.L) {
+      if (atomicCAS(&s_err, 0, DKV_ERR_TABLE_FULL) == 0) s_info = u;
+    }
+    sc.unit_info[u] = make_int4(gh, a, b, 0);
+    my_g += gh;
+    my_r += max(0, gh - nhp - nlp);
+  }
+  int tot_g, tot_r;
+  const int goff = block_exclusive_scan(my_g, s_warp, &tot_g);
+  const int roff = block_exclusive_scan(my_r, s_warp, &tot_r);
+  const unsigned long long start = pv.ctl->start, end = pv.ctl->end;
+  if (threadIdx.x == 0 && s_err == 0 && (unsigned long long)tot_g > end - start) s_err = DKV_ERR_NO_PAGES;
+  __syncthreads();
+  if (s_err != 0) {
+    if (threadIdx.x == 0) latch_error(pv, s_err, s_info);
+    return;
+  }
+  // grant: read the granted page IDs before any reclaim write can overwrite them
+  int o = goff;
+  for (int u = u0; u < u1; u++) {
+    const int gh = sc.unit_info[u].x;
+    int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
+    for (int x = 0; x < gh; x++) gid[x] = pv.list[(start + (unsigned long long)(o + x)) % pv.n_pages];
+    o += gh;
+  }
+  __syncthreads();
+  int r = roff;
+  for (int u = u0; u < u1; u++) {
+    const int i = u / pv.hkv, kvh = u % pv.hkv, slot = ca->slots[i];
+    const int4 ui = sc.unit_info[u];
+    const int gh = ui.x, nhp = (ui.y + pv.hi.t - 1) / pv.hi.t, nlp = (ui.z + pv.lo.t - 1) / pv.lo.t;
+    const int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
+    for (int x = nhp; x < gh - nlp; x++) pv.list[(end + (unsigned long long)(r++)) % pv.n_pages] = gid[x];
+    int* row = pv.row(layer, slot, kvh);
+    for (int e = 0; e < pv.L; e++) row[e] = -1;
+    for (int x = 0; x < nhp; x++) row[x] = gid[x];
+    for (int x = 0; x < nlp; x++) row[pv.L - 1 - x] = gid[gh - 1 - x];
+    int* cn = pv.cnt(layer, slot, kvh);
+    cn[0] = ui.y; cn[1] = ui.z; cn[2] = nhp; cn[3] = nlp;
+    if (kvh == 0) {
+      int* rq = pv.rq(layer, slot);
+      rq[0] = 1; rq[1] = ca->lens[i]; rq[2] = ca->lens[i]; rq[3] = 0;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    pv.ctl->start = start + (unsigned long long)tot_g;
+    pv.ctl->end = end + (unsigned long long)tot_r;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Generation-phase coordination: new pages for every head that needs one, by
+// one prefix sum at the list start (per head hi then lo); emptied tail pages
+// (reclaim_in_decode) by one prefix sum at the list end; table rows,
+// counters and the request lengths updated. All checks precede every write.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int layer, Scratch sc) {
+  if (pv.ctl->fail) return;
+  __shared__ int s_warp[32];
+  __shared__ int s_err, s_info;
+  const CallArgs* ca = pv.call;
+  const int n_units = ca->n_req * pv.hkv;
+  const int per = (n_units + kCoordThreads - 1) / kCoordThreads;
+  const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
+  if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
+  __syncthreads();
+  int my_a = 0, my_f = 0;
+  for (int u = u0; u < u1; u++) {
+    const DecodePlan& p = sc.dplan[u];
+    if (p.err != 0) {
+      if (atomicCAS(&s_err, 0, p.err) == 0) s_info = u;
+    }
+    my_a += p.new_hp + p.new_lp;
+    my_f += p.free_hp + p.free_lp;
+  }
+  int tot_a, tot_f;
+  const int aoff = block_exclusive_scan(my_a, s_warp, &tot_a);
+  const int foff = block_exclusive_scan(my_f, s_warp, &tot_f);
+  const unsigned long long start = pv.ctl->start, end = pv.ctl->end;
+  if (threadIdx.x == 0 && s_err == 0 && (unsigned long long)tot_a > end - start) s_err = DKV_ERR_NO_PAGES;
+  __syncthreads();
+  if (s_err != 0) {
+    if (threadIdx.x == 0) latch_error(pv, s_err, s_info);
+    return;
+  }
+  // New pages are read from [start, start+A), inside the free region; freed
+  // pages are written to [end, end+F), inside the used region (F <= pages in
+  // use), so the two never overlap and one pass suffices.
+  int a = aoff, f = foff;
+  for (int u = u0; u < u1; u++) {
+    const DecodePlan& p = sc.dplan[u];
+    const int i = u / pv.hkv, kvh = u % pv.hkv, slot = ca->slots[i];
+    int* cn = pv.cnt(layer, slot, kvh);
+    int* row = pv.row(layer, slot, kvh);
+    if (p.new_hp) row[cn[2]] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
+    if (p.new_lp) row[pv.L - 1 - cn[3]] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
+    if (p.free_hp) {
+      pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[cn[2] - 1];
+      row[cn[2] - 1] = -1;
+    }
+    if (p.free_lp) {
+      pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[pv.L - cn[3]];
+      row[pv.L - cn[3]] = -1;
+    }
+    cn[0] = p.nh; cn[1] = p.nl; cn[2] = p.php; cn[3] = p.plp;
+    if (kvh == 0) pv.rq(layer, slot)[2] += 1;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    pv.ctl->start = start + (unsigned long long)tot_a;
+    pv.ctl->end = end + (unsigned long long)tot_f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Request completion: every page of the request (all layers, all KV heads;
+// within a head hi pages left to right, then lo pages from the outermost in)
+// appended at the list end by one prefix sum; rows and state cleared.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCoordThreads) k_free_request(PoolView pv, int slot) {
+  if (pv.ctl->error != 0) return;
+  __shared__ int s_warp[32];
+  const int n_units = pv.n_layers * pv.hkv;
+  const int per = (n_units + kCoordThreads - 1) / kCoordThreads;
+  const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
+  int mine = 0;
+  for (int u = u0; u < u1; u++) {
+    const int layer = u / pv.hkv, kvh = u % pv.hkv;
+    if (!pv.rq(layer, slot)[0]) continue;
+    const int* cn = pv.cnt(layer, slot, kvh);
+    mine += cn[2] + cn[3];
+  }
+  int tot;
+  int o = block_exclusive_scan(mine, s_warp, &tot);
+  const unsigned long long end = pv.ctl->end;
+  for (int u = u0; u < u1; u++) {
+    const int layer = u / pv.hkv, kvh = u % pv.hkv;
+    int* cn = pv.cnt(layer, slot, kvh);
+    int* row = pv.row(layer, slot, kvh);
+    if (pv.rq(layer, slot)[0]) {
+      for (int x = 0; x < cn[2]; x++) pv.list[(end + (unsigned long long)(o++)) % pv.n_pages] = row[x];
+      for (int x = 0; x < cn[3]; x++) pv.list[(end + (unsigned long long)(o++)) % pv.n_pages] = row[pv.L - 1 - x];
+    }
+    for (int e = 0; e < pv.L; e++) row[e] = -1;
+    cn[0] = cn[1] = cn[2] = cn[3] = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) pv.ctl->end = end + (unsigned long long)tot;
+  for (int layer = threadIdx.x; layer < pv.n_layers; layer += blockDim.x) {
+    int* rq = pv.rq(layer, slot);
+    rq[0] = rq[1] = rq[2] = rq[3] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+cudaError_t launch_setup(const Pool& P, const CallArgs& args, cudaStream_t st) {
+  k_setup<<<1, 256, 0, st>>>(P.pv, args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prompt_plan(Pool& P, int layer, cudaStream_t st) {
+  k_prompt_plan<<<1, kCoordThreads, 0, st>>>(P.pv, layer, P.sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_alloc(Pool& P, int layer, cudaStream_t st) {
+  k_decode_alloc<<<1, kCoordThreads, 0, st>>>(P.pv, layer, P.sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_free(Pool& P, int slot, cudaStream_t st) {
+  k_free_request<<<1, kCoordThreads, 0, st>>>(P.pv, slot);
+  return cudaGetLastError();
+}
+
+}  // namespace dkv

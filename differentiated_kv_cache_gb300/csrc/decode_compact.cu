@@ -1,0 +1,278 @@
+// decode_compact.cu — generation-phase compaction (DiffKV, compaction policy:
+// generation phase and algorithm flow; memory management: generation
+// workflow). One token per step per head:
+//   1. the newest token enters the recent window, quantized hi;
+//   2. the window's oldest token t_c is classified against alpha_h/N and
+//      alpha_l/N: it stays hi, is re-quantized to lo, or is pruned;
+//   3. if t_c was kept, the least important token t_v of its tier (hi: outside
+//      the window) is considered for demotion (hi -> lo) or pruning.
+// Removal from a tier fills the hole with the tier's last token. The per-head
+// plan is made by k_decode_plan; pages are granted by k_decode_alloc
+// (alloc.cu); k_decode_apply writes the token slots.
+#include "dkv_kernels.cuh"
+
+namespace dkv {
+
+constexpr int kPlanThreads = 256;
+
+struct ArgMin {
+  unsigned long long key;   // order_key(importance) << 32 | position
+  int slot;
+};
+__device__ __forceinline__ ArgMin amin(ArgMin a, ArgMin b) { return b.key < a.key ? b : a; }
+__device__ __forceinline__ ArgMin shfl_amin(ArgMin a, int s) {
+  ArgMin b;
+  b.key = __shfl_xor_sync(0xffffffffu, a.key, s);
+  b.slot = __shfl_xor_sync(0xffffffffu, a.slot, s);
+  return amin(a, b);
+}
+
+__device__ ArgMin block_amin(ArgMin a, ArgMin* s_tmp) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) a = shfl_amin(a, s);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) s_tmp[warp] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); w++) a = amin(a, s_tmp[w]);
+    s_tmp[0] = a;
+  }
+  __syncthreads();
+  a = s_tmp[0];
+  __syncthreads();
+  return a;
+}
+
+__device__ __forceinline__ float key_importance(unsigned long long key) {
+  const uint32_t k = (uint32_t)(key >> 32);
+  const uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(b);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int layer, DecodePlan* plans) {
+  if (pv.ctl->fail) return;
+  __shared__ ArgMin s_tmp[kPlanThreads / 32];
+  __shared__ int s_xc;
+  __shared__ float s_ic;
+  const int kvh = blockIdx.x, i = blockIdx.y;
+  const int slot = pv.call->slots[i];
+  const int unit = i * pv.hkv + kvh;
+  const int* rq = pv.rq(layer, slot);
+  const int n0 = rq[1], n = rq[2] + 1, upd = rq[3];
+  const int* cn = pv.cnt(layer, slot, kvh);
+  const int nh = cn[0], nl = cn[1], php = cn[2], plp = cn[3];
+  const int* row = pv.row(layer, slot, kvh);
+  const int pc = n - pv.window - 1;         // position of t_c
+  const int wlim = n - pv.window;           // hi victims: position < wlim
+  if (threadIdx.x == 0) { s_xc = -1; s_ic = 0.0f; }
+  __syncthreads();
+  ArgMin bh{~0ull, -1}, bl{~0ull, -1};
+  for (int s = threadIdx.x; s < nh; s += blockDim.x) {
+    const uint8_t* pg = pv.page(row[s / pv.hi.t]);
+    const int ip = s % pv.hi.t;
+    const float sc = *reinterpret_cast<const float*>(pg + pv.hi.off[4] + 4 * ip);
+    const int pos = *reinterpret_cast<const int*>(pg + pv.hi.off[5] + 4 * ip);
+    const float imp = __fdiv_rn(sc, (float)score_count(pos, n0, upd));
+    if (pos == pc) { s_xc = s; s_ic = imp; }
+    if (pos < wlim) bh = amin(bh, ArgMin{((unsigned long long)order_key(imp) << 32) | (uint32_t)pos, s});
+  }
+  for (int s = threadIdx.x; s < nl; s += blockDim.x) {
+    const uint8_t* pg = pv.page(row[pv.L - 1 - s / pv.lo.t]);
+    const int ip = s % pv.lo.t;
+    const float sc = *reinterpret_cast<const float*>(pg + pv.lo.off[4] + 4 * ip);
+    const int pos = *reinterpret_cast<const int*>(pg + pv.lo.off[5] + 4 * ip);
+    const float imp = __fdiv_rn(sc, (float)score_count(pos, n0, upd));
+    bl = amin(bl, ArgMin{((unsigned long long)order_key(imp) << 32) | (uint32_t)pos, s});
+  }
+  bh = block_amin(bh, s_tmp);
+  bl = block_amin(bl, s_tmp);
+  if (threadIdx.x != 0) return;
+  const float th_h = __fdiv_rn(pv.alpha_h, (float)n), th_l = __fdiv_rn(pv.alpha_l, (float)n);
+  DecodePlan p;
+  p.err = 0;
+  p.n_moves = 0;
+  int nh2 = nh + 1, nl2 = nl;                 // (1) newest token appended at hi slot nh
+  Move newmv{kTierHi, nh, kSrcNew, -1};
+  if (pc >= 0) {
+    const int xc = s_xc;
+    if (xc < 0) {
+      p.err = DKV_ERR_CHECK;
+    } else {
+      const int tc = classify(s_ic, th_h, th_l, pv.lo_enabled);
+      if (tc == kTierHi) {
+        // (3) hi victim: least important hi token outside the window (t_c included)
+        const int xv = bh.slot;
+        const float iv = key_importance(bh.key);
+        const bool keep = pv.lo_enabled ? (iv > th_h) : (iv >= th_l);
+        if (!keep) {
+          newmv.dst_slot = xv;                // last (newest) token fills the hole
+          nh2 = nh;
+          if (pv.lo_enabled && iv >= th_l) {
+            p.mv[p.n_moves++] = Move{kTierLo, nl, kSrcDemote, xv};
+            nl2 = nl + 1;
+          }
+        }
+      } else if (tc == kTierLo) {
+        newmv.dst_slot = xc;                  // t_c leaves hi; the newest token fills it
+        nh2 = nh;
+        // t_c re-quantized and appended to lo at slot nl; lo victim over lo + t_c
+        const unsigned long long kc = ((unsigned long long)order_key(s_ic) << 32) | (uint32_t)pc;
+        const bool tc_min = (bl.slot < 0) || (kc < bl.key);
+        const float iv = tc_min ? s_ic : key_importance(bl.key);
+        if (iv < th_l) {
+          if (!tc_min) p.mv[p.n_moves++] = Move{kTierLo, bl.slot, kSrcDemote, xc};
+          nl2 = nl;                           // victim pruned (t_c itself, or the victim's
+                                              // slot refilled with t_c)
+        } else {
+          p.mv[p.n_moves++] = Move{kTierLo, nl, kSrcDemote, xc};
+          nl2 = nl + 1;
+        }
+      } else {
+        newmv.dst_slot = xc;                  // t_c pruned
+        nh2 = nh;
+      }
+    }
+  }
+  // the newest token's write goes last in the list: sources are read first anyway
+  p.mv[p.n_moves++] = newmv;
+  p.nh = nh2;
+  p.nl = nl2;
+  const int need_h = (nh2 + pv.hi.t - 1) / pv.hi.t, need_l = (nl2 + pv.lo.t - 1) / pv.lo.t;
+  p.new_hp = p.new_lp = p.free_hp = p.free_lp = 0;
+  p.php = php;
+  p.plp = plp;
+  if (need_h > php) { p.new_hp = need_h - php; p.php = need_h; }
+  else if (pv.reclaim && need_h < php) { p.free_hp = php - need_h; p.php = need_h; }
+  if (need_l > plp) { p.new_lp = need_l - plp; p.plp = need_l; }
+  else if (pv.reclaim && need_l < plp) { p.free_lp = plp - need_l; p.plp = need_l; }
+  if (p.err == 0 && p.php + p.plp > pv.L) p.err = DKV_ERR_TABLE_FULL;
+  plans[unit] = p;
+}
+
+// Token record staged in shared memory between the read and write phases.
+struct TokStage {
+  uint8_t kc[kD], vc[kD];
+  uint32_t kmeta, vmeta;
+  float score;
+  int pos;
+};
+
+// Warp-wide min / max of one value per lane.
+__device__ __forceinline__ void warp_minmax(float& mn, float& mx) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, s));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+  }
+}
+
+// Quantize 4 features per lane (features 4*lane..4*lane+3) into the stage.
+__device__ __forceinline__ void warp_quantize(const float* x, int bits, uint8_t* codes, uint32_t* meta) {
+  const int lane = threadIdx.x & 31;
+  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  warp_minmax(mn, mx);
+  const QParams q = qparams(mn, mx, bits);
+#pragma unroll
+  for (int e = 0; e < 4; e++) codes[4 * lane + e] = (uint8_t)qcode(x[e], q, bits);
+  if (lane == 0) *meta = (uint32_t)q.sh | ((uint32_t)q.zh << 16);
+}
+
+__global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, const DecodePlan* __restrict__ plans,
+                                                      const __half* __restrict__ knew,
+                                                      const __half* __restrict__ vnew) {
+  if (pv.ctl->fail) return;
+  __shared__ TokStage st[2];
+  const int kvh = blockIdx.x, i = blockIdx.y;
+  const int slot = pv.call->slots[i];
+  const int unit = i * pv.hkv + kvh;
+  const DecodePlan& p = plans[unit];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int* row = pv.row(layer, slot, kvh);
+  const int n = pv.rq(layer, slot)[2];       // already advanced by k_decode_alloc
+  // read phase: warp m stages the source of move m
+  if (warp < p.n_moves) {
+    const Move mv = p.mv[warp];
+    TokStage& s = st[warp];
+    float kx[4], vx[4];
+    if (mv.src == kSrcNew) {
+      const __half* kp = knew + ((size_t)i * pv.hkv + kvh) * kD + 4 * lane;
+      const __half* vp = vnew + ((size_t)i * pv.hkv + kvh) * kD + 4 * lane;
+#pragma unroll
+      for (int e = 0; e < 4; e++) { kx[e] = __half2float(kp[e]); vx[e] = __half2float(vp[e]); }
+      warp_quantize(kx, 8, s.kc, &s.kmeta);
+      warp_quantize(vx, 4, s.vc, &s.vmeta);
+      if (lane == 0) { s.score = 0.0f; s.pos = n - 1; }
+    } else {
+      // demote: dequantize the hi slot's codes, quantize again at lo precision
+      const uint8_t* pg = pv.page(row[mv.src_slot / pv.hi.t]);
+      const int ip = mv.src_slot % pv.hi.t;
+      const uint32_t km = *reinterpret_cast<const uint32_t*>(pg + pv.hi.off[2] + 4 * ip);
+      const uint32_t vm = *reinterpret_cast<const uint32_t*>(pg + pv.hi.off[3] + 4 * ip);
+      const uint32_t kw = *reinterpret_cast<const uint32_t*>(pg + pv.hi.off[0] + ip * pv.hi.kbytes + 4 * lane);
+      const uint32_t vw = *reinterpret_cast<const uint32_t*>(pg + pv.hi.off[1] + (ip / 2) * 128 + 4 * lane);
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        kx[e] = dequant((uint16_t)km, (uint16_t)(km >> 16), (kw >> (8 * e)) & 255u);
+        vx[e] = dequant((uint16_t)vm, (uint16_t)(vm >> 16), (vw >> vbit(4, 4 * lane + e, ip & 1)) & 15u);
+      }
+      warp_quantize(kx, 4, s.kc, &s.kmeta);
+      warp_quantize(vx, 2, s.vc, &s.vmeta);
+      if (lane == 0) {
+        s.score = *reinterpret_cast<const float*>(pg + pv.hi.off[4] + 4 * ip);
+        s.pos = *reinterpret_cast<const int*>(pg + pv.hi.off[5] + 4 * ip);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  // write phase: one warp, moves in order (value words shared between slots)
+  for (int m = 0; m < p.n_moves; m++) {
+    const Move mv = p.mv[m];
+    const TokStage& s = st[m];
+    const bool hi = mv.dst_tier == kTierHi;
+    const TierGeom& tg = hi ? pv.hi : pv.lo;
+    const int e_page = hi ? mv.dst_slot / tg.t : pv.L - 1 - mv.dst_slot / tg.t;
+    uint8_t* pg = pv.page(row[e_page]);
+    const int ip = mv.dst_slot % tg.t;
+    const uint8_t* kc = s.kc + 4 * lane;
+    if (hi) {
+      *reinterpret_cast<uint32_t*>(pg + tg.off[0] + ip * 128 + 4 * lane) =
+          kc[0] | (kc[1] << 8) | (kc[2] << 16) | ((uint32_t)kc[3] << 24);
+    } else {
+      *reinterpret_cast<uint16_t*>(pg + tg.off[0] + ip * 64 + 2 * lane) =
+          (uint16_t)(kc[0] | (kc[1] << 4) | (kc[2] << 8) | (kc[3] << 12));
+    }
+    const int vbits = hi ? 4 : 2, gsz = hi ? 2 : 4;
+    uint32_t* vw = reinterpret_cast<uint32_t*>(pg + tg.off[1] + (ip / gsz) * 128) + lane;
+    uint32_t w = *vw;
+    const uint32_t lmask = (1u << vbits) - 1u;
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const int b = vbit(vbits, 4 * lane + e, ip % gsz);
+      w = (w & ~(lmask << b)) | ((uint32_t)s.vc[4 * lane + e] << b);
+    }
+    *vw = w;
+    if (lane == 0) {
+      *reinterpret_cast<uint32_t*>(pg + tg.off[2] + 4 * ip) = s.kmeta;
+      *reinterpret_cast<uint32_t*>(pg + tg.off[3] + 4 * ip) = s.vmeta;
+      *reinterpret_cast<float*>(pg + tg.off[4] + 4 * ip) = s.score;
+      *reinterpret_cast<int*>(pg + tg.off[5] + 4 * ip) = s.pos;
+    }
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_decode_alloc(Pool& P, int layer, cudaStream_t st);
+
+cudaError_t launch_decode(Pool& P, int layer, int n_req, const __half* k, const __half* v, cudaStream_t st) {
+  const dim3 grid(P.pv.hkv, n_req);
+  k_decode_plan<<<grid, kPlanThreads, 0, st>>>(P.pv, layer, P.sc.dplan);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = launch_decode_alloc(P, layer, st)) != cudaSuccess) return e;
+  k_decode_apply<<<grid, 64, 0, st>>>(P.pv, layer, P.sc.dplan, k, v);
+  return cudaGetLastError();
+}
+
+}  // namespace dkv

@@ -1,0 +1,218 @@
+// dkv_common.cuh — device-side definitions shared by the libdkv kernels.
+//
+// Everything here is GPU code written for sm_103a (GB300). The page format,
+// free-list and table conventions are the ones stated in include/dkv.h; the
+// method is DiffKV (SOSP'25): differentiated K/V precision, token-importance
+// tiers and the parallel KV compaction memory manager.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dkv.h"
+
+namespace dkv {
+
+constexpr int kD = 128;            // head_dim
+constexpr int kObs = 32;           // observation queries per prompt
+constexpr int kMaxG = 8;           // query heads per KV head supported by the kernels
+constexpr int kMaxCallReq = 1024;  // requests per call
+constexpr int kTierPrune = 0, kTierLo = 1, kTierHi = 2;
+
+// Geometry of one tier's unified page.
+struct TierGeom {
+  int t;          // tokens per page
+  int kbytes;     // key row bytes (128 for 8-bit, 64 for 4-bit)
+  int off[6];     // K codes, V codes, K meta, V meta, score, position
+};
+
+// Device control block: free-list counters, sticky status, per-call flag.
+struct Ctl {
+  unsigned long long start;   // allocation counter
+  unsigned long long end;     // reclaim counter
+  int error;                  // sticky data-dependent error (0 = none)
+  int error_info;
+  int fail;                   // the current call is a no-op
+  int pad;
+};
+
+// Per-call copy of the caller's host arrays (written by the set-up kernel).
+struct CallArgs {
+  int n_req;
+  int pad;
+  int slots[kMaxCallReq];
+  int lens[kMaxCallReq];
+  long long tok0[kMaxCallReq + 1];
+};
+
+// Device view of a pool, passed by value to every kernel.
+struct PoolView {
+  uint8_t* pages;
+  int* list;
+  int* table;        // [layer][slot][kvh][L]
+  int* counts;       // [layer][slot][kvh][4]: hi tok, lo tok, hi pages, lo pages
+  int* req;          // [layer][slot][4]: active, N0, N, updates
+  Ctl* ctl;
+  CallArgs* call;
+  int n_pages, page_bytes, n_layers, hkv, G, max_req, max_seq, L;
+  int lo_enabled, window, slack, reclaim;
+  float alpha_h, alpha_l;
+  TierGeom hi, lo;
+
+  __device__ __forceinline__ int* row(int layer, int slot, int kvh) const {
+    return table + ((size_t)((size_t)layer * max_req + slot) * hkv + kvh) * L;
+  }
+  __device__ __forceinline__ int* cnt(int layer, int slot, int kvh) const {
+    return counts + ((size_t)((size_t)layer * max_req + slot) * hkv + kvh) * 4;
+  }
+  __device__ __forceinline__ int* rq(int layer, int slot) const {
+    return req + ((size_t)layer * max_req + slot) * 4;
+  }
+  __device__ __forceinline__ uint8_t* page(int id) const {
+    return pages + (size_t)id * page_bytes;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Importance count and three-way tier decision, fp32 correctly rounded.
+// DiffKV, compaction policy: importance = mean attention received, compared
+// with alpha_h/N and alpha_l/N; GQA heads combined with max.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int score_count(int j, int n0, int updates) {
+  int c = (j < n0 ? min(n0 - j, kObs) : 0) + updates - (j >= n0 ? j - n0 : 0);
+  return c < 1 ? 1 : c;
+}
+
+__device__ __forceinline__ int classify(float imp, float th_h, float th_l, int lo_enabled) {
+  if (lo_enabled) {
+    if (imp > th_h) return kTierHi;
+    if (imp >= th_l) return kTierLo;
+    return kTierPrune;
+  }
+  return imp >= th_l ? kTierHi : kTierPrune;
+}
+
+// Total order on floats as unsigned keys (for argmin reductions).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// Quantization codec (DiffKV, background: Q = round((X - z)/s), X^ = sQ + z),
+// per token vector, every step an IEEE operation with explicit rounding so
+// the codes are identical to any other correctly rounded implementation.
+// ---------------------------------------------------------------------------
+struct QParams {
+  float inv;        // 1/s (unused when s == 0)
+  float z;
+  uint16_t sh, zh;  // fp16 bits of scale and zero
+  bool zero_scale;
+};
+
+__device__ __forceinline__ QParams qparams(float mn, float mx, int bits) {
+  QParams q;
+  if (mn == 0.0f) mn = 0.0f;  // -0 taken as +0
+  const float L = (float)((1 << bits) - 1);
+  float s32 = __fdiv_rn(__fsub_rn(mx, mn), L);
+  __half sh = __float2half_rn(s32), zh = __float2half_rn(mn);
+  float s = __half2float(sh);
+  q.z = __half2float(zh);
+  q.sh = __half_as_ushort(sh);
+  q.zh = __half_as_ushort(zh);
+  q.zero_scale = (s == 0.0f);
+  q.inv = q.zero_scale ? 0.0f : __frcp_rn(s);
+  return q;
+}
+
+__device__ __forceinline__ uint32_t qcode(float x, const QParams& q, int bits) {
+  if (q.zero_scale) return 0u;
+  float t = __fmul_rn(__fsub_rn(x, q.z), q.inv);
+  float r = rintf(t);
+  r = fmaxf(r, 0.0f);
+  r = fminf(r, (float)((1 << bits) - 1));
+  return (uint32_t)r;
+}
+
+__device__ __forceinline__ float dequant(uint16_t sh, uint16_t zh, uint32_t code) {
+  return __fmaf_rn(__half2float(__ushort_as_half(sh)), (float)code, __half2float(__ushort_as_half(zh)));
+}
+
+// bit offset of (feature f, slot-in-row e) inside value word f/4
+__device__ __forceinline__ int vbit(int vbits, int f, int e) {
+  int i = f & 3;
+  return vbits == 4 ? 16 * e + 4 * i : 16 * (e & 1) + 4 * i + 2 * (e >> 1);
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (legacy-MMA tensor path, async copies, warp matrix moves).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t* r, uint32_t smem_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte async global->shared copy; src_bytes = 0 zero-fills without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+  uint32_t d;  // (a & mask) | orv
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));
+  return d;
+}
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
+                      *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace dkv

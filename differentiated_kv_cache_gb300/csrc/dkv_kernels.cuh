@@ -1,0 +1,71 @@
+// dkv_kernels.cuh — internal interface between the C-ABI host code (pool.cu)
+// and the kernel files (prompt.cu, alloc.cu, decode_compact.cu, attention.cu).
+#pragma once
+
+#include <vector>
+
+#include "dkv_common.cuh"
+
+namespace dkv {
+
+constexpr int kKeyBlock = 128;     // prompt tokens per scoring / classification block
+constexpr int kChunk = 16;         // decode-attention tokens per mma chunk
+constexpr int kAttnWarps = 4;      // warps per decode-attention CTA
+
+// One slot write of a generation-phase step.
+enum MoveSrc { kSrcNew = 0, kSrcDemote = 1 };
+struct Move {
+  int dst_tier, dst_slot, src, src_slot;
+};
+// Per-head plan of one generation-phase step (written by k_decode_plan).
+struct DecodePlan {
+  int nh, nl;                          // token counts after the step
+  int php, plp;                        // page counts after the step
+  int new_hp, new_lp, free_hp, free_lp;
+  int n_moves, err;
+  Move mv[2];
+};
+
+// Device scratch owned by the pool (sizes fixed at creation).
+struct Scratch {
+  // prompt
+  float2* partial;      // [units][nkb_cap][32*G]
+  float* lse2;          // [units][32*G]
+  float* score;         // [max_tokens][Hkv]
+  uint16_t* tokinfo;    // [max_tokens][Hkv]: rank << 2 | tier
+  int2* bcnt;           // [units][nkb_cap]
+  int2* bbase;          // [units][nkb_cap]
+  int* rank2pos;        // [units][2][max_seq]
+  int4* unit_info;      // [units]: grant pages, hi count, lo count
+  int* grant_ids;       // [units][grant_cap]
+  // decode compaction
+  DecodePlan* dplan;    // [units]
+  // decode attention
+  float* apart;         // [units][max_splits][G*(128+2)]
+  float* alogit;        // [units][max_chunks][16][8]
+  float* alse;          // [units][G]
+  int nkb_cap, grant_cap, max_splits, max_chunks;
+};
+
+// Host side of a pool.
+struct Pool {
+  dkv_config cfg;
+  int device;
+  PoolView pv;           // device pointers + geometry
+  Scratch sc;
+  std::vector<void*> allocations;
+  // host mirror of request state: [layer][slot]
+  std::vector<int> h_active, h_n0, h_n;
+};
+
+// Launchers (return the first CUDA error, cudaSuccess otherwise).
+cudaError_t launch_setup(const Pool& P, const CallArgs& args, cudaStream_t st);
+cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, const __half* k, const __half* v,
+                          const __half* q_obs, const float* scores_in, float* scores_out, cudaStream_t st);
+cudaError_t launch_decode(Pool& P, int layer, int n_req, const __half* k, const __half* v, cudaStream_t st);
+cudaError_t launch_attention(Pool& P, int layer, int n_req, int max_tokens, const __half* q, float* out,
+                             int update_scores, cudaStream_t st);
+cudaError_t launch_free(Pool& P, int slot, cudaStream_t st);
+cudaError_t configure_kernels();
+
+}  // namespace dkv

@@ -1,0 +1,429 @@
+// pool.cu — host implementation of the libdkv C ABI (include/dkv.h).
+//
+// The pool owns every device structure of DiffKV's memory manager (unified
+// pages, circular free page list, bidirectional page tables, counters) plus
+// the kernels' scratch. Calls queue kernels on the caller's stream and never
+// synchronise; request-state checks use a host mirror of the request table,
+// which dkv_pool_clear_error re-reads from the device.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "dkv_kernels.cuh"
+
+using namespace dkv;
+
+struct dkv_pool {
+  Pool P;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+int round16(int x) { return (x + 15) & ~15; }
+
+// Unified page layout of one tier for t tokens; returns bytes used.
+int layout_tier(int t, int kbits, int vbits, TierGeom* tg) {
+  const int g = 8 / vbits;
+  const int sizes[6] = {t * kD * kbits / 8, (t / g) * 128, 4 * t, 4 * t, 4 * t, 4 * t};
+  int o = 0;
+  for (int s = 0; s < 6; s++) {
+    tg->off[s] = o;
+    o = round16(o + sizes[s]);
+  }
+  tg->t = t;
+  tg->kbytes = kD * kbits / 8;
+  return tg->off[5] + sizes[5];
+}
+
+// Tokens per page: the override, or the largest multiple of g that fits.
+int fit_tier(int page_bytes, int kbits, int vbits, int override_t, TierGeom* tg) {
+  const int g = 8 / vbits;
+  if (override_t) {
+    if (override_t < g || override_t % g) return -1;
+    return layout_tier(override_t, kbits, vbits, tg) <= page_bytes ? override_t : -1;
+  }
+  int best = -1;
+  for (int t = g; t * 32 <= page_bytes * 8; t += g) {
+    TierGeom tmp;
+    if (layout_tier(t, kbits, vbits, &tmp) <= page_bytes) best = t; else break;
+  }
+  if (best > 0) layout_tier(best, kbits, vbits, tg);
+  return best;
+}
+
+template <typename T>
+cudaError_t dev_alloc(Pool& P, T** ptr, size_t count) {
+  void* p = nullptr;
+  const size_t bytes = std::max<size_t>(count * sizeof(T), 256);
+  cudaError_t e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) return e;
+  P.allocations.push_back(p);
+  *ptr = reinterpret_cast<T*>(p);
+  return cudaSuccess;
+}
+
+void free_all(Pool& P) {
+  for (void* p : P.allocations) cudaFree(p);
+  P.allocations.clear();
+}
+
+__global__ void k_init_list(int* list, int n) {
+  for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < n; x += gridDim.x * blockDim.x) list[x] = x;
+}
+
+int validate(const dkv_config* c) {
+  if (!c) return DKV_ERR_ARG;
+  if (c->n_layers < 1 || c->n_kv_heads < 1 || c->n_pages < 1 || c->max_requests < 1 || c->max_seq_len < 1)
+    return DKV_ERR_ARG;
+  if (c->page_bytes < 64 || c->page_bytes % 16) return DKV_ERR_ARG;
+  if (c->recent_window < 0 || c->prompt_grant_slack < 0) return DKV_ERR_ARG;
+  if (std::isnan(c->alpha_h) || std::isnan(c->alpha_l)) return DKV_ERR_ARG;
+  if (c->head_dim != kD || c->group_size < 1 || c->group_size > kMaxG || c->obs_window != kObs)
+    return DKV_ERR_UNSUPPORTED;
+  return DKV_OK;
+}
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dkv_strerror(int code) {
+  switch (code) {
+    case DKV_OK: return "ok";
+    case DKV_ERR_ARG: return "invalid argument";
+    case DKV_ERR_CUDA: return "CUDA runtime error";
+    case DKV_ERR_STATE: return "request slot in the wrong state";
+    case DKV_ERR_NO_PAGES: return "free page list exhausted";
+    case DKV_ERR_TABLE_FULL: return "page table row or grant full";
+    case DKV_ERR_TIMEOUT: return "bounded device wait expired";
+    case DKV_ERR_CHECK: return "device consistency check failed";
+    case DKV_ERR_UNSUPPORTED: return "configuration not supported by the kernels";
+    default: return "unknown error";
+  }
+}
+
+int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
+  if (!out) return DKV_ERR_ARG;
+  *out = nullptr;
+  int rc = validate(cfg);
+  if (rc) return rc;
+  TierGeom hi{}, lo{};
+  if (fit_tier(cfg->page_bytes, 8, 4, cfg->tokens_per_hi_page, &hi) < 0) return DKV_ERR_ARG;
+  if (fit_tier(cfg->page_bytes, 4, 2, cfg->tokens_per_lo_page, &lo) < 0) return DKV_ERR_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || cuda_device < 0 || cuda_device >= ndev) return DKV_ERR_ARG;
+  DeviceGuard guard(cuda_device);
+  dkv_pool* pool = new (std::nothrow) dkv_pool();
+  if (!pool) return DKV_ERR_CUDA;
+  Pool& P = pool->P;
+  P.cfg = *cfg;
+  P.device = cuda_device;
+  PoolView& v = P.pv;
+  v.n_pages = cfg->n_pages;
+  v.page_bytes = cfg->page_bytes;
+  v.n_layers = cfg->n_layers;
+  v.hkv = cfg->n_kv_heads;
+  v.G = cfg->group_size;
+  v.max_req = cfg->max_requests;
+  v.max_seq = cfg->max_seq_len;
+  v.L = (cfg->max_seq_len + hi.t - 1) / hi.t + 1;
+  v.lo_enabled = cfg->lo_enabled ? 1 : 0;
+  v.window = cfg->recent_window;
+  v.slack = cfg->prompt_grant_slack;
+  v.reclaim = cfg->reclaim_in_decode ? 1 : 0;
+  v.alpha_h = cfg->alpha_h;
+  v.alpha_l = cfg->alpha_l;
+  v.hi = hi;
+  v.lo = lo;
+  Scratch& s = P.sc;
+  const size_t heads = (size_t)cfg->n_layers * cfg->max_requests * cfg->n_kv_heads;
+  const size_t units = (size_t)cfg->max_requests * cfg->n_kv_heads;
+  const size_t max_tokens = (size_t)cfg->max_requests * cfg->max_seq_len;
+  const int G = cfg->group_size;
+  s.nkb_cap = (cfg->max_seq_len + kKeyBlock - 1) / kKeyBlock;
+  s.grant_cap = (cfg->max_seq_len + hi.t - 1) / hi.t + cfg->prompt_grant_slack;
+  s.max_chunks = (cfg->max_seq_len + kChunk - 1) / kChunk + 1;
+  s.max_splits = s.max_chunks / 8 + 1;
+  cudaError_t e = cudaSuccess;
+  auto A = [&](auto** ptr, size_t n) {
+    if (e == cudaSuccess) e = dev_alloc(P, ptr, n);
+  };
+  A(&v.pages, (size_t)cfg->n_pages * cfg->page_bytes);
+  A(&v.list, (size_t)cfg->n_pages);
+  A(&v.table, heads * v.L);
+  A(&v.counts, heads * 4);
+  A(&v.req, (size_t)cfg->n_layers * cfg->max_requests * 4);
+  A(&v.ctl, 1);
+  A(&v.call, 1);
+  A(&s.partial, units * s.nkb_cap * kObs * G);
+  A(&s.lse2, units * kObs * G);
+  A(&s.score, max_tokens * cfg->n_kv_heads);
+  A(&s.tokinfo, max_tokens * cfg->n_kv_heads);
+  A(&s.bcnt, units * s.nkb_cap);
+  A(&s.bbase, units * s.nkb_cap);
+  A(&s.rank2pos, units * 2 * cfg->max_seq_len);
+  A(&s.unit_info, units);
+  A(&s.grant_ids, units * s.grant_cap);
+  A(&s.dplan, units);
+  A(&s.apart, units * s.max_splits * G * (kD + 2));
+  A(&s.alogit, units * s.max_chunks * kChunk * 8);
+  A(&s.alse, units * G);
+  if (e == cudaSuccess) e = cudaMemset(v.pages, 0, (size_t)cfg->n_pages * cfg->page_bytes);
+  if (e == cudaSuccess) e = cudaMemset(v.table, 0xff, heads * v.L * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(v.counts, 0, heads * 4 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(v.req, 0, (size_t)cfg->n_layers * cfg->max_requests * 4 * sizeof(int));
+  if (e == cudaSuccess) {
+    Ctl c{};
+    c.start = 0;
+    c.end = (unsigned long long)cfg->n_pages;
+    c.error_info = -1;
+    e = cudaMemcpy(v.ctl, &c, sizeof(Ctl), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) {
+    k_init_list<<<256, 256>>>(v.list, cfg->n_pages);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = configure_kernels();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_all(P);
+    delete pool;
+    return DKV_ERR_CUDA;
+  }
+  P.h_active.assign((size_t)cfg->n_layers * cfg->max_requests, 0);
+  P.h_n0.assign(P.h_active.size(), 0);
+  P.h_n.assign(P.h_active.size(), 0);
+  *out = pool;
+  return DKV_OK;
+}
+
+int dkv_pool_destroy(dkv_pool* pool) {
+  if (!pool) return DKV_OK;
+  DeviceGuard guard(pool->P.device);
+  const cudaError_t e = cudaDeviceSynchronize();
+  free_all(pool->P);
+  delete pool;
+  return cuda_err(e);
+}
+
+int dkv_pool_geometry(const dkv_pool* pool, dkv_geometry* out) {
+  if (!pool || !out) return DKV_ERR_ARG;
+  const PoolView& v = pool->P.pv;
+  out->t_hi = v.hi.t;
+  out->t_lo = v.lo.t;
+  out->table_len = v.L;
+  for (int s = 0; s < 6; s++) {
+    out->hi_off[s] = v.hi.off[s];
+    out->lo_off[s] = v.lo.off[s];
+  }
+  TierGeom tmp;
+  out->hi_used = layout_tier(v.hi.t, 8, 4, &tmp);
+  out->lo_used = layout_tier(v.lo.t, 4, 2, &tmp);
+  return DKV_OK;
+}
+
+int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req, const int32_t* req_slots,
+                     const int32_t* seq_lens, const void* k, const void* v, const void* q_obs,
+                     const float* scores_in, float* scores_out, void* stream) {
+  if (!pool || !req_slots || !k || !v) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  if (layer < 0 || layer >= c.n_layers || n_req < 1 || n_req > c.max_requests || n_req > kMaxCallReq)
+    return DKV_ERR_ARG;
+  if (mode != DKV_PROMPT && mode != DKV_DECODE) return DKV_ERR_ARG;
+  for (int i = 0; i < n_req; i++) {
+    if (req_slots[i] < 0 || req_slots[i] >= c.max_requests) return DKV_ERR_ARG;
+    for (int j = 0; j < i; j++)
+      if (req_slots[j] == req_slots[i]) return DKV_ERR_ARG;
+  }
+  const size_t base = (size_t)layer * c.max_requests;
+  CallArgs args;
+  args.n_req = n_req;
+  args.pad = 0;
+  if (mode == DKV_PROMPT) {
+    if (!seq_lens || (!q_obs && !scores_in)) return DKV_ERR_ARG;
+    long long tok = 0;
+    for (int i = 0; i < n_req; i++) {
+      if (seq_lens[i] < 1 || seq_lens[i] > c.max_seq_len) return DKV_ERR_ARG;
+      if (P.h_active[base + req_slots[i]]) return DKV_ERR_STATE;
+      args.slots[i] = req_slots[i];
+      args.lens[i] = seq_lens[i];
+      args.tok0[i] = tok;
+      tok += seq_lens[i];
+    }
+    args.tok0[n_req] = tok;
+  } else {
+    if (seq_lens || q_obs || scores_in || scores_out) return DKV_ERR_ARG;
+    if (c.recent_window < 1) return DKV_ERR_ARG;
+    for (int i = 0; i < n_req; i++) {
+      if (!P.h_active[base + req_slots[i]]) return DKV_ERR_STATE;
+      if (P.h_n[base + req_slots[i]] + 1 > c.max_seq_len) return DKV_ERR_ARG;
+      args.slots[i] = req_slots[i];
+      args.lens[i] = 0;
+      args.tok0[i] = i;
+    }
+    args.tok0[n_req] = n_req;
+  }
+  DeviceGuard guard(P.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_setup(P, args, st);
+  if (e != cudaSuccess) return DKV_ERR_CUDA;
+  if (mode == DKV_PROMPT) {
+    int max_len = 0;
+    for (int i = 0; i < n_req; i++) max_len = std::max(max_len, seq_lens[i]);
+    e = launch_prompt(P, layer, n_req, max_len, static_cast<const __half*>(k), static_cast<const __half*>(v),
+                      static_cast<const __half*>(q_obs), scores_in, scores_out, st);
+    if (e != cudaSuccess) return DKV_ERR_CUDA;
+    for (int i = 0; i < n_req; i++) {
+      P.h_active[base + req_slots[i]] = 1;
+      P.h_n0[base + req_slots[i]] = seq_lens[i];
+      P.h_n[base + req_slots[i]] = seq_lens[i];
+    }
+  } else {
+    e = launch_decode(P, layer, n_req, static_cast<const __half*>(k), static_cast<const __half*>(v), st);
+    if (e != cudaSuccess) return DKV_ERR_CUDA;
+    for (int i = 0; i < n_req; i++) P.h_n[base + req_slots[i]] += 1;
+  }
+  return DKV_OK;
+}
+
+int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req, const int32_t* req_slots, const void* q,
+                         float* out, int32_t update_scores, void* stream) {
+  if (!pool || !req_slots || !q || !out) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  if (layer < 0 || layer >= c.n_layers || n_req < 1 || n_req > c.max_requests || n_req > kMaxCallReq)
+    return DKV_ERR_ARG;
+  const size_t base = (size_t)layer * c.max_requests;
+  CallArgs args;
+  args.n_req = n_req;
+  args.pad = 0;
+  int max_tokens = 1;
+  for (int i = 0; i < n_req; i++) {
+    if (req_slots[i] < 0 || req_slots[i] >= c.max_requests) return DKV_ERR_ARG;
+    for (int j = 0; j < i; j++)
+      if (req_slots[j] == req_slots[i]) return DKV_ERR_ARG;
+    if (!P.h_active[base + req_slots[i]]) return DKV_ERR_STATE;
+    args.slots[i] = req_slots[i];
+    args.lens[i] = P.h_n[base + req_slots[i]];
+    args.tok0[i] = i;
+    max_tokens = std::max(max_tokens, P.h_n[base + req_slots[i]]);
+  }
+  args.tok0[n_req] = n_req;
+  DeviceGuard guard(P.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_setup(P, args, st);
+  if (e == cudaSuccess)
+    e = launch_attention(P, layer, n_req, max_tokens, static_cast<const __half*>(q), out, update_scores ? 1 : 0, st);
+  return cuda_err(e);
+}
+
+int dkv_free_request(dkv_pool* pool, int32_t req_slot, void* stream) {
+  if (!pool) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  if (req_slot < 0 || req_slot >= c.max_requests) return DKV_ERR_ARG;
+  bool any = false;
+  for (int l = 0; l < c.n_layers; l++) any |= P.h_active[(size_t)l * c.max_requests + req_slot] != 0;
+  if (!any) return DKV_ERR_STATE;
+  DeviceGuard guard(P.device);
+  const cudaError_t e = launch_free(P, req_slot, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return DKV_ERR_CUDA;
+  for (int l = 0; l < c.n_layers; l++) {
+    const size_t x = (size_t)l * c.max_requests + req_slot;
+    P.h_active[x] = 0;
+    P.h_n0[x] = 0;
+    P.h_n[x] = 0;
+  }
+  return DKV_OK;
+}
+
+int dkv_pool_status(dkv_pool* pool, dkv_status* out) {
+  if (!pool || !out) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  DeviceGuard guard(P.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return DKV_ERR_CUDA;
+  Ctl c;
+  if (cudaMemcpy(&c, P.pv.ctl, sizeof(Ctl), cudaMemcpyDeviceToHost) != cudaSuccess) return DKV_ERR_CUDA;
+  const size_t heads = (size_t)P.cfg.n_layers * P.cfg.max_requests * P.cfg.n_kv_heads;
+  std::vector<int> cnt(heads * 4);
+  if (cudaMemcpy(cnt.data(), P.pv.counts, cnt.size() * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DKV_ERR_CUDA;
+  out->error = c.error;
+  out->error_info = c.error ? c.error_info : -1;
+  out->list_start = (int64_t)c.start;
+  out->list_end = (int64_t)c.end;
+  out->free_pages = (int64_t)(c.end - c.start);
+  out->hi_tokens = out->lo_tokens = out->hi_pages = out->lo_pages = 0;
+  for (size_t h = 0; h < heads; h++) {
+    out->hi_tokens += cnt[4 * h];
+    out->lo_tokens += cnt[4 * h + 1];
+    out->hi_pages += cnt[4 * h + 2];
+    out->lo_pages += cnt[4 * h + 3];
+  }
+  return DKV_OK;
+}
+
+int dkv_pool_clear_error(dkv_pool* pool) {
+  if (!pool) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  DeviceGuard guard(P.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return DKV_ERR_CUDA;
+  Ctl c;
+  if (cudaMemcpy(&c, P.pv.ctl, sizeof(Ctl), cudaMemcpyDeviceToHost) != cudaSuccess) return DKV_ERR_CUDA;
+  c.error = 0;
+  c.error_info = -1;
+  c.fail = 0;
+  if (cudaMemcpy(P.pv.ctl, &c, sizeof(Ctl), cudaMemcpyHostToDevice) != cudaSuccess) return DKV_ERR_CUDA;
+  std::vector<int> rq((size_t)P.cfg.n_layers * P.cfg.max_requests * 4);
+  if (cudaMemcpy(rq.data(), P.pv.req, rq.size() * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DKV_ERR_CUDA;
+  for (size_t x = 0; x < P.h_active.size(); x++) {
+    P.h_active[x] = rq[4 * x];
+    P.h_n0[x] = rq[4 * x + 1];
+    P.h_n[x] = rq[4 * x + 2];
+  }
+  return DKV_OK;
+}
+
+int dkv_pool_export(dkv_pool* pool, dkv_snapshot* out) {
+  if (!pool || !out) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  DeviceGuard guard(P.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return DKV_ERR_CUDA;
+  const size_t heads = (size_t)c.n_layers * c.max_requests * c.n_kv_heads;
+  cudaError_t e = cudaSuccess;
+  auto cp = [&](void* dst, const void* src, size_t bytes) {
+    if (dst && e == cudaSuccess) e = cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost);
+  };
+  cp(out->pages, P.pv.pages, (size_t)c.n_pages * c.page_bytes);
+  cp(out->free_list, P.pv.list, (size_t)c.n_pages * sizeof(int));
+  cp(out->table, P.pv.table, heads * P.pv.L * sizeof(int));
+  cp(out->head_counts, P.pv.counts, heads * 4 * sizeof(int));
+  cp(out->req_state, P.pv.req, (size_t)c.n_layers * c.max_requests * 4 * sizeof(int));
+  if (out->pointers && e == cudaSuccess) {
+    Ctl ctl;
+    e = cudaMemcpy(&ctl, P.pv.ctl, sizeof(Ctl), cudaMemcpyDeviceToHost);
+    out->pointers[0] = (int64_t)ctl.start;
+    out->pointers[1] = (int64_t)ctl.end;
+  }
+  return cuda_err(e);
+}
+
+}  // extern "C"

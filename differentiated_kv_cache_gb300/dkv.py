@@ -1,0 +1,209 @@
+"""ctypes binding of libdkv (include/dkv.h): same entry-point names, argument
+marshalling only. Every step of the compaction and attention path runs in the
+library's CUDA kernels; there is no fallback — importing this module on a
+machine without the built library raises.
+
+Tensors are PyTorch CUDA tensors (device memory and streams only); host
+arrays are anything numpy can turn into int32.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+DKV_OK, DKV_ERR_ARG, DKV_ERR_CUDA, DKV_ERR_STATE = 0, -1, -2, -3
+DKV_ERR_NO_PAGES, DKV_ERR_TABLE_FULL, DKV_ERR_TIMEOUT, DKV_ERR_CHECK, DKV_ERR_UNSUPPORTED = -4, -5, -6, -7, -8
+DKV_PROMPT, DKV_DECODE = 0, 1
+
+EXPORTED = ("dkv_pool_create", "dkv_pool_destroy", "dkv_pool_geometry", "dkv_compact_step",
+            "dkv_decode_attention", "dkv_free_request", "dkv_pool_status", "dkv_pool_clear_error",
+            "dkv_pool_export", "dkv_strerror")
+
+
+class dkv_config(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "n_layers", "n_kv_heads", "group_size", "head_dim", "page_bytes", "n_pages", "max_requests",
+        "max_seq_len", "tokens_per_hi_page", "tokens_per_lo_page", "lo_enabled")] + \
+        [("alpha_h", C.c_float), ("alpha_l", C.c_float)] + \
+        [(n, C.c_int32) for n in ("recent_window", "obs_window", "prompt_grant_slack", "reclaim_in_decode")]
+
+
+class dkv_geometry(C.Structure):
+    _fields_ = [("t_hi", C.c_int32), ("t_lo", C.c_int32), ("table_len", C.c_int32),
+                ("hi_off", C.c_int32 * 6), ("lo_off", C.c_int32 * 6), ("hi_used", C.c_int32),
+                ("lo_used", C.c_int32)]
+
+
+class dkv_status(C.Structure):
+    _fields_ = [("error", C.c_int32), ("error_info", C.c_int32)] + \
+        [(n, C.c_int64) for n in ("list_start", "list_end", "free_pages", "hi_tokens", "lo_tokens",
+                                  "hi_pages", "lo_pages")]
+
+
+class dkv_snapshot(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("pages", "free_list", "table", "head_counts", "req_state",
+                                          "pointers")]
+
+
+class DkvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {dkv_strerror(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> C.CDLL:
+    """Load libdkv.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"libdkv is not built ({_build.LIB}); run __graft_entry__.build()")
+        L = C.CDLL(_build.LIB)
+        P, I = C.c_void_p, C.c_int32
+        L.dkv_pool_create.argtypes = [C.POINTER(dkv_config), C.c_int, C.POINTER(C.c_void_p)]
+        L.dkv_pool_destroy.argtypes = [P]
+        L.dkv_pool_geometry.argtypes = [P, C.POINTER(dkv_geometry)]
+        L.dkv_compact_step.argtypes = [P, I, I, I, P, P, P, P, P, P, P, P]
+        L.dkv_decode_attention.argtypes = [P, I, I, P, P, P, I, P]
+        L.dkv_free_request.argtypes = [P, I, P]
+        L.dkv_pool_status.argtypes = [P, C.POINTER(dkv_status)]
+        L.dkv_pool_clear_error.argtypes = [P]
+        L.dkv_pool_export.argtypes = [P, C.POINTER(dkv_snapshot)]
+        L.dkv_strerror.argtypes = [C.c_int]
+        L.dkv_strerror.restype = C.c_char_p
+        for f in EXPORTED:
+            if f != "dkv_strerror":
+                getattr(L, f).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def dkv_strerror(code: int) -> str:
+    return load().dkv_strerror(int(code)).decode()
+
+
+def _check(rc: int, what: str) -> int:
+    if rc != DKV_OK:
+        raise DkvError(rc, what)
+    return rc
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32).reshape(-1))
+
+
+def _dptr(t, dtype=None, name="tensor"):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def make_config(**kw) -> dkv_config:
+    c = dkv_config()
+    defaults = dict(head_dim=128, page_bytes=4096, tokens_per_hi_page=0, tokens_per_lo_page=0, lo_enabled=1,
+                    alpha_h=2.0, alpha_l=0.25, recent_window=64, obs_window=32, prompt_grant_slack=1,
+                    reclaim_in_decode=1)
+    defaults.update(kw)
+    for name, _ in dkv_config._fields_:
+        setattr(c, name, defaults[name])
+    return c
+
+
+def dkv_pool_create(cfg, device: int = 0) -> C.c_void_p:
+    if isinstance(cfg, dict):
+        cfg = make_config(**cfg)
+    h = C.c_void_p()
+    _check(load().dkv_pool_create(C.byref(cfg), int(device), C.byref(h)), "dkv_pool_create")
+    return h
+
+
+def dkv_pool_destroy(pool) -> None:
+    _check(load().dkv_pool_destroy(pool), "dkv_pool_destroy")
+
+
+def dkv_pool_geometry(pool) -> dict:
+    g = dkv_geometry()
+    _check(load().dkv_pool_geometry(pool, C.byref(g)), "dkv_pool_geometry")
+    return dict(t_hi=g.t_hi, t_lo=g.t_lo, table_len=g.table_len, hi_off=list(g.hi_off), lo_off=list(g.lo_off),
+                hi_used=g.hi_used, lo_used=g.lo_used)
+
+
+def dkv_compact_step(pool, layer: int, mode: int, req_slots, seq_lens, k, v, q_obs=None, scores_in=None,
+                     scores_out=None, stream=None, check: bool = True) -> int:
+    import torch
+    slots = _i32(req_slots)
+    lens = None if seq_lens is None else _i32(seq_lens)
+    rc = load().dkv_compact_step(
+        pool, int(layer), int(mode), int(slots.size), slots.ctypes.data_as(C.c_void_p),
+        None if lens is None else lens.ctypes.data_as(C.c_void_p),
+        _dptr(k, torch.float16, "k"), _dptr(v, torch.float16, "v"), _dptr(q_obs, torch.float16, "q_obs"),
+        _dptr(scores_in, torch.float32, "scores_in"), _dptr(scores_out, torch.float32, "scores_out"),
+        _stream(stream))
+    return _check(rc, "dkv_compact_step") if check else rc
+
+
+def dkv_decode_attention(pool, layer: int, req_slots, q, out, update_scores: bool = False, stream=None,
+                         check: bool = True) -> int:
+    import torch
+    slots = _i32(req_slots)
+    rc = load().dkv_decode_attention(pool, int(layer), int(slots.size), slots.ctypes.data_as(C.c_void_p),
+                                     _dptr(q, torch.float16, "q"), _dptr(out, torch.float32, "out"),
+                                     int(bool(update_scores)), _stream(stream))
+    return _check(rc, "dkv_decode_attention") if check else rc
+
+
+def dkv_free_request(pool, req_slot: int, stream=None, check: bool = True) -> int:
+    rc = load().dkv_free_request(pool, int(req_slot), _stream(stream))
+    return _check(rc, "dkv_free_request") if check else rc
+
+
+def dkv_pool_status(pool) -> dict:
+    s = dkv_status()
+    _check(load().dkv_pool_status(pool, C.byref(s)), "dkv_pool_status")
+    return {n: getattr(s, n) for n, _ in dkv_status._fields_}
+
+
+def dkv_pool_clear_error(pool) -> None:
+    _check(load().dkv_pool_clear_error(pool), "dkv_pool_clear_error")
+
+
+def dkv_pool_export(pool, cfg: dict, table_len: int, pages: bool = True) -> dict:
+    """Host copy of the device state as numpy arrays, shaped like the oracle's."""
+    nl, mr, hk, npg = cfg["n_layers"], cfg["max_requests"], cfg["n_kv_heads"], cfg["n_pages"]
+    out = dict(
+        pages=np.zeros((npg, cfg["page_bytes"]) if pages else (0,), np.uint8),
+        free_list=np.zeros(npg, np.int32),
+        table=np.zeros((nl, mr, hk, table_len), np.int32),
+        head_counts=np.zeros((nl, mr, hk, 4), np.int32),
+        req_state=np.zeros((nl, mr, 4), np.int32),
+        pointers=np.zeros(2, np.int64))
+    snap = dkv_snapshot()
+    for name in ("free_list", "table", "head_counts", "req_state", "pointers"):
+        setattr(snap, name, out[name].ctypes.data_as(C.c_void_p))
+    snap.pages = out["pages"].ctypes.data_as(C.c_void_p) if pages else None
+    _check(load().dkv_pool_export(pool, C.byref(snap)), "dkv_pool_export")
+    return out

@@ -564,6 +564,9 @@ int orc_decode_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
   const int H = c->n_kv_heads;
   const int th = p->tg[TIER_HI].t, tl = p->tg[TIER_LO].t, L = p->table_len;
   if (layer < 0 || layer >= c->n_layers || n_req < 1 || n_req > c->max_requests) return ORC_ERR_ARG;
+  /* generation-phase compaction needs a recent window of at least one token,
+   * so that the newest token is never its own candidate */
+  if (c->window < 1) return ORC_ERR_ARG;
   for (int i = 0; i < n_req; i++) {
     if (slots[i] < 0 || slots[i] >= c->max_requests) return ORC_ERR_ARG;
     for (int j = 0; j < i; j++) if (slots[j] == slots[i]) return ORC_ERR_ARG;

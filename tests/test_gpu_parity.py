@@ -1,0 +1,363 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs. Integer and page state bit-exact; scores and attention
+within stated tolerances."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests import parity
+from tests.gpu_pool import GPool, stored, tiers_of
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+# Attention: |gpu - ref| <= ATOL + RTOL |ref| elementwise (fp64 reference over
+# the same dequantised values).
+ATT_ATOL, ATT_RTOL = 1e-3, 2e-3
+# Scores: fp32 tensor-core logits and exp2 against fp64 (see the design doc reading).
+SC_ATOL, SC_RTOL = 1e-6, 5e-5
+# Tie band: a token whose fp64 importance lies within this relative distance of
+# a threshold may land on either side.
+TIE_RTOL = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import differentiated_kv_cache_gb300 as dkv
+    dkv.build.build()
+    dkv.load()
+
+
+def cfg_of(**over):
+    c = dict(n_layers=1, n_kv_heads=2, group_size=4, head_dim=128, page_bytes=4096, n_pages=512,
+             max_requests=6, max_seq_len=1200, tokens_per_hi_page=0, tokens_per_lo_page=0, lo_enabled=1,
+             alpha_h=2.0, alpha_l=0.25, recent_window=64, obs_window=32, prompt_grant_slack=1,
+             reclaim_in_decode=1)
+    c.update(over)
+    return c
+
+
+def both(cfg):
+    return GPool(cfg), oracle.Pool(cfg)
+
+
+def assert_same(gp, op, **kw):
+    parity.compare_states(gp.snapshot(), op.snapshot(), gp.t_hi, gp.t_lo, gp.cfg["n_pages"],
+                          gp.cfg["page_bytes"], **kw)
+
+
+# ------------------------------------------------------------------ Figure 6
+def test_figure6_on_gpu():
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "fig6_prompt_workflow.json")))
+    cfg = cfg_of(tokens_per_hi_page=2, tokens_per_lo_page=4, prompt_grant_slack=0, recent_window=0,
+                 n_pages=16, max_requests=1, max_seq_len=8)
+    tiers = {0: "HLLPHLPL", 1: "HHLHLPHP"}
+    imp = {"H": 1.0, "L": 0.1, "P": 0.001}
+    S = np.array([[imp[tiers[h][j]] * min(32, 8 - j) for h in (0, 1)] for j in range(8)], np.float32)
+    k = workloads.random_fp16((8, 2, 128), 1)
+    v = workloads.random_fp16((8, 2, 128), 2)
+    gp, op = both(cfg)
+    with gp:
+        gp.prompt(0, [0], [8], k, v, scores_in=S)
+        assert op.prompt(0, [0], [8], k, v, scores_in=S) == 0
+        snap = gp.snapshot()
+        # the page's example starts with pages 0-4 allocated; here the list starts at 0,
+        # so every page ID is the figure's minus 5
+        sh = gold["config"]["list_start_before"]
+        L = gp.table_len
+        for h, name in ((0, "A"), (1, "B")):
+            row = snap["table"][0, 0, h]
+            hi = gold["expected"]["hi_pages"][name]; lo = gold["expected"]["lo_pages"][name]
+            assert [int(x) + sh for x in row[:len(hi)]] == hi
+            assert [int(row[L - 1 - x]) + sh for x in range(len(lo))] == lo
+        rec = [int(snap["free_list"][c % 16]) + sh for c in range(16, int(snap["pointers"][1]))]
+        assert rec == gold["expected"]["reclaimed_in_order"]
+        assert int(snap["pointers"][0]) + sh == gold["expected"]["list_start_after"]
+        assert_same(gp, op)
+
+
+# ---------------------------------------------------- prompt, given scores
+@pytest.mark.parametrize("G,H,lens", [(4, 2, [512, 700]), (1, 3, [1, 31, 129, 300]), (5, 2, [1029, 64, 65]),
+                                      (7, 1, [777]), (8, 2, [256, 257])])
+def test_prompt_given_scores_bit_exact(G, H, lens):
+    cfg = cfg_of(group_size=G, n_kv_heads=H, n_pages=2048, max_requests=len(lens) + 1)
+    n = sum(lens)
+    k = workloads.random_fp16((n, H, 128), 10 + G, scale=2.0)
+    v = workloads.random_fp16((n, H, 128), 20 + G)
+    S = workloads.given_scores(n, H, seed=G, scale=1.0)
+    slots = list(range(1, len(lens) + 1))           # not starting at 0
+    gp, op = both(cfg)
+    with gp:
+        rc, so = gp.prompt(0, slots, lens, k, v, scores_in=S, want_scores=True)
+        assert op.prompt(0, slots, lens, k, v, scores_in=S) == 0
+        assert (so == S).all()
+        assert_same(gp, op)
+        st = gp.status()
+        assert st["error"] == 0 and st["hi_tokens"] + st["lo_tokens"] > 0
+
+
+@pytest.mark.parametrize("over", [dict(lo_enabled=0), dict(alpha_h=math.inf, alpha_l=0.0),
+                                  dict(alpha_h=0.0, alpha_l=0.0), dict(recent_window=0),
+                                  dict(tokens_per_hi_page=4, tokens_per_lo_page=8, prompt_grant_slack=3)])
+def test_prompt_special_configs_bit_exact(over):
+    cfg = cfg_of(n_pages=2048, **over)
+    lens = [300, 5, 700]
+    n = sum(lens)
+    k = workloads.random_fp16((n, 2, 128), 1)
+    v = workloads.random_fp16((n, 2, 128), 2)
+    S = workloads.given_scores(n, 2, seed=3)
+    gp, op = both(cfg)
+    with gp:
+        gp.prompt(0, [0, 1, 2], lens, k, v, scores_in=S)
+        assert op.prompt(0, [0, 1, 2], lens, k, v, scores_in=S) == 0
+        assert_same(gp, op)
+
+
+# ------------------------------------------------- prompt, computed scores
+def _tie_tokens(S64, lens, H, alpha_h, alpha_l, window, lo_enabled):
+    ties = np.zeros(S64.shape, bool)
+    t0 = 0
+    for n0 in lens:
+        j = np.arange(n0)
+        c = np.minimum(32, n0 - j)[:, None]
+        I = S64[t0:t0 + n0] / c * n0
+        near = np.zeros_like(I, bool)
+        for a in ([alpha_h, alpha_l] if lo_enabled else [alpha_l]):
+            if np.isfinite(a) and a > 0:
+                near |= np.abs(I - a) <= TIE_RTOL * a
+        near[j >= n0 - window] = False
+        ties[t0:t0 + n0] = near
+        t0 += n0
+    return ties
+
+
+def _inputs(name, reqs, max_len, G_override=None):
+    """Workload inputs for a few requests, prompts cut to max_len tokens
+    (the observation queries stay those of the generated prompt)."""
+    if name == "random8":
+        rng_k = workloads.random_fp16((1700, 2, 128), 77, scale=1.5)
+        return dict(k=rng_k, v=workloads.random_fp16((1700, 2, 128), 78),
+                    q_obs=workloads.random_fp16((2, 32, 16, 128), 79), lens=np.array([700, 1000], np.int32)), 2
+    inp = workloads.prompt_inputs(name, 0, requests=reqs)
+    H = workloads.WORKLOADS[name].n_kv_heads
+    lens = [int(x) for x in inp["lens"]]
+    if max(lens) > max_len:
+        ks, vs, t0 = [], [], 0
+        for n0 in lens:
+            m = min(n0, max_len)
+            ks.append(inp["k"][t0:t0 + m]); vs.append(inp["v"][t0:t0 + m])
+            t0 += n0
+        inp["k"], inp["v"] = np.concatenate(ks), np.concatenate(vs)
+        inp["lens"] = np.minimum(inp["lens"], max_len)
+    return inp, H
+
+
+@pytest.mark.parametrize("name,G,reqs", [("tiny", 4, None), ("qwq32b", 5, [0, 1]), ("qwen7b", 7, [0]),
+                                         ("random8", 8, None)])
+def test_prompt_computed_scores(name, G, reqs):
+    inp, H = _inputs(name, reqs, 3000)
+    lens = [int(x) for x in inp["lens"]]
+    lo_enabled = workloads.WORKLOADS[name].lo_enabled if name in workloads.WORKLOADS else 1
+    cfg = cfg_of(n_kv_heads=H, group_size=G, n_pages=4096, max_requests=len(lens), max_seq_len=max(lens) + 8,
+                 lo_enabled=lo_enabled)
+    gp = GPool(cfg)
+    op = oracle.Pool(cfg)
+    slots = list(range(len(lens)))
+    with gp:
+        rc, so = gp.prompt(0, slots, lens, inp["k"], inp["v"], inp["q_obs"], want_scores=True)
+        S64 = np.zeros((sum(lens), H))
+        t0 = 0
+        for i, n0 in enumerate(lens):
+            for h in range(H):
+                S64[t0:t0 + n0, h] = oracle.unit_scores(inp["k"][t0:t0 + n0, h],
+                                                        inp["q_obs"][i][:, h * G:(h + 1) * G])
+            t0 += n0
+        ok, worst = parity.within(so.astype(np.float64), S64, SC_ATOL, SC_RTOL)
+        rel = np.abs(so - S64) / np.maximum(S64, 1e-30)
+        print(f"{name}: score max rel err {rel.max():.3e}, tolerance excess {worst:.3e}")
+        assert ok, worst
+        ties = _tie_tokens(S64, lens, H, cfg["alpha_h"], cfg["alpha_l"], cfg["recent_window"], cfg["lo_enabled"])
+        assert op.prompt(0, slots, lens, inp["k"], inp["v"], inp["q_obs"]) == 0
+        gs, os_ = gp.snapshot(), op.snapshot()
+        t0 = 0
+        clean = []
+        for i, n0 in enumerate(lens):
+            for h in range(H):
+                tg = tiers_of(gs, (0, i, h), n0, gp.t_hi, gp.t_lo)
+                to = tiers_of(os_, (0, i, h), n0, gp.t_hi, gp.t_lo)
+                tie = ties[t0:t0 + n0, h]
+                assert (tg[~tie] == to[~tie]).all(), f"tier differs outside the tie band (req {i}, head {h})"
+                if (tg == to).all():
+                    clean.append((0, i, h))
+            t0 += n0
+        print(f"{name}: {int(ties.sum())} tokens in the tie band; {len(clean)}/{len(lens) * H} heads identical")
+        # heads whose tiers agree: identical pages up to the score words (fp32 vs fp64 sums)
+        parity.compare_states(gs, os_, gp.t_hi, gp.t_lo, cfg["n_pages"], cfg["page_bytes"], heads=clean,
+                              scores=False)
+        if len(clean) == len(lens) * H:
+            parity.compare_states(gs, os_, gp.t_hi, gp.t_lo, cfg["n_pages"], cfg["page_bytes"], scores=False)
+
+
+# --------------------------------------------------------------- decode
+@pytest.mark.parametrize("over", [dict(), dict(alpha_h=1.0, alpha_l=0.6), dict(lo_enabled=0, alpha_l=0.5),
+                                  dict(tokens_per_hi_page=2, tokens_per_lo_page=4, recent_window=3),
+                                  dict(reclaim_in_decode=0, alpha_h=4.0, alpha_l=1.0, recent_window=8)])
+def test_decode_steps_bit_exact(over):
+    cfg = cfg_of(max_seq_len=1000, n_pages=4096, **over)
+    lens = [200, 333, 70]
+    n = sum(lens)
+    H = cfg["n_kv_heads"]
+    k = workloads.random_fp16((n, H, 128), 7)
+    v = workloads.random_fp16((n, H, 128), 8)
+    S = workloads.given_scores(n, H, seed=9)
+    slots = [0, 2, 4]
+    gp, op = both(cfg)
+    with gp:
+        gp.prompt(0, slots, lens, k, v, scores_in=S)
+        assert op.prompt(0, slots, lens, k, v, scores_in=S) == 0
+        for step in range(40):
+            kn = workloads.random_fp16((3, H, 128), 100 + step)
+            vn = workloads.random_fp16((3, H, 128), 200 + step)
+            gp.decode(0, slots, kn, vn)
+            assert op.decode(0, slots, kn, vn) == 0
+            if step % 8 == 7 or step < 3:
+                assert_same(gp, op)
+        for s in slots:
+            gp.free(s)
+            assert op.free_request(s) == 0
+        assert_same(gp, op)
+        st = gp.status()
+        assert st["free_pages"] == cfg["n_pages"] and st["error"] == 0
+
+
+# ------------------------------------------------------------ attention
+@pytest.mark.parametrize("G,H,lens,steps", [(4, 2, [512, 700], 5), (1, 2, [40, 1], 3), (5, 3, [1030, 17], 2),
+                                            (7, 1, [2000], 1), (8, 2, [300, 301], 4)])
+def test_decode_attention_parity(G, H, lens, steps):
+    cfg = cfg_of(group_size=G, n_kv_heads=H, n_pages=4096, max_seq_len=2100, max_requests=len(lens))
+    n = sum(lens)
+    k = workloads.random_fp16((n, H, 128), 30, scale=1.5)
+    v = workloads.random_fp16((n, H, 128), 31)
+    S = workloads.given_scores(n, H, seed=32)
+    slots = list(range(len(lens)))
+    gp, op = both(cfg)
+    with gp:
+        gp.prompt(0, slots, lens, k, v, scores_in=S)
+        op.prompt(0, slots, lens, k, v, scores_in=S)
+        for step in range(steps):
+            kn = workloads.random_fp16((len(lens), H, 128), 300 + step)
+            vn = workloads.random_fp16((len(lens), H, 128), 400 + step)
+            gp.decode(0, slots, kn, vn)
+            op.decode(0, slots, kn, vn)
+            q = workloads.random_fp16((len(lens), H * G, 128), 500 + step, scale=2.0)
+            out = gp.attention(0, slots, q)
+            rc, ref = op.attention(0, slots, q)
+            ok, worst = parity.within(out.astype(np.float64), ref, ATT_ATOL, ATT_RTOL)
+            ratio = (np.abs(out - ref) / (ATT_ATOL + ATT_RTOL * np.abs(ref))).max()
+            print(f"G={G}: attention max abs err {np.abs(out - ref).max():.3e}, max err/tolerance {ratio:.3f}")
+            assert ok, worst
+        assert_same(gp, op)
+
+
+def test_attention_score_update():
+    cfg = cfg_of(group_size=4, n_kv_heads=2, n_pages=2048, max_requests=2)
+    lens = [600, 257]
+    n = sum(lens)
+    k = workloads.random_fp16((n, 2, 128), 40, scale=1.5)
+    v = workloads.random_fp16((n, 2, 128), 41)
+    S = workloads.given_scores(n, 2, seed=42)
+    gp, op = both(cfg)
+    with gp:
+        gp.prompt(0, [0, 1], lens, k, v, scores_in=S)
+        op.prompt(0, [0, 1], lens, k, v, scores_in=S)
+        for step in range(3):
+            q = workloads.random_fp16((2, 8, 128), 600 + step, scale=2.0)
+            gp.attention(0, [0, 1], q, update=True)
+            op.attention(0, [0, 1], q, update_scores=True)
+        gs, os_ = gp.snapshot(), op.snapshot()
+        assert (gs["req_state"] == os_["req_state"]).all()
+        for i in range(2):
+            for h in range(2):
+                for a, b in zip(stored(gs, (0, i, h), gp.t_hi, gp.t_lo, 4, np.float32),
+                                stored(os_, (0, i, h), gp.t_hi, gp.t_lo, 4, np.float32)):
+                    ok, worst = parity.within(a.astype(np.float64), b.astype(np.float64), 1e-6, 1e-4)
+                    assert ok, worst
+
+
+# -------------------------------------------------------------- errors
+def test_errors_are_transactional_and_sticky():
+    cfg = cfg_of(n_pages=40)
+    lens = [500]
+    k = workloads.random_fp16((500, 2, 128), 1)
+    S = workloads.given_scores(500, 2, seed=1)
+    gp, op = both(cfg)
+    with gp:
+        before = gp.snapshot()
+        gp.prompt(0, [0], lens, k, k, scores_in=S)          # needs 2 x 29 pages > 40
+        st = gp.status()
+        assert st["error"] == -4 and st["free_pages"] == 40
+        after = gp.snapshot()
+        for key in ("free_list", "table", "head_counts", "req_state", "pointers"):
+            assert (before[key] == after[key]).all(), key
+        # sticky: a call that would fit is a no-op until the error is cleared
+        gp.prompt(0, [1], [10], k[:10], k[:10], scores_in=S[:10])
+        assert gp.status()["hi_tokens"] == 0
+        import differentiated_kv_cache_gb300 as dkv
+        dkv.dkv_pool_clear_error(gp.h)
+        gp.prompt(0, [1], [10], k[:10], k[:10], scores_in=S[:10])
+        assert op.prompt(0, [1], [10], k[:10], k[:10], scores_in=S[:10]) == 0
+        assert gp.status()["error"] == 0
+        assert_same(gp, op)
+        # host-side state errors return at once
+        assert gp.decode(0, [0], k[:1], k[:1], check=False) == dkv.DKV_ERR_STATE
+        assert gp.free(3, check=False) == dkv.DKV_ERR_STATE
+        assert gp.prompt(0, [1], [10], k[:10], k[:10], scores_in=S[:10], check=False) == dkv.DKV_ERR_STATE
+
+
+def test_grant_short_with_zero_slack():
+    cfg = cfg_of(tokens_per_hi_page=2, tokens_per_lo_page=4, prompt_grant_slack=0, recent_window=0,
+                 max_seq_len=8, n_pages=16)
+    S = np.zeros((2, 2), np.float32); S[0] = 10.0; S[1] = 0.2
+    k = workloads.random_fp16((2, 2, 128), 3)
+    with GPool(cfg) as gp:
+        before = gp.snapshot()
+        gp.prompt(0, [0], [2], k, k, scores_in=S)
+        assert gp.status()["error"] == -5
+        after = gp.snapshot()
+        for key in ("free_list", "table", "head_counts", "req_state", "pointers"):
+            assert (before[key] == after[key]).all(), key
+
+
+def test_attention_on_workload_with_outliers():
+    """The tiny workload itself (outlier channels x8, scores computed from the
+    observation queries), a few decode steps with score updates: attention
+    against the oracle's fp64 attention over its own pages."""
+    w = workloads.WORKLOADS["tiny"]
+    inp = workloads.prompt_inputs("tiny", 0)
+    lens = [int(x) for x in inp["lens"]]
+    cfg = w.pool_config()
+    gp, op = both(cfg)
+    with gp:
+        gp.prompt(0, [0, 1], lens, inp["k"], inp["v"], inp["q_obs"])
+        op.prompt(0, [0, 1], lens, inp["k"], inp["v"], inp["q_obs"])
+        gs, os_ = gp.snapshot(), op.snapshot()
+        if not ((gs["head_counts"] == os_["head_counts"]).all() and (gs["table"] == os_["table"]).all()):
+            pytest.skip("a tie-band token put the two pools on different tiers")
+        worst_ratio = 0.0
+        for step in range(4):
+            d = workloads.decode_inputs("tiny", step)
+            gp.decode(0, [0, 1], d["k"], d["v"])
+            op.decode(0, [0, 1], d["k"], d["v"])
+            out = gp.attention(0, [0, 1], d["q"], update=False)
+            rc, ref = op.attention(0, [0, 1], d["q"], update_scores=False)
+            ratio = (np.abs(out - ref) / (ATT_ATOL + ATT_RTOL * np.abs(ref))).max()
+            worst_ratio = max(worst_ratio, ratio)
+        print(f"tiny workload: attention max err/tolerance {worst_ratio:.3f}")
+        assert worst_ratio <= 1.0
