@@ -9,8 +9,7 @@ namespace dkv {
 
 constexpr int kCoordThreads = 1024;
 
-// Copy the call's host arrays into the pool's device CallArgs and derive the
-// call's no-op flag from the sticky status.
+// Copy the call's host arrays into the pool's device CallArgs.
 __global__ void k_setup(PoolView pv, CallArgs args) {
   CallArgs* c = pv.call;
   const int n = args.n_req;
@@ -22,7 +21,6 @@ __global__ void k_setup(PoolView pv, CallArgs args) {
   if (threadIdx.x == 0) {
     c->n_req = n;
     c->tok0[n] = args.tok0[n];
-    pv.ctl->fail = pv.ctl->error != 0 ? 1 : 0;
   }
 }
 
@@ -55,9 +53,26 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
   return excl;
 }
 
+// In-place exclusive scan of arr[0..n) in shared memory over the whole block
+// (each thread scans a contiguous run); returns the total.
+__device__ int block_scan_array(int* arr, int n, int* s_warp) {
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int a0 = min(n, (int)threadIdx.x * per), a1 = min(n, a0 + per);
+  int sum = 0;
+  for (int x = a0; x < a1; x++) sum += arr[x];
+  int total;
+  int run = block_exclusive_scan(sum, s_warp, &total);
+  for (int x = a0; x < a1; x++) {
+    const int v = arr[x];
+    arr[x] = run;
+    run += v;
+  }
+  __syncthreads();
+  return total;
+}
+
 __device__ __forceinline__ void latch_error(PoolView& pv, int code, int info) {
   if (atomicCAS(&pv.ctl->error, 0, code) == 0) pv.ctl->error_info = info;
-  pv.ctl->fail = 1;
 }
 
 // ---------------------------------------------------------------------------
@@ -68,39 +83,49 @@ __device__ __forceinline__ void latch_error(PoolView& pv, int code, int info) {
 // counters and request state written. All checks precede every write.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCoordThreads) k_prompt_plan(PoolView pv, int layer, Scratch sc) {
-  if (pv.ctl->fail) return;
+  if (pv.noop()) return;
+  extern __shared__ int s_dyn[];
   __shared__ int s_warp[32];
   __shared__ int s_err, s_info;
   const CallArgs* ca = pv.call;
   const int n_units = ca->n_req * pv.hkv;
-  const int per = (n_units + kCoordThreads - 1) / kCoordThreads;
-  const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
+  int* s_g = s_dyn;              // grant pages per unit -> exclusive offsets
+  int* s_r = s_dyn + n_units;    // reclaimed pages per unit -> exclusive offsets
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
   __syncthreads();
-  int my_g = 0, my_r = 0;
-  for (int u = u0; u < u1; u++) {
-    const int i = u / pv.hkv;
-    const int n0 = ca->lens[i];
+  // planning summary per head (warp per head): tier counts, block bases, page needs
+  for (int u = warp; u < n_units; u += nw) {
+    const int n0 = ca->lens[u / pv.hkv];
     const int nkb = (n0 + kKeyBlock - 1) / kKeyBlock;
     int a = 0, b = 0;
-    for (int kb = 0; kb < nkb; kb++) {
-      const int2 c = sc.bcnt[(size_t)u * sc.nkb_cap + kb];
-      sc.bbase[(size_t)u * sc.nkb_cap + kb] = make_int2(a, b);
-      a += c.x;
-      b += c.y;
+    for (int k0 = 0; k0 < nkb; k0 += 32) {
+      const int kb = k0 + lane;
+      const int2 c = kb < nkb ? sc.bcnt[(size_t)u * sc.nkb_cap + kb] : make_int2(0, 0);
+      int x = c.x, y = c.y;
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) {
+        const int xo = __shfl_up_sync(0xffffffffu, x, s), yo = __shfl_up_sync(0xffffffffu, y, s);
+        if (lane >= s) { x += xo; y += yo; }
+      }
+      if (kb < nkb) sc.bbase[(size_t)u * sc.nkb_cap + kb] = make_int2(a + x - c.x, b + y - c.y);
+      a += __shfl_sync(0xffffffffu, x, 31);
+      b += __shfl_sync(0xffffffffu, y, 31);
     }
-    const int gh = (n0 + pv.hi.t - 1) / pv.hi.t + pv.slack;
-    const int nhp = (a + pv.hi.t - 1) / pv.hi.t, nlp = (b + pv.lo.t - 1) / pv.lo.t;
-    if (nhp + nlp > gh || nhp + nlp > pv.L) {
-      if (atomicCAS(&s_err, 0, DKV_ERR_TABLE_FULL) == 0) s_info = u;
+    if (lane == 0) {
+      const int gh = (n0 + pv.hi.t - 1) / pv.hi.t + pv.slack;
+      const int nhp = (a + pv.hi.t - 1) / pv.hi.t, nlp = (b + pv.lo.t - 1) / pv.lo.t;
+      if (nhp + nlp > gh || nhp + nlp > pv.L) {
+        if (atomicCAS(&s_err, 0, DKV_ERR_TABLE_FULL) == 0) s_info = u;
+      }
+      sc.unit_info[u] = make_int4(gh, a, b, 0);
+      s_g[u] = gh;
+      s_r[u] = max(0, gh - nhp - nlp);
     }
-    sc.unit_info[u] = make_int4(gh, a, b, 0);
-    my_g += gh;
-    my_r += max(0, gh - nhp - nlp);
   }
-  int tot_g, tot_r;
-  const int goff = block_exclusive_scan(my_g, s_warp, &tot_g);
-  const int roff = block_exclusive_scan(my_r, s_warp, &tot_r);
+  __syncthreads();
+  const int tot_g = block_scan_array(s_g, n_units, s_warp);
+  const int tot_r = block_scan_array(s_r, n_units, s_warp);
   const unsigned long long start = pv.ctl->start, end = pv.ctl->end;
   if (threadIdx.x == 0 && s_err == 0 && (unsigned long long)tot_g > end - start) s_err = DKV_ERR_NO_PAGES;
   __syncthreads();
@@ -108,31 +133,35 @@ __global__ void __launch_bounds__(kCoordThreads) k_prompt_plan(PoolView pv, int 
     if (threadIdx.x == 0) latch_error(pv, s_err, s_info);
     return;
   }
-  // grant: read the granted page IDs before any reclaim write can overwrite them
-  int o = goff;
-  for (int u = u0; u < u1; u++) {
+  // coordination 1: the granted page IDs, read before any reclaim write
+  for (int u = warp; u < n_units; u += nw) {
     const int gh = sc.unit_info[u].x;
     int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
-    for (int x = 0; x < gh; x++) gid[x] = pv.list[(start + (unsigned long long)(o + x)) % pv.n_pages];
-    o += gh;
+    for (int x = lane; x < gh; x += 32) gid[x] = pv.list[(start + (unsigned long long)(s_g[u] + x)) % pv.n_pages];
   }
   __syncthreads();
-  int r = roff;
-  for (int u = u0; u < u1; u++) {
+  // coordination 2: reclaim the unused middle pages; table rows, counters, state
+  for (int u = warp; u < n_units; u += nw) {
     const int i = u / pv.hkv, kvh = u % pv.hkv, slot = ca->slots[i];
     const int4 ui = sc.unit_info[u];
     const int gh = ui.x, nhp = (ui.y + pv.hi.t - 1) / pv.hi.t, nlp = (ui.z + pv.lo.t - 1) / pv.lo.t;
     const int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
-    for (int x = nhp; x < gh - nlp; x++) pv.list[(end + (unsigned long long)(r++)) % pv.n_pages] = gid[x];
+    for (int x = nhp + lane; x < gh - nlp; x += 32)
+      pv.list[(end + (unsigned long long)(s_r[u] + x - nhp)) % pv.n_pages] = gid[x];
     int* row = pv.row(layer, slot, kvh);
-    for (int e = 0; e < pv.L; e++) row[e] = -1;
-    for (int x = 0; x < nhp; x++) row[x] = gid[x];
-    for (int x = 0; x < nlp; x++) row[pv.L - 1 - x] = gid[gh - 1 - x];
-    int* cn = pv.cnt(layer, slot, kvh);
-    cn[0] = ui.y; cn[1] = ui.z; cn[2] = nhp; cn[3] = nlp;
-    if (kvh == 0) {
-      int* rq = pv.rq(layer, slot);
-      rq[0] = 1; rq[1] = ca->lens[i]; rq[2] = ca->lens[i]; rq[3] = 0;
+    for (int e = lane; e < pv.L; e += 32) {
+      int v = -1;
+      if (e < nhp) v = gid[e];
+      else if (e >= pv.L - nlp) v = gid[gh - 1 - (pv.L - 1 - e)];
+      row[e] = v;
+    }
+    if (lane == 0) {
+      int* cn = pv.cnt(layer, slot, kvh);
+      cn[0] = ui.y; cn[1] = ui.z; cn[2] = nhp; cn[3] = nlp;
+      if (kvh == 0) {
+        int* rq = pv.rq(layer, slot);
+        rq[0] = 1; rq[1] = ca->lens[i]; rq[2] = ca->lens[i]; rq[3] = 0;
+      }
     }
   }
   __syncthreads();
@@ -148,12 +177,12 @@ __global__ void __launch_bounds__(kCoordThreads) k_prompt_plan(PoolView pv, int 
 // (reclaim_in_decode) by one prefix sum at the list end; table rows,
 // counters and the request lengths updated. All checks precede every write.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int layer, Scratch sc) {
-  if (pv.ctl->fail) return;
+__global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int layer, Scratch sc,
+                                                                 SlotArgs sa) {
+  if (pv.noop()) return;
   __shared__ int s_warp[32];
   __shared__ int s_err, s_info;
-  const CallArgs* ca = pv.call;
-  const int n_units = ca->n_req * pv.hkv;
+  const int n_units = sa.n * pv.hkv;
   const int per = (n_units + kCoordThreads - 1) / kCoordThreads;
   const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
   if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
@@ -183,7 +212,7 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
   int a = aoff, f = foff;
   for (int u = u0; u < u1; u++) {
     const DecodePlan& p = sc.dplan[u];
-    const int i = u / pv.hkv, kvh = u % pv.hkv, slot = ca->slots[i];
+    const int i = u / pv.hkv, kvh = u % pv.hkv, slot = sa.slots[i];
     int* cn = pv.cnt(layer, slot, kvh);
     int* row = pv.row(layer, slot, kvh);
     if (p.new_hp) row[cn[2]] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
@@ -212,38 +241,45 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
 // appended at the list end by one prefix sum; rows and state cleared.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCoordThreads) k_free_request(PoolView pv, int slot) {
-  if (pv.ctl->error != 0) return;
+  if (pv.noop()) return;
+  extern __shared__ int s_dyn[];
   __shared__ int s_warp[32];
   const int n_units = pv.n_layers * pv.hkv;
-  const int per = (n_units + kCoordThreads - 1) / kCoordThreads;
-  const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
-  int mine = 0;
-  for (int u = u0; u < u1; u++) {
+  int* s_c = s_dyn;             // pages per (layer, KV head) -> exclusive offsets
+  int* s_h = s_dyn + n_units;   // hi pages per (layer, KV head)
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
     const int layer = u / pv.hkv, kvh = u % pv.hkv;
-    if (!pv.rq(layer, slot)[0]) continue;
     const int* cn = pv.cnt(layer, slot, kvh);
-    mine += cn[2] + cn[3];
-  }
-  int tot;
-  int o = block_exclusive_scan(mine, s_warp, &tot);
-  const unsigned long long end = pv.ctl->end;
-  for (int u = u0; u < u1; u++) {
-    const int layer = u / pv.hkv, kvh = u % pv.hkv;
-    int* cn = pv.cnt(layer, slot, kvh);
-    int* row = pv.row(layer, slot, kvh);
-    if (pv.rq(layer, slot)[0]) {
-      for (int x = 0; x < cn[2]; x++) pv.list[(end + (unsigned long long)(o++)) % pv.n_pages] = row[x];
-      for (int x = 0; x < cn[3]; x++) pv.list[(end + (unsigned long long)(o++)) % pv.n_pages] = row[pv.L - 1 - x];
-    }
-    for (int e = 0; e < pv.L; e++) row[e] = -1;
-    cn[0] = cn[1] = cn[2] = cn[3] = 0;
+    const bool act = pv.rq(layer, slot)[0] != 0;
+    s_c[u] = act ? cn[2] + cn[3] : 0;
+    s_h[u] = act ? cn[2] : 0;
   }
   __syncthreads();
-  if (threadIdx.x == 0) pv.ctl->end = end + (unsigned long long)tot;
+  const int tot = block_scan_array(s_c, n_units, s_warp);
+  const unsigned long long end = pv.ctl->end;
+  for (int u = 0; u < n_units; u++) {
+    const int cnt = (u + 1 < n_units ? s_c[u + 1] : tot) - s_c[u];
+    if (cnt == 0) continue;
+    const int* row = pv.row(u / pv.hkv, slot, u % pv.hkv);
+    const int nh = s_h[u];
+    for (int x = threadIdx.x; x < cnt; x += blockDim.x)
+      pv.list[(end + (unsigned long long)(s_c[u] + x)) % pv.n_pages] = x < nh ? row[x] : row[pv.L - 1 - (x - nh)];
+  }
+  __syncthreads();
+  for (int u = 0; u < n_units; u++) {
+    int* row = pv.row(u / pv.hkv, slot, u % pv.hkv);
+    for (int e = threadIdx.x; e < pv.L; e += blockDim.x) row[e] = -1;
+  }
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
+    int* cn = pv.cnt(u / pv.hkv, slot, u % pv.hkv);
+    cn[0] = cn[1] = cn[2] = cn[3] = 0;
+  }
   for (int layer = threadIdx.x; layer < pv.n_layers; layer += blockDim.x) {
     int* rq = pv.rq(layer, slot);
     rq[0] = rq[1] = rq[2] = rq[3] = 0;
   }
+  __syncthreads();
+  if (threadIdx.x == 0) pv.ctl->end = end + (unsigned long long)tot;
 }
 
 // ---------------------------------------------------------------------------
@@ -252,18 +288,27 @@ cudaError_t launch_setup(const Pool& P, const CallArgs& args, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_prompt_plan(Pool& P, int layer, cudaStream_t st) {
-  k_prompt_plan<<<1, kCoordThreads, 0, st>>>(P.pv, layer, P.sc);
+cudaError_t launch_prompt_plan(Pool& P, int layer, int n_req, cudaStream_t st) {
+  const int smem = 2 * n_req * P.pv.hkv * (int)sizeof(int);
+  k_prompt_plan<<<1, kCoordThreads, smem, st>>>(P.pv, layer, P.sc);
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_alloc(Pool& P, int layer, cudaStream_t st) {
-  k_decode_alloc<<<1, kCoordThreads, 0, st>>>(P.pv, layer, P.sc);
+cudaError_t configure_alloc() {
+  // coordination kernels keep two ints per head in shared memory
+  cudaError_t e = cudaFuncSetAttribute(k_prompt_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_free_request, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+}
+
+cudaError_t launch_decode_alloc(Pool& P, int layer, const SlotArgs& sa, cudaStream_t st) {
+  k_decode_alloc<<<1, kCoordThreads, 0, st>>>(P.pv, layer, P.sc, sa);
   return cudaGetLastError();
 }
 
 cudaError_t launch_free(Pool& P, int slot, cudaStream_t st) {
-  k_free_request<<<1, kCoordThreads, 0, st>>>(P.pv, slot);
+  const int smem = 2 * P.pv.n_layers * P.pv.hkv * (int)sizeof(int);
+  k_free_request<<<1, kCoordThreads, smem, st>>>(P.pv, slot);
   return cudaGetLastError();
 }
 

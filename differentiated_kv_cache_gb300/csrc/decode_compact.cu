@@ -49,13 +49,14 @@ __device__ __forceinline__ float key_importance(unsigned long long key) {
   return __uint_as_float(b);
 }
 
-__global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int layer, DecodePlan* plans) {
-  if (pv.ctl->fail) return;
+__global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int layer, DecodePlan* plans,
+                                                               SlotArgs sa) {
+  if (pv.noop()) return;
   __shared__ ArgMin s_tmp[kPlanThreads / 32];
   __shared__ int s_xc;
   __shared__ float s_ic;
   const int kvh = blockIdx.x, i = blockIdx.y;
-  const int slot = pv.call->slots[i];
+  const int slot = sa.slots[i];
   const int unit = i * pv.hkv + kvh;
   const int* rq = pv.rq(layer, slot);
   const int n0 = rq[1], n = rq[2] + 1, upd = rq[3];
@@ -67,22 +68,32 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
   if (threadIdx.x == 0) { s_xc = -1; s_ic = 0.0f; }
   __syncthreads();
   ArgMin bh{~0ull, -1}, bl{~0ull, -1};
-  for (int s = threadIdx.x; s < nh; s += blockDim.x) {
-    const uint8_t* pg = pv.page(row[s / pv.hi.t]);
-    const int ip = s % pv.hi.t;
-    const float sc = *reinterpret_cast<const float*>(pg + pv.hi.off[4] + 4 * ip);
-    const int pos = *reinterpret_cast<const int*>(pg + pv.hi.off[5] + 4 * ip);
-    const float imp = __fdiv_rn(sc, (float)score_count(pos, n0, upd));
-    if (pos == pc) { s_xc = s; s_ic = imp; }
-    if (pos < wlim) bh = amin(bh, ArgMin{((unsigned long long)order_key(imp) << 32) | (uint32_t)pos, s});
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  // one warp per page: the page's score and position segments are contiguous
+  const int nhp = (nh + pv.hi.t - 1) / pv.hi.t;
+  for (int p = warp; p < nhp; p += nw) {
+    const uint8_t* pg = pv.page(row[p]);
+    for (int ip = lane; ip < pv.hi.t; ip += 32) {
+      const int s = p * pv.hi.t + ip;
+      if (s >= nh) break;
+      const float sc = *reinterpret_cast<const float*>(pg + pv.hi.off[4] + 4 * ip);
+      const int pos = *reinterpret_cast<const int*>(pg + pv.hi.off[5] + 4 * ip);
+      const float imp = __fdiv_rn(sc, (float)score_count(pos, n0, upd));
+      if (pos == pc) { s_xc = s; s_ic = imp; }
+      if (pos < wlim) bh = amin(bh, ArgMin{((unsigned long long)order_key(imp) << 32) | (uint32_t)pos, s});
+    }
   }
-  for (int s = threadIdx.x; s < nl; s += blockDim.x) {
-    const uint8_t* pg = pv.page(row[pv.L - 1 - s / pv.lo.t]);
-    const int ip = s % pv.lo.t;
-    const float sc = *reinterpret_cast<const float*>(pg + pv.lo.off[4] + 4 * ip);
-    const int pos = *reinterpret_cast<const int*>(pg + pv.lo.off[5] + 4 * ip);
-    const float imp = __fdiv_rn(sc, (float)score_count(pos, n0, upd));
-    bl = amin(bl, ArgMin{((unsigned long long)order_key(imp) << 32) | (uint32_t)pos, s});
+  const int nlp = (nl + pv.lo.t - 1) / pv.lo.t;
+  for (int p = warp; p < nlp; p += nw) {
+    const uint8_t* pg = pv.page(row[pv.L - 1 - p]);
+    for (int ip = lane; ip < pv.lo.t; ip += 32) {
+      const int s = p * pv.lo.t + ip;
+      if (s >= nl) break;
+      const float sc = *reinterpret_cast<const float*>(pg + pv.lo.off[4] + 4 * ip);
+      const int pos = *reinterpret_cast<const int*>(pg + pv.lo.off[5] + 4 * ip);
+      const float imp = __fdiv_rn(sc, (float)score_count(pos, n0, upd));
+      bl = amin(bl, ArgMin{((unsigned long long)order_key(imp) << 32) | (uint32_t)pos, s});
+    }
   }
   bh = block_amin(bh, s_tmp);
   bl = block_amin(bl, s_tmp);
@@ -180,11 +191,11 @@ __device__ __forceinline__ void warp_quantize(const float* x, int bits, uint8_t*
 
 __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, const DecodePlan* __restrict__ plans,
                                                       const __half* __restrict__ knew,
-                                                      const __half* __restrict__ vnew) {
-  if (pv.ctl->fail) return;
+                                                      const __half* __restrict__ vnew, SlotArgs sa) {
+  if (pv.noop()) return;
   __shared__ TokStage st[2];
   const int kvh = blockIdx.x, i = blockIdx.y;
-  const int slot = pv.call->slots[i];
+  const int slot = sa.slots[i];
   const int unit = i * pv.hkv + kvh;
   const DecodePlan& p = plans[unit];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -263,15 +274,16 @@ __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, con
   }
 }
 
-cudaError_t launch_decode_alloc(Pool& P, int layer, cudaStream_t st);
+cudaError_t launch_decode_alloc(Pool& P, int layer, const SlotArgs& sa, cudaStream_t st);
 
-cudaError_t launch_decode(Pool& P, int layer, int n_req, const __half* k, const __half* v, cudaStream_t st) {
-  const dim3 grid(P.pv.hkv, n_req);
-  k_decode_plan<<<grid, kPlanThreads, 0, st>>>(P.pv, layer, P.sc.dplan);
+cudaError_t launch_decode(Pool& P, int layer, const SlotArgs& sa, const __half* k, const __half* v,
+                          cudaStream_t st) {
+  const dim3 grid(P.pv.hkv, sa.n);
+  k_decode_plan<<<grid, kPlanThreads, 0, st>>>(P.pv, layer, P.sc.dplan, sa);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if ((e = launch_decode_alloc(P, layer, st)) != cudaSuccess) return e;
-  k_decode_apply<<<grid, 64, 0, st>>>(P.pv, layer, P.sc.dplan, k, v);
+  if ((e = launch_decode_alloc(P, layer, sa, st)) != cudaSuccess) return e;
+  k_decode_apply<<<grid, 64, 0, st>>>(P.pv, layer, P.sc.dplan, k, v, sa);
   return cudaGetLastError();
 }
 

@@ -25,16 +25,25 @@ struct TierGeom {
   int t;          // tokens per page
   int kbytes;     // key row bytes (128 for 8-bit, 64 for 4-bit)
   int off[6];     // K codes, V codes, K meta, V meta, score, position
+  uint32_t magic; // floor(2^32 / t) + 1: s / t == umulhi(s, magic) for s < 2^20
+
+  __device__ __forceinline__ int div(int s) const { return (int)__umulhi((uint32_t)s, magic); }
 };
 
 // Device control block: free-list counters, sticky status, per-call flag.
 struct Ctl {
   unsigned long long start;   // allocation counter
   unsigned long long end;     // reclaim counter
-  int error;                  // sticky data-dependent error (0 = none)
+  int error;                  // sticky data-dependent error (0 = none); while set,
+                              // every kernel of every call returns at once
   int error_info;
-  int fail;                   // the current call is a no-op
-  int pad;
+  int pad[2];
+};
+
+// Request slots of a call, passed by value to the per-step kernels.
+struct SlotArgs {
+  int n;
+  int slots[kMaxCallReq];
 };
 
 // Per-call copy of the caller's host arrays (written by the set-up kernel).
@@ -72,6 +81,7 @@ struct PoolView {
   __device__ __forceinline__ uint8_t* page(int id) const {
     return pages + (size_t)id * page_bytes;
   }
+  __device__ __forceinline__ bool noop() const { return *(volatile int*)&ctl->error != 0; }
 };
 
 // ---------------------------------------------------------------------------
@@ -208,6 +218,50 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+
+// mbarrier + bulk asynchronous copy (global -> shared, completion counted in bytes)
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// try_wait that may suspend the thread for up to `ns` nanoseconds before
+// reporting an incomplete phase (no busy spinning while copies are in flight)
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// Wait for a phase with a time bound (about one second); false on expiry.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_hint(bar, parity, 200000u)) {
+    if (clock64() - t0 > 2000000000LL) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

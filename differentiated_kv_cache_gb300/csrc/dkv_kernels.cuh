@@ -44,6 +44,7 @@ struct Scratch {
   float* apart;         // [units][max_splits][G*(128+2)]
   float* alogit;        // [units][max_chunks][16][8]
   float* alse;          // [units][G]
+  int* adone;           // [units] split counters of the attention merge
   int nkb_cap, grant_cap, max_splits, max_chunks;
 };
 
@@ -51,6 +52,7 @@ struct Scratch {
 struct Pool {
   dkv_config cfg;
   int device;
+  int sm_count;
   PoolView pv;           // device pointers + geometry
   Scratch sc;
   std::vector<void*> allocations;
@@ -62,9 +64,10 @@ struct Pool {
 cudaError_t launch_setup(const Pool& P, const CallArgs& args, cudaStream_t st);
 cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, const __half* k, const __half* v,
                           const __half* q_obs, const float* scores_in, float* scores_out, cudaStream_t st);
-cudaError_t launch_decode(Pool& P, int layer, int n_req, const __half* k, const __half* v, cudaStream_t st);
-cudaError_t launch_attention(Pool& P, int layer, int n_req, int max_tokens, const __half* q, float* out,
-                             int update_scores, cudaStream_t st);
+cudaError_t launch_decode(Pool& P, int layer, const SlotArgs& sa, const __half* k, const __half* v,
+                          cudaStream_t st);
+cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tokens, const __half* q,
+                             float* out, int update_scores, cudaStream_t st);
 cudaError_t launch_free(Pool& P, int slot, cudaStream_t st);
 cudaError_t configure_kernels();
 

@@ -45,6 +45,7 @@ int layout_tier(int t, int kbits, int vbits, TierGeom* tg) {
   }
   tg->t = t;
   tg->kbytes = kD * kbits / 8;
+  tg->magic = (uint32_t)((1ull << 32) / (unsigned)t + 1);
   return tg->off[5] + sizes[5];
 }
 
@@ -98,6 +99,10 @@ int validate(const dkv_config* c) {
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA; }
 
+// Device buffers are read and written with 16-byte vector accesses.
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
 }  // namespace
 
 extern "C" {
@@ -133,6 +138,10 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   Pool& P = pool->P;
   P.cfg = *cfg;
   P.device = cuda_device;
+  if (cudaDeviceGetAttribute(&P.sm_count, cudaDevAttrMultiProcessorCount, cuda_device) != cudaSuccess) {
+    delete pool;
+    return DKV_ERR_CUDA;
+  }
   PoolView& v = P.pv;
   v.n_pages = cfg->n_pages;
   v.page_bytes = cfg->page_bytes;
@@ -158,7 +167,7 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   s.nkb_cap = (cfg->max_seq_len + kKeyBlock - 1) / kKeyBlock;
   s.grant_cap = (cfg->max_seq_len + hi.t - 1) / hi.t + cfg->prompt_grant_slack;
   s.max_chunks = (cfg->max_seq_len + kChunk - 1) / kChunk + 1;
-  s.max_splits = s.max_chunks / 8 + 1;
+  s.max_splits = s.max_chunks / 8 + 2;   // attention partials per head (>= 8 chunks per warp)
   cudaError_t e = cudaSuccess;
   auto A = [&](auto** ptr, size_t n) {
     if (e == cudaSuccess) e = dev_alloc(P, ptr, n);
@@ -180,9 +189,11 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&s.unit_info, units);
   A(&s.grant_ids, units * s.grant_cap);
   A(&s.dplan, units);
-  A(&s.apart, units * s.max_splits * G * (kD + 2));
+  A(&s.apart, units * s.max_splits * (G * kD + 2 * kMaxG));
   A(&s.alogit, units * s.max_chunks * kChunk * 8);
   A(&s.alse, units * G);
+  A(&s.adone, units);
+  if (e == cudaSuccess) e = cudaMemset(s.adone, 0, units * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v.pages, 0, (size_t)cfg->n_pages * cfg->page_bytes);
   if (e == cudaSuccess) e = cudaMemset(v.table, 0xff, heads * v.L * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v.counts, 0, heads * 4 * sizeof(int));
@@ -241,6 +252,8 @@ int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req,
                      const int32_t* seq_lens, const void* k, const void* v, const void* q_obs,
                      const float* scores_in, float* scores_out, void* stream) {
   if (!pool || !req_slots || !k || !v) return DKV_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q_obs) || !aligned4(scores_in) || !aligned4(scores_out))
+    return DKV_ERR_ARG;
   Pool& P = pool->P;
   const dkv_config& c = P.cfg;
   if (layer < 0 || layer >= c.n_layers || n_req < 1 || n_req > c.max_requests || n_req > kMaxCallReq)
@@ -270,34 +283,33 @@ int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req,
   } else {
     if (seq_lens || q_obs || scores_in || scores_out) return DKV_ERR_ARG;
     if (c.recent_window < 1) return DKV_ERR_ARG;
+    SlotArgs sa;
+    sa.n = n_req;
     for (int i = 0; i < n_req; i++) {
       if (!P.h_active[base + req_slots[i]]) return DKV_ERR_STATE;
       if (P.h_n[base + req_slots[i]] + 1 > c.max_seq_len) return DKV_ERR_ARG;
-      args.slots[i] = req_slots[i];
-      args.lens[i] = 0;
-      args.tok0[i] = i;
+      sa.slots[i] = req_slots[i];
     }
-    args.tok0[n_req] = n_req;
+    DeviceGuard guard(P.device);
+    const cudaError_t e = launch_decode(P, layer, sa, static_cast<const __half*>(k), static_cast<const __half*>(v),
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return DKV_ERR_CUDA;
+    for (int i = 0; i < n_req; i++) P.h_n[base + req_slots[i]] += 1;
+    return DKV_OK;
   }
   DeviceGuard guard(P.device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_setup(P, args, st);
   if (e != cudaSuccess) return DKV_ERR_CUDA;
-  if (mode == DKV_PROMPT) {
-    int max_len = 0;
-    for (int i = 0; i < n_req; i++) max_len = std::max(max_len, seq_lens[i]);
-    e = launch_prompt(P, layer, n_req, max_len, static_cast<const __half*>(k), static_cast<const __half*>(v),
-                      static_cast<const __half*>(q_obs), scores_in, scores_out, st);
-    if (e != cudaSuccess) return DKV_ERR_CUDA;
-    for (int i = 0; i < n_req; i++) {
-      P.h_active[base + req_slots[i]] = 1;
-      P.h_n0[base + req_slots[i]] = seq_lens[i];
-      P.h_n[base + req_slots[i]] = seq_lens[i];
-    }
-  } else {
-    e = launch_decode(P, layer, n_req, static_cast<const __half*>(k), static_cast<const __half*>(v), st);
-    if (e != cudaSuccess) return DKV_ERR_CUDA;
-    for (int i = 0; i < n_req; i++) P.h_n[base + req_slots[i]] += 1;
+  int max_len = 0;
+  for (int i = 0; i < n_req; i++) max_len = std::max(max_len, seq_lens[i]);
+  e = launch_prompt(P, layer, n_req, max_len, static_cast<const __half*>(k), static_cast<const __half*>(v),
+                    static_cast<const __half*>(q_obs), scores_in, scores_out, st);
+  if (e != cudaSuccess) return DKV_ERR_CUDA;
+  for (int i = 0; i < n_req; i++) {
+    P.h_active[base + req_slots[i]] = 1;
+    P.h_n0[base + req_slots[i]] = seq_lens[i];
+    P.h_n[base + req_slots[i]] = seq_lens[i];
   }
   return DKV_OK;
 }
@@ -305,31 +317,26 @@ int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req,
 int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req, const int32_t* req_slots, const void* q,
                          float* out, int32_t update_scores, void* stream) {
   if (!pool || !req_slots || !q || !out) return DKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out)) return DKV_ERR_ARG;
   Pool& P = pool->P;
   const dkv_config& c = P.cfg;
   if (layer < 0 || layer >= c.n_layers || n_req < 1 || n_req > c.max_requests || n_req > kMaxCallReq)
     return DKV_ERR_ARG;
   const size_t base = (size_t)layer * c.max_requests;
-  CallArgs args;
-  args.n_req = n_req;
-  args.pad = 0;
+  SlotArgs sa;
+  sa.n = n_req;
   int max_tokens = 1;
   for (int i = 0; i < n_req; i++) {
     if (req_slots[i] < 0 || req_slots[i] >= c.max_requests) return DKV_ERR_ARG;
     for (int j = 0; j < i; j++)
       if (req_slots[j] == req_slots[i]) return DKV_ERR_ARG;
     if (!P.h_active[base + req_slots[i]]) return DKV_ERR_STATE;
-    args.slots[i] = req_slots[i];
-    args.lens[i] = P.h_n[base + req_slots[i]];
-    args.tok0[i] = i;
+    sa.slots[i] = req_slots[i];
     max_tokens = std::max(max_tokens, P.h_n[base + req_slots[i]]);
   }
-  args.tok0[n_req] = n_req;
   DeviceGuard guard(P.device);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_setup(P, args, st);
-  if (e == cudaSuccess)
-    e = launch_attention(P, layer, n_req, max_tokens, static_cast<const __half*>(q), out, update_scores ? 1 : 0, st);
+  const cudaError_t e = launch_attention(P, layer, sa, max_tokens, static_cast<const __half*>(q), out,
+                                         update_scores ? 1 : 0, reinterpret_cast<cudaStream_t>(stream));
   return cuda_err(e);
 }
 
@@ -388,8 +395,10 @@ int dkv_pool_clear_error(dkv_pool* pool) {
   if (cudaMemcpy(&c, P.pv.ctl, sizeof(Ctl), cudaMemcpyDeviceToHost) != cudaSuccess) return DKV_ERR_CUDA;
   c.error = 0;
   c.error_info = -1;
-  c.fail = 0;
   if (cudaMemcpy(P.pv.ctl, &c, sizeof(Ctl), cudaMemcpyHostToDevice) != cudaSuccess) return DKV_ERR_CUDA;
+  // a call cut short by an error can leave attention merge counters behind
+  if (cudaMemset(P.sc.adone, 0, (size_t)P.cfg.max_requests * P.cfg.n_kv_heads * sizeof(int)) != cudaSuccess)
+    return DKV_ERR_CUDA;
   std::vector<int> rq((size_t)P.cfg.n_layers * P.cfg.max_requests * 4);
   if (cudaMemcpy(rq.data(), P.pv.req, rq.size() * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return DKV_ERR_CUDA;

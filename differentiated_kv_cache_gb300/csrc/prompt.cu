@@ -29,7 +29,7 @@ template <int G>
 __global__ void __launch_bounds__(32 * G) k_prompt_lse(PoolView pv, const __half* __restrict__ k,
                                                         const __half* __restrict__ q_obs, float2* partial,
                                                         int nkb_cap) {
-  if (pv.ctl->fail) return;
+  if (pv.noop()) return;
   const int kb = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
   const CallArgs* ca = pv.call;
   const int n0 = ca->lens[i];
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(32 * G) k_prompt_lse(PoolView pv, const __half
 // lse2[unit][h*32 + o] = m + log2(l) over the key blocks (log2 domain);
 // -inf for observation rows with a negative position.
 __global__ void k_prompt_lse_merge(PoolView pv, const float2* __restrict__ partial, float* lse2, int nkb_cap) {
-  if (pv.ctl->fail) return;
+  if (pv.noop()) return;
   const int unit = blockIdx.x, i = unit / pv.hkv;
   const int rows = kObs * pv.G;
   const int n0 = pv.call->lens[i];
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(128) k_prompt_score(PoolView pv, const __half*
                                                        const __half* __restrict__ q_obs,
                                                        const float* __restrict__ lse2, float* score_out,
                                                        uint16_t* tokinfo, int2* bcnt, int nkb_cap) {
-  if (pv.ctl->fail) return;
+  if (pv.noop()) return;
   const int kb = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
   const CallArgs* ca = pv.call;
   const int n0 = ca->lens[i];
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(128) k_prompt_score(PoolView pv, const __half*
 __global__ void __launch_bounds__(128) k_prompt_given(PoolView pv, const float* __restrict__ score_in,
                                                        float* score_out, uint16_t* tokinfo, int2* bcnt,
                                                        int nkb_cap) {
-  if (pv.ctl->fail) return;
+  if (pv.noop()) return;
   __shared__ int s_cnt[8];
   const int kb = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
   const CallArgs* ca = pv.call;
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(128) k_prompt_given(PoolView pv, const float* 
 __global__ void __launch_bounds__(128) k_prompt_scatter(PoolView pv, const uint16_t* __restrict__ tokinfo,
                                                          const int2* __restrict__ bbase, int* rank2pos,
                                                          int nkb_cap) {
-  if (pv.ctl->fail) return;
+  if (pv.noop()) return;
   const int kb = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
   const CallArgs* ca = pv.call;
   const int n0 = ca->lens[i];
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
                                                       const int* __restrict__ rank2pos,
                                                       const int4* __restrict__ unit_info,
                                                       const int* __restrict__ grant_ids, int grant_cap) {
-  if (pv.ctl->fail) return;
+  if (pv.noop()) return;
   __shared__ uint8_t s_vc[8][4][kD];      // [warp][token][feature] value codes
   const int unit = blockIdx.y, tier = blockIdx.z ? kTierHi : kTierLo;
   const int i = unit / pv.hkv, kvh = unit % pv.hkv;
@@ -479,8 +479,9 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
 }
 
 // ---------------------------------------------------------------------------
-cudaError_t launch_prompt_plan(Pool& P, int layer, cudaStream_t st);
+cudaError_t launch_prompt_plan(Pool& P, int layer, int n_req, cudaStream_t st);
 cudaError_t configure_attention();
+cudaError_t configure_alloc();
 
 template <int G>
 static int lse_smem() { return 32 * G * 256 + kKeyBlock * 256; }
@@ -519,6 +520,7 @@ cudaError_t configure_kernels() {
   if ((e = configure_g<6>()) != cudaSuccess) return e;
   if ((e = configure_g<7>()) != cudaSuccess) return e;
   if ((e = configure_g<8>()) != cudaSuccess) return e;
+  if ((e = configure_alloc()) != cudaSuccess) return e;
   return configure_attention();
 }
 
@@ -548,7 +550,7 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, const __ha
     score_src = so;
   }
   if (e != cudaSuccess) return e;
-  if ((e = launch_prompt_plan(P, layer, st)) != cudaSuccess) return e;
+  if ((e = launch_prompt_plan(P, layer, n_req, st)) != cudaSuccess) return e;
   k_prompt_scatter<<<grid, 128, 0, st>>>(P.pv, s.tokinfo, s.bbase, s.rank2pos, s.nkb_cap);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const dim3 gpack((max_len + 31) / 32, n_req * P.pv.hkv, 2);

@@ -31,7 +31,10 @@
  *  - "host" pointers are read before the call returns and may be reused at
  *    once. "device" pointers must stay valid until the work queued on
  *    `stream` (a cudaStream_t passed as void*, NULL = legacy default stream)
- *    completes. The caller owns every input and output buffer.
+ *    completes. The caller owns every input and output buffer. Device
+ *    buffers of fp16/fp32 vectors (k, v, q_obs, q, out) must start on a
+ *    16-byte boundary, score arrays on a 4-byte boundary (DKV_ERR_ARG
+ *    otherwise).
  *  - All calls on one pool must be ordered on one stream (or synchronised by
  *    the caller). compact_step, decode_attention and free_request never
  *    synchronise the host; argument and request-state errors are detected on

@@ -84,10 +84,11 @@ def test_figure6_on_gpu():
 
 
 # ---------------------------------------------------- prompt, given scores
+@pytest.mark.parametrize("pb", [4096, 3584])
 @pytest.mark.parametrize("G,H,lens", [(4, 2, [512, 700]), (1, 3, [1, 31, 129, 300]), (5, 2, [1029, 64, 65]),
                                       (7, 1, [777]), (8, 2, [256, 257])])
-def test_prompt_given_scores_bit_exact(G, H, lens):
-    cfg = cfg_of(group_size=G, n_kv_heads=H, n_pages=2048, max_requests=len(lens) + 1)
+def test_prompt_given_scores_bit_exact(G, H, lens, pb):
+    cfg = cfg_of(group_size=G, n_kv_heads=H, n_pages=2048, max_requests=len(lens) + 1, page_bytes=pb)
     n = sum(lens)
     k = workloads.random_fp16((n, H, 128), 10 + G, scale=2.0)
     v = workloads.random_fp16((n, H, 128), 20 + G)
@@ -208,7 +209,8 @@ def test_prompt_computed_scores(name, G, reqs):
 # --------------------------------------------------------------- decode
 @pytest.mark.parametrize("over", [dict(), dict(alpha_h=1.0, alpha_l=0.6), dict(lo_enabled=0, alpha_l=0.5),
                                   dict(tokens_per_hi_page=2, tokens_per_lo_page=4, recent_window=3),
-                                  dict(reclaim_in_decode=0, alpha_h=4.0, alpha_l=1.0, recent_window=8)])
+                                  dict(reclaim_in_decode=0, alpha_h=4.0, alpha_l=1.0, recent_window=8),
+                                  dict(page_bytes=3584), dict(page_bytes=3584, alpha_h=1.0, alpha_l=0.6)])
 def test_decode_steps_bit_exact(over):
     cfg = cfg_of(max_seq_len=1000, n_pages=4096, **over)
     lens = [200, 333, 70]
@@ -238,10 +240,11 @@ def test_decode_steps_bit_exact(over):
 
 
 # ------------------------------------------------------------ attention
+@pytest.mark.parametrize("pb", [4096, 3584])
 @pytest.mark.parametrize("G,H,lens,steps", [(4, 2, [512, 700], 5), (1, 2, [40, 1], 3), (5, 3, [1030, 17], 2),
                                             (7, 1, [2000], 1), (8, 2, [300, 301], 4)])
-def test_decode_attention_parity(G, H, lens, steps):
-    cfg = cfg_of(group_size=G, n_kv_heads=H, n_pages=4096, max_seq_len=2100, max_requests=len(lens))
+def test_decode_attention_parity(G, H, lens, steps, pb):
+    cfg = cfg_of(group_size=G, n_kv_heads=H, n_pages=4096, max_seq_len=2100, max_requests=len(lens), page_bytes=pb)
     n = sum(lens)
     k = workloads.random_fp16((n, H, 128), 30, scale=1.5)
     v = workloads.random_fp16((n, H, 128), 31)
@@ -266,8 +269,9 @@ def test_decode_attention_parity(G, H, lens, steps):
         assert_same(gp, op)
 
 
-def test_attention_score_update():
-    cfg = cfg_of(group_size=4, n_kv_heads=2, n_pages=2048, max_requests=2)
+@pytest.mark.parametrize("pb", [4096, 3584])
+def test_attention_score_update(pb):
+    cfg = cfg_of(group_size=4, n_kv_heads=2, n_pages=2048, max_requests=2, page_bytes=pb)
     lens = [600, 257]
     n = sum(lens)
     k = workloads.random_fp16((n, 2, 128), 40, scale=1.5)
