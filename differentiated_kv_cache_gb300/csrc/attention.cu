@@ -30,7 +30,7 @@ namespace dkv {
 constexpr int kStages = 3;                 // ring depth per warp (chunked path)
 constexpr int kPageStages = 4;             // ring depth per warp (paged path)
 constexpr int kMinChunks = 8;              // ring work items per warp at least
-constexpr int kCtasPerSm = 4;
+constexpr int kCtasPerSm = 3;
 constexpr int kOffV = 2048;                // chunked stage image: V rows
 constexpr int kOffMeta = 3072;             // chunked stage image: page meta segments
 
@@ -301,8 +301,8 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
 
 // Publish the warp's partial of head u (items [begin, end), warp ranges of C
 // items); the last warp of the head merges every partial into out and lse2.
-__device__ void publish(const PoolView& pv, const AttnArgs& a, const SlotArgs& sa, AttnState& S, int u, int begin,
-                        int end, int C, int gw, int lane) {
+__device__ void publish(const PoolView& pv, const AttnArgs& a, const SlotArgs& sa, AttnState& S, int u, int first,
+                        int last, int gw, int lane) {
   const int G = pv.G, g = lane >> 2, t = lane & 3;
   float l0 = S.l[0], l1 = S.l[1], z0 = S.z[0], z1 = S.z[1];
 #pragma unroll
@@ -313,7 +313,6 @@ __device__ void publish(const PoolView& pv, const AttnArgs& a, const SlotArgs& s
     z1 += __shfl_xor_sync(0xffffffffu, z1, s);
   }
   const int stride = part_stride(G);
-  const int first = begin / C, last = (end - 1) / C;
   float* dst = a.part + ((size_t)u * a.max_parts + (gw - first)) * stride;
 #pragma unroll
   for (int mt = 0; mt < 8; mt++) {
@@ -371,7 +370,9 @@ __device__ int item_prefix(const PoolView& pv, const SlotArgs& sa, int layer, bo
   int sum = 0;
   for (int u = u0; u < u1; u++) {
     const int* cn = pv.cnt(layer, sa.slots[u / pv.hkv], u % pv.hkv);
-    const int items = paged ? (cn[0] + pv.hi.t - 1) / pv.hi.t + (cn[1] + pv.lo.t - 1) / pv.lo.t
+    // paged: pages weighted by their chunks (T / 16); chunked: chunks
+    const int items = paged ? (cn[0] + pv.hi.t - 1) / pv.hi.t * (pv.hi.t / kChunk) +
+                                  (cn[1] + pv.lo.t - 1) / pv.lo.t * (pv.lo.t / kChunk)
                             : (cn[0] + kChunk - 1) / kChunk + (cn[1] + kChunk - 1) / kChunk;
     s_pref[u] = items;
     sum += items;
@@ -420,10 +421,70 @@ __device__ __forceinline__ int find_unit(const int* s_pref, int n_units, int g0)
 }
 
 // ---------------------------------------------------------------------------
-// Paged path: pages of T = 16k tokens (k = 1, 2), work item = one page. One
-// bulk copy per page of its first four segments (K rows, V rows, K meta, V
-// meta are contiguous at the page start).
+// Paged path: pages of T = 16k tokens (k = 1, 2), one bulk copy per page of
+// its first four segments (K rows, V rows, K meta, V meta are contiguous at
+// the page start). The work sequence is measured in chunks (a page weighs
+// T/16); a warp takes the pages that start inside its range of chunks.
 // ---------------------------------------------------------------------------
+struct PageCursor {
+  int u, begin, end;   // head and its chunk range
+  int hp, np;          // hi pages, all pages
+  int nh, nl;
+  const int* row;
+  int p, off;          // current page and its chunk offset
+};
+
+struct PagedCtx {
+  const PoolView& pv;
+  const SlotArgs& sa;
+  const int* s_pref;
+  int layer, n_units, wh, wl;
+
+  __device__ __forceinline__ void at_unit(PageCursor& c, int u) const {
+    c.u = u;
+    c.begin = s_pref[u];
+    c.end = s_pref[u + 1];
+    const int* cn = pv.cnt(layer, sa.slots[u / pv.hkv], u % pv.hkv);
+    c.nh = cn[0];
+    c.nl = cn[1];
+    c.hp = (c.nh + pv.hi.t - 1) / pv.hi.t;
+    c.np = c.hp + (c.nl + pv.lo.t - 1) / pv.lo.t;
+    c.row = pv.row(layer, sa.slots[u / pv.hkv], u % pv.hkv);
+    c.p = 0;
+    c.off = c.begin;
+  }
+  // move past pages of finished heads (and empty heads) while another head follows
+  __device__ __forceinline__ void settle(PageCursor& c) const {
+    while (c.p >= c.np && c.u + 1 < n_units) at_unit(c, c.u + 1);
+  }
+  __device__ __forceinline__ void next(PageCursor& c) const {
+    c.off += c.p < c.hp ? wh : wl;
+    c.p++;
+    settle(c);
+  }
+  // first page starting at chunk offset >= x
+  __device__ __forceinline__ void seek(PageCursor& c, int x) const {
+    at_unit(c, find_unit(s_pref, n_units, x));
+    const int o = x - c.begin;
+    if (o > 0) {
+      if (o <= c.hp * wh) {
+        c.p = (o + wh - 1) / wh;
+        c.off = c.begin + c.p * wh;
+      } else {
+        c.p = c.hp + (o - c.hp * wh + wl - 1) / wl;
+        c.off = c.begin + c.hp * wh + (c.p - c.hp) * wl;
+      }
+    }
+    settle(c);
+  }
+  __device__ __forceinline__ bool valid(const PageCursor& c, int g1) const { return c.p < c.np && c.off < g1; }
+  // warps that own pages of head c.u (range width C)
+  __device__ __forceinline__ void owners(const PageCursor& c, int C, int& first, int& last) const {
+    first = c.begin / C;
+    last = (c.end - (c.np > c.hp ? wl : wh)) / C;
+  }
+};
+
 __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
   if (pv.noop()) return;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -441,9 +502,10 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
   const int gw = blockIdx.x * kAttnWarps + warp;
   const int g0 = gw * C, g1 = min(total, g0 + C);
   if (g0 >= g1) return;           // no block-wide barrier follows
-  Cursor ci, cc;
-  cursor_at(ci, find_unit(s_pref, n_units, g0), s_pref, pv, sa, a.layer, true);
-  cursor_seek(ci, g0, s_pref, pv, sa, a.layer, true);
+  const PagedCtx ctx{pv, sa, s_pref, a.layer, n_units, pv.hi.t / kChunk, pv.lo.t / kChunk};
+  PageCursor ci, cc;
+  ctx.seek(ci, g0);
+  if (!ctx.valid(ci, g1)) return;  // no page starts inside this range
   cc = ci;
   uint32_t bq_hi[8][2], bq_lo[8][2];
   float sq0, sq1;
@@ -456,48 +518,50 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
     fence_proxy_async();
   }
   __syncwarp();
-  // one lane copies the page's K | V | K meta | V meta prefix
-  auto issue = [&](int x) {
-    cursor_seek(ci, x, s_pref, pv, sa, a.layer, true);
+  int issued = 0;
+  // one lane copies the next page's K | V | K meta | V meta prefix
+  auto try_issue = [&]() {
+    if (!ctx.valid(ci, g1)) return;
     if (lane == 0) {
-      const int st = (x - g0) % kPageStages;
-      const int p = x - ci.begin;
-      const bool hi = p < ci.hi_items;
+      const int st = issued % kPageStages;
+      const bool hi = ci.p < ci.hp;
       const TierGeom& tg = hi ? pv.hi : pv.lo;
-      const int e = hi ? p : pv.L - 1 - (p - ci.hi_items);
+      const int e = hi ? ci.p : pv.L - 1 - (ci.p - ci.hp);
       const uint32_t bar = bar0 + 8 * st;
       const uint32_t bytes = tg.off[4];
       mbar_expect_tx(bar, bytes);
       bulk_g2s(smem_u32(wst + st * a.stage_bytes), pv.page(__ldg(ci.row + e)), bytes, bar);
     }
+    issued++;
+    ctx.next(ci);
   };
   AttnState S;
   S.reset();
-  const int n = g1 - g0;
-  for (int x = 0; x < kPageStages - 1 && x < n; x++) issue(g0 + x);
-  for (int x = 0; x < n; x++) {
-    if (x + kPageStages - 1 < n) {
-      __syncwarp();               // every lane is done with the stage being refilled
-      fence_proxy_async();
-      issue(g0 + x + kPageStages - 1);
-    }
+  for (int x = 0; x < kPageStages - 1; x++) try_issue();
+  int cur_u = cc.u;
+  for (int x = 0; x < issued; x++) {
+    __syncwarp();                 // every lane is done with the stage being refilled
+    fence_proxy_async();
+    try_issue();
     if (!mbar_wait_bounded(bar0 + 8 * (x % kPageStages), (x / kPageStages) & 1)) {
       if (lane == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = cc.u;
-      for (int y = x + 1; y < min(n, x + kPageStages); y++)
+      for (int y = x + 1; y < min(issued, x + kPageStages); y++)
         mbar_wait_bounded(bar0 + 8 * (y % kPageStages), (y / kPageStages) & 1);
       return;
     }
-    const int gx = g0 + x;
-    if (gx >= cc.end) {           // the range crosses into the next head
-      publish(pv, a, sa, S, cc.u, cc.begin, cc.end, C, gw, lane);
-      cursor_seek(cc, gx, s_pref, pv, sa, a.layer, true);
+    if (cc.u != cur_u) {          // the range crosses into the next head
+      PageCursor prev = cc;
+      ctx.at_unit(prev, cur_u);
+      int first, last;
+      ctx.owners(prev, C, first, last);
+      publish(pv, a, sa, S, cur_u, first, last, gw, lane);
+      cur_u = cc.u;
       load_q(pv, a, cc.u / pv.hkv, cc.u % pv.hkv, g, t, bq_hi, bq_lo, sq0, sq1);
       S.reset();
     }
-    const int p = gx - cc.begin;
-    const bool hi = p < cc.hi_items;
+    const bool hi = cc.p < cc.hp;
     const TierGeom& tg = hi ? pv.hi : pv.lo;
-    const int pt = hi ? p : p - cc.hi_items;             // page index within the tier
+    const int pt = hi ? cc.p : cc.p - cc.hp;             // page index within the tier
     const int count = (hi ? cc.nh : cc.nl) - pt * tg.t;  // valid slots from this page's start
     const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
     const int jA = chunk_slot(g), jB = chunk_slot(g + 8);
@@ -517,8 +581,15 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
       attend_chunk(S, hi, kA, kB, v0, v1, kmA, kmB, vmA, vmB, sA < count, sB < count, bq_hi, bq_lo, sq0, sq1, lg,
                    G, g, t);
     }
+    ctx.next(cc);
   }
-  publish(pv, a, sa, S, cc.u, cc.begin, cc.end, C, gw, lane);
+  {
+    PageCursor prev = cc;
+    ctx.at_unit(prev, cur_u);
+    int first, last;
+    ctx.owners(prev, C, first, last);
+    publish(pv, a, sa, S, cur_u, first, last, gw, lane);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -623,7 +694,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
     }
     const int gx = g0 + x;
     if (gx >= cc.end) {           // the range crosses into the next head
-      publish(pv, a, sa, S, cc.u, cc.begin, cc.end, C, gw, lane);
+      publish(pv, a, sa, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
       cursor_seek(cc, gx, s_pref, pv, sa, a.layer, false);
       load_q(pv, a, cc.u / pv.hkv, cc.u % pv.hkv, g, t, bq_hi, bq_lo, sq0, sq1);
       S.reset();
@@ -652,7 +723,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
     attend_chunk(S, hi, kA, kB, v0, v1, kmA, kmB, vmA, vmB, base + jA < count, base + jB < count, bq_hi, bq_lo,
                  sq0, sq1, lg, G, g, t);
   }
-  publish(pv, a, sa, S, cc.u, cc.begin, cc.end, C, gw, lane);
+  publish(pv, a, sa, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
 }
 
 // Score update: every stored token's score gains max over the group's heads
