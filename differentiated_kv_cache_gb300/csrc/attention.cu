@@ -22,6 +22,7 @@
 //                  its contiguous K | V | K-meta | V-meta prefix;
 //   k_attn_decode  any page geometry: per 16-slot chunk, one copy per page run.
 #include <algorithm>
+#include <mutex>
 
 #include "dkv_kernels.cuh"
 
@@ -805,6 +806,116 @@ cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tok
   if (update_scores) {
     const int max_chunks_call = (max_tokens + kChunk - 1) / kChunk + 1;
     const dim3 g2((max_chunks_call + 15) / 16, (unsigned)n_units);
+    k_attn_scores<<<g2, 256, 0, st>>>(P.pv, a, sa);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant (dkv_decode_attention_static). The same kernels
+// work in one fixed device array instead of the pool's scratch: the merge
+// counters, the per-head lse2, the per-warp partials and, with score updates,
+// the per-chunk logits. The array is part of this library's device image; the
+// CUDA driver reserves it when the module is loaded, so no call here
+// allocates. Every call shares it and it keeps the last call's contents.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_attn_static_scratch[DKV_ATTN_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxStaticDevices = 64;
+static std::mutex g_static_mu;
+static void* g_static_base[kMaxStaticDevices];
+
+namespace {
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Regions of the array for one call, each 256-byte aligned: merge counters
+// at 0, then lse2, partials, logits. Strides are sized for the call's
+// longest request, not the pool's maximum.
+struct StaticLayout {
+  size_t lse2, part, logit, total;
+  int max_parts, max_chunks;
+};
+
+StaticLayout static_layout(int n_units, int G, int max_tokens, int update_scores) {
+  StaticLayout L;
+  L.max_chunks = (max_tokens + kChunk - 1) / kChunk + 1;
+  L.max_parts = L.max_chunks / kMinChunks + 2;   // warps over one head (ranges >= kMinChunks)
+  size_t off = round256((size_t)n_units * sizeof(int));
+  L.lse2 = off;
+  off = round256(off + (size_t)n_units * G * sizeof(float));
+  L.part = off;
+  off = round256(off + (size_t)n_units * L.max_parts * part_stride(G) * sizeof(float));
+  L.logit = off;
+  if (update_scores) off += (size_t)n_units * L.max_chunks * kChunk * 8 * sizeof(float);
+  L.total = off;
+  return L;
+}
+
+// Address of the array on the current device, looked up once per device.
+cudaError_t static_scratch(int device, uint8_t** base) {
+  if (device < 0 || device >= kMaxStaticDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_base[device]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_base[device] = p;
+  }
+  *base = static_cast<uint8_t*>(g_static_base[device]);
+  return cudaSuccess;
+}
+}  // namespace
+
+size_t attention_static_bytes(const Pool& P, int n_units, int max_tokens, int update_scores) {
+  return static_layout(n_units, P.pv.G, max_tokens, update_scores).total;
+}
+
+cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int max_tokens, const __half* q,
+                                    float* out, int update_scores, cudaStream_t st) {
+  const int n_units = sa.n * P.pv.hkv;
+  const StaticLayout L = static_layout(n_units, P.pv.G, max_tokens, update_scores);
+  if (L.total > DKV_ATTN_STATIC_SCRATCH_BYTES) return cudaErrorInvalidValue;
+  uint8_t* base = nullptr;
+  cudaError_t e = static_scratch(P.device, &base);
+  if (e != cudaSuccess) return e;
+  AttnArgs a;
+  a.q = q;
+  a.out = out;
+  a.done = reinterpret_cast<int*>(base);
+  a.lse2 = reinterpret_cast<float*>(base + L.lse2);
+  a.part = reinterpret_cast<float*>(base + L.part);
+  a.logit = reinterpret_cast<float*>(base + L.logit);
+  a.max_parts = L.max_parts;
+  a.max_chunks = L.max_chunks;
+  a.update = update_scores;
+  a.layer = layer;
+  // The merge counters must start at zero. A finished call leaves them zero,
+  // but one cut short (a wait that timed out) leaves some set.
+  e = cudaMemsetAsync(a.done, 0, (size_t)n_units * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  const bool paged = P.pv.hi.t % kChunk == 0 && P.pv.lo.t % kChunk == 0;
+  int smem;
+  if (paged) {
+    a.mseg = 0;
+    a.maxp = 1;
+    a.stage_bytes = std::max(P.pv.hi.off[4], P.pv.lo.off[4]);
+    smem = kAttnWarps * kPageStages * (a.stage_bytes + 8) + 4 * (n_units + 1);
+  } else {
+    a.mseg = (4 * std::max(P.pv.hi.t, P.pv.lo.t) + 15) & ~15;
+    a.maxp = std::max(pages_per_chunk(P.pv.hi.t), pages_per_chunk(P.pv.lo.t));
+    a.stage_bytes = kOffMeta + 2 * a.maxp * a.mseg;
+    smem = kAttnWarps * kStages * (a.stage_bytes + 8) + 4 * (n_units + 1);
+  }
+  if (smem > kMaxAttnSmem) return cudaErrorInvalidConfiguration;
+  if (paged)
+    k_attn_paged<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
+  else
+    k_attn_decode<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (update_scores) {
+    const dim3 g2((L.max_chunks + 15) / 16, (unsigned)n_units);
     k_attn_scores<<<g2, 256, 0, st>>>(P.pv, a, sa);
     e = cudaGetLastError();
   }

@@ -69,6 +69,11 @@ cudaError_t launch_decode(Pool& P, int layer, const SlotArgs& sa, const __half* 
 cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tokens, const __half* q,
                              float* out, int update_scores, cudaStream_t st);
 cudaError_t launch_free(Pool& P, int slot, cudaStream_t st);
+// Allocation-free attention: bytes of the static array one call needs, and
+// the launcher over that array (attention.cu).
+size_t attention_static_bytes(const Pool& P, int n_units, int max_tokens, int update_scores);
+cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int max_tokens, const __half* q,
+                                    float* out, int update_scores, cudaStream_t st);
 cudaError_t configure_kernels();
 
 }  // namespace dkv

@@ -118,6 +118,7 @@ const char* dkv_strerror(int code) {
     case DKV_ERR_TIMEOUT: return "bounded device wait expired";
     case DKV_ERR_CHECK: return "device consistency check failed";
     case DKV_ERR_UNSUPPORTED: return "configuration not supported by the kernels";
+    case DKV_ERR_SCRATCH: return "call needs more than the fixed scratch array holds";
     default: return "unknown error";
   }
 }
@@ -337,6 +338,37 @@ int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req, const int
   DeviceGuard guard(P.device);
   const cudaError_t e = launch_attention(P, layer, sa, max_tokens, static_cast<const __half*>(q), out,
                                          update_scores ? 1 : 0, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_err(e);
+}
+
+// Same checks and kernels as dkv_decode_attention; scratch in the static
+// array of attention.cu (for callers that cannot allocate device memory).
+int dkv_decode_attention_static(dkv_pool* pool, int32_t layer, int32_t n_req, const int32_t* req_slots,
+                                const void* q, float* out, int32_t update_scores, void* stream) {
+  if (!pool || !req_slots || !q || !out) return DKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out)) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  if (layer < 0 || layer >= c.n_layers || n_req < 1 || n_req > c.max_requests || n_req > kMaxCallReq)
+    return DKV_ERR_ARG;
+  const size_t base = (size_t)layer * c.max_requests;
+  SlotArgs sa;
+  sa.n = n_req;
+  int max_tokens = 1;
+  for (int i = 0; i < n_req; i++) {
+    if (req_slots[i] < 0 || req_slots[i] >= c.max_requests) return DKV_ERR_ARG;
+    for (int j = 0; j < i; j++)
+      if (req_slots[j] == req_slots[i]) return DKV_ERR_ARG;
+    if (!P.h_active[base + req_slots[i]]) return DKV_ERR_STATE;
+    sa.slots[i] = req_slots[i];
+    max_tokens = std::max(max_tokens, P.h_n[base + req_slots[i]]);
+  }
+  const int update = update_scores ? 1 : 0;
+  if (attention_static_bytes(P, n_req * c.n_kv_heads, max_tokens, update) > DKV_ATTN_STATIC_SCRATCH_BYTES)
+    return DKV_ERR_SCRATCH;
+  DeviceGuard guard(P.device);
+  const cudaError_t e = launch_attention_static(P, layer, sa, max_tokens, static_cast<const __half*>(q), out,
+                                                update, reinterpret_cast<cudaStream_t>(stream));
   return cuda_err(e);
 }
 

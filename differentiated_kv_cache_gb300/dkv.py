@@ -17,10 +17,12 @@ from . import build as _build
 
 DKV_OK, DKV_ERR_ARG, DKV_ERR_CUDA, DKV_ERR_STATE = 0, -1, -2, -3
 DKV_ERR_NO_PAGES, DKV_ERR_TABLE_FULL, DKV_ERR_TIMEOUT, DKV_ERR_CHECK, DKV_ERR_UNSUPPORTED = -4, -5, -6, -7, -8
+DKV_ERR_SCRATCH = -9
+DKV_ATTN_STATIC_SCRATCH_BYTES = 64 << 20
 DKV_PROMPT, DKV_DECODE = 0, 1
 
 EXPORTED = ("dkv_pool_create", "dkv_pool_destroy", "dkv_pool_geometry", "dkv_compact_step",
-            "dkv_decode_attention", "dkv_free_request", "dkv_pool_status", "dkv_pool_clear_error",
+            "dkv_decode_attention", "dkv_decode_attention_static", "dkv_free_request", "dkv_pool_status", "dkv_pool_clear_error",
             "dkv_pool_export", "dkv_strerror")
 
 
@@ -174,6 +176,19 @@ def dkv_decode_attention(pool, layer: int, req_slots, q, out, update_scores: boo
                                      _dptr(q, torch.float16, "q"), _dptr(out, torch.float32, "out"),
                                      int(bool(update_scores)), _stream(stream))
     return _check(rc, "dkv_decode_attention") if check else rc
+
+
+def dkv_decode_attention_static(pool, layer: int, req_slots, q, out, update_scores: bool = False, stream=None,
+                                check: bool = True) -> int:
+    """dkv_decode_attention working in the library's fixed 64 MiB device
+    array instead of the pool's scratch (for callers that cannot allocate
+    device memory). Calls that overlap on the GPU race on the array."""
+    import torch
+    slots = _i32(req_slots)
+    rc = load().dkv_decode_attention_static(pool, int(layer), int(slots.size), slots.ctypes.data_as(C.c_void_p),
+                                            _dptr(q, torch.float16, "q"), _dptr(out, torch.float32, "out"),
+                                            int(bool(update_scores)), _stream(stream))
+    return _check(rc, "dkv_decode_attention_static") if check else rc
 
 
 def dkv_free_request(pool, req_slot: int, stream=None, check: bool = True) -> int:

@@ -104,6 +104,7 @@ extern "C" {
 #define DKV_ERR_TIMEOUT     -6  /* a bounded device wait gave up */
 #define DKV_ERR_CHECK       -7  /* a device-side consistency check failed */
 #define DKV_ERR_UNSUPPORTED -8  /* configuration outside what the kernels support */
+#define DKV_ERR_SCRATCH     -9  /* call needs more than the fixed scratch array holds */
 
 /* ---- modes ------------------------------------------------------------ */
 #define DKV_PROMPT 0  /* compact a whole prompt            [Pol-P] [Mem-Fig6] */
@@ -234,6 +235,45 @@ int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req,
 int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
                          const int32_t* req_slots, const void* q, float* out,
                          int32_t update_scores, void* stream);
+
+/* Size of the fixed device array that dkv_decode_attention_static works in. */
+#define DKV_ATTN_STATIC_SCRATCH_BYTES (64u << 20)
+
+/* dkv_decode_attention without the pool's scratch, for callers that cannot
+ * allocate device memory. The paper has no counterpart: it is an interface
+ * addition of this library. Arguments, layouts, results and the other
+ * errors are those of dkv_decode_attention, and it runs the same kernels.
+ *
+ * Who needs it: a host runtime whose own allocator already holds the device's
+ * free memory (a serving engine hands nearly all HBM to its KV page pool at
+ * start-up, so a later cudaMalloc fails or fragments that memory), or code
+ * that must not call cudaMalloc/cudaFree at all because those calls
+ * synchronise the device. Neither attention entry point allocates per call;
+ * this one also needs no scratch sized for the pool's maximum batch and
+ * length: it works in one static array of DKV_ATTN_STATIC_SCRATCH_BYTES
+ * (64 MiB) in the library's device image, reserved by the CUDA driver when
+ * the library's module is loaded. No cudaMalloc, cudaFree or other
+ * allocating routine is called.
+ *
+ * Size limit: with U = n_req * n_kv_heads, C = ceil(max_n / 16) + 1 (max_n =
+ * longest stored sequence among the call's requests) and r(x) = x rounded up
+ * to 256, the call needs r(4U) + r(4UG) + r(4U(C/8 + 2)(128G + 16)) bytes,
+ * plus 512UC if update_scores != 0. A larger call returns DKV_ERR_SCRATCH
+ * and queues nothing.
+ *
+ * Set-up: the first call on a device looks up the array's address on that
+ * device (cudaGetSymbolAddress, with the pool's device current); make that
+ * first call before any stream capture. Every call on a device shares the
+ * array and it keeps the last call's contents; the call clears the part that
+ * must start at zero (its merge counters, by cudaMemsetAsync on `stream`).
+ * Calls that overlap on the GPU (on different streams, or from different
+ * pools of one device) race on the array and give wrong results: order them
+ * on one stream or synchronise between them.
+ * Errors: DKV_ERR_ARG, DKV_ERR_STATE, DKV_ERR_SCRATCH (host, nothing queued);
+ * DKV_ERR_CUDA if the set-up lookup or a launch fails. */
+int dkv_decode_attention_static(dkv_pool* pool, int32_t layer, int32_t n_req,
+                                const int32_t* req_slots, const void* q, float* out,
+                                int32_t update_scores, void* stream);
 
 /* Return every page of request `req_slot` in every layer to the list end
  * (one prefix sum over (layer, KV head); within a head hi pages left to
