@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -59,11 +60,10 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"dkv_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -184,7 +184,11 @@ def run_dkv(args, world, rank, local):
     dv = torch.from_numpy(np.stack([d["v"] for d in dec])).to(dev)
     dq = torch.from_numpy(np.stack([d["q"] for d in dec])).to(dev)
     out = torch.zeros((R, Hq, 128), dtype=torch.float32, device=dev)
+    # L2 flush between decode steps: write a buffer larger than L2, then read a
+    # second one so that the write-back of the dirty lines happens here and not
+    # inside the next timed kernel; L2 then holds none of the path's data.
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
     T = args.decode_steps
 
@@ -204,6 +208,7 @@ def run_dkv(args, world, rank, local):
             counts.append(("prompt", st["hi_tokens"], st["lo_tokens"]))
         for t in range(T):
             flush.fill_(t & 0xFF)
+            torch.amax(flush_rd)
             if record is not None:
                 c0, c1, a0, a1 = ev(), ev(), ev(), ev()
                 c0.record(stream)
@@ -271,8 +276,8 @@ def run_dkv(args, world, rank, local):
                         f"{Hq} q / {H} KV heads, d=128, {T} decode steps with compaction and score update",
             "requests": R, "prompt_len": lens[0], "decode_steps": T, "q_heads": Hq, "kv_heads": H,
             "alpha_h": w.alpha_h, "alpha_l": w.alpha_l, "window": w.recent_window, "page_bytes": w.page_bytes,
-            "l2": "256 MiB write before every decode step (outside the decode_attention events); "
-                  "prompt inputs 537 MB > L2",
+            "l2": "flushed before every decode step, outside the timed events: 256 MiB written, then a "
+                  "second 256 MiB read (L2 left clean); prompt inputs 537 MB > L2",
             "value_is": "decode-attention algorithmic bytes / decode_attention device time (all steps)",
             "parallelism": f"{world} independent pools (one per GPU), no collective in the path",
         },
@@ -285,7 +290,7 @@ def run_dkv(args, world, rank, local):
                                            "pruned": n_th - prompt_counts[1] - prompt_counts[2]},
             "kv_bytes_vs_fp16": round((HI_BYTES * prompt_counts[1] + LO_BYTES * prompt_counts[2]) / (n_th * 512), 4),
         },
-        "roofline": {"bound": "hbm", "kernel": "dkv_decode_attention (k_attn_split + k_attn_merge + k_attn_scores)",
+        "roofline": {"bound": "hbm", "kernel": "dkv_decode_attention call (k_attn_paged + k_attn_scores)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": int(per_launch_bytes), "traffic": args.traffic},

@@ -19,7 +19,8 @@ torch = pytest.importorskip("torch")
 # Attention: |gpu - ref| <= ATOL + RTOL |ref| elementwise (fp64 reference over
 # the same dequantised values).
 ATT_ATOL, ATT_RTOL = 1e-3, 2e-3
-# Scores: fp32 tensor-core logits and exp2 against fp64 (see the design doc reading).
+# Scores: fp32 tensor-core logits and exp2 against fp64: relative error of a
+# few fp32 roundings per term, summed over at most 32 observation queries.
 SC_ATOL, SC_RTOL = 1e-6, 5e-5
 # Tie band: a token whose fp64 importance lies within this relative distance of
 # a threshold may land on either side.
