@@ -31,6 +31,11 @@ namespace dkv {
 constexpr int kStages = 3;                 // ring depth per warp (chunked path)
 constexpr int kPageStages = 4;             // ring depth per warp (paged path)
 constexpr int kMinChunks = 8;              // ring work items per warp at least
+// Paged path: a page's share of a warp's range, in cost units: a fixed part
+// for staging and bookkeeping plus a part per 16-slot chunk (ratio measured
+// from per-warp timings on GB300).
+constexpr int kPageW = 5;
+constexpr int kChunkW = 4;
 constexpr int kCtasPerSm = 3;
 constexpr int kOffV = 2048;                // chunked stage image: V rows
 constexpr int kOffMeta = 3072;             // chunked stage image: page meta segments
@@ -84,12 +89,13 @@ struct AttnArgs {
   float* out;         // [n_req][Hkv*G][128]
   float* part;        // [unit][max_parts][G*128 + 16]: O (G x 128), m (8), l (8); a
                       // multiple of 4 floats so every record is 16-byte aligned
-  float* logit;       // [unit][max_chunks][16][8] (log2-domain logits)
+  float* logit;       // [unit][max_chunks][128]: chunk rows of [query < G][16 slots] (log2-domain logits)
   float* lse2;        // [unit][G]
-  int* done;          // [unit] partials published (zero between calls)
+  int* done;          // [unit] number of partials of the head (written by every publisher)
   int max_parts, max_chunks;
   int update;
   int layer;
+  int paged;          // 1: logit rows also carry the old scores and the page ID (paged path)
   int mseg;           // chunked: bytes per page meta segment in the stage
   int maxp;           // chunked: pages a chunk can touch
   int stage_bytes;
@@ -154,6 +160,49 @@ __device__ __forceinline__ void load_q(const PoolView& pv, const AttnArgs& a, in
   sum += __shfl_xor_sync(0xffffffffu, sum, 2);
   const float sc = 1.4426950408889634f * rsqrtf((float)kD);
   // sum(q) of the thread's two score columns (queries 2t, 2t+1), pre-scaled
+  sq0 = __shfl_sync(0xffffffffu, sum, (2 * t) * 4) * sc;
+  sq1 = __shfl_sync(0xffffffffu, sum, (2 * t + 1) * 4) * sc;
+}
+
+// Query fragments in the feature order of one tier's key rows (hi: 8-bit,
+// lo: 4-bit) and the pre-scaled sums of queries 2t, 2t+1.
+__device__ __forceinline__ void load_q1(const PoolView& pv, const AttnArgs& a, int i, int kvh, int g, int t, bool hi,
+                                        uint32_t (&bq)[8][2], float& sq0, float& sq1) {
+  const int G = pv.G;
+  float qf[32];
+  if (g < G) {
+    const uint4* qp = reinterpret_cast<const uint4*>(a.q + ((size_t)i * pv.hkv * G + (size_t)kvh * G + g) * kD + 32 * t);
+#pragma unroll
+    for (int x = 0; x < 4; x++) {
+      const uint4 u = qp[x];
+      const __half* h = reinterpret_cast<const __half*>(&u);
+#pragma unroll
+      for (int y = 0; y < 8; y++) qf[8 * x + y] = __half2float(h[y]);
+    }
+  } else {
+#pragma unroll
+    for (int x = 0; x < 32; x++) qf[x] = 0.0f;
+  }
+  float sum = 0.0f;
+#pragma unroll
+  for (int x = 0; x < 32; x++) sum += qf[x];
+  if (hi) {
+#pragma unroll
+    for (int kk = 0; kk < 8; kk++) {
+      bq[kk][0] = pack_half2(qf[4 * kk], qf[4 * kk + 1]);
+      bq[kk][1] = pack_half2(qf[4 * kk + 2], qf[4 * kk + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < 8; kk++) {
+      const int w = kk >> 1, na = (kk & 1) ? 2 : 0;
+      bq[kk][0] = pack_half2(qf[8 * w + na], qf[8 * w + na + 4]);
+      bq[kk][1] = pack_half2(qf[8 * w + na + 1], qf[8 * w + na + 5]);
+    }
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  const float sc = 1.4426950408889634f * rsqrtf((float)kD);
   sq0 = __shfl_sync(0xffffffffu, sum, (2 * t) * 4) * sc;
   sq1 = __shfl_sync(0xffffffffu, sum, (2 * t + 1) * 4) * sc;
 }
@@ -231,9 +280,16 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
   l2[1] = vA ? __fmaf_rn(acc0[1] + acc1[1], skA * sc, zkA * sq1) : -INFINITY;
   l2[2] = vB ? __fmaf_rn(acc0[2] + acc1[2], skB * sc, zkB * sq0) : -INFINITY;
   l2[3] = vB ? __fmaf_rn(acc0[3] + acc1[3], skB * sc, zkB * sq1) : -INFINITY;
-  if (lg != nullptr && 2 * t < G) {
-    *reinterpret_cast<float2*>(lg + g * 8 + 2 * t) = make_float2(l2[0], l2[1]);
-    *reinterpret_cast<float2*>(lg + (g + 8) * 8 + 2 * t) = make_float2(l2[2], l2[3]);
+  if (lg != nullptr) {             // logit row of the chunk: [query][slot]
+    const int jA = chunk_slot(g), jB = chunk_slot(g + 8);
+    if (2 * t < G) {
+      lg[(2 * t) * kChunk + jA] = l2[0];
+      lg[(2 * t) * kChunk + jB] = l2[2];
+    }
+    if (2 * t + 1 < G) {
+      lg[(2 * t + 1) * kChunk + jA] = l2[1];
+      lg[(2 * t + 1) * kChunk + jB] = l2[3];
+    }
   }
   float cm0 = fmaxf(l2[0], l2[2]), cm1 = fmaxf(l2[1], l2[3]);
 #pragma unroll
@@ -301,9 +357,12 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
 }
 
 // Publish the warp's partial of head u (items [begin, end), warp ranges of C
-// items); the last warp of the head merges every partial into out and lse2.
-__device__ void publish(const PoolView& pv, const AttnArgs& a, const SlotArgs& sa, AttnState& S, int u, int first,
-                        int last, int gw, int lane) {
+// Publish the warp's partial of head u: O^T (with the value-zero sums added),
+// the running maxima and sums of queries 0..G-1, at index gw - first of the
+// head's partials (warp ranges first..last cover the head). The merge runs in
+// k_attn_merge once every warp is done.
+__device__ void publish(const PoolView& pv, const AttnArgs& a, AttnState& S, int u, int first, int last, int gw,
+                        int lane) {
   const int G = pv.G, g = lane >> 2, t = lane & 3;
   float l0 = S.l[0], l1 = S.l[1], z0 = S.z[0], z1 = S.z[1];
 #pragma unroll
@@ -326,54 +385,21 @@ __device__ void publish(const PoolView& pv, const AttnArgs& a, const SlotArgs& s
     if (2 * t < G) { dst[G * kD + 2 * t] = S.m[0]; dst[G * kD + kMaxG + 2 * t] = l0; }
     if (2 * t + 1 < G) { dst[G * kD + 2 * t + 1] = S.m[1]; dst[G * kD + kMaxG + 2 * t + 1] = l1; }
   }
-  __threadfence();
-  __syncwarp();
-  int prev = 0;
-  if (lane == 0) prev = atomicAdd(&a.done[u], 1);
-  prev = __shfl_sync(0xffffffffu, prev, 0);
-  const int nparts = last - first + 1;
-  if (prev != nparts - 1) return;
-  __threadfence();
-  const float* src = a.part + (size_t)u * a.max_parts * stride;
-  const int i = u / pv.hkv, kvh = u % pv.hkv;
-  for (int qh = 0; qh < G; qh++) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < nparts; sp++) M = fmaxf(M, __ldcg(src + sp * stride + G * kD + qh));
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    float Lsum = 0.0f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < nparts; sp++) {
-        const float ms = __ldcg(src + sp * stride + G * kD + qh);
-        if (ms == -INFINITY) continue;
-        const float w = exp2f(ms - M);
-        const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + sp * stride + qh * kD) + lane);
-        O.x += w * o4.x; O.y += w * o4.y; O.z += w * o4.z; O.w += w * o4.w;
-        Lsum += w * __ldcg(src + sp * stride + G * kD + kMaxG + qh);
-      }
-    }
-    const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-    reinterpret_cast<float4*>(a.out + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qh) * kD)[lane] =
-        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
-    if (lane == 0) a.lse2[(size_t)u * G + qh] = Lsum > 0.0f ? M + log2f(Lsum) : -INFINITY;
-  }
-  if (lane == 0) {
-    a.done[u] = 0;
-    if (a.update && kvh == 0) pv.rq(a.layer, sa.slots[i])[3] += 1;
-  }
+  if (lane == 0) a.done[u] = last - first + 1;
 }
 
 // Prefix over the call's heads of their work items (pages or chunks), in
 // shared memory; every CTA computes the same. Returns the total.
-__device__ int item_prefix(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int* s_pref, int* s_warp) {
+__device__ int item_prefix(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int* s_pref,
+                           int* s_warp) {
   const int n_units = sa.n * pv.hkv;
   const int per = (n_units + blockDim.x - 1) / blockDim.x;
   const int u0 = min(n_units, (int)threadIdx.x * per), u1 = min(n_units, u0 + per);
   int sum = 0;
   for (int u = u0; u < u1; u++) {
     const int* cn = pv.cnt(layer, sa.slots[u / pv.hkv], u % pv.hkv);
-    // paged: pages weighted by their chunks (T / 16); chunked: chunks
-    const int items = paged ? (cn[0] + pv.hi.t - 1) / pv.hi.t * (pv.hi.t / kChunk) +
-                                  (cn[1] + pv.lo.t - 1) / pv.lo.t * (pv.lo.t / kChunk)
+    // paged: pages weighted by their cost (wh, wl); chunked: chunks
+    const int items = paged ? (cn[0] + pv.hi.t - 1) / pv.hi.t * wh + (cn[1] + pv.lo.t - 1) / pv.lo.t * wl
                             : (cn[0] + kChunk - 1) / kChunk + (cn[1] + kChunk - 1) / kChunk;
     s_pref[u] = items;
     sum += items;
@@ -422,17 +448,25 @@ __device__ __forceinline__ int find_unit(const int* s_pref, int n_units, int g0)
 }
 
 // ---------------------------------------------------------------------------
-// Paged path: pages of T = 16k tokens (k = 1, 2), one bulk copy per page of
-// its first four segments (K rows, V rows, K meta, V meta are contiguous at
-// the page start). The work sequence is measured in chunks (a page weighs
-// T/16); a warp takes the pages that start inside its range of chunks.
+// Paged path: pages of T = 16k tokens (k = 1, 2, ...), one bulk copy per page
+// of its first four segments (K rows, V rows, K meta, V meta are contiguous at
+// the page start). The work sequence is measured in cost units (a page weighs
+// kPageW + kChunkW * T/16); a warp takes the pages that start inside its range.
+// One cursor walks the pages on the issue side and leaves a descriptor of
+// each staged page next to its stage. The softmax rescales lazily: a group's
+// probabilities are taken against the running maximum as long as no logit
+// exceeds it by more than kLazy (log2 units), so that the cross-lane maximum
+// and the rescale of O run only when the maximum really moves.
 // ---------------------------------------------------------------------------
+constexpr float kNegBig = -1.0e30f;   // running maximum before the first token
+constexpr float kLazy = 8.0f;         // probabilities stay below 2^kLazy
+
 struct PageCursor {
-  int u, begin, end;   // head and its chunk range
+  int u, begin, end;   // head and its cost range
   int hp, np;          // hi pages, all pages
   int nh, nl;
   const int* row;
-  int p, off;          // current page and its chunk offset
+  int p, off;          // current page and its cost offset
 };
 
 struct PagedCtx {
@@ -463,7 +497,7 @@ struct PagedCtx {
     c.p++;
     settle(c);
   }
-  // first page starting at chunk offset >= x
+  // first page starting at cost offset >= x
   __device__ __forceinline__ void seek(PageCursor& c, int x) const {
     at_unit(c, find_unit(s_pref, n_units, x));
     const int o = x - c.begin;
@@ -479,117 +513,331 @@ struct PagedCtx {
     settle(c);
   }
   __device__ __forceinline__ bool valid(const PageCursor& c, int g1) const { return c.p < c.np && c.off < g1; }
-  // warps that own pages of head c.u (range width C)
-  __device__ __forceinline__ void owners(const PageCursor& c, int C, int& first, int& last) const {
-    first = c.begin / C;
-    last = (c.end - (c.np > c.hp ? wl : wh)) / C;
+  // warps that own pages of head u (range width C); nl: its lo tokens
+  __device__ __forceinline__ void owners(int u, int nl, int C, int& first, int& last) const {
+    first = s_pref[u] / C;
+    last = (s_pref[u + 1] - (nl > 0 ? wl : wh)) / C;
   }
 };
 
+__device__ __forceinline__ void lazy_reset(AttnState& S) {
+#pragma unroll
+  for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+    for (int x = 0; x < 4; x++) S.o[mt][x] = 0.0f;
+  S.m[0] = S.m[1] = kNegBig;
+  S.l[0] = S.l[1] = 0.0f;
+  S.z[0] = S.z[1] = 0.0f;
+}
+
+__device__ __forceinline__ float lo_half(uint32_t w) { return __half2float(__ushort_as_half((uint16_t)w)); }
+__device__ __forceinline__ float hi_half(uint32_t w) { return __half2float(__ushort_as_half((uint16_t)(w >> 16))); }
+
+// NC consecutive chunks c0 .. c0+NC-1 of a staged page, one softmax step.
+// FULL: every slot of the chunks is valid (no masking).
+template <bool HI, int NC, bool FULL>
+__device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, const TierGeom& tg, int c0, int count,
+                                              const uint32_t (&bq)[8][2], float sq0, float sq1, float* lg, int pid,
+                                              int G, int g, int t, int jA, int jB) {
+  constexpr float sc = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+  float l2[NC][4];
+  uint32_t vm[NC][2];
+#pragma unroll
+  for (int c = 0; c < NC; c++) {
+    const int sA = (c0 + c) * kChunk + jA, sB = (c0 + c) * kChunk + jB;
+    float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (HI) {
+      const uint4* pa = reinterpret_cast<const uint4*>(sb + sA * 128 + 32 * t);
+      const uint4* pb = reinterpret_cast<const uint4*>(sb + sB * 128 + 32 * t);
+      const uint4 ka0 = pa[0], ka1 = pa[1], kb0 = pb[0], kb1 = pb[1];
+      const uint32_t kaw[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+      const uint32_t kbw[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) {
+        uint32_t af[4];
+        af[0] = cvt_k8(kaw[kk], 0x4140u);
+        af[1] = cvt_k8(kbw[kk], 0x4140u);
+        af[2] = cvt_k8(kaw[kk], 0x4342u);
+        af[3] = cvt_k8(kbw[kk], 0x4342u);
+        mma16816((kk & 1) ? acc1 : acc0, af, bq[kk][0], bq[kk][1]);
+      }
+    } else {
+      const uint4 ka = *reinterpret_cast<const uint4*>(sb + sA * 64 + 16 * t);
+      const uint4 kb = *reinterpret_cast<const uint4*>(sb + sB * 64 + 16 * t);
+      const uint32_t kaw[4] = {ka.x, ka.y, ka.z, ka.w};
+      const uint32_t kbw[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) {
+        const uint32_t wa = (kk & 1) ? kaw[kk >> 1] >> 8 : kaw[kk >> 1];
+        const uint32_t wb = (kk & 1) ? kbw[kk >> 1] >> 8 : kbw[kk >> 1];
+        uint32_t af[4];
+        af[0] = cvt4_0(wa);
+        af[1] = cvt4_0(wb);
+        af[2] = cvt4_1(wa);
+        af[3] = cvt4_1(wb);
+        mma16816((kk & 1) ? acc1 : acc0, af, bq[kk][0], bq[kk][1]);
+      }
+    }
+    const uint32_t kmA = *reinterpret_cast<const uint32_t*>(sb + tg.off[2] + 4 * sA);
+    const uint32_t kmB = *reinterpret_cast<const uint32_t*>(sb + tg.off[2] + 4 * sB);
+    vm[c][0] = *reinterpret_cast<const uint32_t*>(sb + tg.off[3] + 4 * sA);
+    vm[c][1] = *reinterpret_cast<const uint32_t*>(sb + tg.off[3] + 4 * sB);
+    const float skA = lo_half(kmA) * sc, zkA = hi_half(kmA), skB = lo_half(kmB) * sc, zkB = hi_half(kmB);
+    l2[c][0] = __fmaf_rn(acc0[0] + acc1[0], skA, zkA * sq0);
+    l2[c][1] = __fmaf_rn(acc0[1] + acc1[1], skA, zkA * sq1);
+    l2[c][2] = __fmaf_rn(acc0[2] + acc1[2], skB, zkB * sq0);
+    l2[c][3] = __fmaf_rn(acc0[3] + acc1[3], skB, zkB * sq1);
+    if (!FULL) {
+      if (sA >= count) l2[c][0] = l2[c][1] = -INFINITY;
+      if (sB >= count) l2[c][2] = l2[c][3] = -INFINITY;
+    }
+    if (lg != nullptr) {           // scratch row of the chunk: logits, old scores, page ID
+      float* lc = lg + c * kLogitRow;
+      if (2 * t < G) {
+        lc[(2 * t) * kChunk + jA] = l2[c][0];
+        lc[(2 * t) * kChunk + jB] = l2[c][2];
+      }
+      if (2 * t + 1 < G) {
+        lc[(2 * t + 1) * kChunk + jA] = l2[c][1];
+        lc[(2 * t + 1) * kChunk + jB] = l2[c][3];
+      }
+      if (t == 0) {
+        lc[G * kChunk + jA] = *reinterpret_cast<const float*>(sb + tg.off[4] + 4 * sA);
+        lc[G * kChunk + jB] = *reinterpret_cast<const float*>(sb + tg.off[4] + 4 * sB);
+        if (g == 0) reinterpret_cast<int*>(lc)[(G + 1) * kChunk] = pid;
+      }
+    }
+  }
+  // ---- lazy online softmax over the NC chunks ----
+  float cm0 = fmaxf(l2[0][0], l2[0][2]), cm1 = fmaxf(l2[0][1], l2[0][3]);
+#pragma unroll
+  for (int c = 1; c < NC; c++) {
+    cm0 = fmaxf(cm0, fmaxf(l2[c][0], l2[c][2]));
+    cm1 = fmaxf(cm1, fmaxf(l2[c][1], l2[c][3]));
+  }
+  if (__any_sync(0xffffffffu, cm0 > S.m[0] + kLazy || cm1 > S.m[1] + kLazy)) {
+#pragma unroll
+    for (int s = 4; s <= 16; s <<= 1) {
+      cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, s));
+      cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, s));
+    }
+    const float mn0 = fmaxf(S.m[0], cm0), mn1 = fmaxf(S.m[1], cm1);
+    const float f0 = fast_exp2(S.m[0] - mn0), f1 = fast_exp2(S.m[1] - mn1);
+    S.m[0] = mn0;
+    S.m[1] = mn1;
+    S.l[0] *= f0; S.z[0] *= f0;
+    S.l[1] *= f1; S.z[1] *= f1;
+#pragma unroll
+    for (int mt = 0; mt < 8; mt++) {
+      S.o[mt][0] *= f0; S.o[mt][2] *= f0;
+      S.o[mt][1] *= f1; S.o[mt][3] *= f1;
+    }
+  }
+  // v^ = s (c - off) + (z + off s), off = 8 (hi) or 2 (lo)
+  constexpr float voff = HI ? 8.0f : 2.0f;
+#pragma unroll
+  for (int c = 0; c < NC; c++) {
+    const float p0 = fast_exp2(l2[c][0] - S.m[0]), p1 = fast_exp2(l2[c][1] - S.m[1]);
+    const float p2 = fast_exp2(l2[c][2] - S.m[0]), p3 = fast_exp2(l2[c][3] - S.m[1]);
+    float svA = lo_half(vm[c][0]), svB = lo_half(vm[c][1]);
+    float zvA = __fmaf_rn(voff, svA, hi_half(vm[c][0])), zvB = __fmaf_rn(voff, svB, hi_half(vm[c][1]));
+    if (!FULL) {                   // meta of an unused slot may hold any bits
+      const int sA = (c0 + c) * kChunk + jA, sB = (c0 + c) * kChunk + jB;
+      if (sA >= count) svA = zvA = 0.0f;
+      if (sB >= count) svB = zvB = 0.0f;
+    }
+    S.l[0] += p0 + p2;
+    S.l[1] += p1 + p3;
+    S.z[0] = __fmaf_rn(p0, zvA, __fmaf_rn(p2, zvB, S.z[0]));
+    S.z[1] = __fmaf_rn(p1, zvA, __fmaf_rn(p3, zvB, S.z[1]));
+    // P'^T as B fragments: block of tokens 0-7 and block of tokens 8-15
+    const uint32_t pb0 = movmatrix_trans(pack_half2(p0 * svA, p1 * svA));
+    const uint32_t pb1 = movmatrix_trans(pack_half2(p2 * svB, p3 * svB));
+    // ---- O^T += V^T . P'^T ----
+    if (HI) {
+      const uint8_t* v0 = sb + tg.off[1] + ((c0 + c) * 8 + 2 * t) * 128 + 16 * g;
+      const uint4 vq0 = *reinterpret_cast<const uint4*>(v0);
+      const uint4 vq1 = *reinterpret_cast<const uint4*>(v0 + 128);
+      const uint32_t vw0[4] = {vq0.x, vq0.y, vq0.z, vq0.w};
+      const uint32_t vw1[4] = {vq1.x, vq1.y, vq1.z, vq1.w};
+#pragma unroll
+      for (int mt = 0; mt < 8; mt++) {
+        const uint32_t w0 = (mt & 1) ? vw0[mt >> 1] >> 8 : vw0[mt >> 1];
+        const uint32_t w1 = (mt & 1) ? vw1[mt >> 1] >> 8 : vw1[mt >> 1];
+        uint32_t af[4];
+        af[0] = cvv4_0(w0);   // feature 16g+2mt,   tokens 2t,2t+1
+        af[1] = cvv4_1(w0);   // feature 16g+2mt+1, tokens 2t,2t+1
+        af[2] = cvv4_0(w1);   // feature 16g+2mt,   tokens 2t+8,2t+9
+        af[3] = cvv4_1(w1);   // feature 16g+2mt+1, tokens 2t+8,2t+9
+        mma16816(S.o[mt], af, pb0, pb1);
+      }
+    } else {
+      const uint4 vq = *reinterpret_cast<const uint4*>(sb + tg.off[1] + ((c0 + c) * 4 + t) * 128 + 16 * g);
+      const uint32_t vw[4] = {vq.x, vq.y, vq.z, vq.w};
+#pragma unroll
+      for (int mt = 0; mt < 8; mt++) {
+        const uint32_t w = (mt & 1) ? vw[mt >> 1] >> 8 : vw[mt >> 1];
+        uint32_t af[4];
+        af[0] = cvv2_0(w);    // feature 16g+2mt,   slots e0,e1
+        af[1] = cvv2_2(w);    // feature 16g+2mt+1, slots e0,e1
+        af[2] = cvv2_1(w);    // feature 16g+2mt,   slots e2,e3
+        af[3] = cvv2_3(w);    // feature 16g+2mt+1, slots e2,e3
+        mma16816(S.o[mt], af, pb0, pb1);
+      }
+    }
+  }
+}
+
+// All chunks of one staged page: pairs of chunks share a softmax step.
+template <bool HI>
+__device__ __forceinline__ void attend_page(AttnState& S, const uint8_t* sb, const TierGeom& tg, int nch, int count,
+                                            const uint32_t (&bq)[8][2], float sq0, float sq1, float* lg, int pid,
+                                            int G, int g, int t, int jA, int jB) {
+  if (count >= nch * kChunk) {
+    int c = 0;
+    for (; c + 2 <= nch; c += 2)
+      attend_chunks<HI, 2, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * kLogitRow : nullptr, pid, G, g, t,
+                                 jA, jB);
+    if (c < nch)
+      attend_chunks<HI, 1, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * kLogitRow : nullptr, pid, G, g, t,
+                                 jA, jB);
+  } else {
+    for (int c = 0; c * kChunk < count; c++)
+      attend_chunks<HI, 1, false>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * kLogitRow : nullptr, pid, G, g, t,
+                                  jA, jB);
+  }
+}
+
 __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
+  pdl_launch_dependents();        // the merge grid may launch as SMs free up
   if (pv.noop()) return;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_warp[kAttnWarps];
   const int n_units = sa.n * pv.hkv;
   const int G = pv.G;
+  const int nch_hi = pv.hi.t / kChunk, nch_lo = pv.lo.t / kChunk;
+  const int wh = kPageW + kChunkW * nch_hi, wl = kPageW + kChunkW * nch_lo;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kAttnWarps * kPageStages * a.stage_bytes);
-  int* s_pref = reinterpret_cast<int*>(s_bar + kAttnWarps * kPageStages);
-  const int total = item_prefix(pv, sa, a.layer, true, s_pref, s_warp);
+  int4* s_desc = reinterpret_cast<int4*>(s_bar + kAttnWarps * kPageStages);
+  int* s_pref = reinterpret_cast<int*>(s_desc + 2 * kAttnWarps * kPageStages);   // s_desc: [warp][stage][2]
+  const int total = item_prefix(pv, sa, a.layer, true, wh, wl, s_pref, s_warp);
   const int nwarps = gridDim.x * kAttnWarps;
-  const int C = max(kMinChunks, (total + nwarps - 1) / nwarps);
+  // at least kMinChunks pages of the heaviest kind per range: a head is then
+  // covered by at most (its pages / kMinChunks) + 2 ranges
+  const int C = max(kMinChunks * max(wh, wl), (total + nwarps - 1) / nwarps);
   if (blockIdx.x == 0) zero_empty_heads(pv, a, sa, s_pref);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int gw = blockIdx.x * kAttnWarps + warp;
   const int g0 = gw * C, g1 = min(total, g0 + C);
-  if (g0 >= g1) return;           // no block-wide barrier follows
-  const PagedCtx ctx{pv, sa, s_pref, a.layer, n_units, pv.hi.t / kChunk, pv.lo.t / kChunk};
-  PageCursor ci, cc;
-  ctx.seek(ci, g0);
-  if (!ctx.valid(ci, g1)) return;  // no page starts inside this range
-  cc = ci;
-  uint32_t bq_hi[8][2], bq_lo[8][2];
-  float sq0, sq1;
-  load_q(pv, a, cc.u / pv.hkv, cc.u % pv.hkv, g, t, bq_hi, bq_lo, sq0, sq1);
+  const PagedCtx ctx{pv, sa, s_pref, a.layer, n_units, wh, wl};
+  PageCursor ci;
+  bool active = g0 < g1;
+  if (active) {
+    ctx.seek(ci, g0);
+    active = ctx.valid(ci, g1);     // a page starts inside this range
+  }
   uint8_t* wst = smem + warp * (kPageStages * a.stage_bytes);
+  int4* wdesc = s_desc + 2 * warp * kPageStages;
   const uint32_t bar0 = smem_u32(s_bar + warp * kPageStages);
-  if (lane == 0) {
-    for (int st = 0; st < kPageStages; st++) mbar_init(bar0 + 8 * st, 1);
-    fence_mbar_init();
-    fence_proxy_async();
-  }
-  __syncwarp();
   int issued = 0;
-  // one lane copies the next page's K | V | K meta | V meta prefix
-  auto try_issue = [&]() {
-    if (!ctx.valid(ci, g1)) return;
+  bool failed = false;
+  if (active) {
     if (lane == 0) {
-      const int st = issued % kPageStages;
-      const bool hi = ci.p < ci.hp;
-      const TierGeom& tg = hi ? pv.hi : pv.lo;
-      const int e = hi ? ci.p : pv.L - 1 - (ci.p - ci.hp);
-      const uint32_t bar = bar0 + 8 * st;
-      const uint32_t bytes = tg.off[4];
-      mbar_expect_tx(bar, bytes);
-      bulk_g2s(smem_u32(wst + st * a.stage_bytes), pv.page(__ldg(ci.row + e)), bytes, bar);
+      for (int st = 0; st < kPageStages; st++) mbar_init(bar0 + 8 * st, 1);
+      fence_mbar_init();
+      fence_proxy_async();
     }
-    issued++;
-    ctx.next(ci);
-  };
-  AttnState S;
-  S.reset();
-  for (int x = 0; x < kPageStages - 1; x++) try_issue();
-  int cur_u = cc.u;
-  for (int x = 0; x < issued; x++) {
-    __syncwarp();                 // every lane is done with the stage being refilled
-    fence_proxy_async();
-    try_issue();
-    if (!mbar_wait_bounded(bar0 + 8 * (x % kPageStages), (x / kPageStages) & 1)) {
-      if (lane == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = cc.u;
-      for (int y = x + 1; y < min(issued, x + kPageStages); y++)
-        mbar_wait_bounded(bar0 + 8 * (y % kPageStages), (y / kPageStages) & 1);
-      return;
-    }
-    if (cc.u != cur_u) {          // the range crosses into the next head
-      PageCursor prev = cc;
-      ctx.at_unit(prev, cur_u);
-      int first, last;
-      ctx.owners(prev, C, first, last);
-      publish(pv, a, sa, S, cur_u, first, last, gw, lane);
-      cur_u = cc.u;
-      load_q(pv, a, cc.u / pv.hkv, cc.u % pv.hkv, g, t, bq_hi, bq_lo, sq0, sq1);
-      S.reset();
-    }
-    const bool hi = cc.p < cc.hp;
-    const TierGeom& tg = hi ? pv.hi : pv.lo;
-    const int pt = hi ? cc.p : cc.p - cc.hp;             // page index within the tier
-    const int count = (hi ? cc.nh : cc.nl) - pt * tg.t;  // valid slots from this page's start
-    const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
+    __syncwarp();
+    // page ID of cursor ci, loaded one issue ahead so that the table read is
+    // off the issue path (lane 0 only)
+    int pid = 0;
+    auto load_pid = [&]() {
+      if (lane == 0 && ctx.valid(ci, g1)) {
+        const bool hi = ci.p < ci.hp;
+        pid = __ldg(ci.row + (hi ? ci.p : pv.L - 1 - (ci.p - ci.hp)));
+      }
+    };
+    // lane 0 copies the next page's K | V | K meta | V meta | score prefix and
+    // records {head, page, hi count, lo count} and its page ID beside the stage
+    auto try_issue = [&]() {
+      if (!ctx.valid(ci, g1)) return;
+      if (lane == 0) {
+        const int st = issued % kPageStages;
+        const uint32_t bar = bar0 + 8 * st;
+        const bool hi = ci.p < ci.hp;
+        const uint32_t bytes = hi ? pv.hi.off[5] : pv.lo.off[5];
+        wdesc[2 * st] = make_int4(ci.u, ci.p, ci.nh, ci.nl);
+        wdesc[2 * st + 1] = make_int4(pid, 0, 0, 0);
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(smem_u32(wst + st * a.stage_bytes), pv.page(pid), bytes, bar);
+      }
+      issued++;
+      ctx.next(ci);
+      load_pid();
+    };
+    const int u_first = ci.u, nl_first = ci.nl;
+    const bool hi_first = ci.p < ci.hp;
+    load_pid();
+    for (int x = 0; x < kPageStages - 1; x++) try_issue();
+    AttnState S;
+    lazy_reset(S);
+    // the first head's queries load while its first pages are in flight
+    uint32_t bq[8][2];
+    float sq0, sq1;
+    bool q_hi = hi_first;
+    int cur_u = u_first, cur_nl = nl_first;
+    load_q1(pv, a, u_first / pv.hkv, u_first % pv.hkv, g, t, hi_first, bq, sq0, sq1);
     const int jA = chunk_slot(g), jB = chunk_slot(g + 8);
-    const int n_chunks = tg.t / kChunk;
-    const int chunk0 = hi ? pt * n_chunks : (cc.nh + kChunk - 1) / kChunk + pt * n_chunks;
-    for (int c = 0; c < n_chunks && c * kChunk < count; c++) {
-      const int sA = c * kChunk + jA, sB = c * kChunk + jB;
-      const uint8_t* kA = sb + sA * tg.kbytes + (hi ? 32 * t : 16 * t);
-      const uint8_t* kB = sb + sB * tg.kbytes + (hi ? 32 * t : 16 * t);
-      const uint8_t* v0 = hi ? sb + tg.off[1] + (c * 8 + 2 * t) * 128 + 16 * g : sb + tg.off[1] + (c * 4 + t) * 128 + 16 * g;
-      const uint8_t* v1 = v0 + 128;
-      const uint32_t kmA = *reinterpret_cast<const uint32_t*>(sb + tg.off[2] + 4 * sA);
-      const uint32_t kmB = *reinterpret_cast<const uint32_t*>(sb + tg.off[2] + 4 * sB);
-      const uint32_t vmA = *reinterpret_cast<const uint32_t*>(sb + tg.off[3] + 4 * sA);
-      const uint32_t vmB = *reinterpret_cast<const uint32_t*>(sb + tg.off[3] + 4 * sB);
-      float* lg = a.update ? a.logit + ((size_t)cc.u * a.max_chunks + chunk0 + c) * (kChunk * 8) : nullptr;
-      attend_chunk(S, hi, kA, kB, v0, v1, kmA, kmB, vmA, vmB, sA < count, sB < count, bq_hi, bq_lo, sq0, sq1, lg,
-                   G, g, t);
+    for (int x = 0; x < issued; x++) {
+      __syncwarp();               // every lane is done with the stage being refilled
+      fence_proxy_async();
+      try_issue();
+      if (!mbar_wait_bounded(bar0 + 8 * (x % kPageStages), (x / kPageStages) & 1)) {
+        if (lane == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = cur_u;
+        for (int y = x + 1; y < min(issued, x + kPageStages); y++)
+          mbar_wait_bounded(bar0 + 8 * (y % kPageStages), (y / kPageStages) & 1);
+        failed = true;
+        break;
+      }
+      const int4 d = wdesc[2 * (x % kPageStages)];  // head, page, hi count, lo count
+      const int dpid = wdesc[2 * (x % kPageStages) + 1].x;
+      const int hp = pv.hi.div(d.z + pv.hi.t - 1);
+      const bool hi = d.y < hp;
+      if (d.x != cur_u) {         // the range enters the next head
+        {
+          int first, last;
+          ctx.owners(cur_u, cur_nl, C, first, last);
+          publish(pv, a, S, cur_u, first, last, gw, lane);
+        }
+        cur_u = d.x;
+        cur_nl = d.w;
+        q_hi = hi;
+        load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
+        lazy_reset(S);
+      } else if (hi != q_hi) {    // from the head's hi pages to its lo pages
+        q_hi = hi;
+        load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
+      }
+      const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
+      float* lg0 = a.update ? a.logit + (size_t)cur_u * a.max_chunks * kLogitRow : nullptr;
+      if (hi) {
+        const int count = d.z - d.y * pv.hi.t;      // valid slots from this page's start
+        attend_page<true>(S, sb, pv.hi, nch_hi, count, bq, sq0, sq1,
+                          lg0 ? lg0 + (size_t)(d.y * nch_hi) * kLogitRow : nullptr, dpid, G, g, t, jA, jB);
+      } else {
+        const int pt = d.y - hp;
+        const int count = d.w - pt * pv.lo.t;
+        const int chunk0 = (d.z + kChunk - 1) / kChunk + pt * nch_lo;
+        attend_page<false>(S, sb, pv.lo, nch_lo, count, bq, sq0, sq1,
+                           lg0 ? lg0 + (size_t)chunk0 * kLogitRow : nullptr, dpid, G, g, t, jA, jB);
+      }
     }
-    ctx.next(cc);
-  }
-  {
-    PageCursor prev = cc;
-    ctx.at_unit(prev, cur_u);
-    int first, last;
-    ctx.owners(prev, C, first, last);
-    publish(pv, a, sa, S, cur_u, first, last, gw, lane);
+    if (!failed) {
+      int first, last;
+      ctx.owners(cur_u, cur_nl, C, first, last);
+      publish(pv, a, S, cur_u, first, last, gw, lane);
+    }
   }
 }
 
@@ -599,6 +847,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
 // it touches (the copies spread over the lanes).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, AttnArgs a, SlotArgs sa) {
+  pdl_launch_dependents();        // the merge grid may launch as SMs free up
   if (pv.noop()) return;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_warp[kAttnWarps];
@@ -606,7 +855,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
   const int G = pv.G;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kAttnWarps * kStages * a.stage_bytes);
   int* s_pref = reinterpret_cast<int*>(s_bar + kAttnWarps * kStages);
-  const int total = item_prefix(pv, sa, a.layer, false, s_pref, s_warp);
+  const int total = item_prefix(pv, sa, a.layer, false, 1, 1, s_pref, s_warp);
   const int nwarps = gridDim.x * kAttnWarps;
   const int C = max(kMinChunks, (total + nwarps - 1) / nwarps);
   if (blockIdx.x == 0) zero_empty_heads(pv, a, sa, s_pref);
@@ -695,7 +944,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
     }
     const int gx = g0 + x;
     if (gx >= cc.end) {           // the range crosses into the next head
-      publish(pv, a, sa, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
+      publish(pv, a, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
       cursor_seek(cc, gx, s_pref, pv, sa, a.layer, false);
       load_q(pv, a, cc.u / pv.hkv, cc.u % pv.hkv, g, t, bq_hi, bq_lo, sq0, sq1);
       S.reset();
@@ -720,40 +969,152 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
     const uint8_t* kB = sb + jB * tgc.kbytes + (hi ? 32 * t : 16 * t);
     const uint8_t* v0 = hi ? sb + kOffV + (2 * t) * 128 + 16 * g : sb + kOffV + t * 128 + 16 * g;
     const uint8_t* v1 = v0 + 128;
-    float* lg = a.update ? a.logit + ((size_t)cc.u * a.max_chunks + lc) * (kChunk * 8) : nullptr;
+    float* lg = a.update ? a.logit + ((size_t)cc.u * a.max_chunks + lc) * kLogitRow : nullptr;
     attend_chunk(S, hi, kA, kB, v0, v1, kmA, kmB, vmA, vmB, base + jA < count, base + jB < count, bq_hi, bq_lo,
                  sq0, sq1, lg, G, g, t);
   }
-  publish(pv, a, sa, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
+  publish(pv, a, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
 }
 
-// Score update: every stored token's score gains max over the group's heads
-// of its softmax probability, 2^(l2 - lse2).
-__global__ void __launch_bounds__(256) k_attn_scores(PoolView pv, AttnArgs a, SlotArgs sa) {
+// Merge of each head's partials into out and lse2 and, with update_scores,
+// the score update: every stored token's score gains the maximum over the
+// group's queries of its probability 2^(l2 - lse2). Grid (x, unit); block x
+// covers chunks kMergeChunks*x .. kMergeChunks*(x+1)-1 of the head for the
+// score update, and in block 0 warp q (q < G) also merges query q's output.
+// Launched as a programmatic dependent of the attention kernel: the head
+// counts, page IDs and scores before the update do not depend on it and are
+// loaded before the dependency wait. After it, every warp issues the loads
+// of the partial count, of every partial's maxima and sums (speculatively,
+// within the scratch bounds) and of its logits at once, and derives the
+// head's lse2 on its own, so that no block-wide barrier is needed.
+constexpr int kMergeChunks = 128;
+constexpr int kMergeK = kMergeChunks * kChunk / 256;   // score slots per thread
+
+template <int G>
+__global__ void __launch_bounds__(256, 3) k_attn_merge(PoolView pv, AttnArgs a, SlotArgs sa) {
   if (pv.noop()) return;
   const int unit = blockIdx.y, i = unit / pv.hkv, kvh = unit % pv.hkv;
   const int slot = sa.slots[i];
-  const int G = pv.G;
   const int* cn = pv.cnt(a.layer, slot, kvh);
-  const int nh = cn[0], nl = cn[1];
+  const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
   const int ch_hi = (nh + kChunk - 1) / kChunk;
-  const int c = blockIdx.x * (blockDim.x / kChunk) + threadIdx.x / kChunk;
-  const int r = threadIdx.x % kChunk;
   const int total = ch_hi + (nl + kChunk - 1) / kChunk;
-  if (c >= total) return;
-  const bool hi = c < ch_hi;
-  const int s = (hi ? c : c - ch_hi) * kChunk + chunk_slot(r);
-  if (s >= (hi ? nh : nl)) return;
-  const float* lg = a.logit + ((size_t)unit * a.max_chunks + c) * (kChunk * 8) + r * 8;
-  const float* l2 = a.lse2 + (size_t)unit * G;
-  float pm = 0.0f;
-  for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, exp2f(lg[qh] - l2[qh]));
+  const bool idle = nh + nl == 0 ||            // empty head: done by the attention kernel
+                    (blockIdx.x > 0 && (int)blockIdx.x * kMergeChunks >= total);
+  // ---- independent of the attention kernel ----
+  // chunked path: page IDs and scores before the update from the page table
+  // and the pages; paged path: both come from the scratch rows (below)
   const int* row = pv.row(a.layer, slot, kvh);
-  const TierGeom& tg = hi ? pv.hi : pv.lo;
-  const int d = tg.div(s);
-  uint8_t* pg = pv.page(row[hi ? d : pv.L - 1 - d]);
-  float* sp = reinterpret_cast<float*>(pg + tg.off[4] + 4 * (s - d * tg.t));
-  *sp = *sp + pm;
+  int pid[kMergeK];
+  float old[kMergeK];
+#pragma unroll
+  for (int k = 0; k < kMergeK; k++) {
+    const int x = k * 256 + threadIdx.x;
+    const int c = blockIdx.x * kMergeChunks + x / kChunk;
+    const bool hi = c < ch_hi;
+    const int sl = (hi ? c : c - ch_hi) * kChunk + x % kChunk;
+    const TierGeom& tg = hi ? pv.hi : pv.lo;
+    const int d = tg.div(sl);
+    const bool ok = a.update && !idle && c < total && sl < (hi ? nh : nl);
+    pid[k] = ok ? (a.paged ? 0 : __ldcg(row + (hi ? d : pv.L - 1 - d))) : -1;
+  }
+  if (!a.paged) {
+#pragma unroll
+    for (int k = 0; k < kMergeK; k++) {
+      old[k] = 0.0f;
+      if (pid[k] >= 0) {
+        const int x = k * 256 + threadIdx.x;
+        const int c = blockIdx.x * kMergeChunks + x / kChunk;
+        const bool hi = c < ch_hi;
+        const int sl = (hi ? c : c - ch_hi) * kChunk + x % kChunk;
+        const TierGeom& tg = hi ? pv.hi : pv.lo;
+        old[k] = __ldcg(reinterpret_cast<const float*>(pv.page(pid[k]) + tg.off[4]) + (sl - tg.div(sl) * tg.t));
+      }
+    }
+  }
+  // ---- after the attention kernel ----
+  pdl_wait();
+  if (idle || pv.noop()) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int stride = part_stride(G);
+  const float* src = a.part + (size_t)unit * a.max_parts * stride;
+  const int nparts = __ldcg(a.done + unit);
+  float lgv[kMergeK][G];
+  if (a.update) {
+#pragma unroll
+    for (int k = 0; k < kMergeK; k++) {
+      const int x = k * 256 + threadIdx.x;
+      const int c = min((int)blockIdx.x * kMergeChunks + x / kChunk, a.max_chunks - 1);
+      const float* lg = a.logit + ((size_t)unit * a.max_chunks + c) * kLogitRow;
+#pragma unroll
+      for (int qh = 0; qh < G; qh++) lgv[k][qh] = __ldcg(lg + qh * kChunk + x % kChunk);
+      if (a.paged && pid[k] >= 0) {
+        old[k] = __ldcg(lg + G * kChunk + x % kChunk);
+        pid[k] = __ldcg(reinterpret_cast<const int*>(lg) + (G + 1) * kChunk);
+      }
+    }
+  }
+  // lse2 of every query of the head, in every lane: one pass over the
+  // partials' maxima and sums (the same addresses in every lane), combined
+  // online
+  float M[G], L[G];
+#pragma unroll
+  for (int qh = 0; qh < G; qh++) {
+    M[qh] = -INFINITY;
+    L[qh] = 0.0f;
+  }
+#pragma unroll 8
+  for (int sp = 0; sp < nparts; sp++) {
+#pragma unroll
+    for (int qh = 0; qh < G; qh++) {
+      const float ms = __ldcg(src + sp * stride + G * kD + qh);
+      const float ls = __ldcg(src + sp * stride + G * kD + kMaxG + qh);
+      const float mx = fmaxf(M[qh], ms);
+      if (mx != -INFINITY) {
+        L[qh] = L[qh] * fast_exp2(M[qh] - mx) + ls * fast_exp2(ms - mx);
+        M[qh] = mx;
+      }
+    }
+  }
+  float lse[G];
+#pragma unroll
+  for (int qh = 0; qh < G; qh++) lse[qh] = L[qh] > 0.0f ? M[qh] + log2f(L[qh]) : -INFINITY;
+  if (blockIdx.x == 0 && warp < G) {           // output of query `warp`, features 4 lane .. 4 lane + 3
+    const int qh = warp;
+    float Mq = M[0], Lq = L[0], lq = lse[0];
+#pragma unroll
+    for (int x = 1; x < G; x++)
+      if (x == qh) { Mq = M[x]; Lq = L[x]; lq = lse[x]; }
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int sp = 0; sp < nparts; sp++) {
+      const float ms = __ldcg(src + sp * stride + G * kD + qh);
+      const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + sp * stride + qh * kD) + lane);
+      const float w = ms == -INFINITY ? 0.0f : fast_exp2(ms - Mq);
+      O.x += w * o4.x; O.y += w * o4.y; O.z += w * o4.z; O.w += w * o4.w;
+    }
+    const float inv = Lq > 0.0f ? 1.0f / Lq : 0.0f;
+    reinterpret_cast<float4*>(a.out + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qh) * kD)[lane] =
+        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    if (lane == 0) {
+      a.lse2[(size_t)unit * G + qh] = lq;
+      if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, slot)[3] += 1;
+    }
+  }
+  if (!a.update) return;
+#pragma unroll
+  for (int k = 0; k < kMergeK; k++) {
+    if (pid[k] < 0) continue;
+    const int x = k * 256 + threadIdx.x;
+    const int c = blockIdx.x * kMergeChunks + x / kChunk;
+    const bool hi = c < ch_hi;
+    const int sl = (hi ? c : c - ch_hi) * kChunk + x % kChunk;
+    const TierGeom& tg = hi ? pv.hi : pv.lo;
+    float pm = 0.0f;
+#pragma unroll
+    for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, fast_exp2(lgv[k][qh] - lse[qh]));
+    reinterpret_cast<float*>(pv.page(pid[k]) + tg.off[4])[sl - tg.div(sl) * tg.t] = old[k] + pm;
+  }
 }
 
 constexpr int kMaxAttnSmem = 220 * 1024;
@@ -769,6 +1130,59 @@ static int pages_per_chunk(int t) {
   return m;
 }
 
+// Launch the attention kernel of the pool's page geometry, then the merge
+// (and score update) kernel as its programmatic dependent, over the scratch
+// that `a` points to.
+static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int max_tokens, cudaStream_t st) {
+  const int n_units = sa.n * P.pv.hkv;
+  const bool paged = P.pv.hi.t % kChunk == 0 && P.pv.lo.t % kChunk == 0;
+  int smem;
+  if (paged) {
+    a.mseg = 0;
+    a.maxp = 1;
+    a.stage_bytes = std::max(P.pv.hi.off[5], P.pv.lo.off[5]);
+    smem = kAttnWarps * kPageStages * (a.stage_bytes + 8 + 32) + 4 * (n_units + 1);
+  } else {
+    a.mseg = (4 * std::max(P.pv.hi.t, P.pv.lo.t) + 15) & ~15;
+    a.maxp = std::max(pages_per_chunk(P.pv.hi.t), pages_per_chunk(P.pv.lo.t));
+    a.stage_bytes = kOffMeta + 2 * a.maxp * a.mseg;
+    smem = kAttnWarps * kStages * (a.stage_bytes + 8) + 4 * (n_units + 1);
+  }
+  if (smem > kMaxAttnSmem) return cudaErrorInvalidConfiguration;
+  a.paged = paged ? 1 : 0;
+  cudaError_t e;
+  if (paged)
+    k_attn_paged<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
+  else
+    k_attn_decode<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int call_chunks = (max_tokens + kChunk - 1) / kChunk + 1;   // chunks of the call's longest head
+  const dim3 g2(a.update ? (call_chunks + kMergeChunks - 1) / kMergeChunks : 1, (unsigned)n_units);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = g2;
+  lc.blockDim = dim3(256);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  switch (P.pv.G) {
+    case 1: e = cudaLaunchKernelEx(&lc, k_attn_merge<1>, P.pv, a, sa); break;
+    case 2: e = cudaLaunchKernelEx(&lc, k_attn_merge<2>, P.pv, a, sa); break;
+    case 3: e = cudaLaunchKernelEx(&lc, k_attn_merge<3>, P.pv, a, sa); break;
+    case 4: e = cudaLaunchKernelEx(&lc, k_attn_merge<4>, P.pv, a, sa); break;
+    case 5: e = cudaLaunchKernelEx(&lc, k_attn_merge<5>, P.pv, a, sa); break;
+    case 6: e = cudaLaunchKernelEx(&lc, k_attn_merge<6>, P.pv, a, sa); break;
+    case 7: e = cudaLaunchKernelEx(&lc, k_attn_merge<7>, P.pv, a, sa); break;
+    default: e = cudaLaunchKernelEx(&lc, k_attn_merge<8>, P.pv, a, sa); break;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tokens, const __half* q,
                              float* out, int update_scores, cudaStream_t st) {
   AttnArgs a;
@@ -782,40 +1196,13 @@ cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tok
   a.max_chunks = P.sc.max_chunks;
   a.update = update_scores;
   a.layer = layer;
-  const int n_units = sa.n * P.pv.hkv;
-  const bool paged = P.pv.hi.t % kChunk == 0 && P.pv.lo.t % kChunk == 0;
-  int smem;
-  if (paged) {
-    a.mseg = 0;
-    a.maxp = 1;
-    a.stage_bytes = std::max(P.pv.hi.off[4], P.pv.lo.off[4]);
-    smem = kAttnWarps * kPageStages * (a.stage_bytes + 8) + 4 * (n_units + 1);
-  } else {
-    a.mseg = (4 * std::max(P.pv.hi.t, P.pv.lo.t) + 15) & ~15;
-    a.maxp = std::max(pages_per_chunk(P.pv.hi.t), pages_per_chunk(P.pv.lo.t));
-    a.stage_bytes = kOffMeta + 2 * a.maxp * a.mseg;
-    smem = kAttnWarps * kStages * (a.stage_bytes + 8) + 4 * (n_units + 1);
-  }
-  if (smem > kMaxAttnSmem) return cudaErrorInvalidConfiguration;
-  if (paged)
-    k_attn_paged<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
-  else
-    k_attn_decode<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (update_scores) {
-    const int max_chunks_call = (max_tokens + kChunk - 1) / kChunk + 1;
-    const dim3 g2((max_chunks_call + 15) / 16, (unsigned)n_units);
-    k_attn_scores<<<g2, 256, 0, st>>>(P.pv, a, sa);
-    e = cudaGetLastError();
-  }
-  return e;
+  return launch_kernels(P, a, sa, max_tokens, st);
 }
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant (dkv_decode_attention_static). The same kernels
-// work in one fixed device array instead of the pool's scratch: the merge
-// counters, the per-head lse2, the per-warp partials and, with score updates,
+// work in one fixed device array instead of the pool's scratch: the partial
+// counts, the per-head lse2, the per-warp partials and, with score updates,
 // the per-chunk logits. The array is part of this library's device image; the
 // CUDA driver reserves it when the module is loaded, so no call here
 // allocates. Every call shares it and it keeps the last call's contents.
@@ -829,7 +1216,7 @@ static void* g_static_base[kMaxStaticDevices];
 namespace {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Regions of the array for one call, each 256-byte aligned: merge counters
+// Regions of the array for one call, each 256-byte aligned: partial counts
 // at 0, then lse2, partials, logits. Strides are sized for the call's
 // longest request, not the pool's maximum.
 struct StaticLayout {
@@ -847,7 +1234,7 @@ StaticLayout static_layout(int n_units, int G, int max_tokens, int update_scores
   L.part = off;
   off = round256(off + (size_t)n_units * L.max_parts * part_stride(G) * sizeof(float));
   L.logit = off;
-  if (update_scores) off += (size_t)n_units * L.max_chunks * kChunk * 8 * sizeof(float);
+  if (update_scores) off += (size_t)n_units * L.max_chunks * kLogitRow * sizeof(float);
   L.total = off;
   return L;
 }
@@ -890,41 +1277,22 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
   a.max_chunks = L.max_chunks;
   a.update = update_scores;
   a.layer = layer;
-  // The merge counters must start at zero. A finished call leaves them zero,
-  // but one cut short (a wait that timed out) leaves some set.
-  e = cudaMemsetAsync(a.done, 0, (size_t)n_units * sizeof(int), st);
-  if (e != cudaSuccess) return e;
-  const bool paged = P.pv.hi.t % kChunk == 0 && P.pv.lo.t % kChunk == 0;
-  int smem;
-  if (paged) {
-    a.mseg = 0;
-    a.maxp = 1;
-    a.stage_bytes = std::max(P.pv.hi.off[4], P.pv.lo.off[4]);
-    smem = kAttnWarps * kPageStages * (a.stage_bytes + 8) + 4 * (n_units + 1);
-  } else {
-    a.mseg = (4 * std::max(P.pv.hi.t, P.pv.lo.t) + 15) & ~15;
-    a.maxp = std::max(pages_per_chunk(P.pv.hi.t), pages_per_chunk(P.pv.lo.t));
-    a.stage_bytes = kOffMeta + 2 * a.maxp * a.mseg;
-    smem = kAttnWarps * kStages * (a.stage_bytes + 8) + 4 * (n_units + 1);
-  }
-  if (smem > kMaxAttnSmem) return cudaErrorInvalidConfiguration;
-  if (paged)
-    k_attn_paged<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
-  else
-    k_attn_decode<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (update_scores) {
-    const dim3 g2((L.max_chunks + 15) / 16, (unsigned)n_units);
-    k_attn_scores<<<g2, 256, 0, st>>>(P.pv, a, sa);
-    e = cudaGetLastError();
-  }
-  return e;
+  // Nothing in the array needs clearing: every value a call reads from it
+  // (partial counts, partials, logits) is written earlier in the same call.
+  // The grid barrier of the cooperative path is the pool's own.
+  return launch_kernels(P, a, sa, max_tokens, st);
 }
 
 cudaError_t configure_attention() {
   cudaError_t e = cudaFuncSetAttribute(k_attn_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
   if (e != cudaSuccess) return e;
+  const void* merges[8] = {(const void*)k_attn_merge<1>, (const void*)k_attn_merge<2>, (const void*)k_attn_merge<3>,
+                           (const void*)k_attn_merge<4>, (const void*)k_attn_merge<5>, (const void*)k_attn_merge<6>,
+                           (const void*)k_attn_merge<7>, (const void*)k_attn_merge<8>};
+  for (const void* f : merges) {
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
+    if (e != cudaSuccess) return e;
+  }
   return cudaFuncSetAttribute(k_attn_paged, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
 }
 

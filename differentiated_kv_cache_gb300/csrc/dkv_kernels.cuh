@@ -11,6 +11,10 @@ namespace dkv {
 constexpr int kKeyBlock = 128;     // prompt tokens per scoring / classification block
 constexpr int kChunk = 16;         // decode-attention tokens per mma chunk
 constexpr int kAttnWarps = 4;      // warps per decode-attention CTA
+// Decode-attention scratch row per 16-slot chunk (floats): the log2-domain
+// logits [query < G][16 slots], then (paged path) the scores before the
+// update [16 slots] at row G and the chunk's page ID at row G + 1.
+constexpr int kLogitRow = (kMaxG + 2) * kChunk;
 
 // One slot write of a generation-phase step.
 enum MoveSrc { kSrcNew = 0, kSrcDemote = 1 };
@@ -42,9 +46,9 @@ struct Scratch {
   DecodePlan* dplan;    // [units]
   // decode attention
   float* apart;         // [units][max_splits][G*(128+2)]
-  float* alogit;        // [units][max_chunks][16][8]
+  float* alogit;        // [units][max_chunks][kLogitRow]: per chunk logits, old scores, page ID
   float* alse;          // [units][G]
-  int* adone;           // [units] split counters of the attention merge
+  int* adone;           // [units] number of attention partials of each head
   int nkb_cap, grant_cap, max_splits, max_chunks;
 };
 

@@ -191,7 +191,7 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&s.grant_ids, units * s.grant_cap);
   A(&s.dplan, units);
   A(&s.apart, units * s.max_splits * (G * kD + 2 * kMaxG));
-  A(&s.alogit, units * s.max_chunks * kChunk * 8);
+  A(&s.alogit, units * s.max_chunks * kLogitRow);
   A(&s.alse, units * G);
   A(&s.adone, units);
   if (e == cudaSuccess) e = cudaMemset(s.adone, 0, units * sizeof(int));
@@ -428,9 +428,6 @@ int dkv_pool_clear_error(dkv_pool* pool) {
   c.error = 0;
   c.error_info = -1;
   if (cudaMemcpy(P.pv.ctl, &c, sizeof(Ctl), cudaMemcpyHostToDevice) != cudaSuccess) return DKV_ERR_CUDA;
-  // a call cut short by an error can leave attention merge counters behind
-  if (cudaMemset(P.sc.adone, 0, (size_t)P.cfg.max_requests * P.cfg.n_kv_heads * sizeof(int)) != cudaSuccess)
-    return DKV_ERR_CUDA;
   std::vector<int> rq((size_t)P.cfg.n_layers * P.cfg.max_requests * 4);
   if (cudaMemcpy(rq.data(), P.pv.req, rq.size() * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return DKV_ERR_CUDA;

@@ -258,14 +258,15 @@ int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
  * Size limit: with U = n_req * n_kv_heads, C = ceil(max_n / 16) + 1 (max_n =
  * longest stored sequence among the call's requests) and r(x) = x rounded up
  * to 256, the call needs r(4U) + r(4UG) + r(4U(C/8 + 2)(128G + 16)) bytes,
- * plus 512UC if update_scores != 0. A larger call returns DKV_ERR_SCRATCH
+ * plus 640UC if update_scores != 0. A larger call returns DKV_ERR_SCRATCH
  * and queues nothing.
  *
  * Set-up: the first call on a device looks up the array's address on that
  * device (cudaGetSymbolAddress, with the pool's device current); make that
  * first call before any stream capture. Every call on a device shares the
- * array and it keeps the last call's contents; the call clears the part that
- * must start at zero (its merge counters, by cudaMemsetAsync on `stream`).
+ * array and it keeps the last call's contents; nothing in it has to start at
+ * zero, because every value a call reads from the array (partial counts,
+ * partials, logits) is written earlier in the same call.
  * Calls that overlap on the GPU (on different streams, or from different
  * pools of one device) race on the array and give wrong results: order them
  * on one stream or synchronise between them.
