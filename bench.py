@@ -294,9 +294,9 @@ def run_dkv(args, world, rank, local):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": int(per_launch_bytes), "traffic": args.traffic},
-        # per step: prompt compact_step 7 kernels; per decode step 3 (compaction)
+        # per step: prompt compact_step 9 kernels; per decode step 3 (compaction)
         # + 2 (attention, merge); one free_request kernel per request
-        "gpu_launches": args.steps * (7 + T * 5 + R),
+        "gpu_launches": args.steps * (9 + T * 5 + R),
     }
     result["clocks"] = clk.summary()
     if not args.no_e2e:

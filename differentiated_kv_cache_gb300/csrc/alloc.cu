@@ -80,94 +80,113 @@ __device__ __forceinline__ void latch_error(PoolView& pv, int code, int info) {
 // ceil(N0/T_hi)+slack pages taken at the list start by one prefix sum; hi
 // pages from the left of the grant, lo pages from the right; the unused
 // middle pages appended at the list end by a second prefix sum; table rows,
-// counters and request state written. All checks precede every write.
+// counters and request state written. Three launches over all heads: (1) per
+// head tier counts, key-block bases and page needs; (2) grant offsets (every
+// CTA scans the per-head grants of the call), the list check and the reads
+// of the granted page IDs; (3) reclaim offsets, reclaim writes, table rows
+// and counters. Every check precedes every write of the pool's state: (1)
+// and (2) write only scratch, and a failed check latches the sticky status
+// that turns the later launches into no-ops. All grant reads (2) complete
+// before any reclaim write (3), which may reuse list entries once the list
+// wraps.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kCoordThreads) k_prompt_plan(PoolView pv, int layer, Scratch sc) {
+constexpr int kPlanWarps = 8;   // heads per CTA in the prompt coordination
+
+__global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_heads(PoolView pv, Scratch sc) {
   if (pv.noop()) return;
-  extern __shared__ int s_dyn[];
-  __shared__ int s_warp[32];
-  __shared__ int s_err, s_info;
   const CallArgs* ca = pv.call;
   const int n_units = ca->n_req * pv.hkv;
-  int* s_g = s_dyn;              // grant pages per unit -> exclusive offsets
-  int* s_r = s_dyn + n_units;    // reclaimed pages per unit -> exclusive offsets
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
-  __syncthreads();
-  // planning summary per head (warp per head): tier counts, block bases, page needs
-  for (int u = warp; u < n_units; u += nw) {
-    const int n0 = ca->lens[u / pv.hkv];
-    const int nkb = (n0 + kKeyBlock - 1) / kKeyBlock;
-    int a = 0, b = 0;
-    for (int k0 = 0; k0 < nkb; k0 += 32) {
-      const int kb = k0 + lane;
-      const int2 c = kb < nkb ? sc.bcnt[(size_t)u * sc.nkb_cap + kb] : make_int2(0, 0);
-      int x = c.x, y = c.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x * kPlanWarps + warp;
+  if (u >= n_units) return;
+  const int n0 = ca->lens[u / pv.hkv];
+  const int nkb = (n0 + kKeyBlock - 1) / kKeyBlock;
+  int a = 0, b = 0;
+  for (int k0 = 0; k0 < nkb; k0 += 32) {
+    const int kb = k0 + lane;
+    const int2 c = kb < nkb ? sc.bcnt[(size_t)u * sc.nkb_cap + kb] : make_int2(0, 0);
+    int x = c.x, y = c.y;
 #pragma unroll
-      for (int s = 1; s < 32; s <<= 1) {
-        const int xo = __shfl_up_sync(0xffffffffu, x, s), yo = __shfl_up_sync(0xffffffffu, y, s);
-        if (lane >= s) { x += xo; y += yo; }
-      }
-      if (kb < nkb) sc.bbase[(size_t)u * sc.nkb_cap + kb] = make_int2(a + x - c.x, b + y - c.y);
-      a += __shfl_sync(0xffffffffu, x, 31);
-      b += __shfl_sync(0xffffffffu, y, 31);
+    for (int s = 1; s < 32; s <<= 1) {
+      const int xo = __shfl_up_sync(0xffffffffu, x, s), yo = __shfl_up_sync(0xffffffffu, y, s);
+      if (lane >= s) { x += xo; y += yo; }
     }
-    if (lane == 0) {
-      const int gh = (n0 + pv.hi.t - 1) / pv.hi.t + pv.slack;
-      const int nhp = (a + pv.hi.t - 1) / pv.hi.t, nlp = (b + pv.lo.t - 1) / pv.lo.t;
-      if (nhp + nlp > gh || nhp + nlp > pv.L) {
-        if (atomicCAS(&s_err, 0, DKV_ERR_TABLE_FULL) == 0) s_info = u;
-      }
-      sc.unit_info[u] = make_int4(gh, a, b, 0);
-      s_g[u] = gh;
-      s_r[u] = max(0, gh - nhp - nlp);
-    }
+    if (kb < nkb) sc.bbase[(size_t)u * sc.nkb_cap + kb] = make_int2(a + x - c.x, b + y - c.y);
+    a += __shfl_sync(0xffffffffu, x, 31);
+    b += __shfl_sync(0xffffffffu, y, 31);
   }
+  if (lane == 0) {
+    const int gh = (n0 + pv.hi.t - 1) / pv.hi.t + pv.slack;
+    const int nhp = (a + pv.hi.t - 1) / pv.hi.t, nlp = (b + pv.lo.t - 1) / pv.lo.t;
+    if (nhp + nlp > gh || nhp + nlp > pv.L) latch_error(pv, DKV_ERR_TABLE_FULL, u);
+    sc.unit_info[u] = make_int4(gh, a, b, max(0, gh - nhp - nlp));
+  }
+}
+
+__global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_grant(PoolView pv, Scratch sc) {
+  if (pv.noop()) return;          // a head's pages do not fit its grant or row
+  extern __shared__ int s_g[];    // [unit] grant pages -> exclusive offsets
+  __shared__ int s_warp[32];
+  const CallArgs* ca = pv.call;
+  const int n_units = ca->n_req * pv.hkv;
+  for (int x = threadIdx.x; x < n_units; x += blockDim.x) s_g[x] = sc.unit_info[x].x;
   __syncthreads();
   const int tot_g = block_scan_array(s_g, n_units, s_warp);
-  const int tot_r = block_scan_array(s_r, n_units, s_warp);
   const unsigned long long start = pv.ctl->start, end = pv.ctl->end;
-  if (threadIdx.x == 0 && s_err == 0 && (unsigned long long)tot_g > end - start) s_err = DKV_ERR_NO_PAGES;
-  __syncthreads();
-  if (s_err != 0) {
-    if (threadIdx.x == 0) latch_error(pv, s_err, s_info);
+  if ((unsigned long long)tot_g > end - start) {   // every CTA sees the same
+    if (blockIdx.x == 0 && threadIdx.x == 0) latch_error(pv, DKV_ERR_NO_PAGES, -1);
     return;
   }
-  // coordination 1: the granted page IDs, read before any reclaim write
-  for (int u = warp; u < n_units; u += nw) {
-    const int gh = sc.unit_info[u].x;
-    int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
-    for (int x = lane; x < gh; x += 32) gid[x] = pv.list[(start + (unsigned long long)(s_g[u] + x)) % pv.n_pages];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    sc.pbase[0] = start;
+    sc.pbase[1] = end;
+    sc.pbase[2] = (unsigned long long)tot_g;
   }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x * kPlanWarps + warp;
+  if (u >= n_units) return;
+  const int gh = sc.unit_info[u].x;
+  int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
+  for (int x = lane; x < gh; x += 32) gid[x] = pv.list[(start + (unsigned long long)(s_g[u] + x)) % pv.n_pages];
+}
+
+__global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_commit(PoolView pv, int layer, Scratch sc) {
+  if (pv.noop()) return;
+  extern __shared__ int s_r[];    // [unit] reclaimed pages -> exclusive offsets
+  __shared__ int s_warp[32];
+  const CallArgs* ca = pv.call;
+  const int n_units = ca->n_req * pv.hkv;
+  for (int x = threadIdx.x; x < n_units; x += blockDim.x) s_r[x] = sc.unit_info[x].w;
   __syncthreads();
-  // coordination 2: reclaim the unused middle pages; table rows, counters, state
-  for (int u = warp; u < n_units; u += nw) {
-    const int i = u / pv.hkv, kvh = u % pv.hkv, slot = ca->slots[i];
-    const int4 ui = sc.unit_info[u];
-    const int gh = ui.x, nhp = (ui.y + pv.hi.t - 1) / pv.hi.t, nlp = (ui.z + pv.lo.t - 1) / pv.lo.t;
-    const int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
-    for (int x = nhp + lane; x < gh - nlp; x += 32)
-      pv.list[(end + (unsigned long long)(s_r[u] + x - nhp)) % pv.n_pages] = gid[x];
-    int* row = pv.row(layer, slot, kvh);
-    for (int e = lane; e < pv.L; e += 32) {
-      int v = -1;
-      if (e < nhp) v = gid[e];
-      else if (e >= pv.L - nlp) v = gid[gh - 1 - (pv.L - 1 - e)];
-      row[e] = v;
-    }
-    if (lane == 0) {
-      int* cn = pv.cnt(layer, slot, kvh);
-      cn[0] = ui.y; cn[1] = ui.z; cn[2] = nhp; cn[3] = nlp;
-      if (kvh == 0) {
-        int* rq = pv.rq(layer, slot);
-        rq[0] = 1; rq[1] = ca->lens[i]; rq[2] = ca->lens[i]; rq[3] = 0;
-      }
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    pv.ctl->start = start + (unsigned long long)tot_g;
+  const int tot_r = block_scan_array(s_r, n_units, s_warp);
+  const unsigned long long start = sc.pbase[0], end = sc.pbase[1], tot_g = sc.pbase[2];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    pv.ctl->start = start + tot_g;
     pv.ctl->end = end + (unsigned long long)tot_r;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x * kPlanWarps + warp;
+  if (u >= n_units) return;
+  const int i = u / pv.hkv, kvh = u % pv.hkv, slot = ca->slots[i];
+  const int4 ui = sc.unit_info[u];
+  const int gh = ui.x, nhp = (ui.y + pv.hi.t - 1) / pv.hi.t, nlp = (ui.z + pv.lo.t - 1) / pv.lo.t;
+  const int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
+  for (int x = nhp + lane; x < gh - nlp; x += 32)
+    pv.list[(end + (unsigned long long)(s_r[u] + x - nhp)) % pv.n_pages] = gid[x];
+  int* row = pv.row(layer, slot, kvh);
+  for (int e = lane; e < pv.L; e += 32) {
+    int v = -1;
+    if (e < nhp) v = gid[e];
+    else if (e >= pv.L - nlp) v = gid[gh - 1 - (pv.L - 1 - e)];
+    row[e] = v;
+  }
+  if (lane == 0) {
+    int* cn = pv.cnt(layer, slot, kvh);
+    cn[0] = ui.y; cn[1] = ui.z; cn[2] = nhp; cn[3] = nlp;
+    if (kvh == 0) {
+      int* rq = pv.rq(layer, slot);
+      rq[0] = 1; rq[1] = ca->lens[i]; rq[2] = ca->lens[i]; rq[3] = 0;
+    }
   }
 }
 
@@ -289,14 +308,20 @@ cudaError_t launch_setup(const Pool& P, const CallArgs& args, cudaStream_t st) {
 }
 
 cudaError_t launch_prompt_plan(Pool& P, int layer, int n_req, cudaStream_t st) {
-  const int smem = 2 * n_req * P.pv.hkv * (int)sizeof(int);
-  k_prompt_plan<<<1, kCoordThreads, smem, st>>>(P.pv, layer, P.sc);
+  const int n_units = n_req * P.pv.hkv;
+  const int smem = n_units * (int)sizeof(int);
+  const int grid = (n_units + kPlanWarps - 1) / kPlanWarps;
+  k_prompt_plan_heads<<<grid, 32 * kPlanWarps, 0, st>>>(P.pv, P.sc);
+  k_prompt_plan_grant<<<grid, 32 * kPlanWarps, smem, st>>>(P.pv, P.sc);
+  k_prompt_plan_commit<<<grid, 32 * kPlanWarps, smem, st>>>(P.pv, layer, P.sc);
   return cudaGetLastError();
 }
 
 cudaError_t configure_alloc() {
   // coordination kernels keep two ints per head in shared memory
-  cudaError_t e = cudaFuncSetAttribute(k_prompt_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaError_t e = cudaFuncSetAttribute(k_prompt_plan_grant, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_prompt_plan_commit, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_free_request, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }

@@ -42,6 +42,7 @@ struct Scratch {
   int* rank2pos;        // [units][2][max_seq]
   int4* unit_info;      // [units]: grant pages, hi count, lo count
   int* grant_ids;       // [units][grant_cap]
+  unsigned long long* pbase;   // prompt coordination: list start, end and grant total at the call
   // decode compaction
   DecodePlan* dplan;    // [units]
   // decode attention

@@ -189,6 +189,7 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&s.rank2pos, units * 2 * cfg->max_seq_len);
   A(&s.unit_info, units);
   A(&s.grant_ids, units * s.grant_cap);
+  A(&s.pbase, 4);
   A(&s.dplan, units);
   A(&s.apart, units * s.max_splits * (G * kD + 2 * kMaxG));
   A(&s.alogit, units * s.max_chunks * kLogitRow);
