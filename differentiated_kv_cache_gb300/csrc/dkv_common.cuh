@@ -145,6 +145,39 @@ __device__ __forceinline__ uint32_t qcode(float x, const QParams& q, int bits) {
   return (uint32_t)r;
 }
 
+// Packed fp32 pairs (two IEEE fp32 operations per instruction, each correctly
+// rounded like its scalar form).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// clamp(rint_even(t), 0, 255) in one conversion
+__device__ __forceinline__ uint32_t rint_sat_u8(float t) {
+  uint32_t r;
+  asm("cvt.rni.sat.u8.f32 %0, %1;\n" : "=r"(r) : "f"(t));
+  return r & 0xFFu;
+}
+// codes of the pair (x0, x1) under q, with the same arithmetic as qcode
+__device__ __forceinline__ void qcode2(float x0, float x1, const QParams& q, int bits, uint32_t& c0, uint32_t& c1) {
+  if (q.zero_scale) {
+    c0 = c1 = 0u;
+    return;
+  }
+  const uint64_t t = mul_f32x2(sub_f32x2(f32x2(x0, x1), f32x2(q.z, q.z)), f32x2(q.inv, q.inv));
+  const uint32_t L = (1u << bits) - 1u;
+  c0 = min(rint_sat_u8(__uint_as_float((uint32_t)t)), L);
+  c1 = min(rint_sat_u8(__uint_as_float((uint32_t)(t >> 32))), L);
+}
+
 __device__ __forceinline__ float dequant(uint16_t sh, uint16_t zh, uint32_t code) {
   return __fmaf_rn(__half2float(__ushort_as_half(sh)), (float)code, __half2float(__ushort_as_half(zh)));
 }

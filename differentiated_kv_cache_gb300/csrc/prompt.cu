@@ -356,11 +356,16 @@ __global__ void __launch_bounds__(128) k_prompt_scatter(PoolView pv, const uint1
 }
 
 // ---------------------------------------------------------------------------
-// a4: quantize + pack. Each warp handles 4 consecutive ranks of one (head,
-// tier): 8 lanes per token, 16 features per lane. A warp's 4 tokens fill two
+// a4: quantize + pack. A warp handles groups of 4 consecutive ranks of one
+// (head, tier): 8 lanes per token, 16 features per lane. A group fills two
 // whole value pair-rows (hi) or one value quad-row (lo); the value words are
-// assembled in shared memory and written as full 128-byte rows.
+// assembled in shared memory and written as full 128-byte rows. Each warp
+// takes kPackGroups groups in turn and keeps the loads ahead of the math: the
+// positions of the group after next and the K/V rows of the next group are
+// in flight while a group is quantized and stored.
 // ---------------------------------------------------------------------------
+constexpr int kPackGroups = 4;
+
 __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* __restrict__ k,
                                                       const __half* __restrict__ v,
                                                       const float* __restrict__ score,
@@ -368,113 +373,146 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
                                                       const int4* __restrict__ unit_info,
                                                       const int* __restrict__ grant_ids, int grant_cap) {
   if (pv.noop()) return;
-  __shared__ uint8_t s_vc[8][4][kD];      // [warp][token][feature] value codes
+  __shared__ uint32_t s_vw[8][4][32];     // [warp][token][value word] code bits of the token
   const int unit = blockIdx.y, tier = blockIdx.z ? kTierHi : kTierLo;
   const int i = unit / pv.hkv, kvh = unit % pv.hkv;
   const int4 ui = unit_info[unit];        // grant pages, hi count, lo count, -
   const int count = tier == kTierHi ? ui.y : ui.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = (blockIdx.x * 8 + warp) * 4;
-  if (r0 >= count) return;
+  // group x of this warp starts at rank base + 32 x
+  const int base = (blockIdx.x * kPackGroups * 8 + warp) * 4;
+  if (base >= count) return;
   const TierGeom& tg = tier == kTierHi ? pv.hi : pv.lo;
   const int kbits = tier == kTierHi ? 8 : 4, vbits = tier == kTierHi ? 4 : 2;
   const int e = lane >> 3, q = lane & 7;  // token e of the 4, features 16q..16q+15
-  const int r = r0 + e;
-  const bool valid = r < count;
   const CallArgs* ca = pv.call;
-  uint8_t vcode[16];
-  // every lane takes part in the group reductions; invalid lanes use zeros
-  int j = 0;
-  size_t tok = 0;
-  uint4 k0 = make_uint4(0, 0, 0, 0), k1 = k0, v0 = k0, v1 = k0;
-  if (valid) {
-    j = rank2pos[((size_t)unit * 2 + (tier == kTierHi ? 1 : 0)) * pv.max_seq + r];
-    tok = (size_t)(ca->tok0[i] + j) * pv.hkv + kvh;
-    const uint4* kp = reinterpret_cast<const uint4*>(k + tok * kD + q * 16);
-    const uint4* vp = reinterpret_cast<const uint4*>(v + tok * kD + q * 16);
-    k0 = kp[0]; k1 = kp[1]; v0 = vp[0]; v1 = vp[1];
-  }
-  float kx[16], vx[16];
-  {
-    const __half* kh0 = reinterpret_cast<const __half*>(&k0);
-    const __half* kh1 = reinterpret_cast<const __half*>(&k1);
-    const __half* vh0 = reinterpret_cast<const __half*>(&v0);
-    const __half* vh1 = reinterpret_cast<const __half*>(&v1);
-#pragma unroll
-    for (int x = 0; x < 8; x++) {
-      kx[x] = __half2float(kh0[x]); kx[8 + x] = __half2float(kh1[x]);
-      vx[x] = __half2float(vh0[x]); vx[8 + x] = __half2float(vh1[x]);
-    }
-  }
-  float kmn = kx[0], kmx = kx[0], vmn = vx[0], vmx = vx[0];
-#pragma unroll
-  for (int x = 1; x < 16; x++) {
-    kmn = fminf(kmn, kx[x]); kmx = fmaxf(kmx, kx[x]);
-    vmn = fminf(vmn, vx[x]); vmx = fmaxf(vmx, vx[x]);
-  }
-#pragma unroll
-  for (int s = 1; s <= 4; s <<= 1) {
-    kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, s, 8));
-    kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, s, 8));
-    vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, s, 8));
-    vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, s, 8));
-  }
-  const QParams kq = qparams(kmn, kmx, kbits), vq = qparams(vmn, vmx, vbits);
-#pragma unroll
-  for (int x = 0; x < 16; x++) vcode[x] = valid ? (uint8_t)qcode(vx[x], vq, vbits) : (uint8_t)0;
-  if (valid) {
-    // page and slot of rank r: hi from the left of the grant, lo from the right
-    const int gcnt = ui.x;
-    const int pidx = tier == kTierHi ? r / tg.t : gcnt - 1 - r / tg.t;
-    const int slot = r % tg.t;
-    uint8_t* page = pv.page(grant_ids[(size_t)unit * grant_cap + pidx]);
-    uint8_t* krow = page + tg.off[0] + slot * tg.kbytes;
-    if (kbits == 8) {
-      uint32_t w[4];
-#pragma unroll
-      for (int x = 0; x < 4; x++)
-        w[x] = qcode(kx[4 * x], kq, 8) | (qcode(kx[4 * x + 1], kq, 8) << 8) |
-               (qcode(kx[4 * x + 2], kq, 8) << 16) | (qcode(kx[4 * x + 3], kq, 8) << 24);
-      *reinterpret_cast<uint4*>(krow + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else {
-      uint32_t w[2];
-#pragma unroll
-      for (int x = 0; x < 2; x++) {
-        uint32_t acc = 0;
-#pragma unroll
-        for (int y = 0; y < 8; y++) acc |= qcode(kx[8 * x + y], kq, 4) << (4 * y);
-        w[x] = acc;
-      }
-      *reinterpret_cast<uint2*>(krow + 8 * q) = make_uint2(w[0], w[1]);
-    }
-    if (q == 0) {
-      *reinterpret_cast<uint32_t*>(page + tg.off[2] + 4 * slot) = (uint32_t)kq.sh | ((uint32_t)kq.zh << 16);
-      *reinterpret_cast<uint32_t*>(page + tg.off[3] + 4 * slot) = (uint32_t)vq.sh | ((uint32_t)vq.zh << 16);
-      *reinterpret_cast<float*>(page + tg.off[4] + 4 * slot) = score[tok];
-      *reinterpret_cast<int*>(page + tg.off[5] + 4 * slot) = j;
-    }
-  }
-#pragma unroll
-  for (int x = 0; x < 16; x++) s_vc[warp][e][q * 16 + x] = vcode[x];
-  __syncwarp();
-  // value rows: hi = 2 pair-rows (tokens 0,1 and 2,3), lo = 1 quad-row
-  const int gsz = 8 / vbits;
-  const int nrows = 4 / gsz;
+  const int* r2p = rank2pos + ((size_t)unit * 2 + (tier == kTierHi ? 1 : 0)) * pv.max_seq;
+  const size_t tok_base = (size_t)ca->tok0[i];
   const int gcnt = ui.x;
-  for (int row = 0; row < nrows; row++) {
-    const int rfirst = r0 + row * gsz;
-    if (rfirst >= count) break;
-    const int pidx = tier == kTierHi ? rfirst / tg.t : gcnt - 1 - rfirst / tg.t;
-    const int slot0 = rfirst % tg.t;
-    uint8_t* page = pv.page(grant_ids[(size_t)unit * grant_cap + pidx]);
-    uint32_t word = 0;
-#pragma unroll
-    for (int x = 0; x < 4; x++) {
-      const int f = 4 * lane + x;
-      for (int ee = 0; ee < gsz; ee++)
-        word |= (uint32_t)s_vc[warp][row * gsz + ee][f] << vbit(vbits, f, ee);
+  auto pos_of = [&](int x) { const int r = base + 32 * x + e; return r < count ? __ldg(r2p + r) : -1; };
+  auto load_kv = [&](int j, uint4 (&kv)[4]) {
+    if (j >= 0) {
+      const size_t tok = (tok_base + j) * pv.hkv + kvh;
+      const uint4* kp = reinterpret_cast<const uint4*>(k + tok * kD + q * 16);
+      const uint4* vp = reinterpret_cast<const uint4*>(v + tok * kD + q * 16);
+      kv[0] = __ldg(kp); kv[1] = __ldg(kp + 1); kv[2] = __ldg(vp); kv[3] = __ldg(vp + 1);
+    } else {
+      kv[0] = kv[1] = kv[2] = kv[3] = make_uint4(0, 0, 0, 0);
     }
-    *reinterpret_cast<uint32_t*>(page + tg.off[1] + (slot0 / gsz) * 128 + 4 * lane) = word;
+  };
+  int j_cur = pos_of(0), j_next = pos_of(1);
+  uint4 kv_cur[4], kv_next[4];
+  load_kv(j_cur, kv_cur);
+  for (int x = 0; x < kPackGroups; x++) {
+    const int r0 = base + 32 * x;
+    if (r0 >= count) break;
+    int j_after = -1;
+    if (x + 1 < kPackGroups) load_kv(j_next, kv_next);
+    if (x + 2 < kPackGroups) j_after = pos_of(x + 2);
+    const int r = r0 + e;
+    const bool valid = r < count;
+    const int j = j_cur;
+    float kx[16], vx[16];
+    float kmn, kmx, vmn, vmx;
+    {
+      const __half2* kh = reinterpret_cast<const __half2*>(&kv_cur[0]);   // 8 pairs: kv_cur[0..1]
+      const __half2* vh = reinterpret_cast<const __half2*>(&kv_cur[2]);
+      __half2 kmn2 = kh[0], kmx2 = kh[0], vmn2 = vh[0], vmx2 = vh[0];
+#pragma unroll
+      for (int y = 1; y < 8; y++) {   // min / max of fp16 values are exact
+        kmn2 = __hmin2(kmn2, kh[y]); kmx2 = __hmax2(kmx2, kh[y]);
+        vmn2 = __hmin2(vmn2, vh[y]); vmx2 = __hmax2(vmx2, vh[y]);
+      }
+      kmn = fminf(__low2float(kmn2), __high2float(kmn2));
+      kmx = fmaxf(__low2float(kmx2), __high2float(kmx2));
+      vmn = fminf(__low2float(vmn2), __high2float(vmn2));
+      vmx = fmaxf(__low2float(vmx2), __high2float(vmx2));
+#pragma unroll
+      for (int y = 0; y < 8; y++) {
+        const float2 kf = __half22float2(kh[y]), vf = __half22float2(vh[y]);
+        kx[2 * y] = kf.x; kx[2 * y + 1] = kf.y;
+        vx[2 * y] = vf.x; vx[2 * y + 1] = vf.y;
+      }
+    }
+    // every lane takes part in the group reductions; invalid lanes hold zeros
+#pragma unroll
+    for (int sh = 1; sh <= 4; sh <<= 1) {
+      kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, sh, 8));
+      kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, sh, 8));
+      vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, sh, 8));
+      vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, sh, 8));
+    }
+    const QParams kq = qparams(kmn, kmx, kbits), vq = qparams(vmn, vmx, vbits);
+    // the token's bits of value words 4q .. 4q+3 (feature 4w+i, slot e of the row)
+    const int gsz = 8 / vbits;
+    const int eb = vbits == 4 ? 16 * (e % 2) : 16 * (e & 1) + 2 * (e >> 1);
+    uint32_t vw[4];
+#pragma unroll
+    for (int w = 0; w < 4; w++) {
+      uint32_t c0, c1, c2, c3;
+      qcode2(vx[4 * w], vx[4 * w + 1], vq, vbits, c0, c1);
+      qcode2(vx[4 * w + 2], vx[4 * w + 3], vq, vbits, c2, c3);
+      vw[w] = valid ? (c0 | (c1 << 4) | (c2 << 8) | (c3 << 12)) << eb : 0u;
+    }
+    __syncwarp();                        // the previous group's value rows are written
+#pragma unroll
+    for (int w = 0; w < 4; w++) s_vw[warp][e][4 * q + w] = vw[w];
+    if (valid) {
+      // page and slot of rank r: hi from the left of the grant, lo from the right
+      const int pidx = tier == kTierHi ? r / tg.t : gcnt - 1 - r / tg.t;
+      const int slot = r % tg.t;
+      uint8_t* page = pv.page(grant_ids[(size_t)unit * grant_cap + pidx]);
+      uint8_t* krow = page + tg.off[0] + slot * tg.kbytes;
+      if (kbits == 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int y = 0; y < 4; y++) {
+          uint32_t c0, c1, c2, c3;
+          qcode2(kx[4 * y], kx[4 * y + 1], kq, 8, c0, c1);
+          qcode2(kx[4 * y + 2], kx[4 * y + 3], kq, 8, c2, c3);
+          w[y] = __byte_perm(c0 | (c2 << 16), c1 | (c3 << 16), 0x6240);
+        }
+        *reinterpret_cast<uint4*>(krow + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        uint32_t w[2];
+#pragma unroll
+        for (int y = 0; y < 2; y++) {
+          uint32_t acc = 0;
+#pragma unroll
+          for (int z = 0; z < 8; z += 2) {
+            uint32_t c0, c1;
+            qcode2(kx[8 * y + z], kx[8 * y + z + 1], kq, 4, c0, c1);
+            acc |= (c0 | (c1 << 4)) << (4 * z);
+          }
+          w[y] = acc;
+        }
+        *reinterpret_cast<uint2*>(krow + 8 * q) = make_uint2(w[0], w[1]);
+      }
+      if (q == 0) {
+        const size_t tok = (tok_base + j) * pv.hkv + kvh;
+        *reinterpret_cast<uint32_t*>(page + tg.off[2] + 4 * slot) = (uint32_t)kq.sh | ((uint32_t)kq.zh << 16);
+        *reinterpret_cast<uint32_t*>(page + tg.off[3] + 4 * slot) = (uint32_t)vq.sh | ((uint32_t)vq.zh << 16);
+        *reinterpret_cast<float*>(page + tg.off[4] + 4 * slot) = score[tok];
+        *reinterpret_cast<int*>(page + tg.off[5] + 4 * slot) = j;
+      }
+    }
+    __syncwarp();
+    // value rows: hi = 2 pair-rows (tokens 0,1 and 2,3), lo = 1 quad-row
+    const int nrows = 4 / gsz;
+    for (int row = 0; row < nrows; row++) {
+      const int rfirst = r0 + row * gsz;
+      if (rfirst >= count) break;
+      const int pidx = tier == kTierHi ? rfirst / tg.t : gcnt - 1 - rfirst / tg.t;
+      const int slot0 = rfirst % tg.t;
+      uint8_t* page = pv.page(grant_ids[(size_t)unit * grant_cap + pidx]);
+      uint32_t word = 0;
+      for (int ee = 0; ee < gsz; ee++) word |= s_vw[warp][row * gsz + ee][lane];
+      *reinterpret_cast<uint32_t*>(page + tg.off[1] + (slot0 / gsz) * 128 + 4 * lane) = word;
+    }
+    j_cur = j_next;
+    j_next = j_after;
+#pragma unroll
+    for (int y = 0; y < 4; y++) kv_cur[y] = kv_next[y];
   }
 }
 
@@ -553,7 +591,7 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, const __ha
   if ((e = launch_prompt_plan(P, layer, n_req, st)) != cudaSuccess) return e;
   k_prompt_scatter<<<grid, 128, 0, st>>>(P.pv, s.tokinfo, s.bbase, s.rank2pos, s.nkb_cap);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const dim3 gpack((max_len + 31) / 32, n_req * P.pv.hkv, 2);
+  const dim3 gpack((max_len + 32 * kPackGroups - 1) / (32 * kPackGroups), n_req * P.pv.hkv, 2);
   k_prompt_pack<<<gpack, 256, 0, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info, s.grant_ids, s.grant_cap);
   return cudaGetLastError();
 }
