@@ -272,8 +272,10 @@ def run_dkv(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
         "data": "synthetic (seeded numpy; model-shaped K/V/Q, no weights or datasets)",
         "config": {
-            "workload": f"{w.name}: Llama-3-8B-shaped layer, {R} requests x {lens[0]}-token prompts, "
-                        f"{Hq} q / {H} KV heads, d=128, {T} decode steps with compaction and score update",
+            "workload": f"{w.name}: {w.shape or 'synthetic'}-shaped layer, {R} requests x "
+                        f"{min(lens)}-{max(lens) if max(lens) != min(lens) else ''}".rstrip("-") +
+                        f"-token prompts, {Hq} q / {H} KV heads, d=128, {T} decode steps with compaction and "
+                        f"score update",
             "requests": R, "prompt_len": lens[0], "decode_steps": T, "q_heads": Hq, "kv_heads": H,
             "alpha_h": w.alpha_h, "alpha_l": w.alpha_l, "window": w.recent_window, "page_bytes": w.page_bytes,
             "l2": "flushed before every decode step, outside the timed events: 256 MiB written, then a "

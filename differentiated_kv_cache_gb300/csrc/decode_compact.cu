@@ -9,6 +9,8 @@
 // Removal from a tier fills the hole with the tier's last token. The per-head
 // plan is made by k_decode_plan; pages are granted by k_decode_alloc
 // (alloc.cu); k_decode_apply writes the token slots.
+#include <algorithm>
+
 #include "dkv_kernels.cuh"
 
 namespace dkv {
@@ -49,55 +51,23 @@ __device__ __forceinline__ float key_importance(unsigned long long key) {
   return __uint_as_float(b);
 }
 
-__global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int layer, DecodePlan* plans,
-                                                               SlotArgs sa) {
-  if (pv.noop()) return;
-  __shared__ ArgMin s_tmp[kPlanThreads / 32];
-  __shared__ int s_xc;
-  __shared__ float s_ic;
-  const int kvh = blockIdx.x, i = blockIdx.y;
-  const int slot = sa.slots[i];
-  const int unit = i * pv.hkv + kvh;
+// The scan of a head's slots is cut into CTAs of kScanSlots slots (hi slots,
+// then lo slots); each CTA leaves its partial (least important hi token
+// outside the window, least important lo token, the slot of t_c) and the last
+// CTA of the head (per-head arrival counter, no waiting) reduces the partials
+// and makes the plan.
+constexpr int kScanSlots = kPlanThreads * 8;   // 2048: the pool sizes its scan partials with it
+
+// The plan of one head from the reduced scan (thread 0 of the last CTA).
+__device__ void decide_plan(const PoolView& pv, int layer, int slot, int kvh, int unit, ArgMin bh, ArgMin bl, int xc_in,
+                            float ic_in, DecodePlan* plans) {
   const int* rq = pv.rq(layer, slot);
-  const int n0 = rq[1], n = rq[2] + 1, upd = rq[3];
+  const int n = rq[2] + 1;
   const int* cn = pv.cnt(layer, slot, kvh);
   const int nh = cn[0], nl = cn[1], php = cn[2], plp = cn[3];
-  const int* row = pv.row(layer, slot, kvh);
-  const int pc = n - pv.window - 1;         // position of t_c
-  const int wlim = n - pv.window;           // hi victims: position < wlim
-  if (threadIdx.x == 0) { s_xc = -1; s_ic = 0.0f; }
-  __syncthreads();
-  ArgMin bh{~0ull, -1}, bl{~0ull, -1};
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  // one warp per page: the page's score and position segments are contiguous
-  const int nhp = (nh + pv.hi.t - 1) / pv.hi.t;
-  for (int p = warp; p < nhp; p += nw) {
-    const uint8_t* pg = pv.page(row[p]);
-    for (int ip = lane; ip < pv.hi.t; ip += 32) {
-      const int s = p * pv.hi.t + ip;
-      if (s >= nh) break;
-      const float sc = *reinterpret_cast<const float*>(pg + pv.hi.off[4] + 4 * ip);
-      const int pos = *reinterpret_cast<const int*>(pg + pv.hi.off[5] + 4 * ip);
-      const float imp = __fdiv_rn(sc, (float)score_count(pos, n0, upd));
-      if (pos == pc) { s_xc = s; s_ic = imp; }
-      if (pos < wlim) bh = amin(bh, ArgMin{((unsigned long long)order_key(imp) << 32) | (uint32_t)pos, s});
-    }
-  }
-  const int nlp = (nl + pv.lo.t - 1) / pv.lo.t;
-  for (int p = warp; p < nlp; p += nw) {
-    const uint8_t* pg = pv.page(row[pv.L - 1 - p]);
-    for (int ip = lane; ip < pv.lo.t; ip += 32) {
-      const int s = p * pv.lo.t + ip;
-      if (s >= nl) break;
-      const float sc = *reinterpret_cast<const float*>(pg + pv.lo.off[4] + 4 * ip);
-      const int pos = *reinterpret_cast<const int*>(pg + pv.lo.off[5] + 4 * ip);
-      const float imp = __fdiv_rn(sc, (float)score_count(pos, n0, upd));
-      bl = amin(bl, ArgMin{((unsigned long long)order_key(imp) << 32) | (uint32_t)pos, s});
-    }
-  }
-  bh = block_amin(bh, s_tmp);
-  bl = block_amin(bl, s_tmp);
-  if (threadIdx.x != 0) return;
+  const int pc = n - pv.window - 1;
+  int s_xc = xc_in;
+  float s_ic = ic_in;
   const float th_h = __fdiv_rn(pv.alpha_h, (float)n), th_l = __fdiv_rn(pv.alpha_l, (float)n);
   DecodePlan p;
   p.err = 0;
@@ -158,6 +128,88 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
   else if (pv.reclaim && need_l < plp) { p.free_lp = plp - need_l; p.plp = need_l; }
   if (p.err == 0 && p.php + p.plp > pv.L) p.err = DKV_ERR_TABLE_FULL;
   plans[unit] = p;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int layer, DecodePlan* plans,
+                                                               ScanPart* parts, int* arrivals, int max_parts,
+                                                               SlotArgs sa) {
+  if (pv.noop()) return;
+  __shared__ ArgMin s_tmp[kPlanThreads / 32];
+  __shared__ int s_xc, s_last;
+  __shared__ float s_ic;
+  const int c = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
+  const int slot = sa.slots[i];
+  const int unit = i * pv.hkv + kvh;
+  const int* rq = pv.rq(layer, slot);
+  const int n0 = rq[1], n = rq[2] + 1, upd = rq[3];
+  const int* cn = pv.cnt(layer, slot, kvh);
+  const int nh = cn[0], nl = cn[1];
+  const int nparts = max(1, (nh + nl + kScanSlots - 1) / kScanSlots);
+  if (c >= nparts) return;
+  const int* row = pv.row(layer, slot, kvh);
+  const int pc = n - pv.window - 1;         // position of t_c
+  const int wlim = n - pv.window;           // hi victims: position < wlim
+  if (threadIdx.x == 0) { s_xc = -1; s_ic = 0.0f; }
+  __syncthreads();
+  ArgMin bh{~0ull, -1}, bl{~0ull, -1};
+  // slots c*kScanSlots + k*kPlanThreads + tid: consecutive threads read
+  // consecutive score / position entries of a page
+  float sc[8];
+  int pos[8], sl[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    const int x = c * kScanSlots + k * kPlanThreads + threadIdx.x;
+    sl[k] = -1;
+    sc[k] = 0.0f;
+    pos[k] = 0;
+    if (x >= nh + nl) continue;
+    const bool hi = x < nh;
+    const int s = hi ? x : x - nh;
+    const TierGeom& tg = hi ? pv.hi : pv.lo;
+    const int d = tg.div(s);
+    const uint8_t* pg = pv.page(__ldg(row + (hi ? d : pv.L - 1 - d)));
+    sc[k] = *reinterpret_cast<const float*>(pg + tg.off[4] + 4 * (s - d * tg.t));
+    pos[k] = *reinterpret_cast<const int*>(pg + tg.off[5] + 4 * (s - d * tg.t));
+    sl[k] = x;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    if (sl[k] < 0) continue;
+    const float imp = __fdiv_rn(sc[k], (float)score_count(pos[k], n0, upd));
+    const unsigned long long key = ((unsigned long long)order_key(imp) << 32) | (uint32_t)pos[k];
+    if (sl[k] < nh) {
+      if (pos[k] == pc) { s_xc = sl[k]; s_ic = imp; }
+      if (pos[k] < wlim) bh = amin(bh, ArgMin{key, sl[k]});
+    } else {
+      bl = amin(bl, ArgMin{key, sl[k] - nh});
+    }
+  }
+  bh = block_amin(bh, s_tmp);
+  bl = block_amin(bl, s_tmp);
+  if (threadIdx.x == 0) {
+    ScanPart& part = parts[(size_t)unit * max_parts + c];
+    part.kh = bh.key; part.sh = bh.slot;
+    part.kl = bl.key; part.sl = bl.slot;
+    part.xc = s_xc; part.ic = s_ic;
+    __threadfence();
+    s_last = atomicAdd(arrivals + unit, 1) == nparts - 1;
+  }
+  __syncthreads();
+  if (!s_last || threadIdx.x != 0) return;
+  __threadfence();
+  arrivals[unit] = 0;                       // ready for the next step
+  ArgMin rh{~0ull, -1}, rl{~0ull, -1};
+  int xc = -1;
+  float ic = 0.0f;
+  for (int q = 0; q < nparts; q++) {
+    const ScanPart& part = parts[(size_t)unit * max_parts + q];
+    const ArgMin ph{__ldcg(&part.kh), __ldcg(&part.sh)}, pl{__ldcg(&part.kl), __ldcg(&part.sl)};
+    rh = amin(rh, ph);
+    rl = amin(rl, pl);
+    const int pxc = __ldcg(&part.xc);
+    if (pxc >= 0) { xc = pxc; ic = __ldcg(&part.ic); }
+  }
+  decide_plan(pv, layer, slot, kvh, unit, rh, rl, xc, ic, plans);
 }
 
 // Token record staged in shared memory between the read and write phases.
@@ -279,7 +331,13 @@ cudaError_t launch_decode_alloc(Pool& P, int layer, const SlotArgs& sa, cudaStre
 cudaError_t launch_decode(Pool& P, int layer, const SlotArgs& sa, const __half* k, const __half* v,
                           cudaStream_t st) {
   const dim3 grid(P.pv.hkv, sa.n);
-  k_decode_plan<<<grid, kPlanThreads, 0, st>>>(P.pv, layer, P.sc.dplan, sa);
+  int max_n = 1;
+  for (int i = 0; i < sa.n; i++) max_n = std::max(max_n, P.h_n[(size_t)layer * P.cfg.max_requests + sa.slots[i]]);
+  const int scan_ctas = (max_n + 1 + kScanSlots - 1) / kScanSlots;   // stored tokens <= N + 1
+  if (scan_ctas > P.sc.max_scan) return cudaErrorInvalidConfiguration;
+  const dim3 gscan(scan_ctas, P.pv.hkv, sa.n);
+  k_decode_plan<<<gscan, kPlanThreads, 0, st>>>(P.pv, layer, P.sc.dplan, P.sc.dscan, P.sc.darrive, P.sc.max_scan,
+                                                 sa);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = launch_decode_alloc(P, layer, sa, st)) != cudaSuccess) return e;

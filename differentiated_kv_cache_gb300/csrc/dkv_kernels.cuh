@@ -30,6 +30,14 @@ struct DecodePlan {
   Move mv[2];
 };
 
+// Partial of a generation-phase scan over part of a head's slots.
+struct ScanPart {
+  unsigned long long kh, kl;   // argmin keys: hi outside the window, lo
+  int sh, sl;                  // their slots (-1: none)
+  int xc;                      // hi slot of t_c if in this part (-1: not here)
+  float ic;                    // importance of t_c
+};
+
 // Device scratch owned by the pool (sizes fixed at creation).
 struct Scratch {
   // prompt
@@ -45,12 +53,14 @@ struct Scratch {
   unsigned long long* pbase;   // prompt coordination: list start, end and grant total at the call
   // decode compaction
   DecodePlan* dplan;    // [units]
+  ScanPart* dscan;      // [units][max_scan] partials of the generation-phase scan
+  int* darrive;         // [units] scan CTAs arrived (zero between calls)
   // decode attention
   float* apart;         // [units][max_splits][G*(128+2)]
   float* alogit;        // [units][max_chunks][kLogitRow]: per chunk logits, old scores, page ID
   float* alse;          // [units][G]
   int* adone;           // [units] number of attention partials of each head
-  int nkb_cap, grant_cap, max_splits, max_chunks;
+  int nkb_cap, grant_cap, max_splits, max_chunks, max_scan;
 };
 
 // Host side of a pool.

@@ -169,6 +169,7 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   s.grant_cap = (cfg->max_seq_len + hi.t - 1) / hi.t + cfg->prompt_grant_slack;
   s.max_chunks = (cfg->max_seq_len + kChunk - 1) / kChunk + 1;
   s.max_splits = s.max_chunks / 8 + 2;   // attention partials per head (>= 8 chunks per warp)
+  s.max_scan = (cfg->max_seq_len + 1 + 2047) / 2048;   // generation-phase scan CTAs per head
   cudaError_t e = cudaSuccess;
   auto A = [&](auto** ptr, size_t n) {
     if (e == cudaSuccess) e = dev_alloc(P, ptr, n);
@@ -191,11 +192,14 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&s.grant_ids, units * s.grant_cap);
   A(&s.pbase, 4);
   A(&s.dplan, units);
+  A(&s.dscan, units * s.max_scan);
+  A(&s.darrive, units);
   A(&s.apart, units * s.max_splits * (G * kD + 2 * kMaxG));
   A(&s.alogit, units * s.max_chunks * kLogitRow);
   A(&s.alse, units * G);
   A(&s.adone, units);
   if (e == cudaSuccess) e = cudaMemset(s.adone, 0, units * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(s.darrive, 0, units * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v.pages, 0, (size_t)cfg->n_pages * cfg->page_bytes);
   if (e == cudaSuccess) e = cudaMemset(v.table, 0xff, heads * v.L * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v.counts, 0, heads * 4 * sizeof(int));
@@ -429,6 +433,9 @@ int dkv_pool_clear_error(dkv_pool* pool) {
   c.error = 0;
   c.error_info = -1;
   if (cudaMemcpy(P.pv.ctl, &c, sizeof(Ctl), cudaMemcpyHostToDevice) != cudaSuccess) return DKV_ERR_CUDA;
+  // a step cut short can leave generation-phase scan arrivals behind
+  if (cudaMemset(P.sc.darrive, 0, (size_t)P.cfg.max_requests * P.cfg.n_kv_heads * sizeof(int)) != cudaSuccess)
+    return DKV_ERR_CUDA;
   std::vector<int> rq((size_t)P.cfg.n_layers * P.cfg.max_requests * 4);
   if (cudaMemcpy(rq.data(), P.pv.req, rq.size() * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return DKV_ERR_CUDA;

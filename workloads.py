@@ -47,6 +47,7 @@ class Workload:
     prompt_grant_slack: int = 1
     reclaim_in_decode: int = 1
     note: str = ""
+    shape: str = ""                          # the model the layer is shaped like
 
     @property
     def n_q_heads(self) -> int:
@@ -82,21 +83,21 @@ WORKLOADS: dict[str, Workload] = {
     # Llama-3-8B-shaped layer: 32 q / 8 KV heads, batch 32, ctx 4096, rank-4 bias.
     "llama8b": Workload("llama8b", n_layers=1, n_kv_heads=8, group_size=4, n_requests=32,
                         prompt_len=4096, decode_steps=128, n_pages=84800, bias_rank=4,
-                        page_bytes=3584),
+                        page_bytes=3584, shape="Llama-3-8B"),
     # Llama-3-70B-shaped layer: 64 q / 8 KV heads, batch 8, ctx 32768, 2% heavy hitters.
     "llama70b": Workload("llama70b", n_layers=1, n_kv_heads=8, group_size=8, n_requests=8,
                          prompt_len=32768, decode_steps=32, n_pages=164096, bias_rank=4,
-                         heavy_frac=0.02, page_bytes=3584),
+                         heavy_frac=0.02, page_bytes=3584, shape="Llama-3-70B"),
     # QwQ-32B-shaped long generation: 40 q / 8 KV heads, batch 64, 1024-token prompt,
     # 8192 decode steps with compaction every step and tail-page frees.
     "qwq32b": Workload("qwq32b", n_layers=1, n_kv_heads=8, group_size=5, n_requests=64,
                        prompt_len=1024, decode_steps=8192, n_pages=230000, bias_rank=4,
-                       page_bytes=3584),
+                       page_bytes=3584, shape="QwQ-32B"),
     # Qwen2.5-7B-shaped GQA-7: 28 q / 4 KV heads, batch 128, ctx U{1K..16K}, lo tier off,
     # skewed per-head sparsity from a per-KV-head key temperature.
     "qwen7b": Workload("qwen7b", n_layers=1, n_kv_heads=4, group_size=7, n_requests=128,
                        prompt_len=(1024, 16384), decode_steps=16, n_pages=350000, page_bytes=3584,
-                       lo_enabled=0, temp_log2_range=(0.5, 3.5)),
+                       lo_enabled=0, temp_log2_range=(0.5, 3.5), shape="Qwen2.5-7B"),
 }
 
 
