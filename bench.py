@@ -292,13 +292,13 @@ def run_dkv(args, world, rank, local):
                                            "pruned": n_th - prompt_counts[1] - prompt_counts[2]},
             "kv_bytes_vs_fp16": round((HI_BYTES * prompt_counts[1] + LO_BYTES * prompt_counts[2]) / (n_th * 512), 4),
         },
-        "roofline": {"bound": "hbm", "kernel": "dkv_decode_attention call (k_attn_paged + k_attn_merge)",
+        "roofline": {"bound": "hbm", "kernel": "dkv_decode_attention call (k_attn_paged + k_attn_merge + k_attn_scores)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": int(per_launch_bytes), "traffic": args.traffic},
         # per step: prompt compact_step 9 kernels; per decode step 3 (compaction)
-        # + 2 (attention, merge); one free_request kernel per request
-        "gpu_launches": args.steps * (9 + T * 5 + R),
+        # + 3 (attention, merge, score update); one free_request kernel per request
+        "gpu_launches": args.steps * (9 + T * 6 + R),
     }
     result["clocks"] = clk.summary()
     if not args.no_e2e:

@@ -976,22 +976,65 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
   publish(pv, a, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
 }
 
-// Merge of each head's partials into out and lse2 and, with update_scores,
-// the score update: every stored token's score gains the maximum over the
-// group's queries of its probability 2^(l2 - lse2). Grid (x, unit); block x
-// covers chunks kMergeChunks*x .. kMergeChunks*(x+1)-1 of the head for the
-// score update, and in block 0 warp q (q < G) also merges query q's output.
-// Launched as a programmatic dependent of the attention kernel: the head
-// counts, page IDs and scores before the update do not depend on it and are
-// loaded before the dependency wait. After it, every warp issues the loads
-// of the partial count, of every partial's maxima and sums (speculatively,
-// within the scratch bounds) and of its logits at once, and derives the
-// head's lse2 on its own, so that no block-wide barrier is needed.
-constexpr int kMergeChunks = 128;
-constexpr int kMergeK = kMergeChunks * kChunk / 256;   // score slots per thread
+// Merge of each head's partials into out and lse2: one CTA per head, warp q
+// merges query q (lane = feature quad) after every warp has derived the
+// head's maxima and sums (lane = partial, warp reductions). Launched as a
+// programmatic dependent of the attention kernel.
+template <int G>
+__global__ void __launch_bounds__(32 * G) k_attn_merge(PoolView pv, AttnArgs a, SlotArgs sa) {
+  pdl_launch_dependents();        // the score-update grid may launch as SMs free up
+  if (pv.noop()) return;
+  const int unit = blockIdx.x, i = unit / pv.hkv, kvh = unit % pv.hkv;
+  const int slot = sa.slots[i];
+  const int* cn = pv.cnt(a.layer, slot, kvh);
+  const bool empty = __ldcg(cn) + __ldcg(cn + 1) == 0;   // done by the attention kernel
+  pdl_wait();
+  if (empty || pv.noop()) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int stride = part_stride(G);
+  const float* src = a.part + (size_t)unit * a.max_parts * stride;
+  const int nparts = __ldcg(a.done + unit);
+  // maxima and sums of query `warp` (lane = partial, then warp reductions)
+  const int qh = warp;
+  float M = -INFINITY;
+  for (int sp = lane; sp < nparts; sp += 32) M = fmaxf(M, __ldcg(src + sp * stride + G * kD + qh));
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+  float L = 0.0f;
+  for (int sp = lane; sp < nparts; sp += 32) {
+    const float ms = __ldcg(src + sp * stride + G * kD + qh);
+    if (ms != -INFINITY) L += __ldcg(src + sp * stride + G * kD + kMaxG + qh) * fast_exp2(ms - M);
+  }
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) L += __shfl_xor_sync(0xffffffffu, L, s);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+  for (int sp = 0; sp < nparts; sp++) {
+    const float ms = __ldcg(src + sp * stride + G * kD + qh);
+    const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + sp * stride + qh * kD) + lane);
+    const float w = ms == -INFINITY ? 0.0f : fast_exp2(ms - M);
+    o.x += w * o4.x; o.y += w * o4.y; o.z += w * o4.z; o.w += w * o4.w;
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  reinterpret_cast<float4*>(a.out + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qh) * kD)[lane] =
+      make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+  if (lane == 0) {
+    a.lse2[(size_t)unit * G + qh] = L > 0.0f ? M + log2f(L) : -INFINITY;
+    if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, slot)[3] += 1;
+  }
+}
+
+// Score update: every stored token's score gains the maximum over the
+// group's queries of its probability 2^(l2 - lse2). Grid (blocks of
+// kScoreChunks chunks, head); kScoreK slots per thread, whose loads are all
+// issued before any is used. Launched as a programmatic dependent of
+// k_attn_merge: the slots' pages and positions in the head do not depend on
+// it; the logits, lse2 and (paged path) old scores and page IDs do.
+constexpr int kScoreK = 4;
+constexpr int kScoreChunks = 256 * kScoreK / kChunk;
 
 template <int G>
-__global__ void __launch_bounds__(256, 3) k_attn_merge(PoolView pv, AttnArgs a, SlotArgs sa) {
+__global__ void __launch_bounds__(256) k_attn_scores(PoolView pv, AttnArgs a, SlotArgs sa) {
   if (pv.noop()) return;
   const int unit = blockIdx.y, i = unit / pv.hkv, kvh = unit % pv.hkv;
   const int slot = sa.slots[i];
@@ -999,121 +1042,59 @@ __global__ void __launch_bounds__(256, 3) k_attn_merge(PoolView pv, AttnArgs a, 
   const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
   const int ch_hi = (nh + kChunk - 1) / kChunk;
   const int total = ch_hi + (nl + kChunk - 1) / kChunk;
-  const bool idle = nh + nl == 0 ||            // empty head: done by the attention kernel
-                    (blockIdx.x > 0 && (int)blockIdx.x * kMergeChunks >= total);
-  // ---- independent of the attention kernel ----
-  // chunked path: page IDs and scores before the update from the page table
-  // and the pages; paged path: both come from the scratch rows (below)
-  const int* row = pv.row(a.layer, slot, kvh);
-  int pid[kMergeK];
-  float old[kMergeK];
+  if ((int)blockIdx.x * kScoreChunks >= total) return;
+  int sl[kScoreK], pid[kScoreK];
+  float old[kScoreK];
 #pragma unroll
-  for (int k = 0; k < kMergeK; k++) {
+  for (int k = 0; k < kScoreK; k++) {
     const int x = k * 256 + threadIdx.x;
-    const int c = blockIdx.x * kMergeChunks + x / kChunk;
+    const int c = blockIdx.x * kScoreChunks + x / kChunk;
     const bool hi = c < ch_hi;
-    const int sl = (hi ? c : c - ch_hi) * kChunk + x % kChunk;
-    const TierGeom& tg = hi ? pv.hi : pv.lo;
-    const int d = tg.div(sl);
-    const bool ok = a.update && !idle && c < total && sl < (hi ? nh : nl);
-    pid[k] = ok ? (a.paged ? 0 : __ldcg(row + (hi ? d : pv.L - 1 - d))) : -1;
+    sl[k] = (hi ? c : c - ch_hi) * kChunk + x % kChunk;
+    if (c >= total || sl[k] >= (hi ? nh : nl)) sl[k] = -1;
+    pid[k] = -1;
+    old[k] = 0.0f;
+    if (sl[k] >= 0 && !a.paged) {            // chunked path: from the table and the page
+      const TierGeom& tg = hi ? pv.hi : pv.lo;
+      const int d = tg.div(sl[k]);
+      pid[k] = __ldcg(pv.row(a.layer, slot, kvh) + (hi ? d : pv.L - 1 - d));
+    }
   }
   if (!a.paged) {
 #pragma unroll
-    for (int k = 0; k < kMergeK; k++) {
-      old[k] = 0.0f;
-      if (pid[k] >= 0) {
-        const int x = k * 256 + threadIdx.x;
-        const int c = blockIdx.x * kMergeChunks + x / kChunk;
-        const bool hi = c < ch_hi;
-        const int sl = (hi ? c : c - ch_hi) * kChunk + x % kChunk;
-        const TierGeom& tg = hi ? pv.hi : pv.lo;
-        old[k] = __ldcg(reinterpret_cast<const float*>(pv.page(pid[k]) + tg.off[4]) + (sl - tg.div(sl) * tg.t));
+    for (int k = 0; k < kScoreK; k++)
+      if (sl[k] >= 0) {
+        const int c = blockIdx.x * kScoreChunks + (k * 256 + threadIdx.x) / kChunk;
+        const TierGeom& tg = c < ch_hi ? pv.hi : pv.lo;
+        old[k] = __ldcg(reinterpret_cast<const float*>(pv.page(pid[k]) + tg.off[4]) + (sl[k] - tg.div(sl[k]) * tg.t));
       }
-    }
   }
-  // ---- after the attention kernel ----
   pdl_wait();
-  if (idle || pv.noop()) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int stride = part_stride(G);
-  const float* src = a.part + (size_t)unit * a.max_parts * stride;
-  const int nparts = __ldcg(a.done + unit);
-  float lgv[kMergeK][G];
-  if (a.update) {
+  if (pv.noop()) return;
+  float lse[G], lgv[kScoreK][G];
 #pragma unroll
-    for (int k = 0; k < kMergeK; k++) {
-      const int x = k * 256 + threadIdx.x;
-      const int c = min((int)blockIdx.x * kMergeChunks + x / kChunk, a.max_chunks - 1);
-      const float* lg = a.logit + ((size_t)unit * a.max_chunks + c) * kLogitRow;
+  for (int qh = 0; qh < G; qh++) lse[qh] = __ldcg(a.lse2 + (size_t)unit * G + qh);
 #pragma unroll
-      for (int qh = 0; qh < G; qh++) lgv[k][qh] = __ldcg(lg + qh * kChunk + x % kChunk);
-      if (a.paged && pid[k] >= 0) {
-        old[k] = __ldcg(lg + G * kChunk + x % kChunk);
-        pid[k] = __ldcg(reinterpret_cast<const int*>(lg) + (G + 1) * kChunk);
-      }
-    }
-  }
-  // lse2 of every query of the head, in every lane: one pass over the
-  // partials' maxima and sums (the same addresses in every lane), combined
-  // online
-  float M[G], L[G];
-#pragma unroll
-  for (int qh = 0; qh < G; qh++) {
-    M[qh] = -INFINITY;
-    L[qh] = 0.0f;
-  }
-#pragma unroll 8
-  for (int sp = 0; sp < nparts; sp++) {
-#pragma unroll
-    for (int qh = 0; qh < G; qh++) {
-      const float ms = __ldcg(src + sp * stride + G * kD + qh);
-      const float ls = __ldcg(src + sp * stride + G * kD + kMaxG + qh);
-      const float mx = fmaxf(M[qh], ms);
-      if (mx != -INFINITY) {
-        L[qh] = L[qh] * fast_exp2(M[qh] - mx) + ls * fast_exp2(ms - mx);
-        M[qh] = mx;
-      }
-    }
-  }
-  float lse[G];
-#pragma unroll
-  for (int qh = 0; qh < G; qh++) lse[qh] = L[qh] > 0.0f ? M[qh] + log2f(L[qh]) : -INFINITY;
-  if (blockIdx.x == 0 && warp < G) {           // output of query `warp`, features 4 lane .. 4 lane + 3
-    const int qh = warp;
-    float Mq = M[0], Lq = L[0], lq = lse[0];
-#pragma unroll
-    for (int x = 1; x < G; x++)
-      if (x == qh) { Mq = M[x]; Lq = L[x]; lq = lse[x]; }
-    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int sp = 0; sp < nparts; sp++) {
-      const float ms = __ldcg(src + sp * stride + G * kD + qh);
-      const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + sp * stride + qh * kD) + lane);
-      const float w = ms == -INFINITY ? 0.0f : fast_exp2(ms - Mq);
-      O.x += w * o4.x; O.y += w * o4.y; O.z += w * o4.z; O.w += w * o4.w;
-    }
-    const float inv = Lq > 0.0f ? 1.0f / Lq : 0.0f;
-    reinterpret_cast<float4*>(a.out + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qh) * kD)[lane] =
-        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
-    if (lane == 0) {
-      a.lse2[(size_t)unit * G + qh] = lq;
-      if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, slot)[3] += 1;
-    }
-  }
-  if (!a.update) return;
-#pragma unroll
-  for (int k = 0; k < kMergeK; k++) {
-    if (pid[k] < 0) continue;
+  for (int k = 0; k < kScoreK; k++) {
     const int x = k * 256 + threadIdx.x;
-    const int c = blockIdx.x * kMergeChunks + x / kChunk;
-    const bool hi = c < ch_hi;
-    const int sl = (hi ? c : c - ch_hi) * kChunk + x % kChunk;
-    const TierGeom& tg = hi ? pv.hi : pv.lo;
+    const int c = min((int)blockIdx.x * kScoreChunks + x / kChunk, a.max_chunks - 1);
+    const float* lg = a.logit + ((size_t)unit * a.max_chunks + c) * kLogitRow;
+#pragma unroll
+    for (int qh = 0; qh < G; qh++) lgv[k][qh] = __ldcg(lg + qh * kChunk + x % kChunk);
+    if (a.paged && sl[k] >= 0) {
+      old[k] = __ldcg(lg + G * kChunk + x % kChunk);
+      pid[k] = __ldcg(reinterpret_cast<const int*>(lg) + (G + 1) * kChunk);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kScoreK; k++) {
+    if (sl[k] < 0) continue;
+    const int c = blockIdx.x * kScoreChunks + (k * 256 + threadIdx.x) / kChunk;
+    const TierGeom& tg = c < ch_hi ? pv.hi : pv.lo;
     float pm = 0.0f;
 #pragma unroll
     for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, fast_exp2(lgv[k][qh] - lse[qh]));
-    reinterpret_cast<float*>(pv.page(pid[k]) + tg.off[4])[sl - tg.div(sl) * tg.t] = old[k] + pm;
+    reinterpret_cast<float*>(pv.page(pid[k]) + tg.off[4])[sl[k] - tg.div(sl[k]) * tg.t] = old[k] + pm;
   }
 }
 
@@ -1157,11 +1138,9 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
     k_attn_decode<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int call_chunks = (max_tokens + kChunk - 1) / kChunk + 1;   // chunks of the call's longest head
-  const dim3 g2(a.update ? (call_chunks + kMergeChunks - 1) / kMergeChunks : 1, (unsigned)n_units);
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = g2;
-  lc.blockDim = dim3(256);
+  lc.gridDim = dim3((unsigned)n_units);
+  lc.blockDim = dim3(32 * P.pv.G);
   lc.dynamicSmemBytes = 0;
   lc.stream = st;
   cudaLaunchAttribute attr[1];
@@ -1178,6 +1157,20 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
     case 6: e = cudaLaunchKernelEx(&lc, k_attn_merge<6>, P.pv, a, sa); break;
     case 7: e = cudaLaunchKernelEx(&lc, k_attn_merge<7>, P.pv, a, sa); break;
     default: e = cudaLaunchKernelEx(&lc, k_attn_merge<8>, P.pv, a, sa); break;
+  }
+  if (e != cudaSuccess || !a.update) return e;
+  const int call_chunks = (max_tokens + kChunk - 1) / kChunk + 1;   // chunks of the call's longest head
+  lc.gridDim = dim3((unsigned)((call_chunks + kScoreChunks - 1) / kScoreChunks), (unsigned)n_units);
+  lc.blockDim = dim3(256);
+  switch (P.pv.G) {
+    case 1: e = cudaLaunchKernelEx(&lc, k_attn_scores<1>, P.pv, a, sa); break;
+    case 2: e = cudaLaunchKernelEx(&lc, k_attn_scores<2>, P.pv, a, sa); break;
+    case 3: e = cudaLaunchKernelEx(&lc, k_attn_scores<3>, P.pv, a, sa); break;
+    case 4: e = cudaLaunchKernelEx(&lc, k_attn_scores<4>, P.pv, a, sa); break;
+    case 5: e = cudaLaunchKernelEx(&lc, k_attn_scores<5>, P.pv, a, sa); break;
+    case 6: e = cudaLaunchKernelEx(&lc, k_attn_scores<6>, P.pv, a, sa); break;
+    case 7: e = cudaLaunchKernelEx(&lc, k_attn_scores<7>, P.pv, a, sa); break;
+    default: e = cudaLaunchKernelEx(&lc, k_attn_scores<8>, P.pv, a, sa); break;
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1286,13 +1279,6 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
 cudaError_t configure_attention() {
   cudaError_t e = cudaFuncSetAttribute(k_attn_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
   if (e != cudaSuccess) return e;
-  const void* merges[8] = {(const void*)k_attn_merge<1>, (const void*)k_attn_merge<2>, (const void*)k_attn_merge<3>,
-                           (const void*)k_attn_merge<4>, (const void*)k_attn_merge<5>, (const void*)k_attn_merge<6>,
-                           (const void*)k_attn_merge<7>, (const void*)k_attn_merge<8>};
-  for (const void* f : merges) {
-    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
-    if (e != cudaSuccess) return e;
-  }
   return cudaFuncSetAttribute(k_attn_paged, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
 }
 
