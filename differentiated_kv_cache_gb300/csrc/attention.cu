@@ -976,10 +976,14 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
   publish(pv, a, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
 }
 
-// Merge of each head's partials into out and lse2: one CTA per head, warp q
-// merges query q (lane = feature quad) after every warp has derived the
-// head's maxima and sums (lane = partial, warp reductions). Launched as a
+// Merge of each head's partials into out and lse2. Grid (head, kMergeSplit
+// feature slices); warp q merges query q: every lane first derives the
+// query's maximum and sum (lane = partial, warp reductions), then lane
+// (quad, group) sums partials group, group + 4, ... of one feature quad of
+// the slice and the four groups are added by shuffles. Launched as a
 // programmatic dependent of the attention kernel.
+constexpr int kMergeSplit = 4;   // feature slices of 32 per head
+
 template <int G>
 __global__ void __launch_bounds__(32 * G) k_attn_merge(PoolView pv, AttnArgs a, SlotArgs sa) {
   pdl_launch_dependents();        // the score-update grid may launch as SMs free up
@@ -994,31 +998,47 @@ __global__ void __launch_bounds__(32 * G) k_attn_merge(PoolView pv, AttnArgs a, 
   const int stride = part_stride(G);
   const float* src = a.part + (size_t)unit * a.max_parts * stride;
   const int nparts = __ldcg(a.done + unit);
-  // maxima and sums of query `warp` (lane = partial, then warp reductions)
   const int qh = warp;
-  float M = -INFINITY;
-  for (int sp = lane; sp < nparts; sp += 32) M = fmaxf(M, __ldcg(src + sp * stride + G * kD + qh));
+  // the query's maximum and rescaled sum over the partials
+  float mlane = -INFINITY, llane = 0.0f;
+  if (lane < nparts) {
+    mlane = __ldcg(src + lane * stride + G * kD + qh);
+    llane = __ldcg(src + lane * stride + G * kD + kMaxG + qh);
+  }
+  float M = mlane;
+  for (int sp = lane + 32; sp < nparts; sp += 32) M = fmaxf(M, __ldcg(src + sp * stride + G * kD + qh));
 #pragma unroll
   for (int s = 1; s < 32; s <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
-  float L = 0.0f;
-  for (int sp = lane; sp < nparts; sp += 32) {
+  float L = mlane != -INFINITY ? llane * fast_exp2(mlane - M) : 0.0f;
+  for (int sp = lane + 32; sp < nparts; sp += 32) {
     const float ms = __ldcg(src + sp * stride + G * kD + qh);
     if (ms != -INFINITY) L += __ldcg(src + sp * stride + G * kD + kMaxG + qh) * fast_exp2(ms - M);
   }
 #pragma unroll
   for (int s = 1; s < 32; s <<= 1) L += __shfl_xor_sync(0xffffffffu, L, s);
+  // output quad q of the slice, partial group pg
+  const int q = blockIdx.y * 8 + (lane & 7), pg = lane >> 3;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int sp = 0; sp < nparts; sp++) {
+#pragma unroll 4
+  for (int sp = pg; sp < nparts; sp += 4) {
     const float ms = __ldcg(src + sp * stride + G * kD + qh);
-    const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + sp * stride + qh * kD) + lane);
+    const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + sp * stride + qh * kD) + q);
     const float w = ms == -INFINITY ? 0.0f : fast_exp2(ms - M);
     o.x += w * o4.x; o.y += w * o4.y; o.z += w * o4.z; o.w += w * o4.w;
   }
-  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  reinterpret_cast<float4*>(a.out + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qh) * kD)[lane] =
-      make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-  if (lane == 0) {
+#pragma unroll
+  for (int s = 8; s <= 16; s <<= 1) {
+    o.x += __shfl_xor_sync(0xffffffffu, o.x, s);
+    o.y += __shfl_xor_sync(0xffffffffu, o.y, s);
+    o.z += __shfl_xor_sync(0xffffffffu, o.z, s);
+    o.w += __shfl_xor_sync(0xffffffffu, o.w, s);
+  }
+  if (pg == 0) {
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    reinterpret_cast<float4*>(a.out + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qh) * kD)[q] =
+        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+  }
+  if (blockIdx.y == 0 && lane == 0) {
     a.lse2[(size_t)unit * G + qh] = L > 0.0f ? M + log2f(L) : -INFINITY;
     if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, slot)[3] += 1;
   }
@@ -1139,7 +1159,7 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)n_units);
+  lc.gridDim = dim3((unsigned)n_units, kMergeSplit);
   lc.blockDim = dim3(32 * P.pv.G);
   lc.dynamicSmemBytes = 0;
   lc.stream = st;
