@@ -35,9 +35,9 @@ import workloads  # noqa: E402
 METRIC = "compressed-KV decode attn GB/s (% of GB300 HBM peak); compact_step µs/layer"
 HI_BYTES, LO_BYTES, SCORE_RMW = 200, 104, 8
 
-# DRAM bytes of one decode-attention call (k_attn_paged + k_attn_merge +
-# k_attn_scores: dram__bytes_read.sum + dram__bytes_write.sum, caches flushed
-# by ncu before each kernel), third decode step of the llama8b bench step.
+# DRAM bytes of one decode-attention call (k_attn_paged + k_attn_epi:
+# dram__bytes_read.sum + dram__bytes_write.sum, caches flushed by ncu before
+# each kernel), third decode step of the llama8b bench step.
 # Valid only for the kernel sources it was taken on: any change to them
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {
@@ -321,14 +321,14 @@ def run_dkv(args, world, rank, local):
                                            "pruned": n_th - prompt_counts[1] - prompt_counts[2]},
             "kv_bytes_vs_fp16": round((HI_BYTES * prompt_counts[1] + LO_BYTES * prompt_counts[2]) / (n_th * 512), 4),
         },
-        "roofline": {"bound": "hbm", "kernel": "dkv_decode_attention call (k_attn_paged + k_attn_merge + k_attn_scores)",
+        "roofline": {"bound": "hbm", "kernel": "dkv_decode_attention call (k_attn_paged + k_attn_epi)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": int(per_launch_bytes),
                      "traffic": args.traffic if args.traffic is not None else recorded_traffic(args.workload)},
         # per step: prompt compact_step 9 kernels; per decode step 3 (compaction)
-        # + 3 (attention, merge, score update); one free_request kernel per request
-        "gpu_launches": args.steps * (9 + T * 6 + R),
+        # + 2 (attention, epilogue); one free_request kernel per request
+        "gpu_launches": args.steps * (9 + T * 5 + R),
     }
     result["clocks"] = clk.summary()
     if not args.no_e2e:

@@ -89,10 +89,12 @@ struct AttnArgs {
   float* out;         // [n_req][Hkv*G][128]
   float* part;        // [unit][max_parts][G*128 + 16]: O (G x 128), m (8), l (8); a
                       // multiple of 4 floats so every record is 16-byte aligned
-  float* logit;       // [unit][max_chunks][128]: chunk rows of [query < G][16 slots] (log2-domain logits)
+  float* logit;       // [unit][max_chunks][lrow]: chunk rows of [query < G][16 slots] log2-domain
+                      // logits, then (paged path) the 16 old scores and the page ID
   float* lse2;        // [unit][G]
-  int* done;          // [unit] number of partials of the head (written by every publisher)
   int max_parts, max_chunks;
+  int lrow;           // floats per chunk row: (G + 2) * 16
+  int nwarps;         // warps of the attention grid
   int update;
   int layer;
   int paged;          // 1: logit rows also carry the old scores and the page ID (paged path)
@@ -356,13 +358,26 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
   }
 }
 
-// Publish the warp's partial of head u (items [begin, end), warp ranges of C
+// Width C of each attention warp's range of the work sequence (cost units on
+// the paged path, chunks on the chunked path), and the warps first..last whose
+// ranges cover head u (its items start at s_pref[u]; nl: its lo tokens). A
+// warp's partial of head u is record (warp - first) of the head.
+__host__ __device__ __forceinline__ int range_width(int total, int nwarps, bool paged, int wh, int wl) {
+  const int per = (total + nwarps - 1) / nwarps;
+  const int lo = paged ? kMinChunks * (wh > wl ? wh : wl) : kMinChunks;
+  return per > lo ? per : lo;
+}
+__device__ __forceinline__ void head_parts(const int* s_pref, int u, int C, bool paged, int nl, int wh, int wl,
+                                           int& first, int& last) {
+  first = s_pref[u] / C;
+  last = paged ? (s_pref[u + 1] - (nl > 0 ? wl : wh)) / C : (s_pref[u + 1] - 1) / C;
+}
+
 // Publish the warp's partial of head u: O^T (with the value-zero sums added),
 // the running maxima and sums of queries 0..G-1, at index gw - first of the
 // head's partials (warp ranges first..last cover the head). The merge runs in
-// k_attn_merge once every warp is done.
-__device__ void publish(const PoolView& pv, const AttnArgs& a, AttnState& S, int u, int first, int last, int gw,
-                        int lane) {
+// the epilogue kernel once every warp is done.
+__device__ void publish(const PoolView& pv, const AttnArgs& a, AttnState& S, int u, int first, int gw, int lane) {
   const int G = pv.G, g = lane >> 2, t = lane & 3;
   float l0 = S.l[0], l1 = S.l[1], z0 = S.z[0], z1 = S.z[1];
 #pragma unroll
@@ -385,7 +400,6 @@ __device__ void publish(const PoolView& pv, const AttnArgs& a, AttnState& S, int
     if (2 * t < G) { dst[G * kD + 2 * t] = S.m[0]; dst[G * kD + kMaxG + 2 * t] = l0; }
     if (2 * t + 1 < G) { dst[G * kD + 2 * t + 1] = S.m[1]; dst[G * kD + kMaxG + 2 * t + 1] = l1; }
   }
-  if (lane == 0) a.done[u] = last - first + 1;
 }
 
 // Prefix over the call's heads of their work items (pages or chunks), in
@@ -513,10 +527,11 @@ struct PagedCtx {
     settle(c);
   }
   __device__ __forceinline__ bool valid(const PageCursor& c, int g1) const { return c.p < c.np && c.off < g1; }
-  // warps that own pages of head u (range width C); nl: its lo tokens
-  __device__ __forceinline__ void owners(int u, int nl, int C, int& first, int& last) const {
-    first = s_pref[u] / C;
-    last = (s_pref[u + 1] - (nl > 0 ? wl : wh)) / C;
+  // first warp that owns pages of head u (range width C)
+  __device__ __forceinline__ int first_owner(int u, int nl, int C) const {
+    int first, last;
+    head_parts(s_pref, u, C, true, nl, wh, wl, first, last);
+    return first;
   }
 };
 
@@ -537,8 +552,8 @@ __device__ __forceinline__ float hi_half(uint32_t w) { return __half2float(__ush
 // FULL: every slot of the chunks is valid (no masking).
 template <bool HI, int NC, bool FULL>
 __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, const TierGeom& tg, int c0, int count,
-                                              const uint32_t (&bq)[8][2], float sq0, float sq1, float* lg, int pid,
-                                              int G, int g, int t, int jA, int jB) {
+                                              const uint32_t (&bq)[8][2], float sq0, float sq1, float* lg, int lrow,
+                                              int pid, int G, int g, int t, int jA, int jB) {
   constexpr float sc = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
   float l2[NC][4];
   uint32_t vm[NC][2];
@@ -592,7 +607,7 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
       if (sB >= count) l2[c][2] = l2[c][3] = -INFINITY;
     }
     if (lg != nullptr) {           // scratch row of the chunk: logits, old scores, page ID
-      float* lc = lg + c * kLogitRow;
+      float* lc = lg + c * lrow;
       if (2 * t < G) {
         lc[(2 * t) * kChunk + jA] = l2[c][0];
         lc[(2 * t) * kChunk + jB] = l2[c][2];
@@ -691,19 +706,19 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
 // All chunks of one staged page: pairs of chunks share a softmax step.
 template <bool HI>
 __device__ __forceinline__ void attend_page(AttnState& S, const uint8_t* sb, const TierGeom& tg, int nch, int count,
-                                            const uint32_t (&bq)[8][2], float sq0, float sq1, float* lg, int pid,
-                                            int G, int g, int t, int jA, int jB) {
+                                            const uint32_t (&bq)[8][2], float sq0, float sq1, float* lg, int lrow,
+                                            int pid, int G, int g, int t, int jA, int jB) {
   if (count >= nch * kChunk) {
     int c = 0;
     for (; c + 2 <= nch; c += 2)
-      attend_chunks<HI, 2, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * kLogitRow : nullptr, pid, G, g, t,
+      attend_chunks<HI, 2, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G, g, t,
                                  jA, jB);
     if (c < nch)
-      attend_chunks<HI, 1, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * kLogitRow : nullptr, pid, G, g, t,
+      attend_chunks<HI, 1, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G, g, t,
                                  jA, jB);
   } else {
     for (int c = 0; c * kChunk < count; c++)
-      attend_chunks<HI, 1, false>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * kLogitRow : nullptr, pid, G, g, t,
+      attend_chunks<HI, 1, false>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G, g, t,
                                   jA, jB);
   }
 }
@@ -724,7 +739,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
   const int nwarps = gridDim.x * kAttnWarps;
   // at least kMinChunks pages of the heaviest kind per range: a head is then
   // covered by at most (its pages / kMinChunks) + 2 ranges
-  const int C = max(kMinChunks * max(wh, wl), (total + nwarps - 1) / nwarps);
+  const int C = range_width(total, nwarps, true, wh, wl);
   if (blockIdx.x == 0) zero_empty_heads(pv, a, sa, s_pref);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -805,11 +820,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
       const int hp = pv.hi.div(d.z + pv.hi.t - 1);
       const bool hi = d.y < hp;
       if (d.x != cur_u) {         // the range enters the next head
-        {
-          int first, last;
-          ctx.owners(cur_u, cur_nl, C, first, last);
-          publish(pv, a, S, cur_u, first, last, gw, lane);
-        }
+        publish(pv, a, S, cur_u, ctx.first_owner(cur_u, cur_nl, C), gw, lane);
         cur_u = d.x;
         cur_nl = d.w;
         q_hi = hi;
@@ -820,24 +831,20 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
         load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
       }
       const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
-      float* lg0 = a.update ? a.logit + (size_t)cur_u * a.max_chunks * kLogitRow : nullptr;
+      float* lg0 = a.update ? a.logit + (size_t)cur_u * a.max_chunks * a.lrow : nullptr;
       if (hi) {
         const int count = d.z - d.y * pv.hi.t;      // valid slots from this page's start
         attend_page<true>(S, sb, pv.hi, nch_hi, count, bq, sq0, sq1,
-                          lg0 ? lg0 + (size_t)(d.y * nch_hi) * kLogitRow : nullptr, dpid, G, g, t, jA, jB);
+                          lg0 ? lg0 + (size_t)(d.y * nch_hi) * a.lrow : nullptr, a.lrow, dpid, G, g, t, jA, jB);
       } else {
         const int pt = d.y - hp;
         const int count = d.w - pt * pv.lo.t;
         const int chunk0 = (d.z + kChunk - 1) / kChunk + pt * nch_lo;
         attend_page<false>(S, sb, pv.lo, nch_lo, count, bq, sq0, sq1,
-                           lg0 ? lg0 + (size_t)chunk0 * kLogitRow : nullptr, dpid, G, g, t, jA, jB);
+                           lg0 ? lg0 + (size_t)chunk0 * a.lrow : nullptr, a.lrow, dpid, G, g, t, jA, jB);
       }
     }
-    if (!failed) {
-      int first, last;
-      ctx.owners(cur_u, cur_nl, C, first, last);
-      publish(pv, a, S, cur_u, first, last, gw, lane);
-    }
+    if (!failed) publish(pv, a, S, cur_u, ctx.first_owner(cur_u, cur_nl, C), gw, lane);
   }
 }
 
@@ -857,7 +864,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
   int* s_pref = reinterpret_cast<int*>(s_bar + kAttnWarps * kStages);
   const int total = item_prefix(pv, sa, a.layer, false, 1, 1, s_pref, s_warp);
   const int nwarps = gridDim.x * kAttnWarps;
-  const int C = max(kMinChunks, (total + nwarps - 1) / nwarps);
+  const int C = range_width(total, nwarps, false, 1, 1);
   if (blockIdx.x == 0) zero_empty_heads(pv, a, sa, s_pref);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -944,7 +951,7 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
     }
     const int gx = g0 + x;
     if (gx >= cc.end) {           // the range crosses into the next head
-      publish(pv, a, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
+      publish(pv, a, S, cc.u, cc.begin / C, gw, lane);
       cursor_seek(cc, gx, s_pref, pv, sa, a.layer, false);
       load_q(pv, a, cc.u / pv.hkv, cc.u % pv.hkv, g, t, bq_hi, bq_lo, sq0, sq1);
       S.reset();
@@ -969,62 +976,143 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
     const uint8_t* kB = sb + jB * tgc.kbytes + (hi ? 32 * t : 16 * t);
     const uint8_t* v0 = hi ? sb + kOffV + (2 * t) * 128 + 16 * g : sb + kOffV + t * 128 + 16 * g;
     const uint8_t* v1 = v0 + 128;
-    float* lg = a.update ? a.logit + ((size_t)cc.u * a.max_chunks + lc) * kLogitRow : nullptr;
+    float* lg = a.update ? a.logit + ((size_t)cc.u * a.max_chunks + lc) * a.lrow : nullptr;
     attend_chunk(S, hi, kA, kB, v0, v1, kmA, kmB, vmA, vmB, base + jA < count, base + jB < count, bq_hi, bq_lo,
                  sq0, sq1, lg, G, g, t);
   }
-  publish(pv, a, S, cc.u, cc.begin / C, (cc.end - 1) / C, gw, lane);
+  publish(pv, a, S, cc.u, cc.begin / C, gw, lane);
 }
 
-// Merge of each head's partials into out and lse2. Grid (head, kMergeSplit
-// feature slices); warp q merges query q: every lane first derives the
-// query's maximum and sum (lane = partial, warp reductions), then lane
-// (quad, group) sums partials group, group + 4, ... of one feature quad of
-// the slice and the four groups are added by shuffles. Launched as a
-// programmatic dependent of the attention kernel.
-constexpr int kMergeSplit = 4;   // feature slices of 32 per head
+// ---------------------------------------------------------------------------
+// Epilogue of a decode-attention call, launched as a programmatic dependent of
+// the attention kernel: the merge of each head's partials into out and lse2
+// and, with score updates, every stored token's new score
+//   S_j += max over the group's queries of 2^(l2_j - lse2).
+// Grid (block, head). With score updates block x of a head takes its chunks
+// x EC .. x EC + EC - 1: warp 0 stages their scratch rows with one bulk copy
+// and derives the head's lse2 from its partials, warps 1..7 take the block's
+// share of the head's merge tasks (task t of a head spread over n blocks goes
+// to block t mod n; task = query t / 4, features 32 (t % 4) ..), then every
+// thread writes new scores. Without score updates the head's blocks share its
+// merge tasks on all warps. Everything a block needs before the attention
+// kernel completes (its head's counts and partial count in the attention
+// kernels' range partition) it derives from the head counts while it waits.
+// ---------------------------------------------------------------------------
+constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr int kSlices = kD / 32;             // merge tasks per query: feature slices of 32
+constexpr int kMergeRegs = 4;                // partials per lane held in registers by a merge task
 
+// chunks per epilogue step: 8 slots a thread for G <= 4, 4 above
+__host__ __device__ constexpr int epi_chunks(int G) { return G <= 4 ? 128 : 64; }
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, s));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
+  return x;
+}
+
+// Shared-memory layout of the epilogue (bytes), the same on host and device:
+// the step's chunk rows (score updates only), lse2 of the head, mbarrier.
+struct EpiSmem {
+  int rows, lse, misc, total;
+  __host__ __device__ EpiSmem(int G, bool update) {
+    rows = 0;
+    lse = update ? epi_chunks(G) * (G + 2) * kChunk * 4 : 0;
+    misc = lse + 4 * kMaxG;
+    total = misc + 16;
+  }
+};
+
+// Items of head u in the attention kernels' partition (pages weighted by
+// cost on the paged path, chunks on the chunked path): the offset of its
+// first item and the total over the call, from one block-wide reduction over
+// the heads' counts.
+__device__ void head_span(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int u,
+                          int* s_red, int& begin, int& total) {
+  const int n_units = sa.n * pv.hkv;
+  int before = 0, all = 0;
+  for (int v = threadIdx.x; v < n_units; v += blockDim.x) {
+    const int* cn = pv.cnt(layer, sa.slots[v / pv.hkv], v % pv.hkv);
+    const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
+    const int items = paged ? (nh + pv.hi.t - 1) / pv.hi.t * wh + (nl + pv.lo.t - 1) / pv.lo.t * wl
+                            : (nh + kChunk - 1) / kChunk + (nl + kChunk - 1) / kChunk;
+    all += items;
+    if (v < u) before += items;
+  }
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, s);
+    all += __shfl_xor_sync(0xffffffffu, all, s);
+  }
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    s_red[2 * warp] = before;
+    s_red[2 * warp + 1] = all;
+  }
+  __syncthreads();
+  begin = 0;
+  total = 0;
+  for (int w = 0; w < nw; w++) {
+    begin += s_red[2 * w];
+    total += s_red[2 * w + 1];
+  }
+}
+
+// Merge task of head u (np partials): query qh, features 32 sl .. 32 sl + 31.
+// Lane (quad q, group pg) sums partials pg, pg + 4, ... of feature quad q;
+// every lane also takes partial `lane` (lane + 32, ...) for the query's
+// maximum M and rescaled sum L. The loads of the first 16 partials (and of
+// the first 32 for M and L) are all issued before any is used.
 template <int G>
-__global__ void __launch_bounds__(32 * G) k_attn_merge(PoolView pv, AttnArgs a, SlotArgs sa) {
-  pdl_launch_dependents();        // the score-update grid may launch as SMs free up
-  if (pv.noop()) return;
-  const int unit = blockIdx.x, i = unit / pv.hkv, kvh = unit % pv.hkv;
-  const int slot = sa.slots[i];
-  const int* cn = pv.cnt(a.layer, slot, kvh);
-  const bool empty = __ldcg(cn) + __ldcg(cn + 1) == 0;   // done by the attention kernel
-  pdl_wait();
-  if (empty || pv.noop()) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ void merge_task(const PoolView& pv, const AttnArgs& a, const SlotArgs& sa, int u, int np, int qh, int sl,
+                           int lane) {
   const int stride = part_stride(G);
-  const float* src = a.part + (size_t)unit * a.max_parts * stride;
-  const int nparts = __ldcg(a.done + unit);
-  const int qh = warp;
-  // the query's maximum and rescaled sum over the partials
-  float mlane = -INFINITY, llane = 0.0f;
-  if (lane < nparts) {
-    mlane = __ldcg(src + lane * stride + G * kD + qh);
-    llane = __ldcg(src + lane * stride + G * kD + kMaxG + qh);
-  }
-  float M = mlane;
-  for (int sp = lane + 32; sp < nparts; sp += 32) M = fmaxf(M, __ldcg(src + sp * stride + G * kD + qh));
+  const float* src = a.part + (size_t)u * a.max_parts * stride;
+  const int q = sl * 8 + (lane & 7), pg = lane >> 3;
+  float4 o4[kMergeRegs];
+  float mo[kMergeRegs];
 #pragma unroll
-  for (int s = 1; s < 32; s <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
-  float L = mlane != -INFINITY ? llane * fast_exp2(mlane - M) : 0.0f;
-  for (int sp = lane + 32; sp < nparts; sp += 32) {
-    const float ms = __ldcg(src + sp * stride + G * kD + qh);
-    if (ms != -INFINITY) L += __ldcg(src + sp * stride + G * kD + kMaxG + qh) * fast_exp2(ms - M);
+  for (int r = 0; r < kMergeRegs; r++) {
+    const int p = pg + 4 * r;
+    o4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    mo[r] = -INFINITY;
+    if (p < np) {
+      o4[r] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)p * stride + qh * kD) + q);
+      mo[r] = __ldcg(src + (size_t)p * stride + G * kD + qh);
+    }
   }
-#pragma unroll
-  for (int s = 1; s < 32; s <<= 1) L += __shfl_xor_sync(0xffffffffu, L, s);
-  // output quad q of the slice, partial group pg
-  const int q = blockIdx.y * 8 + (lane & 7), pg = lane >> 3;
+  float ml = -INFINITY, ll = 0.0f;
+  if (lane < np) {
+    ml = __ldcg(src + (size_t)lane * stride + G * kD + qh);
+    ll = __ldcg(src + (size_t)lane * stride + G * kD + kMaxG + qh);
+  }
+  float M = ml;
+  for (int p = lane + 32; p < np; p += 32) M = fmaxf(M, __ldcg(src + (size_t)p * stride + G * kD + qh));
+  M = warp_max(M);
+  float L = ml != -INFINITY ? ll * fast_exp2(ml - M) : 0.0f;
+  for (int p = lane + 32; p < np; p += 32) {
+    const float ms = __ldcg(src + (size_t)p * stride + G * kD + qh);
+    if (ms != -INFINITY) L += __ldcg(src + (size_t)p * stride + G * kD + kMaxG + qh) * fast_exp2(ms - M);
+  }
+  L = warp_sum(L);
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int r = 0; r < kMergeRegs; r++) {
+    const float w = mo[r] == -INFINITY ? 0.0f : fast_exp2(mo[r] - M);
+    o.x += w * o4[r].x; o.y += w * o4[r].y; o.z += w * o4[r].z; o.w += w * o4[r].w;
+  }
 #pragma unroll 4
-  for (int sp = pg; sp < nparts; sp += 4) {
-    const float ms = __ldcg(src + sp * stride + G * kD + qh);
-    const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + sp * stride + qh * kD) + q);
+  for (int p = pg + 4 * kMergeRegs; p < np; p += 4) {   // heads of more than 16 partials
+    const float ms = __ldcg(src + (size_t)p * stride + G * kD + qh);
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)p * stride + qh * kD) + q);
     const float w = ms == -INFINITY ? 0.0f : fast_exp2(ms - M);
-    o.x += w * o4.x; o.y += w * o4.y; o.z += w * o4.z; o.w += w * o4.w;
+    o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
   }
 #pragma unroll
   for (int s = 8; s <= 16; s <<= 1) {
@@ -1033,88 +1121,148 @@ __global__ void __launch_bounds__(32 * G) k_attn_merge(PoolView pv, AttnArgs a, 
     o.z += __shfl_xor_sync(0xffffffffu, o.z, s);
     o.w += __shfl_xor_sync(0xffffffffu, o.w, s);
   }
+  const int i = u / pv.hkv, kvh = u % pv.hkv;
   if (pg == 0) {
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     reinterpret_cast<float4*>(a.out + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qh) * kD)[q] =
         make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
   }
-  if (blockIdx.y == 0 && lane == 0) {
-    a.lse2[(size_t)unit * G + qh] = L > 0.0f ? M + log2f(L) : -INFINITY;
-    if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, slot)[3] += 1;
+  if (sl == 0 && lane == 0) {
+    a.lse2[(size_t)u * G + qh] = L > 0.0f ? M + log2f(L) : -INFINITY;
+    if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, sa.slots[i])[3] += 1;
   }
 }
 
-// Score update: every stored token's score gains the maximum over the
-// group's queries of its probability 2^(l2 - lse2). Grid (blocks of
-// kScoreChunks chunks, head); kScoreK slots per thread, whose loads are all
-// issued before any is used. Launched as a programmatic dependent of
-// k_attn_merge: the slots' pages and positions in the head do not depend on
-// it; the logits, lse2 and (paged path) old scores and page IDs do.
-constexpr int kScoreK = 4;
-constexpr int kScoreChunks = 256 * kScoreK / kChunk;
+// lse2 of head u's G queries from its np partials (lane = partial; lanes fold
+// partials beyond the 32nd in online), written to dst[0 .. G).
+template <int G>
+__device__ void head_lse(const AttnArgs& a, int u, int np, int lane, float* dst) {
+  const int stride = part_stride(G);
+  const float* src = a.part + (size_t)u * a.max_parts * stride + G * kD;
+  float m[G], l[G];
+#pragma unroll
+  for (int qh = 0; qh < G; qh++) {
+    m[qh] = -INFINITY;
+    l[qh] = 0.0f;
+  }
+  if (lane < np) {
+#pragma unroll
+    for (int qh = 0; qh < G; qh++) {
+      m[qh] = __ldcg(src + (size_t)lane * stride + qh);
+      l[qh] = __ldcg(src + (size_t)lane * stride + kMaxG + qh);
+    }
+  }
+  for (int p = lane + 32; p < np; p += 32) {
+#pragma unroll
+    for (int qh = 0; qh < G; qh++) {
+      const float mp = __ldcg(src + (size_t)p * stride + qh), lp = __ldcg(src + (size_t)p * stride + kMaxG + qh);
+      const float mn = fmaxf(m[qh], mp);
+      l[qh] = l[qh] * fast_exp2(m[qh] - mn) + lp * fast_exp2(mp - mn);
+      m[qh] = mn;
+    }
+  }
+#pragma unroll
+  for (int qh = 0; qh < G; qh++) {
+    const float M = warp_max(m[qh]);
+    const float L = warp_sum(m[qh] != -INFINITY ? l[qh] * fast_exp2(m[qh] - M) : 0.0f);
+    if (lane == 0) dst[qh] = L > 0.0f ? M + log2f(L) : -INFINITY;
+  }
+}
 
 template <int G>
-__global__ void __launch_bounds__(256) k_attn_scores(PoolView pv, AttnArgs a, SlotArgs sa) {
+__global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnArgs a, SlotArgs sa) {
   if (pv.noop()) return;
-  const int unit = blockIdx.y, i = unit / pv.hkv, kvh = unit % pv.hkv;
-  const int slot = sa.slots[i];
-  const int* cn = pv.cnt(a.layer, slot, kvh);
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_red[2 * kEpiWarps];
+  constexpr int EC = epi_chunks(G);
+  const int u = blockIdx.y, xb = blockIdx.x;
+  const int i = u / pv.hkv, kvh = u % pv.hkv;
+  const bool paged = a.paged != 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int* cn = pv.cnt(a.layer, sa.slots[i], kvh);
   const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
-  const int ch_hi = (nh + kChunk - 1) / kChunk;
-  const int total = ch_hi + (nl + kChunk - 1) / kChunk;
-  if ((int)blockIdx.x * kScoreChunks >= total) return;
-  int sl[kScoreK], pid[kScoreK];
-  float old[kScoreK];
-#pragma unroll
-  for (int k = 0; k < kScoreK; k++) {
-    const int x = k * 256 + threadIdx.x;
-    const int c = blockIdx.x * kScoreChunks + x / kChunk;
-    const bool hi = c < ch_hi;
-    sl[k] = (hi ? c : c - ch_hi) * kChunk + x % kChunk;
-    if (c >= total || sl[k] >= (hi ? nh : nl)) sl[k] = -1;
-    pid[k] = -1;
-    old[k] = 0.0f;
-    if (sl[k] >= 0 && !a.paged) {            // chunked path: from the table and the page
-      const TierGeom& tg = hi ? pv.hi : pv.lo;
-      const int d = tg.div(sl[k]);
-      pid[k] = __ldcg(pv.row(a.layer, slot, kvh) + (hi ? d : pv.L - 1 - d));
-    }
+  if (nh + nl == 0) return;       // an empty head: done by the attention kernel
+  const int ch_hi = (nh + kChunk - 1) / kChunk, nch = ch_hi + (nl + kChunk - 1) / kChunk;
+  // blocks of the head: its chunk steps (score updates), else every block
+  const int nb = a.update ? (nch + EC - 1) / EC : (int)gridDim.x;
+  if (xb >= nb) return;
+  // the head's partial count in the attention kernels' range partition
+  const int wh = paged ? kPageW + kChunkW * (pv.hi.t / kChunk) : 1;
+  const int wl = paged ? kPageW + kChunkW * (pv.lo.t / kChunk) : 1;
+  int begin, total;
+  head_span(pv, sa, a.layer, paged, wh, wl, u, s_red, begin, total);
+  const int items = paged ? (nh + pv.hi.t - 1) / pv.hi.t * wh + (nl + pv.lo.t - 1) / pv.lo.t * wl : nch;
+  const int C = range_width(total, a.nwarps, paged, wh, wl);
+  const int first = begin / C;
+  const int last = paged ? (begin + items - (nl > 0 ? wl : wh)) / C : (begin + items - 1) / C;
+  const int np = last - first + 1;
+  const EpiSmem L(G, a.update != 0);
+  float* s_rows = reinterpret_cast<float*>(smem + L.rows);
+  float* s_lse = reinterpret_cast<float*>(smem + L.lse);
+  const uint32_t bar = smem_u32(smem + L.misc);
+  const int c0 = xb * EC, c1 = min(nch, c0 + EC);
+  if (a.update && threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
   }
-  if (!a.paged) {
-#pragma unroll
-    for (int k = 0; k < kScoreK; k++)
-      if (sl[k] >= 0) {
-        const int c = blockIdx.x * kScoreChunks + (k * 256 + threadIdx.x) / kChunk;
-        const TierGeom& tg = c < ch_hi ? pv.hi : pv.lo;
-        old[k] = __ldcg(reinterpret_cast<const float*>(pv.page(pid[k]) + tg.off[4]) + (sl[k] - tg.div(sl[k]) * tg.t));
-      }
-  }
+  // partials and chunk rows: written by the attention kernel. A device error
+  // it raised itself leaves this call's outputs undefined (the status says so)
   pdl_wait();
-  if (pv.noop()) return;
-  float lse[G], lgv[kScoreK][G];
-#pragma unroll
-  for (int qh = 0; qh < G; qh++) lse[qh] = __ldcg(a.lse2 + (size_t)unit * G + qh);
-#pragma unroll
-  for (int k = 0; k < kScoreK; k++) {
-    const int x = k * 256 + threadIdx.x;
-    const int c = min((int)blockIdx.x * kScoreChunks + x / kChunk, a.max_chunks - 1);
-    const float* lg = a.logit + ((size_t)unit * a.max_chunks + c) * kLogitRow;
-#pragma unroll
-    for (int qh = 0; qh < G; qh++) lgv[k][qh] = __ldcg(lg + qh * kChunk + x % kChunk);
-    if (a.paged && sl[k] >= 0) {
-      old[k] = __ldcg(lg + G * kChunk + x % kChunk);
-      pid[k] = __ldcg(reinterpret_cast<const int*>(lg) + (G + 1) * kChunk);
+  // merge tasks of this block: tasks xb, xb + nb, ... of the head, on warps
+  // 1.. with score updates (warp 0 derives lse2 and stages the rows), else on
+  // every warp
+  const int w0 = a.update ? 1 : 0;
+  if (a.update && warp == 0) {
+    if (lane == 0) {
+      const uint32_t bytes = (uint32_t)(c1 - c0) * a.lrow * 4u;
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(smem_u32(s_rows), a.logit + ((size_t)u * a.max_chunks + c0) * a.lrow, bytes, bar);
     }
+    head_lse<G>(a, u, np, lane, s_lse);
   }
+  if (warp >= w0) {
+    int j = 0;
+    for (int task = xb; task < G * kSlices; task += nb, j++)
+      if (j % (kEpiWarps - w0) == warp - w0) merge_task<G>(pv, a, sa, u, np, task / kSlices, task % kSlices, lane);
+  }
+  if (!a.update) return;
+  __syncthreads();                // s_lse
+  if (!mbar_wait_bounded(bar, 0)) {
+    if (threadIdx.x == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = u;
+    mbar_wait_bounded(bar, 0);
+    return;
+  }
+  // new scores of the block's slots: S_j += max over queries of 2^(l2 - lse2)
+  float lse[G];
 #pragma unroll
-  for (int k = 0; k < kScoreK; k++) {
-    if (sl[k] < 0) continue;
-    const int c = blockIdx.x * kScoreChunks + (k * 256 + threadIdx.x) / kChunk;
-    const TierGeom& tg = c < ch_hi ? pv.hi : pv.lo;
+  for (int qh = 0; qh < G; qh++) lse[qh] = s_lse[qh];
+  const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
+#pragma unroll
+  for (int k = 0; k < EC * kChunk / kEpiThreads; k++) {
+    const int x = k * kEpiThreads + threadIdx.x;
+    const int lc = c0 + x / kChunk, j = x % kChunk;
+    if (lc >= c1) break;
+    const bool hi_t = lc < ch_hi;
+    const int slot = (hi_t ? lc : lc - ch_hi) * kChunk + j;
+    if (slot >= (hi_t ? nh : nl)) continue;
+    const float* row = s_rows + (size_t)(lc - c0) * a.lrow;
     float pm = 0.0f;
 #pragma unroll
-    for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, fast_exp2(lgv[k][qh] - lse[qh]));
-    reinterpret_cast<float*>(pv.page(pid[k]) + tg.off[4])[sl[k] - tg.div(sl[k]) * tg.t] = old[k] + pm;
+    for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, fast_exp2(row[qh * kChunk + j] - lse[qh]));
+    const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+    const int d = tg.div(slot);
+    float* sp;
+    float old;
+    if (paged) {
+      sp = reinterpret_cast<float*>(pv.page(reinterpret_cast<const int*>(row)[(G + 1) * kChunk]) + tg.off[4]) +
+           (slot - d * tg.t);
+      old = row[G * kChunk + j];
+    } else {                      // chunked path: page from the table, old score from the page
+      const int pid = __ldcg(row_tab + (hi_t ? d : pv.L - 1 - d));
+      sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (slot - d * tg.t);
+      old = __ldcg(sp);
+    }
+    *sp = old + pm;
   }
 }
 
@@ -1131,9 +1279,9 @@ static int pages_per_chunk(int t) {
   return m;
 }
 
-// Launch the attention kernel of the pool's page geometry, then the merge
-// (and score update) kernel as its programmatic dependent, over the scratch
-// that `a` points to.
+// Launch the attention kernel of the pool's page geometry, then the epilogue
+// kernel (merge and score update) as its programmatic dependent, over the
+// scratch that `a` points to.
 static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int max_tokens, cudaStream_t st) {
   const int n_units = sa.n * P.pv.hkv;
   const bool paged = P.pv.hi.t % kChunk == 0 && P.pv.lo.t % kChunk == 0;
@@ -1151,6 +1299,8 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   }
   if (smem > kMaxAttnSmem) return cudaErrorInvalidConfiguration;
   a.paged = paged ? 1 : 0;
+  a.lrow = (P.pv.G + 2) * kChunk;
+  a.nwarps = P.sm_count * kCtasPerSm * kAttnWarps;
   cudaError_t e;
   if (paged)
     k_attn_paged<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
@@ -1158,39 +1308,35 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
     k_attn_decode<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // epilogue: merge and (with score updates) the new scores
+  const int G = P.pv.G;
+  const EpiSmem es(G, a.update != 0);
+  unsigned gx;
+  if (a.update) {
+    const int call_chunks = (max_tokens + kChunk - 1) / kChunk + 1;   // chunks of the call's longest head
+    gx = (unsigned)((call_chunks + epi_chunks(G) - 1) / epi_chunks(G));
+  } else {
+    gx = (unsigned)((G * kSlices + kEpiWarps - 1) / kEpiWarps);
+  }
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)n_units, kMergeSplit);
-  lc.blockDim = dim3(32 * P.pv.G);
-  lc.dynamicSmemBytes = 0;
+  lc.gridDim = dim3(gx, (unsigned)n_units);
+  lc.blockDim = dim3(kEpiThreads);
+  lc.dynamicSmemBytes = (size_t)es.total;
   lc.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  switch (P.pv.G) {
-    case 1: e = cudaLaunchKernelEx(&lc, k_attn_merge<1>, P.pv, a, sa); break;
-    case 2: e = cudaLaunchKernelEx(&lc, k_attn_merge<2>, P.pv, a, sa); break;
-    case 3: e = cudaLaunchKernelEx(&lc, k_attn_merge<3>, P.pv, a, sa); break;
-    case 4: e = cudaLaunchKernelEx(&lc, k_attn_merge<4>, P.pv, a, sa); break;
-    case 5: e = cudaLaunchKernelEx(&lc, k_attn_merge<5>, P.pv, a, sa); break;
-    case 6: e = cudaLaunchKernelEx(&lc, k_attn_merge<6>, P.pv, a, sa); break;
-    case 7: e = cudaLaunchKernelEx(&lc, k_attn_merge<7>, P.pv, a, sa); break;
-    default: e = cudaLaunchKernelEx(&lc, k_attn_merge<8>, P.pv, a, sa); break;
-  }
-  if (e != cudaSuccess || !a.update) return e;
-  const int call_chunks = (max_tokens + kChunk - 1) / kChunk + 1;   // chunks of the call's longest head
-  lc.gridDim = dim3((unsigned)((call_chunks + kScoreChunks - 1) / kScoreChunks), (unsigned)n_units);
-  lc.blockDim = dim3(256);
-  switch (P.pv.G) {
-    case 1: e = cudaLaunchKernelEx(&lc, k_attn_scores<1>, P.pv, a, sa); break;
-    case 2: e = cudaLaunchKernelEx(&lc, k_attn_scores<2>, P.pv, a, sa); break;
-    case 3: e = cudaLaunchKernelEx(&lc, k_attn_scores<3>, P.pv, a, sa); break;
-    case 4: e = cudaLaunchKernelEx(&lc, k_attn_scores<4>, P.pv, a, sa); break;
-    case 5: e = cudaLaunchKernelEx(&lc, k_attn_scores<5>, P.pv, a, sa); break;
-    case 6: e = cudaLaunchKernelEx(&lc, k_attn_scores<6>, P.pv, a, sa); break;
-    case 7: e = cudaLaunchKernelEx(&lc, k_attn_scores<7>, P.pv, a, sa); break;
-    default: e = cudaLaunchKernelEx(&lc, k_attn_scores<8>, P.pv, a, sa); break;
+  switch (G) {
+    case 1: e = cudaLaunchKernelEx(&lc, k_attn_epi<1>, P.pv, a, sa); break;
+    case 2: e = cudaLaunchKernelEx(&lc, k_attn_epi<2>, P.pv, a, sa); break;
+    case 3: e = cudaLaunchKernelEx(&lc, k_attn_epi<3>, P.pv, a, sa); break;
+    case 4: e = cudaLaunchKernelEx(&lc, k_attn_epi<4>, P.pv, a, sa); break;
+    case 5: e = cudaLaunchKernelEx(&lc, k_attn_epi<5>, P.pv, a, sa); break;
+    case 6: e = cudaLaunchKernelEx(&lc, k_attn_epi<6>, P.pv, a, sa); break;
+    case 7: e = cudaLaunchKernelEx(&lc, k_attn_epi<7>, P.pv, a, sa); break;
+    default: e = cudaLaunchKernelEx(&lc, k_attn_epi<8>, P.pv, a, sa); break;
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1204,7 +1350,6 @@ cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tok
   a.part = P.sc.apart;
   a.logit = P.sc.alogit;
   a.lse2 = P.sc.alse;
-  a.done = P.sc.adone;
   a.max_parts = P.sc.max_splits;
   a.max_chunks = P.sc.max_chunks;
   a.update = update_scores;
@@ -1214,9 +1359,9 @@ cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tok
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant (dkv_decode_attention_static). The same kernels
-// work in one fixed device array instead of the pool's scratch: the partial
-// counts, the per-head lse2, the per-warp partials and, with score updates,
-// the per-chunk logits. The array is part of this library's device image; the
+// work in one fixed device array instead of the pool's scratch: the per-head
+// lse2, the per-warp partials and, with score updates, the per-chunk rows of
+// logits, old scores and page IDs. The array is part of this library's device image; the
 // CUDA driver reserves it when the module is loaded, so no call here
 // allocates. Every call shares it and it keeps the last call's contents.
 // ---------------------------------------------------------------------------
@@ -1229,9 +1374,9 @@ static void* g_static_base[kMaxStaticDevices];
 namespace {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Regions of the array for one call, each 256-byte aligned: partial counts
-// at 0, then lse2, partials, logits. Strides are sized for the call's
-// longest request, not the pool's maximum.
+// Regions of the array for one call, each 256-byte aligned: lse2 at 0, then
+// partials, chunk rows. Strides are sized for the call's longest request, not
+// the pool's maximum.
 struct StaticLayout {
   size_t lse2, part, logit, total;
   int max_parts, max_chunks;
@@ -1241,13 +1386,13 @@ StaticLayout static_layout(int n_units, int G, int max_tokens, int update_scores
   StaticLayout L;
   L.max_chunks = (max_tokens + kChunk - 1) / kChunk + 1;
   L.max_parts = L.max_chunks / kMinChunks + 2;   // warps over one head (ranges >= kMinChunks)
-  size_t off = round256((size_t)n_units * sizeof(int));
+  size_t off = 0;
   L.lse2 = off;
   off = round256(off + (size_t)n_units * G * sizeof(float));
   L.part = off;
   off = round256(off + (size_t)n_units * L.max_parts * part_stride(G) * sizeof(float));
   L.logit = off;
-  if (update_scores) off += (size_t)n_units * L.max_chunks * kLogitRow * sizeof(float);
+  if (update_scores) off += (size_t)n_units * L.max_chunks * (G + 2) * kChunk * sizeof(float);
   L.total = off;
   return L;
 }
@@ -1282,7 +1427,6 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
   AttnArgs a;
   a.q = q;
   a.out = out;
-  a.done = reinterpret_cast<int*>(base);
   a.lse2 = reinterpret_cast<float*>(base + L.lse2);
   a.part = reinterpret_cast<float*>(base + L.part);
   a.logit = reinterpret_cast<float*>(base + L.logit);
@@ -1291,15 +1435,21 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
   a.update = update_scores;
   a.layer = layer;
   // Nothing in the array needs clearing: every value a call reads from it
-  // (partial counts, partials, logits) is written earlier in the same call.
-  // The grid barrier of the cooperative path is the pool's own.
+  // (partials, chunk rows) is written earlier in the same call.
   return launch_kernels(P, a, sa, max_tokens, st);
 }
 
 cudaError_t configure_attention() {
-  cudaError_t e = cudaFuncSetAttribute(k_attn_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_attn_paged, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
+  const void* fns[] = {reinterpret_cast<const void*>(k_attn_decode), reinterpret_cast<const void*>(k_attn_paged),
+                       reinterpret_cast<const void*>(k_attn_epi<1>), reinterpret_cast<const void*>(k_attn_epi<2>),
+                       reinterpret_cast<const void*>(k_attn_epi<3>), reinterpret_cast<const void*>(k_attn_epi<4>),
+                       reinterpret_cast<const void*>(k_attn_epi<5>), reinterpret_cast<const void*>(k_attn_epi<6>),
+                       reinterpret_cast<const void*>(k_attn_epi<7>), reinterpret_cast<const void*>(k_attn_epi<8>)};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace dkv

@@ -81,7 +81,11 @@ struct PoolView {
   __device__ __forceinline__ uint8_t* page(int id) const {
     return pages + (size_t)id * page_bytes;
   }
-  __device__ __forceinline__ bool noop() const { return *(volatile int*)&ctl->error != 0; }
+  // Sticky status set by an earlier kernel of the stream (visible at kernel
+  // start). Read through L1: the first warp of an SM fetches the line and the
+  // others hit, instead of every warp of a large grid queueing on the same
+  // L2 line.
+  __device__ __forceinline__ bool noop() const { return __ldca(&ctl->error) != 0; }
 };
 
 // ---------------------------------------------------------------------------

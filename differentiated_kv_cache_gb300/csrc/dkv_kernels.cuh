@@ -14,7 +14,6 @@ constexpr int kAttnWarps = 4;      // warps per decode-attention CTA
 // Decode-attention scratch row per 16-slot chunk (floats): the log2-domain
 // logits [query < G][16 slots], then (paged path) the scores before the
 // update [16 slots] at row G and the chunk's page ID at row G + 1.
-constexpr int kLogitRow = (kMaxG + 2) * kChunk;
 
 // One slot write of a generation-phase step.
 enum MoveSrc { kSrcNew = 0, kSrcDemote = 1 };
@@ -57,9 +56,8 @@ struct Scratch {
   int* darrive;         // [units] scan CTAs arrived (zero between calls)
   // decode attention
   float* apart;         // [units][max_splits][G*(128+2)]
-  float* alogit;        // [units][max_chunks][kLogitRow]: per chunk logits, old scores, page ID
+  float* alogit;        // [units][max_chunks][(G + 2) * 16]: per chunk logits, old scores, page ID
   float* alse;          // [units][G]
-  int* adone;           // [units] number of attention partials of each head
   int nkb_cap, grant_cap, max_splits, max_chunks, max_scan;
 };
 

@@ -195,10 +195,8 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&s.dscan, units * s.max_scan);
   A(&s.darrive, units);
   A(&s.apart, units * s.max_splits * (G * kD + 2 * kMaxG));
-  A(&s.alogit, units * s.max_chunks * kLogitRow);
+  A(&s.alogit, units * s.max_chunks * (G + 2) * kChunk);
   A(&s.alse, units * G);
-  A(&s.adone, units);
-  if (e == cudaSuccess) e = cudaMemset(s.adone, 0, units * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(s.darrive, 0, units * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v.pages, 0, (size_t)cfg->n_pages * cfg->page_bytes);
   if (e == cudaSuccess) e = cudaMemset(v.table, 0xff, heads * v.L * sizeof(int));

@@ -43,7 +43,10 @@
  *    detected on the device before anything is written: the whole call
  *    becomes a no-op and the code latches in the pool's sticky status word.
  *    While the sticky status is non-zero every later call is a device no-op;
- *    dkv_pool_status reads it and dkv_pool_clear_error resets it.
+ *    dkv_pool_status reads it and dkv_pool_clear_error resets it. A bounded
+ *    device wait that gives up (DKV_ERR_TIMEOUT) latches the same way; the
+ *    call that raised it leaves its own outputs (attention out, the scores
+ *    it updates) undefined.
  *
  * Unified page format  [Mem-UP]
  * -----------------------------
@@ -257,16 +260,17 @@ int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
  *
  * Size limit: with U = n_req * n_kv_heads, C = ceil(max_n / 16) + 1 (max_n =
  * longest stored sequence among the call's requests) and r(x) = x rounded up
- * to 256, the call needs r(4U) + r(4UG) + r(4U(C/8 + 2)(128G + 16)) bytes,
- * plus 640UC if update_scores != 0. A larger call returns DKV_ERR_SCRATCH
+ * to 256, the call needs r(4UG) + r(4U(C/8 + 2)(128G + 16)) bytes, plus
+ * 64(G + 2)UC if update_scores != 0. A larger call returns DKV_ERR_SCRATCH
  * and queues nothing.
  *
  * Set-up: the first call on a device looks up the array's address on that
  * device (cudaGetSymbolAddress, with the pool's device current); make that
  * first call before any stream capture. Every call on a device shares the
  * array and it keeps the last call's contents; nothing in it has to start at
- * zero, because every value a call reads from the array (partial counts,
- * partials, logits) is written earlier in the same call.
+ * zero, because every value a call reads from the array (partials and the
+ * per-chunk rows of logits, old scores and page IDs) is written earlier in
+ * the same call.
  * Calls that overlap on the GPU (on different streams, or from different
  * pools of one device) race on the array and give wrong results: order them
  * on one stream or synchronise between them.

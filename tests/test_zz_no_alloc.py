@@ -49,8 +49,8 @@ def need_bytes(n_units, G, max_n, update):
     """Scratch bytes of one call, from the formula the header states."""
     r = lambda x: (x + 255) // 256 * 256
     C = (max_n + 15) // 16 + 1
-    b = r(4 * n_units) + r(4 * n_units * G) + r(4 * n_units * (C // 8 + 2) * (128 * G + 16))
-    return b + (640 * n_units * C if update else 0)
+    b = r(4 * n_units * G) + r(4 * n_units * (C // 8 + 2) * (128 * G + 16))
+    return b + (64 * (G + 2) * n_units * C if update else 0)
 
 
 @pytest.mark.parametrize("pb", [4096, 3584])
