@@ -307,7 +307,8 @@ int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req,
   if (e != cudaSuccess) return DKV_ERR_CUDA;
   int max_len = 0;
   for (int i = 0; i < n_req; i++) max_len = std::max(max_len, seq_lens[i]);
-  e = launch_prompt(P, layer, n_req, max_len, static_cast<const __half*>(k), static_cast<const __half*>(v),
+  e = launch_prompt(P, layer, n_req, max_len, args.tok0[n_req], static_cast<const __half*>(k),
+                    static_cast<const __half*>(v),
                     static_cast<const __half*>(q_obs), scores_in, scores_out, st);
   if (e != cudaSuccess) return DKV_ERR_CUDA;
   for (int i = 0; i < n_req; i++) {

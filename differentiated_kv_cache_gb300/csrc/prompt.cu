@@ -1,165 +1,16 @@
 // prompt.cu — prompt-phase compaction kernels (DiffKV, compaction policy,
 // prompt phase; memory management, prompt workflow, Figure 6).
 //
-//   k_prompt_lse      observation-window log-sum-exp, per key block (partial)
-//   k_prompt_lse_merge  merge of the key-block partials
-//   k_prompt_score    token score S_j and tier, per key block
 //   k_prompt_given    tier from caller-given scores
 //   k_prompt_scatter  rank -> position map per (head, tier)
 //   k_prompt_pack     quantize and pack surviving tokens into the granted pages
 //
-// The allocation step between score and scatter (grant prefix sum, reclaim,
-// table) is in alloc.cu.
+// Token scores from the observation queries (log-sum-exp pass, merge, score
+// pass) run on the tensor cores in prompt_tc.cu; the allocation step between
+// score and scatter (grant prefix sum, reclaim, table) is in alloc.cu.
 #include "dkv_kernels.cuh"
 
 namespace dkv {
-
-// swizzled byte offset of 16-byte chunk `ch` of a 256-byte row `r` in shared memory
-__device__ __forceinline__ int swz(int r, int ch) { return r * 256 + ((ch ^ (r & 7)) << 4); }
-
-constexpr float kLog2e = 1.4426950408889634f;
-
-// ---------------------------------------------------------------------------
-// a1: lse_{h,p} = log sum_{j<=p} exp(q_{h,p}.k_j / sqrt(d)), per key block.
-// CTA = (key block of 128 keys, KV head, request); warp h = query head h of
-// the group, holding its 32 observation rows as mma A fragments. Scores are
-// kept in the log2 domain (x * log2(e) / sqrt(d)).
-// ---------------------------------------------------------------------------
-template <int G>
-__global__ void __launch_bounds__(32 * G) k_prompt_lse(PoolView pv, const __half* __restrict__ k,
-                                                        const __half* __restrict__ q_obs, float2* partial,
-                                                        int nkb_cap) {
-  if (pv.noop()) return;
-  const int kb = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
-  const CallArgs* ca = pv.call;
-  const int n0 = ca->lens[i];
-  const int key0 = kb * kKeyBlock;
-  if (key0 >= n0) return;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sQ = smem;                   // 32*G rows x 256 B
-  uint8_t* sK = smem + 32 * G * 256;    // kKeyBlock rows x 256 B
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Hq = pv.hkv * G;
-  for (int c = tid; c < 32 * G * 16; c += blockDim.x) {
-    const int r = c >> 4, ch = c & 15, h = r >> 5, o = r & 31;
-    const __half* src = q_obs + (((size_t)i * kObs + o) * Hq + (size_t)kvh * G + h) * kD + ch * 8;
-    cp_async16(smem_u32(sQ + swz(r, ch)), src, 16);
-  }
-  const __half* kbase = k + ((size_t)ca->tok0[i] * pv.hkv + kvh) * kD;
-  for (int c = tid; c < kKeyBlock * 16; c += blockDim.x) {
-    const int r = c >> 4, ch = c & 15, j = key0 + r;
-    const __half* src = kbase + (size_t)min(j, n0 - 1) * pv.hkv * kD + ch * 8;
-    cp_async16(smem_u32(sK + swz(r, ch)), src, j < n0 ? 16 : 0);
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-
-  const int g = lane >> 2, t = lane & 3;
-  uint32_t a[2][8][4];
-#pragma unroll
-  for (int mt = 0; mt < 2; mt++)
-#pragma unroll
-    for (int kk = 0; kk < 8; kk++) {
-      const int r = warp * 32 + mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-      ldmatrix_x4(a[mt][kk], smem_u32(sQ + swz(r, 2 * kk + (lane >> 4))));
-    }
-  const float sc = kLog2e * rsqrtf((float)kD);
-  float m_run[4], l_run[4];   // rows (mt, rr): o = 16 mt + 8 rr + g
-#pragma unroll
-  for (int x = 0; x < 4; x++) { m_run[x] = -INFINITY; l_run[x] = 0.0f; }
-  const int nkeys = min(kKeyBlock, n0 - key0);
-  for (int n16 = 0; n16 < nkeys; n16 += 16) {
-    float acc[2][2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; nt++)
-#pragma unroll
-      for (int mt = 0; mt < 2; mt++)
-#pragma unroll
-        for (int x = 0; x < 4; x++) acc[nt][mt][x] = 0.0f;
-#pragma unroll
-    for (int kk = 0; kk < 8; kk += 2) {
-#pragma unroll
-      for (int nt = 0; nt < 2; nt++) {
-        uint32_t b[4];
-        const int r = n16 + nt * 8 + (lane & 7);
-        ldmatrix_x4(b, smem_u32(sK + swz(r, 2 * kk + (lane >> 3))));
-#pragma unroll
-        for (int mt = 0; mt < 2; mt++) {
-          mma16816(acc[nt][mt], a[mt][kk], b[0], b[1]);
-          mma16816(acc[nt][mt], a[mt][kk + 1], b[2], b[3]);
-        }
-      }
-    }
-#pragma unroll
-    for (int mt = 0; mt < 2; mt++)
-#pragma unroll
-      for (int rr = 0; rr < 2; rr++) {
-        const int o = 16 * mt + 8 * rr + g, p = n0 - kObs + o;
-        float v[4];
-        float vmax = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 2; nt++)
-#pragma unroll
-          for (int e = 0; e < 2; e++) {
-            const int j = key0 + n16 + nt * 8 + 2 * t + e;
-            float x = acc[nt][mt][2 * rr + e] * sc;
-            x = (j <= p) ? x : -INFINITY;
-            v[nt * 2 + e] = x;
-            vmax = fmaxf(vmax, x);
-          }
-        const int x = mt * 2 + rr;
-        const float mn = fmaxf(m_run[x], vmax);
-        if (mn == -INFINITY) continue;
-        float l = l_run[x] * fast_exp2(m_run[x] - mn);
-#pragma unroll
-        for (int e = 0; e < 4; e++) l += fast_exp2(v[e] - mn);
-        m_run[x] = mn;
-        l_run[x] = l;
-      }
-  }
-  // merge the four lanes that share a row
-#pragma unroll
-  for (int x = 0; x < 4; x++) {
-#pragma unroll
-    for (int s = 1; s <= 2; s <<= 1) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m_run[x], s);
-      const float lo = __shfl_xor_sync(0xffffffffu, l_run[x], s);
-      const float mn = fmaxf(m_run[x], mo);
-      if (mn != -INFINITY) {
-        l_run[x] = l_run[x] * fast_exp2(m_run[x] - mn) + lo * fast_exp2(mo - mn);
-        m_run[x] = mn;
-      }
-    }
-  }
-  if (t == 0) {
-    const size_t unit = (size_t)i * pv.hkv + kvh;
-    float2* dst = partial + (unit * nkb_cap + kb) * (kObs * G) + warp * kObs;
-#pragma unroll
-    for (int x = 0; x < 4; x++) dst[16 * (x >> 1) + 8 * (x & 1) + g] = make_float2(m_run[x], l_run[x]);
-  }
-}
-
-// lse2[unit][h*32 + o] = m + log2(l) over the key blocks (log2 domain);
-// -inf for observation rows with a negative position.
-__global__ void k_prompt_lse_merge(PoolView pv, const float2* __restrict__ partial, float* lse2, int nkb_cap) {
-  if (pv.noop()) return;
-  const int unit = blockIdx.x, i = unit / pv.hkv;
-  const int rows = kObs * pv.G;
-  const int n0 = pv.call->lens[i];
-  const int nkb = (n0 + kKeyBlock - 1) / kKeyBlock;
-  for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-    float m = -INFINITY, l = 0.0f;
-    for (int kb = 0; kb < nkb; kb++) {
-      const float2 pl = partial[((size_t)unit * nkb_cap + kb) * rows + r];
-      const float mn = fmaxf(m, pl.x);
-      if (mn == -INFINITY) continue;
-      l = l * exp2f(m - mn) + pl.y * exp2f(pl.x - mn);
-      m = mn;
-    }
-    lse2[(size_t)unit * rows + r] = (l > 0.0f) ? m + log2f(l) : -INFINITY;
-  }
-}
 
 // Tier of one prompt token and its rank among same-tier tokens of the block
 // (block of kKeyBlock consecutive positions handled by 128 threads).
@@ -185,133 +36,6 @@ __device__ __forceinline__ void classify_block(const PoolView& pv, int n0, int j
   rank = tier == kTierHi ? bh0 + __popc(bh & below) : (tier == kTierLo ? bl0 + __popc(bl & below) : 0);
   if (tid == 0 && bcnt_out)
     *bcnt_out = make_int2(s_cnt[0] + s_cnt[1] + s_cnt[2] + s_cnt[3], s_cnt[4] + s_cnt[5] + s_cnt[6] + s_cnt[7]);
-}
-
-// ---------------------------------------------------------------------------
-// a2: S_j = sum_{p >= j} max_h exp(l_{h,p,j} - lse_{h,p}); exp is monotone,
-// so the max over the group's heads is taken on the exponent and one exp2
-// per (observation query, key) remains. CTA = 128 keys, 4 warps x 32 keys;
-// the warp keeps its keys as B fragments and walks all 2G row tiles.
-// ---------------------------------------------------------------------------
-template <int G>
-__global__ void __launch_bounds__(128) k_prompt_score(PoolView pv, const __half* __restrict__ k,
-                                                       const __half* __restrict__ q_obs,
-                                                       const float* __restrict__ lse2, float* score_out,
-                                                       uint16_t* tokinfo, int2* bcnt, int nkb_cap) {
-  if (pv.noop()) return;
-  const int kb = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
-  const CallArgs* ca = pv.call;
-  const int n0 = ca->lens[i];
-  const int key0 = kb * kKeyBlock;
-  if (key0 >= n0) return;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sQ = smem;                          // 32*G rows x 256 B
-  uint8_t* sK = smem + 32 * G * 256;           // 128 rows x 256 B
-  float* sL = (float*)(sK + kKeyBlock * 256);  // 32*G lse2
-  float* sS = sL + 32 * G;                     // 128 scores
-  __shared__ int s_cnt[8];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Hq = pv.hkv * G;
-  const size_t unit = (size_t)i * pv.hkv + kvh;
-  for (int c = tid; c < 32 * G * 16; c += blockDim.x) {
-    const int r = c >> 4, ch = c & 15, h = r >> 5, o = r & 31;
-    const __half* src = q_obs + (((size_t)i * kObs + o) * Hq + (size_t)kvh * G + h) * kD + ch * 8;
-    cp_async16(smem_u32(sQ + swz(r, ch)), src, 16);
-  }
-  const __half* kbase = k + ((size_t)ca->tok0[i] * pv.hkv + kvh) * kD;
-  for (int c = tid; c < kKeyBlock * 16; c += blockDim.x) {
-    const int r = c >> 4, ch = c & 15, j = key0 + r;
-    const __half* src = kbase + (size_t)min(j, n0 - 1) * pv.hkv * kD + ch * 8;
-    cp_async16(smem_u32(sK + swz(r, ch)), src, j < n0 ? 16 : 0);
-  }
-  cp_async_commit();
-  for (int r = tid; r < 32 * G; r += blockDim.x) sL[r] = lse2[unit * 32 * G + r];
-  cp_async_wait<0>();
-  __syncthreads();
-
-  const int g = lane >> 2, t = lane & 3;
-  uint32_t b[4][8][2];
-#pragma unroll
-  for (int nt = 0; nt < 4; nt++)
-#pragma unroll
-    for (int kk = 0; kk < 8; kk += 2) {
-      uint32_t r4[4];
-      const int r = warp * 32 + nt * 8 + (lane & 7);
-      ldmatrix_x4(r4, smem_u32(sK + swz(r, 2 * kk + (lane >> 3))));
-      b[nt][kk][0] = r4[0]; b[nt][kk][1] = r4[1];
-      b[nt][kk + 1][0] = r4[2]; b[nt][kk + 1][1] = r4[3];
-    }
-  const float sc = kLog2e * rsqrtf((float)kD);
-  float ymax[2][2][4][2];   // [half][rr][nt][e]
-#pragma unroll
-  for (int hf = 0; hf < 2; hf++)
-#pragma unroll
-    for (int rr = 0; rr < 2; rr++)
-#pragma unroll
-      for (int nt = 0; nt < 4; nt++) { ymax[hf][rr][nt][0] = -INFINITY; ymax[hf][rr][nt][1] = -INFINITY; }
-#pragma unroll 1
-  for (int h = 0; h < G; h++) {
-#pragma unroll
-    for (int hf = 0; hf < 2; hf++) {
-      float acc[4][4];
-#pragma unroll
-      for (int nt = 0; nt < 4; nt++)
-#pragma unroll
-        for (int x = 0; x < 4; x++) acc[nt][x] = 0.0f;
-#pragma unroll
-      for (int kk = 0; kk < 8; kk++) {
-        uint32_t a[4];
-        const int r = h * 32 + hf * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-        ldmatrix_x4(a, smem_u32(sQ + swz(r, 2 * kk + (lane >> 4))));
-#pragma unroll
-        for (int nt = 0; nt < 4; nt++) mma16816(acc[nt], a, b[nt][kk][0], b[nt][kk][1]);
-      }
-#pragma unroll
-      for (int rr = 0; rr < 2; rr++) {
-        const int o = 16 * hf + 8 * rr + g;
-        const float l2 = sL[h * 32 + o];
-#pragma unroll
-        for (int nt = 0; nt < 4; nt++)
-#pragma unroll
-          for (int e = 0; e < 2; e++)
-            ymax[hf][rr][nt][e] = fmaxf(ymax[hf][rr][nt][e], __fmaf_rn(acc[nt][2 * rr + e], sc, -l2));
-      }
-    }
-  }
-  float ssum[4][2];
-#pragma unroll
-  for (int nt = 0; nt < 4; nt++)
-#pragma unroll
-    for (int e = 0; e < 2; e++) {
-      const int j = key0 + warp * 32 + nt * 8 + 2 * t + e;
-      float s = 0.0f;
-#pragma unroll
-      for (int hf = 0; hf < 2; hf++)
-#pragma unroll
-        for (int rr = 0; rr < 2; rr++) {
-          const int p = n0 - kObs + 16 * hf + 8 * rr + g;
-          if (j <= p) s += exp2f(ymax[hf][rr][nt][e]);
-        }
-#pragma unroll
-      for (int sh = 4; sh <= 16; sh <<= 1) s += __shfl_xor_sync(0xffffffffu, s, sh);
-      ssum[nt][e] = s;
-    }
-  if (g == 0) {
-#pragma unroll
-    for (int nt = 0; nt < 4; nt++)
-#pragma unroll
-      for (int e = 0; e < 2; e++) sS[warp * 32 + nt * 8 + 2 * t + e] = ssum[nt][e];
-  }
-  __syncthreads();
-  const int j = key0 + tid;
-  const float s = sS[tid];
-  int tier, rank;
-  classify_block(pv, n0, j, s, tier, rank, s_cnt, bcnt + unit * nkb_cap + kb);
-  if (j < n0) {
-    const size_t tok = (size_t)(ca->tok0[i] + j) * pv.hkv + kvh;
-    score_out[tok] = s;
-    tokinfo[tok] = (uint16_t)((rank << 2) | tier);
-  }
 }
 
 // Tier from caller-given scores (score_in), same rule and ranks.
@@ -520,50 +244,20 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
 cudaError_t launch_prompt_plan(Pool& P, int layer, int n_req, cudaStream_t st);
 cudaError_t configure_attention();
 cudaError_t configure_alloc();
-
-template <int G>
-static int lse_smem() { return 32 * G * 256 + kKeyBlock * 256; }
-template <int G>
-static int score_smem() { return 32 * G * 256 + kKeyBlock * 256 + 32 * G * 4 + kKeyBlock * 4; }
-
-template <int G>
-static cudaError_t launch_scoring(Pool& P, dim3 grid, const __half* k, const __half* q_obs, float* score_out,
-                                  cudaStream_t st) {
-  const Scratch& s = P.sc;
-  k_prompt_lse<G><<<grid, 32 * G, lse_smem<G>(), st>>>(P.pv, k, q_obs, s.partial, s.nkb_cap);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const unsigned units = grid.y * grid.z;
-  k_prompt_lse_merge<<<units, 256, 0, st>>>(P.pv, s.partial, s.lse2, s.nkb_cap);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_prompt_score<G><<<grid, 128, score_smem<G>(), st>>>(P.pv, k, q_obs, s.lse2, score_out, s.tokinfo, s.bcnt,
-                                                        s.nkb_cap);
-  return cudaGetLastError();
-}
-
-template <int G>
-static cudaError_t configure_g() {
-  cudaError_t e = cudaFuncSetAttribute(k_prompt_lse<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, lse_smem<G>());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_prompt_score<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, score_smem<G>());
-}
+cudaError_t configure_prompt_tc();
+cudaError_t launch_scoring_tc(Pool& P, const __half* k, const __half* q_obs, long long n_tok, int n_req,
+                              float* score_out, cudaStream_t st);
 
 cudaError_t configure_kernels() {
   cudaError_t e;
-  if ((e = configure_g<1>()) != cudaSuccess) return e;
-  if ((e = configure_g<2>()) != cudaSuccess) return e;
-  if ((e = configure_g<3>()) != cudaSuccess) return e;
-  if ((e = configure_g<4>()) != cudaSuccess) return e;
-  if ((e = configure_g<5>()) != cudaSuccess) return e;
-  if ((e = configure_g<6>()) != cudaSuccess) return e;
-  if ((e = configure_g<7>()) != cudaSuccess) return e;
-  if ((e = configure_g<8>()) != cudaSuccess) return e;
+  if ((e = configure_prompt_tc()) != cudaSuccess) return e;
   if ((e = configure_alloc()) != cudaSuccess) return e;
   return configure_attention();
 }
 
-cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, const __half* k, const __half* v,
-                          const __half* q_obs, const float* scores_in, float* scores_out, cudaStream_t st) {
+cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long n_tok, const __half* k,
+                          const __half* v, const __half* q_obs, const float* scores_in, float* scores_out,
+                          cudaStream_t st) {
   const Scratch& s = P.sc;
   const int nkb = (max_len + kKeyBlock - 1) / kKeyBlock;
   const dim3 grid(nkb, P.pv.hkv, n_req);
@@ -575,16 +269,7 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, const __ha
     score_src = scores_in;
   } else {
     float* so = scores_out ? scores_out : s.score;
-    switch (P.pv.G) {
-      case 1: e = launch_scoring<1>(P, grid, k, q_obs, so, st); break;
-      case 2: e = launch_scoring<2>(P, grid, k, q_obs, so, st); break;
-      case 3: e = launch_scoring<3>(P, grid, k, q_obs, so, st); break;
-      case 4: e = launch_scoring<4>(P, grid, k, q_obs, so, st); break;
-      case 5: e = launch_scoring<5>(P, grid, k, q_obs, so, st); break;
-      case 6: e = launch_scoring<6>(P, grid, k, q_obs, so, st); break;
-      case 7: e = launch_scoring<7>(P, grid, k, q_obs, so, st); break;
-      default: e = launch_scoring<8>(P, grid, k, q_obs, so, st); break;
-    }
+    e = launch_scoring_tc(P, k, q_obs, n_tok, n_req, so, st);
     score_src = so;
   }
   if (e != cudaSuccess) return e;
