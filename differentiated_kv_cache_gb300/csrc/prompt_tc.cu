@@ -310,34 +310,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int i = x.i, n0 = ca->lens[i], key0 = x.kb * kKeyBlock;
       const int unit = i * hkv + x.kvh;
       if (!SCORE) {
+        // the row's 128 logits of the tile: max first, then one exp2 each;
+        // eight independent partial maxima and sums keep the chains short
         float m[C::MT], l[C::MT];
+        const bool full = key0 + kKeyBlock - 1 <= n0 - kObs;    // no key after any query row's position
 #pragma unroll
         for (int mt = 0; mt < C::MT; mt++) {
-          m[mt] = -INFINITY;
-          l[mt] = 0.0f;
           const int r = 128 * mt + row;                  // query row (o, h): r = o G + h
           const int p = n0 - kObs + r / G;               // its position
+          float v[kKeyBlock];
 #pragma unroll
-          for (int c0 = 0; c0 < kKeyBlock; c0 += 32) {
-            float v[32];
-            tmem_ld32(tl + ab * C::ACC + 128 * mt + c0, v);
-            float cm = -INFINITY;
+          for (int c0 = 0; c0 < kKeyBlock; c0 += 32) tmem_ld32_nowait(tl + ab * C::ACC + 128 * mt + c0, v + c0);
+          tmem_wait_ld();
+          if (mt == C::MT - 1) {
+            tc_fence_before();
+            mbar_arrive(aempty(ab));                     // the accumulator is free for the MMA after next
+          }
+          if (!full) {
 #pragma unroll
-            for (int e = 0; e < 32; e++) {
-              v[e] = key0 + c0 + e <= p ? v[e] * sc : -INFINITY;
-              cm = fmaxf(cm, v[e]);
-            }
-            const float mn = fmaxf(m[mt], cm);
-            if (mn == -INFINITY) continue;
-            float s = l[mt] * fast_exp2(m[mt] - mn);
+            for (int e = 0; e < kKeyBlock; e++)
+              if (key0 + e > p) v[e] = -INFINITY;
+          }
+          float pm[8];
 #pragma unroll
-            for (int e = 0; e < 32; e++) s += fast_exp2(v[e] - mn);
-            m[mt] = mn;
-            l[mt] = s;
+          for (int e = 0; e < 8; e++) pm[e] = v[e];
+#pragma unroll
+          for (int e = 8; e < kKeyBlock; e++) pm[e & 7] = fmaxf(pm[e & 7], v[e]);
+          const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                 fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+          m[mt] = mx * sc;                               // sc > 0: the max commutes with the scale
+          l[mt] = 0.0f;
+          if (mx != -INFINITY) {
+            float ps[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) ps[e] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < kKeyBlock; e++) ps[e & 7] += fast_exp2(__fmaf_rn(v[e], sc, -m[mt]));
+            l[mt] = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
           }
         }
-        tc_fence_before();
-        mbar_arrive(aempty(ab));
 #pragma unroll
         for (int mt = 0; mt < C::MT; mt++) {
           const int r = 128 * mt + row;
@@ -354,23 +365,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           lse_unit = unit;
         }
         const int j = key0 + row;
-        float s = 0.0f, y = -INFINITY;
+        const bool full = j <= n0 - kObs;                // the key precedes every observation query
+        // columns (o, h) = o G + h, 128 at a time: max over the heads of one
+        // observation query, then one exp2 per query into four partial sums
+        float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float y = -INFINITY;
 #pragma unroll
-        for (int c0 = 0; c0 < kObs * G; c0 += 32) {
-          float v[32];
-          tmem_ld32(tl + ab * C::ACC + c0, v);
+        for (int c0 = 0; c0 < kObs * G; c0 += 128) {
+          constexpr int W = kObs * G < 128 ? kObs * G : 128;
+          float v[W];
 #pragma unroll
-          for (int e = 0; e < 32; e++) {
-            const int col = c0 + e, o = col / G, h = col % G;    // column = query row (o, h)
+          for (int c = 0; c < W; c += 32)
+            if (c0 + c < kObs * G) tmem_ld32_nowait(tl + ab * C::ACC + c0 + c, v + c);
+          tmem_wait_ld();
+          if (c0 + W >= kObs * G) {
+            tc_fence_before();
+            mbar_arrive(aempty(ab));
+          }
+#pragma unroll
+          for (int e = 0; e < W; e++) {
+            const int col = c0 + e, o = col / G, h = col % G;
+            if (col >= kObs * G) break;
             y = fmaxf(y, __fmaf_rn(v[e], sc, -s_lse[h * kObs + o]));
             if (h == G - 1) {
-              if (j <= n0 - kObs + o) s += exp2f(y);
+              if (full || j <= n0 - kObs + o) ps[o & 3] += exp2f(y);
               y = -INFINITY;
             }
           }
         }
-        tc_fence_before();
-        mbar_arrive(aempty(ab));
+        const float s = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         int tier, rank;
         classify_epi(pv, n0, j, s, tier, rank, s_cnt + 8 * ab, bcnt + (size_t)unit * nkb_cap + x.kb);
         if (j < n0) {
