@@ -80,55 +80,82 @@ __global__ void __launch_bounds__(128) k_prompt_scatter(PoolView pv, const uint1
 }
 
 // ---------------------------------------------------------------------------
-// a4: quantize + pack. A warp handles groups of 4 consecutive ranks of one
-// (head, tier): 8 lanes per token, 16 features per lane. A group fills two
-// whole value pair-rows (hi) or one value quad-row (lo); the value words are
-// assembled in shared memory and written as full 128-byte rows. Each warp
-// takes kPackGroups groups in turn and keeps the loads ahead of the math: the
-// positions of the group after next and the K/V rows of the next group are
-// in flight while a group is quantized and stored.
+// a4: quantize + pack, one kernel per tier (HI: K8V4, LO: K4V2). A warp
+// handles groups of 8 consecutive ranks of one head: 4 lanes per token, 32
+// features per lane. A group fills whole value rows (4 pair-rows hi, 2
+// quad-rows lo); the value words are assembled in shared memory and written
+// as full 128-byte rows. Each warp takes kPackGroups groups in turn and keeps
+// the loads ahead of the math: the positions of the group after next and the
+// K/V rows of the next group are in flight while a group is quantized and
+// stored. The codes follow qcode (the oracle's arithmetic); a zero scale has
+// inv = 0, which gives code 0 without a branch.
 // ---------------------------------------------------------------------------
-constexpr int kPackGroups = 4;
+constexpr int kPackGroups = 4;   // groups per warp
+constexpr int kPackTok = 8;      // tokens per group
 
+// codes of the pair (x0, x1), b-bit, under q (qcode's arithmetic)
+template <int B>
+__device__ __forceinline__ void qcode2_t(float x0, float x1, const QParams& q, uint32_t& c0, uint32_t& c1) {
+  const uint64_t t = mul_f32x2(sub_f32x2(f32x2(x0, x1), f32x2(q.z, q.z)), f32x2(q.inv, q.inv));
+  c0 = rint_sat_u8(__uint_as_float((uint32_t)t));
+  c1 = rint_sat_u8(__uint_as_float((uint32_t)(t >> 32)));
+  if (B < 8) {
+    c0 = min(c0, (1u << B) - 1u);
+    c1 = min(c1, (1u << B) - 1u);
+  }
+}
+
+template <bool HI>
 __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* __restrict__ k,
                                                       const __half* __restrict__ v,
                                                       const float* __restrict__ score,
                                                       const int* __restrict__ rank2pos,
                                                       const int4* __restrict__ unit_info,
                                                       const int* __restrict__ grant_ids, int grant_cap) {
+  constexpr int KB = HI ? 8 : 4, VB = HI ? 4 : 2, GSZ = 8 / VB;   // GSZ: tokens per value row
   if (pv.noop()) return;
-  __shared__ uint32_t s_vw[8][4][32];     // [warp][token][value word] code bits of the token
-  const int unit = blockIdx.y, tier = blockIdx.z ? kTierHi : kTierLo;
+  __shared__ uint32_t s_vw[8][kPackTok][32];   // [warp][token][value word] code bits of the token
+  const int unit = blockIdx.y;
   const int i = unit / pv.hkv, kvh = unit % pv.hkv;
-  const int4 ui = unit_info[unit];        // grant pages, hi count, lo count, -
-  const int count = tier == kTierHi ? ui.y : ui.z;
+  const int4 ui = unit_info[unit];             // grant pages, hi count, lo count, -
+  const int count = HI ? ui.y : ui.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // group x of this warp starts at rank base + 32 x
-  const int base = (blockIdx.x * kPackGroups * 8 + warp) * 4;
+  // group x of this warp starts at rank base + 64 x
+  const int base = (blockIdx.x * kPackGroups * 8 + warp) * kPackTok;
   if (base >= count) return;
-  const TierGeom& tg = tier == kTierHi ? pv.hi : pv.lo;
-  const int kbits = tier == kTierHi ? 8 : 4, vbits = tier == kTierHi ? 4 : 2;
-  const int e = lane >> 3, q = lane & 7;  // token e of the 4, features 16q..16q+15
+  const TierGeom& tg = HI ? pv.hi : pv.lo;
+  const int e = lane >> 2, q = lane & 3;       // token e of the 8, features 32q..32q+31
   const CallArgs* ca = pv.call;
-  const int* r2p = rank2pos + ((size_t)unit * 2 + (tier == kTierHi ? 1 : 0)) * pv.max_seq;
+  const int* r2p = rank2pos + ((size_t)unit * 2 + (HI ? 1 : 0)) * pv.max_seq;
   const size_t tok_base = (size_t)ca->tok0[i];
   const int gcnt = ui.x;
-  auto pos_of = [&](int x) { const int r = base + 32 * x + e; return r < count ? __ldg(r2p + r) : -1; };
-  auto load_kv = [&](int j, uint4 (&kv)[4]) {
+  auto pos_of = [&](int x) {
+    const int r = base + 8 * kPackTok * x + e;
+    return r < count ? __ldg(r2p + r) : -1;
+  };
+  auto load_kv = [&](int j, uint4 (&kv)[8]) {
     if (j >= 0) {
       const size_t tok = (tok_base + j) * pv.hkv + kvh;
-      const uint4* kp = reinterpret_cast<const uint4*>(k + tok * kD + q * 16);
-      const uint4* vp = reinterpret_cast<const uint4*>(v + tok * kD + q * 16);
-      kv[0] = __ldg(kp); kv[1] = __ldg(kp + 1); kv[2] = __ldg(vp); kv[3] = __ldg(vp + 1);
+      const uint4* kp = reinterpret_cast<const uint4*>(k + tok * kD + q * 32);
+      const uint4* vp = reinterpret_cast<const uint4*>(v + tok * kD + q * 32);
+#pragma unroll
+      for (int y = 0; y < 4; y++) {
+        kv[y] = __ldg(kp + y);
+        kv[4 + y] = __ldg(vp + y);
+      }
     } else {
-      kv[0] = kv[1] = kv[2] = kv[3] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int y = 0; y < 8; y++) kv[y] = make_uint4(0, 0, 0, 0);
     }
   };
   int j_cur = pos_of(0), j_next = pos_of(1);
-  uint4 kv_cur[4], kv_next[4];
+  uint4 kv_cur[8], kv_next[8];
   load_kv(j_cur, kv_cur);
+  // bit offset of this token's slot inside a value word
+  const int slot_e = e % GSZ;
+  const int eb = VB == 4 ? 16 * slot_e : 16 * (slot_e & 1) + 2 * (slot_e >> 1);
   for (int x = 0; x < kPackGroups; x++) {
-    const int r0 = base + 32 * x;
+    const int r0 = base + 8 * kPackTok * x;
     if (r0 >= count) break;
     int j_after = -1;
     if (x + 1 < kPackGroups) load_kv(j_next, kv_next);
@@ -136,81 +163,76 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
     const int r = r0 + e;
     const bool valid = r < count;
     const int j = j_cur;
-    float kx[16], vx[16];
+    const __half2* kh = reinterpret_cast<const __half2*>(&kv_cur[0]);   // 16 pairs
+    const __half2* vh = reinterpret_cast<const __half2*>(&kv_cur[4]);
     float kmn, kmx, vmn, vmx;
     {
-      const __half2* kh = reinterpret_cast<const __half2*>(&kv_cur[0]);   // 8 pairs: kv_cur[0..1]
-      const __half2* vh = reinterpret_cast<const __half2*>(&kv_cur[2]);
       __half2 kmn2 = kh[0], kmx2 = kh[0], vmn2 = vh[0], vmx2 = vh[0];
 #pragma unroll
-      for (int y = 1; y < 8; y++) {   // min / max of fp16 values are exact
-        kmn2 = __hmin2(kmn2, kh[y]); kmx2 = __hmax2(kmx2, kh[y]);
-        vmn2 = __hmin2(vmn2, vh[y]); vmx2 = __hmax2(vmx2, vh[y]);
+      for (int y = 1; y < 16; y++) {   // min / max of fp16 values are exact
+        kmn2 = __hmin2(kmn2, kh[y]);
+        kmx2 = __hmax2(kmx2, kh[y]);
+        vmn2 = __hmin2(vmn2, vh[y]);
+        vmx2 = __hmax2(vmx2, vh[y]);
       }
       kmn = fminf(__low2float(kmn2), __high2float(kmn2));
       kmx = fmaxf(__low2float(kmx2), __high2float(kmx2));
       vmn = fminf(__low2float(vmn2), __high2float(vmn2));
       vmx = fmaxf(__low2float(vmx2), __high2float(vmx2));
-#pragma unroll
-      for (int y = 0; y < 8; y++) {
-        const float2 kf = __half22float2(kh[y]), vf = __half22float2(vh[y]);
-        kx[2 * y] = kf.x; kx[2 * y + 1] = kf.y;
-        vx[2 * y] = vf.x; vx[2 * y + 1] = vf.y;
-      }
     }
-    // every lane takes part in the group reductions; invalid lanes hold zeros
+    // every lane takes part in the token reductions; invalid lanes hold zeros
 #pragma unroll
-    for (int sh = 1; sh <= 4; sh <<= 1) {
-      kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, sh, 8));
-      kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, sh, 8));
-      vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, sh, 8));
-      vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, sh, 8));
+    for (int sh = 1; sh <= 2; sh <<= 1) {
+      kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, sh, 4));
+      kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, sh, 4));
+      vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, sh, 4));
+      vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, sh, 4));
     }
-    const QParams kq = qparams(kmn, kmx, kbits), vq = qparams(vmn, vmx, vbits);
-    // the token's bits of value words 4q .. 4q+3 (feature 4w+i, slot e of the row)
-    const int gsz = 8 / vbits;
-    const int eb = vbits == 4 ? 16 * (e % 2) : 16 * (e & 1) + 2 * (e >> 1);
-    uint32_t vw[4];
+    const QParams kq = qparams(kmn, kmx, KB), vq = qparams(vmn, vmx, VB);
+    // the token's bits of value words 8q .. 8q+7 (features 4w .. 4w+3)
+    __syncwarp();                              // the previous group's value rows are written
 #pragma unroll
-    for (int w = 0; w < 4; w++) {
+    for (int w = 0; w < 8; w++) {
+      const float2 a = __half22float2(vh[2 * w]), b = __half22float2(vh[2 * w + 1]);
       uint32_t c0, c1, c2, c3;
-      qcode2(vx[4 * w], vx[4 * w + 1], vq, vbits, c0, c1);
-      qcode2(vx[4 * w + 2], vx[4 * w + 3], vq, vbits, c2, c3);
-      vw[w] = valid ? (c0 | (c1 << 4) | (c2 << 8) | (c3 << 12)) << eb : 0u;
+      qcode2_t<VB>(a.x, a.y, vq, c0, c1);
+      qcode2_t<VB>(b.x, b.y, vq, c2, c3);
+      s_vw[warp][e][8 * q + w] = valid ? (c0 | (c1 << 4) | (c2 << 8) | (c3 << 12)) << eb : 0u;
     }
-    __syncwarp();                        // the previous group's value rows are written
-#pragma unroll
-    for (int w = 0; w < 4; w++) s_vw[warp][e][4 * q + w] = vw[w];
     if (valid) {
       // page and slot of rank r: hi from the left of the grant, lo from the right
-      const int pidx = tier == kTierHi ? r / tg.t : gcnt - 1 - r / tg.t;
-      const int slot = r % tg.t;
+      const int pidx = HI ? tg.div(r) : gcnt - 1 - tg.div(r);
+      const int slot = r - tg.div(r) * tg.t;
       uint8_t* page = pv.page(grant_ids[(size_t)unit * grant_cap + pidx]);
       uint8_t* krow = page + tg.off[0] + slot * tg.kbytes;
-      if (kbits == 8) {
+      if (HI) {
+        uint32_t w[8];
+#pragma unroll
+        for (int y = 0; y < 8; y++) {
+          const float2 a = __half22float2(kh[2 * y]), b = __half22float2(kh[2 * y + 1]);
+          uint32_t c0, c1, c2, c3;
+          qcode2_t<8>(a.x, a.y, kq, c0, c1);
+          qcode2_t<8>(b.x, b.y, kq, c2, c3);
+          w[y] = __byte_perm(c0 | (c2 << 16), c1 | (c3 << 16), 0x6240);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(krow + 32 * q);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else {
         uint32_t w[4];
 #pragma unroll
         for (int y = 0; y < 4; y++) {
-          uint32_t c0, c1, c2, c3;
-          qcode2(kx[4 * y], kx[4 * y + 1], kq, 8, c0, c1);
-          qcode2(kx[4 * y + 2], kx[4 * y + 3], kq, 8, c2, c3);
-          w[y] = __byte_perm(c0 | (c2 << 16), c1 | (c3 << 16), 0x6240);
-        }
-        *reinterpret_cast<uint4*>(krow + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
-      } else {
-        uint32_t w[2];
-#pragma unroll
-        for (int y = 0; y < 2; y++) {
           uint32_t acc = 0;
 #pragma unroll
-          for (int z = 0; z < 8; z += 2) {
+          for (int z = 0; z < 4; z++) {
+            const float2 a = __half22float2(kh[4 * y + z]);
             uint32_t c0, c1;
-            qcode2(kx[8 * y + z], kx[8 * y + z + 1], kq, 4, c0, c1);
-            acc |= (c0 | (c1 << 4)) << (4 * z);
+            qcode2_t<4>(a.x, a.y, kq, c0, c1);
+            acc |= (c0 | (c1 << 4)) << (8 * z);
           }
           w[y] = acc;
         }
-        *reinterpret_cast<uint2*>(krow + 8 * q) = make_uint2(w[0], w[1]);
+        *reinterpret_cast<uint4*>(krow + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       if (q == 0) {
         const size_t tok = (tok_base + j) * pv.hkv + kvh;
@@ -221,22 +243,23 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
       }
     }
     __syncwarp();
-    // value rows: hi = 2 pair-rows (tokens 0,1 and 2,3), lo = 1 quad-row
-    const int nrows = 4 / gsz;
-    for (int row = 0; row < nrows; row++) {
-      const int rfirst = r0 + row * gsz;
+    // value rows: GSZ tokens each (4 pair-rows hi, 2 quad-rows lo)
+#pragma unroll
+    for (int row = 0; row < kPackTok / GSZ; row++) {
+      const int rfirst = r0 + row * GSZ;
       if (rfirst >= count) break;
-      const int pidx = tier == kTierHi ? rfirst / tg.t : gcnt - 1 - rfirst / tg.t;
-      const int slot0 = rfirst % tg.t;
+      const int pidx = HI ? tg.div(rfirst) : gcnt - 1 - tg.div(rfirst);
+      const int slot0 = rfirst - tg.div(rfirst) * tg.t;
       uint8_t* page = pv.page(grant_ids[(size_t)unit * grant_cap + pidx]);
       uint32_t word = 0;
-      for (int ee = 0; ee < gsz; ee++) word |= s_vw[warp][row * gsz + ee][lane];
-      *reinterpret_cast<uint32_t*>(page + tg.off[1] + (slot0 / gsz) * 128 + 4 * lane) = word;
+#pragma unroll
+      for (int ee = 0; ee < GSZ; ee++) word |= s_vw[warp][row * GSZ + ee][lane];
+      *reinterpret_cast<uint32_t*>(page + tg.off[1] + (slot0 / GSZ) * 128 + 4 * lane) = word;
     }
     j_cur = j_next;
     j_next = j_after;
 #pragma unroll
-    for (int y = 0; y < 4; y++) kv_cur[y] = kv_next[y];
+    for (int y = 0; y < 8; y++) kv_cur[y] = kv_next[y];
   }
 }
 
@@ -276,8 +299,12 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long 
   if ((e = launch_prompt_plan(P, layer, n_req, st)) != cudaSuccess) return e;
   k_prompt_scatter<<<grid, 128, 0, st>>>(P.pv, s.tokinfo, s.bbase, s.rank2pos, s.nkb_cap);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const dim3 gpack((max_len + 32 * kPackGroups - 1) / (32 * kPackGroups), n_req * P.pv.hkv, 2);
-  k_prompt_pack<<<gpack, 256, 0, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info, s.grant_ids, s.grant_cap);
+  const dim3 gpack((max_len + 8 * kPackTok * kPackGroups - 1) / (8 * kPackTok * kPackGroups), n_req * P.pv.hkv);
+  k_prompt_pack<true><<<gpack, 256, 0, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info, s.grant_ids,
+                                             s.grant_cap);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_prompt_pack<false><<<gpack, 256, 0, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info, s.grant_ids,
+                                              s.grant_cap);
   return cudaGetLastError();
 }
 
