@@ -28,9 +28,10 @@
 
 namespace dkv {
 
-constexpr int kTcThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kTcEpi = 128;          // epilogue threads
+constexpr int kTcThreads = 320;      // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kTcEpi = 256;          // epilogue threads: two per accumulator row
 constexpr int kTcBarEpi = 1;         // named barrier of the epilogue warps
+constexpr int kTcBarRow = 2;         // named barrier of the first epilogue half (one thread per row)
 
 template <int G>
 struct TcCfg {
@@ -49,7 +50,8 @@ struct TcCfg {
 
 template <int G>
 static int tc_smem_bytes(int n_req) {
-  return 1024 + TcCfg<G>::OFF_MISC + 8 * (2 * TcCfg<G>::KS + 8) + 16 + 4 * (n_req + 1) + 4 * kObs * G + 64;
+  return 1024 + TcCfg<G>::OFF_MISC + 8 * (2 * TcCfg<G>::KS + 8) + 16 + 4 * (n_req + 1) + 4 * kObs * G + 64 +
+         8 * 2 * 2 * 128 + 16;
 }
 
 // lse2[unit][h*32 + o] = m + log2(l) over the key tiles' partials (log2
@@ -73,9 +75,9 @@ __global__ void k_prompt_lse_merge(PoolView pv, const float2* __restrict__ parti
   }
 }
 
-// Tier and in-block rank of key j (score s) over the epilogue's 128 threads
-// (one key each; warp w holds keys 32 (w % 4) ..), the rule of the CUDA-core
-// classification; cnt: 8 ints of shared memory.
+// Tier and in-block rank of key j (score s) over the first epilogue half's
+// 128 threads (one key each; warp w holds keys 32 (w % 4) ..), the rule of
+// the CUDA-core classification; cnt: 8 ints of shared memory.
 __device__ __forceinline__ void classify_epi(const PoolView& pv, int n0, int j, float s, int& tier, int& rank,
                                              int* cnt, int2* bcnt_out) {
   const int et = threadIdx.x - 64, lane = et & 31, ew = (threadIdx.x >> 5) & 3;
@@ -94,7 +96,7 @@ __device__ __forceinline__ void classify_epi(const PoolView& pv, int n0, int j, 
     cnt[ew] = __popc(bh);
     cnt[4 + ew] = __popc(bl);
   }
-  named_sync(kTcBarEpi, kTcEpi);
+  named_sync(kTcBarRow, 128);
   int bh0 = 0, bl0 = 0;
   for (int w = 0; w < ew; w++) {
     bh0 += cnt[w];
@@ -132,6 +134,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const CallArgs* ca = pv.call;
   const int n_req = ca->n_req, hkv = pv.hkv;
   float* s_lse = reinterpret_cast<float*>(s_roff + n_req + 1);   // [32 G] lse2 of the current head (a2)
+  // [2][MT][128] partial (max, sum) of the second epilogue half (a1), or
+  // [2][128] partial scores (a2), by accumulator
+  float2* s_half = reinterpret_cast<float2*>(
+      (reinterpret_cast<uintptr_t>(s_lse + kObs * G) + 15) & ~uintptr_t(15));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // tiles of the call: request i holds hkv heads x nkb(i) key tiles
@@ -294,33 +300,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (issued >= 0) mbar_wait_bounded(afull(issued & 1), (issued >> 1) & 1);
     }
   } else {
-    // ---- epilogue: warps 2..5, thread = accumulator row (lane group warp % 4) ----
-    const int lg = warp & 3, row = 32 * lg + lane;
+    // ---- epilogue: warps 2..9; thread = accumulator row (lane group warp % 4)
+    // and half hf of the row's columns ----
+    const int lg = warp & 3, row = 32 * lg + lane, hf = (warp - 2) >> 2;
     const uint32_t tl = tbase + ((uint32_t)(32 * lg) << 16);
     const float sc = 1.4426950408889634f * rsqrtf((float)kD);
     Tile x = locate(t0);
     int lse_unit = -1;
     for (int it = 0; it < t1 - t0; it++, next(x)) {
       const int ab = it & 1;
-      bool ok = mbar_wait_bounded(afull(ab), (it >> 1) & 1);
+      // on expiry the tile still runs through its barriers (with whatever the
+      // accumulator holds); the combine barrier below makes one decision for
+      // all epilogue threads, so that none is left waiting at a barrier
+      const bool ok = mbar_wait_bounded(afull(ab), (it >> 1) & 1);
       if (!ok) fail(6);
-      // one decision for all epilogue threads, so that none is left at a barrier
-      if (!named_all(kTcBarEpi, kTcEpi, ok && !failed())) break;
       tc_fence_after();
       const int i = x.i, n0 = ca->lens[i], key0 = x.kb * kKeyBlock;
       const int unit = i * hkv + x.kvh;
       if (!SCORE) {
-        // the row's 128 logits of the tile: max first, then one exp2 each;
+        // keys 64 hf .. 64 hf + 63 of the row: max first, then one exp2 each;
         // eight independent partial maxima and sums keep the chains short
+        constexpr int NK = kKeyBlock / 2;
         float m[C::MT], l[C::MT];
         const bool full = key0 + kKeyBlock - 1 <= n0 - kObs;    // no key after any query row's position
 #pragma unroll
         for (int mt = 0; mt < C::MT; mt++) {
           const int r = 128 * mt + row;                  // query row (o, h): r = o G + h
           const int p = n0 - kObs + r / G;               // its position
-          float v[kKeyBlock];
+          const int kc = key0 + NK * hf;                 // first key of the half
+          float v[NK];
 #pragma unroll
-          for (int c0 = 0; c0 < kKeyBlock; c0 += 32) tmem_ld32_nowait(tl + ab * C::ACC + 128 * mt + c0, v + c0);
+          for (int c0 = 0; c0 < NK; c0 += 32) tmem_ld32_nowait(tl + ab * C::ACC + 128 * mt + NK * hf + c0, v + c0);
           tmem_wait_ld();
           if (mt == C::MT - 1) {
             tc_fence_before();
@@ -328,14 +338,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           if (!full) {
 #pragma unroll
-            for (int e = 0; e < kKeyBlock; e++)
-              if (key0 + e > p) v[e] = -INFINITY;
+            for (int e = 0; e < NK; e++)
+              if (kc + e > p) v[e] = -INFINITY;
           }
           float pm[8];
 #pragma unroll
           for (int e = 0; e < 8; e++) pm[e] = v[e];
 #pragma unroll
-          for (int e = 8; e < kKeyBlock; e++) pm[e & 7] = fmaxf(pm[e & 7], v[e]);
+          for (int e = 8; e < NK; e++) pm[e & 7] = fmaxf(pm[e & 7], v[e]);
           const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                  fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
           m[mt] = mx * sc;                               // sc > 0: the max commutes with the scale
@@ -345,61 +355,84 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; e++) ps[e] = 0.0f;
 #pragma unroll
-            for (int e = 0; e < kKeyBlock; e++) ps[e & 7] += fast_exp2(__fmaf_rn(v[e], sc, -m[mt]));
+            for (int e = 0; e < NK; e++) ps[e & 7] += fast_exp2(__fmaf_rn(v[e], sc, -m[mt]));
             l[mt] = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
           }
         }
+        // the two halves of each row combine in the first half
+        float2* hb = s_half + ab * C::MT * 128;
+        if (hf == 1) {
 #pragma unroll
-        for (int mt = 0; mt < C::MT; mt++) {
-          const int r = 128 * mt + row;
-          if (r < kObs * G) {
-            const int o = r / G, h = r % G;
-            partial[((size_t)unit * nkb_cap + x.kb) * (kObs * G) + h * kObs + o] = make_float2(m[mt], l[mt]);
+          for (int mt = 0; mt < C::MT; mt++) hb[mt * 128 + row] = make_float2(m[mt], l[mt]);
+        }
+        if (!named_all(kTcBarEpi, kTcEpi, ok && !failed())) break;
+        if (hf == 0) {
+#pragma unroll
+          for (int mt = 0; mt < C::MT; mt++) {
+            const int r = 128 * mt + row;
+            if (r < kObs * G) {
+              const float2 o2 = hb[mt * 128 + row];
+              const float mn = fmaxf(m[mt], o2.x);
+              float lt = 0.0f;
+              if (mn != -INFINITY) lt = l[mt] * fast_exp2(m[mt] - mn) + o2.y * fast_exp2(o2.x - mn);
+              const int o = r / G, h = r % G;
+              partial[((size_t)unit * nkb_cap + x.kb) * (kObs * G) + h * kObs + o] = make_float2(mn, lt);
+            }
           }
         }
       } else {
         if (unit != lse_unit) {                          // lse2 of the head's query rows
-          named_sync(kTcBarEpi, kTcEpi);
+          named_sync(kTcBarEpi, kTcEpi);                 // the previous head's values are no longer read
           for (int r = threadIdx.x - 64; r < kObs * G; r += kTcEpi) s_lse[r] = lse2[(size_t)unit * kObs * G + r];
           named_sync(kTcBarEpi, kTcEpi);
           lse_unit = unit;
         }
         const int j = key0 + row;
         const bool full = j <= n0 - kObs;                // the key precedes every observation query
-        // columns (o, h) = o G + h, 128 at a time: max over the heads of one
-        // observation query, then one exp2 per query into four partial sums
+        // observation queries 16 hf .. 16 hf + 15: columns (o, h) = o G + h,
+        // the max over the heads of one query, then one exp2 per query into
+        // four partial sums
+        constexpr int NC = kObs / 2 * G;                 // columns of a half
+        const int cbase = NC * hf;
         float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         float y = -INFINITY;
 #pragma unroll
-        for (int c0 = 0; c0 < kObs * G; c0 += 128) {
-          constexpr int W = kObs * G < 128 ? kObs * G : 128;
+        for (int c0 = 0; c0 < NC; c0 += 64) {
+          constexpr int W = NC < 64 ? NC : 64;
           float v[W];
 #pragma unroll
-          for (int c = 0; c < W; c += 32)
-            if (c0 + c < kObs * G) tmem_ld32_nowait(tl + ab * C::ACC + c0 + c, v + c);
+          for (int c = 0; c < W; c += 16)
+            if (c0 + c < NC) tmem_ld16_nowait(tl + ab * C::ACC + cbase + c0 + c, v + c);
           tmem_wait_ld();
-          if (c0 + W >= kObs * G) {
+          if (c0 + W >= NC) {
             tc_fence_before();
             mbar_arrive(aempty(ab));
           }
 #pragma unroll
           for (int e = 0; e < W; e++) {
-            const int col = c0 + e, o = col / G, h = col % G;
-            if (col >= kObs * G) break;
-            y = fmaxf(y, __fmaf_rn(v[e], sc, -s_lse[h * kObs + o]));
+            const int col = c0 + e, o = col / G, h = col % G;    // o relative to the half
+            if (col >= NC) break;
+            const int og = kObs / 2 * hf + o;
+            y = fmaxf(y, __fmaf_rn(v[e], sc, -s_lse[h * kObs + og]));
             if (h == G - 1) {
-              if (full || j <= n0 - kObs + o) ps[o & 3] += exp2f(y);
+              if (full || j <= n0 - kObs + og) ps[o & 3] += exp2f(y);
               y = -INFINITY;
             }
           }
         }
-        const float s = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        int tier, rank;
-        classify_epi(pv, n0, j, s, tier, rank, s_cnt + 8 * ab, bcnt + (size_t)unit * nkb_cap + x.kb);
-        if (j < n0) {
-          const size_t tok = (size_t)(ca->tok0[i] + j) * hkv + x.kvh;
-          score_out[tok] = s;
-          tokinfo[tok] = (uint16_t)((rank << 2) | tier);
+        const float sh = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        float* hb = reinterpret_cast<float*>(s_half) + ab * 128;
+        if (hf == 1) hb[row] = sh;
+        if (!named_all(kTcBarEpi, kTcEpi, ok && !failed())) break;
+        if (hf == 0) {
+          const float s = sh + hb[row];
+          int tier, rank;
+          classify_epi(pv, n0, j, s, tier, rank, s_cnt + 8 * ab, bcnt + (size_t)unit * nkb_cap + x.kb);
+          if (j < n0) {
+            const size_t tok = (size_t)(ca->tok0[i] + j) * hkv + x.kvh;
+            score_out[tok] = s;
+            tokinfo[tok] = (uint16_t)((rank << 2) | tier);
+          }
         }
       }
     }
