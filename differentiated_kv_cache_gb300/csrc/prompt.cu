@@ -1,13 +1,14 @@
 // prompt.cu — prompt-phase compaction kernels (DiffKV, compaction policy,
 // prompt phase; memory management, prompt workflow, Figure 6).
 //
-//   k_prompt_given    tier from caller-given scores
+//   k_prompt_given    tier and in-block rank from scores (caller-given or computed)
 //   k_prompt_scatter  rank -> position map per (head, tier)
 //   k_prompt_pack     quantize and pack surviving tokens into the granted pages
 //
 // Token scores from the observation queries (log-sum-exp pass, merge, score
-// pass) run on the tensor cores in prompt_tc.cu; the allocation step between
-// score and scatter (grant prefix sum, reclaim, table) is in alloc.cu.
+// pass) run on the tensor cores in prompt_tc.cu, and k_prompt_given then
+// takes the tiers and ranks from them; the allocation step between score and
+// scatter (grant prefix sum, reclaim, table) is in alloc.cu.
 #include "dkv_kernels.cuh"
 
 namespace dkv {
@@ -293,6 +294,10 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long 
   } else {
     float* so = scores_out ? scores_out : s.score;
     e = launch_scoring_tc(P, k, q_obs, n_tok, n_req, so, st);
+    if (e == cudaSuccess) {      // tiers and in-block ranks from the scores
+      k_prompt_given<<<grid, 128, 0, st>>>(P.pv, so, nullptr, s.tokinfo, s.bcnt, s.nkb_cap);
+      e = cudaGetLastError();
+    }
     score_src = so;
   }
   if (e != cudaSuccess) return e;

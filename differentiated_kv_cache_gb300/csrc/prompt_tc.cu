@@ -8,8 +8,7 @@
 //       row folding the tile's 128 keys into (max, sum) in the log2 domain.
 //   a2  S_j = sum_{p>=j} max_h exp(l_{h,p,j} - lse_{h,p}): D = K Q^T, one
 //       accumulator row per key, one epilogue thread per key taking the max
-//       over the group's heads and the sum over the observation queries, then
-//       the tier and the in-block rank (the same rule as the CUDA-core path).
+//       over the group's heads and the sum over the observation queries.
 //
 // One persistent CTA per SM takes a contiguous range of the call's (head, key
 // tile) pairs, tiles of one head consecutive. Warp 0 issues the TMA copies
@@ -31,7 +30,6 @@ namespace dkv {
 constexpr int kTcThreads = 320;      // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr int kTcEpi = 256;          // epilogue threads: two per accumulator row
 constexpr int kTcBarEpi = 1;         // named barrier of the epilogue warps
-constexpr int kTcBarRow = 2;         // named barrier of the first epilogue half (one thread per row)
 
 template <int G>
 struct TcCfg {
@@ -75,45 +73,13 @@ __global__ void k_prompt_lse_merge(PoolView pv, const float2* __restrict__ parti
   }
 }
 
-// Tier and in-block rank of key j (score s) over the first epilogue half's
-// 128 threads (one key each; warp w holds keys 32 (w % 4) ..), the rule of
-// the CUDA-core classification; cnt: 8 ints of shared memory.
-__device__ __forceinline__ void classify_epi(const PoolView& pv, int n0, int j, float s, int& tier, int& rank,
-                                             int* cnt, int2* bcnt_out) {
-  const int et = threadIdx.x - 64, lane = et & 31, ew = (threadIdx.x >> 5) & 3;
-  tier = kTierPrune;
-  if (j < n0) {
-    if (j >= n0 - pv.window) {
-      tier = kTierHi;
-    } else {
-      const float imp = __fdiv_rn(s, (float)score_count(j, n0, 0));
-      tier = classify(imp, __fdiv_rn(pv.alpha_h, (float)n0), __fdiv_rn(pv.alpha_l, (float)n0), pv.lo_enabled);
-    }
-  }
-  const unsigned bh = __ballot_sync(0xffffffffu, tier == kTierHi);
-  const unsigned bl = __ballot_sync(0xffffffffu, tier == kTierLo);
-  if (lane == 0) {
-    cnt[ew] = __popc(bh);
-    cnt[4 + ew] = __popc(bl);
-  }
-  named_sync(kTcBarRow, 128);
-  int bh0 = 0, bl0 = 0;
-  for (int w = 0; w < ew; w++) {
-    bh0 += cnt[w];
-    bl0 += cnt[4 + w];
-  }
-  const unsigned below = (1u << lane) - 1u;
-  rank = tier == kTierHi ? bh0 + __popc(bh & below) : (tier == kTierLo ? bl0 + __popc(bl & below) : 0);
-  if (et == 0 && bcnt_out) *bcnt_out = make_int2(cnt[0] + cnt[1] + cnt[2] + cnt[3], cnt[4] + cnt[5] + cnt[6] + cnt[7]);
-}
-
 // SCORE = false: a1 (partial max and sum per query row and key tile).
-// SCORE = true: a2 (scores, tiers, ranks, per-tile tier counts).
+// SCORE = true: a2 (the scores; tiers and ranks follow from them in
+// k_prompt_given, the classification of the CUDA-core path).
 template <int G, bool SCORE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_prompt_tc(PoolView pv, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tq,
-                const float* __restrict__ lse2, float2* partial, float* score_out, uint16_t* tokinfo, int2* bcnt,
-                int nkb_cap) {
+                const float* __restrict__ lse2, float2* partial, float* score_out, int nkb_cap) {
   using C = TcCfg<G>;
   if (pv.noop()) return;
   extern __shared__ uint8_t smem_raw[];
@@ -129,7 +95,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto aempty = [&](int b) { return b0 + 8u * (2 * C::KS + 6 + b); };
   uint32_t* s_taddr = reinterpret_cast<uint32_t*>(bars + 2 * C::KS + 8);
   int* s_fail = reinterpret_cast<int*>(s_taddr + 1);
-  int* s_cnt = s_fail + 1;                              // [2][8] classification counts
+  int* s_cnt = s_fail + 1;                              // [16] scan scratch
   int* s_roff = s_cnt + 16;                             // [n_req + 1] first tile of each request
   const CallArgs* ca = pv.call;
   const int n_req = ca->n_req, hkv = pv.hkv;
@@ -424,16 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float* hb = reinterpret_cast<float*>(s_half) + ab * 128;
         if (hf == 1) hb[row] = sh;
         if (!named_all(kTcBarEpi, kTcEpi, ok && !failed())) break;
-        if (hf == 0) {
-          const float s = sh + hb[row];
-          int tier, rank;
-          classify_epi(pv, n0, j, s, tier, rank, s_cnt + 8 * ab, bcnt + (size_t)unit * nkb_cap + x.kb);
-          if (j < n0) {
-            const size_t tok = (size_t)(ca->tok0[i] + j) * hkv + x.kvh;
-            score_out[tok] = s;
-            tokinfo[tok] = (uint16_t)((rank << 2) | tier);
-          }
-        }
+        if (hf == 0 && j < n0) score_out[(size_t)(ca->tok0[i] + j) * hkv + x.kvh] = sh + hb[row];
       }
     }
   }
@@ -502,14 +459,13 @@ cudaError_t launch_tc_g(Pool& P, const CUtensorMap& mk, const CUtensorMap& mq, i
                         cudaStream_t st) {
   const Scratch& s = P.sc;
   const int smem = tc_smem_bytes<G>(n_req);
-  k_prompt_tc<G, false><<<P.sm_count, kTcThreads, smem, st>>>(P.pv, mk, mq, nullptr, s.partial, nullptr, nullptr,
-                                                              nullptr, s.nkb_cap);
+  k_prompt_tc<G, false><<<P.sm_count, kTcThreads, smem, st>>>(P.pv, mk, mq, nullptr, s.partial, nullptr,
+                                                              s.nkb_cap);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k_prompt_lse_merge<<<n_req * P.pv.hkv, 256, 0, st>>>(P.pv, s.partial, s.lse2, s.nkb_cap);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_prompt_tc<G, true><<<P.sm_count, kTcThreads, smem, st>>>(P.pv, mk, mq, s.lse2, nullptr, score_out, s.tokinfo,
-                                                             s.bcnt, s.nkb_cap);
+  k_prompt_tc<G, true><<<P.sm_count, kTcThreads, smem, st>>>(P.pv, mk, mq, s.lse2, nullptr, score_out, s.nkb_cap);
   return cudaGetLastError();
 }
 
