@@ -42,11 +42,11 @@ HI_BYTES, LO_BYTES, SCORE_RMW = 200, 104, 8
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 126_765_568 + 4_393_216 + 22_253_824,
+    "bytes_per_call": 119_534_080 + 7_031_296 + 24_741_888 + 512,
     "sources": {
-        "attention.cu": "c76b3f395214da74158f89003568fffb7b0c7f754032a9684a62d2e2fe64e972",
-        "dkv_common.cuh": "3b0e1f4c1c8cae4ca109b8723f8e3f63d3cac5fc6abaa82c8ab970c208a68b5f",
-        "dkv_kernels.cuh": "3936f7261364e608fe96e00768ae57454fd63a28db1b10e200fa2d128e35be03",
+        "attention.cu": "7f56e726c784322533b67c67682f374b98e42d803ea1cfae3b89fcbbf8d192af",
+        "dkv_common.cuh": "082cb5d80fa0467928e2ad7b21af577aab51d6bd5d467981f852af61875b3434",
+        "dkv_kernels.cuh": "a07ad26642e091ab4ea67a4c69515e355893e74e4b258f2a45703b9fdfd749e4",
     },
 }
 
@@ -326,9 +326,9 @@ def run_dkv(args, world, rank, local):
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": int(per_launch_bytes),
                      "traffic": args.traffic if args.traffic is not None else recorded_traffic(args.workload)},
-        # per step: prompt compact_step 9 kernels; per decode step 3 (compaction)
+        # per step: prompt compact_step 11 kernels; per decode step 3 (compaction)
         # + 2 (attention, epilogue); one free_request kernel per request
-        "gpu_launches": args.steps * (9 + T * 5 + R),
+        "gpu_launches": args.steps * (11 + T * 5 + R),
     }
     result["clocks"] = clk.summary()
     if not args.no_e2e:
