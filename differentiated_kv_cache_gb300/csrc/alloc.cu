@@ -198,7 +198,10 @@ __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_commit(PoolView
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int layer, Scratch sc,
                                                                  SlotArgs sa) {
+  pdl_launch_dependents();        // k_decode_apply may launch; it waits for this grid
   if (pv.noop()) return;
+  pdl_wait();                     // the plans of k_decode_plan
+  if (pv.noop_after_wait()) return;
   __shared__ int s_warp[32];
   __shared__ int s_err, s_info;
   const int n_units = sa.n * pv.hkv;
@@ -326,8 +329,19 @@ cudaError_t configure_alloc() {
   return cudaFuncSetAttribute(k_free_request, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
 
+// A programmatic dependent of k_decode_plan.
 cudaError_t launch_decode_alloc(Pool& P, int layer, const SlotArgs& sa, cudaStream_t st) {
-  k_decode_alloc<<<1, kCoordThreads, 0, st>>>(P.pv, layer, P.sc, sa);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(1);
+  lc.blockDim = dim3(kCoordThreads);
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&lc, k_decode_alloc, P.pv, layer, P.sc, sa);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

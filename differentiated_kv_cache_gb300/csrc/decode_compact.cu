@@ -133,6 +133,7 @@ __device__ void decide_plan(const PoolView& pv, int layer, int slot, int kvh, in
 __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int layer, DecodePlan* plans,
                                                                ScanPart* parts, int* arrivals, int max_parts,
                                                                SlotArgs sa) {
+  pdl_launch_dependents();        // k_decode_alloc may launch; it waits for this grid
   if (pv.noop()) return;
   __shared__ ArgMin s_tmp[kPlanThreads / 32];
   __shared__ int s_xc, s_last;
@@ -245,6 +246,8 @@ __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, con
                                                       const __half* __restrict__ knew,
                                                       const __half* __restrict__ vnew, SlotArgs sa) {
   if (pv.noop()) return;
+  pdl_wait();                     // the plans and pages of k_decode_alloc
+  if (pv.noop_after_wait()) return;
   __shared__ TokStage st[2];
   const int kvh = blockIdx.x, i = blockIdx.y;
   const int slot = sa.slots[i];
@@ -341,7 +344,18 @@ cudaError_t launch_decode(Pool& P, int layer, const SlotArgs& sa, const __half* 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = launch_decode_alloc(P, layer, sa, st)) != cudaSuccess) return e;
-  k_decode_apply<<<grid, 64, 0, st>>>(P.pv, layer, P.sc.dplan, k, v, sa);
+  // a programmatic dependent of k_decode_alloc
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = dim3(64);
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, k_decode_apply, P.pv, layer, (const DecodePlan*)P.sc.dplan, k, v, sa);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -86,6 +86,10 @@ struct PoolView {
   // others hit, instead of every warp of a large grid queueing on the same
   // L2 line.
   __device__ __forceinline__ bool noop() const { return __ldca(&ctl->error) != 0; }
+  // The same status read from L2, for a programmatic dependent after its
+  // griddepcontrol.wait: an error its primary latched may postdate the line
+  // an L1 read at the kernel's start fetched.
+  __device__ __forceinline__ bool noop_after_wait() const { return *(volatile int*)&ctl->error != 0; }
 };
 
 // ---------------------------------------------------------------------------
