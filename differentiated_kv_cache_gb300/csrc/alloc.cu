@@ -11,6 +11,7 @@ constexpr int kCoordThreads = 1024;
 
 // Copy the call's host arrays into the pool's device CallArgs.
 __global__ void k_setup(PoolView pv, CallArgs args) {
+  pdl_launch_dependents();        // the call's first kernel may launch; it waits for this one
   CallArgs* c = pv.call;
   const int n = args.n_req;
   for (int x = threadIdx.x; x < n; x += blockDim.x) {
@@ -93,7 +94,7 @@ __device__ __forceinline__ void latch_error(PoolView& pv, int code, int info) {
 constexpr int kPlanWarps = 8;   // heads per CTA in the prompt coordination
 
 __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_heads(PoolView pv, Scratch sc) {
-  if (pv.noop()) return;
+  if (!dependent_begin(pv)) return;
   const CallArgs* ca = pv.call;
   const int n_units = ca->n_req * pv.hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_heads(PoolView 
 }
 
 __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_grant(PoolView pv, Scratch sc) {
-  if (pv.noop()) return;          // a head's pages do not fit its grant or row
+  if (!dependent_begin(pv)) return;          // a head's pages do not fit its grant or row
   extern __shared__ int s_g[];    // [unit] grant pages -> exclusive offsets
   __shared__ int s_warp[32];
   const CallArgs* ca = pv.call;
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_grant(PoolView 
 }
 
 __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_commit(PoolView pv, int layer, Scratch sc) {
-  if (pv.noop()) return;
+  if (!dependent_begin(pv)) return;
   extern __shared__ int s_r[];    // [unit] reclaimed pages -> exclusive offsets
   __shared__ int s_warp[32];
   const CallArgs* ca = pv.call;
@@ -314,10 +315,11 @@ cudaError_t launch_prompt_plan(Pool& P, int layer, int n_req, cudaStream_t st) {
   const int n_units = n_req * P.pv.hkv;
   const int smem = n_units * (int)sizeof(int);
   const int grid = (n_units + kPlanWarps - 1) / kPlanWarps;
-  k_prompt_plan_heads<<<grid, 32 * kPlanWarps, 0, st>>>(P.pv, P.sc);
-  k_prompt_plan_grant<<<grid, 32 * kPlanWarps, smem, st>>>(P.pv, P.sc);
-  k_prompt_plan_commit<<<grid, 32 * kPlanWarps, smem, st>>>(P.pv, layer, P.sc);
-  return cudaGetLastError();
+  cudaError_t e = launch_dependent(k_prompt_plan_heads, grid, dim3(32 * kPlanWarps), 0, st, P.pv, P.sc);
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(k_prompt_plan_grant, grid, dim3(32 * kPlanWarps), (size_t)smem, st, P.pv, P.sc);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(k_prompt_plan_commit, grid, dim3(32 * kPlanWarps), (size_t)smem, st, P.pv, layer, P.sc);
 }
 
 cudaError_t configure_alloc() {

@@ -90,4 +90,40 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
                                     float* out, int update_scores, cudaStream_t st);
 cudaError_t configure_kernels();
 
+// Prologue of a kernel launched as a programmatic dependent (small grids:
+// one status read per block): let the next kernel of the chain launch, skip
+// on an earlier error, then wait for the kernel before (griddepcontrol.wait)
+// ahead of any read of what it wrote, and re-read the status it may have set.
+// Called by every thread of the block.
+__device__ __forceinline__ bool dependent_begin(const PoolView& pv) {
+  __shared__ int s_stop;
+  pdl_launch_dependents();
+  if (pv.noop()) return false;
+  pdl_wait();
+  if (threadIdx.x == 0) s_stop = pv.noop_after_wait() ? 1 : 0;
+  __syncthreads();
+  return s_stop == 0;
+}
+
+// Launch `kernel` as a programmatic dependent of the kernel before it on the
+// stream (its blocks may become resident while that kernel drains; the
+// kernel itself starts with dependent_begin).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace dkv

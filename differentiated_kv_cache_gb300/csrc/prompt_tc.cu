@@ -55,7 +55,7 @@ static int tc_smem_bytes(int n_req) {
 // lse2[unit][h*32 + o] = m + log2(l) over the key tiles' partials (log2
 // domain); -inf for observation rows with a negative position.
 __global__ void k_prompt_lse_merge(PoolView pv, const float2* __restrict__ partial, float* lse2, int nkb_cap) {
-  if (pv.noop()) return;
+  if (!dependent_begin(pv)) return;
   const int unit = blockIdx.x, i = unit / pv.hkv;
   const int rows = kObs * pv.G;
   const int n0 = pv.call->lens[i];
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     k_prompt_tc(PoolView pv, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tq,
                 const float* __restrict__ lse2, float2* partial, float* score_out, int nkb_cap) {
   using C = TcCfg<G>;
-  if (pv.noop()) return;
+  if (!dependent_begin(pv)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_MISC);
@@ -459,14 +459,14 @@ cudaError_t launch_tc_g(Pool& P, const CUtensorMap& mk, const CUtensorMap& mq, i
                         cudaStream_t st) {
   const Scratch& s = P.sc;
   const int smem = tc_smem_bytes<G>(n_req);
-  k_prompt_tc<G, false><<<P.sm_count, kTcThreads, smem, st>>>(P.pv, mk, mq, nullptr, s.partial, nullptr,
-                                                              s.nkb_cap);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(k_prompt_tc<G, false>, dim3(P.sm_count), dim3(kTcThreads), (size_t)smem, st, P.pv,
+                                   mk, mq, (const float*)nullptr, s.partial, (float*)nullptr, s.nkb_cap);
   if (e != cudaSuccess) return e;
-  k_prompt_lse_merge<<<n_req * P.pv.hkv, 256, 0, st>>>(P.pv, s.partial, s.lse2, s.nkb_cap);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_prompt_tc<G, true><<<P.sm_count, kTcThreads, smem, st>>>(P.pv, mk, mq, s.lse2, nullptr, score_out, s.nkb_cap);
-  return cudaGetLastError();
+  e = launch_dependent(k_prompt_lse_merge, dim3(n_req * P.pv.hkv), dim3(256), 0, st, P.pv, (const float2*)s.partial,
+                       s.lse2, s.nkb_cap);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(k_prompt_tc<G, true>, dim3(P.sm_count), dim3(kTcThreads), (size_t)smem, st, P.pv, mk, mq,
+                          (const float*)s.lse2, (float2*)nullptr, score_out, s.nkb_cap);
 }
 
 template <int G>
