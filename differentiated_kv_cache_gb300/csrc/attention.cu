@@ -29,14 +29,14 @@
 namespace dkv {
 
 constexpr int kStages = 3;                 // ring depth per warp (chunked path)
-constexpr int kPageStages = 4;             // ring depth per warp (paged path)
+constexpr int kPageStages = 3;             // ring depth per warp (paged path)
 constexpr int kMinChunks = 8;              // ring work items per warp at least
 // Paged path: a page's share of a warp's range, in cost units: a fixed part
 // for staging and bookkeeping plus a part per 16-slot chunk (ratio measured
 // from per-warp timings on GB300).
 constexpr int kPageW = 5;
 constexpr int kChunkW = 4;
-constexpr int kCtasPerSm = 3;
+constexpr int kCtasPerSm = 4;
 constexpr int kOffV = 2048;                // chunked stage image: V rows
 constexpr int kOffMeta = 3072;             // chunked stage image: page meta segments
 
