@@ -168,11 +168,12 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// clamp(rint_even(t), 0, 255) in one conversion
+// clamp(rint_even(t), 0, 255) in one conversion (NaN gives 0); the 8-bit
+// result is zero-extended into the 32-bit register
 __device__ __forceinline__ uint32_t rint_sat_u8(float t) {
   uint32_t r;
   asm("cvt.rni.sat.u8.f32 %0, %1;\n" : "=r"(r) : "f"(t));
-  return r & 0xFFu;
+  return r;
 }
 // codes of the pair (x0, x1) under q, with the same arithmetic as qcode
 __device__ __forceinline__ void qcode2(float x0, float x1, const QParams& q, int bits, uint32_t& c0, uint32_t& c1) {

@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
       uint32_t c0, c1, c2, c3;
       qcode2_t<VB>(a.x, a.y, vq, c0, c1);
       qcode2_t<VB>(b.x, b.y, vq, c2, c3);
-      s_vw[warp][e][8 * q + w] = valid ? (c0 | (c1 << 4) | (c2 << 8) | (c3 << 12)) << eb : 0u;
+      // fields do not overlap: the sum is the bitwise or
+      s_vw[warp][e][8 * q + w] = valid ? (c0 + (c1 << 4) + (c2 << 8) + (c3 << 12)) << eb : 0u;
     }
     if (valid) {
       // page and slot of rank r: hi from the left of the grant, lo from the right
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
           uint32_t c0, c1, c2, c3;
           qcode2_t<8>(a.x, a.y, kq, c0, c1);
           qcode2_t<8>(b.x, b.y, kq, c2, c3);
-          w[y] = __byte_perm(c0 | (c2 << 16), c1 | (c3 << 16), 0x6240);
+          w[y] = __byte_perm(c0 + (c2 << 16), c1 + (c3 << 16), 0x6240);
         }
         uint4* dst = reinterpret_cast<uint4*>(krow + 32 * q);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
             const float2 a = __half22float2(kh[4 * y + z]);
             uint32_t c0, c1;
             qcode2_t<4>(a.x, a.y, kq, c0, c1);
-            acc |= (c0 | (c1 << 4)) << (8 * z);
+            acc += (c0 + (c1 << 4)) << (8 * z);
           }
           w[y] = acc;
         }
