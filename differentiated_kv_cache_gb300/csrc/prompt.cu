@@ -94,16 +94,23 @@ __global__ void __launch_bounds__(128) k_prompt_scatter(PoolView pv, const uint1
 constexpr int kPackGroups = 4;   // groups per warp
 constexpr int kPackTok = 8;      // tokens per group
 
-// codes of the pair (x0, x1), b-bit, under q (qcode's arithmetic)
-template <int B>
-__device__ __forceinline__ void qcode2_t(float x0, float x1, const QParams& q, uint32_t& c0, uint32_t& c1) {
+// Code arithmetic of qcode, taken apart: t = (x - z) * inv for a pair in
+// packed fp32, then round to nearest even into s32 (saturating; NaN gives 0),
+// and the clamp to [0, 2^B - 1] happens in the packing instruction, which
+// shifts the word built so far up and inserts two saturated fields:
+//   cvt.pack.sat.uB.s32.b32 d, a, b, c:  d = (c << 2B) | (sat(a) << B) | sat(b)
+__device__ __forceinline__ void qt2(float x0, float x1, const QParams& q, int& r0, int& r1) {
   const uint64_t t = mul_f32x2(sub_f32x2(f32x2(x0, x1), f32x2(q.z, q.z)), f32x2(q.inv, q.inv));
-  c0 = rint_sat_u8(__uint_as_float((uint32_t)t));
-  c1 = rint_sat_u8(__uint_as_float((uint32_t)(t >> 32)));
-  if (B < 8) {
-    c0 = min(c0, (1u << B) - 1u);
-    c1 = min(c1, (1u << B) - 1u);
-  }
+  asm("cvt.rni.s32.f32 %0, %1;\n" : "=r"(r0) : "f"(__uint_as_float((uint32_t)t)));
+  asm("cvt.rni.s32.f32 %0, %1;\n" : "=r"(r1) : "f"(__uint_as_float((uint32_t)(t >> 32))));
+}
+template <int B>
+__device__ __forceinline__ uint32_t pack_sat(int a, int b, uint32_t c) {
+  uint32_t d;
+  if (B == 8) asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  if (B == 4) asm("cvt.pack.sat.u4.s32.b32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  if (B == 2) asm("cvt.pack.sat.u2.s32.b32 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 template <bool HI>
@@ -194,12 +201,18 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
     __syncwarp();                              // the previous group's value rows are written
 #pragma unroll
     for (int w = 0; w < 8; w++) {
+      // the token's codes of features 4w .. 4w+3 at bits 4i of its 16-bit field
       const float2 a = __half22float2(vh[2 * w]), b = __half22float2(vh[2 * w + 1]);
-      uint32_t c0, c1, c2, c3;
-      qcode2_t<VB>(a.x, a.y, vq, c0, c1);
-      qcode2_t<VB>(b.x, b.y, vq, c2, c3);
-      // fields do not overlap: the sum is the bitwise or
-      s_vw[warp][e][8 * q + w] = valid ? (c0 + (c1 << 4) + (c2 << 8) + (c3 << 12)) << eb : 0u;
+      int c0, c1, c2, c3;
+      qt2(a.x, a.y, vq, c0, c1);
+      qt2(b.x, b.y, vq, c2, c3);
+      uint32_t f;
+      if (VB == 4) {
+        f = pack_sat<4>(c1, c0, pack_sat<4>(c3, c2, 0u));
+      } else {                               // 2-bit codes 4 bits apart (zero between)
+        f = pack_sat<2>(0, c0, pack_sat<2>(0, c1, pack_sat<2>(0, c2, pack_sat<2>(0, c3, 0u))));
+      }
+      s_vw[warp][e][8 * q + w] = valid ? f << eb : 0u;
     }
     if (valid) {
       // page and slot of rank r: hi from the left of the grant, lo from the right
@@ -210,12 +223,12 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
       if (HI) {
         uint32_t w[8];
 #pragma unroll
-        for (int y = 0; y < 8; y++) {
+        for (int y = 0; y < 8; y++) {             // bytes 4y .. 4y+3
           const float2 a = __half22float2(kh[2 * y]), b = __half22float2(kh[2 * y + 1]);
-          uint32_t c0, c1, c2, c3;
-          qcode2_t<8>(a.x, a.y, kq, c0, c1);
-          qcode2_t<8>(b.x, b.y, kq, c2, c3);
-          w[y] = __byte_perm(c0 + (c2 << 16), c1 + (c3 << 16), 0x6240);
+          int c0, c1, c2, c3;
+          qt2(a.x, a.y, kq, c0, c1);
+          qt2(b.x, b.y, kq, c2, c3);
+          w[y] = pack_sat<8>(c1, c0, pack_sat<8>(c3, c2, 0u));
         }
         uint4* dst = reinterpret_cast<uint4*>(krow + 32 * q);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -223,14 +236,14 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
       } else {
         uint32_t w[4];
 #pragma unroll
-        for (int y = 0; y < 4; y++) {
-          uint32_t acc = 0;
+        for (int y = 0; y < 4; y++) {             // bytes 4y .. 4y+3: features 8y .. 8y+7
+          uint32_t acc = 0u;
 #pragma unroll
-          for (int z = 0; z < 4; z++) {
+          for (int z = 3; z >= 0; z--) {          // byte z: feature 2z low nibble, 2z + 1 high
             const float2 a = __half22float2(kh[4 * y + z]);
-            uint32_t c0, c1;
-            qcode2_t<4>(a.x, a.y, kq, c0, c1);
-            acc += (c0 + (c1 << 4)) << (8 * z);
+            int c0, c1;
+            qt2(a.x, a.y, kq, c0, c1);
+            acc = pack_sat<4>(c1, c0, acc);
           }
           w[y] = acc;
         }
