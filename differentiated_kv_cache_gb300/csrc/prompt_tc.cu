@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float sc = 1.4426950408889634f * rsqrtf((float)kD);
     Tile x = locate(t0);
     int lse_unit = -1;
+    // a2 with G <= 4: -lse2 of this thread's 16 G columns held in registers
+    constexpr bool kLseReg = G <= 4;
+    float nlse[kLseReg ? kObs / 2 * G : 1];
     for (int it = 0; it < t1 - t0; it++, next(x)) {
       const int ab = it & 1;
       // on expiry the tile still runs through its barriers (with whatever the
@@ -351,6 +354,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           named_sync(kTcBarEpi, kTcEpi);                 // the previous head's values are no longer read
           for (int r = threadIdx.x - 64; r < kObs * G; r += kTcEpi) s_lse[r] = lse2[(size_t)unit * kObs * G + r];
           named_sync(kTcBarEpi, kTcEpi);
+          if (kLseReg) {
+#pragma unroll
+            for (int c = 0; c < (kLseReg ? kObs / 2 * G : 1); c++)
+              nlse[c] = -s_lse[(c % G) * kObs + kObs / 2 * hf + c / G];
+          }
           lse_unit = unit;
         }
         const int j = key0 + row;
@@ -379,9 +387,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int col = c0 + e, o = col / G, h = col % G;    // o relative to the half
             if (col >= NC) break;
             const int og = kObs / 2 * hf + o;
-            y = fmaxf(y, __fmaf_rn(v[e], sc, -s_lse[h * kObs + og]));
+            y = fmaxf(y, __fmaf_rn(v[e], sc, kLseReg ? nlse[col] : -s_lse[h * kObs + og]));
             if (h == G - 1) {
-              if (full || j <= n0 - kObs + og) ps[o & 3] += exp2f(y);
+              if (full || j <= n0 - kObs + og) ps[o & 3] += fast_exp2(y);
               y = -INFINITY;
             }
           }
