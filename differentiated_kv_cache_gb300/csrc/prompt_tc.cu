@@ -152,16 +152,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     x.kb = off % x.nkb;
     return x;
   };
+  // a1 walks the range forward, a2 backward: the key tiles a1 read last are
+  // the ones still in L2 when a2 starts
   auto next = [&](Tile& x) {
-    if (++x.kb == x.nkb) {
-      x.kb = 0;
-      if (++x.kvh == hkv) {
-        x.kvh = 0;
-        x.i++;
-        x.nkb = x.i < n_req ? (ca->lens[x.i] + kKeyBlock - 1) / kKeyBlock : 1;
+    if (!SCORE) {
+      if (++x.kb == x.nkb) {
+        x.kb = 0;
+        if (++x.kvh == hkv) {
+          x.kvh = 0;
+          x.i++;
+          x.nkb = x.i < n_req ? (ca->lens[x.i] + kKeyBlock - 1) / kKeyBlock : 1;
+        }
       }
+    } else if (--x.kb < 0) {
+      if (--x.kvh < 0) {
+        x.kvh = hkv - 1;
+        x.i--;
+        x.nkb = x.i >= 0 ? (ca->lens[x.i] + kKeyBlock - 1) / kKeyBlock : 1;
+      }
+      x.kb = x.nkb - 1;
     }
   };
+  const int t_first = SCORE ? t1 - 1 : t0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::KS; s++) {
@@ -191,7 +203,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ---- producer: the head's queries on a head change, then the key tile ----
     if (lane == 0) {
-      Tile x = locate(t0);
+      Tile x = locate(t_first);
       int qi = 0, prev_unit = -1, last_s[8], last_q[2];
       for (int s = 0; s < 8; s++) last_s[s] = -1;
       last_q[0] = last_q[1] = -1;
@@ -226,7 +238,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ---- MMA issuer ----
     if (lane == 0) {
-      Tile x = locate(t0);
+      Tile x = locate(t_first);
       int qi = -1, prev_unit = -1, issued = -1;
       for (int it = 0; it < t1 - t0 && !failed(); it++) {
         const int unit = x.i * hkv + x.kvh;
@@ -271,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int lg = warp & 3, row = 32 * lg + lane, hf = (warp - 2) >> 2;
     const uint32_t tl = tbase + ((uint32_t)(32 * lg) << 16);
     const float sc = 1.4426950408889634f * rsqrtf((float)kD);
-    Tile x = locate(t0);
+    Tile x = locate(t_first);
     int lse_unit = -1;
     // a2 with G <= 4: -lse2 of this thread's 16 G columns held in registers
     constexpr bool kLseReg = G <= 4;
