@@ -724,8 +724,9 @@ __device__ __forceinline__ void attend_page(AttnState& S, const uint8_t* sb, con
 }
 
 __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
-  pdl_launch_dependents();        // the merge grid may launch as SMs free up
-  if (pv.noop()) return;
+  // a programmatic dependent of the kernel before it (counts, pages); the
+  // epilogue grid may launch as SMs free up
+  if (!dependent_begin(pv)) return;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_warp[kAttnWarps];
   const int n_units = sa.n * pv.hkv;
@@ -854,8 +855,9 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
 // it touches (the copies spread over the lanes).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, AttnArgs a, SlotArgs sa) {
-  pdl_launch_dependents();        // the merge grid may launch as SMs free up
-  if (pv.noop()) return;
+  // a programmatic dependent of the kernel before it (counts, pages); the
+  // epilogue grid may launch as SMs free up
+  if (!dependent_begin(pv)) return;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_warp[kAttnWarps];
   const int n_units = sa.n * pv.hkv;
@@ -1301,12 +1303,8 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   a.paged = paged ? 1 : 0;
   a.lrow = (P.pv.G + 2) * kChunk;
   a.nwarps = P.sm_count * kCtasPerSm * kAttnWarps;
-  cudaError_t e;
-  if (paged)
-    k_attn_paged<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
-  else
-    k_attn_decode<<<P.sm_count * kCtasPerSm, 128, smem, st>>>(P.pv, a, sa);
-  e = cudaGetLastError();
+  cudaError_t e = launch_dependent(paged ? k_attn_paged : k_attn_decode, dim3(P.sm_count * kCtasPerSm), dim3(128),
+                                   (size_t)smem, st, P.pv, a, sa);
   if (e != cudaSuccess) return e;
   // epilogue: merge and (with score updates) the new scores
   const int G = P.pv.G;

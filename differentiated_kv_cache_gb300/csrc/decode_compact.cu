@@ -245,6 +245,7 @@ __device__ __forceinline__ void warp_quantize(const float* x, int bits, uint8_t*
 __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, const DecodePlan* __restrict__ plans,
                                                       const __half* __restrict__ knew,
                                                       const __half* __restrict__ vnew, SlotArgs sa) {
+  pdl_launch_dependents();        // a decode-attention call may follow: it waits for this grid
   if (pv.noop()) return;
   pdl_wait();                     // the plans and pages of k_decode_alloc
   if (pv.noop_after_wait()) return;
