@@ -42,11 +42,11 @@ HI_BYTES, LO_BYTES, SCORE_RMW = 200, 104, 8
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 119_534_080 + 7_031_296 + 24_741_888 + 512,
+    "bytes_per_call": 119_609_856 + 7_254_528 + 26_008_320,
     "sources": {
-        "attention.cu": "7f56e726c784322533b67c67682f374b98e42d803ea1cfae3b89fcbbf8d192af",
-        "dkv_common.cuh": "082cb5d80fa0467928e2ad7b21af577aab51d6bd5d467981f852af61875b3434",
-        "dkv_kernels.cuh": "a07ad26642e091ab4ea67a4c69515e355893e74e4b258f2a45703b9fdfd749e4",
+        "attention.cu": "0127c875960fc2ee085452e15b114d9fc7d4a6330cfcc1fb68f01421918b33ea",
+        "dkv_common.cuh": "50700ec7133401c8a9ffdf09baa24d69e575a7052f53a11e2cd0d7c6e01ee4ea",
+        "dkv_kernels.cuh": "2b14eca5551f653b7108f9b27c6796ab45beb49711c28bc26887a6b37feebddb",
     },
 }
 
