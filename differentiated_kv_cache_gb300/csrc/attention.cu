@@ -1070,10 +1070,11 @@ __device__ void head_span(const PoolView& pv, const SlotArgs& sa, int layer, boo
 // Lane (quad q, group pg) sums partials pg, pg + 4, ... of feature quad q;
 // every lane also takes partial `lane` (lane + 32, ...) for the query's
 // maximum M and rescaled sum L. The loads of the first 16 partials (and of
-// the first 32 for M and L) are all issued before any is used.
+// the first 32 for M and L) are all issued before any is used. lse_dst, when
+// given, receives the query's lse2 (M + log2 L).
 template <int G>
 __device__ void merge_task(const PoolView& pv, const AttnArgs& a, const SlotArgs& sa, int u, int np, int qh, int sl,
-                           int lane) {
+                           int lane, float* lse_dst) {
   const int stride = part_stride(G);
   const float* src = a.part + (size_t)u * a.max_parts * stride;
   const int q = sl * 8 + (lane & 7), pg = lane >> 3;
@@ -1129,9 +1130,13 @@ __device__ void merge_task(const PoolView& pv, const AttnArgs& a, const SlotArgs
     reinterpret_cast<float4*>(a.out + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qh) * kD)[q] =
         make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
   }
-  if (sl == 0 && lane == 0) {
-    a.lse2[(size_t)u * G + qh] = L > 0.0f ? M + log2f(L) : -INFINITY;
-    if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, sa.slots[i])[3] += 1;
+  if (lane == 0 && (sl == 0 || lse_dst != nullptr)) {
+    const float lse2 = L > 0.0f ? M + log2f(L) : -INFINITY;
+    if (lse_dst != nullptr) *lse_dst = lse2;
+    if (sl == 0) {
+      a.lse2[(size_t)u * G + qh] = lse2;
+      if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, sa.slots[i])[3] += 1;
+    }
   }
 }
 
@@ -1210,22 +1215,27 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   // partials and chunk rows: written by the attention kernel. A device error
   // it raised itself leaves this call's outputs undefined (the status says so)
   pdl_wait();
-  // merge tasks of this block: tasks xb, xb + nb, ... of the head, on warps
-  // 1.. with score updates (warp 0 derives lse2 and stages the rows), else on
-  // every warp
-  const int w0 = a.update ? 1 : 0;
+  // merge tasks of this block: tasks xb, xb + nb, ... of the head (task =
+  // query x feature slice). With nb <= kSlices every query has a task in every
+  // block, and the task of slice < nb hands the block its lse2; otherwise warp
+  // 0 derives lse2 from the partials and the tasks run on warps 1..
+  const bool own_lse = a.update && nb > kSlices;
+  const int w0 = own_lse ? 1 : 0;
   if (a.update && warp == 0) {
     if (lane == 0) {
       const uint32_t bytes = (uint32_t)(c1 - c0) * a.lrow * 4u;
       mbar_expect_tx(bar, bytes);
       bulk_g2s(smem_u32(s_rows), a.logit + ((size_t)u * a.max_chunks + c0) * a.lrow, bytes, bar);
     }
-    head_lse<G>(a, u, np, lane, s_lse);
+    if (own_lse) head_lse<G>(a, u, np, lane, s_lse);
   }
   if (warp >= w0) {
     int j = 0;
     for (int task = xb; task < G * kSlices; task += nb, j++)
-      if (j % (kEpiWarps - w0) == warp - w0) merge_task<G>(pv, a, sa, u, np, task / kSlices, task % kSlices, lane);
+      if (j % (kEpiWarps - w0) == warp - w0) {
+        const int qh = task / kSlices, sl = task % kSlices;
+        merge_task<G>(pv, a, sa, u, np, qh, sl, lane, a.update && !own_lse && sl < nb ? s_lse + qh : nullptr);
+      }
   }
   if (!a.update) return;
   __syncthreads();                // s_lse
@@ -1238,6 +1248,46 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   float lse[G];
 #pragma unroll
   for (int qh = 0; qh < G; qh++) lse[qh] = s_lse[qh];
+  if (paged) {
+    // four consecutive slots of one chunk per thread (pages hold whole
+    // chunks, so the four share a page and their scores one 16-byte word):
+    // S_j += 2^(max over queries of (l2 - lse2))
+#pragma unroll
+    for (int k = 0; k < EC * kChunk / 4 / kEpiThreads; k++) {
+      const int x = k * kEpiThreads + threadIdx.x;
+      const int lc = c0 + (x >> 2), j0 = 4 * (x & 3);
+      if (lc >= c1) break;
+      const bool hi_t = lc < ch_hi;
+      const int s0 = (hi_t ? lc : lc - ch_hi) * kChunk + j0;
+      const int n = (hi_t ? nh : nl) - s0;      // valid slots among the four
+      if (n <= 0) continue;
+      const float* row = s_rows + (size_t)(lc - c0) * a.lrow;
+      float4 mx = *reinterpret_cast<const float4*>(row + j0);
+      mx.x -= lse[0]; mx.y -= lse[0]; mx.z -= lse[0]; mx.w -= lse[0];
+#pragma unroll
+      for (int qh = 1; qh < G; qh++) {
+        const float4 v = *reinterpret_cast<const float4*>(row + qh * kChunk + j0);
+        mx.x = fmaxf(mx.x, v.x - lse[qh]);
+        mx.y = fmaxf(mx.y, v.y - lse[qh]);
+        mx.z = fmaxf(mx.z, v.z - lse[qh]);
+        mx.w = fmaxf(mx.w, v.w - lse[qh]);
+      }
+      const float4 old = *reinterpret_cast<const float4*>(row + G * kChunk + j0);
+      const int pid = reinterpret_cast<const int*>(row)[(G + 1) * kChunk];
+      const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+      float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (s0 - tg.div(s0) * tg.t);
+      const float4 nw = make_float4(old.x + fast_exp2(mx.x), old.y + fast_exp2(mx.y), old.z + fast_exp2(mx.z),
+                                    old.w + fast_exp2(mx.w));
+      if (n >= 4) {
+        *reinterpret_cast<float4*>(sp) = nw;
+      } else {
+        sp[0] = nw.x;
+        if (n > 1) sp[1] = nw.y;
+        if (n > 2) sp[2] = nw.z;
+      }
+    }
+    return;
+  }
   const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
 #pragma unroll
   for (int k = 0; k < EC * kChunk / kEpiThreads; k++) {
@@ -1251,20 +1301,12 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
     float pm = 0.0f;
 #pragma unroll
     for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, fast_exp2(row[qh * kChunk + j] - lse[qh]));
+    // chunked path: page from the table, old score from the page
     const TierGeom& tg = hi_t ? pv.hi : pv.lo;
     const int d = tg.div(slot);
-    float* sp;
-    float old;
-    if (paged) {
-      sp = reinterpret_cast<float*>(pv.page(reinterpret_cast<const int*>(row)[(G + 1) * kChunk]) + tg.off[4]) +
-           (slot - d * tg.t);
-      old = row[G * kChunk + j];
-    } else {                      // chunked path: page from the table, old score from the page
-      const int pid = __ldcg(row_tab + (hi_t ? d : pv.L - 1 - d));
-      sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (slot - d * tg.t);
-      old = __ldcg(sp);
-    }
-    *sp = old + pm;
+    const int pid = __ldcg(row_tab + (hi_t ? d : pv.L - 1 - d));
+    float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (slot - d * tg.t);
+    *sp = __ldcg(sp) + pm;
   }
 }
 
