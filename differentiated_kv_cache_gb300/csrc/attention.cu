@@ -31,12 +31,20 @@ namespace dkv {
 constexpr int kStages = 3;                 // ring depth per warp (chunked path)
 constexpr int kPageStages = 3;             // ring depth per warp (paged path)
 constexpr int kMinChunks = 8;              // ring work items per warp at least
+// Attention warps per SM: on the paged path one CTA of 16 warps (four CTAs
+// of 4 warps when 16 page rings do not fit in shared memory), on the chunked
+// path four CTAs of 4 warps. With several CTAs per SM the warps of the CTA
+// placed first are issued ahead of the others, so that the same work takes
+// the fourth CTA 15 % longer (per-warp timelines on GB300); one CTA per SM
+// has no such order among its warps.
+constexpr int kWarpsPerSm = 16;
 // Paged path: a page's share of a warp's range, in cost units: a fixed part
-// for staging and bookkeeping plus a part per 16-slot chunk (ratio measured
-// from per-warp timings on GB300).
-constexpr int kPageW = 5;
-constexpr int kChunkW = 4;
-constexpr int kCtasPerSm = 4;
+// for staging and bookkeeping plus a part per 16-slot chunk, whose ratio
+// grows with the group size (from per-warp timelines on GB300: a lo page of
+// two chunks takes 1.8 times a hi page at G = 4, 1.6 times at G = 8).
+__host__ __device__ __forceinline__ int page_cost(int G, int chunks) {
+  return G <= 4 ? 1 + 4 * chunks : 3 + 5 * chunks;
+}
 constexpr int kOffV = 2048;                // chunked stage image: V rows
 constexpr int kOffMeta = 3072;             // chunked stage image: page meta segments
 
@@ -439,19 +447,6 @@ __device__ int item_prefix(const PoolView& pv, const SlotArgs& sa, int layer, bo
   return s_pref[n_units];
 }
 
-// Heads without any stored token get a zero output (CTA 0).
-__device__ void zero_empty_heads(const PoolView& pv, const AttnArgs& a, const SlotArgs& sa, const int* s_pref) {
-  const int n_units = sa.n * pv.hkv, G = pv.G;
-  for (int u = 0; u < n_units; u++) {
-    if (s_pref[u + 1] != s_pref[u]) continue;
-    const int i = u / pv.hkv, kvh = u % pv.hkv;
-    for (int x = threadIdx.x; x < G * kD; x += blockDim.x)
-      a.out[((size_t)i * pv.hkv * G + (size_t)kvh * G) * kD + x] = 0.0f;
-    if (threadIdx.x < G) a.lse2[(size_t)u * G + threadIdx.x] = -INFINITY;
-    if (threadIdx.x == 0 && a.update && kvh == 0) pv.rq(a.layer, sa.slots[i])[3] += 1;
-  }
-}
-
 __device__ __forceinline__ int find_unit(const int* s_pref, int n_units, int g0) {
   int lo_u = 0, hi_u = n_units - 1;   // last u with s_pref[u] <= g0 (never an empty head)
   while (lo_u < hi_u) {
@@ -465,7 +460,7 @@ __device__ __forceinline__ int find_unit(const int* s_pref, int n_units, int g0)
 // Paged path: pages of T = 16k tokens (k = 1, 2, ...), one bulk copy per page
 // of its first four segments (K rows, V rows, K meta, V meta are contiguous at
 // the page start). The work sequence is measured in cost units (a page weighs
-// kPageW + kChunkW * T/16); a warp takes the pages that start inside its range.
+// page_cost(G, T/16)); a warp takes the pages that start inside its range.
 // One cursor walks the pages on the issue side and leaves a descriptor of
 // each staged page next to its stage. The softmax rescales lazily: a group's
 // probabilities are taken against the running maximum as long as no logit
@@ -723,28 +718,29 @@ __device__ __forceinline__ void attend_page(AttnState& S, const uint8_t* sb, con
   }
 }
 
-__global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
+template <int W>   // warps per CTA: 16 (one CTA per SM) or 4 (four CTAs per SM)
+__global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
   // a programmatic dependent of the kernel before it (counts, pages); the
-  // epilogue grid may launch as SMs free up
-  if (!dependent_begin(pv)) return;
+  // epilogue grid, which reads the counts before its own wait, may launch
+  // once every block is past the wait
+  if (!dependent_begin<true>(pv)) return;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_warp[kAttnWarps];
+  __shared__ int s_warp[W];
   const int n_units = sa.n * pv.hkv;
   const int G = pv.G;
   const int nch_hi = pv.hi.t / kChunk, nch_lo = pv.lo.t / kChunk;
-  const int wh = kPageW + kChunkW * nch_hi, wl = kPageW + kChunkW * nch_lo;
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kAttnWarps * kPageStages * a.stage_bytes);
-  int4* s_desc = reinterpret_cast<int4*>(s_bar + kAttnWarps * kPageStages);
-  int* s_pref = reinterpret_cast<int*>(s_desc + 2 * kAttnWarps * kPageStages);   // s_desc: [warp][stage][2]
+  const int wh = page_cost(G, nch_hi), wl = page_cost(G, nch_lo);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + W * kPageStages * a.stage_bytes);
+  int4* s_desc = reinterpret_cast<int4*>(s_bar + W * kPageStages);
+  int* s_pref = reinterpret_cast<int*>(s_desc + 2 * W * kPageStages);   // s_desc: [warp][stage][2]
   const int total = item_prefix(pv, sa, a.layer, true, wh, wl, s_pref, s_warp);
-  const int nwarps = gridDim.x * kAttnWarps;
+  const int nwarps = gridDim.x * W;
   // at least kMinChunks pages of the heaviest kind per range: a head is then
   // covered by at most (its pages / kMinChunks) + 2 ranges
   const int C = range_width(total, nwarps, true, wh, wl);
-  if (blockIdx.x == 0) zero_empty_heads(pv, a, sa, s_pref);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int gw = blockIdx.x * kAttnWarps + warp;
+  const int gw = blockIdx.x * W + warp;
   const int g0 = gw * C, g1 = min(total, g0 + C);
   const PagedCtx ctx{pv, sa, s_pref, a.layer, n_units, wh, wl};
   PageCursor ci;
@@ -854,10 +850,12 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_paged(PoolView pv, Att
 // the chunk's runs of K rows and V rows plus the meta segments of every page
 // it touches (the copies spread over the lanes).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, AttnArgs a, SlotArgs sa) {
+__global__ void __launch_bounds__(32 * kAttnWarps, kWarpsPerSm / kAttnWarps) k_attn_decode(PoolView pv, AttnArgs a,
+                                                                                          SlotArgs sa) {
   // a programmatic dependent of the kernel before it (counts, pages); the
-  // epilogue grid may launch as SMs free up
-  if (!dependent_begin(pv)) return;
+  // epilogue grid, which reads the counts before its own wait, may launch
+  // once every block is past the wait
+  if (!dependent_begin<true>(pv)) return;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_warp[kAttnWarps];
   const int n_units = sa.n * pv.hkv;
@@ -867,7 +865,6 @@ __global__ void __launch_bounds__(128, kCtasPerSm) k_attn_decode(PoolView pv, At
   const int total = item_prefix(pv, sa, a.layer, false, 1, 1, s_pref, s_warp);
   const int nwarps = gridDim.x * kAttnWarps;
   const int C = range_width(total, nwarps, false, 1, 1);
-  if (blockIdx.x == 0) zero_empty_heads(pv, a, sa, s_pref);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int gw = blockIdx.x * kAttnWarps + warp;
@@ -1176,6 +1173,16 @@ __device__ void head_lse(const AttnArgs& a, int u, int np, int lane, float* dst)
   }
 }
 
+// A head that stores no token: zero output (G rows), lse2 = -inf, and the
+// request's update count (rq, when given) advanced, after the attention
+// kernel, whose writes come first.
+__device__ __noinline__ void empty_head(float* out, float* lse2, int* rq, int G) {
+  pdl_wait();
+  for (int x = threadIdx.x; x < G * kD; x += blockDim.x) out[x] = 0.0f;
+  if (threadIdx.x < G) lse2[threadIdx.x] = -INFINITY;
+  if (threadIdx.x == 0 && rq != nullptr) rq[3] += 1;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnArgs a, SlotArgs sa) {
   if (pv.noop()) return;
@@ -1188,14 +1195,19 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int* cn = pv.cnt(a.layer, sa.slots[i], kvh);
   const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
-  if (nh + nl == 0) return;       // an empty head: done by the attention kernel
+  if (nh + nl == 0) {             // an empty head: zero output, lse2 = -inf
+    if (xb == 0)
+      empty_head(a.out + ((size_t)i * pv.hkv + kvh) * G * kD, a.lse2 + (size_t)u * G,
+                 a.update && kvh == 0 ? pv.rq(a.layer, sa.slots[i]) : nullptr, G);
+    return;
+  }
   const int ch_hi = (nh + kChunk - 1) / kChunk, nch = ch_hi + (nl + kChunk - 1) / kChunk;
   // blocks of the head: its chunk steps (score updates), else every block
   const int nb = a.update ? (nch + EC - 1) / EC : (int)gridDim.x;
   if (xb >= nb) return;
   // the head's partial count in the attention kernels' range partition
-  const int wh = paged ? kPageW + kChunkW * (pv.hi.t / kChunk) : 1;
-  const int wl = paged ? kPageW + kChunkW * (pv.lo.t / kChunk) : 1;
+  const int wh = paged ? page_cost(G, pv.hi.t / kChunk) : 1;
+  const int wl = paged ? page_cost(G, pv.lo.t / kChunk) : 1;
   int begin, total;
   head_span(pv, sa, a.layer, paged, wh, wl, u, s_red, begin, total);
   const int items = paged ? (nh + pv.hi.t - 1) / pv.hi.t * wh + (nl + pv.lo.t - 1) / pv.lo.t * wl : nch;
@@ -1329,24 +1341,29 @@ static int pages_per_chunk(int t) {
 static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int max_tokens, cudaStream_t st) {
   const int n_units = sa.n * P.pv.hkv;
   const bool paged = P.pv.hi.t % kChunk == 0 && P.pv.lo.t % kChunk == 0;
-  int smem;
+  int smem, w;   // w: warps per CTA
   if (paged) {
     a.mseg = 0;
     a.maxp = 1;
     a.stage_bytes = std::max(P.pv.hi.off[5], P.pv.lo.off[5]);
-    smem = kAttnWarps * kPageStages * (a.stage_bytes + 8 + 32) + 4 * (n_units + 1);
+    auto need = [&](int warps) { return warps * kPageStages * (a.stage_bytes + 8 + 32) + 4 * (n_units + 1); };
+    w = need(kWarpsPerSm) <= kMaxAttnSmem ? kWarpsPerSm : kAttnWarps;
+    smem = need(w);
   } else {
     a.mseg = (4 * std::max(P.pv.hi.t, P.pv.lo.t) + 15) & ~15;
     a.maxp = std::max(pages_per_chunk(P.pv.hi.t), pages_per_chunk(P.pv.lo.t));
     a.stage_bytes = kOffMeta + 2 * a.maxp * a.mseg;
+    w = kAttnWarps;
     smem = kAttnWarps * kStages * (a.stage_bytes + 8) + 4 * (n_units + 1);
   }
   if (smem > kMaxAttnSmem) return cudaErrorInvalidConfiguration;
   a.paged = paged ? 1 : 0;
   a.lrow = (P.pv.G + 2) * kChunk;
-  a.nwarps = P.sm_count * kCtasPerSm * kAttnWarps;
-  cudaError_t e = launch_dependent(paged ? k_attn_paged : k_attn_decode, dim3(P.sm_count * kCtasPerSm), dim3(128),
-                                   (size_t)smem, st, P.pv, a, sa);
+  a.nwarps = P.sm_count * kWarpsPerSm;
+  const dim3 grid(P.sm_count * (kWarpsPerSm / w)), block(32 * w);
+  cudaError_t e = !paged          ? launch_dependent(k_attn_decode, grid, block, (size_t)smem, st, P.pv, a, sa)
+                  : w == kWarpsPerSm ? launch_dependent(k_attn_paged<kWarpsPerSm>, grid, block, (size_t)smem, st, P.pv, a, sa)
+                                   : launch_dependent(k_attn_paged<kAttnWarps>, grid, block, (size_t)smem, st, P.pv, a, sa);
   if (e != cudaSuccess) return e;
   // epilogue: merge and (with score updates) the new scores
   const int G = P.pv.G;
@@ -1480,7 +1497,9 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
 }
 
 cudaError_t configure_attention() {
-  const void* fns[] = {reinterpret_cast<const void*>(k_attn_decode), reinterpret_cast<const void*>(k_attn_paged),
+  const void* fns[] = {reinterpret_cast<const void*>(k_attn_decode),
+                       reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm>),
+                       reinterpret_cast<const void*>(k_attn_paged<kAttnWarps>),
                        reinterpret_cast<const void*>(k_attn_epi<1>), reinterpret_cast<const void*>(k_attn_epi<2>),
                        reinterpret_cast<const void*>(k_attn_epi<3>), reinterpret_cast<const void*>(k_attn_epi<4>),
                        reinterpret_cast<const void*>(k_attn_epi<5>), reinterpret_cast<const void*>(k_attn_epi<6>),

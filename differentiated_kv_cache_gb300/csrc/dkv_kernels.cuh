@@ -94,12 +94,16 @@ cudaError_t configure_kernels();
 // one status read per block): let the next kernel of the chain launch, skip
 // on an earlier error, then wait for the kernel before (griddepcontrol.wait)
 // ahead of any read of what it wrote, and re-read the status it may have set.
-// Called by every thread of the block.
+// Called by every thread of the block. LATE: let the next kernel launch only
+// after the wait, when it reads before its own wait what kernels before this
+// one wrote.
+template <bool LATE = false>
 __device__ __forceinline__ bool dependent_begin(const PoolView& pv) {
   __shared__ int s_stop;
-  pdl_launch_dependents();
+  if (!LATE) pdl_launch_dependents();
   if (pv.noop()) return false;
   pdl_wait();
+  if (LATE) pdl_launch_dependents();
   if (threadIdx.x == 0) s_stop = pv.noop_after_wait() ? 1 : 0;
   __syncthreads();
   return s_stop == 0;
