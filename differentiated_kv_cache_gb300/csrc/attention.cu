@@ -45,6 +45,9 @@ constexpr int kWarpsPerSm = 16;
 __host__ __device__ __forceinline__ int page_cost(int G, int chunks) {
   return G <= 4 ? 1 + 4 * chunks : 3 + 5 * chunks;
 }
+// A head's items start with a fixed cost for the warp that enters it mid-range
+// (the previous head's partial, the new queries): 2.5 to 3 us on GB300.
+__host__ __device__ __forceinline__ int head_cost(int G) { return G <= 4 ? 8 : 14; }
 constexpr int kOffV = 2048;                // chunked stage image: V rows
 constexpr int kOffMeta = 3072;             // chunked stage image: page meta segments
 
@@ -368,16 +371,17 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
 
 // Width C of each attention warp's range of the work sequence (cost units on
 // the paged path, chunks on the chunked path), and the warps first..last whose
-// ranges cover head u (its items start at s_pref[u]; nl: its lo tokens). A
-// warp's partial of head u is record (warp - first) of the head.
+// ranges cover head u (its items start at s_pref[u], its first page hw later;
+// nl: its lo tokens). A warp's partial of head u is record (warp - first) of
+// the head.
 __host__ __device__ __forceinline__ int range_width(int total, int nwarps, bool paged, int wh, int wl) {
   const int per = (total + nwarps - 1) / nwarps;
   const int lo = paged ? kMinChunks * (wh > wl ? wh : wl) : kMinChunks;
   return per > lo ? per : lo;
 }
 __device__ __forceinline__ void head_parts(const int* s_pref, int u, int C, bool paged, int nl, int wh, int wl,
-                                           int& first, int& last) {
-  first = s_pref[u] / C;
+                                           int hw, int& first, int& last) {
+  first = (s_pref[u] + hw) / C;
   last = paged ? (s_pref[u + 1] - (nl > 0 ? wl : wh)) / C : (s_pref[u + 1] - 1) / C;
 }
 
@@ -410,19 +414,25 @@ __device__ void publish(const PoolView& pv, const AttnArgs& a, AttnState& S, int
   }
 }
 
+// Work items of a head with nh hi and nl lo tokens: on the paged path its
+// pages weighted by their cost (wh, wl) after the head's own (hw), on the
+// chunked path its chunks.
+__device__ __forceinline__ int head_items(const PoolView& pv, int nh, int nl, bool paged, int wh, int wl, int hw) {
+  return paged ? (nh + nl > 0 ? hw : 0) + (nh + pv.hi.t - 1) / pv.hi.t * wh + (nl + pv.lo.t - 1) / pv.lo.t * wl
+               : (nh + kChunk - 1) / kChunk + (nl + kChunk - 1) / kChunk;
+}
+
 // Prefix over the call's heads of their work items (pages or chunks), in
 // shared memory; every CTA computes the same. Returns the total.
-__device__ int item_prefix(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int* s_pref,
-                           int* s_warp) {
+__device__ int item_prefix(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int hw,
+                           int* s_pref, int* s_warp) {
   const int n_units = sa.n * pv.hkv;
   const int per = (n_units + blockDim.x - 1) / blockDim.x;
   const int u0 = min(n_units, (int)threadIdx.x * per), u1 = min(n_units, u0 + per);
   int sum = 0;
   for (int u = u0; u < u1; u++) {
     const int* cn = pv.cnt(layer, sa.slots[u / pv.hkv], u % pv.hkv);
-    // paged: pages weighted by their cost (wh, wl); chunked: chunks
-    const int items = paged ? (cn[0] + pv.hi.t - 1) / pv.hi.t * wh + (cn[1] + pv.lo.t - 1) / pv.lo.t * wl
-                            : (cn[0] + kChunk - 1) / kChunk + (cn[1] + kChunk - 1) / kChunk;
+    const int items = head_items(pv, cn[0], cn[1], paged, wh, wl, hw);
     s_pref[u] = items;
     sum += items;
   }
@@ -482,7 +492,7 @@ struct PagedCtx {
   const PoolView& pv;
   const SlotArgs& sa;
   const int* s_pref;
-  int layer, n_units, wh, wl;
+  int layer, n_units, wh, wl, hw;
 
   __device__ __forceinline__ void at_unit(PageCursor& c, int u) const {
     c.u = u;
@@ -495,7 +505,7 @@ struct PagedCtx {
     c.np = c.hp + (c.nl + pv.lo.t - 1) / pv.lo.t;
     c.row = pv.row(layer, sa.slots[u / pv.hkv], u % pv.hkv);
     c.p = 0;
-    c.off = c.begin;
+    c.off = c.begin + hw;
   }
   // move past pages of finished heads (and empty heads) while another head follows
   __device__ __forceinline__ void settle(PageCursor& c) const {
@@ -509,14 +519,14 @@ struct PagedCtx {
   // first page starting at cost offset >= x
   __device__ __forceinline__ void seek(PageCursor& c, int x) const {
     at_unit(c, find_unit(s_pref, n_units, x));
-    const int o = x - c.begin;
+    const int o = x - c.off;        // from the head's first page
     if (o > 0) {
       if (o <= c.hp * wh) {
         c.p = (o + wh - 1) / wh;
-        c.off = c.begin + c.p * wh;
+        c.off += c.p * wh;
       } else {
         c.p = c.hp + (o - c.hp * wh + wl - 1) / wl;
-        c.off = c.begin + c.hp * wh + (c.p - c.hp) * wl;
+        c.off += c.hp * wh + (c.p - c.hp) * wl;
       }
     }
     settle(c);
@@ -525,7 +535,7 @@ struct PagedCtx {
   // first warp that owns pages of head u (range width C)
   __device__ __forceinline__ int first_owner(int u, int nl, int C) const {
     int first, last;
-    head_parts(s_pref, u, C, true, nl, wh, wl, first, last);
+    head_parts(s_pref, u, C, true, nl, wh, wl, hw, first, last);
     return first;
   }
 };
@@ -729,11 +739,11 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
   const int n_units = sa.n * pv.hkv;
   const int G = pv.G;
   const int nch_hi = pv.hi.t / kChunk, nch_lo = pv.lo.t / kChunk;
-  const int wh = page_cost(G, nch_hi), wl = page_cost(G, nch_lo);
+  const int wh = page_cost(G, nch_hi), wl = page_cost(G, nch_lo), hw = head_cost(G);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + W * kPageStages * a.stage_bytes);
   int4* s_desc = reinterpret_cast<int4*>(s_bar + W * kPageStages);
   int* s_pref = reinterpret_cast<int*>(s_desc + 2 * W * kPageStages);   // s_desc: [warp][stage][2]
-  const int total = item_prefix(pv, sa, a.layer, true, wh, wl, s_pref, s_warp);
+  const int total = item_prefix(pv, sa, a.layer, true, wh, wl, hw, s_pref, s_warp);
   const int nwarps = gridDim.x * W;
   // at least kMinChunks pages of the heaviest kind per range: a head is then
   // covered by at most (its pages / kMinChunks) + 2 ranges
@@ -742,7 +752,7 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
   const int g = lane >> 2, t = lane & 3;
   const int gw = blockIdx.x * W + warp;
   const int g0 = gw * C, g1 = min(total, g0 + C);
-  const PagedCtx ctx{pv, sa, s_pref, a.layer, n_units, wh, wl};
+  const PagedCtx ctx{pv, sa, s_pref, a.layer, n_units, wh, wl, hw};
   PageCursor ci;
   bool active = g0 < g1;
   if (active) {
@@ -862,7 +872,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps, kWarpsPerSm / kAttnWarps) k_a
   const int G = pv.G;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kAttnWarps * kStages * a.stage_bytes);
   int* s_pref = reinterpret_cast<int*>(s_bar + kAttnWarps * kStages);
-  const int total = item_prefix(pv, sa, a.layer, false, 1, 1, s_pref, s_warp);
+  const int total = item_prefix(pv, sa, a.layer, false, 1, 1, 0, s_pref, s_warp);
   const int nwarps = gridDim.x * kAttnWarps;
   const int C = range_width(total, nwarps, false, 1, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1032,15 +1042,14 @@ struct EpiSmem {
 // cost on the paged path, chunks on the chunked path): the offset of its
 // first item and the total over the call, from one block-wide reduction over
 // the heads' counts.
-__device__ void head_span(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int u,
-                          int* s_red, int& begin, int& total) {
+__device__ void head_span(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int hw,
+                          int u, int* s_red, int& begin, int& total) {
   const int n_units = sa.n * pv.hkv;
   int before = 0, all = 0;
   for (int v = threadIdx.x; v < n_units; v += blockDim.x) {
     const int* cn = pv.cnt(layer, sa.slots[v / pv.hkv], v % pv.hkv);
     const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
-    const int items = paged ? (nh + pv.hi.t - 1) / pv.hi.t * wh + (nl + pv.lo.t - 1) / pv.lo.t * wl
-                            : (nh + kChunk - 1) / kChunk + (nl + kChunk - 1) / kChunk;
+    const int items = head_items(pv, nh, nl, paged, wh, wl, hw);
     all += items;
     if (v < u) before += items;
   }
@@ -1208,11 +1217,12 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   // the head's partial count in the attention kernels' range partition
   const int wh = paged ? page_cost(G, pv.hi.t / kChunk) : 1;
   const int wl = paged ? page_cost(G, pv.lo.t / kChunk) : 1;
+  const int hw = paged ? head_cost(G) : 0;
   int begin, total;
-  head_span(pv, sa, a.layer, paged, wh, wl, u, s_red, begin, total);
-  const int items = paged ? (nh + pv.hi.t - 1) / pv.hi.t * wh + (nl + pv.lo.t - 1) / pv.lo.t * wl : nch;
+  head_span(pv, sa, a.layer, paged, wh, wl, hw, u, s_red, begin, total);
+  const int items = head_items(pv, nh, nl, paged, wh, wl, hw);
   const int C = range_width(total, a.nwarps, paged, wh, wl);
-  const int first = begin / C;
+  const int first = (begin + hw) / C;
   const int last = paged ? (begin + items - (nl > 0 ? wl : wh)) / C : (begin + items - 1) / C;
   const int np = last - first + 1;
   const EpiSmem L(G, a.update != 0);
