@@ -781,7 +781,9 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
       }
     };
     // lane 0 copies the next page's K | V | K meta | V meta | score prefix and
-    // records {head, page, hi count, lo count} and its page ID beside the stage
+    // records beside the stage {head, tier (1 = hi), valid slots from the
+    // page start, the head's chunk index of the page's first chunk} and {page
+    // ID, the head's lo count}
     auto try_issue = [&]() {
       if (!ctx.valid(ci, g1)) return;
       if (lane == 0) {
@@ -789,8 +791,11 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
         const uint32_t bar = bar0 + 8 * st;
         const bool hi = ci.p < ci.hp;
         const uint32_t bytes = hi ? pv.hi.off[5] : pv.lo.off[5];
-        wdesc[2 * st] = make_int4(ci.u, ci.p, ci.nh, ci.nl);
-        wdesc[2 * st + 1] = make_int4(pid, 0, 0, 0);
+        const int pt = hi ? ci.p : ci.p - ci.hp;
+        const int count = hi ? ci.nh - pt * pv.hi.t : ci.nl - pt * pv.lo.t;
+        const int chunk0 = hi ? pt * nch_hi : (ci.nh + kChunk - 1) / kChunk + pt * nch_lo;
+        wdesc[2 * st] = make_int4(ci.u, hi ? 1 : 0, count, chunk0);
+        wdesc[2 * st + 1] = make_int4(pid, ci.nl, 0, 0);
         mbar_expect_tx(bar, bytes);
         bulk_g2s(smem_u32(wst + st * a.stage_bytes), pv.page(pid), bytes, bar);
       }
@@ -822,14 +827,13 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
         failed = true;
         break;
       }
-      const int4 d = wdesc[2 * (x % kPageStages)];  // head, page, hi count, lo count
-      const int dpid = wdesc[2 * (x % kPageStages) + 1].x;
-      const int hp = pv.hi.div(d.z + pv.hi.t - 1);
-      const bool hi = d.y < hp;
+      const int4 d = wdesc[2 * (x % kPageStages)];  // head, tier, valid slots, first chunk
+      const int2 d1 = *reinterpret_cast<const int2*>(wdesc + 2 * (x % kPageStages) + 1);   // page ID, lo count
+      const bool hi = d.y != 0;
       if (d.x != cur_u) {         // the range enters the next head
         publish(pv, a, S, cur_u, ctx.first_owner(cur_u, cur_nl, C), gw, lane);
         cur_u = d.x;
-        cur_nl = d.w;
+        cur_nl = d1.y;
         q_hi = hi;
         load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
         lazy_reset(S);
@@ -838,18 +842,11 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
         load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
       }
       const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
-      float* lg0 = a.update ? a.logit + (size_t)cur_u * a.max_chunks * a.lrow : nullptr;
-      if (hi) {
-        const int count = d.z - d.y * pv.hi.t;      // valid slots from this page's start
-        attend_page<true>(S, sb, pv.hi, nch_hi, count, bq, sq0, sq1,
-                          lg0 ? lg0 + (size_t)(d.y * nch_hi) * a.lrow : nullptr, a.lrow, dpid, G, g, t, jA, jB);
-      } else {
-        const int pt = d.y - hp;
-        const int count = d.w - pt * pv.lo.t;
-        const int chunk0 = (d.z + kChunk - 1) / kChunk + pt * nch_lo;
-        attend_page<false>(S, sb, pv.lo, nch_lo, count, bq, sq0, sq1,
-                           lg0 ? lg0 + (size_t)chunk0 * a.lrow : nullptr, a.lrow, dpid, G, g, t, jA, jB);
-      }
+      float* lgp = a.update ? a.logit + ((size_t)cur_u * a.max_chunks + d.w) * a.lrow : nullptr;
+      if (hi)
+        attend_page<true>(S, sb, pv.hi, nch_hi, d.z, bq, sq0, sq1, lgp, a.lrow, d1.x, G, g, t, jA, jB);
+      else
+        attend_page<false>(S, sb, pv.lo, nch_lo, d.z, bq, sq0, sq1, lgp, a.lrow, d1.x, G, g, t, jA, jB);
     }
     if (!failed) publish(pv, a, S, cur_u, ctx.first_owner(cur_u, cur_nl, C), gw, lane);
   }
