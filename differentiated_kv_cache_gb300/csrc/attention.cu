@@ -370,19 +370,14 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
 }
 
 // Width C of each attention warp's range of the work sequence (cost units on
-// the paged path, chunks on the chunked path), and the warps first..last whose
-// ranges cover head u (its items start at s_pref[u], its first page hw later;
-// nl: its lo tokens). A warp's partial of head u is record (warp - first) of
-// the head.
+// the paged path, chunks on the chunked path). The warps whose ranges hold a
+// page (a chunk) of head u are first = (s_pref[u] + hw) / C (its first page
+// starts hw after its items) to last = (offset of its last page) / C; a
+// warp's partial of head u is record (warp - first) of the head.
 __host__ __device__ __forceinline__ int range_width(int total, int nwarps, bool paged, int wh, int wl) {
   const int per = (total + nwarps - 1) / nwarps;
   const int lo = paged ? kMinChunks * (wh > wl ? wh : wl) : kMinChunks;
   return per > lo ? per : lo;
-}
-__device__ __forceinline__ void head_parts(const int* s_pref, int u, int C, bool paged, int nl, int wh, int wl,
-                                           int hw, int& first, int& last) {
-  first = (s_pref[u] + hw) / C;
-  last = paged ? (s_pref[u + 1] - (nl > 0 ? wl : wh)) / C : (s_pref[u + 1] - 1) / C;
 }
 
 // Publish the warp's partial of head u: O^T (with the value-zero sums added),
@@ -511,11 +506,6 @@ struct PagedCtx {
   __device__ __forceinline__ void settle(PageCursor& c) const {
     while (c.p >= c.np && c.u + 1 < n_units) at_unit(c, c.u + 1);
   }
-  __device__ __forceinline__ void next(PageCursor& c) const {
-    c.off += c.p < c.hp ? wh : wl;
-    c.p++;
-    settle(c);
-  }
   // first page starting at cost offset >= x
   __device__ __forceinline__ void seek(PageCursor& c, int x) const {
     at_unit(c, find_unit(s_pref, n_units, x));
@@ -533,11 +523,7 @@ struct PagedCtx {
   }
   __device__ __forceinline__ bool valid(const PageCursor& c, int g1) const { return c.p < c.np && c.off < g1; }
   // first warp that owns pages of head u (range width C)
-  __device__ __forceinline__ int first_owner(int u, int nl, int C) const {
-    int first, last;
-    head_parts(s_pref, u, C, true, nl, wh, wl, hw, first, last);
-    return first;
-  }
+  __device__ __forceinline__ int first_owner(int u, int C) const { return (s_pref[u] + hw) / C; }
 };
 
 __device__ __forceinline__ void lazy_reset(AttnState& S) {
@@ -741,8 +727,8 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
   const int nch_hi = pv.hi.t / kChunk, nch_lo = pv.lo.t / kChunk;
   const int wh = page_cost(G, nch_hi), wl = page_cost(G, nch_lo), hw = head_cost(G);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + W * kPageStages * a.stage_bytes);
-  int4* s_desc = reinterpret_cast<int4*>(s_bar + W * kPageStages);
-  int* s_pref = reinterpret_cast<int*>(s_desc + 2 * W * kPageStages);   // s_desc: [warp][stage][2]
+  int4* s_tab = reinterpret_cast<int4*>(s_bar + W * kPageStages);   // [warp][2][32] page descriptors
+  int* s_pref = reinterpret_cast<int*>(s_tab + W * 2 * 32);
   const int total = item_prefix(pv, sa, a.layer, true, wh, wl, hw, s_pref, s_warp);
   const int nwarps = gridDim.x * W;
   // at least kMinChunks pages of the heaviest kind per range: a head is then
@@ -760,96 +746,120 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
     active = ctx.valid(ci, g1);     // a page starts inside this range
   }
   uint8_t* wst = smem + warp * (kPageStages * a.stage_bytes);
-  int4* wdesc = s_desc + 2 * warp * kPageStages;
+  int4* wtab = s_tab + warp * 64;
   const uint32_t bar0 = smem_u32(s_bar + warp * kPageStages);
-  int issued = 0;
-  bool failed = false;
-  if (active) {
-    if (lane == 0) {
-      for (int st = 0; st < kPageStages; st++) mbar_init(bar0 + 8 * st, 1);
-      fence_mbar_init();
-      fence_proxy_async();
-    }
-    __syncwarp();
-    // page ID of cursor ci, loaded one issue ahead so that the table read is
-    // off the issue path (lane 0 only)
-    int pid = 0;
-    auto load_pid = [&]() {
-      if (lane == 0 && ctx.valid(ci, g1)) {
-        const bool hi = ci.p < ci.hp;
-        pid = __ldg(ci.row + (hi ? ci.p : pv.L - 1 - (ci.p - ci.hp)));
-      }
-    };
-    // lane 0 copies the next page's K | V | K meta | V meta | score prefix and
-    // records beside the stage {head, tier (1 = hi), valid slots from the
-    // page start, the head's chunk index of the page's first chunk} and {page
-    // ID, the head's lo count}
-    auto try_issue = [&]() {
-      if (!ctx.valid(ci, g1)) return;
-      if (lane == 0) {
-        const int st = issued % kPageStages;
-        const uint32_t bar = bar0 + 8 * st;
-        const bool hi = ci.p < ci.hp;
-        const uint32_t bytes = hi ? pv.hi.off[5] : pv.lo.off[5];
-        const int pt = hi ? ci.p : ci.p - ci.hp;
-        const int count = hi ? ci.nh - pt * pv.hi.t : ci.nl - pt * pv.lo.t;
-        const int chunk0 = hi ? pt * nch_hi : (ci.nh + kChunk - 1) / kChunk + pt * nch_lo;
-        wdesc[2 * st] = make_int4(ci.u, hi ? 1 : 0, count, chunk0);
-        wdesc[2 * st + 1] = make_int4(pid, ci.nl, 0, 0);
-        mbar_expect_tx(bar, bytes);
-        bulk_g2s(smem_u32(wst + st * a.stage_bytes), pv.page(pid), bytes, bar);
-      }
-      issued++;
-      ctx.next(ci);
-      load_pid();
-    };
-    const int u_first = ci.u, nl_first = ci.nl;
-    const bool hi_first = ci.p < ci.hp;
-    load_pid();
-    for (int x = 0; x < kPageStages - 1; x++) try_issue();
-    AttnState S;
-    lazy_reset(S);
-    // the first head's queries load while its first pages are in flight
-    uint32_t bq[8][2];
-    float sq0, sq1;
-    bool q_hi = hi_first;
-    int cur_u = u_first, cur_nl = nl_first;
-    load_q1(pv, a, u_first / pv.hkv, u_first % pv.hkv, g, t, hi_first, bq, sq0, sq1);
-    const int jA = chunk_slot(g), jB = chunk_slot(g + 8);
-    for (int x = 0; x < issued; x++) {
-      __syncwarp();               // every lane is done with the stage being refilled
-      fence_proxy_async();
-      try_issue();
-      if (!mbar_wait_bounded(bar0 + 8 * (x % kPageStages), (x / kPageStages) & 1)) {
-        if (lane == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = cur_u;
-        for (int y = x + 1; y < min(issued, x + kPageStages); y++)
-          mbar_wait_bounded(bar0 + 8 * (y % kPageStages), (y / kPageStages) & 1);
-        failed = true;
+  if (!active) return;
+  if (lane == 0) {
+    for (int st = 0; st < kPageStages; st++) mbar_init(bar0 + 8 * st, 1);
+    fence_mbar_init();
+    fence_proxy_async();
+  }
+  __syncwarp();
+  // The warp's pages in batches of 32, one page a lane: lane k of batch b
+  // walks from the batch's first page (head bu, page bp of the head) k pages
+  // on, across heads, and writes table entry (b & 1, k) = {head, page ID,
+  // valid slots from the page start (bit 31: hi tier), the head's chunk index
+  // of the page's first chunk}, or head -1 past the range. The 32 page-ID
+  // loads are in flight together. Entries of batch b are replaced by batch
+  // b + 2 only, after every page of batch b was consumed.
+  int bu = ci.u, bp = ci.p;
+  auto fill_batch = [&](int b) -> int {
+    int u = bu, p = bp + lane;
+    int nh = 0, nl = 0, hp = 0, np = 0;
+    bool ok = true;
+    for (;;) {
+      const int* cn = pv.cnt(a.layer, sa.slots[u / pv.hkv], u % pv.hkv);
+      nh = cn[0];
+      nl = cn[1];
+      hp = pv.hi.div(nh + pv.hi.t - 1);
+      np = hp + pv.lo.div(nl + pv.lo.t - 1);
+      if (p < np) break;
+      p -= np;
+      if (++u >= n_units) {
+        ok = false;
         break;
       }
-      const int4 d = wdesc[2 * (x % kPageStages)];  // head, tier, valid slots, first chunk
-      const int2 d1 = *reinterpret_cast<const int2*>(wdesc + 2 * (x % kPageStages) + 1);   // page ID, lo count
-      const bool hi = d.y != 0;
-      if (d.x != cur_u) {         // the range enters the next head
-        publish(pv, a, S, cur_u, ctx.first_owner(cur_u, cur_nl, C), gw, lane);
-        cur_u = d.x;
-        cur_nl = d1.y;
-        q_hi = hi;
-        load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
-        lazy_reset(S);
-      } else if (hi != q_hi) {    // from the head's hi pages to its lo pages
-        q_hi = hi;
-        load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
-      }
-      const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
-      float* lgp = a.update ? a.logit + ((size_t)cur_u * a.max_chunks + d.w) * a.lrow : nullptr;
-      if (hi)
-        attend_page<true>(S, sb, pv.hi, nch_hi, d.z, bq, sq0, sq1, lgp, a.lrow, d1.x, G, g, t, jA, jB);
-      else
-        attend_page<false>(S, sb, pv.lo, nch_lo, d.z, bq, sq0, sq1, lgp, a.lrow, d1.x, G, g, t, jA, jB);
     }
-    if (!failed) publish(pv, a, S, cur_u, ctx.first_owner(cur_u, cur_nl, C), gw, lane);
+    const bool hi = p < hp;
+    const int pt = hi ? p : p - hp;
+    if (ok) ok = s_pref[u] + hw + (hi ? pt * wh : hp * wh + pt * wl) < g1;
+    int4 dsc = make_int4(-1, 0, 0, 0);
+    if (ok) {
+      const int count = hi ? nh - pt * pv.hi.t : nl - pt * pv.lo.t;
+      const int chunk0 = hi ? pt * nch_hi : (nh + kChunk - 1) / kChunk + pt * nch_lo;
+      const int pid = __ldg(pv.row(a.layer, sa.slots[u / pv.hkv], u % pv.hkv) + (hi ? pt : pv.L - 1 - pt));
+      dsc = make_int4(u, pid, hi ? (int)(0x80000000u | (uint32_t)count) : count, chunk0);
+    }
+    wtab[(b & 1) * 32 + lane] = dsc;
+    const unsigned vm = __ballot_sync(0xffffffffu, ok);
+    bu = __shfl_sync(0xffffffffu, u, 31);
+    bp = __shfl_sync(0xffffffffu, p, 31) + 1;
+    __syncwarp();
+    return vm == 0xffffffffu ? 32 : __popc(vm);
+  };
+  // lane 0 copies page xi's K | V | K meta | V meta | score prefix into stage
+  // xi % kPageStages
+  auto issue = [&](int xi) {
+    if (lane == 0) {
+      const int4 dsc = wtab[((xi >> 5) & 1) * 32 + (xi & 31)];
+      const int st = xi % kPageStages;
+      const uint32_t bar = bar0 + 8 * st;
+      const uint32_t bytes = dsc.z < 0 ? pv.hi.off[5] : pv.lo.off[5];
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(smem_u32(wst + st * a.stage_bytes), pv.page(dsc.y), bytes, bar);
+    }
+  };
+  int n_pages = fill_batch(0);    // pages known so far; a full batch may have successors
+  bool more = n_pages == 32;
+  for (int x = 0; x < kPageStages - 1 && x < n_pages; x++) issue(x);
+  AttnState S;
+  lazy_reset(S);
+  // the first head's queries load while its first pages are in flight
+  uint32_t bq[8][2];
+  float sq0, sq1;
+  bool q_hi = ci.p < ci.hp;
+  int cur_u = ci.u;
+  load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, q_hi, bq, sq0, sq1);
+  const int jA = chunk_slot(g), jB = chunk_slot(g + 8);
+  bool failed = false;
+  for (int x = 0; x < n_pages; x++) {
+    __syncwarp();                 // every lane is done with the stage being refilled
+    fence_proxy_async();
+    const int xi = x + kPageStages - 1;
+    if (more && xi == n_pages) {  // the next batch
+      const int v = fill_batch(xi >> 5);
+      n_pages += v;
+      more = v == 32;
+    }
+    if (xi < n_pages) issue(xi);
+    if (!mbar_wait_bounded(bar0 + 8 * (x % kPageStages), (x / kPageStages) & 1)) {
+      if (lane == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = cur_u;
+      for (int y = x + 1; y < min(n_pages, x + kPageStages); y++)
+        mbar_wait_bounded(bar0 + 8 * (y % kPageStages), (y / kPageStages) & 1);
+      failed = true;
+      break;
+    }
+    const int4 d = wtab[((x >> 5) & 1) * 32 + (x & 31)];   // head, page ID, valid slots | hi, first chunk
+    const bool hi = d.z < 0;
+    const int count = d.z & 0x7fffffff;
+    if (d.x != cur_u) {           // the range enters the next head
+      publish(pv, a, S, cur_u, ctx.first_owner(cur_u, C), gw, lane);
+      cur_u = d.x;
+      q_hi = hi;
+      load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
+      lazy_reset(S);
+    } else if (hi != q_hi) {      // from the head's hi pages to its lo pages
+      q_hi = hi;
+      load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
+    }
+    const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
+    float* lgp = a.update ? a.logit + ((size_t)cur_u * a.max_chunks + d.w) * a.lrow : nullptr;
+    if (hi)
+      attend_page<true>(S, sb, pv.hi, nch_hi, count, bq, sq0, sq1, lgp, a.lrow, d.y, G, g, t, jA, jB);
+    else
+      attend_page<false>(S, sb, pv.lo, nch_lo, count, bq, sq0, sq1, lgp, a.lrow, d.y, G, g, t, jA, jB);
   }
+  if (!failed) publish(pv, a, S, cur_u, ctx.first_owner(cur_u, C), gw, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1353,7 +1363,8 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
     a.mseg = 0;
     a.maxp = 1;
     a.stage_bytes = std::max(P.pv.hi.off[5], P.pv.lo.off[5]);
-    auto need = [&](int warps) { return warps * kPageStages * (a.stage_bytes + 8 + 32) + 4 * (n_units + 1); };
+    // per warp its page ring with mbarriers and its descriptor table; the head prefix
+    auto need = [&](int warps) { return warps * (kPageStages * (a.stage_bytes + 8) + 64 * 16) + 4 * (n_units + 1); };
     w = need(kWarpsPerSm) <= kMaxAttnSmem ? kWarpsPerSm : kAttnWarps;
     smem = need(w);
   } else {
