@@ -144,9 +144,12 @@ __device__ __forceinline__ void cursor_seek(Cursor& c, int x, const int* s_pref,
 __device__ __forceinline__ void load_q(const PoolView& pv, const AttnArgs& a, int i, int kvh, int g, int t,
                                        uint32_t (&bq_hi)[8][2], uint32_t (&bq_lo)[8][2], float& sq0, float& sq1) {
   const int G = pv.G;
+  // query of mma column g: with G <= 4 columns 4..7 repeat queries 0..3 (their
+  // P.V columns carry the fp16 residuals of P')
+  const int qg = G <= 4 ? (g & 3) : g;
   float qf[32];
-  if (g < G) {
-    const uint4* qp = reinterpret_cast<const uint4*>(a.q + ((size_t)i * pv.hkv * G + (size_t)kvh * G + g) * kD + 32 * t);
+  if (qg < G) {
+    const uint4* qp = reinterpret_cast<const uint4*>(a.q + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qg) * kD + 32 * t);
 #pragma unroll
     for (int x = 0; x < 4; x++) {
       const uint4 u = qp[x];
@@ -182,9 +185,12 @@ __device__ __forceinline__ void load_q(const PoolView& pv, const AttnArgs& a, in
 __device__ __forceinline__ void load_q1(const PoolView& pv, const AttnArgs& a, int i, int kvh, int g, int t, bool hi,
                                         uint32_t (&bq)[8][2], float& sq0, float& sq1) {
   const int G = pv.G;
+  // query of mma column g: with G <= 4 columns 4..7 repeat queries 0..3 (their
+  // P.V columns carry the fp16 residuals of P')
+  const int qg = G <= 4 ? (g & 3) : g;
   float qf[32];
-  if (g < G) {
-    const uint4* qp = reinterpret_cast<const uint4*>(a.q + ((size_t)i * pv.hkv * G + (size_t)kvh * G + g) * kD + 32 * t);
+  if (qg < G) {
+    const uint4* qp = reinterpret_cast<const uint4*>(a.q + ((size_t)i * pv.hkv * G + (size_t)kvh * G + qg) * kD + 32 * t);
 #pragma unroll
     for (int x = 0; x < 4; x++) {
       const uint4 u = qp[x];
@@ -338,8 +344,14 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
     }
   }
   // P'^T as B fragments: block of tokens 0-7 and block of tokens 8-15
-  const uint32_t pb0 = movmatrix_trans(pack_half2(p0 * svA, p1 * svA));
-  const uint32_t pb1 = movmatrix_trans(pack_half2(p2 * svB, p3 * svB));
+  // P' as fp16 pairs plus their fp16 residuals: with G <= 4 the residuals take
+  // the spare query columns 4..7 (threads t >= 2), else a second P.V product
+  uint32_t h0, l0, h1, l1;
+  split_half2(p0 * svA, p1 * svA, h0, l0);
+  split_half2(p2 * svB, p3 * svB, h1, l1);
+  const bool two = G > 4, res = !two && t >= 2;
+  const uint32_t pb0 = movmatrix_trans(res ? l0 : h0), pb1 = movmatrix_trans(res ? l1 : h1);
+  const uint32_t pr0 = two ? movmatrix_trans(l0) : 0u, pr1 = two ? movmatrix_trans(l1) : 0u;
   // ---- O^T += V^T . P'^T ----
   const uint32_t vw0[4] = {vq0.x, vq0.y, vq0.z, vq0.w};
   const uint32_t vw1[4] = {vq1.x, vq1.y, vq1.z, vq1.w};
@@ -354,6 +366,7 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
       af[2] = cvv4_0(w1);   // feature 16g+2mt,   tokens 2t+8,2t+9
       af[3] = cvv4_1(w1);   // feature 16g+2mt+1, tokens 2t+8,2t+9
       mma16816(S.o[mt], af, pb0, pb1);
+      if (two) mma16816(S.o[mt], af, pr0, pr1);
     }
   } else {
 #pragma unroll
@@ -365,6 +378,7 @@ __device__ __forceinline__ void attend_chunk(AttnState& S, bool hi, const uint8_
       af[2] = cvv2_1(w);    // feature 16g+2mt,   slots e2,e3
       af[3] = cvv2_3(w);    // feature 16g+2mt+1, slots e2,e3
       mma16816(S.o[mt], af, pb0, pb1);
+      if (two) mma16816(S.o[mt], af, pr0, pr1);
     }
   }
 }
@@ -386,6 +400,12 @@ __host__ __device__ __forceinline__ int range_width(int total, int nwarps, bool 
 // the epilogue kernel once every warp is done.
 __device__ void publish(const PoolView& pv, const AttnArgs& a, AttnState& S, int u, int first, int gw, int lane) {
   const int G = pv.G, g = lane >> 2, t = lane & 3;
+  if (G <= 4) {                   // the residual columns (threads t ^ 2) into the query columns
+#pragma unroll
+    for (int mt = 0; mt < 8; mt++)
+#pragma unroll
+      for (int x = 0; x < 4; x++) S.o[mt][x] += __shfl_xor_sync(0xffffffffu, S.o[mt][x], 2);
+  }
   float l0 = S.l[0], l1 = S.l[1], z0 = S.z[0], z1 = S.z[1];
 #pragma unroll
   for (int s = 4; s <= 16; s <<= 1) {
@@ -657,8 +677,15 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
     S.z[0] = __fmaf_rn(p0, zvA, __fmaf_rn(p2, zvB, S.z[0]));
     S.z[1] = __fmaf_rn(p1, zvA, __fmaf_rn(p3, zvB, S.z[1]));
     // P'^T as B fragments: block of tokens 0-7 and block of tokens 8-15
-    const uint32_t pb0 = movmatrix_trans(pack_half2(p0 * svA, p1 * svA));
-    const uint32_t pb1 = movmatrix_trans(pack_half2(p2 * svB, p3 * svB));
+    // P' as fp16 pairs plus their fp16 residuals: with G <= 4 the residuals
+    // take the spare query columns 4..7 (threads t >= 2), else a second P.V
+    // product
+    uint32_t h0, l0, h1, l1;
+    split_half2(p0 * svA, p1 * svA, h0, l0);
+    split_half2(p2 * svB, p3 * svB, h1, l1);
+    const bool two = G > 4, res = !two && t >= 2;
+    const uint32_t pb0 = movmatrix_trans(res ? l0 : h0), pb1 = movmatrix_trans(res ? l1 : h1);
+    const uint32_t pr0 = two ? movmatrix_trans(l0) : 0u, pr1 = two ? movmatrix_trans(l1) : 0u;
     // ---- O^T += V^T . P'^T ----
     if (HI) {
       const uint8_t* v0 = sb + tg.off[1] + ((c0 + c) * 8 + 2 * t) * 128 + 16 * g;
@@ -676,6 +703,7 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
         af[2] = cvv4_0(w1);   // feature 16g+2mt,   tokens 2t+8,2t+9
         af[3] = cvv4_1(w1);   // feature 16g+2mt+1, tokens 2t+8,2t+9
         mma16816(S.o[mt], af, pb0, pb1);
+        if (two) mma16816(S.o[mt], af, pr0, pr1);
       }
     } else {
       const uint4 vq = *reinterpret_cast<const uint4*>(sb + tg.off[1] + ((c0 + c) * 4 + t) * 128 + 16 * g);
@@ -689,6 +717,7 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
         af[2] = cvv2_1(w);    // feature 16g+2mt,   slots e2,e3
         af[3] = cvv2_3(w);    // feature 16g+2mt+1, slots e2,e3
         mma16816(S.o[mt], af, pb0, pb1);
+        if (two) mma16816(S.o[mt], af, pr0, pr1);
       }
     }
   }
@@ -1218,8 +1247,11 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
     return;
   }
   const int ch_hi = (nh + kChunk - 1) / kChunk, nch = ch_hi + (nl + kChunk - 1) / kChunk;
-  // blocks of the head: its chunk steps (score updates), else every block
-  const int nb = a.update ? (nch + EC - 1) / EC : (int)gridDim.x;
+  // blocks of the head: with score updates one per chunk step of EC chunks
+  // up to the grid's width (block x takes steps x, x + nb, ...), else every
+  // block
+  const int nsteps = (nch + EC - 1) / EC;
+  const int nb = a.update ? min(nsteps, (int)gridDim.x) : (int)gridDim.x;
   if (xb >= nb) return;
   // the head's partial count in the attention kernels' range partition
   const int wh = paged ? page_cost(G, pv.hi.t / kChunk) : 1;
@@ -1236,7 +1268,6 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   float* s_rows = reinterpret_cast<float*>(smem + L.rows);
   float* s_lse = reinterpret_cast<float*>(smem + L.lse);
   const uint32_t bar = smem_u32(smem + L.misc);
-  const int c0 = xb * EC, c1 = min(nch, c0 + EC);
   if (a.update && threadIdx.x == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
@@ -1251,7 +1282,8 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   const bool own_lse = a.update && nb > kSlices;
   const int w0 = own_lse ? 1 : 0;
   if (a.update && warp == 0) {
-    if (lane == 0) {
+    if (lane == 0) {              // the rows of the block's first step
+      const int c0 = xb * EC, c1 = min(nch, c0 + EC);
       const uint32_t bytes = (uint32_t)(c1 - c0) * a.lrow * 4u;
       mbar_expect_tx(bar, bytes);
       bulk_g2s(smem_u32(s_rows), a.logit + ((size_t)u * a.max_chunks + c0) * a.lrow, bytes, bar);
@@ -1268,15 +1300,27 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   }
   if (!a.update) return;
   __syncthreads();                // s_lse
-  if (!mbar_wait_bounded(bar, 0)) {
-    if (threadIdx.x == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = u;
-    mbar_wait_bounded(bar, 0);
-    return;
-  }
   // new scores of the block's slots: S_j += max over queries of 2^(l2 - lse2)
   float lse[G];
 #pragma unroll
   for (int qh = 0; qh < G; qh++) lse[qh] = s_lse[qh];
+  const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
+  for (int step = xb, it = 0; step < nsteps; step += nb, it++) {
+  const int c0 = step * EC, c1 = min(nch, c0 + EC);
+  if (it > 0) {                   // the rows of this step, after every thread is done with the last
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t bytes = (uint32_t)(c1 - c0) * a.lrow * 4u;
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(smem_u32(s_rows), a.logit + ((size_t)u * a.max_chunks + c0) * a.lrow, bytes, bar);
+    }
+  }
+  // one decision for the block, so that no thread is left at a barrier
+  if (__syncthreads_or(!mbar_wait_bounded(bar, it & 1))) {
+    if (threadIdx.x == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = u;
+    mbar_wait_bounded(bar, it & 1);
+    return;
+  }
   if (paged) {
     // four consecutive slots of one chunk per thread (pages hold whole
     // chunks, so the four share a page and their scores one 16-byte word):
@@ -1315,9 +1359,8 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
         if (n > 2) sp[2] = nw.z;
       }
     }
-    return;
+    continue;
   }
-  const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
 #pragma unroll
   for (int k = 0; k < EC * kChunk / kEpiThreads; k++) {
     const int x = k * kEpiThreads + threadIdx.x;
@@ -1336,6 +1379,7 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
     const int pid = __ldcg(row_tab + (hi_t ? d : pv.L - 1 - d));
     float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (slot - d * tg.t);
     *sp = __ldcg(sp) + pm;
+  }
   }
 }
 
@@ -1388,8 +1432,11 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   const EpiSmem es(G, a.update != 0);
   unsigned gx;
   if (a.update) {
-    const int call_chunks = (max_tokens + kChunk - 1) / kChunk + 1;   // chunks of the call's longest head
-    gx = (unsigned)((call_chunks + epi_chunks(G) - 1) / epi_chunks(G));
+    // chunk steps of the call's longest head, at most one wave of blocks
+    // (four per SM) over all heads
+    const int call_chunks = (max_tokens + kChunk - 1) / kChunk + 1;
+    const int steps = (call_chunks + epi_chunks(G) - 1) / epi_chunks(G);
+    gx = (unsigned)std::max(1, std::min(steps, 4 * P.sm_count / std::max(1, n_units)));
   } else {
     gx = (unsigned)((G * kSlices + kEpiWarps - 1) / kEpiWarps);
   }

@@ -260,6 +260,15 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+// (a, b) as the sum of two fp16 pairs: hi = fp16(x), lo = fp16(x - hi), about
+// 22 significant bits together.
+__device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  __half2 h = __floats2half2_rn(a, b);
+  const float2 f = __half22float2(h);
+  __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
 
 // mbarrier + bulk asynchronous copy (global -> shared, completion counted in bytes)
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
