@@ -42,11 +42,11 @@ HI_BYTES, LO_BYTES, SCORE_RMW = 200, 104, 8
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 119_609_856 + 7_254_528 + 26_008_320,
+    "bytes_per_call": 119_588_352 + 7_548_672 + 25_958_656,
     "sources": {
-        "attention.cu": "0127c875960fc2ee085452e15b114d9fc7d4a6330cfcc1fb68f01421918b33ea",
-        "dkv_common.cuh": "50700ec7133401c8a9ffdf09baa24d69e575a7052f53a11e2cd0d7c6e01ee4ea",
-        "dkv_kernels.cuh": "2b14eca5551f653b7108f9b27c6796ab45beb49711c28bc26887a6b37feebddb",
+        "attention.cu": "3f1e277015c6efcef8d4b7b9e45bdc96f92a883c65768453326a61c0785354b8",
+        "dkv_common.cuh": "90d758348e6dbf3a1ae34973ef9bef33cbbd31e8c1a636103b676ac54b52f649",
+        "dkv_kernels.cuh": "a11e8c64feb0a4bcfea04df84fe718b26a0fa6dc53df45de115fabf6c95d12fe",
     },
 }
 
