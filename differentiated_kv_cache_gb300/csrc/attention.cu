@@ -182,9 +182,10 @@ __device__ __forceinline__ void load_q(const PoolView& pv, const AttnArgs& a, in
 
 // Query fragments in the feature order of one tier's key rows (hi: 8-bit,
 // lo: 4-bit) and the pre-scaled sums of queries 2t, 2t+1.
+template <int GT>   // the group size when fixed at compile time, else 0 (pv.G)
 __device__ __forceinline__ void load_q1(const PoolView& pv, const AttnArgs& a, int i, int kvh, int g, int t, bool hi,
                                         uint32_t (&bq)[8][2], float& sq0, float& sq1) {
-  const int G = pv.G;
+  const int G = GT > 0 ? GT : pv.G;
   // query of mma column g: with G <= 4 columns 4..7 repeat queries 0..3 (their
   // P.V columns carry the fp16 residuals of P')
   const int qg = G <= 4 ? (g & 3) : g;
@@ -398,8 +399,10 @@ __host__ __device__ __forceinline__ int range_width(int total, int nwarps, bool 
 // the running maxima and sums of queries 0..G-1, at index gw - first of the
 // head's partials (warp ranges first..last cover the head). The merge runs in
 // the epilogue kernel once every warp is done.
-__device__ void publish(const PoolView& pv, const AttnArgs& a, AttnState& S, int u, int first, int gw, int lane) {
-  const int G = pv.G, g = lane >> 2, t = lane & 3;
+template <int GT>   // the group size when fixed at compile time, else 0 (pv.G)
+__device__ __forceinline__ void publish(const PoolView& pv, const AttnArgs& a, AttnState& S, int u, int first, int gw,
+                                        int lane) {
+  const int G = GT > 0 ? GT : pv.G, g = lane >> 2, t = lane & 3;
   if (G <= 4) {                   // the residual columns (threads t ^ 2) into the query columns
 #pragma unroll
     for (int mt = 0; mt < 8; mt++)
@@ -743,7 +746,9 @@ __device__ __forceinline__ void attend_page(AttnState& S, const uint8_t* sb, con
   }
 }
 
-template <int W>   // warps per CTA: 16 (one CTA per SM) or 4 (four CTAs per SM)
+// W: warps per CTA, 16 (one CTA per SM) or 4 (four CTAs per SM); GT: the
+// group size when fixed at compile time (4, 8), else 0 (pv.G)
+template <int W, int GT>
 __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
   // a programmatic dependent of the kernel before it (counts, pages); the
   // epilogue grid, which reads the counts before its own wait, may launch
@@ -752,7 +757,7 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_warp[W];
   const int n_units = sa.n * pv.hkv;
-  const int G = pv.G;
+  const int G = GT > 0 ? GT : pv.G;
   const int nch_hi = pv.hi.t / kChunk, nch_lo = pv.lo.t / kChunk;
   const int wh = page_cost(G, nch_hi), wl = page_cost(G, nch_lo), hw = head_cost(G);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + W * kPageStages * a.stage_bytes);
@@ -848,7 +853,7 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
   float sq0, sq1;
   bool q_hi = ci.p < ci.hp;
   int cur_u = ci.u;
-  load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, q_hi, bq, sq0, sq1);
+  load_q1<GT>(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, q_hi, bq, sq0, sq1);
   const int jA = chunk_slot(g), jB = chunk_slot(g + 8);
   bool failed = false;
   for (int x = 0; x < n_pages; x++) {
@@ -872,14 +877,14 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
     const bool hi = d.z < 0;
     const int count = d.z & 0x7fffffff;
     if (d.x != cur_u) {           // the range enters the next head
-      publish(pv, a, S, cur_u, ctx.first_owner(cur_u, C), gw, lane);
+      publish<GT>(pv, a, S, cur_u, ctx.first_owner(cur_u, C), gw, lane);
       cur_u = d.x;
       q_hi = hi;
-      load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
+      load_q1<GT>(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
       lazy_reset(S);
     } else if (hi != q_hi) {      // from the head's hi pages to its lo pages
       q_hi = hi;
-      load_q1(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
+      load_q1<GT>(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
     }
     const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
     float* lgp = a.update ? a.logit + ((size_t)cur_u * a.max_chunks + d.w) * a.lrow : nullptr;
@@ -888,7 +893,7 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
     else
       attend_page<false>(S, sb, pv.lo, nch_lo, count, bq, sq0, sq1, lgp, a.lrow, d.y, G, g, t, jA, jB);
   }
-  if (!failed) publish(pv, a, S, cur_u, ctx.first_owner(cur_u, C), gw, lane);
+  if (!failed) publish<GT>(pv, a, S, cur_u, ctx.first_owner(cur_u, C), gw, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -996,7 +1001,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps, kWarpsPerSm / kAttnWarps) k_a
     }
     const int gx = g0 + x;
     if (gx >= cc.end) {           // the range crosses into the next head
-      publish(pv, a, S, cc.u, cc.begin / C, gw, lane);
+      publish<0>(pv, a, S, cc.u, cc.begin / C, gw, lane);
       cursor_seek(cc, gx, s_pref, pv, sa, a.layer, false);
       load_q(pv, a, cc.u / pv.hkv, cc.u % pv.hkv, g, t, bq_hi, bq_lo, sq0, sq1);
       S.reset();
@@ -1025,7 +1030,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps, kWarpsPerSm / kAttnWarps) k_a
     attend_chunk(S, hi, kA, kB, v0, v1, kmA, kmB, vmA, vmB, base + jA < count, base + jB < count, bq_hi, bq_lo,
                  sq0, sq1, lg, G, g, t);
   }
-  publish(pv, a, S, cc.u, cc.begin / C, gw, lane);
+  publish<0>(pv, a, S, cc.u, cc.begin / C, gw, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1423,9 +1428,17 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   a.lrow = (P.pv.G + 2) * kChunk;
   a.nwarps = P.sm_count * kWarpsPerSm;
   const dim3 grid(P.sm_count * (kWarpsPerSm / w)), block(32 * w);
-  cudaError_t e = !paged          ? launch_dependent(k_attn_decode, grid, block, (size_t)smem, st, P.pv, a, sa)
-                  : w == kWarpsPerSm ? launch_dependent(k_attn_paged<kWarpsPerSm>, grid, block, (size_t)smem, st, P.pv, a, sa)
-                                   : launch_dependent(k_attn_paged<kAttnWarps>, grid, block, (size_t)smem, st, P.pv, a, sa);
+  cudaError_t e;
+  if (!paged)
+    e = launch_dependent(k_attn_decode, grid, block, (size_t)smem, st, P.pv, a, sa);
+  else if (w != kWarpsPerSm)
+    e = launch_dependent(k_attn_paged<kAttnWarps, 0>, grid, block, (size_t)smem, st, P.pv, a, sa);
+  else if (P.pv.G == 4)
+    e = launch_dependent(k_attn_paged<kWarpsPerSm, 4>, grid, block, (size_t)smem, st, P.pv, a, sa);
+  else if (P.pv.G == 8)
+    e = launch_dependent(k_attn_paged<kWarpsPerSm, 8>, grid, block, (size_t)smem, st, P.pv, a, sa);
+  else
+    e = launch_dependent(k_attn_paged<kWarpsPerSm, 0>, grid, block, (size_t)smem, st, P.pv, a, sa);
   if (e != cudaSuccess) return e;
   // epilogue: merge and (with score updates) the new scores
   const int G = P.pv.G;
@@ -1563,8 +1576,10 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
 
 cudaError_t configure_attention() {
   const void* fns[] = {reinterpret_cast<const void*>(k_attn_decode),
-                       reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm>),
-                       reinterpret_cast<const void*>(k_attn_paged<kAttnWarps>),
+                       reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 4>),
+                       reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 8>),
+                       reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 0>),
+                       reinterpret_cast<const void*>(k_attn_paged<kAttnWarps, 0>),
                        reinterpret_cast<const void*>(k_attn_epi<1>), reinterpret_cast<const void*>(k_attn_epi<2>),
                        reinterpret_cast<const void*>(k_attn_epi<3>), reinterpret_cast<const void*>(k_attn_epi<4>),
                        reinterpret_cast<const void*>(k_attn_epi<5>), reinterpret_cast<const void*>(k_attn_epi<6>),
