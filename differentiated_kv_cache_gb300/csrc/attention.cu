@@ -39,15 +39,15 @@ constexpr int kMinChunks = 8;              // ring work items per warp at least
 // has no such order among its warps.
 constexpr int kWarpsPerSm = 16;
 // Paged path: a page's share of a warp's range, in cost units: a fixed part
-// for staging and bookkeeping plus a part per 16-slot chunk, whose ratio
-// grows with the group size (from per-warp timelines on GB300: a lo page of
-// two chunks takes 1.8 times a hi page at G = 4, 1.6 times at G = 8).
+// for staging and bookkeeping plus a part per 16-slot chunk (from per-warp
+// timelines on GB300: a lo page of two chunks takes 1.6 times a hi page at
+// G = 4 and at G = 8).
 __host__ __device__ __forceinline__ int page_cost(int G, int chunks) {
-  return G <= 4 ? 1 + 4 * chunks : 3 + 5 * chunks;
+  return G <= 4 ? 3 + 4 * chunks : 3 + 5 * chunks;
 }
 // A head's items start with a fixed cost for the warp that enters it mid-range
-// (the previous head's partial, the new queries): 2.5 to 3 us on GB300.
-__host__ __device__ __forceinline__ int head_cost(int G) { return G <= 4 ? 8 : 14; }
+// (the previous head's partial, the new queries): about one hi page.
+__host__ __device__ __forceinline__ int head_cost(int G) { return G <= 4 ? 9 : 8; }
 constexpr int kOffV = 2048;                // chunked stage image: V rows
 constexpr int kOffMeta = 3072;             // chunked stage image: page meta segments
 
