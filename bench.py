@@ -44,7 +44,7 @@ ATTN_TRAFFIC = {
     "workload": "llama8b",
     "bytes_per_call": 119_673_600 + 8_354_304 + 25_937_664,
     "sources": {
-        "attention.cu": "8706dbc71f636c9fb9e5bbc6a71a3121626dffb6a91b7de5228b243d312c8415",
+        "attention.cu": "698d960b729c03922d29c7d9cfad8c6cd063d4b7bc8d69b31a1222a246023e03",
         "dkv_common.cuh": "90d758348e6dbf3a1ae34973ef9bef33cbbd31e8c1a636103b676ac54b52f649",
         "dkv_kernels.cuh": "a11e8c64feb0a4bcfea04df84fe718b26a0fa6dc53df45de115fabf6c95d12fe",
     },

@@ -10,16 +10,20 @@
 //   O^T[128 x 8]       += Vcodes^T[128 x 16] . P'^T      (8 m-tiles)
 //   zsum[q]           += sum_tok p z_v                   (added to every feature)
 // Codes become exact fp16 integers in registers (byte/nibble placed under a
-// 1024 exponent, then the 1024 removed by hsub2/hfma2).
+// 1024 exponent, then the 1024 removed by hsub2/hfma2). P' enters the product
+// as an fp16 pair plus its fp16 residual (for G <= 4 in the spare query
+// columns 4..7, else in a second product).
 //
 // Work distribution: the sequences of all KV heads of the call are
-// concatenated and cut into equal contiguous ranges, one per warp of a
-// persistent grid (the sequence split of the page's kernel, balanced). A warp
-// writes a partial (m, l, O) for every head its range touches; the last warp
-// to finish a head merges the head's partials. Data is staged in shared memory
-// by bulk asynchronous copies completing on per-stage mbarriers:
+// concatenated (pages weighted by their measured cost) and cut into equal
+// contiguous ranges, one per warp of a persistent grid (the sequence split of
+// the page's kernel, balanced). A warp writes a partial (m, l, O) for every
+// head its range touches; the epilogue kernel, a programmatic dependent of
+// the attention kernel, merges each head's partials and updates its scores.
+// Data is staged in shared memory by bulk asynchronous copies completing on
+// per-stage mbarriers:
 //   k_attn_paged   pages of 16k tokens (chunk-aligned): one copy per page of
-//                  its contiguous K | V | K-meta | V-meta prefix;
+//                  its contiguous K | V | K-meta | V-meta | score prefix;
 //   k_attn_decode  any page geometry: per 16-slot chunk, one copy per page run.
 #include <algorithm>
 #include <mutex>
@@ -486,11 +490,11 @@ __device__ __forceinline__ int find_unit(const int* s_pref, int n_units, int g0)
 
 // ---------------------------------------------------------------------------
 // Paged path: pages of T = 16k tokens (k = 1, 2, ...), one bulk copy per page
-// of its first four segments (K rows, V rows, K meta, V meta are contiguous at
-// the page start). The work sequence is measured in cost units (a page weighs
-// page_cost(G, T/16)); a warp takes the pages that start inside its range.
-// One cursor walks the pages on the issue side and leaves a descriptor of
-// each staged page next to its stage. The softmax rescales lazily: a group's
+// of its first five segments (K rows, V rows, K meta, V meta, scores are
+// contiguous at the page start). The work sequence is measured in cost units
+// (a page weighs page_cost(G, T/16), a head starts with head_cost(G)); a warp
+// takes the pages that start inside its range, walked in batches of 32 pages
+// one per lane into a table of page descriptors. The softmax rescales lazily: a group's
 // probabilities are taken against the running maximum as long as no logit
 // exceeds it by more than kLazy (log2 units), so that the cross-lane maximum
 // and the rescale of O run only when the maximum really moves.
@@ -1038,15 +1042,17 @@ __global__ void __launch_bounds__(32 * kAttnWarps, kWarpsPerSm / kAttnWarps) k_a
 // the attention kernel: the merge of each head's partials into out and lse2
 // and, with score updates, every stored token's new score
 //   S_j += max over the group's queries of 2^(l2_j - lse2).
-// Grid (block, head). With score updates block x of a head takes its chunks
-// x EC .. x EC + EC - 1: warp 0 stages their scratch rows with one bulk copy
-// and derives the head's lse2 from its partials, warps 1..7 take the block's
-// share of the head's merge tasks (task t of a head spread over n blocks goes
-// to block t mod n; task = query t / 4, features 32 (t % 4) ..), then every
-// thread writes new scores. Without score updates the head's blocks share its
-// merge tasks on all warps. Everything a block needs before the attention
-// kernel completes (its head's counts and partial count in the attention
-// kernels' range partition) it derives from the head counts while it waits.
+// Grid (block, head), at most one wave of blocks. With score updates block x
+// of a head takes its chunk steps x, x + nb, ... (EC chunks each): warp 0
+// stages a step's scratch rows with one bulk copy; the head's merge tasks
+// (task t of a head spread over nb blocks goes to block t mod nb; task =
+// query t / 4, features 32 (t % 4) ..) run on the block's warps and, when
+// every query has a task in the block, hand it the head's lse2 (else warp 0
+// derives it from the partials); then every thread writes new scores.
+// Without score updates the head's blocks share its merge tasks on all
+// warps. Everything a block needs before the attention kernel completes (its
+// head's counts and partial count in the attention kernels' range partition)
+// it derives from the head counts while it waits.
 // ---------------------------------------------------------------------------
 constexpr int kEpiThreads = 256;
 constexpr int kEpiWarps = kEpiThreads / 32;
