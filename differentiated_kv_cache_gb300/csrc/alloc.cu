@@ -209,6 +209,9 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
   const int per = (n_units + kCoordThreads - 1) / kCoordThreads;
   const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
   if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
+  // the list counters, loaded with the plans (only this kernel moves them
+  // during a generation step)
+  const unsigned long long start = pv.ctl->start, end = pv.ctl->end;
   __syncthreads();
   int my_a = 0, my_f = 0;
   for (int u = u0; u < u1; u++) {
@@ -222,7 +225,6 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
   int tot_a, tot_f;
   const int aoff = block_exclusive_scan(my_a, s_warp, &tot_a);
   const int foff = block_exclusive_scan(my_f, s_warp, &tot_f);
-  const unsigned long long start = pv.ctl->start, end = pv.ctl->end;
   if (threadIdx.x == 0 && s_err == 0 && (unsigned long long)tot_a > end - start) s_err = DKV_ERR_NO_PAGES;
   __syncthreads();
   if (s_err != 0) {
@@ -238,15 +240,17 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
     const int i = u / pv.hkv, kvh = u % pv.hkv, slot = sa.slots[i];
     int* cn = pv.cnt(layer, slot, kvh);
     int* row = pv.row(layer, slot, kvh);
-    if (p.new_hp) row[cn[2]] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
-    if (p.new_lp) row[pv.L - 1 - cn[3]] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
+    // the page counts before the step, from the plan (new = old + new - freed)
+    const int php0 = p.php - p.new_hp + p.free_hp, plp0 = p.plp - p.new_lp + p.free_lp;
+    if (p.new_hp) row[php0] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
+    if (p.new_lp) row[pv.L - 1 - plp0] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
     if (p.free_hp) {
-      pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[cn[2] - 1];
-      row[cn[2] - 1] = -1;
+      pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[php0 - 1];
+      row[php0 - 1] = -1;
     }
     if (p.free_lp) {
-      pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[pv.L - cn[3]];
-      row[pv.L - cn[3]] = -1;
+      pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[pv.L - plp0];
+      row[pv.L - plp0] = -1;
     }
     cn[0] = p.nh; cn[1] = p.nl; cn[2] = p.php; cn[3] = p.plp;
     if (kvh == 0) pv.rq(layer, slot)[2] += 1;
