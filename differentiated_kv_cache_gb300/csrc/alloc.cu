@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
   __shared__ int s_warp[32];
   __shared__ int s_err, s_info;
   const int n_units = sa.n * pv.hkv;
-  const int per = (n_units + kCoordThreads - 1) / kCoordThreads;
+  const int per = (n_units + blockDim.x - 1) / blockDim.x;
   const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
   if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
   // the list counters, loaded with the plans (only this kernel moves them
@@ -335,11 +335,13 @@ cudaError_t configure_alloc() {
   return cudaFuncSetAttribute(k_free_request, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
 
-// A programmatic dependent of k_decode_plan.
+// A programmatic dependent of k_decode_plan. One CTA, a thread per head up to
+// 1024 (its block-wide scans wait at barriers for every warp of the block).
 cudaError_t launch_decode_alloc(Pool& P, int layer, const SlotArgs& sa, cudaStream_t st) {
+  const int n_units = sa.n * P.pv.hkv;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(1);
-  lc.blockDim = dim3(kCoordThreads);
+  lc.blockDim = dim3(std::min(kCoordThreads, (n_units + 31) / 32 * 32));
   lc.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
