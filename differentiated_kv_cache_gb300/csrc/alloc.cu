@@ -284,13 +284,18 @@ __global__ void __launch_bounds__(kCoordThreads) k_free_request(PoolView pv, int
   __syncthreads();
   const int tot = block_scan_array(s_c, n_units, s_warp);
   const unsigned long long end = pv.ctl->end;
-  for (int u = 0; u < n_units; u++) {
-    const int cnt = (u + 1 < n_units ? s_c[u + 1] : tot) - s_c[u];
-    if (cnt == 0) continue;
-    const int* row = pv.row(u / pv.hkv, slot, u % pv.hkv);
-    const int nh = s_h[u];
-    for (int x = threadIdx.x; x < cnt; x += blockDim.x)
-      pv.list[(end + (unsigned long long)(s_c[u] + x)) % pv.n_pages] = x < nh ? row[x] : row[pv.L - 1 - (x - nh)];
+  // page x of the request (in (layer, KV head) order, hi pages then lo pages
+  // from the outermost inward) goes to list position end + x; its head is the
+  // last u with s_c[u] <= x
+  for (int x = threadIdx.x; x < tot; x += blockDim.x) {
+    int lo = 0, hi = n_units - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_c[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int* row = pv.row(lo / pv.hkv, slot, lo % pv.hkv);
+    const int k = x - s_c[lo], nh = s_h[lo];
+    pv.list[(end + (unsigned long long)x) % pv.n_pages] = k < nh ? row[k] : row[pv.L - 1 - (k - nh)];
   }
   __syncthreads();
   for (int u = 0; u < n_units; u++) {
