@@ -29,20 +29,31 @@ __device__ __forceinline__ ArgMin shfl_amin(ArgMin a, int s) {
   return amin(a, b);
 }
 
-__device__ ArgMin block_amin(ArgMin a, ArgMin* s_tmp) {
+// Block-wide argmin of two keys at once (s_tmp: two entries per warp); every
+// thread returns with both results.
+__device__ void block_amin2(ArgMin& a, ArgMin& b, ArgMin* s_tmp) {
 #pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) a = shfl_amin(a, s);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) s_tmp[warp] = a;
+  for (int s = 16; s >= 1; s >>= 1) {
+    a = shfl_amin(a, s);
+    b = shfl_amin(b, s);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) {
+    s_tmp[warp] = a;
+    s_tmp[nw + warp] = b;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < (int)(blockDim.x >> 5); w++) a = amin(a, s_tmp[w]);
+    for (int w = 1; w < nw; w++) {
+      a = amin(a, s_tmp[w]);
+      b = amin(b, s_tmp[nw + w]);
+    }
     s_tmp[0] = a;
+    s_tmp[nw] = b;
   }
   __syncthreads();
   a = s_tmp[0];
-  __syncthreads();
-  return a;
+  b = s_tmp[nw];
 }
 
 __device__ __forceinline__ float key_importance(unsigned long long key) {
@@ -135,7 +146,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
                                                                SlotArgs sa) {
   pdl_launch_dependents();        // k_decode_alloc may launch; it waits for this grid
   if (pv.noop()) return;
-  __shared__ ArgMin s_tmp[kPlanThreads / 32];
+  __shared__ ArgMin s_tmp[2 * (kPlanThreads / 32)];
   __shared__ int s_xc, s_last;
   __shared__ float s_ic;
   const int c = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
@@ -185,8 +196,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
       bl = amin(bl, ArgMin{key, sl[k] - nh});
     }
   }
-  bh = block_amin(bh, s_tmp);
-  bl = block_amin(bl, s_tmp);
+  block_amin2(bh, bl, s_tmp);
   if (threadIdx.x == 0) {
     ScanPart& part = parts[(size_t)unit * max_parts + c];
     part.kh = bh.key; part.sh = bh.slot;
