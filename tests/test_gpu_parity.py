@@ -270,6 +270,37 @@ def test_decode_attention_parity(G, H, lens, steps, pb):
         assert_same(gp, op)
 
 
+def test_attention_large_pages_four_warp_ctas():
+    """Pages of 32 hi / 64 lo tokens (8 KB): the paged kernel's rings of 16
+    warps do not fit in shared memory, so it runs as four CTAs of 4 warps per
+    SM; outputs with and without score updates against the oracle."""
+    G, H, lens = 4, 2, [900, 333]
+    cfg = cfg_of(group_size=G, n_kv_heads=H, n_pages=1024, max_seq_len=1000, max_requests=2, page_bytes=8192,
+                 tokens_per_hi_page=32, tokens_per_lo_page=64)
+    n = sum(lens)
+    k = workloads.random_fp16((n, H, 128), 60, scale=1.5)
+    v = workloads.random_fp16((n, H, 128), 61)
+    S = workloads.given_scores(n, H, seed=62)
+    gp, op = both(cfg)
+    with gp:
+        assert (gp.t_hi, gp.t_lo) == (32, 64)
+        gp.prompt(0, [0, 1], lens, k, v, scores_in=S)
+        op.prompt(0, [0, 1], lens, k, v, scores_in=S)
+        for step, update in enumerate([False, True, True]):
+            q = workloads.random_fp16((2, H * G, 128), 650 + step, scale=2.0)
+            out = gp.attention(0, [0, 1], q, update=update)
+            rc, ref = op.attention(0, [0, 1], q, update_scores=update)
+            ok, worst = parity.within(out.astype(np.float64), ref, ATT_ATOL, ATT_RTOL)
+            assert ok, (step, worst)
+        gs, os_ = gp.snapshot(), op.snapshot()
+        for i in range(2):
+            for h in range(H):
+                for a, b in zip(stored(gs, (0, i, h), gp.t_hi, gp.t_lo, 4, np.float32),
+                                stored(os_, (0, i, h), gp.t_hi, gp.t_lo, 4, np.float32)):
+                    ok, worst = parity.within(a.astype(np.float64), b.astype(np.float64), 1e-6, 1e-4)
+                    assert ok, worst
+
+
 @pytest.mark.parametrize("pb", [4096, 3584])
 def test_attention_score_update(pb):
     cfg = cfg_of(group_size=4, n_kv_heads=2, n_pages=2048, max_requests=2, page_bytes=pb)
