@@ -51,7 +51,9 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            L = C.CDLL(build())
+            # DKV_ORACLE_LIB: load a separately built copy instead (the test that
+            # plants mistakes in copies of the oracle uses it)
+            L = C.CDLL(os.environ.get("DKV_ORACLE_LIB") or build())
             P, I, I64 = C.c_void_p, C.c_int, C.c_int64
             L.orc_half_to_float.argtypes = [C.c_uint16]; L.orc_half_to_float.restype = C.c_float
             L.orc_float_to_half.argtypes = [C.c_float]; L.orc_float_to_half.restype = C.c_uint16

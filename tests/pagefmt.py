@@ -97,3 +97,22 @@ def check_invariants(snap: dict, t_hi: int, t_lo: int, n_pages: int, reclaim: bo
             assert php == need_h and plp == need_l, (idx, c)
         else:
             assert php >= need_h and plp >= need_l, (idx, c)
+
+
+def segment_values(snap: dict, head: tuple, t_hi: int, t_lo: int, seg: int, dtype) -> tuple[np.ndarray, np.ndarray]:
+    """(hi, lo) arrays of segment `seg` (4 = score, 5 = position) of one
+    head's stored slots, in slot order (head = (layer, slot, kvh))."""
+    cnt = snap["head_counts"][head]
+    row = snap["table"][head]
+    L = row.shape[0]
+    out = []
+    for tier, n, t in ((HI, int(cnt[0]), t_hi), (LO, int(cnt[1]), t_lo)):
+        kb, vb = BITS[tier]
+        offs, _ = segment_offsets(t, kb, vb)
+        vals = []
+        for x in range(-(-n // t)):
+            page = row[x] if tier == HI else row[L - 1 - x]
+            nv = min(t, n - x * t)
+            vals.append(snap["pages"][page, offs[seg]: offs[seg] + 4 * nv].view(dtype))
+        out.append(np.concatenate(vals) if vals else np.zeros(0, dtype))
+    return out[0], out[1]
