@@ -97,3 +97,10 @@ def tiers_of(snap: dict, head: tuple, n: int, t_hi: int, t_lo: int) -> np.ndarra
     t[hi] = 2
     t[lo] = 1
     return t
+
+
+def load_into(op, snap: dict):
+    """Make oracle pool `op` hold the state of snapshot `snap` (the same
+    configuration): every later oracle step then starts from the GPU's state."""
+    for key in ("pages", "free_list", "table", "head_counts", "req_state", "pointers"):
+        getattr(op, key)[...] = snap[key]
