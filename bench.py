@@ -7,11 +7,19 @@ workload (32 requests x 4096-token prompts, 32 q / 8 KV heads):
   then 128 decode steps: [L2 flush] decode compact_step + decode_attention
   (with score update), then free_request for every request.
 value = decode-attention GB/s: algorithmic bytes (hi token 200 B, lo token
-104 B, +8 B score update, + q and out) over the device time of the
-decode_attention calls (CUDA events on the launch stream, L2 flushed before
-each call). compact_step is reported in us per layer.
+104 B, +8 B score update, + q and out) over the device time of one
+decode_attention call timed alone between CUDA events on its stream (L2
+flushed before each decode step). compact_step is reported in us per layer.
+
+The same loop then runs, untimed for the headline, on the 70B-shaped layer,
+on the 8B-shaped layer with 4 KB pages (the kernel for any page geometry),
+and on the Qwen2.5-7B-shaped GQA-7 batch; their figures, each with its own
+fraction of the HBM roofline, are in `parts`.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dkv|reference]
+
+With --gpus N > 1 outside torchrun the script starts N ranks itself (one
+process per GPU, torch.distributed.run on 127.0.0.1).
 """
 from __future__ import annotations
 
@@ -19,11 +27,13 @@ import argparse
 import hashlib
 import json
 import os
+import socket
 import statistics
 import subprocess
 import sys
 import tempfile
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -34,6 +44,11 @@ import workloads  # noqa: E402
 
 METRIC = "compressed-KV decode attn GB/s (% of GB300 HBM peak); compact_step µs/layer"
 HI_BYTES, LO_BYTES, SCORE_RMW = 200, 104, 8
+# kernels the library launches: prompt compact_step (setup, two tensor-core
+# scoring passes, lse merge, classification, three plan kernels, scatter,
+# two pack kernels), decode compact_step (plan, alloc, apply), decode
+# attention (attention, epilogue), free_request (one)
+LAUNCHES = {"prompt": 11, "decode": 3, "attention": 2, "free": 1}
 
 # DRAM bytes of one decode-attention call (k_attn_paged + k_attn_epi:
 # dram__bytes_read.sum + dram__bytes_write.sum, caches flushed by ncu before
@@ -49,20 +64,20 @@ ATTN_TRAFFIC = {
         "dkv_kernels.cuh": "a11e8c64feb0a4bcfea04df84fe718b26a0fa6dc53df45de115fabf6c95d12fe",
     },
 }
+L2_FLUSH_BYTES = 256 << 20
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, page_bytes: int | None = None):
     """The recorded per-call DRAM traffic when the attention sources still
     hash to those it was captured on, else None."""
-    if workload != ATTN_TRAFFIC["workload"]:
+    if workload != ATTN_TRAFFIC["workload"] or page_bytes not in (None, workloads.WORKLOADS[workload].page_bytes):
         return None
-    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "differentiated_kv_cache_gb300", "csrc")
+    csrc = os.path.join(ROOT, "differentiated_kv_cache_gb300", "csrc")
     for name, digest in ATTN_TRAFFIC["sources"].items():
         with open(os.path.join(csrc, name), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() != digest:
                 return None
     return ATTN_TRAFFIC["bytes_per_call"]
-L2_FLUSH_BYTES = 256 << 20
 
 
 def peaks():
@@ -95,7 +110,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -169,14 +184,21 @@ def barrier(dist):
         dist.barrier()
 
 
+def free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_ranks(n: int) -> int:
+    """Run this script as n ranks on this node (one process per GPU) and
+    return the launcher's exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 # --------------------------------------------------------------- workload
-def load_inputs(name: str, seed: int, decode_steps: int):
-    w = workloads.WORKLOADS[name]
-    inp = workloads.prompt_inputs(name, seed)
-    dec = [workloads.decode_inputs(name, t, seed) for t in range(decode_steps)]
-    return w, inp, dec
-
-
 def attn_bytes(hi_tokens: int, lo_tokens: int, n_req: int, hq: int, update: bool) -> int:
     per = HI_BYTES * hi_tokens + LO_BYTES * lo_tokens
     if update:
@@ -188,6 +210,159 @@ def prompt_bytes(hi_tokens: int, lo_tokens: int, n_tokens_heads: int, n_req: int
     return 512 * n_tokens_heads + 208 * hi_tokens + 112 * lo_tokens + n_req * 32 * hq * 256
 
 
+def describe(w, lens, T, page_bytes) -> str:
+    rng = f"{min(lens)}" if min(lens) == max(lens) else f"U{{{min(lens)}..{max(lens)}}}"
+    return (f"{w.name}: {w.shape or 'synthetic'}-shaped layer, {len(lens)} requests x {rng}-token prompts, "
+            f"{w.n_q_heads} q / {w.n_kv_heads} KV heads, d=128, {page_bytes}-byte pages, "
+            f"{T} decode steps with compaction and score update" + ("" if w.lo_enabled else ", low tier off"))
+
+
+class Loop:
+    """One workload on one GPU: its pool, device-resident inputs and the
+    benchmark step (prompt, T x [flush, decode compaction, attention with
+    score update], free every request)."""
+
+    def __init__(self, dkv, name: str, seed: int, dev, decode_steps: int | None = None,
+                 page_bytes: int | None = None, inputs=None):
+        import torch
+        self.dkv, self.torch, self.dev = dkv, torch, dev
+        self.w = w = workloads.WORKLOADS[name]
+        self.T = w.decode_steps if decode_steps is None else decode_steps
+        self.inp = inputs if inputs is not None else workloads.prompt_inputs(name, seed)
+        self.dec = [workloads.decode_inputs(name, t, seed) for t in range(self.T)]
+        self.lens = [int(x) for x in self.inp["lens"]]
+        cfg = w.pool_config()
+        cfg["max_seq_len"] = max(self.lens) + self.T
+        if page_bytes:
+            cfg["page_bytes"] = page_bytes
+        self.page_bytes = cfg["page_bytes"]
+        self.cfg = cfg
+        self.pool = dkv.dkv_pool_create(dkv.make_config(**{k: v for k, v in cfg.items()
+                                                          if k in dict(dkv.dkv_config._fields_)}), dev.index)
+        self.slots = list(range(w.n_requests))
+        self.k_d = torch.from_numpy(self.inp["k"]).to(dev)
+        self.v_d = torch.from_numpy(self.inp["v"]).to(dev)
+        self.q_d = torch.from_numpy(self.inp["q_obs"]).to(dev)
+        self.dk = torch.from_numpy(np.stack([d["k"] for d in self.dec])).to(dev)
+        self.dv = torch.from_numpy(np.stack([d["v"] for d in self.dec])).to(dev)
+        self.dq = torch.from_numpy(np.stack([d["q"] for d in self.dec])).to(dev)
+        self.out = torch.zeros((w.n_requests, w.n_q_heads, 128), dtype=torch.float32, device=dev)
+        # L2 flush between decode steps: write a buffer larger than L2, then
+        # read a second one so that the write-back of the dirty lines happens
+        # here and not inside the next timed kernel; L2 then holds none of the
+        # path's data.
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+
+    def close(self):
+        self.dkv.dkv_pool_destroy(self.pool)
+        self.pool = None
+
+    def launches_per_step(self) -> int:
+        return LAUNCHES["prompt"] + self.T * (LAUNCHES["decode"] + LAUNCHES["attention"]) + \
+            len(self.slots) * LAUNCHES["free"]
+
+    def step(self, record=None, counts=None):
+        """One pass of the path. record: dict of event-pair lists; counts:
+        list to fill with (phase, hi, lo) stored tokens (syncs)."""
+        dkv, torch, st = self.dkv, self.torch, self.stream
+        ev = lambda: torch.cuda.Event(enable_timing=True)
+        if record is not None:
+            e0, e1 = ev(), ev()
+            e0.record(st)
+        dkv.dkv_compact_step(self.pool, 0, dkv.DKV_PROMPT, self.slots, self.lens, self.k_d, self.v_d, self.q_d)
+        if record is not None:
+            e1.record(st)
+            record["prompt"].append((e0, e1))
+        if counts is not None:
+            s = dkv.dkv_pool_status(self.pool)
+            counts.append(("prompt", s["hi_tokens"], s["lo_tokens"]))
+        for t in range(self.T):
+            self.flush.fill_(t & 0xFF)
+            torch.amax(self.flush_rd)
+            # Even steps put an event between compaction and attention: the
+            # compaction and the call are timed alone. Odd steps do not: there
+            # the attention kernel launches while the compaction drains, as in
+            # a decode loop, and (compaction + attention) is timed as one.
+            split = t % 2 == 0
+            if record is not None:
+                c0, c1, a1 = ev(), ev(), ev()
+                c0.record(st)
+            dkv.dkv_compact_step(self.pool, 0, dkv.DKV_DECODE, self.slots, None, self.dk[t], self.dv[t])
+            if record is not None and split:
+                c1.record(st)
+            dkv.dkv_decode_attention(self.pool, 0, self.slots, self.dq[t], self.out, True)
+            if record is not None:
+                a1.record(st)
+                if split:
+                    record["compact"].append((c0, c1))
+                    record["attn_alone"].append((c1, a1))
+                else:
+                    record["pair"].append((c0, a1))
+            if counts is not None:
+                s = dkv.dkv_pool_status(self.pool)
+                counts.append(("attn", s["hi_tokens"], s["lo_tokens"]))
+        for s in self.slots:
+            dkv.dkv_free_request(self.pool, s)
+
+    def warm(self, n: int):
+        counts = []
+        for i in range(max(n, 1)):
+            self.step(counts=counts if i == 0 else None)
+        self.torch.cuda.synchronize()
+        st = self.dkv.dkv_pool_status(self.pool)
+        assert st["error"] == 0, st
+        self.prompt_counts = counts[0]
+        w = self.w
+        self.bytes_per_attn = [attn_bytes(c[1], c[2], w.n_requests, w.n_q_heads, True)
+                               for c in counts if c[0] == "attn"]
+        self.n_th = sum(self.lens) * w.n_kv_heads
+        self.pbytes = prompt_bytes(self.prompt_counts[1], self.prompt_counts[2], self.n_th, w.n_requests,
+                                   w.n_q_heads)
+
+    def timed(self, steps: int) -> dict:
+        torch = self.torch
+        rec = {"prompt": [], "compact": [], "attn_alone": [], "pair": []}
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        for _ in range(steps):
+            self.step(record=rec)
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        ms = lambda pairs: [a.elapsed_time(b) for a, b in pairs]
+        r = {"step_ms": t0.elapsed_time(t1) / steps, "prompt_ms": statistics.mean(ms(rec["prompt"])),
+             "compact_ms": statistics.mean(ms(rec["compact"])),
+             "alone_ms": statistics.mean(ms(rec["attn_alone"]))}
+        # in the loop: (compaction + attention) of the odd steps less the
+        # compaction alone of the even steps
+        r["loop_ms"] = statistics.mean(ms(rec["pair"])) - r["compact_ms"] if rec["pair"] else r["alone_ms"]
+        r["attn_bytes"] = sum(self.bytes_per_attn) / len(self.bytes_per_attn)
+        return r
+
+    def summary(self, r: dict, peak: float) -> dict:
+        """Per-workload figures, each against the HBM roofline."""
+        gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+        a_alone, a_loop = gbs(r["attn_bytes"], r["alone_ms"]), gbs(r["attn_bytes"], r["loop_ms"])
+        p = gbs(self.pbytes, r["prompt_ms"])
+        pc = self.prompt_counts
+        return {
+            "workload": describe(self.w, self.lens, self.T, self.page_bytes),
+            "decode_attention_us": round(r["alone_ms"] * 1e3, 2),
+            "decode_attention_gbs": round(a_alone, 1), "decode_attention_frac": round(a_alone / peak, 4),
+            "decode_attention_in_loop_us": round(r["loop_ms"] * 1e3, 2),
+            "decode_attention_in_loop_gbs": round(a_loop, 1),
+            "decode_attention_in_loop_frac": round(a_loop / peak, 4),
+            "attention_bytes_per_call": int(r["attn_bytes"]),
+            "compact_step_prompt_us_per_layer": round(r["prompt_ms"] * 1e3, 1),
+            "compact_step_prompt_gbs": round(p, 1), "compact_step_prompt_frac": round(p / peak, 4),
+            "compact_step_prompt_bytes": int(self.pbytes),
+            "compact_step_decode_us_per_layer": round(r["compact_ms"] * 1e3, 2),
+            "stored_tokens_after_prompt": {"hi": pc[1], "lo": pc[2], "pruned": self.n_th - pc[1] - pc[2]},
+            "kv_bytes_vs_fp16": round((HI_BYTES * pc[1] + LO_BYTES * pc[2]) / (self.n_th * 512), 4),
+        }
+
+
 # ------------------------------------------------------------- dkv (GPU)
 def run_dkv(args, world, rank, local):
     import torch
@@ -196,180 +371,89 @@ def run_dkv(args, world, rank, local):
     torch.cuda.set_device(local)
     dist = init_dist(world, "nccl")
     dev = torch.device("cuda", local)
-    w, inp, dec = load_inputs(args.workload, args.seed + rank, args.decode_steps)
-    H, G, R = w.n_kv_heads, w.group_size, w.n_requests
-    Hq = H * G
-    lens = [int(x) for x in inp["lens"]]
-    cfg = w.pool_config()
-    cfg["max_seq_len"] = max(lens) + args.decode_steps
-    pool = dkv.dkv_pool_create(dkv.make_config(**{k: v for k, v in cfg.items()
-                                                   if k in dict(dkv.dkv_config._fields_)}), local)
-    slots = list(range(R))
-    # device-resident inputs
-    k_d = torch.from_numpy(inp["k"]).to(dev)
-    v_d = torch.from_numpy(inp["v"]).to(dev)
-    q_d = torch.from_numpy(inp["q_obs"]).to(dev)
-    dk = torch.from_numpy(np.stack([d["k"] for d in dec])).to(dev)
-    dv = torch.from_numpy(np.stack([d["v"] for d in dec])).to(dev)
-    dq = torch.from_numpy(np.stack([d["q"] for d in dec])).to(dev)
-    out = torch.zeros((R, Hq, 128), dtype=torch.float32, device=dev)
-    # L2 flush between decode steps: write a buffer larger than L2, then read a
-    # second one so that the write-back of the dirty lines happens here and not
-    # inside the next timed kernel; L2 then holds none of the path's data.
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
-    T = args.decode_steps
-
-    def step(record=None, counts=None):
-        """One pass of the path. record: dict of event lists; counts: list to
-        fill with (hi, lo) stored tokens at each decode_attention (syncs)."""
-        ev = lambda: torch.cuda.Event(enable_timing=True)
-        if record is not None:
-            e0, e1 = ev(), ev()
-            e0.record(stream)
-        dkv.dkv_compact_step(pool, 0, dkv.DKV_PROMPT, slots, lens, k_d, v_d, q_d)
-        if record is not None:
-            e1.record(stream)
-            record["prompt"].append((e0, e1))
-        if counts is not None:
-            st = dkv.dkv_pool_status(pool)
-            counts.append(("prompt", st["hi_tokens"], st["lo_tokens"]))
-        for t in range(T):
-            flush.fill_(t & 0xFF)
-            torch.amax(flush_rd)
-            # Even steps put an event between compaction and attention (the
-            # compaction alone), odd steps do not: there the attention kernel
-            # launches while the compaction drains, as in a decode loop, and
-            # (compaction + attention) is timed as one.
-            split = t % 2 == 0
-            if record is not None:
-                c0, c1, a1 = ev(), ev(), ev()
-                c0.record(stream)
-            dkv.dkv_compact_step(pool, 0, dkv.DKV_DECODE, slots, None, dk[t], dv[t])
-            if record is not None and split:
-                c1.record(stream)
-            dkv.dkv_decode_attention(pool, 0, slots, dq[t], out, True)
-            if record is not None:
-                a1.record(stream)
-                if split:
-                    record["compact"].append((c0, c1))
-                    record["attn_split"].append((c1, a1))
-                else:
-                    record["pair"].append((c0, a1))
-            if counts is not None:
-                st = dkv.dkv_pool_status(pool)
-                counts.append(("attn", st["hi_tokens"], st["lo_tokens"]))
-        for s in slots:
-            dkv.dkv_free_request(pool, s)
-
-    # warm-up; the first warm-up step also records the stored-token counts
-    counts = []
-    for i in range(max(args.warmup, 1)):
-        step(counts=counts if i == 0 else None)
-    torch.cuda.synchronize()
-    st = dkv.dkv_pool_status(pool)
-    assert st["error"] == 0, st
-    prompt_counts = counts[0]
-    attn_counts = [c for c in counts if c[0] == "attn"]
-    bytes_per_attn = [attn_bytes(c[1], c[2], R, Hq, True) for c in attn_counts]
-    n_th = sum(lens) * H
-    pbytes = prompt_bytes(prompt_counts[1], prompt_counts[2], n_th, R, Hq)
-
-    rec = {"prompt": [], "compact": [], "attn_split": [], "pair": []}
+    peak, peak_kind = hbm_peak()
+    # each rank serves its own shard of requests: its own seed, its own pool
+    loop = Loop(dkv, args.workload, args.seed + rank, dev, decode_steps=args.decode_steps)
+    w = loop.w
+    loop.warm(args.warmup)
     barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for _ in range(args.steps):
-            step(record=rec)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+        r = loop.timed(args.steps)
     barrier(dist)
-    step_ms = t_start.elapsed_time(t_end) / args.steps
-    compact_ms = [a.elapsed_time(b) for a, b in rec["compact"]]
-    prompt_ms = [a.elapsed_time(b) for a, b in rec["prompt"]]
-    pair_ms = [a.elapsed_time(b) for a, b in rec["pair"]]
-    # a decode-attention call's time: (compaction + attention) of the odd
-    # steps less the compaction alone of the even steps; with one decode step
-    # only, the even step's attention after its event
-    if pair_ms:
-        call_ms = statistics.mean(pair_ms) - statistics.mean(compact_ms)
-    else:
-        call_ms = statistics.mean([a.elapsed_time(b) for a, b in rec["attn_split"]])
-    attn_ms = [call_ms] * (T * args.steps)
-    attn_total_ms = sum(attn_ms)
-    attn_total_bytes = sum(bytes_per_attn) * args.steps
-    step_ms_max = reduce_max(dist, step_ms, dev)
-    attn_ms_max = reduce_max(dist, attn_total_ms, dev)
-    all_bytes = reduce_sum(dist, attn_total_bytes, dev)
-    value = all_bytes / (attn_ms_max * 1e-3) / 1e9
-    peak, peak_kind = hbm_peak()
-    per_launch_bytes = sum(bytes_per_attn) / len(bytes_per_attn)
-    per_launch_ms = attn_total_ms / len(attn_ms)
-    achieved = per_launch_bytes / (per_launch_ms * 1e-3) / 1e9
+    step_ms_max = reduce_max(dist, r["step_ms"], dev)
+    call_ms_max = reduce_max(dist, r["alone_ms"], dev)
+    all_bytes = reduce_sum(dist, r["attn_bytes"], dev)
+    value = all_bytes / (call_ms_max * 1e-3) / 1e9
+    achieved = r["attn_bytes"] / (r["alone_ms"] * 1e-3) / 1e9
+    parts = loop.summary(r, peak)
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms_max, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
         "data": "synthetic (seeded numpy; model-shaped K/V/Q, no weights or datasets)",
         "config": {
-            "workload": f"{w.name}: {w.shape or 'synthetic'}-shaped layer, {R} requests x "
-                        f"{min(lens)}-{max(lens) if max(lens) != min(lens) else ''}".rstrip("-") +
-                        f"-token prompts, {Hq} q / {H} KV heads, d=128, {T} decode steps with compaction and "
-                        f"score update",
-            "requests": R, "prompt_len": lens[0], "decode_steps": T, "q_heads": Hq, "kv_heads": H,
-            "alpha_h": w.alpha_h, "alpha_l": w.alpha_l, "window": w.recent_window, "page_bytes": w.page_bytes,
+            "workload": parts["workload"],
+            "requests": w.n_requests, "prompt_len": loop.lens[0], "decode_steps": loop.T,
+            "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "alpha_h": w.alpha_h, "alpha_l": w.alpha_l,
+            "window": w.recent_window, "page_bytes": loop.page_bytes,
             "l2": "flushed before every decode step, outside the timed events: 256 MiB written, then a "
                   "second 256 MiB read (L2 left clean); prompt inputs 537 MB > L2",
-            "value_is": "decode-attention algorithmic bytes / decode_attention device time; a call's time is "
-                        "(compaction + attention) timed as one on odd decode steps, where the attention kernel "
-                        "launches while the compaction drains as in a decode loop, less the compaction alone "
-                        "timed on even steps",
-            "parallelism": f"{world} independent pools (one per GPU), no collective in the path",
+            "value_is": "decode-attention algorithmic bytes / device time of one decode_attention call timed "
+                        "alone between CUDA events on its stream (even decode steps), max over ranks; "
+                        "parts.decode_attention_in_loop_* time the call inside the decode loop, where it "
+                        "launches while the compaction drains",
+            "parallelism": f"{world} independent pools (one per GPU, each its own request shard), "
+                           f"no collective in the path",
         },
-        "parts": {
-            "compact_step_prompt_us_per_layer": round(statistics.mean(prompt_ms) * 1e3, 1),
-            "compact_step_prompt_gbs": round(pbytes / (statistics.mean(prompt_ms) * 1e-3) / 1e9, 1),
-            "compact_step_decode_us_per_layer": round(statistics.mean(compact_ms) * 1e3, 2),
-            "decode_attention_us": round(statistics.mean(attn_ms) * 1e3, 2),
-            "stored_tokens_after_prompt": {"hi": prompt_counts[1], "lo": prompt_counts[2],
-                                           "pruned": n_th - prompt_counts[1] - prompt_counts[2]},
-            "kv_bytes_vs_fp16": round((HI_BYTES * prompt_counts[1] + LO_BYTES * prompt_counts[2]) / (n_th * 512), 4),
-        },
+        "parts": parts,
         "roofline": {"bound": "hbm", "kernel": "dkv_decode_attention call (k_attn_paged + k_attn_epi)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                     "bytes_per_launch": int(per_launch_bytes),
+                     "bytes_per_launch": int(r["attn_bytes"]),
                      "traffic": args.traffic if args.traffic is not None else recorded_traffic(args.workload)},
-        # per step: prompt compact_step 11 kernels; per decode step 3 (compaction)
-        # + 2 (attention, epilogue); one free_request kernel per request
-        "gpu_launches": args.steps * (11 + T * 5 + R),
+        "gpu_launches": args.steps * loop.launches_per_step(),
     }
     result["clocks"] = clk.summary()
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, dkv, pool, w, inp, dec, lens, slots, sum(bytes_per_attn), dev, dist)
+        result["e2e"] = run_e2e(args, loop, dist)
+    loop.close()
+    headline_inputs = loop.inp
+    del loop
+    torch.cuda.empty_cache()
+    # the other configurations, each its own pool, outside the headline's timed region
+    extras = [] if args.extras in ("", "none") else args.extras.split(",")
+    result["parts"]["other_configs"] = {}
+    for name in extras:
+        wl, _, pb = name.partition("@")
+        ex = Loop(dkv, wl, args.seed + rank, dev, page_bytes=int(pb) if pb else None,
+                  decode_steps=min(workloads.WORKLOADS[wl].decode_steps, 32),
+                  inputs=headline_inputs if wl == args.workload else None)
+        ex.warm(1)
+        rr = ex.timed(args.extra_steps)
+        result["parts"]["other_configs"][name] = ex.summary(rr, peak)
+        ex.close()
+        del ex
+        torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args)
-    dkv.dkv_pool_destroy(pool)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 
 
-def run_e2e(args, dkv, pool, w, inp, dec, lens, slots, attn_bytes_step, dev, dist):
+def run_e2e(args, loop: Loop, dist):
     """The same step through the C ABI with inputs in pinned host memory:
     every step copies the prompt K/V/Q and each decode step's K/V/q to the
     device and reads each decode step's attention output back."""
     import torch
+    dkv, dev, w = loop.dkv, loop.dev, loop.w
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    hk, hv, hq = pin(inp["k"]), pin(inp["v"]), pin(inp["q_obs"])
-    hdk = [pin(d["k"]) for d in dec]
-    hdv = [pin(d["v"]) for d in dec]
-    hdq = [pin(d["q"]) for d in dec]
+    hk, hv, hq = pin(loop.inp["k"]), pin(loop.inp["v"]), pin(loop.inp["q_obs"])
+    hdk = [pin(d["k"]) for d in loop.dec]
+    hdv = [pin(d["v"]) for d in loop.dec]
+    hdq = [pin(d["q"]) for d in loop.dec]
     R, Hq = w.n_requests, w.n_q_heads
     hout = torch.empty((R, Hq, 128), dtype=torch.float32).pin_memory()
     k_d = torch.empty(hk.shape, dtype=torch.float16, device=dev)
@@ -379,11 +463,11 @@ def run_e2e(args, dkv, pool, w, inp, dec, lens, slots, attn_bytes_step, dev, dis
     dv = torch.empty_like(dk)
     dq = torch.empty(hdq[0].shape, dtype=torch.float16, device=dev)
     out = torch.empty((R, Hq, 128), dtype=torch.float32, device=dev)
-    T = args.decode_steps
+    T, pool, slots = loop.T, loop.pool, loop.slots
 
     def step():
         k_d.copy_(hk, non_blocking=True); v_d.copy_(hv, non_blocking=True); q_d.copy_(hq, non_blocking=True)
-        dkv.dkv_compact_step(pool, 0, dkv.DKV_PROMPT, slots, lens, k_d, v_d, q_d)
+        dkv.dkv_compact_step(pool, 0, dkv.DKV_PROMPT, slots, loop.lens, k_d, v_d, q_d)
         for t in range(T):
             dk.copy_(hdk[t], non_blocking=True); dv.copy_(hdv[t], non_blocking=True)
             dq.copy_(hdq[t], non_blocking=True)
@@ -402,7 +486,8 @@ def run_e2e(args, dkv, pool, w, inp, dec, lens, slots, attn_bytes_step, dev, dis
     dt = (time.perf_counter() - t0) / args.steps
     dt = reduce_max(dist, dt, dev)
     n = dist.get_world_size() if dist is not None else 1
-    h2d = hk.numel() * 2 + hv.numel() * 2 + hq.numel() * 2 + T * (hdk[0].numel() + hdv[0].numel() + hdq[0].numel()) * 2
+    attn_bytes_step = sum(loop.bytes_per_attn)
+    h2d = (hk.numel() + hv.numel() + hq.numel()) * 2 + T * (hdk[0].numel() + hdv[0].numel() + hdq[0].numel()) * 2
     d2h = T * hout.numel() * 4
     return {"value": round(n * attn_bytes_step / dt / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -412,41 +497,67 @@ def run_e2e(args, dkv, pool, w, inp, dec, lens, slots, attn_bytes_step, dev, dis
 
 
 # --------------------------------------------------- oracle (CPU baseline)
-def oracle_sample(name: str, seed: int, n_decode: int):
-    """The oracle as it stands on a bounded sample of the workload: one
-    request's prompt compaction (fp64 scoring) and n_decode decode steps
-    (compaction + fp64 attention with score update). Returns
-    (attention bytes, attention seconds, prompt seconds per layer-request)."""
+def _oracle_request(name: str, seed: int, r: int, n_decode: int):
+    """The oracle's pool for request r of the workload after its prompt
+    compaction (fp64 scoring); returns (pool, prompt seconds)."""
     import oracle
     w = workloads.WORKLOADS[name]
-    inp = workloads.prompt_inputs(name, seed, requests=[0])
-    cfg = w.pool_config(max_requests=1, max_seq_len=int(inp["lens"][0]) + n_decode, n_pages=
-                        2 * w.n_kv_heads * (int(inp["lens"][0]) // 18 + n_decode + 8))
+    inp = workloads.prompt_inputs(name, seed, requests=[r])
+    n0 = int(inp["lens"][0])
+    cfg = w.pool_config(max_requests=1, max_seq_len=n0 + n_decode,
+                        n_pages=2 * w.n_kv_heads * (n0 // 16 + n_decode + 8))
     pool = oracle.Pool(cfg)
     t0 = time.perf_counter()
-    rc = pool.prompt(0, [0], inp["lens"], inp["k"], inp["v"], inp["q_obs"])
-    tp = time.perf_counter() - t0
-    assert rc == 0
-    ab, at = 0, 0.0
-    for t in range(n_decode):
-        d = workloads.decode_inputs(name, t, seed, requests=[0])
-        assert pool.decode(0, [0], d["k"], d["v"]) == 0
-        hc = pool.head_counts[0, 0]
-        hi, lo = int(hc[:, 0].sum()), int(hc[:, 1].sum())
+    assert pool.prompt(0, [0], inp["lens"], inp["k"], inp["v"], inp["q_obs"]) == 0
+    return pool, time.perf_counter() - t0
+
+
+def oracle_sample(name: str, seed: int, requests: list[int], n_decode: int, threads: int) -> dict:
+    """The oracle as it stands on a bounded sample of the workload: the
+    prompt compaction (fp64 scoring) of each sampled request, then n_decode
+    decode steps (compaction, then fp64 attention with score update), the
+    requests run side by side on `threads` host threads (the oracle's C code
+    runs without the GIL; every request has a pool of its own). Times are
+    wall-clock over all threads: the prompt phase, and the attention calls
+    (decode compaction untimed)."""
+    import oracle
+    oracle.build()
+    w = workloads.WORKLOADS[name]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
         t0 = time.perf_counter()
-        rc, _ = pool.attention(0, [0], d["q"], update_scores=True)
-        at += time.perf_counter() - t0
-        ab += attn_bytes(hi, lo, 1, w.n_q_heads, True)
-    return ab, at, tp
+        res = list(ex.map(lambda r: _oracle_request(name, seed, r, n_decode), requests))
+        t_prompt = time.perf_counter() - t0        # includes drawing the inputs
+        pools = [p for p, _ in res]
+        prompt_cpu = sum(t for _, t in res)
+        ab, at = 0, 0.0
+        for t in range(n_decode):
+            d = [workloads.decode_inputs(name, t, seed, requests=[r]) for r in requests]
+            list(ex.map(lambda x: pools[x].decode(0, [0], d[x]["k"], d[x]["v"]), range(len(pools))))
+            for p in pools:
+                hc = p.head_counts[0, 0]
+                ab += attn_bytes(int(hc[:, 0].sum()), int(hc[:, 1].sum()), 1, w.n_q_heads, True)
+            t1 = time.perf_counter()
+            rcs = list(ex.map(lambda x: pools[x].attention(0, [0], d[x]["q"], update_scores=True)[0],
+                              range(len(pools))))
+            at += time.perf_counter() - t1
+            assert all(rc == 0 for rc in rcs)
+    return {"attn_bytes": ab, "attn_s": at, "prompt_wall_s": t_prompt, "prompt_cpu_s": prompt_cpu}
 
 
 def cpu_baseline(args) -> dict:
-    n_dec = 16
-    ab, at, tp = oracle_sample(args.workload, args.seed, n_dec)
-    return {"value": round(ab / at / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"1 of 32 requests (4096-token prompt, 8 KV heads), {n_dec} decode steps; "
-                      f"prompt compact_step of that request {tp * 1e3:.0f} ms (fp64 scoring)",
-            "compact_step_prompt_us_per_request_layer": round(tp * 1e6, 0)}
+    n_dec = 8
+    cores = os.cpu_count() or 1
+    w = workloads.WORKLOADS[args.workload]
+    reqs = list(range(min(cores, w.n_requests)))
+    mt = oracle_sample(args.workload, args.seed, reqs, n_dec, threads=len(reqs))
+    st = oracle_sample(args.workload, args.seed, [0], n_dec, threads=1)
+    return {"value": round(mt["attn_bytes"] / mt["attn_s"] / 1e9, 4), "unit": "GB/s", "cores": len(reqs),
+            "kind": "oracle",
+            "sample": f"{len(reqs)} of {w.n_requests} requests, one per host thread ({cores} cores seen), "
+                      f"{n_dec} decode steps each: decode attention (fp64) timed wall-clock over all threads",
+            "value_1thread": round(st["attn_bytes"] / st["attn_s"] / 1e9, 4),
+            "compact_step_prompt_us_per_request_layer_1thread": round(st["prompt_cpu_s"] * 1e6, 0),
+            "compact_step_prompt_us_per_request_layer": round(mt["prompt_cpu_s"] / len(reqs) * 1e6, 0)}
 
 
 def run_reference(args, world, rank):
@@ -455,46 +566,73 @@ def run_reference(args, world, rank):
         return
     import oracle
     oracle.build()
-    n_dec = 8
+    n_dec = 4
+    cores = os.cpu_count() or 1
+    w = workloads.WORKLOADS[args.workload]
+    reqs = list(range(min(cores, w.n_requests)))
     for _ in range(args.warmup):
-        oracle_sample(args.workload, args.seed, 1)
-    tot_b, tot_t, t_all = 0, 0.0, 0.0
+        oracle_sample(args.workload, args.seed, reqs[:1], 1, threads=1)
+    tot_b, tot_t = 0, 0.0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        ab, at, tp = oracle_sample(args.workload, args.seed, n_dec)
-        tot_b += ab
-        tot_t += at
+        s = oracle_sample(args.workload, args.seed, reqs, n_dec, threads=len(reqs))
+        tot_b += s["attn_bytes"]
+        tot_t += s["attn_s"]
     t_all = time.perf_counter() - t0
     value = tot_b / tot_t / 1e9
-    sample = f"1 of 32 requests (4096-token prompt, 8 KV heads), {n_dec} decode steps per step"
+    sample = (f"{len(reqs)} of {w.n_requests} requests, one per host thread, {n_dec} decode steps per step; "
+              f"decode attention (fp64) timed wall-clock over all threads")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_all / args.steps * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": f"{args.workload} (bounded sample: {sample})"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": len(reqs), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def run_dry(args, world, rank):
+    """--dry-run: the rank logic alone (gloo, no GPU): every rank joins, takes
+    its request shard, and rank 0 prints who took part."""
+    dist = init_dist(world, "gloo")
+    barrier(dist)
+    ranks = reduce_sum(dist, float(1 << rank))
+    seeds = reduce_sum(dist, float(args.seed + rank))
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "n_gpus": world, "rank_mask": int(ranks), "seed_sum": int(seeds)}),
+              flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["dkv", "reference"], default="dkv")
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--decode-steps", type=int, default=None)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--extras", default="llama70b,llama8b@4096,qwen7b",
+                    help="other configurations measured after the headline (workload[@page_bytes],...; 'none')")
+    ap.add_argument("--extra-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--dry-run", action="store_true", help="rank start-up and reductions only (gloo, no GPU)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu DRAM bytes per decode_attention launch, when known for this build")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(args.gpus))
     if args.decode_steps is None:
         args.decode_steps = workloads.WORKLOADS[args.workload].decode_steps
     world, rank, local = dist_env()
-    if args.impl == "reference":
+    if args.dry_run:
+        run_dry(args, world, rank)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_dkv(args, world, rank, local)

@@ -22,9 +22,11 @@ ATT_ATOL, ATT_RTOL = 1e-3, 2e-3
 # Scores: fp32 tensor-core logits and exp2 against fp64: relative error of a
 # few fp32 roundings per term, summed over at most 32 observation queries.
 SC_ATOL, SC_RTOL = 1e-6, 5e-5
-# Tie band: a token whose fp64 importance lies within this relative distance of
-# a threshold may land on either side.
-TIE_RTOL = 2e-3
+# Tie band, from the score tolerance: a GPU score within SC_ATOL + SC_RTOL*S of
+# the fp64 score gives an importance within that error over c, plus the fp32
+# roundings of I and of alpha/N (2^-22 relative); only a token whose fp64
+# importance lies that close to a threshold may land on the other side.
+ROUND_REL = 2.0 ** -22
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -128,12 +130,13 @@ def _tie_tokens(S64, lens, H, alpha_h, alpha_l, window, lo_enabled):
     t0 = 0
     for n0 in lens:
         j = np.arange(n0)
-        c = np.minimum(32, n0 - j)[:, None]
+        c = np.minimum(32, n0 - j)[:, None].astype(np.float64)
         I = S64[t0:t0 + n0] / c * n0
+        err = (SC_RTOL + ROUND_REL) * I + SC_ATOL / c * n0
         near = np.zeros_like(I, bool)
         for a in ([alpha_h, alpha_l] if lo_enabled else [alpha_l]):
             if np.isfinite(a) and a > 0:
-                near |= np.abs(I - a) <= TIE_RTOL * a
+                near |= np.abs(I - a) <= err + ROUND_REL * a
         near[j >= n0 - window] = False
         ties[t0:t0 + n0] = near
         t0 += n0

@@ -73,3 +73,13 @@ def test_reference_arm_other_ranks_exit_without_work(tmp_path):
                         "--steps", "1", "--warmup", "1"], env=env, capture_output=True, text=True, timeout=300)
     assert p.returncode == 0, p.stderr
     assert p.stdout.strip() == ""
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` outside torchrun starts two ranks itself; both join
+    the process group and take distinct request shards (seeds 0 and 1)."""
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--dry-run"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert p.returncode == 0, p.stderr
+    line = json.loads(p.stdout.strip().splitlines()[-1])
+    assert line["n_gpus"] == 2 and line["rank_mask"] == 3 and line["seed_sum"] == 1
