@@ -107,7 +107,9 @@ struct AttnArgs {
   float* logit;       // [unit][max_chunks][lrow]: chunk rows of [query < G][16 slots] log2-domain
                       // logits, then (paged path) the 16 old scores and the page ID
   float* lse2;        // [unit][G]
-  int max_parts, max_chunks;
+  ScanPart* vpart;    // [unit][max_vparts] victim-key partials of the epilogue's blocks, with
+  int* varrive;       // [unit] arrival counters (zero between calls); NULL: no victim keys
+  int max_parts, max_chunks, max_vparts;
   int lrow;           // floats per chunk row: (G + 2) * 16
   int nwarps;         // warps of the attention grid
   int update;
@@ -752,12 +754,22 @@ __device__ __forceinline__ void attend_page(AttnState& S, const uint8_t* sb, con
 
 // W: warps per CTA, 16 (one CTA per SM) or 4 (four CTAs per SM); GT: the
 // group size when fixed at compile time (4, 8), else 0 (pv.G)
+// With score updates, every request of the call counts one more update (the
+// importance denominator of the generation phase). Done by the attention
+// kernel's first block after its wait, so that the whole epilogue, which
+// waits for the attention grid, reads the advanced count.
+__device__ __forceinline__ void count_update(const PoolView& pv, const AttnArgs& a, const SlotArgs& sa) {
+  if (a.update && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < sa.n; i += blockDim.x) pv.rq(a.layer, sa.slots[i])[3] += 1;
+}
+
 template <int W, int GT>
 __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
   // a programmatic dependent of the kernel before it (counts, pages); the
   // epilogue grid, which reads the counts before its own wait, may launch
   // once every block is past the wait
   if (!dependent_begin<true>(pv)) return;
+  count_update(pv, a, sa);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_warp[W];
   const int n_units = sa.n * pv.hkv;
@@ -911,6 +923,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps, kWarpsPerSm / kAttnWarps) k_a
   // epilogue grid, which reads the counts before its own wait, may launch
   // once every block is past the wait
   if (!dependent_begin<true>(pv)) return;
+  count_update(pv, a, sa);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_warp[kAttnWarps];
   const int n_units = sa.n * pv.hkv;
@@ -1186,10 +1199,7 @@ __device__ void merge_task(const PoolView& pv, const AttnArgs& a, const SlotArgs
   if (lane == 0 && (sl == 0 || lse_dst != nullptr)) {
     const float lse2 = L > 0.0f ? M + log2f(L) : -INFINITY;
     if (lse_dst != nullptr) *lse_dst = lse2;
-    if (sl == 0) {
-      a.lse2[(size_t)u * G + qh] = lse2;
-      if (qh == 0 && a.update && kvh == 0) pv.rq(a.layer, sa.slots[i])[3] += 1;
-    }
+    if (sl == 0) a.lse2[(size_t)u * G + qh] = lse2;
   }
 }
 
@@ -1229,14 +1239,62 @@ __device__ void head_lse(const AttnArgs& a, int u, int np, int lane, float* dst)
   }
 }
 
-// A head that stores no token: zero output (G rows), lse2 = -inf, and the
-// request's update count (rq, when given) advanced, after the attention
-// kernel, whose writes come first.
-__device__ __noinline__ void empty_head(float* out, float* lse2, int* rq, int G) {
+// A head that stores no token: zero output (G rows) and lse2 = -inf, after
+// the attention kernel, whose writes come first.
+__device__ __noinline__ void empty_head(float* out, float* lse2, int G) {
   pdl_wait();
   for (int x = threadIdx.x; x < G * kD; x += blockDim.x) out[x] = 0.0f;
   if (threadIdx.x < G) lse2[threadIdx.x] = -INFINITY;
-  if (threadIdx.x == 0 && rq != nullptr) rq[3] += 1;
+}
+
+
+// Registers of a thread's slot positions per chunk step: four slots a
+// chunk-quarter (paged) or one slot (chunked) per iteration; at most 8.
+constexpr int kPosRegs = 8;
+static_assert(epi_chunks(1) * kChunk / kEpiThreads <= kPosRegs, "position registers");
+
+// Positions of this thread's slots in chunk step `step` of the head, in the
+// order the score-update loops visit them (0 where a slot is not stored).
+// Read from the pages through the table, neither of which the call changes.
+template <int EC>
+__device__ __forceinline__ void load_positions(const PoolView& pv, const int* row_tab, bool paged, int step, int nch,
+                                               int ch_hi, int nh, int nl, int* vp) {
+  const int c0 = step * EC, c1 = min(nch, c0 + EC);
+#pragma unroll
+  for (int e = 0; e < kPosRegs; e++) vp[e] = 0;
+  if (paged) {
+#pragma unroll
+    for (int k = 0; k < EC * kChunk / 4 / kEpiThreads; k++) {
+      const int x = k * kEpiThreads + threadIdx.x;
+      const int lc = c0 + (x >> 2), j0 = 4 * (x & 3);
+      if (lc >= c1) break;
+      const bool hi_t = lc < ch_hi;
+      const int s0 = (hi_t ? lc : lc - ch_hi) * kChunk + j0;
+      if (s0 >= (hi_t ? nh : nl)) continue;
+      const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+      const int d = tg.div(s0);
+      const int pid = __ldg(row_tab + (hi_t ? d : pv.L - 1 - d));
+      const int4 p = __ldcg(reinterpret_cast<const int4*>(pv.page(pid) + tg.off[5]) + ((s0 - d * tg.t) >> 2));
+      vp[4 * k] = p.x;
+      vp[4 * k + 1] = p.y;
+      vp[4 * k + 2] = p.z;
+      vp[4 * k + 3] = p.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < EC * kChunk / kEpiThreads; k++) {
+      const int x = k * kEpiThreads + threadIdx.x;
+      const int lc = c0 + x / kChunk, j = x % kChunk;
+      if (lc >= c1) break;
+      const bool hi_t = lc < ch_hi;
+      const int slot = (hi_t ? lc : lc - ch_hi) * kChunk + j;
+      if (slot >= (hi_t ? nh : nl)) continue;
+      const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+      const int d = tg.div(slot);
+      const int pid = __ldg(row_tab + (hi_t ? d : pv.L - 1 - d));
+      vp[k] = __ldcg(reinterpret_cast<const int*>(pv.page(pid) + tg.off[5]) + (slot - d * tg.t));
+    }
+  }
 }
 
 template <int G>
@@ -1253,8 +1311,7 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
   if (nh + nl == 0) {             // an empty head: zero output, lse2 = -inf
     if (xb == 0)
-      empty_head(a.out + ((size_t)i * pv.hkv + kvh) * G * kD, a.lse2 + (size_t)u * G,
-                 a.update && kvh == 0 ? pv.rq(a.layer, sa.slots[i]) : nullptr, G);
+      empty_head(a.out + ((size_t)i * pv.hkv + kvh) * G * kD, a.lse2 + (size_t)u * G, G);
     return;
   }
   const int ch_hi = (nh + kChunk - 1) / kChunk, nch = ch_hi + (nl + kChunk - 1) / kChunk;
@@ -1276,6 +1333,19 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   const int last = paged ? (begin + items - (nl > 0 ? wl : wh)) / C : (begin + items - 1) / C;
   const int np = last - first + 1;
   const EpiSmem L(G, a.update != 0);
+  // With score updates the block also leaves victim keys (pool scratch only);
+  // the positions of its first step's slots load now, before the wait: the
+  // table and the pages' position segments do not change in this call.
+  __shared__ int s_xc, s_last;
+  __shared__ float s_ic;
+  __shared__ ArgMin s_amin[2 * kEpiWarps];
+  const bool victims = a.update && a.vpart != nullptr && nb <= a.max_vparts;
+  const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
+  int vp[kPosRegs];
+  if (victims) {
+    load_positions<EC>(pv, row_tab, paged, xb, nch, ch_hi, nh, nl, vp);
+    if (threadIdx.x == 0) s_xc = -1;
+  }
   float* s_rows = reinterpret_cast<float*>(smem + L.rows);
   float* s_lse = reinterpret_cast<float*>(smem + L.lse);
   const uint32_t bar = smem_u32(smem + L.misc);
@@ -1315,82 +1385,161 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   float lse[G];
 #pragma unroll
   for (int qh = 0; qh < G; qh++) lse[qh] = s_lse[qh];
-  const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
+  // Victim keys of the head's next generation step, from the new scores:
+  // the step after this call has length N + 1, so t_c is position N - W and
+  // hi victims lie before N + 1 - W. The update count was advanced by the
+  // attention kernel, which this grid waited for.
+  int vn0 = 0, vN = 0, vupd = 0;
+  if (victims) {
+    const int* rq = pv.rq(a.layer, sa.slots[i]);
+    vn0 = __ldcg(rq + 1);
+    vN = __ldcg(rq + 2);
+    vupd = __ldcg(rq + 3);
+  }
+  const int vpc = vN - pv.window, vwlim = vN + 1 - pv.window;
+  ArgMin bh{~0ull, -1}, bl{~0ull, -1};
+  int xc = -1;
+  float ic = 0.0f;
   for (int step = xb, it = 0; step < nsteps; step += nb, it++) {
-  const int c0 = step * EC, c1 = min(nch, c0 + EC);
-  if (it > 0) {                   // the rows of this step, after every thread is done with the last
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t bytes = (uint32_t)(c1 - c0) * a.lrow * 4u;
-      mbar_expect_tx(bar, bytes);
-      bulk_g2s(smem_u32(s_rows), a.logit + ((size_t)u * a.max_chunks + c0) * a.lrow, bytes, bar);
-    }
-  }
-  // one decision for the block, so that no thread is left at a barrier
-  if (__syncthreads_or(!mbar_wait_bounded(bar, it & 1))) {
-    if (threadIdx.x == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = u;
-    mbar_wait_bounded(bar, it & 1);
-    return;
-  }
-  if (paged) {
-    // four consecutive slots of one chunk per thread (pages hold whole
-    // chunks, so the four share a page and their scores one 16-byte word):
-    // S_j += 2^(max over queries of (l2 - lse2))
-#pragma unroll
-    for (int k = 0; k < EC * kChunk / 4 / kEpiThreads; k++) {
-      const int x = k * kEpiThreads + threadIdx.x;
-      const int lc = c0 + (x >> 2), j0 = 4 * (x & 3);
-      if (lc >= c1) break;
-      const bool hi_t = lc < ch_hi;
-      const int s0 = (hi_t ? lc : lc - ch_hi) * kChunk + j0;
-      const int n = (hi_t ? nh : nl) - s0;      // valid slots among the four
-      if (n <= 0) continue;
-      const float* row = s_rows + (size_t)(lc - c0) * a.lrow;
-      float4 mx = *reinterpret_cast<const float4*>(row + j0);
-      mx.x -= lse[0]; mx.y -= lse[0]; mx.z -= lse[0]; mx.w -= lse[0];
-#pragma unroll
-      for (int qh = 1; qh < G; qh++) {
-        const float4 v = *reinterpret_cast<const float4*>(row + qh * kChunk + j0);
-        mx.x = fmaxf(mx.x, v.x - lse[qh]);
-        mx.y = fmaxf(mx.y, v.y - lse[qh]);
-        mx.z = fmaxf(mx.z, v.z - lse[qh]);
-        mx.w = fmaxf(mx.w, v.w - lse[qh]);
-      }
-      const float4 old = *reinterpret_cast<const float4*>(row + G * kChunk + j0);
-      const int pid = reinterpret_cast<const int*>(row)[(G + 1) * kChunk];
-      const TierGeom& tg = hi_t ? pv.hi : pv.lo;
-      float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (s0 - tg.div(s0) * tg.t);
-      const float4 nw = make_float4(old.x + fast_exp2(mx.x), old.y + fast_exp2(mx.y), old.z + fast_exp2(mx.z),
-                                    old.w + fast_exp2(mx.w));
-      if (n >= 4) {
-        *reinterpret_cast<float4*>(sp) = nw;
-      } else {
-        sp[0] = nw.x;
-        if (n > 1) sp[1] = nw.y;
-        if (n > 2) sp[2] = nw.z;
+    const int c0 = step * EC, c1 = min(nch, c0 + EC);
+    if (it > 0) {                 // the rows of this step, after every thread is done with the last
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)(c1 - c0) * a.lrow * 4u;
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(smem_u32(s_rows), a.logit + ((size_t)u * a.max_chunks + c0) * a.lrow, bytes, bar);
       }
     }
-    continue;
+    // the positions of the block's next step, in flight during this one
+    int vq[kPosRegs];
+    if (victims && step + nb < nsteps) load_positions<EC>(pv, row_tab, paged, step + nb, nch, ch_hi, nh, nl, vq);
+    // one decision for the block, so that no thread is left at a barrier
+    if (__syncthreads_or(!mbar_wait_bounded(bar, it & 1))) {
+      if (threadIdx.x == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = u;
+      mbar_wait_bounded(bar, it & 1);
+      return;
+    }
+    if (paged) {
+      // four consecutive slots of one chunk per thread (pages hold whole
+      // chunks, so the four share a page and their scores one 16-byte word):
+      // S_j += 2^(max over queries of (l2 - lse2))
+#pragma unroll
+      for (int k = 0; k < EC * kChunk / 4 / kEpiThreads; k++) {
+        const int x = k * kEpiThreads + threadIdx.x;
+        const int lc = c0 + (x >> 2), j0 = 4 * (x & 3);
+        if (lc >= c1) break;
+        const bool hi_t = lc < ch_hi;
+        const int s0 = (hi_t ? lc : lc - ch_hi) * kChunk + j0;
+        const int n = (hi_t ? nh : nl) - s0;      // valid slots among the four
+        if (n <= 0) continue;
+        const float* row = s_rows + (size_t)(lc - c0) * a.lrow;
+        float4 mx = *reinterpret_cast<const float4*>(row + j0);
+        mx.x -= lse[0]; mx.y -= lse[0]; mx.z -= lse[0]; mx.w -= lse[0];
+#pragma unroll
+        for (int qh = 1; qh < G; qh++) {
+          const float4 v = *reinterpret_cast<const float4*>(row + qh * kChunk + j0);
+          mx.x = fmaxf(mx.x, v.x - lse[qh]);
+          mx.y = fmaxf(mx.y, v.y - lse[qh]);
+          mx.z = fmaxf(mx.z, v.z - lse[qh]);
+          mx.w = fmaxf(mx.w, v.w - lse[qh]);
+        }
+        const float4 old = *reinterpret_cast<const float4*>(row + G * kChunk + j0);
+        const int pid = reinterpret_cast<const int*>(row)[(G + 1) * kChunk];
+        const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+        float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (s0 - tg.div(s0) * tg.t);
+        const float4 nw = make_float4(old.x + fast_exp2(mx.x), old.y + fast_exp2(mx.y), old.z + fast_exp2(mx.z),
+                                      old.w + fast_exp2(mx.w));
+        if (n >= 4) {
+          *reinterpret_cast<float4*>(sp) = nw;
+        } else {
+          sp[0] = nw.x;
+          if (n > 1) sp[1] = nw.y;
+          if (n > 2) sp[2] = nw.z;
+        }
+        if (victims) {
+          victim_token(nw.x, vp[4 * k], s0, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
+          if (n > 1) victim_token(nw.y, vp[4 * k + 1], s0 + 1, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
+          if (n > 2) victim_token(nw.z, vp[4 * k + 2], s0 + 2, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
+          if (n > 3) victim_token(nw.w, vp[4 * k + 3], s0 + 3, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < EC * kChunk / kEpiThreads; k++) {
+        const int x = k * kEpiThreads + threadIdx.x;
+        const int lc = c0 + x / kChunk, j = x % kChunk;
+        if (lc >= c1) break;
+        const bool hi_t = lc < ch_hi;
+        const int slot = (hi_t ? lc : lc - ch_hi) * kChunk + j;
+        if (slot >= (hi_t ? nh : nl)) continue;
+        const float* row = s_rows + (size_t)(lc - c0) * a.lrow;
+        float pm = 0.0f;
+#pragma unroll
+        for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, fast_exp2(row[qh * kChunk + j] - lse[qh]));
+        // chunked path: page from the table, old score from the page
+        const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+        const int d = tg.div(slot);
+        const int pid = __ldcg(row_tab + (hi_t ? d : pv.L - 1 - d));
+        float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (slot - d * tg.t);
+        const float ns = __ldcg(sp) + pm;
+        *sp = ns;
+        if (victims) victim_token(ns, vp[k], slot, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kPosRegs; e++) vp[e] = vq[e];
+  }
+  if (!victims) return;
+  // the block's victim keys, then the head's: the last of its nb blocks to
+  // arrive reduces the partials (warp 0, a partial a lane) and stamps the
+  // head's cache entry
+  if (xc >= 0) {                  // t_c is one slot of the head: at most one thread
+    s_xc = xc;
+    s_ic = ic;
+  }
+  block_amin2(bh, bl, s_amin);
+  if (threadIdx.x == 0) {
+    ScanPart& part = a.vpart[(size_t)u * a.max_vparts + xb];
+    part.kh = bh.key;
+    part.sh = bh.slot;
+    part.kl = bl.key;
+    part.sl = bl.slot;
+    part.xc = s_xc;
+    part.ic = s_ic;
+    __threadfence();
+    s_last = atomicAdd(a.varrive + u, 1) == nb - 1;
+  }
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  __threadfence();
+  ArgMin rh{~0ull, -1}, rl{~0ull, -1};
+  int rx = -1;
+  float ri = 0.0f;
+  for (int q = lane; q < nb; q += 32) {
+    const ScanPart* part = a.vpart + (size_t)u * a.max_vparts + q;
+    rh = amin(rh, ArgMin{__ldcg(&part->kh), __ldcg(&part->sh)});
+    rl = amin(rl, ArgMin{__ldcg(&part->kl), __ldcg(&part->sl)});
+    const int pxc = __ldcg(&part->xc);
+    if (pxc >= 0) {
+      rx = pxc;
+      ri = __ldcg(&part->ic);
+    }
   }
 #pragma unroll
-  for (int k = 0; k < EC * kChunk / kEpiThreads; k++) {
-    const int x = k * kEpiThreads + threadIdx.x;
-    const int lc = c0 + x / kChunk, j = x % kChunk;
-    if (lc >= c1) break;
-    const bool hi_t = lc < ch_hi;
-    const int slot = (hi_t ? lc : lc - ch_hi) * kChunk + j;
-    if (slot >= (hi_t ? nh : nl)) continue;
-    const float* row = s_rows + (size_t)(lc - c0) * a.lrow;
-    float pm = 0.0f;
-#pragma unroll
-    for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, fast_exp2(row[qh * kChunk + j] - lse[qh]));
-    // chunked path: page from the table, old score from the page
-    const TierGeom& tg = hi_t ? pv.hi : pv.lo;
-    const int d = tg.div(slot);
-    const int pid = __ldcg(row_tab + (hi_t ? d : pv.L - 1 - d));
-    float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (slot - d * tg.t);
-    *sp = __ldcg(sp) + pm;
+  for (int sft = 16; sft >= 1; sft >>= 1) {
+    rh = shfl_amin(rh, sft);
+    rl = shfl_amin(rl, sft);
   }
+  const unsigned has = __ballot_sync(0xffffffffu, rx >= 0);
+  const int src = has ? __ffs(has) - 1 : 0;
+  rx = __shfl_sync(0xffffffffu, rx, src);
+  ri = __shfl_sync(0xffffffffu, ri, src);
+  if (lane == 0) {
+    a.varrive[u] = 0;             // ready for the next call
+    VictimCache* vc = pv.vc(a.layer, sa.slots[i], kvh);
+    vc->p = ScanPart{rh.key, rl.key, rh.slot, rl.slot, rx, ri};
+    vc->n_stamp = vN;
+    vc->u_stamp = vupd;
   }
 }
 
@@ -1491,6 +1640,9 @@ cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tok
   a.part = P.sc.apart;
   a.logit = P.sc.alogit;
   a.lse2 = P.sc.alse;
+  a.vpart = P.sc.vpart;
+  a.varrive = P.sc.varrive;
+  a.max_vparts = P.sc.max_vparts;
   a.max_parts = P.sc.max_splits;
   a.max_chunks = P.sc.max_chunks;
   a.update = update_scores;
@@ -1573,6 +1725,9 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
   a.logit = reinterpret_cast<float*>(base + L.logit);
   a.max_parts = L.max_parts;
   a.max_chunks = L.max_chunks;
+  a.vpart = nullptr;              // no victim keys: the next generation step scans
+  a.varrive = nullptr;
+  a.max_vparts = 0;
   a.update = update_scores;
   a.layer = layer;
   // Nothing in the array needs clearing: every value a call reads from it

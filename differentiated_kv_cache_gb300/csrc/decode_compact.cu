@@ -17,45 +17,6 @@ namespace dkv {
 
 constexpr int kPlanThreads = 256;
 
-struct ArgMin {
-  unsigned long long key;   // order_key(importance) << 32 | position
-  int slot;
-};
-__device__ __forceinline__ ArgMin amin(ArgMin a, ArgMin b) { return b.key < a.key ? b : a; }
-__device__ __forceinline__ ArgMin shfl_amin(ArgMin a, int s) {
-  ArgMin b;
-  b.key = __shfl_xor_sync(0xffffffffu, a.key, s);
-  b.slot = __shfl_xor_sync(0xffffffffu, a.slot, s);
-  return amin(a, b);
-}
-
-// Block-wide argmin of two keys at once (s_tmp: two entries per warp); every
-// thread returns with both results.
-__device__ void block_amin2(ArgMin& a, ArgMin& b, ArgMin* s_tmp) {
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
-    a = shfl_amin(a, s);
-    b = shfl_amin(b, s);
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (lane == 0) {
-    s_tmp[warp] = a;
-    s_tmp[nw + warp] = b;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < nw; w++) {
-      a = amin(a, s_tmp[w]);
-      b = amin(b, s_tmp[nw + w]);
-    }
-    s_tmp[0] = a;
-    s_tmp[nw] = b;
-  }
-  __syncthreads();
-  a = s_tmp[0];
-  b = s_tmp[nw];
-}
-
 __device__ __forceinline__ float key_importance(unsigned long long key) {
   const uint32_t k = (uint32_t)(key >> 32);
   const uint32_t b = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
@@ -156,6 +117,17 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
   const int n0 = rq[1], n = rq[2] + 1, upd = rq[3];
   const int* cn = pv.cnt(layer, slot, kvh);
   const int nh = cn[0], nl = cn[1];
+  // The victim keys the last decode-attention call's score update left for
+  // this head, while the head is as that call left it (same length, same
+  // update count): no scan. The condition is the same for every thread.
+  const VictimCache* vc = pv.vc(layer, slot, kvh);
+  if (__ldcg(&vc->n_stamp) == rq[2] && __ldcg(&vc->u_stamp) == upd) {
+    if (c == 0 && threadIdx.x == 0) {
+      const ArgMin ch{__ldcg(&vc->p.kh), __ldcg(&vc->p.sh)}, cl{__ldcg(&vc->p.kl), __ldcg(&vc->p.sl)};
+      decide_plan(pv, layer, slot, kvh, unit, ch, cl, __ldcg(&vc->p.xc), __ldcg(&vc->p.ic), plans);
+    }
+    return;
+  }
   const int nparts = max(1, (nh + nl + kScanSlots - 1) / kScanSlots);
   if (c >= nparts) return;
   const int* row = pv.row(layer, slot, kvh);

@@ -55,6 +55,27 @@ struct CallArgs {
   long long tok0[kMaxCallReq + 1];
 };
 
+// Least important tokens of one head: the argmin keys (order_key(importance)
+// << 32 | position) of the hi tokens outside the recent window and of the lo
+// tokens, their slots (-1: none), and the hi slot and importance of t_c (-1:
+// not there). A partial covers part of a head's slots.
+struct ScanPart {
+  unsigned long long kh, kl;
+  int sh, sl;
+  int xc;
+  float ic;
+};
+
+// The victim keys of a head as the next generation step will see them,
+// computed by the score update of a decode-attention call, stamped with the
+// request's length N and update count after that call. A generation step
+// uses them only while both stamps still match the request state, else it
+// scans the head.
+struct VictimCache {
+  ScanPart p;
+  int n_stamp, u_stamp;
+};
+
 // Device view of a pool, passed by value to every kernel.
 struct PoolView {
   uint8_t* pages;
@@ -64,6 +85,7 @@ struct PoolView {
   int* req;          // [layer][slot][4]: active, N0, N, updates
   Ctl* ctl;
   CallArgs* call;
+  VictimCache* vcache;  // [layer][slot][kvh]
   int n_pages, page_bytes, n_layers, hkv, G, max_req, max_seq, L;
   int lo_enabled, window, slack, reclaim;
   float alpha_h, alpha_l;
@@ -74,6 +96,9 @@ struct PoolView {
   }
   __device__ __forceinline__ int* cnt(int layer, int slot, int kvh) const {
     return counts + ((size_t)((size_t)layer * max_req + slot) * hkv + kvh) * 4;
+  }
+  __device__ __forceinline__ VictimCache* vc(int layer, int slot, int kvh) const {
+    return vcache + ((size_t)layer * max_req + slot) * hkv + kvh;
   }
   __device__ __forceinline__ int* rq(int layer, int slot) const {
     return req + ((size_t)layer * max_req + slot) * 4;

@@ -29,13 +29,67 @@ struct DecodePlan {
   Move mv[2];
 };
 
-// Partial of a generation-phase scan over part of a head's slots.
-struct ScanPart {
-  unsigned long long kh, kl;   // argmin keys: hi outside the window, lo
-  int sh, sl;                  // their slots (-1: none)
-  int xc;                      // hi slot of t_c if in this part (-1: not here)
-  float ic;                    // importance of t_c
+// Argmin over tokens of (importance, position): key = order_key(importance)
+// << 32 | position, unique within a head; smaller wins (ties in importance go
+// to the smaller position).
+struct ArgMin {
+  unsigned long long key;
+  int slot;
 };
+__device__ __forceinline__ ArgMin amin(ArgMin a, ArgMin b) { return b.key < a.key ? b : a; }
+__device__ __forceinline__ ArgMin shfl_amin(ArgMin a, int s) {
+  ArgMin b;
+  b.key = __shfl_xor_sync(0xffffffffu, a.key, s);
+  b.slot = __shfl_xor_sync(0xffffffffu, a.slot, s);
+  return amin(a, b);
+}
+
+// Block-wide argmin of two keys at once (s_tmp: two entries per warp); every
+// thread returns with both results.
+__device__ __forceinline__ void block_amin2(ArgMin& a, ArgMin& b, ArgMin* s_tmp) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    a = shfl_amin(a, s);
+    b = shfl_amin(b, s);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) {
+    s_tmp[warp] = a;
+    s_tmp[nw + warp] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < nw; w++) {
+      a = amin(a, s_tmp[w]);
+      b = amin(b, s_tmp[nw + w]);
+    }
+    s_tmp[0] = a;
+    s_tmp[nw] = b;
+  }
+  __syncthreads();
+  a = s_tmp[0];
+  b = s_tmp[nw];
+}
+
+// One stored token's part in the victim search of the next generation step
+// (length n = N + 1 after its append, update count upd): its importance
+// S / c and argmin key; hi tokens before wlim = n - W are hi-victim
+// candidates, the hi token at pc = n - W - 1 is t_c, every lo token is a
+// lo-victim candidate.
+__device__ __forceinline__ void victim_token(float score, int pos, int slot, bool hi, int n0, int upd, int pc,
+                                             int wlim, ArgMin& bh, ArgMin& bl, int& xc, float& ic) {
+  const float imp = __fdiv_rn(score, (float)score_count(pos, n0, upd));
+  const unsigned long long key = ((unsigned long long)order_key(imp) << 32) | (uint32_t)pos;
+  if (hi) {
+    if (pos == pc) {
+      xc = slot;
+      ic = imp;
+    }
+    if (pos < wlim) bh = amin(bh, ArgMin{key, slot});
+  } else {
+    bl = amin(bl, ArgMin{key, slot});
+  }
+}
 
 // Device scratch owned by the pool (sizes fixed at creation).
 struct Scratch {
@@ -54,11 +108,14 @@ struct Scratch {
   DecodePlan* dplan;    // [units]
   ScanPart* dscan;      // [units][max_scan] partials of the generation-phase scan
   int* darrive;         // [units] scan CTAs arrived (zero between calls)
+  // victim keys from the attention epilogue's score update
+  ScanPart* vpart;      // [units][max_vparts] partials, one per epilogue block of a head
+  int* varrive;         // [units] epilogue blocks arrived (zero between calls)
   // decode attention
   float* apart;         // [units][max_splits][G*(128+2)]
   float* alogit;        // [units][max_chunks][(G + 2) * 16]: per chunk logits, old scores, page ID
   float* alse;          // [units][G]
-  int nkb_cap, grant_cap, max_splits, max_chunks, max_scan;
+  int nkb_cap, grant_cap, max_splits, max_chunks, max_scan, max_vparts;
 };
 
 // Host side of a pool.

@@ -287,3 +287,59 @@ def test_benchmark_loop_llama8b():
         assert st["error"] == 0
         assert int(gp.snapshot(pages=False)["req_state"][0, 0, 3]) == w.decode_steps
         print(f"llama8b: {len(check)} steps compared; stored hi {st['hi_tokens']} lo {st['lo_tokens']}")
+
+
+def test_generation_steps_after_mixed_attention_calls():
+    """Generation steps whose previous attention calls vary: score updates on
+    every request, on a subset, twice in a row, followed by a call without
+    update, through the allocation-free entry point, or no attention at all.
+    A step takes the victim keys a call's score update left only while the
+    request is as that call left it, and otherwise searches the head; every
+    step is compared with the oracle from the GPU's state."""
+    import differentiated_kv_cache_gb300 as dkv
+    H, G, lens, slots = 2, 4, [3000, 500, 40], [0, 1, 2]
+    cfg = dict(n_layers=2, n_kv_heads=H, group_size=G, head_dim=128, page_bytes=3584, n_pages=3000,
+               max_requests=3, max_seq_len=3200, tokens_per_hi_page=0, tokens_per_lo_page=0, lo_enabled=1,
+               alpha_h=2.0, alpha_l=0.25, recent_window=16, obs_window=32, prompt_grant_slack=1,
+               reclaim_in_decode=1)
+    n = sum(lens)
+    k = workloads.random_fp16((n, H, 128), 91, scale=1.5)
+    v = workloads.random_fp16((n, H, 128), 92)
+    S = workloads.given_scores(n, H, seed=93, scale=0.2)
+    op = oracle.Pool(cfg)
+
+    def attend(gp, layer, sl, step, update, static=False):
+        q = gp.dev(workloads.random_fp16((len(sl), H * G, 128), 3000 + 10 * step + len(sl), scale=2.0))
+        out = torch.empty((len(sl), H * G, 128), dtype=torch.float32, device="cuda")
+        f = dkv.dkv_decode_attention_static if static else dkv.dkv_decode_attention
+        f(gp.h, layer, sl, q, out, update)
+        torch.cuda.synchronize()
+
+    with GPool(cfg) as gp:
+        for layer in (0, 1):
+            gp.prompt(layer, slots, lens, k, v, scores_in=S)
+        for step in range(40):
+            layer = step % 2
+            kn = workloads.random_fp16((3, H, 128), 4000 + step)
+            vn = workloads.random_fp16((3, H, 128), 5000 + step)
+            load_into(op, gp.snapshot())
+            gp.decode(layer, slots, kn, vn)
+            assert op.decode(layer, slots, kn, vn) == 0
+            assert gp.status()["error"] == 0
+            _compare(gp, op)
+            kind = (step // 2) % 6
+            if kind == 0:
+                attend(gp, layer, slots, step, True)
+            elif kind == 1:
+                attend(gp, layer, [2, 0], step, True)
+                attend(gp, layer, slots, step, False)
+            elif kind == 2:
+                attend(gp, layer, slots, step, True)
+                attend(gp, layer, [1], step, True)
+            elif kind == 3:
+                attend(gp, layer, slots, step, True, static=True)
+            elif kind == 4:
+                attend(gp, layer, [1, 2], step, True)
+                attend(gp, 1 - layer, slots, step, True)
+            # kind 5: no attention before the next step of this layer
+        print("40 generation steps bit-exact after mixed attention calls")
