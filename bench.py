@@ -363,6 +363,98 @@ class Loop:
         }
 
 
+# ------------------------------------------------------------------ churn
+def run_churn(dkv, dev, seed: int, ticks: int, peak: float) -> dict:
+    """QwQ-32B-shaped long generation with requests arriving and finishing
+    (40 q / 8 KV heads, 1024-token prompts, U{128..512} generated tokens, at
+    most 64 at once): every tick admits waiting requests whose grant and
+    growth fit (one prompt compact_step), runs one generation compact_step
+    and one decode_attention with score update over every active request, and
+    frees the finished ones, so that the free list's counters wrap the pool.
+    Compaction and attention are timed alone with CUDA events."""
+    import torch
+    name = "qwq32b"
+    w = workloads.WORKLOADS[name]
+    H, Hq, R = w.n_kv_heads, w.n_q_heads, w.n_requests
+    gen_lo, gen_hi, n0 = 128, 512, 1024
+    n_pages = 32000
+    cfg = w.pool_config(n_pages=n_pages, max_seq_len=n0 + gen_hi + 1)
+    pool = dkv.dkv_pool_create(dkv.make_config(**{k: v for k, v in cfg.items()
+                                                  if k in dict(dkv.dkv_config._fields_)}), dev.index)
+    t_hi = dkv.dkv_pool_geometry(pool)["t_hi"]
+    rng = np.random.default_rng([seed, 0xC4])
+    inp = workloads.prompt_inputs(name, seed, requests=list(range(8)))
+    pk = torch.from_numpy(inp["k"]).to(dev)
+    pv_ = torch.from_numpy(inp["v"]).to(dev)
+    pq = torch.from_numpy(inp["q_obs"]).to(dev)
+    steps = [workloads.decode_inputs(name, t, seed) for t in range(16)]
+    dk = [torch.from_numpy(d["k"]).to(dev) for d in steps]
+    dv = [torch.from_numpy(d["v"]).to(dev) for d in steps]
+    dq = [torch.from_numpy(d["q"]).to(dev) for d in steps]
+    out = torch.empty((R, Hq, 128), dtype=torch.float32, device=dev)
+    st_ = torch.cuda.current_stream()
+    active, done = {}, 0
+    growth = lambda g: 2 * H * (g // t_hi + 2)
+    grant = H * (-(-n0 // t_hi) + 1)
+    comp, att, nact, abytes = [], [], [], []
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for tick in range(ticks):
+        s = dkv.dkv_pool_status(pool)
+        assert s["error"] == 0, s
+        budget = s["free_pages"] - sum(growth(t - g) for g, t in active.values())
+        new = []
+        for slot in range(R):
+            if slot in active or budget < grant + growth(gen_hi):
+                continue
+            active[slot] = [0, int(rng.integers(gen_lo, gen_hi + 1))]
+            budget -= grant + growth(active[slot][1])
+            new.append(slot)
+        for j in range(0, len(new), 8):      # prompts of 8 requests (the drawn inputs' batch)
+            sl = new[j:j + 8]
+            r = len(sl)
+            dkv.dkv_compact_step(pool, 0, dkv.DKV_PROMPT, sl, [n0] * r, pk[:r * n0], pv_[:r * n0], pq[:r])
+        if not active:
+            continue
+        slots = sorted(active)
+        n = len(slots)
+        x = tick % len(steps)
+        # the status read above left the GPU idle: a short device wait lets the
+        # tick's launches queue up behind it, so the events time the kernels
+        # and not the host's launch calls
+        torch.cuda._sleep(200_000)
+        e0, e1, e2 = ev(), ev(), ev()
+        e0.record(st_)
+        dkv.dkv_compact_step(pool, 0, dkv.DKV_DECODE, slots, None, dk[x][:n], dv[x][:n])
+        e1.record(st_)
+        dkv.dkv_decode_attention(pool, 0, slots, dq[x][:n], out[:n], True)
+        e2.record(st_)
+        comp.append((e0, e1))
+        att.append((e1, e2))
+        nact.append(n)
+        abytes.append(attn_bytes(s["hi_tokens"], s["lo_tokens"], n, Hq, True))
+        for slot in slots:
+            active[slot][0] += 1
+            if active[slot][0] >= active[slot][1]:
+                dkv.dkv_free_request(pool, slot)
+                del active[slot]
+                done += 1
+    torch.cuda.synchronize()
+    s = dkv.dkv_pool_status(pool)
+    assert s["error"] == 0, s
+    dkv.dkv_pool_destroy(pool)
+    c_us = [a.elapsed_time(b) * 1e3 for a, b in comp][16:]
+    a_us = [a.elapsed_time(b) * 1e3 for a, b in att][16:]
+    gbs = sum(abytes[16:]) / (sum(a_us) * 1e-6) / 1e9
+    return {"workload": f"{name}: QwQ-32B-shaped layer, {Hq} q / {H} KV heads, {n0}-token prompts, "
+                        f"U{{{gen_lo}..{gen_hi}}} generated tokens each, at most {R} requests at once, "
+                        f"{n_pages} pages, {ticks} ticks of admit / compact / attend / free",
+            "requests_finished": done, "mean_active": round(float(np.mean(nact)), 1),
+            "compact_step_decode_us_per_layer": round(float(np.mean(c_us)), 2),
+            "decode_attention_us": round(float(np.mean(a_us)), 2), "decode_attention_gbs": round(gbs, 1),
+            "decode_attention_frac": round(gbs / peak, 4),
+            "list_start": s["list_start"], "list_end": s["list_end"], "list_wraps": s["list_end"] // n_pages}
+
+
 # ------------------------------------------------------------- dkv (GPU)
 def run_dkv(args, world, rank, local):
     import torch
@@ -434,6 +526,9 @@ def run_dkv(args, world, rank, local):
         result["parts"]["other_configs"][name] = ex.summary(rr, peak)
         ex.close()
         del ex
+        torch.cuda.empty_cache()
+    if args.churn_ticks > 0:
+        result["parts"]["churn"] = run_churn(dkv, dev, args.seed + rank, args.churn_ticks, peak)
         torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args)
@@ -619,6 +714,8 @@ def main():
     ap.add_argument("--extras", default="llama70b,llama8b@4096,qwen7b",
                     help="other configurations measured after the headline (workload[@page_bytes],...; 'none')")
     ap.add_argument("--extra-steps", type=int, default=2)
+    ap.add_argument("--churn-ticks", type=int, default=1500,
+                    help="ticks of the QwQ-32B-shaped arrival / completion workload (0: skip)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--dry-run", action="store_true", help="rank start-up and reductions only (gloo, no GPU)")
