@@ -26,7 +26,6 @@
 //                  its contiguous K | V | K-meta | V-meta | score prefix;
 //   k_attn_decode  any page geometry: per 16-slot chunk, one copy per page run.
 #include <algorithm>
-#include <mutex>
 
 #include "dkv_kernels.cuh"
 
@@ -1660,10 +1659,6 @@ cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tok
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_attn_static_scratch[DKV_ATTN_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxStaticDevices = 64;
-static std::mutex g_static_mu;
-static void* g_static_base[kMaxStaticDevices];
-
 namespace {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -1690,20 +1685,16 @@ StaticLayout static_layout(int n_units, int G, int max_tokens, int update_scores
   return L;
 }
 
-// Address of the array on the current device, looked up once per device.
-cudaError_t static_scratch(int device, uint8_t** base) {
-  if (device < 0 || device >= kMaxStaticDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_base[device]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_static_base[device] = p;
-  }
-  *base = static_cast<uint8_t*>(g_static_base[device]);
-  return cudaSuccess;
-}
 }  // namespace
+
+// Address of the array on the current device (call with the pool's device
+// current). dkv_pool_create looks it up once and keeps it in the pool: a pool
+// made after the device's context was reset holds the address in the new
+// context.
+cudaError_t static_scratch_address(void** base) {
+  *base = nullptr;
+  return cudaGetSymbolAddress(base, g_attn_static_scratch);
+}
 
 size_t attention_static_bytes(const Pool& P, int n_units, int max_tokens, int update_scores) {
   return static_layout(n_units, P.pv.G, max_tokens, update_scores).total;
@@ -1714,9 +1705,8 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
   const int n_units = sa.n * P.pv.hkv;
   const StaticLayout L = static_layout(n_units, P.pv.G, max_tokens, update_scores);
   if (L.total > DKV_ATTN_STATIC_SCRATCH_BYTES) return cudaErrorInvalidValue;
-  uint8_t* base = nullptr;
-  cudaError_t e = static_scratch(P.device, &base);
-  if (e != cudaSuccess) return e;
+  uint8_t* base = static_cast<uint8_t*>(P.static_base);
+  if (base == nullptr) return cudaErrorInvalidSymbol;
   AttnArgs a;
   a.q = q;
   a.out = out;

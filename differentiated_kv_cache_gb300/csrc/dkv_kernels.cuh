@@ -128,6 +128,9 @@ struct Pool {
   std::vector<void*> allocations;
   // host mirror of request state: [layer][slot]
   std::vector<int> h_active, h_n0, h_n;
+  // device address of the static array of the allocation-free attention
+  // entry point on this pool's device (looked up at creation)
+  void* static_base = nullptr;
 };
 
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
@@ -143,6 +146,7 @@ cudaError_t launch_free(Pool& P, int slot, cudaStream_t st);
 // Allocation-free attention: bytes of the static array one call needs, and
 // the launcher over that array (attention.cu).
 size_t attention_static_bytes(const Pool& P, int n_units, int max_tokens, int update_scores);
+cudaError_t static_scratch_address(void** base);
 cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int max_tokens, const __half* q,
                                     float* out, int update_scores, cudaStream_t st);
 cudaError_t configure_kernels();

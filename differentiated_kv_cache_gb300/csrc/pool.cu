@@ -221,6 +221,8 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = configure_kernels();
+  // the allocation-free attention's array on this device, in this context
+  if (e == cudaSuccess) e = static_scratch_address(&P.static_base);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     free_all(P);

@@ -259,23 +259,28 @@ int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
  * allocating routine is called.
  *
  * Size limit: with U = n_req * n_kv_heads, C = ceil(max_n / 16) + 1 (max_n =
- * longest stored sequence among the call's requests) and r(x) = x rounded up
- * to 256, the call needs r(4UG) + r(4U(C/8 + 2)(128G + 16)) bytes, plus
- * 64(G + 2)UC if update_scores != 0. A larger call returns DKV_ERR_SCRATCH
- * and queues nothing.
+ * the largest current length N among the call's requests: prompt length
+ * plus generated tokens, pruned tokens included, not the stored count) and
+ * r(x) = x rounded up to 256, the call needs r(4UG) + r(4U(C/8 + 2)(128G + 16))
+ * bytes, plus 64(G + 2)UC if update_scores != 0. A larger call returns
+ * DKV_ERR_SCRATCH and queues nothing.
  *
- * Set-up: the first call on a device looks up the array's address on that
- * device (cudaGetSymbolAddress, with the pool's device current); make that
- * first call before any stream capture. Every call on a device shares the
- * array and it keeps the last call's contents; nothing in it has to start at
- * zero, because every value a call reads from the array (partials and the
- * per-chunk rows of logits, old scores and page IDs) is written earlier in
- * the same call.
+ * Set-up: dkv_pool_create looks up the array's address on the pool's device
+ * (cudaGetSymbolAddress, with that device current) and keeps it in the pool,
+ * so a call does no set-up of its own. A pool created after the device's
+ * context was reset (cudaDeviceReset) holds the address in the new context;
+ * pools from before a reset are unusable anyway. Every call on a device
+ * shares the array and it keeps the last call's contents; nothing in it has
+ * to start at zero, because every value a call reads from the array
+ * (partials and the per-chunk rows of logits, old scores and page IDs) is
+ * written earlier in the same call.
+ * This entry point leaves no victim keys for the next generation step, which
+ * then searches the heads itself (same result, more work).
  * Calls that overlap on the GPU (on different streams, or from different
  * pools of one device) race on the array and give wrong results: order them
  * on one stream or synchronise between them.
  * Errors: DKV_ERR_ARG, DKV_ERR_STATE, DKV_ERR_SCRATCH (host, nothing queued);
- * DKV_ERR_CUDA if the set-up lookup or a launch fails. */
+ * DKV_ERR_CUDA if a launch fails. */
 int dkv_decode_attention_static(dkv_pool* pool, int32_t layer, int32_t n_req,
                                 const int32_t* req_slots, const void* q, float* out,
                                 int32_t update_scores, void* stream);

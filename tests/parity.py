@@ -77,5 +77,9 @@ def compare_states(g: dict, o: dict, t_hi: int, t_lo: int, n_pages: int, page_by
 
 
 def within(gpu: np.ndarray, ref: np.ndarray, atol: float, rtol: float) -> tuple[bool, float]:
+    """Element-wise |gpu - ref| <= atol + rtol |ref|; (holds, worst excess)."""
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    if gpu.size == 0:
+        return True, -np.inf
     err = np.abs(gpu - ref) - (atol + rtol * np.abs(ref))
     return bool((err <= 0).all()), float(err.max())

@@ -1,18 +1,20 @@
 """dkv_decode_attention_static, the allocation-free decode attention, against
-dkv_decode_attention through the C ABI.
+dkv_decode_attention through the C ABI, and against the oracle.
 
 The static variant works in one fixed device array shared by every call, so
 the checks run two calls in a row (the second sees the first's leftovers)
 and compare each against the pool-scratch entry point on a twin pool holding
-the same state. This file is collected last so that, in a full run, the
-array has also seen every earlier use in the process."""
+the same state; the device's free memory must not change across any static
+call. This file is collected last so that, in a full run, the array has also
+seen every earlier use in the process."""
 from __future__ import annotations
 
 import numpy as np
 import pytest
 
+import oracle
 import workloads
-from tests.gpu_pool import GPool, stored
+from tests.gpu_pool import GPool, load_into, stored
 from tests import parity
 
 torch = pytest.importorskip("torch")
@@ -36,13 +38,26 @@ def cfg_of(**over):
     return c
 
 
+FREE_SEEN = []     # device free bytes around every static call: (before, after)
+
+
 def attend(gp, fn, slots, q, update):
+    """One attention call; around a static call the device's free memory is
+    recorded with everything the call uses already allocated."""
     import differentiated_kv_cache_gb300 as dkv
     qd = gp.dev(q)
     out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    before = torch.cuda.mem_get_info()[0]
     rc = getattr(dkv, fn)(gp.h, 0, slots, qd, out, update, check=False)
     torch.cuda.synchronize()
+    if fn.endswith("_static"):
+        FREE_SEEN.append((before, torch.cuda.mem_get_info()[0]))
     return rc, out.cpu().numpy()
+
+
+def assert_nothing_allocated():
+    assert FREE_SEEN and all(a == b for a, b in FREE_SEEN), FREE_SEEN
 
 
 def need_bytes(n_units, G, max_n, update):
@@ -53,9 +68,13 @@ def need_bytes(n_units, G, max_n, update):
     return b + (64 * (G + 2) * n_units * C if update else 0)
 
 
-@pytest.mark.parametrize("pb", [4096, 3584])
+@pytest.mark.parametrize("pb", [4096, 3584, 8192])
 def test_static_matches_pool_scratch_on_consecutive_calls(pb):
-    cfg = cfg_of(page_bytes=pb)
+    """4 KB pages (the kernel for any geometry), 3.5 KB pages (16 / 32 tokens,
+    the paged kernel) and 8 KB pages (32 / 64 tokens, the paged kernel as
+    four CTAs of 4 warps per SM)."""
+    FREE_SEEN.clear()
+    cfg = cfg_of(page_bytes=pb, **(dict(tokens_per_hi_page=32, tokens_per_lo_page=64) if pb == 8192 else {}))
     lens = [600, 257, 1100]
     n = sum(lens)
     k = workloads.random_fp16((n, 2, 128), 70, scale=1.5)
@@ -83,6 +102,66 @@ def test_static_matches_pool_scratch_on_consecutive_calls(pb):
                                 stored(sb, (0, i, h), gb.t_hi, gb.t_lo, 4, np.float32)):
                     ok, worst = parity.within(b.astype(np.float64), a.astype(np.float64), 1e-6, 1e-4)
                     assert ok, worst
+    assert_nothing_allocated()
+
+
+def test_static_against_oracle():
+    """Two static calls in a row with score updates, each against the
+    oracle's fp64 attention over the same state (outputs and updated scores),
+    so that a fault shared by both GPU entry points cannot pass unseen."""
+    FREE_SEEN.clear()
+    cfg = cfg_of(page_bytes=3584)
+    lens = [900, 333, 64]
+    n = sum(lens)
+    k = workloads.random_fp16((n, 2, 128), 90, scale=1.5)
+    v = workloads.random_fp16((n, 2, 128), 91)
+    S = workloads.given_scores(n, 2, seed=92)
+    op = oracle.Pool(cfg)
+    with GPool(cfg) as gp:
+        gp.prompt(0, [0, 1, 2], lens, k, v, scores_in=S)
+        for step in range(2):
+            load_into(op, gp.snapshot())
+            q = workloads.random_fp16((3, 8, 128), 900 + step, scale=2.0)
+            rc, out = attend(gp, "dkv_decode_attention_static", [0, 1, 2], q, True)
+            assert rc == 0
+            rc, ref = op.attention(0, [0, 1, 2], q, update_scores=True)
+            assert rc == 0
+            ok, worst = parity.within(out.astype(np.float64), ref, ATT_ATOL, ATT_RTOL)
+            assert ok, (step, worst)
+            gs, os_ = gp.snapshot(), op.snapshot()
+            assert (gs["req_state"] == os_["req_state"]).all()
+            for i in range(3):
+                for h in range(2):
+                    for a, b in zip(stored(gs, (0, i, h), gp.t_hi, gp.t_lo, 4, np.float32),
+                                    stored(os_, (0, i, h), gp.t_hi, gp.t_lo, 4, np.float32)):
+                        ok, worst = parity.within(a.astype(np.float64), b.astype(np.float64), 1e-6, 1e-4)
+                        assert ok, worst
+    assert_nothing_allocated()
+
+
+def test_static_limit_counts_pruned_tokens():
+    """The size limit follows each request's length N, pruned tokens
+    included: 64 requests of 4096 tokens with every token outside the recent
+    window pruned store 64 tokens a head, yet the call is refused, as the
+    header's formula with max_n = N says."""
+    import differentiated_kv_cache_gb300 as dkv
+    R, L, H, G = 64, 4096, 8, 8
+    cfg = cfg_of(n_kv_heads=H, group_size=G, max_requests=R, max_seq_len=L, page_bytes=3584,
+                 n_pages=R * H * (L // 16 + 2))
+    assert need_bytes(R * H, G, L, False) > dkv.DKV_ATTN_STATIC_SCRATCH_BYTES
+    assert need_bytes(R * H, G, 64, True) <= dkv.DKV_ATTN_STATIC_SCRATCH_BYTES
+    n = R * L
+    k = np.zeros((n, H, 128), np.float16)
+    S = np.zeros((n, H), np.float32)                 # importance 0: pruned outside the window
+    with GPool(cfg) as gp:
+        gp.prompt(0, list(range(R)), [L] * R, k, k, scores_in=S)
+        st = gp.status()
+        assert st["hi_tokens"] == R * H * 64 and st["lo_tokens"] == 0, st
+        q = workloads.random_fp16((R, H * G, 128), 95)
+        for update in (False, True):
+            rc, out = attend(gp, "dkv_decode_attention_static", list(range(R)), q, update)
+            assert rc == dkv.DKV_ERR_SCRATCH, rc
+            assert np.isnan(out).all()
 
 
 def test_static_rejects_calls_beyond_the_array():
@@ -90,6 +169,7 @@ def test_static_rejects_calls_beyond_the_array():
     partials: the call is refused on the host with nothing queued; half of
     them fit and match the pool-scratch entry point."""
     import differentiated_kv_cache_gb300 as dkv
+    FREE_SEEN.clear()
     R, L, H, G = 1024, 40, 8, 8
     cfg = cfg_of(n_kv_heads=H, group_size=G, max_requests=R, max_seq_len=64, n_pages=R * H * 5)
     assert need_bytes(R * H, G, L, False) > dkv.DKV_ATTN_STATIC_SCRATCH_BYTES
@@ -122,3 +202,4 @@ def test_static_rejects_calls_beyond_the_array():
             ok, worst = parity.within(out.astype(np.float64), ref.astype(np.float64), ATT_ATOL, ATT_RTOL)
             assert ok, (step, worst)
         assert (ga.snapshot(pages=False)["req_state"] == gb.snapshot(pages=False)["req_state"]).all()
+    assert_nothing_allocated()
