@@ -751,8 +751,6 @@ __device__ __forceinline__ void attend_page(AttnState& S, const uint8_t* sb, con
   }
 }
 
-// W: warps per CTA, 16 (one CTA per SM) or 4 (four CTAs per SM); GT: the
-// group size when fixed at compile time (4, 8), else 0 (pv.G)
 // With score updates, every request of the call counts one more update (the
 // importance denominator of the generation phase). Done by the attention
 // kernel's first block after its wait, so that the whole epilogue, which
@@ -762,6 +760,8 @@ __device__ __forceinline__ void count_update(const PoolView& pv, const AttnArgs&
     for (int i = threadIdx.x; i < sa.n; i += blockDim.x) pv.rq(a.layer, sa.slots[i])[3] += 1;
 }
 
+// W: warps per CTA, 16 (one CTA per SM) or 4 (four CTAs per SM); GT: the
+// group size when fixed at compile time (4, 8), else 0 (pv.G)
 template <int W, int GT>
 __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
   // a programmatic dependent of the kernel before it (counts, pages); the
