@@ -53,24 +53,36 @@ static int tc_smem_bytes(int n_req) {
 }
 
 // lse2[unit][h*32 + o] = m + log2(l) over the key tiles' partials (log2
-// domain); -inf for observation rows with a negative position.
-__global__ void k_prompt_lse_merge(PoolView pv, const float2* __restrict__ partial, float* lse2, int nkb_cap) {
+// domain); -inf for observation rows with a negative position. A warp per
+// row: lane k folds the partials of tiles k, k + 32, ... (their loads all in
+// flight at once), then the lanes combine by shuffles. Grid: (unit, row group
+// of kMergeWarps rows).
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(32 * kMergeWarps) k_prompt_lse_merge(PoolView pv, const float2* __restrict__ partial,
+                                                                       float* lse2, int nkb_cap) {
   if (!dependent_begin(pv)) return;
   const int unit = blockIdx.x, i = unit / pv.hkv;
   const int rows = kObs * pv.G;
+  const int r = blockIdx.y * kMergeWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= rows) return;
   const int n0 = pv.call->lens[i];
   const int nkb = (n0 + kKeyBlock - 1) / kKeyBlock;
-  for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-    float m = -INFINITY, l = 0.0f;
-    for (int kb = 0; kb < nkb; kb++) {
-      const float2 pl = partial[((size_t)unit * nkb_cap + kb) * rows + r];
-      const float mn = fmaxf(m, pl.x);
-      if (mn == -INFINITY) continue;
-      l = l * exp2f(m - mn) + pl.y * exp2f(pl.x - mn);
-      m = mn;
-    }
-    lse2[(size_t)unit * rows + r] = (l > 0.0f) ? m + log2f(l) : -INFINITY;
+  const float2* src = partial + (size_t)unit * nkb_cap * rows + r;
+  float m = -INFINITY, l = 0.0f;
+  for (int kb = lane; kb < nkb; kb += 32) {
+    const float2 pl = __ldcg(src + (size_t)kb * rows);
+    const float mn = fmaxf(m, pl.x);
+    if (mn == -INFINITY) continue;
+    l = l * exp2f(m - mn) + pl.y * exp2f(pl.x - mn);
+    m = mn;
   }
+  float M = m;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+  float L = M == -INFINITY || m == -INFINITY ? 0.0f : l * exp2f(m - M);
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) L += __shfl_xor_sync(0xffffffffu, L, s);
+  if (lane == 0) lse2[(size_t)unit * rows + r] = (L > 0.0f) ? M + log2f(L) : -INFINITY;
 }
 
 // SCORE = false: a1 (partial max and sum per query row and key tile).
@@ -482,8 +494,8 @@ cudaError_t launch_tc_g(Pool& P, const CUtensorMap& mk, const CUtensorMap& mq, i
   cudaError_t e = launch_dependent(k_prompt_tc<G, false>, dim3(P.sm_count), dim3(kTcThreads), (size_t)smem, st, P.pv,
                                    mk, mq, (const float*)nullptr, s.partial, (float*)nullptr, s.nkb_cap);
   if (e != cudaSuccess) return e;
-  e = launch_dependent(k_prompt_lse_merge, dim3(n_req * P.pv.hkv), dim3(256), 0, st, P.pv, (const float2*)s.partial,
-                       s.lse2, s.nkb_cap);
+  e = launch_dependent(k_prompt_lse_merge, dim3(n_req * P.pv.hkv, (kObs * P.pv.G + kMergeWarps - 1) / kMergeWarps),
+                       dim3(32 * kMergeWarps), 0, st, P.pv, (const float2*)s.partial, s.lse2, s.nkb_cap);
   if (e != cudaSuccess) return e;
   return launch_dependent(k_prompt_tc<G, true>, dim3(P.sm_count), dim3(kTcThreads), (size_t)smem, st, P.pv, mk, mq,
                           (const float*)s.lse2, (float2*)nullptr, score_out, s.nkb_cap);
