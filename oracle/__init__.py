@@ -71,6 +71,8 @@ def lib():
             L.orc_unit_attention.argtypes = [P, I, I, I, P, P, P]; L.orc_unit_attention.restype = I
             L.orc_decode_attention.argtypes = [P, I, I, P, P, P, I]; L.orc_decode_attention.restype = I
             L.orc_free_request.argtypes = [P, I]; L.orc_free_request.restype = I
+            L.orc_set_thresholds.argtypes = [P, I, P, P]; L.orc_set_thresholds.restype = I
+            L.orc_thresholds.argtypes = [P]; L.orc_thresholds.restype = P
             _lib = L
     return _lib
 
@@ -221,7 +223,22 @@ class Pool:
     def free_request(self, slot):
         return lib().orc_free_request(self._h, int(slot))
 
+    def set_thresholds(self, layer, alpha_h, alpha_l):
+        """Per-head thresholds of one layer (arrays of n_kv_heads floats)."""
+        ah = np.ascontiguousarray(alpha_h, dtype=np.float32)
+        al = np.ascontiguousarray(alpha_l, dtype=np.float32)
+        assert ah.size == al.size == self.cfg["n_kv_heads"]
+        return lib().orc_set_thresholds(self._h, int(layer), _ptr(ah), _ptr(al))
+
+    @property
+    def thresholds(self):
+        """Live view [layer][kvh][alpha_h, alpha_l]."""
+        c = self.cfg
+        return self._view("orc_thresholds", np.float32, c["n_layers"] * c["n_kv_heads"] * 2).reshape(
+            c["n_layers"], c["n_kv_heads"], 2)
+
     def snapshot(self) -> dict:
         return dict(pages=self.pages.copy(), free_list=self.free_list.copy(),
                     pointers=self.pointers.copy(), table=self.table.copy(),
-                    head_counts=self.head_counts.copy(), req_state=self.req_state.copy())
+                    head_counts=self.head_counts.copy(), req_state=self.req_state.copy(),
+                    thresholds=self.thresholds.copy())

@@ -134,6 +134,7 @@ typedef struct {
   int32_t* table;              /* [layer][slot][kvh][table_len] */
   int32_t* counts;             /* [layer][slot][kvh][4] hi tok, lo tok, hi pages, lo pages */
   int32_t* req;                /* [layer][slot][4] active, N0, N, updates */
+  float* alpha;                /* [layer][kvh][2] alpha_h, alpha_l of each head */
 } orc_pool;
 
 static int round16(int x) { return (x + 15) & ~15; }
@@ -191,12 +192,35 @@ orc_pool* orc_pool_new(const orc_config* c) {
   for (size_t i = 0; i < heads * p->table_len; i++) p->table[i] = -1;
   p->counts = (int32_t*)calloc(heads * 4, sizeof(int32_t));
   p->req = (int32_t*)calloc((size_t)c->n_layers * c->max_requests * 4, sizeof(int32_t));
+  /* every head starts with the configuration's thresholds */
+  p->alpha = (float*)malloc(sizeof(float) * 2 * (size_t)c->n_layers * c->n_kv_heads);
+  for (int x = 0; x < c->n_layers * c->n_kv_heads; x++) {
+    p->alpha[2 * x] = c->alpha_h;
+    p->alpha[2 * x + 1] = c->alpha_l;
+  }
   return p;
 }
 
+/* Compaction policy, extensibility: thresholds set for each head on its own
+ * (here per layer and KV head). Later steps of `layer` compare head h's
+ * tokens with ah[h]/N and al[h]/N. */
+int orc_set_thresholds(orc_pool* p, int layer, const float* ah, const float* al) {
+  if (layer < 0 || layer >= p->c.n_layers || !ah || !al) return ORC_ERR_ARG;
+  for (int h = 0; h < p->c.n_kv_heads; h++) {
+    if (isnan(ah[h]) || isnan(al[h])) return ORC_ERR_ARG;
+  }
+  for (int h = 0; h < p->c.n_kv_heads; h++) {
+    p->alpha[2 * ((size_t)layer * p->c.n_kv_heads + h)] = ah[h];
+    p->alpha[2 * ((size_t)layer * p->c.n_kv_heads + h) + 1] = al[h];
+  }
+  return ORC_OK;
+}
+
+float* orc_thresholds(orc_pool* p) { return p->alpha; }
+
 void orc_pool_free(orc_pool* p) {
   if (!p) return;
-  free(p->pages); free(p->list); free(p->table); free(p->counts); free(p->req);
+  free(p->pages); free(p->list); free(p->table); free(p->counts); free(p->req); free(p->alpha);
   free(p);
 }
 
@@ -339,10 +363,10 @@ static int score_count(int j, int n0, int updates) {
 
 static float importance(float score, int count) { return score / (float)count; }
 
-/* three-way split against alpha_h/N and alpha_l/N; with the lo tier disabled
- * a token that would be lo is kept at hi precision */
-static int classify(const orc_config* c, float imp, int n) {
-  float th_h = c->alpha_h / (float)n, th_l = c->alpha_l / (float)n;
+/* three-way split against alpha_h/N and alpha_l/N (the head's thresholds);
+ * with the lo tier disabled a token that would be lo is kept at hi precision */
+static int classify(const orc_config* c, const float* alpha, float imp, int n) {
+  float th_h = alpha[0] / (float)n, th_l = alpha[1] / (float)n;
   if (c->lo_enabled) {
     if (imp > th_h) return TIER_HI;
     if (imp >= th_l) return TIER_LO;
@@ -446,7 +470,7 @@ int orc_prompt_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
         S32[t] = s32;
         int tr;
         if (j >= n0 - c->window) tr = TIER_HI;            /* recent window */
-        else tr = classify(c, importance(s32, score_count(j, n0, 0)), n0);
+        else tr = classify(c, p->alpha + 2 * ((size_t)layer * H + h), importance(s32, score_count(j, n0, 0)), n0);
         tier[t] = (uint8_t)tr;
         if (tr == TIER_HI) nhi[i * H + h]++;
         else if (tr == TIER_LO) nlo[i * H + h]++;
@@ -581,8 +605,9 @@ int orc_decode_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
   for (int i = 0; i < n_req; i++) {
     int32_t* rs = rstate(p, layer, slots[i]);
     const int n0 = rs[1], n = rs[2] + 1, upd = rs[3];
-    const float th_h = c->alpha_h / (float)n, th_l = c->alpha_l / (float)n;
     for (int h = 0; h < H; h++) {
+      const float* alpha = p->alpha + 2 * ((size_t)layer * H + h);
+      const float th_h = alpha[0] / (float)n, th_l = alpha[1] / (float)n;
       head_plan* q = &pl[i * H + h];
       int32_t* cn = hcnt(p, layer, slots[i], h);
       int32_t* row = trow(p, layer, slots[i], h);
@@ -615,7 +640,7 @@ int orc_decode_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
         for (int x = 0; x < q->nh; x++) if (q->hi[x].pos == pc) { xc = x; break; }
         if (xc < 0) { status = ORC_ERR_CHECK; }
         else {
-          int tc = classify(c, q->hi[xc].imp, n);
+          int tc = classify(c, alpha, q->hi[xc].imp, n);
           if (tc == TIER_HI) {
             /* t_c stays hi; the least important hi token outside the window is the victim */
             int xv = argmin_imp(q->hi, q->nh, n - c->window);

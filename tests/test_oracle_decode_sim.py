@@ -254,6 +254,8 @@ def same_record(a: dict, b: dict) -> bool:
 # -------------------------------------------------------------------- test
 VARIANTS = {
     "updates": dict(updates=True, lo_enabled=1, recent_window=4),
+    # thresholds set for each KV head on its own (Compaction policy, extensibility)
+    "per_head_thresholds": dict(updates=True, lo_enabled=1, recent_window=4, per_head=((2.0, 0.25), (1.0, 0.6))),
     "no_updates_w1": dict(updates=False, lo_enabled=1, recent_window=1),
     "lo_disabled": dict(updates=True, lo_enabled=0, recent_window=4),
     "close_thresholds": dict(updates=True, lo_enabled=1, recent_window=3, alpha_h=1.0, alpha_l=0.6),
@@ -264,6 +266,7 @@ VARIANTS = {
 def test_decode_step_matches_simulator(variant):
     v = dict(VARIANTS[variant])
     updates = v.pop("updates")
+    per_head = v.pop("per_head", None)
     cfg = dict(n_layers=1, n_kv_heads=2, group_size=1, head_dim=128, page_bytes=4096, n_pages=900,
                max_requests=4, max_seq_len=400, tokens_per_hi_page=4, tokens_per_lo_page=8, lo_enabled=1,
                alpha_h=2.0, alpha_l=0.25, recent_window=4, obs_window=32, prompt_grant_slack=1,
@@ -274,6 +277,10 @@ def test_decode_step_matches_simulator(variant):
     slots, lens = [0, 1, 3], [40, 2, 70]
     n_tok = sum(lens)
     pool = oracle.Pool(cfg)
+    alphas = [(cfg["alpha_h"], cfg["alpha_l"])] * H
+    if per_head is not None:
+        alphas = list(per_head)
+        assert pool.set_thresholds(0, [a for a, _ in alphas], [b for _, b in alphas]) == 0
     k = workloads.random_fp16((n_tok, H, 128), 5)
     vv = workloads.random_fp16((n_tok, H, 128), 6)
     assert pool.prompt(0, slots, lens, k, vv, scores_in=workloads.given_scores(n_tok, H, seed=7)) == 0
@@ -295,8 +302,8 @@ def test_decode_step_matches_simulator(variant):
         # crafted scores, written into the oracle's pages
         for s in slots:
             n = N[s] + 1
-            th_h, th_l = F32(cfg["alpha_h"]) / F32(n), F32(cfg["alpha_l"]) / F32(n)
             for kvh in range(H):
+                th_h, th_l = F32(alphas[kvh][0]) / F32(n), F32(alphas[kvh][1]) / F32(n)
                 h = sim[(s, kvh)]
                 info = design_scores(h, n, W, th_h, th_l, lo_enabled, rng)
                 b = (info.get("branch"), info.get("floor"))
@@ -312,8 +319,8 @@ def test_decode_step_matches_simulator(variant):
         aoff = 0
         for i, s in enumerate(slots):
             n = N[s] + 1
-            th_h, th_l = F32(cfg["alpha_h"]) / F32(n), F32(cfg["alpha_l"]) / F32(n)
             for kvh in range(H):
+                th_h, th_l = F32(alphas[kvh][0]) / F32(n), F32(alphas[kvh][1]) / F32(n)
                 h = sim[(s, kvh)]
                 old_hi, old_lo = list(h.hi), list(h.lo)
                 demoted = sim_step(h, n, W, th_h, th_l, lo_enabled)
@@ -390,6 +397,8 @@ MUTANTS = {
     "lo_victim_prune_inclusive": ("if (q->lo[xv].imp < th_l)", "if (q->lo[xv].imp <= th_l)"),
     "window_ignored": ("argmin_imp(q->hi, q->nh, n - c->window)", "argmin_imp(q->hi, q->nh, n)"),
     "demoted_pruned_instead": ("if (c->lo_enabled && iv >= th_l) {", "if (c->lo_enabled && iv > th_h) {"),
+    "thresholds_of_head0": ("const float* alpha = p->alpha + 2 * ((size_t)layer * H + h);",
+                            "const float* alpha = p->alpha + 2 * ((size_t)layer * H);"),
 }
 
 

@@ -471,3 +471,44 @@ def test_errors_are_no_ops():
     after = pool2.snapshot()
     for key in before:
         assert (before[key] == after[key]).all()
+
+
+# ------------------------------------------------- per-head thresholds -----
+def _head_records(pool, slot, kvh):
+    """A head's stored tokens, tier by tier in slot order, without page IDs."""
+    toks = pagefmt.head_tokens(pool.snapshot(), 0, slot, kvh, pool.t_hi, pool.t_lo)
+    key = lambda r: (r["pos"], tuple(r["kc"]), tuple(r["vc"]), r["ks"], r["kz"], r["vs"], r["vz"],
+                     np.float32(r["score"]).view(np.uint32).item())
+    return [key(r) for r in toks["hi"]], [key(r) for r in toks["lo"]]
+
+
+def test_per_head_thresholds_equal_uniform_pools_head_by_head():
+    """Compaction policy, extensibility (thresholds for each head on its
+    own): a pool whose two KV heads carry different (alpha_h, alpha_l) stores,
+    head by head, exactly what a pool configured with that head's pair for
+    every head stores, through a prompt and generation steps with score
+    updates (the attention of a KV head sees only its own tokens)."""
+    pairs = [(2.0, 0.25), (0.8, 0.5)]
+    base = small_cfg(recent_window=8, max_seq_len=400, n_pages=512, tokens_per_hi_page=4, tokens_per_lo_page=8)
+    n0, steps, H, G = 150, 25, 2, 4
+    k = workloads.random_fp16((n0, H, 128), 31)
+    v = workloads.random_fp16((n0, H, 128), 32)
+    S = workloads.given_scores(n0, H, seed=33, scale=0.5)
+    pools = [oracle.Pool(base)] + [oracle.Pool(dict(base, alpha_h=a, alpha_l=b)) for a, b in pairs]
+    assert pools[0].set_thresholds(0, [a for a, _ in pairs], [b for _, b in pairs]) == 0
+    assert (pools[0].thresholds[0] == np.array(pairs, np.float32)).all()
+    for p in pools:
+        assert p.prompt(0, [0], [n0], k, v, scores_in=S) == 0
+    for t in range(steps):
+        kn = workloads.random_fp16((1, H, 128), 400 + t)
+        vn = workloads.random_fp16((1, H, 128), 500 + t)
+        q = workloads.random_fp16((1, H * G, 128), 600 + t)
+        for p in pools:
+            assert p.decode(0, [0], kn, vn) == 0
+            assert p.attention(0, [0], q, update_scores=True)[0] == 0
+        for h in range(H):
+            assert _head_records(pools[0], 0, h) == _head_records(pools[1 + h], 0, h), (t, h)
+    # the two pairs really differ in what they keep
+    assert _head_records(pools[1], 0, 0) != _head_records(pools[2], 0, 0)
+    assert pools[0].set_thresholds(0, [np.nan, 1.0], [0.1, 0.1]) == oracle.ERR["ARG"]
+    assert pools[0].set_thresholds(1, [1.0, 1.0], [0.1, 0.1]) == oracle.ERR["ARG"]
