@@ -40,7 +40,8 @@ __device__ void decide_plan(const PoolView& pv, int layer, int slot, int kvh, in
   const int pc = n - pv.window - 1;
   int s_xc = xc_in;
   float s_ic = ic_in;
-  const float th_h = __fdiv_rn(pv.alpha_h, (float)n), th_l = __fdiv_rn(pv.alpha_l, (float)n);
+  const float2 al = pv.thresholds(layer, kvh);   // the head's pair
+  const float th_h = __fdiv_rn(al.x, (float)n), th_l = __fdiv_rn(al.y, (float)n);
   DecodePlan p;
   p.err = 0;
   p.n_moves = 0;

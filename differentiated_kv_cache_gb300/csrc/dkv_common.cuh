@@ -86,9 +86,9 @@ struct PoolView {
   Ctl* ctl;
   CallArgs* call;
   VictimCache* vcache;  // [layer][slot][kvh]
+  float2* alpha;        // [layer][kvh]: the head's (alpha_h, alpha_l)
   int n_pages, page_bytes, n_layers, hkv, G, max_req, max_seq, L;
   int lo_enabled, window, slack, reclaim;
-  float alpha_h, alpha_l;
   TierGeom hi, lo;
 
   __device__ __forceinline__ int* row(int layer, int slot, int kvh) const {
@@ -99,6 +99,9 @@ struct PoolView {
   }
   __device__ __forceinline__ VictimCache* vc(int layer, int slot, int kvh) const {
     return vcache + ((size_t)layer * max_req + slot) * hkv + kvh;
+  }
+  __device__ __forceinline__ float2 thresholds(int layer, int kvh) const {
+    return alpha[(size_t)layer * hkv + kvh];
   }
   __device__ __forceinline__ int* rq(int layer, int slot) const {
     return req + ((size_t)layer * max_req + slot) * 4;

@@ -156,8 +156,6 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   v.window = cfg->recent_window;
   v.slack = cfg->prompt_grant_slack;
   v.reclaim = cfg->reclaim_in_decode ? 1 : 0;
-  v.alpha_h = cfg->alpha_h;
-  v.alpha_l = cfg->alpha_l;
   v.hi = hi;
   v.lo = lo;
   Scratch& s = P.sc;
@@ -183,6 +181,7 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&v.ctl, 1);
   A(&v.call, 1);
   A(&v.vcache, heads);
+  A(&v.alpha, (size_t)cfg->n_layers * cfg->n_kv_heads);
   A(&s.partial, units * s.nkb_cap * kObs * G);
   A(&s.lse2, units * kObs * G);
   A(&s.score, max_tokens * cfg->n_kv_heads);
@@ -215,6 +214,10 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
     c.end = (unsigned long long)cfg->n_pages;
     c.error_info = -1;
     e = cudaMemcpy(v.ctl, &c, sizeof(Ctl), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) {        // every head starts with the configuration's pair
+    std::vector<float2> al((size_t)cfg->n_layers * cfg->n_kv_heads, make_float2(cfg->alpha_h, cfg->alpha_l));
+    e = cudaMemcpy(v.alpha, al.data(), al.size() * sizeof(float2), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) {
     k_init_list<<<256, 256>>>(v.list, cfg->n_pages);
@@ -382,6 +385,25 @@ int dkv_decode_attention_static(dkv_pool* pool, int32_t layer, int32_t n_req, co
   DeviceGuard guard(P.device);
   const cudaError_t e = launch_attention_static(P, layer, sa, max_tokens, static_cast<const __half*>(q), out,
                                                 update, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_err(e);
+}
+
+int dkv_pool_set_thresholds(dkv_pool* pool, int32_t layer, const float* alpha_h, const float* alpha_l,
+                            void* stream) {
+  if (!pool || !alpha_h || !alpha_l) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  if (layer < 0 || layer >= c.n_layers) return DKV_ERR_ARG;
+  std::vector<float2> al(c.n_kv_heads);
+  for (int h = 0; h < c.n_kv_heads; h++) {
+    if (std::isnan(alpha_h[h]) || std::isnan(alpha_l[h])) return DKV_ERR_ARG;
+    al[h] = make_float2(alpha_h[h], alpha_l[h]);
+  }
+  DeviceGuard guard(P.device);
+  // from pageable memory: the call returns once the values are staged
+  const cudaError_t e = cudaMemcpyAsync(P.pv.alpha + (size_t)layer * c.n_kv_heads, al.data(),
+                                        al.size() * sizeof(float2), cudaMemcpyHostToDevice,
+                                        reinterpret_cast<cudaStream_t>(stream));
   return cuda_err(e);
 }
 

@@ -15,7 +15,7 @@ namespace dkv {
 
 // Tier of one prompt token and its rank among same-tier tokens of the block
 // (block of kKeyBlock consecutive positions handled by 128 threads).
-__device__ __forceinline__ void classify_block(const PoolView& pv, int n0, int j, float s, int& tier,
+__device__ __forceinline__ void classify_block(const PoolView& pv, float2 al, int n0, int j, float s, int& tier,
                                                int& rank, int* s_cnt /*[2*4]*/, int2* bcnt_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   tier = kTierPrune;
@@ -24,7 +24,7 @@ __device__ __forceinline__ void classify_block(const PoolView& pv, int n0, int j
       tier = kTierHi;
     } else {
       const float imp = __fdiv_rn(s, (float)score_count(j, n0, 0));
-      tier = classify(imp, __fdiv_rn(pv.alpha_h, (float)n0), __fdiv_rn(pv.alpha_l, (float)n0), pv.lo_enabled);
+      tier = classify(imp, __fdiv_rn(al.x, (float)n0), __fdiv_rn(al.y, (float)n0), pv.lo_enabled);
     }
   }
   const unsigned bh = __ballot_sync(0xffffffffu, tier == kTierHi);
@@ -39,8 +39,9 @@ __device__ __forceinline__ void classify_block(const PoolView& pv, int n0, int j
     *bcnt_out = make_int2(s_cnt[0] + s_cnt[1] + s_cnt[2] + s_cnt[3], s_cnt[4] + s_cnt[5] + s_cnt[6] + s_cnt[7]);
 }
 
-// Tier from caller-given scores (score_in), same rule and ranks.
-__global__ void __launch_bounds__(128) k_prompt_given(PoolView pv, const float* __restrict__ score_in,
+// Tier from caller-given scores (score_in), same rule and ranks, against the
+// thresholds of the token's head.
+__global__ void __launch_bounds__(128) k_prompt_given(PoolView pv, int layer, const float* __restrict__ score_in,
                                                        float* score_out, uint16_t* tokinfo, int2* bcnt,
                                                        int nkb_cap) {
   if (pv.noop()) return;
@@ -54,7 +55,8 @@ __global__ void __launch_bounds__(128) k_prompt_given(PoolView pv, const float* 
   const size_t tok = (size_t)(ca->tok0[i] + j) * pv.hkv + kvh;
   const float s = j < n0 ? score_in[tok] : 0.0f;
   int tier, rank;
-  classify_block(pv, n0, j, s, tier, rank, s_cnt, bcnt + ((size_t)i * pv.hkv + kvh) * nkb_cap + kb);
+  classify_block(pv, pv.thresholds(layer, kvh), n0, j, s, tier, rank, s_cnt,
+                 bcnt + ((size_t)i * pv.hkv + kvh) * nkb_cap + kb);
   if (j < n0) {
     if (score_out) score_out[tok] = s;
     tokinfo[tok] = (uint16_t)((rank << 2) | tier);
@@ -302,14 +304,14 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long 
   cudaError_t e = cudaSuccess;
   const float* score_src;
   if (scores_in) {
-    k_prompt_given<<<grid, 128, 0, st>>>(P.pv, scores_in, scores_out, s.tokinfo, s.bcnt, s.nkb_cap);
+    k_prompt_given<<<grid, 128, 0, st>>>(P.pv, layer, scores_in, scores_out, s.tokinfo, s.bcnt, s.nkb_cap);
     e = cudaGetLastError();
     score_src = scores_in;
   } else {
     float* so = scores_out ? scores_out : s.score;
     e = launch_scoring_tc(P, k, q_obs, n_tok, n_req, so, st);
     if (e == cudaSuccess) {      // tiers and in-block ranks from the scores
-      k_prompt_given<<<grid, 128, 0, st>>>(P.pv, so, nullptr, s.tokinfo, s.bcnt, s.nkb_cap);
+      k_prompt_given<<<grid, 128, 0, st>>>(P.pv, layer, so, nullptr, s.tokinfo, s.bcnt, s.nkb_cap);
       e = cudaGetLastError();
     }
     score_src = so;

@@ -23,7 +23,7 @@ DKV_PROMPT, DKV_DECODE = 0, 1
 
 EXPORTED = ("dkv_pool_create", "dkv_pool_destroy", "dkv_pool_geometry", "dkv_compact_step",
             "dkv_decode_attention", "dkv_decode_attention_static", "dkv_free_request", "dkv_pool_status", "dkv_pool_clear_error",
-            "dkv_pool_export", "dkv_strerror")
+            "dkv_pool_export", "dkv_pool_set_thresholds", "dkv_strerror")
 
 
 class dkv_config(C.Structure):
@@ -78,6 +78,7 @@ def load() -> C.CDLL:
         L.dkv_compact_step.argtypes = [P, I, I, I, P, P, P, P, P, P, P, P]
         L.dkv_decode_attention.argtypes = [P, I, I, P, P, P, I, P]
         L.dkv_free_request.argtypes = [P, I, P]
+        L.dkv_pool_set_thresholds.argtypes = [P, I, P, P, P]
         L.dkv_pool_status.argtypes = [P, C.POINTER(dkv_status)]
         L.dkv_pool_clear_error.argtypes = [P]
         L.dkv_pool_export.argtypes = [P, C.POINTER(dkv_snapshot)]
@@ -189,6 +190,15 @@ def dkv_decode_attention_static(pool, layer: int, req_slots, q, out, update_scor
                                             _dptr(q, torch.float16, "q"), _dptr(out, torch.float32, "out"),
                                             int(bool(update_scores)), _stream(stream))
     return _check(rc, "dkv_decode_attention_static") if check else rc
+
+
+def dkv_pool_set_thresholds(pool, layer: int, alpha_h, alpha_l, stream=None, check: bool = True) -> int:
+    """Per-KV-head thresholds of one layer (host arrays of n_kv_heads floats)."""
+    ah = np.ascontiguousarray(alpha_h, dtype=np.float32)
+    al = np.ascontiguousarray(alpha_l, dtype=np.float32)
+    rc = load().dkv_pool_set_thresholds(pool, int(layer), ah.ctypes.data_as(C.c_void_p),
+                                        al.ctypes.data_as(C.c_void_p), _stream(stream))
+    return _check(rc, "dkv_pool_set_thresholds") if check else rc
 
 
 def dkv_free_request(pool, req_slot: int, stream=None, check: bool = True) -> int:

@@ -24,6 +24,8 @@
  *   [Mem-Gen]  Memory management — generation-phase workflow.
  *   [Impl-Kern] System implementation — custom attention kernel (hi pages
  *              first, then lo pages; key / value layouts; sequence split).
+ *   [Pol-Ext]  Compaction policy — extensibility (more precision levels;
+ *              thresholds adjusted for each head individually).
  *
  * Conventions for every entry point
  * ---------------------------------
@@ -284,6 +286,18 @@ int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
 int dkv_decode_attention_static(dkv_pool* pool, int32_t layer, int32_t n_req,
                                 const int32_t* req_slots, const void* q, float* out,
                                 int32_t update_scores, void* stream);
+
+/* Thresholds for each KV head of one layer [Pol-Ext]: from the next
+ * compaction step of `layer` on (stream order), head h's tokens are compared
+ * with alpha_h[h]/N and alpha_l[h]/N instead of the configuration's pair
+ * (prompt classification and the generation step's t_c and victims).
+ * alpha_h, alpha_l: host arrays of n_kv_heads floats, copied before the call
+ * returns (the copy from pageable memory may wait for work already queued on
+ * `stream`). Until set, every head of every layer uses config.alpha_h and
+ * config.alpha_l. Decode attention does not use thresholds.
+ * Errors: DKV_ERR_ARG (NULL, layer out of range, NaN); DKV_ERR_CUDA. */
+int dkv_pool_set_thresholds(dkv_pool* pool, int32_t layer, const float* alpha_h, const float* alpha_l,
+                            void* stream);
 
 /* Return every page of request `req_slot` in every layer to the list end
  * (one prefix sum over (layer, KV head); within a head hi pages left to

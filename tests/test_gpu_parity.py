@@ -400,3 +400,49 @@ def test_attention_on_workload_with_outliers():
             worst_ratio = max(worst_ratio, ratio)
         print(f"tiny workload: attention max err/tolerance {worst_ratio:.3f}")
         assert worst_ratio <= 1.0
+
+
+# ------------------------------------------------- per-head thresholds
+def test_per_head_thresholds_bit_exact():
+    """Thresholds for each KV head (DiffKV compaction policy, extensibility),
+    two layers with different pairs, changed between generation steps: the
+    prompt with caller scores, then steps of (compaction, attention with
+    score update) with the oracle taken over from the GPU state before each
+    step; every state bit-exact."""
+    import differentiated_kv_cache_gb300 as dkv
+    from tests.gpu_pool import load_into
+    H, G = 4, 4
+    cfg = cfg_of(n_layers=2, n_kv_heads=H, group_size=G, n_pages=4096, max_seq_len=1400, page_bytes=3584,
+                 recent_window=16)
+    lens, slots = [900, 400], [1, 0]
+    n = sum(lens)
+    k = workloads.random_fp16((n, H, 128), 51, scale=1.5)
+    v = workloads.random_fp16((n, H, 128), 52)
+    S = workloads.given_scores(n, H, seed=53, scale=0.2)
+    pairs = {0: ([2.0, 0.5, 4.0, 1.0], [0.25, 0.05, 1.0, 0.9]), 1: ([1.0, 1.0, 8.0, 0.3], [0.6, 0.0, 0.5, 0.3])}
+    gp, op = both(cfg)
+    with gp:
+        for layer, (ah, al) in pairs.items():
+            dkv.dkv_pool_set_thresholds(gp.h, layer, ah, al)
+            assert op.set_thresholds(layer, ah, al) == 0
+        for layer in (0, 1):
+            gp.prompt(layer, slots, lens, k, v, scores_in=S)
+            assert op.prompt(layer, slots, lens, k, v, scores_in=S) == 0
+        assert_same(gp, op)
+        for step in range(30):
+            if step == 15:                       # new pairs for layer 0 mid-run
+                ah, al = [0.5, 3.0, 1.0, 2.0], [0.1, 0.5, 0.5, 0.0]
+                dkv.dkv_pool_set_thresholds(gp.h, 0, ah, al)
+                assert op.set_thresholds(0, ah, al) == 0
+            layer = step % 2
+            kn = workloads.random_fp16((2, H, 128), 5000 + step)
+            vn = workloads.random_fp16((2, H, 128), 6000 + step)
+            load_into(op, gp.snapshot())
+            gp.decode(layer, slots, kn, vn)
+            assert op.decode(layer, slots, kn, vn) == 0
+            assert_same(gp, op)
+            q = workloads.random_fp16((2, H * G, 128), 7000 + step, scale=2.0)
+            gp.attention(layer, slots, q, update=True)
+        assert gp.status()["error"] == 0
+        assert dkv.dkv_pool_set_thresholds(gp.h, 0, [float("nan")] * H, [0.1] * H, check=False) == dkv.DKV_ERR_ARG
+        assert dkv.dkv_pool_set_thresholds(gp.h, 2, [1.0] * H, [0.1] * H, check=False) == dkv.DKV_ERR_ARG
