@@ -50,34 +50,47 @@ HI_BYTES, LO_BYTES, SCORE_RMW = 200, 104, 8
 # attention (attention, epilogue), free_request (one)
 LAUNCHES = {"prompt": 11, "decode": 3, "attention": 2, "free": 1}
 
-# DRAM bytes of one decode-attention call (k_attn_paged + k_attn_epi:
-# dram__bytes_read.sum + dram__bytes_write.sum, caches flushed by ncu before
-# each kernel), third decode step of the llama8b bench step.
-# Valid only for the kernel sources it was taken on: any change to them
+# DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum, caches
+# flushed by ncu before each kernel) of the llama8b bench step:
+#   one decode-attention call (k_attn_paged + k_attn_epi, third decode step);
+#   one prompt compact_step (its 11 kernels, timed step).
+# Valid only for the kernel sources they were taken on: any change to them
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 119_673_600 + 8_354_304 + 25_937_664,
+    "bytes_per_call": 119_721_472 + 4_718_592 + 30_604_800,
     "sources": {
-        "attention.cu": "698d960b729c03922d29c7d9cfad8c6cd063d4b7bc8d69b31a1222a246023e03",
-        "dkv_common.cuh": "90d758348e6dbf3a1ae34973ef9bef33cbbd31e8c1a636103b676ac54b52f649",
-        "dkv_kernels.cuh": "a11e8c64feb0a4bcfea04df84fe718b26a0fa6dc53df45de115fabf6c95d12fe",
+        "attention.cu": "b0273bced4432a3eca8deb4e5a1f832c3de2fa4a1113c47c78b43f15ecfbc1cd",
+        "dkv_common.cuh": "bcd6734e6c5b4bd5fc941201972200f49e4eed4b73ae8e36152d81d14831054a",
+        "dkv_kernels.cuh": "1af05a5c3c6beb7a744278fb7fe797da5149d278f8177afc2dcb8418855110f2",
+    },
+}
+PROMPT_TRAFFIC = {
+    "workload": "llama8b",
+    "bytes_per_call": 1_022_412_800 + 80_523_008,
+    "sources": {
+        "prompt.cu": "96c5fde7c38c3a74cef6db6489935e4c7609d3fddd4be3347bdedaf7df55c45c",
+        "prompt_tc.cu": "e3397f1f6e2da567f1ffcd33c9571d0dc34a882aaf3878b22c8bb86779f9287a",
+        "alloc.cu": "4b1b90d8af16eca24a790b2bfff5e6c9ac5de18f04712cde3b02fdaedde08e40",
+        "dkv_tc.cuh": "6988ad672fc0d64fda8ef7e915b2b0097fc3a5e8361ee2245de3fa50606bcb39",
+        "dkv_common.cuh": "bcd6734e6c5b4bd5fc941201972200f49e4eed4b73ae8e36152d81d14831054a",
+        "dkv_kernels.cuh": "1af05a5c3c6beb7a744278fb7fe797da5149d278f8177afc2dcb8418855110f2",
     },
 }
 L2_FLUSH_BYTES = 256 << 20
 
 
-def recorded_traffic(workload: str, page_bytes: int | None = None):
-    """The recorded per-call DRAM traffic when the attention sources still
-    hash to those it was captured on, else None."""
-    if workload != ATTN_TRAFFIC["workload"] or page_bytes not in (None, workloads.WORKLOADS[workload].page_bytes):
+def recorded_traffic(record: dict, workload: str, page_bytes: int | None = None):
+    """A recorded DRAM-traffic figure when the kernel sources still hash to
+    those it was captured on (and the workload is the one captured), else None."""
+    if workload != record["workload"] or page_bytes not in (None, workloads.WORKLOADS[workload].page_bytes):
         return None
     csrc = os.path.join(ROOT, "differentiated_kv_cache_gb300", "csrc")
-    for name, digest in ATTN_TRAFFIC["sources"].items():
+    for name, digest in record["sources"].items():
         with open(os.path.join(csrc, name), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() != digest:
                 return None
-    return ATTN_TRAFFIC["bytes_per_call"]
+    return record["bytes_per_call"]
 
 
 def peaks():
@@ -479,6 +492,7 @@ def run_dkv(args, world, rank, local):
     value = all_bytes / (call_ms_max * 1e-3) / 1e9
     achieved = r["attn_bytes"] / (r["alone_ms"] * 1e-3) / 1e9
     parts = loop.summary(r, peak)
+    parts["compact_step_prompt_traffic"] = recorded_traffic(PROMPT_TRAFFIC, args.workload)
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms_max, 3), "higher_is_better": True,
@@ -503,7 +517,8 @@ def run_dkv(args, world, rank, local):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": int(r["attn_bytes"]),
-                     "traffic": args.traffic if args.traffic is not None else recorded_traffic(args.workload)},
+                     "traffic": args.traffic if args.traffic is not None else
+                     recorded_traffic(ATTN_TRAFFIC, args.workload)},
         "gpu_launches": args.steps * loop.launches_per_step(),
     }
     result["clocks"] = clk.summary()
