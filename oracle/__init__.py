@@ -72,6 +72,8 @@ def lib():
             L.orc_decode_attention.argtypes = [P, I, I, P, P, P, I]; L.orc_decode_attention.restype = I
             L.orc_free_request.argtypes = [P, I]; L.orc_free_request.restype = I
             L.orc_set_thresholds.argtypes = [P, I, P, P]; L.orc_set_thresholds.restype = I
+            L.orc_prefill_attention.argtypes = [I, I, P, I64, P, P, I64, P, P]
+            L.orc_prefill_attention.restype = None
             L.orc_thresholds.argtypes = [P]; L.orc_thresholds.restype = P
             _lib = L
     return _lib
@@ -119,6 +121,19 @@ def unit_scores(k_head: np.ndarray, q_group: np.ndarray) -> np.ndarray:
     S = np.zeros(n0, dtype=np.float64)
     lib().orc_unit_scores(n0, G, _ptr(k), 128, _ptr(q), G * 128, 128, _ptr(S))
     return S
+
+
+def prefill_attention(q_group: np.ndarray, k_head: np.ndarray, v_head: np.ndarray):
+    """fp64 causal attention of one KV head's G query heads over a prompt.
+    q_group fp16 [N0, G, 128]; k_head, v_head fp16 [N0, 128]. Returns
+    (out fp64 [N0, G, 128], lse2 fp64 [N0, G]: base-2 log-sum-exp of the
+    scaled logits)."""
+    q = _u16(q_group); k = _u16(k_head); v = _u16(v_head)
+    n0, G = q.shape[0], q.shape[1]
+    out = np.zeros((n0, G, 128), np.float64)
+    lse2 = np.zeros((n0, G), np.float64)
+    lib().orc_prefill_attention(n0, G, _ptr(q), G * 128, _ptr(k), _ptr(v), 128, _ptr(out), _ptr(lse2))
+    return out, lse2
 
 
 # ---- pool -------------------------------------------------------------------

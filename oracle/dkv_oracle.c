@@ -416,6 +416,50 @@ void orc_unit_scores(int n0, int G, const uint16_t* k, int64_t k_stride, const u
   free(kd); free(logit); free(pmax);
 }
 
+/* Causal prefill attention of one KV head's G query heads, fp64 — the
+ * model's own attention over the prompt, after which DiffKV's compactor runs
+ * (System implementation, architecture overview; Background, attention
+ * equation): out[p][h] = sum_{j <= p} softmax_j(q_{p,h} . k_j / sqrt(d)) v_j,
+ * and lse2[p][h] = log2 sum_{j <= p} exp(q_{p,h} . k_j / sqrt(d)), the
+ * log-sum-exp in base 2 that the score pass of the prompt compaction uses.
+ * q rows are q + p * q_stride + h * D; k / v rows k + j * kv_stride. */
+void orc_prefill_attention(int n0, int G, const uint16_t* q, int64_t q_stride, const uint16_t* k,
+                           const uint16_t* v, int64_t kv_stride, double* out, double* lse2) {
+  double* kd = (double*)malloc(sizeof(double) * (size_t)n0 * D);
+  double* vd = (double*)malloc(sizeof(double) * (size_t)n0 * D);
+  double* w = (double*)malloc(sizeof(double) * (size_t)n0);
+  for (int64_t j = 0; j < n0; j++)
+    for (int f = 0; f < D; f++) {
+      kd[j * D + f] = orc_half_to_float(k[j * kv_stride + f]);
+      vd[j * D + f] = orc_half_to_float(v[j * kv_stride + f]);
+    }
+  const double scale = 1.0 / sqrt((double)D);
+  for (int p = 0; p < n0; p++)
+    for (int h = 0; h < G; h++) {
+      double qd[D];
+      for (int f = 0; f < D; f++) qd[f] = orc_half_to_float(q[(int64_t)p * q_stride + (int64_t)h * D + f]);
+      double m = -INFINITY;
+      for (int j = 0; j <= p; j++) {
+        double acc = 0.0;
+        for (int f = 0; f < D; f++) acc += qd[f] * kd[(int64_t)j * D + f];
+        w[j] = acc * scale;
+        if (w[j] > m) m = w[j];
+      }
+      double sum = 0.0;
+      for (int j = 0; j <= p; j++) {
+        w[j] = exp(w[j] - m);
+        sum += w[j];
+      }
+      double* o = out + ((int64_t)p * G + h) * D;
+      for (int f = 0; f < D; f++) o[f] = 0.0;
+      for (int j = 0; j <= p; j++)
+        for (int f = 0; f < D; f++) o[f] += w[j] * vd[(int64_t)j * D + f];
+      for (int f = 0; f < D; f++) o[f] /= sum;
+      lse2[(int64_t)p * G + h] = (m + log(sum)) / log(2.0);
+    }
+  free(kd); free(vd); free(w);
+}
+
 /* ------------------------------------------------------------------ */
 /* Prompt phase — Memory management, prompt workflow (Figure 6).       */
 /* ------------------------------------------------------------------ */

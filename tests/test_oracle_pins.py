@@ -512,3 +512,49 @@ def test_per_head_thresholds_equal_uniform_pools_head_by_head():
     assert _head_records(pools[1], 0, 0) != _head_records(pools[2], 0, 0)
     assert pools[0].set_thresholds(0, [np.nan, 1.0], [0.1, 0.1]) == oracle.ERR["ARG"]
     assert pools[0].set_thresholds(1, [1.0, 1.0], [0.1, 0.1]) == oracle.ERR["ARG"]
+
+
+# ------------------------------------------------------ prefill attention ---
+def _dense_causal(q, k, v):
+    """numpy / scipy causal attention: q [N, G, 128], k, v [N, 128] (float64)."""
+    n, G = q.shape[0], q.shape[1]
+    logits = np.einsum("pgf,jf->pgj", q, k) / np.sqrt(128.0)
+    mask = np.tril(np.ones((n, n), bool))[:, None, :]
+    logits = np.where(mask, logits, -np.inf)
+    p = scipy.special.softmax(logits, axis=-1)
+    lse = scipy.special.logsumexp(logits, axis=-1)
+    return np.einsum("pgj,jf->pgf", p, v), lse / np.log(2.0)
+
+
+@pytest.mark.parametrize("n0,G", [(1, 1), (37, 3), (130, 4)])
+def test_prefill_attention_matches_scipy(n0, G):
+    q = workloads.random_fp16((n0, G, 128), 700 + n0, scale=1.5)
+    k = workloads.random_fp16((n0, 128), 701 + n0)
+    v = workloads.random_fp16((n0, 128), 702 + n0)
+    out, lse2 = oracle.prefill_attention(q, k, v)
+    ref, rlse = _dense_causal(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64))
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse2, rlse, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_attention_equal_keys_and_causality():
+    """Equal keys: every visible key has the same weight, so row p's output is
+    the mean of v[0..p] and its base-2 log-sum-exp is log2(p + 1) + q.k /
+    (sqrt(128) ln 2); changing later values changes no earlier row."""
+    n0, G = 50, 2
+    q = workloads.random_fp16((n0, G, 128), 710)
+    krow = workloads.random_fp16((1, 128), 711)
+    k = np.repeat(krow, n0, axis=0)
+    v = workloads.random_fp16((n0, 128), 712)
+    out, lse2 = oracle.prefill_attention(q, k, v)
+    vd = v.astype(np.float64)
+    means = np.cumsum(vd, axis=0) / np.arange(1, n0 + 1)[:, None]
+    for g in range(G):
+        np.testing.assert_allclose(out[:, g], means, rtol=1e-12, atol=1e-12)
+        qk = q[:, g].astype(np.float64) @ krow[0].astype(np.float64) / np.sqrt(128.0)
+        np.testing.assert_allclose(lse2[:, g], np.log2(np.arange(1, n0 + 1)) + qk / np.log(2.0), rtol=1e-12,
+                                   atol=1e-12)
+    v2 = v.copy()
+    v2[30:] = workloads.random_fp16((n0 - 30, 128), 713)
+    out2, _ = oracle.prefill_attention(q, k, v2)
+    assert (out2[:30] == out[:30]).all() and not (out2[30:] == out[30:]).all()
