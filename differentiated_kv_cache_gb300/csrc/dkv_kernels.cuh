@@ -135,9 +135,14 @@ struct Pool {
 
 // Launchers (return the first CUDA error, cudaSuccess otherwise).
 cudaError_t launch_setup(const Pool& P, const CallArgs& args, cudaStream_t st);
+// lse_obs: the observation rows' base-2 log-sum-exps from the prompt's own
+// attention ([n_req][Hq][32]); null: the score pass computes them itself.
 cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long n_tok, const __half* k,
-                          const __half* v, const __half* q_obs, const float* scores_in, float* scores_out,
-                          cudaStream_t st);
+                          const __half* v, const __half* q_obs, const float* lse_obs, const float* scores_in,
+                          float* scores_out, cudaStream_t st);
+// Causal prompt attention of a call (prefill.cu).
+cudaError_t launch_prefill(Pool& P, const CallArgs& args, int max_len, const __half* q, const __half* k,
+                           const __half* v, float* out, float* lse_obs, cudaStream_t st);
 cudaError_t launch_decode(Pool& P, int layer, const SlotArgs& sa, const __half* k, const __half* v,
                           cudaStream_t st);
 cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tokens, const __half* q,

@@ -321,7 +321,81 @@ int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req,
   for (int i = 0; i < n_req; i++) max_len = std::max(max_len, seq_lens[i]);
   e = launch_prompt(P, layer, n_req, max_len, args.tok0[n_req], static_cast<const __half*>(k),
                     static_cast<const __half*>(v),
-                    static_cast<const __half*>(q_obs), scores_in, scores_out, st);
+                    static_cast<const __half*>(q_obs), nullptr, scores_in, scores_out, st);
+  if (e != cudaSuccess) return DKV_ERR_CUDA;
+  for (int i = 0; i < n_req; i++) {
+    P.h_active[base + req_slots[i]] = 1;
+    P.h_n0[base + req_slots[i]] = seq_lens[i];
+    P.h_n[base + req_slots[i]] = seq_lens[i];
+  }
+  return DKV_OK;
+}
+
+int dkv_prefill_attention(dkv_pool* pool, int32_t n_req, const int32_t* seq_lens, const void* q, const void* k,
+                          const void* v, float* out, float* lse_obs, void* stream) {
+  if (!pool || !seq_lens || !q || !k || !v || !out) return DKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(lse_obs)) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  if (n_req < 1 || n_req > kMaxCallReq) return DKV_ERR_ARG;
+  CallArgs args;
+  args.n_req = n_req;
+  args.pad = 0;
+  long long tok = 0;
+  int max_len = 0;
+  for (int i = 0; i < n_req; i++) {
+    if (seq_lens[i] < 1 || seq_lens[i] > c.max_seq_len) return DKV_ERR_ARG;
+    args.slots[i] = -1;
+    args.lens[i] = seq_lens[i];
+    args.tok0[i] = tok;
+    tok += seq_lens[i];
+    max_len = std::max(max_len, seq_lens[i]);
+  }
+  args.tok0[n_req] = tok;
+  DeviceGuard guard(P.device);
+  const cudaError_t e = launch_prefill(P, args, max_len, static_cast<const __half*>(q), static_cast<const __half*>(k),
+                                       static_cast<const __half*>(v), out, lse_obs,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
+}
+
+int dkv_compact_step_prefilled(dkv_pool* pool, int32_t layer, int32_t n_req, const int32_t* req_slots,
+                               const int32_t* seq_lens, const void* k, const void* v, const void* q_obs,
+                               const float* lse_obs, float* scores_out, void* stream) {
+  if (!pool || !req_slots || !seq_lens || !k || !v || !q_obs || !lse_obs) return DKV_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q_obs) || !aligned4(lse_obs) || !aligned4(scores_out))
+    return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  if (layer < 0 || layer >= c.n_layers || n_req < 1 || n_req > c.max_requests || n_req > kMaxCallReq)
+    return DKV_ERR_ARG;
+  const size_t base = (size_t)layer * c.max_requests;
+  CallArgs args;
+  args.n_req = n_req;
+  args.pad = 0;
+  long long tok = 0;
+  int max_len = 0;
+  for (int i = 0; i < n_req; i++) {
+    if (req_slots[i] < 0 || req_slots[i] >= c.max_requests) return DKV_ERR_ARG;
+    for (int j = 0; j < i; j++)
+      if (req_slots[j] == req_slots[i]) return DKV_ERR_ARG;
+    if (seq_lens[i] < 1 || seq_lens[i] > c.max_seq_len) return DKV_ERR_ARG;
+  }
+  for (int i = 0; i < n_req; i++) {
+    if (P.h_active[base + req_slots[i]]) return DKV_ERR_STATE;
+    args.slots[i] = req_slots[i];
+    args.lens[i] = seq_lens[i];
+    args.tok0[i] = tok;
+    tok += seq_lens[i];
+    max_len = std::max(max_len, seq_lens[i]);
+  }
+  args.tok0[n_req] = tok;
+  DeviceGuard guard(P.device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_setup(P, args, st);
+  if (e != cudaSuccess) return DKV_ERR_CUDA;
+  e = launch_prompt(P, layer, n_req, max_len, tok, static_cast<const __half*>(k), static_cast<const __half*>(v),
+                    static_cast<const __half*>(q_obs), lse_obs, nullptr, scores_out, st);
   if (e != cudaSuccess) return DKV_ERR_CUDA;
   for (int i = 0; i < n_req; i++) {
     P.h_active[base + req_slots[i]] = 1;

@@ -285,19 +285,21 @@ cudaError_t launch_prompt_plan(Pool& P, int layer, int n_req, cudaStream_t st);
 cudaError_t configure_attention();
 cudaError_t configure_alloc();
 cudaError_t configure_prompt_tc();
-cudaError_t launch_scoring_tc(Pool& P, const __half* k, const __half* q_obs, long long n_tok, int n_req,
-                              float* score_out, cudaStream_t st);
+cudaError_t configure_prefill();
+cudaError_t launch_scoring_tc(Pool& P, const __half* k, const __half* q_obs, const float* lse_obs, long long n_tok,
+                              int n_req, float* score_out, cudaStream_t st);
 
 cudaError_t configure_kernels() {
   cudaError_t e;
   if ((e = configure_prompt_tc()) != cudaSuccess) return e;
   if ((e = configure_alloc()) != cudaSuccess) return e;
+  if ((e = configure_prefill()) != cudaSuccess) return e;
   return configure_attention();
 }
 
 cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long n_tok, const __half* k,
-                          const __half* v, const __half* q_obs, const float* scores_in, float* scores_out,
-                          cudaStream_t st) {
+                          const __half* v, const __half* q_obs, const float* lse_obs, const float* scores_in,
+                          float* scores_out, cudaStream_t st) {
   const Scratch& s = P.sc;
   const int nkb = (max_len + kKeyBlock - 1) / kKeyBlock;
   const dim3 grid(nkb, P.pv.hkv, n_req);
@@ -309,7 +311,7 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long 
     score_src = scores_in;
   } else {
     float* so = scores_out ? scores_out : s.score;
-    e = launch_scoring_tc(P, k, q_obs, n_tok, n_req, so, st);
+    e = launch_scoring_tc(P, k, q_obs, lse_obs, n_tok, n_req, so, st);
     if (e == cudaSuccess) {      // tiers and in-block ranks from the scores
       k_prompt_given<<<grid, 128, 0, st>>>(P.pv, layer, so, nullptr, s.tokinfo, s.bcnt, s.nkb_cap);
       e = cudaGetLastError();

@@ -487,10 +487,13 @@ cudaError_t make_maps(const Pool& P, const __half* k, const __half* q_obs, long 
 }
 
 template <int G>
-cudaError_t launch_tc_g(Pool& P, const CUtensorMap& mk, const CUtensorMap& mq, int n_req, float* score_out,
-                        cudaStream_t st) {
+cudaError_t launch_tc_g(Pool& P, const CUtensorMap& mk, const CUtensorMap& mq, const float* lse_obs, int n_req,
+                        float* score_out, cudaStream_t st) {
   const Scratch& s = P.sc;
   const int smem = tc_smem_bytes<G>(n_req);
+  if (lse_obs)                    // the prompt's attention left the log-sum-exps: a2 alone
+    return launch_dependent(k_prompt_tc<G, true>, dim3(P.sm_count), dim3(kTcThreads), (size_t)smem, st, P.pv, mk,
+                            mq, lse_obs, (float2*)nullptr, score_out, s.nkb_cap);
   cudaError_t e = launch_dependent(k_prompt_tc<G, false>, dim3(P.sm_count), dim3(kTcThreads), (size_t)smem, st, P.pv,
                                    mk, mq, (const float*)nullptr, s.partial, (float*)nullptr, s.nkb_cap);
   if (e != cudaSuccess) return e;
@@ -522,21 +525,22 @@ cudaError_t configure_prompt_tc() {
   return configure_tc_g<8>();
 }
 
-// a1, the partial merge and a2 of one prompt call on the tensor cores.
-cudaError_t launch_scoring_tc(Pool& P, const __half* k, const __half* q_obs, long long n_tok, int n_req,
-                              float* score_out, cudaStream_t st) {
+// a1, the partial merge and a2 of one prompt call on the tensor cores (a2
+// alone when the log-sum-exps are given).
+cudaError_t launch_scoring_tc(Pool& P, const __half* k, const __half* q_obs, const float* lse_obs, long long n_tok,
+                              int n_req, float* score_out, cudaStream_t st) {
   CUtensorMap mk, mq;
   cudaError_t e = make_maps(P, k, q_obs, n_tok, n_req, &mk, &mq);
   if (e != cudaSuccess) return e;
   switch (P.pv.G) {
-    case 1: return launch_tc_g<1>(P, mk, mq, n_req, score_out, st);
-    case 2: return launch_tc_g<2>(P, mk, mq, n_req, score_out, st);
-    case 3: return launch_tc_g<3>(P, mk, mq, n_req, score_out, st);
-    case 4: return launch_tc_g<4>(P, mk, mq, n_req, score_out, st);
-    case 5: return launch_tc_g<5>(P, mk, mq, n_req, score_out, st);
-    case 6: return launch_tc_g<6>(P, mk, mq, n_req, score_out, st);
-    case 7: return launch_tc_g<7>(P, mk, mq, n_req, score_out, st);
-    default: return launch_tc_g<8>(P, mk, mq, n_req, score_out, st);
+    case 1: return launch_tc_g<1>(P, mk, mq, lse_obs, n_req, score_out, st);
+    case 2: return launch_tc_g<2>(P, mk, mq, lse_obs, n_req, score_out, st);
+    case 3: return launch_tc_g<3>(P, mk, mq, lse_obs, n_req, score_out, st);
+    case 4: return launch_tc_g<4>(P, mk, mq, lse_obs, n_req, score_out, st);
+    case 5: return launch_tc_g<5>(P, mk, mq, lse_obs, n_req, score_out, st);
+    case 6: return launch_tc_g<6>(P, mk, mq, lse_obs, n_req, score_out, st);
+    case 7: return launch_tc_g<7>(P, mk, mq, lse_obs, n_req, score_out, st);
+    default: return launch_tc_g<8>(P, mk, mq, lse_obs, n_req, score_out, st);
   }
 }
 

@@ -23,7 +23,8 @@ DKV_PROMPT, DKV_DECODE = 0, 1
 
 EXPORTED = ("dkv_pool_create", "dkv_pool_destroy", "dkv_pool_geometry", "dkv_compact_step",
             "dkv_decode_attention", "dkv_decode_attention_static", "dkv_free_request", "dkv_pool_status", "dkv_pool_clear_error",
-            "dkv_pool_export", "dkv_pool_set_thresholds", "dkv_strerror")
+            "dkv_pool_export", "dkv_pool_set_thresholds", "dkv_prefill_attention", "dkv_compact_step_prefilled",
+            "dkv_strerror")
 
 
 class dkv_config(C.Structure):
@@ -77,6 +78,8 @@ def load() -> C.CDLL:
         L.dkv_pool_geometry.argtypes = [P, C.POINTER(dkv_geometry)]
         L.dkv_compact_step.argtypes = [P, I, I, I, P, P, P, P, P, P, P, P]
         L.dkv_decode_attention.argtypes = [P, I, I, P, P, P, I, P]
+        L.dkv_prefill_attention.argtypes = [P, I, P, P, P, P, P, P, P]
+        L.dkv_compact_step_prefilled.argtypes = [P, I, I, P, P, P, P, P, P, P, P]
         L.dkv_free_request.argtypes = [P, I, P]
         L.dkv_pool_set_thresholds.argtypes = [P, I, P, P, P]
         L.dkv_pool_status.argtypes = [P, C.POINTER(dkv_status)]
@@ -167,6 +170,34 @@ def dkv_compact_step(pool, layer: int, mode: int, req_slots, seq_lens, k, v, q_o
         _dptr(scores_in, torch.float32, "scores_in"), _dptr(scores_out, torch.float32, "scores_out"),
         _stream(stream))
     return _check(rc, "dkv_compact_step") if check else rc
+
+
+def dkv_prefill_attention(pool, seq_lens, q, k, v, out, lse_obs=None, stream=None, check: bool = True) -> int:
+    """Causal attention over whole prompts (requests back to back): q fp16
+    [sum(seq_lens)][Hq][128], k and v fp16 [sum(seq_lens)][Hkv][128], out fp32
+    like q; lse_obs None or fp32 [n_req][Hq][32] for the last 32 rows'
+    base-2 log-sum-exps."""
+    import torch
+    lens = _i32(seq_lens)
+    rc = load().dkv_prefill_attention(pool, int(lens.size), lens.ctypes.data_as(C.c_void_p),
+                                      _dptr(q, torch.float16, "q"), _dptr(k, torch.float16, "k"),
+                                      _dptr(v, torch.float16, "v"), _dptr(out, torch.float32, "out"),
+                                      _dptr(lse_obs, torch.float32, "lse_obs"), _stream(stream))
+    return _check(rc, "dkv_prefill_attention") if check else rc
+
+
+def dkv_compact_step_prefilled(pool, layer: int, req_slots, seq_lens, k, v, q_obs, lse_obs, scores_out=None,
+                               stream=None, check: bool = True) -> int:
+    """PROMPT compaction with the observation rows' log-sum-exps given by
+    dkv_prefill_attention."""
+    import torch
+    slots = _i32(req_slots)
+    lens = _i32(seq_lens)
+    rc = load().dkv_compact_step_prefilled(
+        pool, int(layer), int(slots.size), slots.ctypes.data_as(C.c_void_p), lens.ctypes.data_as(C.c_void_p),
+        _dptr(k, torch.float16, "k"), _dptr(v, torch.float16, "v"), _dptr(q_obs, torch.float16, "q_obs"),
+        _dptr(lse_obs, torch.float32, "lse_obs"), _dptr(scores_out, torch.float32, "scores_out"), _stream(stream))
+    return _check(rc, "dkv_compact_step_prefilled") if check else rc
 
 
 def dkv_decode_attention(pool, layer: int, req_slots, q, out, update_scores: bool = False, stream=None,

@@ -26,6 +26,9 @@
  *              first, then lo pages; key / value layouts; sequence split).
  *   [Pol-Ext]  Compaction policy — extensibility (more precision levels;
  *              thresholds adjusted for each head individually).
+ *   [Impl-Arch] System implementation — architecture overview (the KV
+ *              compactor is invoked once the layer's keys and values exist,
+ *              next to the model's own attention over the prompt).
  *
  * Conventions for every entry point
  * ---------------------------------
@@ -226,6 +229,40 @@ int dkv_compact_step(dkv_pool* pool, int32_t layer, int32_t mode, int32_t n_req,
                      const int32_t* req_slots, const int32_t* seq_lens,
                      const void* k, const void* v, const void* q_obs,
                      const float* scores_in, float* scores_out, void* stream);
+
+/* Causal attention over whole prompts [Bkg-Attn] [Impl-Arch], the model's
+ * own prompt attention, computed by the same library so that its
+ * observation rows' log-sum-exps can feed the compactor (the prompt's
+ * scores then need one pass over the keys instead of two). For request i
+ * (seq_lens[i] tokens, host, 1..max_seq_len; requests back to back in call
+ * order) and query head h (KV head h / G):
+ *   out[t][h] = sum_{j<=p} softmax_j(q[t][h] . k_j / sqrt(128)) v_j
+ * for the token t at position p, over the request's keys j = 0..p.
+ *   q       device fp16 [sum(seq_lens)][n_kv_heads*G][128]
+ *   k, v    device fp16 [sum(seq_lens)][n_kv_heads][128]
+ *   out     device fp32 [sum(seq_lens)][n_kv_heads*G][128]
+ *   lse_obs NULL or device fp32 [n_req][n_kv_heads*G][32]: row o receives
+ *           log2 sum_{j<=p} 2^(q.k_j log2(e)/sqrt(128)) for position
+ *           p = seq_len-32+o (the base-2 log-sum-exp of the observation
+ *           query at p), -inf where p < 0.
+ * The pool supplies the geometry and the stream order; no pool state is
+ * read or written (a latched sticky error makes it a device no-op like
+ * every other call). fp16 products accumulate in fp32; the probabilities
+ * enter the value product as an fp16 pair of about 22 significant bits.
+ * Errors: DKV_ERR_ARG (host, nothing queued); DKV_ERR_CUDA. */
+int dkv_prefill_attention(dkv_pool* pool, int32_t n_req, const int32_t* seq_lens, const void* q,
+                          const void* k, const void* v, float* out, float* lse_obs, void* stream);
+
+/* PROMPT compaction [Pol-P] [Mem-PC] [Mem-Fig6] [Impl-Arch] with the
+ * observation rows' log-sum-exps already known (lse_obs of
+ * dkv_prefill_attention over the same requests, in the same order): the
+ * score pass reads the keys once instead of twice. Arguments, results and
+ * errors are those of dkv_compact_step in PROMPT mode with scores_in = NULL;
+ * q_obs holds the last 32 query rows of each prompt, the rows lse_obs was
+ * computed for. lse_obs: device fp32 [n_req][n_kv_heads*G][32]. */
+int dkv_compact_step_prefilled(dkv_pool* pool, int32_t layer, int32_t n_req, const int32_t* req_slots,
+                               const int32_t* seq_lens, const void* k, const void* v, const void* q_obs,
+                               const float* lse_obs, float* scores_out, void* stream);
 
 /* Decode attention of one layer over the mixed-precision pages [Impl-Kern]
  * [Bkg-Attn]: for each request i and query head h,

@@ -74,6 +74,8 @@ def lib():
             L.orc_set_thresholds.argtypes = [P, I, P, P]; L.orc_set_thresholds.restype = I
             L.orc_prefill_attention.argtypes = [I, I, P, I64, P, P, I64, P, P]
             L.orc_prefill_attention.restype = None
+            L.orc_prefill_rows.argtypes = [I, I, P, P, I64, P, P, I64, P, P]
+            L.orc_prefill_rows.restype = None
             L.orc_thresholds.argtypes = [P]; L.orc_thresholds.restype = P
             _lib = L
     return _lib
@@ -133,6 +135,20 @@ def prefill_attention(q_group: np.ndarray, k_head: np.ndarray, v_head: np.ndarra
     out = np.zeros((n0, G, 128), np.float64)
     lse2 = np.zeros((n0, G), np.float64)
     lib().orc_prefill_attention(n0, G, _ptr(q), G * 128, _ptr(k), _ptr(v), 128, _ptr(out), _ptr(lse2))
+    return out, lse2
+
+
+def prefill_rows(positions, q_rows: np.ndarray, k_head: np.ndarray, v_head: np.ndarray):
+    """The same attention at selected positions only: q_rows fp16 [m, G, 128]
+    (row r is the query at positions[r]); k_head, v_head fp16 [n, 128] with
+    n > max(positions). Returns (out fp64 [m, G, 128], lse2 fp64 [m, G])."""
+    pos = np.ascontiguousarray(positions, dtype=np.int32).reshape(-1)
+    q = _u16(q_rows); k = _u16(k_head); v = _u16(v_head)
+    m, G = q.shape[0], q.shape[1]
+    assert pos.size == m and (pos >= 0).all() and int(pos.max()) < k.shape[0]
+    out = np.zeros((m, G, 128), np.float64)
+    lse2 = np.zeros((m, G), np.float64)
+    lib().orc_prefill_rows(m, G, _ptr(pos), _ptr(q), G * 128, _ptr(k), _ptr(v), 128, _ptr(out), _ptr(lse2))
     return out, lse2
 
 

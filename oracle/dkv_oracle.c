@@ -422,40 +422,71 @@ void orc_unit_scores(int n0, int G, const uint16_t* k, int64_t k_stride, const u
  * equation): out[p][h] = sum_{j <= p} softmax_j(q_{p,h} . k_j / sqrt(d)) v_j,
  * and lse2[p][h] = log2 sum_{j <= p} exp(q_{p,h} . k_j / sqrt(d)), the
  * log-sum-exp in base 2 that the score pass of the prompt compaction uses.
- * q rows are q + p * q_stride + h * D; k / v rows k + j * kv_stride. */
+ * One query row qd (D doubles) at position p over keys kd / vd (rows of D
+ * doubles); w holds p + 1 doubles of work space. */
+static void prefill_row(int p, const double* qd, const double* kd, const double* vd, double* w, double* o,
+                        double* lse2) {
+  const double scale = 1.0 / sqrt((double)D);
+  double m = -INFINITY;
+  for (int j = 0; j <= p; j++) {
+    double acc = 0.0;
+    for (int f = 0; f < D; f++) acc += qd[f] * kd[(int64_t)j * D + f];
+    w[j] = acc * scale;
+    if (w[j] > m) m = w[j];
+  }
+  double sum = 0.0;
+  for (int j = 0; j <= p; j++) {
+    w[j] = exp(w[j] - m);
+    sum += w[j];
+  }
+  for (int f = 0; f < D; f++) o[f] = 0.0;
+  for (int j = 0; j <= p; j++)
+    for (int f = 0; f < D; f++) o[f] += w[j] * vd[(int64_t)j * D + f];
+  for (int f = 0; f < D; f++) o[f] /= sum;
+  *lse2 = (m + log(sum)) / log(2.0);
+}
+
+static void widen_rows(int n, const uint16_t* x, int64_t stride, double* xd) {
+  for (int64_t j = 0; j < n; j++)
+    for (int f = 0; f < D; f++) xd[j * D + f] = orc_half_to_float(x[j * stride + f]);
+}
+
+/* Every row of a prompt of n0 tokens: q rows are q + p * q_stride + h * D,
+ * k / v rows k + j * kv_stride; out [n0][G][D], lse2 [n0][G]. */
 void orc_prefill_attention(int n0, int G, const uint16_t* q, int64_t q_stride, const uint16_t* k,
                            const uint16_t* v, int64_t kv_stride, double* out, double* lse2) {
   double* kd = (double*)malloc(sizeof(double) * (size_t)n0 * D);
   double* vd = (double*)malloc(sizeof(double) * (size_t)n0 * D);
   double* w = (double*)malloc(sizeof(double) * (size_t)n0);
-  for (int64_t j = 0; j < n0; j++)
-    for (int f = 0; f < D; f++) {
-      kd[j * D + f] = orc_half_to_float(k[j * kv_stride + f]);
-      vd[j * D + f] = orc_half_to_float(v[j * kv_stride + f]);
-    }
-  const double scale = 1.0 / sqrt((double)D);
+  widen_rows(n0, k, kv_stride, kd);
+  widen_rows(n0, v, kv_stride, vd);
   for (int p = 0; p < n0; p++)
     for (int h = 0; h < G; h++) {
       double qd[D];
       for (int f = 0; f < D; f++) qd[f] = orc_half_to_float(q[(int64_t)p * q_stride + (int64_t)h * D + f]);
-      double m = -INFINITY;
-      for (int j = 0; j <= p; j++) {
-        double acc = 0.0;
-        for (int f = 0; f < D; f++) acc += qd[f] * kd[(int64_t)j * D + f];
-        w[j] = acc * scale;
-        if (w[j] > m) m = w[j];
-      }
-      double sum = 0.0;
-      for (int j = 0; j <= p; j++) {
-        w[j] = exp(w[j] - m);
-        sum += w[j];
-      }
-      double* o = out + ((int64_t)p * G + h) * D;
-      for (int f = 0; f < D; f++) o[f] = 0.0;
-      for (int j = 0; j <= p; j++)
-        for (int f = 0; f < D; f++) o[f] += w[j] * vd[(int64_t)j * D + f];
-      for (int f = 0; f < D; f++) o[f] /= sum;
-      lse2[(int64_t)p * G + h] = (m + log(sum)) / log(2.0);
+      prefill_row(p, qd, kd, vd, w, out + ((int64_t)p * G + h) * D, lse2 + (int64_t)p * G + h);
+    }
+  free(kd); free(vd); free(w);
+}
+
+/* Selected rows of the same attention: row r is the query at position
+ * pos[r] (q + r * q_stride + h * D), over keys 0..pos[r] of k / v; out
+ * [m][G][D], lse2 [m][G]. For checking single outputs of long prompts. */
+void orc_prefill_rows(int m, int G, const int32_t* pos, const uint16_t* q, int64_t q_stride, const uint16_t* k,
+                      const uint16_t* v, int64_t kv_stride, double* out, double* lse2) {
+  int n = 0;
+  for (int r = 0; r < m; r++)
+    if (pos[r] + 1 > n) n = pos[r] + 1;
+  double* kd = (double*)malloc(sizeof(double) * (size_t)n * D);
+  double* vd = (double*)malloc(sizeof(double) * (size_t)n * D);
+  double* w = (double*)malloc(sizeof(double) * (size_t)n);
+  widen_rows(n, k, kv_stride, kd);
+  widen_rows(n, v, kv_stride, vd);
+  for (int r = 0; r < m; r++)
+    for (int h = 0; h < G; h++) {
+      double qd[D];
+      for (int f = 0; f < D; f++) qd[f] = orc_half_to_float(q[(int64_t)r * q_stride + (int64_t)h * D + f]);
+      prefill_row(pos[r], qd, kd, vd, w, out + ((int64_t)r * G + h) * D, lse2 + (int64_t)r * G + h);
     }
   free(kd); free(vd); free(w);
 }

@@ -558,3 +558,24 @@ def test_prefill_attention_equal_keys_and_causality():
     v2[30:] = workloads.random_fp16((n0 - 30, 128), 713)
     out2, _ = oracle.prefill_attention(q, k, v2)
     assert (out2[:30] == out[:30]).all() and not (out2[30:] == out[30:]).all()
+
+
+def test_prefill_rows_match_scipy_and_the_full_prompt():
+    """Selected rows: each equals the scipy row at its position (keys 0..p),
+    and the same row of the whole-prompt computation bit for bit."""
+    n0, G = 90, 3
+    q = workloads.random_fp16((n0, G, 128), 720, scale=1.5)
+    k = workloads.random_fp16((n0, 128), 721)
+    v = workloads.random_fp16((n0, 128), 722)
+    pos = np.array([0, 89, 17, 45, 45, 63])
+    out, lse2 = oracle.prefill_rows(pos, q[pos], k, v)
+    ref, rlse = _dense_causal(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64))
+    np.testing.assert_allclose(out, ref[pos], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse2, rlse[pos], rtol=1e-12, atol=1e-12)
+    full, flse = oracle.prefill_attention(q, k, v)
+    assert (out == full[pos]).all() and (lse2 == flse[pos]).all()
+    # keys after the largest position are never read
+    k2, v2 = k.copy(), v.copy()
+    k2[64:], v2[64:] = 1000.0, -1000.0
+    out3, _ = oracle.prefill_rows(pos[pos < 64], q[pos[pos < 64]], k2, v2)
+    assert (out3 == out[pos < 64]).all()

@@ -202,6 +202,38 @@ def prompt_inputs(name: str, seed: int = 0, requests: list[int] | None = None) -
                 lens=lens_all[reqs].astype(np.int32))
 
 
+def prefill_inputs(name: str, seed: int = 0, requests: list[int] | None = None,
+                   max_len: int | None = None) -> dict:
+    """Inputs of the prompt's own attention: prompt_inputs plus q fp16
+    [sum(lens), Hq, 128], every prompt position's query (requests back to
+    back). The last 32 rows of each request are its observation queries
+    (q_obs row o = position len-32+o); the earlier rows come from a stream of
+    their own with the same per-head structure. max_len truncates every
+    prompt to its first max_len tokens, whose last 32 rows then form q_obs."""
+    w = WORKLOADS[name]
+    st = head_structure(w, seed)
+    base = prompt_inputs(name, seed, requests)
+    reqs = list(range(w.n_requests)) if requests is None else list(requests)
+    ks, vs, qs, qo, lens = [], [], [], [], []
+    t0 = 0
+    for i, r in enumerate(reqs):
+        n = int(base["lens"][i])
+        rng = _rng(name, seed, "prefill_q", r)
+        early = _normal16(rng, (max(n - OBS_WINDOW, 0), w.n_q_heads, HEAD_DIM))
+        _shape_q(early, st, w)
+        q = np.concatenate([early.astype(np.float16), base["q_obs"][i][max(OBS_WINDOW - n, 0):]])
+        m = n if max_len is None else min(n, max_len)
+        ks.append(base["k"][t0:t0 + m]); vs.append(base["v"][t0:t0 + m]); qs.append(q[:m])
+        obs = np.zeros((OBS_WINDOW, w.n_q_heads, HEAD_DIM), np.float16)
+        take = min(m, OBS_WINDOW)
+        obs[OBS_WINDOW - take:] = q[m - take:m]
+        qo.append(obs)
+        lens.append(m)
+        t0 += n
+    return dict(k=np.concatenate(ks), v=np.concatenate(vs), q=np.concatenate(qs), q_obs=np.stack(qo),
+                lens=np.array(lens, dtype=np.int32))
+
+
 def _add_heavy_hitters(k: np.ndarray, q: np.ndarray, w: Workload, rng: np.random.Generator):
     """Give heavy_frac of the keys outside the recent window a key component
     along the unit mean of the group's observation queries, sized so that the
