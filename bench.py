@@ -14,7 +14,9 @@ flushed before each decode step). compact_step is reported in us per layer.
 The same loop then runs, untimed for the headline, on the 70B-shaped layer,
 on the 8B-shaped layer with 4 KB pages (the kernel for any page geometry),
 and on the Qwen2.5-7B-shaped GQA-7 batch; their figures, each with its own
-fraction of the HBM roofline, are in `parts`.
+fraction of the HBM roofline, are in `parts`. `parts.prefill` times the
+prompt's own causal attention (TFLOP/s against the tensor-core roofline) and
+the prompt compact_step that takes that attention's log-sum-exps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dkv|reference]
 
@@ -105,6 +107,14 @@ def hbm_peak():
     if "hbm_gbs" in p:
         return float(p["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """Dense fp16/bf16 tensor-core peak for a kernel timed alone (burst)."""
+    p = peaks()
+    if "bf16_tflops" in p:
+        return float(p["bf16_tflops"]), "measured bf16 burst"
+    return 1900.0, "fallback"
 
 
 # --------------------------------------------------------------------- clocks
@@ -468,6 +478,95 @@ def run_churn(dkv, dev, seed: int, ticks: int, peak: float) -> dict:
             "list_start": s["list_start"], "list_end": s["list_end"], "list_wraps": s["list_end"] // n_pages}
 
 
+# ---------------------------------------------------------------- prefill
+def prefill_flops(lens, hq: int) -> float:
+    """Algorithmic FLOPs of causal attention over the prompts: q.k and p.v,
+    2 d each, for every (query, key <= query) pair of every query head."""
+    return float(sum(4 * 128 * n * (n + 1) // 2 for n in lens) * hq)
+
+
+def run_prefill(dkv, dev, name: str, seed: int, reps: int, peak: float, n_req: int | None = None) -> dict:
+    """The prompt's own causal attention (dkv_prefill_attention) and the
+    PROMPT compaction that takes its observation rows' log-sum-exps
+    (dkv_compact_step_prefilled) beside the compaction that computes them
+    itself (dkv_compact_step), each timed alone with CUDA events from a
+    flushed L2 on the same batch."""
+    import torch
+    w = workloads.WORKLOADS[name]
+    inp = workloads.prefill_inputs(name, seed, None if n_req is None else list(range(n_req)))
+    lens = [int(x) for x in inp["lens"]]
+    Hq = w.n_q_heads
+    cfg = w.pool_config()
+    pool = dkv.dkv_pool_create(dkv.make_config(**{k: v for k, v in cfg.items()
+                                                  if k in dict(dkv.dkv_config._fields_)}), dev.index)
+    q = torch.from_numpy(inp["q"]).to(dev)
+    k = torch.from_numpy(inp["k"]).to(dev)
+    v = torch.from_numpy(inp["v"]).to(dev)
+    qo = torch.from_numpy(inp["q_obs"]).to(dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((len(lens), Hq, 32), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    st_ = torch.cuda.current_stream()
+    slots = list(range(len(lens)))
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, after=None):
+        ts = []
+        for it in range(reps + 2):
+            flush.fill_(it & 0xFF)
+            torch.amax(flush_rd)
+            torch.cuda._sleep(200_000)      # the launches queue behind a device wait
+            e0, e1 = ev(), ev()
+            e0.record(st_)
+            fn()
+            e1.record(st_)
+            if after is not None:
+                after()
+            if it >= 2:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+    def free_all():
+        for s_ in slots:
+            dkv.dkv_free_request(pool, s_)
+
+    pf_ms = timed(lambda: dkv.dkv_prefill_attention(pool, lens, q, k, v, out, lse))
+    cp_ms = timed(lambda: dkv.dkv_compact_step_prefilled(pool, 0, slots, lens, k, v, qo, lse), free_all)
+    dkv.dkv_compact_step_prefilled(pool, 0, slots, lens, k, v, qo, lse)
+    s = dkv.dkv_pool_status(pool)
+    assert s["error"] == 0, s
+    counts = (s["hi_tokens"], s["lo_tokens"])
+    free_all()
+    cs_ms = timed(lambda: dkv.dkv_compact_step(pool, 0, dkv.DKV_PROMPT, slots, lens, k, v, qo), free_all)
+    s = dkv.dkv_pool_status(pool)
+    assert s["error"] == 0, s
+    dkv.dkv_pool_destroy(pool)
+    n_th = sum(lens) * w.n_kv_heads
+    pbytes = prompt_bytes(counts[0], counts[1], n_th, len(lens), Hq)
+    fl = prefill_flops(lens, Hq)
+    tf = fl / (pf_ms * 1e-3) / 1e12
+    tpk, tkind = tensor_peak()
+    gb = lambda ms: pbytes / (ms * 1e-3) / 1e9
+    return {
+        "workload": f"{name}: {w.shape}-shaped layer, {len(lens)} prompts of {lens[0]} tokens, {Hq} q / "
+                    f"{w.n_kv_heads} KV heads, d=128, fp16 q/k/v, fp32 out",
+        "prefill_attention_ms": round(pf_ms, 3),
+        "prefill_attention_tflops": round(tf, 1),
+        "prefill_attention_frac": round(tf / tpk, 4),
+        "prefill_peak": f"{tpk} TFLOP/s ({tkind}; fp16 and bf16 share the tensor-core rate)",
+        "prefill_flops": fl,
+        "prefill_flops_are": "algorithmic: 4 d per causal (query, key) pair per query head; the kernel "
+                             "executes 1.5x (the probabilities enter the value product as an fp16 pair)",
+        "compact_step_prefilled_us_per_layer": round(cp_ms * 1e3, 1),
+        "compact_step_prefilled_gbs": round(gb(cp_ms), 1),
+        "compact_step_prefilled_frac": round(gb(cp_ms) / peak, 4),
+        "compact_step_same_batch_us_per_layer": round(cs_ms * 1e3, 1),
+        "compact_step_bytes": int(pbytes),
+    }
+
+
 # ------------------------------------------------------------- dkv (GPU)
 def run_dkv(args, world, rank, local):
     import torch
@@ -541,6 +640,10 @@ def run_dkv(args, world, rank, local):
         result["parts"]["other_configs"][name] = ex.summary(rr, peak)
         ex.close()
         del ex
+        torch.cuda.empty_cache()
+    if args.prefill_reps > 0:
+        result["parts"]["prefill"] = run_prefill(dkv, dev, args.workload, args.seed + rank, args.prefill_reps,
+                                                 peak, args.prefill_requests)
         torch.cuda.empty_cache()
     if args.churn_ticks > 0:
         result["parts"]["churn"] = run_churn(dkv, dev, args.seed + rank, args.churn_ticks, peak)
@@ -731,6 +834,10 @@ def main():
     ap.add_argument("--extra-steps", type=int, default=2)
     ap.add_argument("--churn-ticks", type=int, default=1500,
                     help="ticks of the QwQ-32B-shaped arrival / completion workload (0: skip)")
+    ap.add_argument("--prefill-reps", type=int, default=3,
+                    help="timed repetitions of the prompt attention and prefilled compaction (0: skip)")
+    ap.add_argument("--prefill-requests", type=int, default=None,
+                    help="first N requests of the workload for the prefill part (default: all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--dry-run", action="store_true", help="rank start-up and reductions only (gloo, no GPU)")
