@@ -21,6 +21,20 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t addr) {
   return d;
 }
 
+// The same layout read as an MN-major operand (the N dimension contiguous):
+// rows of 128 bytes hold 64 consecutive N elements, 8-row groups along K are
+// 1024 bytes apart (stride byte offset) and the next 64 N elements start
+// `lbo` bytes further (leading byte offset). A k-step of 16 rows advances the
+// start address by two 8-row groups (2048 bytes).
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t addr, uint32_t lbo) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;       // leading byte offset: next 64 N elements
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset: next 8 K rows
+  d |= (uint64_t)1 << 46;                            // descriptor version
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor of kind::f16: fp16 A and B (both K-major), fp32 D,
 // M x N x 16.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
@@ -33,6 +47,17 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
           d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+// D (tensor memory) = A B^T (+ D) with A read from tensor memory: row m of A
+// in lane m, two 16-bit K elements per 32-bit column (the lower half holds
+// the even element), K/2 columns from a_tmem.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::
+          "r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
 // One arrival on the mbarrier once every tcgen05 operation this thread issued
@@ -74,6 +99,27 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float* v) {
         "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15])
       : "r"(taddr));
 }
+// 16 consecutive 32-bit columns of the calling thread's lane from v[0..16).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+// 32 consecutive 32-bit columns of the calling thread's lane from v[0..32).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 // 32 consecutive fp32 columns of the calling thread's lane, waited for.

@@ -513,6 +513,9 @@ cudaError_t configure_tc_g() {
 }
 }  // namespace
 
+// The driver's tensor-map encoder, looked up once (shared with prefill_tc.cu).
+cudaError_t tma_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) { return encoder(fn); }
+
 cudaError_t configure_prompt_tc() {
   cudaError_t e;
   if ((e = configure_tc_g<1>()) != cudaSuccess) return e;
