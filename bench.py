@@ -48,14 +48,14 @@ METRIC = "compressed-KV decode attn GB/s (% of GB300 HBM peak); compact_step µs
 HI_BYTES, LO_BYTES, SCORE_RMW = 200, 104, 8
 # kernels the library launches: prompt compact_step (setup, two tensor-core
 # scoring passes, lse merge, classification, three plan kernels, scatter,
-# two pack kernels), decode compact_step (plan, alloc, apply), decode
-# attention (attention, epilogue), free_request (one)
-LAUNCHES = {"prompt": 11, "decode": 3, "attention": 2, "free": 1}
+# pack), decode compact_step (plan, alloc, apply), decode attention
+# (attention, epilogue), free_request (one)
+LAUNCHES = {"prompt": 10, "decode": 3, "attention": 2, "free": 1}
 
 # DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum, caches
 # flushed by ncu before each kernel) of the llama8b bench step:
 #   one decode-attention call (k_attn_paged + k_attn_epi, third decode step);
-#   one prompt compact_step (its 11 kernels, timed step).
+#   one prompt compact_step (its 10 kernels, timed step).
 # Valid only for the kernel sources they were taken on: any change to them
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {

@@ -83,17 +83,13 @@ __global__ void __launch_bounds__(128) k_prompt_scatter(PoolView pv, const uint1
 }
 
 // ---------------------------------------------------------------------------
-// a4: quantize + pack, one kernel per tier (HI: K8V4, LO: K4V2). A warp
-// handles groups of 8 consecutive ranks of one head: 4 lanes per token, 32
-// features per lane. A group fills whole value rows (4 pair-rows hi, 2
-// quad-rows lo); the value words are assembled in shared memory and written
-// as full 128-byte rows. Each warp takes kPackGroups groups in turn and keeps
-// the loads ahead of the math: the positions of the group after next and the
-// K/V rows of the next group are in flight while a group is quantized and
-// stored. The codes follow qcode (the oracle's arithmetic); a zero scale has
+// a4: quantize + pack (hi: K8V4, lo: K4V2). A warp handles groups of 8
+// consecutive ranks of one head's tier: 4 lanes per token, 32 features per
+// lane. A group fills whole value rows (4 pair-rows hi, 2 quad-rows lo); the
+// value words are assembled in shared memory and written as full 128-byte
+// rows. The codes follow qcode (the oracle's arithmetic); a zero scale has
 // inv = 0, which gives code 0 without a branch.
 // ---------------------------------------------------------------------------
-constexpr int kPackGroups = 4;   // groups per warp
 constexpr int kPackTok = 8;      // tokens per group
 
 // Code arithmetic of qcode, taken apart: t = (x - z) * inv for a pair in
@@ -115,37 +111,200 @@ __device__ __forceinline__ uint32_t pack_sat(int a, int b, uint32_t c) {
   return d;
 }
 
+// The group of 8 consecutive ranks r0 .. r0+7 of one head's tier. Lane
+// (e, q) holds token e's K and V features 32q .. 32q+31 in kv (4 uint4 of K,
+// then 4 of V) and its position j (-1 past the tier's count); grant: the
+// head's granted page IDs; s_vw: the warp's [token][value word] scratch.
 template <bool HI>
-__global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* __restrict__ k,
-                                                      const __half* __restrict__ v,
-                                                      const float* __restrict__ score,
-                                                      const int* __restrict__ rank2pos,
-                                                      const int4* __restrict__ unit_info,
-                                                      const int* __restrict__ grant_ids, int grant_cap) {
+__device__ __forceinline__ void pack_group(const PoolView& pv, const uint4 (&kv)[8], int j, int r0, int count,
+                                           int gcnt, const int* __restrict__ grant, const float* __restrict__ score,
+                                           size_t tok_base, int kvh, uint32_t (*s_vw)[32]) {
   constexpr int KB = HI ? 8 : 4, VB = HI ? 4 : 2, GSZ = 8 / VB;   // GSZ: tokens per value row
-  if (pv.noop()) return;
-  __shared__ uint32_t s_vw[8][kPackTok][32];   // [warp][token][value word] code bits of the token
-  const int unit = blockIdx.y;
-  const int i = unit / pv.hkv, kvh = unit % pv.hkv;
-  const int4 ui = unit_info[unit];             // grant pages, hi count, lo count, -
-  const int count = HI ? ui.y : ui.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // group x of this warp starts at rank base + 64 x
-  const int base = (blockIdx.x * kPackGroups * 8 + warp) * kPackTok;
-  if (base >= count) return;
   const TierGeom& tg = HI ? pv.hi : pv.lo;
-  const int e = lane >> 2, q = lane & 3;       // token e of the 8, features 32q..32q+31
-  const CallArgs* ca = pv.call;
-  const int* r2p = rank2pos + ((size_t)unit * 2 + (HI ? 1 : 0)) * pv.max_seq;
-  const size_t tok_base = (size_t)ca->tok0[i];
-  const int gcnt = ui.x;
-  auto pos_of = [&](int x) {
-    const int r = base + 8 * kPackTok * x + e;
-    return r < count ? __ldg(r2p + r) : -1;
-  };
-  auto load_kv = [&](int j, uint4 (&kv)[8]) {
-    if (j >= 0) {
+  const int lane = threadIdx.x & 31, e = lane >> 2, q = lane & 3;   // token e of the 8, features 32q..32q+31
+  // bit offset of this token's slot inside a value word
+  const int slot_e = e % GSZ;
+  const int eb = VB == 4 ? 16 * slot_e : 16 * (slot_e & 1) + 2 * (slot_e >> 1);
+  const int r = r0 + e;
+  const bool valid = r < count;
+  const __half2* kh = reinterpret_cast<const __half2*>(&kv[0]);   // 16 pairs
+  const __half2* vh = reinterpret_cast<const __half2*>(&kv[4]);
+  float kmn, kmx, vmn, vmx;
+  {
+    __half2 kmn2 = kh[0], kmx2 = kh[0], vmn2 = vh[0], vmx2 = vh[0];
+#pragma unroll
+    for (int y = 1; y < 16; y++) {   // min / max of fp16 values are exact
+      kmn2 = __hmin2(kmn2, kh[y]);
+      kmx2 = __hmax2(kmx2, kh[y]);
+      vmn2 = __hmin2(vmn2, vh[y]);
+      vmx2 = __hmax2(vmx2, vh[y]);
+    }
+    kmn = fminf(__low2float(kmn2), __high2float(kmn2));
+    kmx = fmaxf(__low2float(kmx2), __high2float(kmx2));
+    vmn = fminf(__low2float(vmn2), __high2float(vmn2));
+    vmx = fmaxf(__low2float(vmx2), __high2float(vmx2));
+  }
+  // every lane takes part in the token reductions; invalid lanes hold zeros
+#pragma unroll
+  for (int sh = 1; sh <= 2; sh <<= 1) {
+    kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, sh, 4));
+    kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, sh, 4));
+    vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, sh, 4));
+    vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, sh, 4));
+  }
+  const QParams kq = qparams(kmn, kmx, KB), vq = qparams(vmn, vmx, VB);
+  // the token's bits of value words 8q .. 8q+7 (features 4w .. 4w+3)
+  __syncwarp();                              // the previous group's value rows are written
+#pragma unroll
+  for (int w = 0; w < 8; w++) {
+    // the token's codes of features 4w .. 4w+3 at bits 4i of its 16-bit field
+    const float2 a = __half22float2(vh[2 * w]), b = __half22float2(vh[2 * w + 1]);
+    int c0, c1, c2, c3;
+    qt2(a.x, a.y, vq, c0, c1);
+    qt2(b.x, b.y, vq, c2, c3);
+    uint32_t f;
+    if (VB == 4) {
+      f = pack_sat<4>(c1, c0, pack_sat<4>(c3, c2, 0u));
+    } else {                               // 2-bit codes 4 bits apart (zero between)
+      f = pack_sat<2>(0, c0, pack_sat<2>(0, c1, pack_sat<2>(0, c2, pack_sat<2>(0, c3, 0u))));
+    }
+    s_vw[e][8 * q + w] = valid ? f << eb : 0u;
+  }
+  if (valid) {
+    // page and slot of rank r: hi from the left of the grant, lo from the right
+    const int pidx = HI ? tg.div(r) : gcnt - 1 - tg.div(r);
+    const int slot = r - tg.div(r) * tg.t;
+    uint8_t* page = pv.page(grant[pidx]);
+    uint8_t* krow = page + tg.off[0] + slot * tg.kbytes;
+    if (HI) {
+      uint32_t w[8];
+#pragma unroll
+      for (int y = 0; y < 8; y++) {             // bytes 4y .. 4y+3
+        const float2 a = __half22float2(kh[2 * y]), b = __half22float2(kh[2 * y + 1]);
+        int c0, c1, c2, c3;
+        qt2(a.x, a.y, kq, c0, c1);
+        qt2(b.x, b.y, kq, c2, c3);
+        w[y] = pack_sat<8>(c1, c0, pack_sat<8>(c3, c2, 0u));
+      }
+      uint4* dst = reinterpret_cast<uint4*>(krow + 32 * q);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int y = 0; y < 4; y++) {             // bytes 4y .. 4y+3: features 8y .. 8y+7
+        uint32_t acc = 0u;
+#pragma unroll
+        for (int z = 3; z >= 0; z--) {          // byte z: feature 2z low nibble, 2z + 1 high
+          const float2 a = __half22float2(kh[4 * y + z]);
+          int c0, c1;
+          qt2(a.x, a.y, kq, c0, c1);
+          acc = pack_sat<4>(c1, c0, acc);
+        }
+        w[y] = acc;
+      }
+      *reinterpret_cast<uint4*>(krow + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (q == 0) {
       const size_t tok = (tok_base + j) * pv.hkv + kvh;
+      *reinterpret_cast<uint32_t*>(page + tg.off[2] + 4 * slot) = (uint32_t)kq.sh | ((uint32_t)kq.zh << 16);
+      *reinterpret_cast<uint32_t*>(page + tg.off[3] + 4 * slot) = (uint32_t)vq.sh | ((uint32_t)vq.zh << 16);
+      *reinterpret_cast<float*>(page + tg.off[4] + 4 * slot) = score[tok];
+      *reinterpret_cast<int*>(page + tg.off[5] + 4 * slot) = j;
+    }
+  }
+  __syncwarp();
+  // value rows: GSZ tokens each (4 pair-rows hi, 2 quad-rows lo)
+#pragma unroll
+  for (int row = 0; row < kPackTok / GSZ; row++) {
+    const int rfirst = r0 + row * GSZ;
+    if (rfirst >= count) break;
+    const int pidx = HI ? tg.div(rfirst) : gcnt - 1 - tg.div(rfirst);
+    const int slot0 = rfirst - tg.div(rfirst) * tg.t;
+    uint8_t* page = pv.page(grant[pidx]);
+    uint32_t word = 0;
+#pragma unroll
+    for (int ee = 0; ee < GSZ; ee++) word |= s_vw[row * GSZ + ee][lane];
+    *reinterpret_cast<uint32_t*>(page + tg.off[1] + (slot0 / GSZ) * 128 + 4 * lane) = word;
+  }
+}
+
+// One persistent grid over both tiers of every head of the call: the groups
+// are numbered head by head (the head's hi groups, then its lo groups) and
+// warp w of the grid takes groups w, w + W, w + 2W, ... (W warps in all), so
+// that every warp streams one long sequence with its loads ahead of the math:
+// the positions of the group after next and the K/V rows of the next group
+// are in flight while a group is quantized and stored.
+__global__ void __launch_bounds__(256, 2) k_prompt_pack(PoolView pv, const __half* __restrict__ k,
+                                                         const __half* __restrict__ v,
+                                                         const float* __restrict__ score,
+                                                         const int* __restrict__ rank2pos,
+                                                         const int4* __restrict__ unit_info,
+                                                         const int* __restrict__ grant_ids, int grant_cap) {
+  if (pv.noop()) return;
+  extern __shared__ int s_pref[];              // [n_units + 1] first group of each head
+  __shared__ uint32_t s_vw[8][kPackTok][32];   // [warp][token][value word] code bits of the token
+  __shared__ int s_warp[8];
+  const CallArgs* ca = pv.call;
+  const int hkv = pv.hkv, n_units = ca->n_req * hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, e = lane >> 2, q = lane & 3;
+  {
+    // exclusive prefix over the heads of their group counts (a contiguous run of heads per thread)
+    const int per = (n_units + blockDim.x - 1) / blockDim.x;
+    const int u0 = min(n_units, (int)threadIdx.x * per), u1 = min(n_units, u0 + per);
+    int sum = 0;
+    for (int u = u0; u < u1; u++) {
+      const int4 ui = unit_info[u];
+      sum += (ui.y + kPackTok - 1) / kPackTok + (ui.z + kPackTok - 1) / kPackTok;
+    }
+    int x = sum;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, s);
+      if (lane >= s) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    int run = x - sum;
+    for (int w = 0; w < warp; w++) run += s_warp[w];
+    for (int u = u0; u < u1; u++) {
+      s_pref[u] = run;
+      const int4 ui = unit_info[u];
+      run += (ui.y + kPackTok - 1) / kPackTok + (ui.z + kPackTok - 1) / kPackTok;
+    }
+    if (threadIdx.x == blockDim.x - 1) s_pref[n_units] = run;
+    __syncthreads();
+  }
+  const int total = s_pref[n_units];
+  const int W = gridDim.x * 8;
+  struct Grp {
+    int unit, r0, count, gcnt;
+    bool hi;
+  };
+  auto describe = [&](int x, Grp& d) {
+    if (x >= total) return false;
+    int lo = 0, hi = n_units - 1;              // last head with s_pref <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pref[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int4 ui = unit_info[lo];
+    const int gh = (ui.y + kPackTok - 1) / kPackTok, off = x - s_pref[lo];
+    d.unit = lo;
+    d.hi = off < gh;
+    d.r0 = kPackTok * (d.hi ? off : off - gh);
+    d.count = d.hi ? ui.y : ui.z;
+    d.gcnt = ui.x;
+    return true;
+  };
+  auto pos_of = [&](bool has, const Grp& d) {
+    if (!has) return -1;
+    const int r = d.r0 + e;
+    return r < d.count ? __ldg(rank2pos + ((size_t)d.unit * 2 + (d.hi ? 1 : 0)) * pv.max_seq + r) : -1;
+  };
+  auto load_kv = [&](const Grp& d, int j, uint4 (&kv)[8]) {
+    if (j >= 0) {
+      const size_t tok = (size_t)(ca->tok0[d.unit / hkv] + j) * hkv + d.unit % hkv;
       const uint4* kp = reinterpret_cast<const uint4*>(k + tok * kD + q * 32);
       const uint4* vp = reinterpret_cast<const uint4*>(v + tok * kD + q * 32);
 #pragma unroll
@@ -158,125 +317,31 @@ __global__ void __launch_bounds__(256) k_prompt_pack(PoolView pv, const __half* 
       for (int y = 0; y < 8; y++) kv[y] = make_uint4(0, 0, 0, 0);
     }
   };
-  int j_cur = pos_of(0), j_next = pos_of(1);
-  uint4 kv_cur[8], kv_next[8];
-  load_kv(j_cur, kv_cur);
-  // bit offset of this token's slot inside a value word
-  const int slot_e = e % GSZ;
-  const int eb = VB == 4 ? 16 * slot_e : 16 * (slot_e & 1) + 2 * (slot_e >> 1);
-  for (int x = 0; x < kPackGroups; x++) {
-    const int r0 = base + 8 * kPackTok * x;
-    if (r0 >= count) break;
-    int j_after = -1;
-    if (x + 1 < kPackGroups) load_kv(j_next, kv_next);
-    if (x + 2 < kPackGroups) j_after = pos_of(x + 2);
-    const int r = r0 + e;
-    const bool valid = r < count;
-    const int j = j_cur;
-    const __half2* kh = reinterpret_cast<const __half2*>(&kv_cur[0]);   // 16 pairs
-    const __half2* vh = reinterpret_cast<const __half2*>(&kv_cur[4]);
-    float kmn, kmx, vmn, vmx;
-    {
-      __half2 kmn2 = kh[0], kmx2 = kh[0], vmn2 = vh[0], vmx2 = vh[0];
+  int x = blockIdx.x * 8 + warp;
+  Grp dc, dn, da;
+  bool hc = describe(x, dc), hn = describe(x + W, dn);
+  int jc = pos_of(hc, dc), jn = pos_of(hn, dn);
+  uint4 kvc[8], kvn[8];
+  if (hc) load_kv(dc, jc, kvc);
+  while (hc) {
+    if (hn) load_kv(dn, jn, kvn);
+    const bool ha = describe(x + 2 * W, da);
+    const int ja = pos_of(ha, da);
+    const int i = dc.unit / hkv, kvh = dc.unit % hkv;
+    const int* grant = grant_ids + (size_t)dc.unit * grant_cap;
+    if (dc.hi)
+      pack_group<true>(pv, kvc, jc, dc.r0, dc.count, dc.gcnt, grant, score, (size_t)ca->tok0[i], kvh, s_vw[warp]);
+    else
+      pack_group<false>(pv, kvc, jc, dc.r0, dc.count, dc.gcnt, grant, score, (size_t)ca->tok0[i], kvh, s_vw[warp]);
+    dc = dn;
+    hc = hn;
+    jc = jn;
+    dn = da;
+    hn = ha;
+    jn = ja;
 #pragma unroll
-      for (int y = 1; y < 16; y++) {   // min / max of fp16 values are exact
-        kmn2 = __hmin2(kmn2, kh[y]);
-        kmx2 = __hmax2(kmx2, kh[y]);
-        vmn2 = __hmin2(vmn2, vh[y]);
-        vmx2 = __hmax2(vmx2, vh[y]);
-      }
-      kmn = fminf(__low2float(kmn2), __high2float(kmn2));
-      kmx = fmaxf(__low2float(kmx2), __high2float(kmx2));
-      vmn = fminf(__low2float(vmn2), __high2float(vmn2));
-      vmx = fmaxf(__low2float(vmx2), __high2float(vmx2));
-    }
-    // every lane takes part in the token reductions; invalid lanes hold zeros
-#pragma unroll
-    for (int sh = 1; sh <= 2; sh <<= 1) {
-      kmn = fminf(kmn, __shfl_xor_sync(0xffffffffu, kmn, sh, 4));
-      kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, sh, 4));
-      vmn = fminf(vmn, __shfl_xor_sync(0xffffffffu, vmn, sh, 4));
-      vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, sh, 4));
-    }
-    const QParams kq = qparams(kmn, kmx, KB), vq = qparams(vmn, vmx, VB);
-    // the token's bits of value words 8q .. 8q+7 (features 4w .. 4w+3)
-    __syncwarp();                              // the previous group's value rows are written
-#pragma unroll
-    for (int w = 0; w < 8; w++) {
-      // the token's codes of features 4w .. 4w+3 at bits 4i of its 16-bit field
-      const float2 a = __half22float2(vh[2 * w]), b = __half22float2(vh[2 * w + 1]);
-      int c0, c1, c2, c3;
-      qt2(a.x, a.y, vq, c0, c1);
-      qt2(b.x, b.y, vq, c2, c3);
-      uint32_t f;
-      if (VB == 4) {
-        f = pack_sat<4>(c1, c0, pack_sat<4>(c3, c2, 0u));
-      } else {                               // 2-bit codes 4 bits apart (zero between)
-        f = pack_sat<2>(0, c0, pack_sat<2>(0, c1, pack_sat<2>(0, c2, pack_sat<2>(0, c3, 0u))));
-      }
-      s_vw[warp][e][8 * q + w] = valid ? f << eb : 0u;
-    }
-    if (valid) {
-      // page and slot of rank r: hi from the left of the grant, lo from the right
-      const int pidx = HI ? tg.div(r) : gcnt - 1 - tg.div(r);
-      const int slot = r - tg.div(r) * tg.t;
-      uint8_t* page = pv.page(grant_ids[(size_t)unit * grant_cap + pidx]);
-      uint8_t* krow = page + tg.off[0] + slot * tg.kbytes;
-      if (HI) {
-        uint32_t w[8];
-#pragma unroll
-        for (int y = 0; y < 8; y++) {             // bytes 4y .. 4y+3
-          const float2 a = __half22float2(kh[2 * y]), b = __half22float2(kh[2 * y + 1]);
-          int c0, c1, c2, c3;
-          qt2(a.x, a.y, kq, c0, c1);
-          qt2(b.x, b.y, kq, c2, c3);
-          w[y] = pack_sat<8>(c1, c0, pack_sat<8>(c3, c2, 0u));
-        }
-        uint4* dst = reinterpret_cast<uint4*>(krow + 32 * q);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      } else {
-        uint32_t w[4];
-#pragma unroll
-        for (int y = 0; y < 4; y++) {             // bytes 4y .. 4y+3: features 8y .. 8y+7
-          uint32_t acc = 0u;
-#pragma unroll
-          for (int z = 3; z >= 0; z--) {          // byte z: feature 2z low nibble, 2z + 1 high
-            const float2 a = __half22float2(kh[4 * y + z]);
-            int c0, c1;
-            qt2(a.x, a.y, kq, c0, c1);
-            acc = pack_sat<4>(c1, c0, acc);
-          }
-          w[y] = acc;
-        }
-        *reinterpret_cast<uint4*>(krow + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      if (q == 0) {
-        const size_t tok = (tok_base + j) * pv.hkv + kvh;
-        *reinterpret_cast<uint32_t*>(page + tg.off[2] + 4 * slot) = (uint32_t)kq.sh | ((uint32_t)kq.zh << 16);
-        *reinterpret_cast<uint32_t*>(page + tg.off[3] + 4 * slot) = (uint32_t)vq.sh | ((uint32_t)vq.zh << 16);
-        *reinterpret_cast<float*>(page + tg.off[4] + 4 * slot) = score[tok];
-        *reinterpret_cast<int*>(page + tg.off[5] + 4 * slot) = j;
-      }
-    }
-    __syncwarp();
-    // value rows: GSZ tokens each (4 pair-rows hi, 2 quad-rows lo)
-#pragma unroll
-    for (int row = 0; row < kPackTok / GSZ; row++) {
-      const int rfirst = r0 + row * GSZ;
-      if (rfirst >= count) break;
-      const int pidx = HI ? tg.div(rfirst) : gcnt - 1 - tg.div(rfirst);
-      const int slot0 = rfirst - tg.div(rfirst) * tg.t;
-      uint8_t* page = pv.page(grant_ids[(size_t)unit * grant_cap + pidx]);
-      uint32_t word = 0;
-#pragma unroll
-      for (int ee = 0; ee < GSZ; ee++) word |= s_vw[warp][row * GSZ + ee][lane];
-      *reinterpret_cast<uint32_t*>(page + tg.off[1] + (slot0 / GSZ) * 128 + 4 * lane) = word;
-    }
-    j_cur = j_next;
-    j_next = j_after;
-#pragma unroll
-    for (int y = 0; y < 8; y++) kv_cur[y] = kv_next[y];
+    for (int y = 0; y < 8; y++) kvc[y] = kvn[y];
+    x += W;
   }
 }
 
@@ -294,6 +359,10 @@ cudaError_t configure_kernels() {
   if ((e = configure_prompt_tc()) != cudaSuccess) return e;
   if ((e = configure_alloc()) != cudaSuccess) return e;
   if ((e = configure_prefill()) != cudaSuccess) return e;
+  // the pack kernel keeps one int per head of the call in shared memory
+  if ((e = cudaFuncSetAttribute(k_prompt_pack, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) !=
+      cudaSuccess)
+    return e;
   return configure_attention();
 }
 
@@ -322,12 +391,9 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long 
   if ((e = launch_prompt_plan(P, layer, n_req, st)) != cudaSuccess) return e;
   k_prompt_scatter<<<grid, 128, 0, st>>>(P.pv, s.tokinfo, s.bbase, s.rank2pos, s.nkb_cap);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const dim3 gpack((max_len + 8 * kPackTok * kPackGroups - 1) / (8 * kPackTok * kPackGroups), n_req * P.pv.hkv);
-  k_prompt_pack<true><<<gpack, 256, 0, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info, s.grant_ids,
-                                             s.grant_cap);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  k_prompt_pack<false><<<gpack, 256, 0, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info, s.grant_ids,
-                                              s.grant_cap);
+  const size_t pref = sizeof(int) * ((size_t)n_req * P.pv.hkv + 1);
+  k_prompt_pack<<<2 * P.sm_count, 256, pref, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info, s.grant_ids,
+                                                   s.grant_cap);
   return cudaGetLastError();
 }
 
