@@ -60,23 +60,23 @@ LAUNCHES = {"prompt": 10, "decode": 3, "attention": 2, "free": 1}
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 119_721_472 + 4_718_592 + 30_604_800,
+    "bytes_per_call": 119_645_952 + 4_707_072 + 30_606_336,
     "sources": {
         "attention.cu": "b0273bced4432a3eca8deb4e5a1f832c3de2fa4a1113c47c78b43f15ecfbc1cd",
         "dkv_common.cuh": "bcd6734e6c5b4bd5fc941201972200f49e4eed4b73ae8e36152d81d14831054a",
-        "dkv_kernels.cuh": "1af05a5c3c6beb7a744278fb7fe797da5149d278f8177afc2dcb8418855110f2",
+        "dkv_kernels.cuh": "8b696d22cc7aad5a45af9c7632518d943f3eb86e086728ea9c67a90bc1b2ce06",
     },
 }
 PROMPT_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 1_022_412_800 + 80_523_008,
+    "bytes_per_call": 1_018_308_096 + 103_099_648,
     "sources": {
-        "prompt.cu": "96c5fde7c38c3a74cef6db6489935e4c7609d3fddd4be3347bdedaf7df55c45c",
-        "prompt_tc.cu": "e3397f1f6e2da567f1ffcd33c9571d0dc34a882aaf3878b22c8bb86779f9287a",
+        "prompt.cu": "e7677c71cd5c346b45bb412ebcba1827dc7640e58abe352da3618341f309fde7",
+        "prompt_tc.cu": "fa63d0ced7a2f9d8266fe4673083378e67dddf037238d1f050656313a455b8c1",
         "alloc.cu": "4b1b90d8af16eca24a790b2bfff5e6c9ac5de18f04712cde3b02fdaedde08e40",
-        "dkv_tc.cuh": "6988ad672fc0d64fda8ef7e915b2b0097fc3a5e8361ee2245de3fa50606bcb39",
+        "dkv_tc.cuh": "acb3452effe630c9cbc898bc8a87929dbf4ecd2f43abeb537319b63ad151c2fb",
         "dkv_common.cuh": "bcd6734e6c5b4bd5fc941201972200f49e4eed4b73ae8e36152d81d14831054a",
-        "dkv_kernels.cuh": "1af05a5c3c6beb7a744278fb7fe797da5149d278f8177afc2dcb8418855110f2",
+        "dkv_kernels.cuh": "8b696d22cc7aad5a45af9c7632518d943f3eb86e086728ea9c67a90bc1b2ce06",
     },
 }
 L2_FLUSH_BYTES = 256 << 20
