@@ -658,37 +658,43 @@ def run_dkv(args, world, rank, local):
 
 def run_e2e(args, loop: Loop, dist):
     """The same step through the C ABI with inputs in pinned host memory:
-    every step copies the prompt K/V/Q and each decode step's K/V/q to the
-    device and reads each decode step's attention output back."""
+    every step copies its inputs (the prompt K/V/Q and every decode step's
+    K/V/q, staged back to back in one pinned buffer) to the device with one
+    copy, runs the path, and reads every decode step's attention output back
+    with one copy."""
     import torch
     dkv, dev, w = loop.dkv, loop.dev, loop.w
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    hk, hv, hq = pin(loop.inp["k"]), pin(loop.inp["v"]), pin(loop.inp["q_obs"])
-    hdk = [pin(d["k"]) for d in loop.dec]
-    hdv = [pin(d["v"]) for d in loop.dec]
-    hdq = [pin(d["q"]) for d in loop.dec]
-    R, Hq = w.n_requests, w.n_q_heads
-    hout = torch.empty((R, Hq, 128), dtype=torch.float32).pin_memory()
-    k_d = torch.empty(hk.shape, dtype=torch.float16, device=dev)
-    v_d = torch.empty_like(k_d)
-    q_d = torch.empty(hq.shape, dtype=torch.float16, device=dev)
-    dk = torch.empty(hdk[0].shape, dtype=torch.float16, device=dev)
-    dv = torch.empty_like(dk)
-    dq = torch.empty(hdq[0].shape, dtype=torch.float16, device=dev)
-    out = torch.empty((R, Hq, 128), dtype=torch.float32, device=dev)
     T, pool, slots = loop.T, loop.pool, loop.slots
+    R, Hq = w.n_requests, w.n_q_heads
+    parts = [loop.inp["k"], loop.inp["v"], loop.inp["q_obs"]]
+    for d in loop.dec:
+        parts += [d["k"], d["v"], d["q"]]
+    sizes = [a.size for a in parts]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    hin = torch.empty(int(offs[-1]), dtype=torch.float16).pin_memory()
+    hin_np = hin.numpy()
+    for a, o in zip(parts, offs[:-1]):
+        hin_np[o:o + a.size] = a.reshape(-1)
+    din = torch.empty(hin.shape, dtype=torch.float16, device=dev)
+    views = [din[int(o):int(o) + a.size].view(a.shape) for a, o in zip(parts, offs[:-1])]
+    k_d, v_d, q_d = views[:3]
+    dec = [views[3 + 3 * t: 6 + 3 * t] for t in range(T)]
+    out = torch.empty((T, R, Hq, 128), dtype=torch.float32, device=dev)
+    hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    st = torch.cuda.current_stream()
+    slots_np = np.asarray(slots, dtype=np.int32)
+    lens_np = np.asarray(loop.lens, dtype=np.int32)
 
     def step():
-        k_d.copy_(hk, non_blocking=True); v_d.copy_(hv, non_blocking=True); q_d.copy_(hq, non_blocking=True)
-        dkv.dkv_compact_step(pool, 0, dkv.DKV_PROMPT, slots, loop.lens, k_d, v_d, q_d)
+        din.copy_(hin, non_blocking=True)
+        dkv.dkv_compact_step(pool, 0, dkv.DKV_PROMPT, slots_np, lens_np, k_d, v_d, q_d, stream=st)
         for t in range(T):
-            dk.copy_(hdk[t], non_blocking=True); dv.copy_(hdv[t], non_blocking=True)
-            dq.copy_(hdq[t], non_blocking=True)
-            dkv.dkv_compact_step(pool, 0, dkv.DKV_DECODE, slots, None, dk, dv)
-            dkv.dkv_decode_attention(pool, 0, slots, dq, out, True)
-            hout.copy_(out, non_blocking=True)
-        for s in slots:
-            dkv.dkv_free_request(pool, s)
+            dk, dv, dq = dec[t]
+            dkv.dkv_compact_step(pool, 0, dkv.DKV_DECODE, slots_np, None, dk, dv, stream=st)
+            dkv.dkv_decode_attention(pool, 0, slots_np, dq, out[t], True, stream=st)
+        hout.copy_(out, non_blocking=True)
+        for s_ in slots:
+            dkv.dkv_free_request(pool, s_, stream=st)
         torch.cuda.synchronize()
 
     step()
@@ -700,13 +706,15 @@ def run_e2e(args, loop: Loop, dist):
     dt = reduce_max(dist, dt, dev)
     n = dist.get_world_size() if dist is not None else 1
     attn_bytes_step = sum(loop.bytes_per_attn)
-    h2d = (hk.numel() + hv.numel() + hq.numel()) * 2 + T * (hdk[0].numel() + hdv[0].numel() + hdq[0].numel()) * 2
-    d2h = T * hout.numel() * 4
+    h2d = int(hin.numel()) * 2
+    d2h = int(hout.numel()) * 4
     return {"value": round(n * attn_bytes_step / dt / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3, 2),
             "what": "decode-attention algorithmic bytes of a step / wall time of the whole step through the "
-                    "C ABI from pinned host buffers (host sync at the end of each step)"}
+                    "C ABI: one copy of the step's inputs from pinned host memory (prompt K/V/Q and every "
+                    "decode step's K/V/q), the path, one copy of every decode step's output back (host sync "
+                    "at the end of each step)"}
 
 
 # --------------------------------------------------- oracle (CPU baseline)
