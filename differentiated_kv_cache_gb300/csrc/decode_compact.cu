@@ -230,30 +230,35 @@ __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, con
                                                       const __half* __restrict__ vnew, SlotArgs sa) {
   pdl_launch_dependents();        // a decode-attention call may follow: it waits for this grid
   if (pv.noop()) return;
+  __shared__ TokStage st[3];      // [0], [1]: demoted sources of moves 0, 1; [2]: the new token
+  const int kvh = blockIdx.x, i = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The new token's hi codes do not depend on the plan: warp 1 quantizes
+  // them (from the caller's buffers) while the plan and allocation finish.
+  if (warp == 1) {
+    TokStage& s = st[2];
+    const __half* kp = knew + ((size_t)i * pv.hkv + kvh) * kD + 4 * lane;
+    const __half* vp = vnew + ((size_t)i * pv.hkv + kvh) * kD + 4 * lane;
+    float kx[4], vx[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) { kx[e] = __half2float(kp[e]); vx[e] = __half2float(vp[e]); }
+    warp_quantize(kx, 8, s.kc, &s.kmeta);
+    warp_quantize(vx, 4, s.vc, &s.vmeta);
+  }
   pdl_wait();                     // the plans and pages of k_decode_alloc
   if (pv.noop_after_wait()) return;
-  __shared__ TokStage st[2];
-  const int kvh = blockIdx.x, i = blockIdx.y;
   const int slot = sa.slots[i];
   const int unit = i * pv.hkv + kvh;
   const DecodePlan& p = plans[unit];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int* row = pv.row(layer, slot, kvh);
   const int n = pv.rq(layer, slot)[2];       // already advanced by k_decode_alloc
-  // read phase: warp m stages the source of move m
-  if (warp < p.n_moves) {
+  if (threadIdx.x == 0) { st[2].score = 0.0f; st[2].pos = n - 1; }
+  // read phase: warp m stages the source of move m when it is a demotion
+  if (warp < p.n_moves && p.mv[warp].src != kSrcNew) {
     const Move mv = p.mv[warp];
     TokStage& s = st[warp];
     float kx[4], vx[4];
-    if (mv.src == kSrcNew) {
-      const __half* kp = knew + ((size_t)i * pv.hkv + kvh) * kD + 4 * lane;
-      const __half* vp = vnew + ((size_t)i * pv.hkv + kvh) * kD + 4 * lane;
-#pragma unroll
-      for (int e = 0; e < 4; e++) { kx[e] = __half2float(kp[e]); vx[e] = __half2float(vp[e]); }
-      warp_quantize(kx, 8, s.kc, &s.kmeta);
-      warp_quantize(vx, 4, s.vc, &s.vmeta);
-      if (lane == 0) { s.score = 0.0f; s.pos = n - 1; }
-    } else {
+    {
       // demote: dequantize the hi slot's codes, quantize again at lo precision
       const uint8_t* pg = pv.page(row[mv.src_slot / pv.hi.t]);
       const int ip = mv.src_slot % pv.hi.t;
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, con
   // write phase: one warp, moves in order (value words shared between slots)
   for (int m = 0; m < p.n_moves; m++) {
     const Move mv = p.mv[m];
-    const TokStage& s = st[m];
+    const TokStage& s = st[mv.src == kSrcNew ? 2 : m];
     const bool hi = mv.dst_tier == kTierHi;
     const TierGeom& tg = hi ? pv.hi : pv.lo;
     const int e_page = hi ? mv.dst_slot / tg.t : pv.L - 1 - mv.dst_slot / tg.t;
