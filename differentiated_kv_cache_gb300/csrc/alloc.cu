@@ -201,17 +201,21 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
                                                                  SlotArgs sa) {
   pdl_launch_dependents();        // k_decode_apply may launch; it waits for this grid
   if (pv.noop()) return;
-  pdl_wait();                     // the plans of k_decode_plan
-  if (pv.noop_after_wait()) return;
+  extern __shared__ int s_list[];  // [2 n_units] the list entries from the start: the pages a grant can take
   __shared__ int s_warp[32];
   __shared__ int s_err, s_info;
   const int n_units = sa.n * pv.hkv;
   const int per = (n_units + blockDim.x - 1) / blockDim.x;
   const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
   if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
-  // the list counters, loaded with the plans (only this kernel moves them
-  // during a generation step)
+  // The list counters and the entries from the start (a head takes at most a
+  // hi and a lo page): only this kernel moves or reads them during a
+  // generation step, so they load while the plans finish.
   const unsigned long long start = pv.ctl->start, end = pv.ctl->end;
+  for (int x = threadIdx.x; x < 2 * n_units; x += blockDim.x)
+    s_list[x] = pv.list[(start + (unsigned long long)x) % pv.n_pages];
+  pdl_wait();                     // the plans of k_decode_plan
+  if (pv.noop_after_wait()) return;
   __syncthreads();
   int my_a = 0, my_f = 0;
   for (int u = u0; u < u1; u++) {
@@ -242,8 +246,8 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
     int* row = pv.row(layer, slot, kvh);
     // the page counts before the step, from the plan (new = old + new - freed)
     const int php0 = p.php - p.new_hp + p.free_hp, plp0 = p.plp - p.new_lp + p.free_lp;
-    if (p.new_hp) row[php0] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
-    if (p.new_lp) row[pv.L - 1 - plp0] = pv.list[(start + (unsigned long long)(a++)) % pv.n_pages];
+    if (p.new_hp) row[php0] = s_list[a++];
+    if (p.new_lp) row[pv.L - 1 - plp0] = s_list[a++];
     if (p.free_hp) {
       pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[php0 - 1];
       row[php0 - 1] = -1;
@@ -337,7 +341,9 @@ cudaError_t configure_alloc() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_prompt_plan_commit, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_free_request, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  e = cudaFuncSetAttribute(k_free_request, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_decode_alloc, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
 
 // A programmatic dependent of k_decode_plan. One CTA, a thread per head up to
@@ -347,6 +353,7 @@ cudaError_t launch_decode_alloc(Pool& P, int layer, const SlotArgs& sa, cudaStre
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(1);
   lc.blockDim = dim3(std::min(kCoordThreads, (n_units + 31) / 32 * 32));
+  lc.dynamicSmemBytes = 2 * (size_t)n_units * sizeof(int);   // the list window
   lc.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
