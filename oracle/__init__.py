@@ -24,7 +24,7 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-TIER_PRUNE, TIER_LO, TIER_HI = 0, 1, 2
+TIER_PRUNE, TIER_LO, TIER_HI, TIER_MID = 0, 1, 2, 3
 ERR = dict(OK=0, ARG=-1, STATE=-3, NO_PAGES=-4, TABLE_FULL=-5, CHECK=-7)
 
 
@@ -44,7 +44,8 @@ class _Config(C.Structure):
                                           "n_pages", "max_requests", "max_seq_len", "t_hi", "t_lo",
                                           "lo_enabled")] + \
                [("alpha_h", C.c_float), ("alpha_l", C.c_float)] + \
-               [(n, C.c_int32) for n in ("window", "grant_slack", "reclaim_in_decode")]
+               [(n, C.c_int32) for n in ("window", "grant_slack", "reclaim_in_decode", "mid_enabled")] + \
+               [("alpha_m", C.c_float), ("t_mid", C.c_int32)]
 
 
 def lib():
@@ -77,6 +78,8 @@ def lib():
             L.orc_prefill_rows.argtypes = [I, I, P, P, I64, P, P, I64, P, P]
             L.orc_prefill_rows.restype = None
             L.orc_thresholds.argtypes = [P]; L.orc_thresholds.restype = P
+            L.orc_set_mid_thresholds.argtypes = [P, I, P]; L.orc_set_mid_thresholds.restype = I
+            L.orc_mid_thresholds.argtypes = [P]; L.orc_mid_thresholds.restype = P
             _lib = L
     return _lib
 
@@ -164,13 +167,20 @@ class Pool:
                     max_seq_len=cfg["max_seq_len"], t_hi=cfg.get("tokens_per_hi_page", 0),
                     t_lo=cfg.get("tokens_per_lo_page", 0), lo_enabled=cfg["lo_enabled"],
                     alpha_h=cfg["alpha_h"], alpha_l=cfg["alpha_l"], window=cfg["recent_window"],
-                    grant_slack=cfg["prompt_grant_slack"], reclaim_in_decode=cfg["reclaim_in_decode"])
+                    grant_slack=cfg["prompt_grant_slack"], reclaim_in_decode=cfg["reclaim_in_decode"],
+                    mid_enabled=cfg.get("mid_enabled", 0), alpha_m=cfg.get("alpha_m", 0.0),
+                    t_mid=cfg.get("tokens_per_mid_page", 0))
+        self.mid = bool(cfg.get("mid_enabled", 0))
         self._h = lib().orc_pool_new(C.byref(c))
-        g = np.zeros(17, dtype=np.int32)
+        g = np.zeros(28, dtype=np.int32)
         lib().orc_geometry(self._h, _ptr(g))
         self.t_hi, self.t_lo, self.table_len = int(g[0]), int(g[1]), int(g[2])
         self.hi_off, self.lo_off = g[3:9].copy(), g[9:15].copy()
         self.hi_used, self.lo_used = int(g[15]), int(g[16])
+        # the third level (mid, K8V2) and the one-way part of the table rows
+        self.t_mid, self.mid_len = int(g[17]), int(g[18])
+        self.mid_off, self.mid_used = g[19:25].copy(), int(g[25])
+        self.row_len, self.cstride = int(g[26]), int(g[27])
 
     def __del__(self):
         if getattr(self, "_h", None):
@@ -200,15 +210,15 @@ class Pool:
     def table(self):
         c = self.cfg
         n = c["n_layers"] * c["max_requests"] * c["n_kv_heads"]
-        return self._view("orc_table", np.int32, n * self.table_len).reshape(
-            c["n_layers"], c["max_requests"], c["n_kv_heads"], self.table_len)
+        return self._view("orc_table", np.int32, n * self.row_len).reshape(
+            c["n_layers"], c["max_requests"], c["n_kv_heads"], self.row_len)
 
     @property
     def head_counts(self):
         c = self.cfg
         n = c["n_layers"] * c["max_requests"] * c["n_kv_heads"]
-        return self._view("orc_head_counts", np.int32, n * 4).reshape(
-            c["n_layers"], c["max_requests"], c["n_kv_heads"], 4)
+        return self._view("orc_head_counts", np.int32, n * self.cstride).reshape(
+            c["n_layers"], c["max_requests"], c["n_kv_heads"], self.cstride)
 
     @property
     def req_state(self):
@@ -242,10 +252,11 @@ class Pool:
 
     def unit_attention(self, layer, slot, kvh, q_group):
         """fp64 attention of one KV head (q_group fp16 [G, 128]); returns
-        (out [G,128] fp64, pmax over stored tokens (hi slots then lo slots))."""
+        (out [G,128] fp64, pmax over stored tokens (hi slots, mid slots, then
+        lo slots))."""
         qu = _u16(q_group)
         cnt = self.head_counts[layer, slot, kvh]
-        n = int(cnt[0] + cnt[1])
+        n = int(cnt[0] + cnt[1] + (cnt[4] if self.mid else 0))
         out = np.zeros(qu.shape, np.float64)
         pm = np.zeros(max(n, 1), np.float64)
         lib().orc_unit_attention(self._h, layer, slot, kvh, _ptr(qu), _ptr(out), _ptr(pm))
@@ -261,6 +272,19 @@ class Pool:
         assert ah.size == al.size == self.cfg["n_kv_heads"]
         return lib().orc_set_thresholds(self._h, int(layer), _ptr(ah), _ptr(al))
 
+    def set_mid_thresholds(self, layer, alpha_m):
+        """Per-head thresholds of the mid level of one layer (n_kv_heads floats)."""
+        am = np.ascontiguousarray(alpha_m, dtype=np.float32)
+        assert am.size == self.cfg["n_kv_heads"]
+        return lib().orc_set_mid_thresholds(self._h, int(layer), _ptr(am))
+
+    @property
+    def mid_thresholds(self):
+        """Live view [layer][kvh] of alpha_m."""
+        c = self.cfg
+        return self._view("orc_mid_thresholds", np.float32, c["n_layers"] * c["n_kv_heads"]).reshape(
+            c["n_layers"], c["n_kv_heads"])
+
     @property
     def thresholds(self):
         """Live view [layer][kvh][alpha_h, alpha_l]."""
@@ -272,4 +296,4 @@ class Pool:
         return dict(pages=self.pages.copy(), free_list=self.free_list.copy(),
                     pointers=self.pointers.copy(), table=self.table.copy(),
                     head_counts=self.head_counts.copy(), req_state=self.req_state.copy(),
-                    thresholds=self.thresholds.copy())
+                    thresholds=self.thresholds.copy(), mid_thresholds=self.mid_thresholds.copy())

@@ -36,6 +36,7 @@
 #define TIER_PRUNE 0
 #define TIER_LO 1
 #define TIER_HI 2
+#define TIER_MID 3   /* the optional third precision level, between hi and lo */
 
 /* ------------------------------------------------------------------ */
 /* IEEE binary16 <-> binary32, written from the IEEE 754 definition.   */
@@ -115,6 +116,9 @@ typedef struct {
   int32_t lo_enabled;
   float alpha_h, alpha_l;
   int32_t window, grant_slack, reclaim_in_decode;
+  int32_t mid_enabled;         /* 1: a third level K8V2 between hi and lo */
+  float alpha_m;               /* its threshold alpha_m / N */
+  int32_t t_mid;               /* 0 = derive from page_bytes */
 } orc_config;
 
 typedef struct {
@@ -126,15 +130,20 @@ typedef struct {
 
 typedef struct {
   orc_config c;
-  tier_geom tg[3];             /* indexed by TIER_LO / TIER_HI */
-  int table_len;
+  tier_geom tg[4];             /* indexed by TIER_LO / TIER_HI / TIER_MID */
+  int table_len;               /* entries of the two-way part of a row (hi | lo) */
+  int mid_len;                 /* entries of the one-way part (mid pages), 0 without mid */
+  int row_len;                 /* table_len + mid_len */
+  int cstride;                 /* ints of per-head counters: 4, or 8 with mid */
   uint8_t* pages;
   int32_t* list;
   int64_t ptr[2];              /* start, end */
-  int32_t* table;              /* [layer][slot][kvh][table_len] */
-  int32_t* counts;             /* [layer][slot][kvh][4] hi tok, lo tok, hi pages, lo pages */
+  int32_t* table;              /* [layer][slot][kvh][row_len] */
+  int32_t* counts;             /* [layer][slot][kvh][cstride] hi tok, lo tok, hi pages, lo pages
+                                  (then mid tok, mid pages, 0, 0 with mid) */
   int32_t* req;                /* [layer][slot][4] active, N0, N, updates */
   float* alpha;                /* [layer][kvh][2] alpha_h, alpha_l of each head */
+  float* alpha_mid;            /* [layer][kvh] alpha_m of each head */
 } orc_pool;
 
 static int round16(int x) { return (x + 15) & ~15; }
@@ -160,10 +169,10 @@ static int fit_tokens(tier_geom* g, int page_bytes) {
 }
 
 static int32_t* trow(orc_pool* p, int layer, int slot, int kvh) {
-  return p->table + (((int64_t)layer * p->c.max_requests + slot) * p->c.n_kv_heads + kvh) * p->table_len;
+  return p->table + (((int64_t)layer * p->c.max_requests + slot) * p->c.n_kv_heads + kvh) * p->row_len;
 }
 static int32_t* hcnt(orc_pool* p, int layer, int slot, int kvh) {
-  return p->counts + (((int64_t)layer * p->c.max_requests + slot) * p->c.n_kv_heads + kvh) * 4;
+  return p->counts + (((int64_t)layer * p->c.max_requests + slot) * p->c.n_kv_heads + kvh) * p->cstride;
 }
 static int32_t* rstate(orc_pool* p, int layer, int slot) {
   return p->req + ((int64_t)layer * p->c.max_requests + slot) * 4;
@@ -175,22 +184,31 @@ orc_pool* orc_pool_new(const orc_config* c) {
   p->c = *c;
   p->tg[TIER_HI].kbits = 8; p->tg[TIER_HI].vbits = 4; p->tg[TIER_HI].g = 2;
   p->tg[TIER_LO].kbits = 4; p->tg[TIER_LO].vbits = 2; p->tg[TIER_LO].g = 4;
+  p->tg[TIER_MID].kbits = 8; p->tg[TIER_MID].vbits = 2; p->tg[TIER_MID].g = 4;
   int th = c->t_hi ? c->t_hi : fit_tokens(&p->tg[TIER_HI], c->page_bytes);
   int tl = c->t_lo ? c->t_lo : fit_tokens(&p->tg[TIER_LO], c->page_bytes);
+  int tm = c->t_mid ? c->t_mid : fit_tokens(&p->tg[TIER_MID], c->page_bytes);
   layout(&p->tg[TIER_HI], th);
   layout(&p->tg[TIER_LO], tl);
+  layout(&p->tg[TIER_MID], tm);
   /* Bidirectional page table entry length: max sequence length over tokens per
    * hi page, plus one page for a hi/lo split whose two partial pages exceed it. */
   p->table_len = (c->max_seq_len + th - 1) / th + 1;
+  /* With a third level the row composes the two-way table with a one-way
+   * table of mid pages (Memory management, generation workflow: further
+   * precision levels by combining one-way or two-way page tables). */
+  p->mid_len = c->mid_enabled ? (c->max_seq_len + tm - 1) / tm + 1 : 0;
+  p->row_len = p->table_len + p->mid_len;
+  p->cstride = c->mid_enabled ? 8 : 4;
   p->pages = (uint8_t*)calloc((size_t)c->n_pages, (size_t)c->page_bytes);
   p->list = (int32_t*)malloc(sizeof(int32_t) * (size_t)c->n_pages);
   for (int i = 0; i < c->n_pages; i++) p->list[i] = i;
   p->ptr[0] = 0;
   p->ptr[1] = c->n_pages;
   size_t heads = (size_t)c->n_layers * c->max_requests * c->n_kv_heads;
-  p->table = (int32_t*)malloc(sizeof(int32_t) * heads * p->table_len);
-  for (size_t i = 0; i < heads * p->table_len; i++) p->table[i] = -1;
-  p->counts = (int32_t*)calloc(heads * 4, sizeof(int32_t));
+  p->table = (int32_t*)malloc(sizeof(int32_t) * heads * p->row_len);
+  for (size_t i = 0; i < heads * p->row_len; i++) p->table[i] = -1;
+  p->counts = (int32_t*)calloc(heads * p->cstride, sizeof(int32_t));
   p->req = (int32_t*)calloc((size_t)c->n_layers * c->max_requests * 4, sizeof(int32_t));
   /* every head starts with the configuration's thresholds */
   p->alpha = (float*)malloc(sizeof(float) * 2 * (size_t)c->n_layers * c->n_kv_heads);
@@ -198,6 +216,8 @@ orc_pool* orc_pool_new(const orc_config* c) {
     p->alpha[2 * x] = c->alpha_h;
     p->alpha[2 * x + 1] = c->alpha_l;
   }
+  p->alpha_mid = (float*)malloc(sizeof(float) * (size_t)c->n_layers * c->n_kv_heads);
+  for (int x = 0; x < c->n_layers * c->n_kv_heads; x++) p->alpha_mid[x] = c->alpha_m;
   return p;
 }
 
@@ -218,13 +238,26 @@ int orc_set_thresholds(orc_pool* p, int layer, const float* ah, const float* al)
 
 float* orc_thresholds(orc_pool* p) { return p->alpha; }
 
+/* The mid level's threshold of each head of `layer` (am[h]/N). */
+int orc_set_mid_thresholds(orc_pool* p, int layer, const float* am) {
+  if (layer < 0 || layer >= p->c.n_layers || !am || !p->c.mid_enabled) return ORC_ERR_ARG;
+  for (int h = 0; h < p->c.n_kv_heads; h++)
+    if (isnan(am[h])) return ORC_ERR_ARG;
+  for (int h = 0; h < p->c.n_kv_heads; h++) p->alpha_mid[(size_t)layer * p->c.n_kv_heads + h] = am[h];
+  return ORC_OK;
+}
+
+float* orc_mid_thresholds(orc_pool* p) { return p->alpha_mid; }
+
 void orc_pool_free(orc_pool* p) {
   if (!p) return;
   free(p->pages); free(p->list); free(p->table); free(p->counts); free(p->req); free(p->alpha);
+  free(p->alpha_mid);
   free(p);
 }
 
-/* geometry: t_hi, t_lo, table_len, hi off[6], lo off[6], hi used, lo used */
+/* geometry: t_hi, t_lo, table_len, hi off[6], lo off[6], hi used, lo used,
+ * t_mid, mid_len, mid off[6], mid used, row_len, cstride */
 void orc_geometry(const orc_pool* p, int32_t* out) {
   out[0] = p->tg[TIER_HI].t;
   out[1] = p->tg[TIER_LO].t;
@@ -233,6 +266,12 @@ void orc_geometry(const orc_pool* p, int32_t* out) {
   for (int i = 0; i < 6; i++) out[9 + i] = p->tg[TIER_LO].off[i];
   out[15] = p->tg[TIER_HI].used;
   out[16] = p->tg[TIER_LO].used;
+  out[17] = p->tg[TIER_MID].t;
+  out[18] = p->mid_len;
+  for (int i = 0; i < 6; i++) out[19 + i] = p->tg[TIER_MID].off[i];
+  out[25] = p->tg[TIER_MID].used;
+  out[26] = p->row_len;
+  out[27] = p->cstride;
 }
 
 uint8_t* orc_pages(orc_pool* p) { return p->pages; }
@@ -329,22 +368,24 @@ static void half_vec(const uint16_t* h, float* out) {
   for (int i = 0; i < D; i++) out[i] = orc_half_to_float(h[i]);
 }
 
-/* hi -> lo re-quantization of a stored token: dequantize, quantize again */
-static void demote(const token_rec* hi, const tier_geom* lo, token_rec* out) {
+/* Re-quantization of a stored token to another level (hi -> lo, hi -> mid,
+ * mid -> lo): dequantize its codes, quantize the values again */
+static void requant(const token_rec* src, const tier_geom* dst, token_rec* out) {
   float k[D], v[D];
   for (int f = 0; f < D; f++) {
-    k[f] = orc_dequant(hi->ks, hi->kz, hi->kc[f]);
-    v[f] = orc_dequant(hi->vs, hi->vz, hi->vc[f]);
+    k[f] = orc_dequant(src->ks, src->kz, src->kc[f]);
+    v[f] = orc_dequant(src->vs, src->vz, src->vc[f]);
   }
-  make_token(k, v, lo, hi->score, hi->pos, out);
+  make_token(k, v, dst, src->score, src->pos, out);
 }
 
-/* page holding slot s of a tier (through the bidirectional table row) and
- * the slot's index inside that page */
+/* page holding slot s of a tier (through the head's table row: hi pages from
+ * the left of the two-way part, lo pages from its right, mid pages in the
+ * one-way part after it) and the slot's index inside that page */
 static uint8_t* slot_loc(orc_pool* p, const int32_t* row, int tier, int s, int* in_page) {
   const int t = p->tg[tier].t;
   *in_page = s % t;
-  int e = tier == TIER_HI ? s / t : p->table_len - 1 - s / t;
+  int e = tier == TIER_HI ? s / t : tier == TIER_LO ? p->table_len - 1 - s / t : p->table_len + s / t;
   return page_ptr(p, row[e]);
 }
 
@@ -364,15 +405,23 @@ static int score_count(int j, int n0, int updates) {
 static float importance(float score, int count) { return score / (float)count; }
 
 /* three-way split against alpha_h/N and alpha_l/N (the head's thresholds);
- * with the lo tier disabled a token that would be lo is kept at hi precision */
-static int classify(const orc_config* c, const float* alpha, float imp, int n) {
+ * with the lo tier disabled a token that would be lo is kept at hi precision;
+ * with the mid level a token at or above alpha_m/N that is not hi is mid.
+ * alpha: the head's {alpha_h, alpha_l}; am: its alpha_m. */
+static int classify(const orc_config* c, const float* alpha, float am, float imp, int n) {
   float th_h = alpha[0] / (float)n, th_l = alpha[1] / (float)n;
   if (c->lo_enabled) {
     if (imp > th_h) return TIER_HI;
+    if (c->mid_enabled && imp >= am / (float)n) return TIER_MID;
     if (imp >= th_l) return TIER_LO;
     return TIER_PRUNE;
   }
   return imp >= th_l ? TIER_HI : TIER_PRUNE;
+}
+
+/* precision order of the levels: prune < lo < mid < hi */
+static int tier_rank(int tier) {
+  return tier == TIER_HI ? 3 : tier == TIER_MID ? 2 : tier == TIER_LO ? 1 : 0;
 }
 
 /* Prompt scores of one KV head, fp64. Compaction policy, prompt phase: the
@@ -499,7 +548,7 @@ int orc_prompt_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
                     const float* scores_in, float* scores_out) {
   const orc_config* c = &p->c;
   const int H = c->n_kv_heads, G = c->group_size, Hq = H * G;
-  const int th = p->tg[TIER_HI].t, tl = p->tg[TIER_LO].t;
+  const int th = p->tg[TIER_HI].t, tl = p->tg[TIER_LO].t, tm = p->tg[TIER_MID].t;
   if (layer < 0 || layer >= c->n_layers || n_req < 1 || n_req > c->max_requests) return ORC_ERR_ARG;
   for (int i = 0; i < n_req; i++) {
     if (slots[i] < 0 || slots[i] >= c->max_requests) return ORC_ERR_ARG;
@@ -528,6 +577,7 @@ int orc_prompt_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
   uint8_t* tier = (uint8_t*)malloc((size_t)tok0[n_req] * H);
   int* nhi = (int*)calloc(nh, sizeof(int));
   int* nlo = (int*)calloc(nh, sizeof(int));
+  int* nmid = (int*)calloc(nh, sizeof(int));
   int status = ORC_OK;
   for (int i = 0; i < n_req && status == ORC_OK; i++) {
     const int n0 = lens[i];
@@ -539,24 +589,28 @@ int orc_prompt_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
         orc_unit_scores(n0, G, k + (tok0[i] * H + h) * D, (int64_t)H * D,
                         q_obs + ((int64_t)i * OBS * Hq + (int64_t)h * G) * D, (int64_t)Hq * D, D, S);
       }
+      const size_t hx = (size_t)layer * H + h;
       for (int j = 0; j < n0; j++) {
         int64_t t = (tok0[i] + j) * H + h;
         float s32 = (float)S[j];
         S32[t] = s32;
         int tr;
         if (j >= n0 - c->window) tr = TIER_HI;            /* recent window */
-        else tr = classify(c, p->alpha + 2 * ((size_t)layer * H + h), importance(s32, score_count(j, n0, 0)), n0);
+        else tr = classify(c, p->alpha + 2 * hx, p->alpha_mid[hx], importance(s32, score_count(j, n0, 0)), n0);
         tier[t] = (uint8_t)tr;
         if (tr == TIER_HI) nhi[i * H + h]++;
         else if (tr == TIER_LO) nlo[i * H + h]++;
+        else if (tr == TIER_MID) nmid[i * H + h]++;
       }
       int php = (nhi[i * H + h] + th - 1) / th, plp = (nlo[i * H + h] + tl - 1) / tl;
-      if (php + plp > grant[i * H + h] || php + plp > p->table_len) status = ORC_ERR_TABLE_FULL;
+      int pmp = (nmid[i * H + h] + tm - 1) / tm;
+      if (php + pmp + plp > grant[i * H + h] || php + plp > p->table_len || pmp > p->mid_len)
+        status = ORC_ERR_TABLE_FULL;
     }
     free(S);
   }
   if (status != ORC_OK) {
-    free(tok0); free(grant); free(S32); free(tier); free(nhi); free(nlo);
+    free(tok0); free(grant); free(S32); free(tier); free(nhi); free(nlo); free(nmid);
     return status;
   }
 
@@ -569,11 +623,13 @@ int orc_prompt_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
     off += grant[hd];
   }
 
-  /* pack: hi tokens fill the grant from the left, lo tokens from the right */
+  /* pack: hi tokens fill the grant from the left, lo tokens from the right,
+   * mid tokens (third level) the grant pages after the hi ones */
   for (int i = 0; i < n_req; i++) {
     const int n0 = lens[i];
     for (int h = 0; h < H; h++) {
-      int hd = i * H + h, rh = 0, rl = 0;
+      int hd = i * H + h, rh = 0, rl = 0, rm = 0;
+      const int php = (nhi[hd] + th - 1) / th;
       for (int j = 0; j < n0; j++) {
         int64_t t = (tok0[i] + j) * H + h;
         if (tier[t] == TIER_PRUNE) continue;
@@ -581,36 +637,41 @@ int orc_prompt_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
         half_vec(k + t * D, kx);
         half_vec(v + t * D, vx);
         token_rec r;
+        make_token(kx, vx, &p->tg[tier[t]], S32[t], j, &r);
         if (tier[t] == TIER_HI) {
-          make_token(kx, vx, &p->tg[TIER_HI], S32[t], j, &r);
           put_token(page_ptr(p, gp[hd][rh / th]), &p->tg[TIER_HI], rh % th, &r);
           rh++;
-        } else {
-          make_token(kx, vx, &p->tg[TIER_LO], S32[t], j, &r);
+        } else if (tier[t] == TIER_LO) {
           put_token(page_ptr(p, gp[hd][grant[hd] - 1 - rl / tl]), &p->tg[TIER_LO], rl % tl, &r);
           rl++;
+        } else {
+          put_token(page_ptr(p, gp[hd][php + rm / tm]), &p->tg[TIER_MID], rm % tm, &r);
+          rm++;
         }
       }
     }
   }
 
   /* coordination 2: exclusive prefix sum of unused middle pages at the list end;
-   * the bidirectional table records hi pages from the left, lo from the right */
+   * the bidirectional table records hi pages from the left, lo from the right,
+   * and its one-way part the mid pages */
   int64_t roff = 0;
   for (int i = 0; i < n_req; i++)
     for (int h = 0; h < H; h++) {
       int hd = i * H + h;
-      int php = (nhi[hd] + th - 1) / th, plp = (nlo[hd] + tl - 1) / tl;
-      for (int x = php; x < grant[hd] - plp; x++) {
+      int php = (nhi[hd] + th - 1) / th, plp = (nlo[hd] + tl - 1) / tl, pmp = (nmid[hd] + tm - 1) / tm;
+      for (int x = php + pmp; x < grant[hd] - plp; x++) {
         p->list[(p->ptr[1] + roff) % c->n_pages] = gp[hd][x];
         roff++;
       }
       int32_t* row = trow(p, layer, slots[i], h);
-      for (int e = 0; e < p->table_len; e++) row[e] = -1;
+      for (int e = 0; e < p->row_len; e++) row[e] = -1;
       for (int x = 0; x < php; x++) row[x] = gp[hd][x];
       for (int x = 0; x < plp; x++) row[p->table_len - 1 - x] = gp[hd][grant[hd] - 1 - x];
+      for (int x = 0; x < pmp; x++) row[p->table_len + x] = gp[hd][php + x];
       int32_t* cn = hcnt(p, layer, slots[i], h);
       cn[0] = nhi[hd]; cn[1] = nlo[hd]; cn[2] = php; cn[3] = plp;
+      if (c->mid_enabled) { cn[4] = nmid[hd]; cn[5] = pmp; }
     }
   p->ptr[0] += total;
   p->ptr[1] += roff;
@@ -620,7 +681,7 @@ int orc_prompt_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
   }
   if (scores_out) memcpy(scores_out, S32, sizeof(float) * (size_t)tok0[n_req] * H);
   for (int hd = 0; hd < nh; hd++) free(gp[hd]);
-  free(gp); free(tok0); free(grant); free(S32); free(tier); free(nhi); free(nlo);
+  free(gp); free(tok0); free(grant); free(S32); free(tier); free(nhi); free(nlo); free(nmid);
   return ORC_OK;
 }
 
@@ -629,15 +690,17 @@ int orc_prompt_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
 /* flow) and Memory management (generation workflow).                 */
 /* ------------------------------------------------------------------ */
 
-/* A slot's content after the step, described by where it comes from. */
-enum { SRC_HI = 0, SRC_LO = 1, SRC_NEW = 2, SRC_DEMOTED = 3 };
-typedef struct { int kind, slot; float imp; int pos; } src_t;
+/* A slot's content after the step, described by where it comes from: a
+ * token stored before the step (its tier and slot then), or the new token. */
+enum { SRC_STORED = 0, SRC_NEW = 1 };
+typedef struct { int kind, tier, slot; float imp; int pos; } src_t;
+
+/* the levels a head can hold, in the order of their page allocations */
+static const int k_tiers[3] = {TIER_HI, TIER_LO, TIER_MID};
 
 typedef struct {
-  src_t* hi; int nh, cap_h;
-  src_t* lo; int nl, cap_l;
-  int new_hp, new_lp, free_hp, free_lp;    /* page changes of this head */
-  int php, plp;                            /* page counts after the step */
+  src_t* a[4]; int n[4];                   /* slots of each tier after the step */
+  int np[4], newp[4], freep[4];            /* page counts after, new and freed pages */
 } head_plan;
 
 static void remove_at(src_t* a, int* n, int x) {   /* swap-with-last */
@@ -657,11 +720,19 @@ static int argmin_imp(const src_t* a, int n, int limit) {
   return best;
 }
 
+/* ints of per-tier counters in a head's counter row: tokens, pages */
+static int cnt_tok(int tier) { return tier == TIER_HI ? 0 : tier == TIER_LO ? 1 : 4; }
+static int cnt_pg(int tier) { return tier == TIER_HI ? 2 : tier == TIER_LO ? 3 : 5; }
+/* table entry of page k of a tier */
+static int tab_entry(const orc_pool* p, int tier, int k) {
+  return tier == TIER_HI ? k : tier == TIER_LO ? p->table_len - 1 - k : p->table_len + k;
+}
+
 int orc_decode_step(orc_pool* p, int layer, int n_req, const int32_t* slots, const uint16_t* k,
                     const uint16_t* v) {
   const orc_config* c = &p->c;
-  const int H = c->n_kv_heads;
-  const int th = p->tg[TIER_HI].t, tl = p->tg[TIER_LO].t, L = p->table_len;
+  const int H = c->n_kv_heads, L = p->table_len;
+  const int ntiers = c->mid_enabled ? 3 : 2;
   if (layer < 0 || layer >= c->n_layers || n_req < 1 || n_req > c->max_requests) return ORC_ERR_ARG;
   /* generation-phase compaction needs a recent window of at least one token,
    * so that the newest token is never its own candidate */
@@ -681,85 +752,89 @@ int orc_decode_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
     int32_t* rs = rstate(p, layer, slots[i]);
     const int n0 = rs[1], n = rs[2] + 1, upd = rs[3];
     for (int h = 0; h < H; h++) {
-      const float* alpha = p->alpha + 2 * ((size_t)layer * H + h);
-      const float th_h = alpha[0] / (float)n, th_l = alpha[1] / (float)n;
+      const size_t hx = (size_t)layer * H + h;
+      const float* alpha = p->alpha + 2 * hx;
+      const float am = p->alpha_mid[hx];
       head_plan* q = &pl[i * H + h];
       int32_t* cn = hcnt(p, layer, slots[i], h);
       int32_t* row = trow(p, layer, slots[i], h);
-      q->cap_h = cn[0] + 2; q->cap_l = cn[1] + 2;
-      q->hi = (src_t*)malloc(sizeof(src_t) * q->cap_h);
-      q->lo = (src_t*)malloc(sizeof(src_t) * q->cap_l);
-      q->nh = cn[0]; q->nl = cn[1];
-      for (int tr = 0; tr < 2; tr++) {
-        int tier = tr ? TIER_LO : TIER_HI, cnt = tr ? cn[1] : cn[0];
-        src_t* a = tr ? q->lo : q->hi;
+      for (int x = 0; x < ntiers; x++) {
+        const int tier = k_tiers[x], cnt = cn[cnt_tok(tier)];
+        const tier_geom* g = &p->tg[tier];
+        src_t* a = q->a[tier] = (src_t*)malloc(sizeof(src_t) * (cnt + 2));
+        q->n[tier] = cnt;
         for (int s = 0; s < cnt; s++) {
-          const tier_geom* g = &p->tg[tier];
           int ip;
           const uint8_t* pg = slot_loc(p, row, tier, s, &ip);
           float sc; int32_t pos;
           memcpy(&sc, pg + g->off[4] + 4 * ip, 4);
           memcpy(&pos, pg + g->off[5] + 4 * ip, 4);
-          a[s].kind = tr ? SRC_LO : SRC_HI; a[s].slot = s; a[s].pos = pos;
+          a[s].kind = SRC_STORED; a[s].tier = tier; a[s].slot = s; a[s].pos = pos;
           a[s].imp = importance(sc, score_count(pos, n0, upd));
         }
       }
+      src_t* hi = q->a[TIER_HI];
       /* (1) the newest token enters the recent window at high precision */
-      q->hi[q->nh].kind = SRC_NEW; q->hi[q->nh].slot = -1; q->hi[q->nh].pos = n - 1;
-      q->hi[q->nh].imp = 0.0f;
-      q->nh++;
+      src_t nw = {SRC_NEW, TIER_HI, -1, 0.0f, n - 1};
+      hi[q->n[TIER_HI]++] = nw;
       /* (2) the window's oldest token t_c leaves it and is classified */
       const int pc = n - c->window - 1;
       if (pc >= 0) {
         int xc = -1;
-        for (int x = 0; x < q->nh; x++) if (q->hi[x].pos == pc) { xc = x; break; }
+        for (int x = 0; x < q->n[TIER_HI]; x++) if (hi[x].pos == pc) { xc = x; break; }
         if (xc < 0) { status = ORC_ERR_CHECK; }
         else {
-          int tc = classify(c, alpha, q->hi[xc].imp, n);
+          const int tc = classify(c, alpha, am, hi[xc].imp, n);
+          int vt;                                   /* tier whose victim is considered */
           if (tc == TIER_HI) {
-            /* t_c stays hi; the least important hi token outside the window is the victim */
-            int xv = argmin_imp(q->hi, q->nh, n - c->window);
-            float iv = q->hi[xv].imp;
-            int keep = c->lo_enabled ? (iv > th_h) : (iv >= th_l);
-            if (!keep) {
-              src_t t = q->hi[xv];
-              remove_at(q->hi, &q->nh, xv);
-              if (c->lo_enabled && iv >= th_l) {               /* re-quantize to lo */
-                src_t d = t; d.kind = SRC_DEMOTED;
-                q->lo[q->nl++] = d;
-              }
+            vt = TIER_HI;                           /* t_c stays hi */
+          } else if (tc == TIER_PRUNE) {
+            vt = -1;
+            remove_at(hi, &q->n[TIER_HI], xc);
+          } else {                                  /* t_c moves to its lower level */
+            src_t t = hi[xc];
+            remove_at(hi, &q->n[TIER_HI], xc);
+            q->a[tc][q->n[tc]++] = t;
+            vt = tc;
+          }
+          /* (3) the victim: the least important token of the level t_c ended
+           * in (hi: outside the window; t_c itself is eligible), kept if it
+           * still classifies at that level or above, else moved to the level
+           * it classifies at, or pruned */
+          if (vt >= 0) {
+            src_t* a = q->a[vt];
+            const int xv = argmin_imp(a, q->n[vt], vt == TIER_HI ? n - c->window : 0x7fffffff);
+            const int cv = classify(c, alpha, am, a[xv].imp, n);
+            if (tier_rank(cv) < tier_rank(vt)) {
+              src_t t = a[xv];
+              remove_at(a, &q->n[vt], xv);
+              if (cv != TIER_PRUNE) q->a[cv][q->n[cv]++] = t;
             }
-          } else if (tc == TIER_LO) {
-            src_t t = q->hi[xc];
-            remove_at(q->hi, &q->nh, xc);
-            src_t d = t; d.kind = SRC_DEMOTED;
-            q->lo[q->nl++] = d;
-            /* the least important lo token is the victim; pruned below alpha_l/N */
-            int xv = argmin_imp(q->lo, q->nl, 0x7fffffff);
-            if (q->lo[xv].imp < th_l) remove_at(q->lo, &q->nl, xv);
-          } else {
-            remove_at(q->hi, &q->nh, xc);
           }
         }
       }
       /* page need of the step, from the net change of each tier */
-      int hp_need = (q->nh + th - 1) / th, lp_need = (q->nl + tl - 1) / tl;
-      q->php = cn[2]; q->plp = cn[3];
-      if (hp_need > q->php) { q->new_hp = hp_need - q->php; q->php = hp_need; }
-      else if (c->reclaim_in_decode && hp_need < q->php) { q->free_hp = q->php - hp_need; q->php = hp_need; }
-      if (lp_need > q->plp) { q->new_lp = lp_need - q->plp; q->plp = lp_need; }
-      else if (c->reclaim_in_decode && lp_need < q->plp) { q->free_lp = q->plp - lp_need; q->plp = lp_need; }
-      if (q->php + q->plp > L && status == ORC_OK) status = ORC_ERR_TABLE_FULL;
-      need += q->new_hp + q->new_lp;
+      for (int x = 0; x < ntiers; x++) {
+        const int tier = k_tiers[x], t = p->tg[tier].t;
+        const int pneed = (q->n[tier] + t - 1) / t, p0 = cn[cnt_pg(tier)];
+        q->np[tier] = p0;
+        if (pneed > p0) { q->newp[tier] = pneed - p0; q->np[tier] = pneed; }
+        else if (c->reclaim_in_decode && pneed < p0) { q->freep[tier] = p0 - pneed; q->np[tier] = pneed; }
+        need += q->newp[tier];
+      }
+      if (status == ORC_OK &&
+          (q->np[TIER_HI] + q->np[TIER_LO] > L || (c->mid_enabled && q->np[TIER_MID] > p->mid_len)))
+        status = ORC_ERR_TABLE_FULL;
     }
   }
   if (status == ORC_OK && need > p->ptr[1] - p->ptr[0]) status = ORC_ERR_NO_PAGES;
   if (status != ORC_OK) {
-    for (int hd = 0; hd < nh; hd++) { free(pl[hd].hi); free(pl[hd].lo); }
+    for (int hd = 0; hd < nh; hd++) for (int x = 0; x < ntiers; x++) free(pl[hd].a[k_tiers[x]]);
     free(pl);
     return status;
   }
-  /* commit: new pages by one prefix sum at the list start (per head hi then lo) */
+  /* commit: new pages by one prefix sum at the list start (per head hi, lo,
+   * then mid), emptied tail pages by one at the list end (same order) */
   int64_t aoff = 0, roff = 0;
   for (int i = 0; i < n_req; i++) {
     int32_t* rs = rstate(p, layer, slots[i]);
@@ -769,73 +844,63 @@ int orc_decode_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
       int32_t* cn = hcnt(p, layer, slots[i], h);
       int32_t* row = trow(p, layer, slots[i], h);
       /* read every source record from the state before the step */
-      token_rec* hi_new = (token_rec*)malloc(sizeof(token_rec) * (q->nh + 1));
-      token_rec* lo_new = (token_rec*)malloc(sizeof(token_rec) * (q->nl + 1));
-      int* hi_dirty = (int*)calloc(q->nh + 1, sizeof(int));
-      int* lo_dirty = (int*)calloc(q->nl + 1, sizeof(int));
-      for (int x = 0; x < q->nh; x++) {
-        src_t s = q->hi[x];
-        if (s.kind == SRC_HI && s.slot == x) continue;      /* unchanged */
-        hi_dirty[x] = 1;
-        if (s.kind == SRC_NEW) {
-          float kx[D], vx[D];
-          half_vec(k + ((int64_t)i * H + h) * D, kx);
-          half_vec(v + ((int64_t)i * H + h) * D, vx);
-          make_token(kx, vx, &p->tg[TIER_HI], 0.0f, n - 1, &hi_new[x]);
-        } else {
-          int ip;
-          const uint8_t* pg = slot_loc(p, row, TIER_HI, s.slot, &ip);
-          get_token(pg, &p->tg[TIER_HI], ip, &hi_new[x]);
-        }
-      }
-      for (int x = 0; x < q->nl; x++) {
-        src_t s = q->lo[x];
-        if (s.kind == SRC_LO && s.slot == x) continue;
-        lo_dirty[x] = 1;
-        int ip;
-        if (s.kind == SRC_DEMOTED) {
-          token_rec t;
-          const uint8_t* pg = slot_loc(p, row, TIER_HI, s.slot, &ip);
-          get_token(pg, &p->tg[TIER_HI], ip, &t);
-          demote(&t, &p->tg[TIER_LO], &lo_new[x]);
-        } else {
-          const uint8_t* pg = slot_loc(p, row, TIER_LO, s.slot, &ip);
-          get_token(pg, &p->tg[TIER_LO], ip, &lo_new[x]);
+      token_rec* recs[4] = {0, 0, 0, 0};
+      int* dirty[4] = {0, 0, 0, 0};
+      for (int y = 0; y < ntiers; y++) {
+        const int tier = k_tiers[y];
+        recs[tier] = (token_rec*)malloc(sizeof(token_rec) * (q->n[tier] + 1));
+        dirty[tier] = (int*)calloc(q->n[tier] + 1, sizeof(int));
+        for (int x = 0; x < q->n[tier]; x++) {
+          src_t s = q->a[tier][x];
+          if (s.kind == SRC_STORED && s.tier == tier && s.slot == x) continue;   /* unchanged */
+          dirty[tier][x] = 1;
+          if (s.kind == SRC_NEW) {
+            float kx[D], vx[D];
+            half_vec(k + ((int64_t)i * H + h) * D, kx);
+            half_vec(v + ((int64_t)i * H + h) * D, vx);
+            make_token(kx, vx, &p->tg[TIER_HI], 0.0f, n - 1, &recs[tier][x]);
+          } else {
+            int ip;
+            token_rec t;
+            const uint8_t* pg = slot_loc(p, row, s.tier, s.slot, &ip);
+            get_token(pg, &p->tg[s.tier], ip, &t);
+            if (s.tier == tier) recs[tier][x] = t;                  /* moved inside its level */
+            else requant(&t, &p->tg[tier], &recs[tier][x]);        /* to a lower level */
+          }
         }
       }
       /* allocate, then free, then write */
-      for (int x = 0; x < q->new_hp; x++) row[cn[2] + x] = p->list[(p->ptr[0] + aoff++) % c->n_pages];
-      for (int x = 0; x < q->new_lp; x++) row[L - 1 - (cn[3] + x)] = p->list[(p->ptr[0] + aoff++) % c->n_pages];
-      for (int x = 0; x < q->free_hp; x++) {
-        int e = cn[2] - 1 - x;
-        p->list[(p->ptr[1] + roff++) % c->n_pages] = row[e];
-        row[e] = -1;
+      for (int y = 0; y < ntiers; y++) {
+        const int tier = k_tiers[y];
+        for (int x = 0; x < q->newp[tier]; x++)
+          row[tab_entry(p, tier, cn[cnt_pg(tier)] + x)] = p->list[(p->ptr[0] + aoff++) % c->n_pages];
       }
-      for (int x = 0; x < q->free_lp; x++) {
-        int e = L - cn[3] + x;
-        p->list[(p->ptr[1] + roff++) % c->n_pages] = row[e];
-        row[e] = -1;
+      for (int y = 0; y < ntiers; y++) {
+        const int tier = k_tiers[y];
+        for (int x = 0; x < q->freep[tier]; x++) {
+          int e = tab_entry(p, tier, cn[cnt_pg(tier)] - 1 - x);
+          p->list[(p->ptr[1] + roff++) % c->n_pages] = row[e];
+          row[e] = -1;
+        }
       }
-      for (int x = 0; x < q->nh; x++) {
-        if (!hi_dirty[x]) continue;
-        int ip;
-        uint8_t* pg = slot_loc(p, row, TIER_HI, x, &ip);
-        put_token(pg, &p->tg[TIER_HI], ip, &hi_new[x]);
+      for (int y = 0; y < ntiers; y++) {
+        const int tier = k_tiers[y];
+        for (int x = 0; x < q->n[tier]; x++) {
+          if (!dirty[tier][x]) continue;
+          int ip;
+          uint8_t* pg = slot_loc(p, row, tier, x, &ip);
+          put_token(pg, &p->tg[tier], ip, &recs[tier][x]);
+        }
+        cn[cnt_tok(tier)] = q->n[tier];
+        cn[cnt_pg(tier)] = q->np[tier];
+        free(recs[tier]); free(dirty[tier]);
       }
-      for (int x = 0; x < q->nl; x++) {
-        if (!lo_dirty[x]) continue;
-        int ip;
-        uint8_t* pg = slot_loc(p, row, TIER_LO, x, &ip);
-        put_token(pg, &p->tg[TIER_LO], ip, &lo_new[x]);
-      }
-      cn[0] = q->nh; cn[1] = q->nl; cn[2] = q->php; cn[3] = q->plp;
-      free(hi_new); free(lo_new); free(hi_dirty); free(lo_dirty);
     }
     rs[2] = n;
   }
   p->ptr[0] += aoff;
   p->ptr[1] += roff;
-  for (int hd = 0; hd < nh; hd++) { free(pl[hd].hi); free(pl[hd].lo); }
+  for (int hd = 0; hd < nh; hd++) for (int x = 0; x < ntiers; x++) free(pl[hd].a[k_tiers[x]]);
   free(pl);
   return ORC_OK;
 }
@@ -844,6 +909,15 @@ int orc_decode_step(orc_pool* p, int layer, int n_req, const int32_t* slots, con
 /* Decode attention — Background, attention equation, over the         */
 /* dequantized mixed-precision pages (hi pages first, then lo).        */
 /* ------------------------------------------------------------------ */
+
+/* Stored token j of a head in attention order (hi slots, then mid slots,
+ * then lo slots): its tier and slot. cn: the head's counters; nm: its mid
+ * tokens (0 without the mid level). */
+static void stored_index(const int32_t* cn, int nm, int j, int* tier, int* s) {
+  if (j < cn[0]) { *tier = TIER_HI; *s = j; }
+  else if (j < cn[0] + nm) { *tier = TIER_MID; *s = j - cn[0]; }
+  else { *tier = TIER_LO; *s = j - cn[0] - nm; }
+}
 
 /* Attention of one KV head's G query heads (q: G x 128 fp16, contiguous)
  * over its stored tokens; out: G x 128 fp64; if pmax is non-NULL it
@@ -854,11 +928,13 @@ int orc_unit_attention(orc_pool* p, int layer, int slot, int kvh, const uint16_t
   const int G = p->c.group_size;
   int32_t* cn = hcnt(p, layer, slot, kvh);
   int32_t* row = trow(p, layer, slot, kvh);
-  const int n = cn[0] + cn[1];
+  const int nm = p->c.mid_enabled ? cn[4] : 0;
+  const int n = cn[0] + nm + cn[1];
   double* kh = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * D);
   double* vh = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * D);
   for (int j = 0; j < n; j++) {
-    int tier = j < cn[0] ? TIER_HI : TIER_LO, s = j < cn[0] ? j : j - cn[0];
+    int tier, s;
+    stored_index(cn, nm, j, &tier, &s);
     token_rec r;
     int ip;
     const uint8_t* pg = slot_loc(p, row, tier, s, &ip);
@@ -908,13 +984,15 @@ int orc_decode_attention(orc_pool* p, int layer, int n_req, const int32_t* slots
     for (int h = 0; h < H; h++) {
       int32_t* cn = hcnt(p, layer, slots[i], h);
       int32_t* row = trow(p, layer, slots[i], h);
-      int n = cn[0] + cn[1];
+      const int nm = p->c.mid_enabled ? cn[4] : 0;
+      int n = cn[0] + nm + cn[1];
       double* pm = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
       orc_unit_attention(p, layer, slots[i], h, q + ((int64_t)i * H * G + (int64_t)h * G) * D,
                          out + ((int64_t)i * H * G + (int64_t)h * G) * D, pm);
       if (update_scores) {
         for (int j = 0; j < n; j++) {
-          int tier = j < cn[0] ? TIER_HI : TIER_LO, s = j < cn[0] ? j : j - cn[0];
+          int tier, s;
+          stored_index(cn, nm, j, &tier, &s);
           const tier_geom* g = &p->tg[tier];
           int ip;
           uint8_t* sp = slot_loc(p, row, tier, s, &ip) + g->off[4] + 4 * ip;
@@ -947,8 +1025,10 @@ int orc_free_request(orc_pool* p, int slot) {
       int32_t* row = trow(p, l, slot, h);
       for (int x = 0; x < cn[2]; x++) p->list[(p->ptr[1]++) % c->n_pages] = row[x];
       for (int x = 0; x < cn[3]; x++) p->list[(p->ptr[1]++) % c->n_pages] = row[p->table_len - 1 - x];
-      for (int e = 0; e < p->table_len; e++) row[e] = -1;
-      cn[0] = cn[1] = cn[2] = cn[3] = 0;
+      if (c->mid_enabled)
+        for (int x = 0; x < cn[5]; x++) p->list[(p->ptr[1]++) % c->n_pages] = row[p->table_len + x];
+      for (int e = 0; e < p->row_len; e++) row[e] = -1;
+      for (int x = 0; x < p->cstride; x++) cn[x] = 0;
     }
     int32_t* rs = rstate(p, l, slot);
     rs[0] = rs[1] = rs[2] = rs[3] = 0;

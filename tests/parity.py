@@ -36,11 +36,14 @@ def valid_mask(page_bytes: int, tier: int, t: int, nvalid: int, scores: bool = T
 
 
 def compare_states(g: dict, o: dict, t_hi: int, t_lo: int, n_pages: int, page_bytes: int,
-                   heads: list | None = None, check_list: bool = True, scores: bool = True):
+                   heads: list | None = None, check_list: bool = True, scores: bool = True,
+                   table_len: int | None = None, t_mid: int = 0):
     """Assert that GPU snapshot g equals oracle snapshot o. If `heads` is
     given, only those (layer, slot, kvh) rows and their pages are compared
     (the pool-wide list then is not). scores=False leaves the score words out
-    (when the two sides computed them in different precisions)."""
+    (when the two sides computed them in different precisions). With the mid
+    level, table_len is the length of the rows' two-way part and t_mid the
+    mid level's tokens per page."""
     if heads is None:
         assert (g["pointers"] == o["pointers"]).all(), (g["pointers"], o["pointers"])
         if check_list:
@@ -51,17 +54,20 @@ def compare_states(g: dict, o: dict, t_hi: int, t_lo: int, n_pages: int, page_by
         assert (g["head_counts"] == o["head_counts"]).all(), "head counters differ"
         assert (g["req_state"] == o["req_state"]).all(), "request state differs"
         heads = list(np.ndindex(*o["table"].shape[:-1]))
-    L = o["table"].shape[-1]
+    L = o["table"].shape[-1] if table_len is None else table_len
     groups: dict[tuple, list] = {}
     for h in heads:
         cnt = o["head_counts"][h]
         row = o["table"][h]
         assert (g["table"][h] == row).all(), ("table row", h)
         assert (g["head_counts"][h] == cnt).all(), ("counts", h)
-        for tier, n, t in ((pagefmt.HI, int(cnt[0]), t_hi), (pagefmt.LO, int(cnt[1]), t_lo)):
+        tiers = [(pagefmt.HI, int(cnt[0]), t_hi), (pagefmt.LO, int(cnt[1]), t_lo)]
+        if cnt.shape[0] > 4:
+            tiers.append((pagefmt.MID, int(cnt[4]), t_mid))
+        for tier, n, t in tiers:
             npg = -(-n // t)
             for x in range(npg):
-                page = row[x] if tier == pagefmt.HI else row[L - 1 - x]
+                page = pagefmt.tier_page(row, tier, x, L)
                 nvalid = min(t, n - x * t)
                 groups.setdefault((tier, t, nvalid), []).append(int(page))
     for (tier, t, nvalid), pages in groups.items():

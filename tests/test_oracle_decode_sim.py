@@ -393,11 +393,13 @@ MUTANTS = {
     "hi_threshold_inclusive": ("if (imp > th_h) return TIER_HI;", "if (imp >= th_h) return TIER_HI;"),
     "lo_threshold_exclusive": ("if (imp >= th_l) return TIER_LO;", "if (imp > th_l) return TIER_LO;"),
     "count_off_by_one": ("+ updates - (j >= n0 ? j - n0 : 0)", "+ updates + 1 - (j >= n0 ? j - n0 : 0)"),
-    "victim_keep_inclusive": ("(iv > th_h) : (iv >= th_l)", "(iv >= th_h) : (iv >= th_l)"),
-    "lo_victim_prune_inclusive": ("if (q->lo[xv].imp < th_l)", "if (q->lo[xv].imp <= th_l)"),
-    "window_ignored": ("argmin_imp(q->hi, q->nh, n - c->window)", "argmin_imp(q->hi, q->nh, n)"),
-    "demoted_pruned_instead": ("if (c->lo_enabled && iv >= th_l) {", "if (c->lo_enabled && iv > th_h) {"),
-    "thresholds_of_head0": ("const float* alpha = p->alpha + 2 * ((size_t)layer * H + h);",
+    "victim_moved_within_its_level": ("if (tier_rank(cv) < tier_rank(vt)) {", "if (tier_rank(cv) <= tier_rank(vt)) {"),
+    "victim_never_moved": ("if (tier_rank(cv) < tier_rank(vt)) {", "if (0) {"),
+    "window_ignored": ("argmin_imp(a, q->n[vt], vt == TIER_HI ? n - c->window : 0x7fffffff)",
+                       "argmin_imp(a, q->n[vt], 0x7fffffff)"),
+    "demoted_pruned_instead": ("if (cv != TIER_PRUNE) q->a[cv][q->n[cv]++] = t;",
+                               "if (0) q->a[cv][q->n[cv]++] = t;"),
+    "thresholds_of_head0": ("const float* alpha = p->alpha + 2 * hx;",
                             "const float* alpha = p->alpha + 2 * ((size_t)layer * H);"),
 }
 
