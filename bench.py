@@ -46,6 +46,7 @@ import workloads  # noqa: E402
 
 METRIC = "compressed-KV decode attn GB/s (% of GB300 HBM peak); compact_step µs/layer"
 HI_BYTES, LO_BYTES, SCORE_RMW = 200, 104, 8
+MID_BYTES = 168          # the three-tier variant's mid token: 8-bit key, 2-bit value, metadata
 # kernels the library launches: prompt compact_step (setup, two tensor-core
 # scoring passes, lse merge, classification, three plan kernels, scatter,
 # pack), decode compact_step (plan, alloc, apply), decode attention
@@ -222,22 +223,24 @@ def launch_ranks(n: int) -> int:
 
 
 # --------------------------------------------------------------- workload
-def attn_bytes(hi_tokens: int, lo_tokens: int, n_req: int, hq: int, update: bool) -> int:
-    per = HI_BYTES * hi_tokens + LO_BYTES * lo_tokens
+def attn_bytes(hi_tokens: int, lo_tokens: int, n_req: int, hq: int, update: bool, mid_tokens: int = 0) -> int:
+    per = HI_BYTES * hi_tokens + LO_BYTES * lo_tokens + MID_BYTES * mid_tokens
     if update:
-        per += SCORE_RMW * (hi_tokens + lo_tokens)
+        per += SCORE_RMW * (hi_tokens + lo_tokens + mid_tokens)
     return per + n_req * hq * (128 * 2 + 128 * 4)
 
 
-def prompt_bytes(hi_tokens: int, lo_tokens: int, n_tokens_heads: int, n_req: int, hq: int) -> int:
-    return 512 * n_tokens_heads + 208 * hi_tokens + 112 * lo_tokens + n_req * 32 * hq * 256
+def prompt_bytes(hi_tokens: int, lo_tokens: int, n_tokens_heads: int, n_req: int, hq: int,
+                 mid_tokens: int = 0) -> int:
+    return 512 * n_tokens_heads + 208 * hi_tokens + 112 * lo_tokens + 176 * mid_tokens + n_req * 32 * hq * 256
 
 
-def describe(w, lens, T, page_bytes) -> str:
+def describe(w, lens, T, page_bytes, mid: bool = False) -> str:
     rng = f"{min(lens)}" if min(lens) == max(lens) else f"U{{{min(lens)}..{max(lens)}}}"
     return (f"{w.name}: {w.shape or 'synthetic'}-shaped layer, {len(lens)} requests x {rng}-token prompts, "
             f"{w.n_q_heads} q / {w.n_kv_heads} KV heads, d=128, {page_bytes}-byte pages, "
-            f"{T} decode steps with compaction and score update" + ("" if w.lo_enabled else ", low tier off"))
+            f"{T} decode steps with compaction and score update" + ("" if w.lo_enabled else ", low tier off") +
+            (", three tiers (hi K8V4 above 2/N, mid K8V2 from 1/N, lo K4V2 from 0.25/N)" if mid else ""))
 
 
 class Loop:
@@ -246,7 +249,7 @@ class Loop:
     score update], free every request)."""
 
     def __init__(self, dkv, name: str, seed: int, dev, decode_steps: int | None = None,
-                 page_bytes: int | None = None, inputs=None):
+                 page_bytes: int | None = None, inputs=None, pool_over: dict | None = None):
         import torch
         self.dkv, self.torch, self.dev = dkv, torch, dev
         self.w = w = workloads.WORKLOADS[name]
@@ -258,6 +261,8 @@ class Loop:
         cfg["max_seq_len"] = max(self.lens) + self.T
         if page_bytes:
             cfg["page_bytes"] = page_bytes
+        cfg.update(pool_over or {})
+        self.mid = bool(cfg.get("mid_enabled", 0))
         self.page_bytes = cfg["page_bytes"]
         self.cfg = cfg
         self.pool = dkv.dkv_pool_create(dkv.make_config(**{k: v for k, v in cfg.items()
@@ -300,7 +305,7 @@ class Loop:
             record["prompt"].append((e0, e1))
         if counts is not None:
             s = dkv.dkv_pool_status(self.pool)
-            counts.append(("prompt", s["hi_tokens"], s["lo_tokens"]))
+            counts.append(("prompt", s["hi_tokens"], s["lo_tokens"], s["mid_tokens"]))
         for t in range(self.T):
             self.flush.fill_(t & 0xFF)
             torch.amax(self.flush_rd)
@@ -325,7 +330,7 @@ class Loop:
                     record["pair"].append((c0, a1))
             if counts is not None:
                 s = dkv.dkv_pool_status(self.pool)
-                counts.append(("attn", s["hi_tokens"], s["lo_tokens"]))
+                counts.append(("attn", s["hi_tokens"], s["lo_tokens"], s["mid_tokens"]))
         for s in self.slots:
             dkv.dkv_free_request(self.pool, s)
 
@@ -338,11 +343,11 @@ class Loop:
         assert st["error"] == 0, st
         self.prompt_counts = counts[0]
         w = self.w
-        self.bytes_per_attn = [attn_bytes(c[1], c[2], w.n_requests, w.n_q_heads, True)
+        self.bytes_per_attn = [attn_bytes(c[1], c[2], w.n_requests, w.n_q_heads, True, c[3])
                                for c in counts if c[0] == "attn"]
         self.n_th = sum(self.lens) * w.n_kv_heads
         self.pbytes = prompt_bytes(self.prompt_counts[1], self.prompt_counts[2], self.n_th, w.n_requests,
-                                   w.n_q_heads)
+                                   w.n_q_heads, self.prompt_counts[3])
 
     def timed(self, steps: int) -> dict:
         torch = self.torch
@@ -370,7 +375,7 @@ class Loop:
         p = gbs(self.pbytes, r["prompt_ms"])
         pc = self.prompt_counts
         return {
-            "workload": describe(self.w, self.lens, self.T, self.page_bytes),
+            "workload": describe(self.w, self.lens, self.T, self.page_bytes, self.mid),
             "decode_attention_us": round(r["alone_ms"] * 1e3, 2),
             "decode_attention_gbs": round(a_alone, 1), "decode_attention_frac": round(a_alone / peak, 4),
             "decode_attention_in_loop_us": round(r["loop_ms"] * 1e3, 2),
@@ -381,8 +386,10 @@ class Loop:
             "compact_step_prompt_gbs": round(p, 1), "compact_step_prompt_frac": round(p / peak, 4),
             "compact_step_prompt_bytes": int(self.pbytes),
             "compact_step_decode_us_per_layer": round(r["compact_ms"] * 1e3, 2),
-            "stored_tokens_after_prompt": {"hi": pc[1], "lo": pc[2], "pruned": self.n_th - pc[1] - pc[2]},
-            "kv_bytes_vs_fp16": round((HI_BYTES * pc[1] + LO_BYTES * pc[2]) / (self.n_th * 512), 4),
+            "stored_tokens_after_prompt": {"hi": pc[1], "lo": pc[2], "pruned": self.n_th - pc[1] - pc[2] - pc[3],
+                                           **({"mid": pc[3]} if self.mid else {})},
+            "kv_bytes_vs_fp16": round((HI_BYTES * pc[1] + LO_BYTES * pc[2] + MID_BYTES * pc[3]) / (self.n_th * 512),
+                                      4),
         }
 
 
@@ -631,10 +638,14 @@ def run_dkv(args, world, rank, local):
     extras = [] if args.extras in ("", "none") else args.extras.split(",")
     result["parts"]["other_configs"] = {}
     for name in extras:
+        # "<workload>[@<page bytes>][+mid]": +mid runs the workload's inputs on a three-tier pool
         wl, _, pb = name.partition("@")
+        three = name.endswith("+mid")
+        wl, pb = wl.removesuffix("+mid"), pb.removesuffix("+mid")
         ex = Loop(dkv, wl, args.seed + rank, dev, page_bytes=int(pb) if pb else None,
                   decode_steps=min(workloads.WORKLOADS[wl].decode_steps, 32),
-                  inputs=headline_inputs if wl == args.workload else None)
+                  inputs=headline_inputs if wl == args.workload else None,
+                  pool_over=workloads.THREE_TIER if three else None)
         ex.warm(1)
         rr = ex.timed(args.extra_steps)
         result["parts"]["other_configs"][name] = ex.summary(rr, peak)
@@ -837,7 +848,7 @@ def main():
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--decode-steps", type=int, default=None)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--extras", default="llama70b,llama8b@4096,qwen7b",
+    ap.add_argument("--extras", default="llama70b,llama8b@4096,qwen7b,llama8b+mid",
                     help="other configurations measured after the headline (workload[@page_bytes],...; 'none')")
     ap.add_argument("--extra-steps", type=int, default=2)
     ap.add_argument("--churn-ticks", type=int, default=1500,

@@ -102,25 +102,34 @@ __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_heads(PoolView 
   if (u >= n_units) return;
   const int n0 = ca->lens[u / pv.hkv];
   const int nkb = (n0 + kKeyBlock - 1) / kKeyBlock;
-  int a = 0, b = 0;
+  int a = 0, b = 0, m = 0;
   for (int k0 = 0; k0 < nkb; k0 += 32) {
     const int kb = k0 + lane;
-    const int2 c = kb < nkb ? sc.bcnt[(size_t)u * sc.nkb_cap + kb] : make_int2(0, 0);
-    int x = c.x, y = c.y;
+    const size_t bx = (size_t)u * sc.nkb_cap + kb;
+    const int2 c = kb < nkb ? sc.bcnt[bx] : make_int2(0, 0);
+    const int cm = pv.mid_enabled && kb < nkb ? sc.bcnt_m[bx] : 0;
+    int x = c.x, y = c.y, z = cm;
 #pragma unroll
     for (int s = 1; s < 32; s <<= 1) {
       const int xo = __shfl_up_sync(0xffffffffu, x, s), yo = __shfl_up_sync(0xffffffffu, y, s);
-      if (lane >= s) { x += xo; y += yo; }
+      const int zo = __shfl_up_sync(0xffffffffu, z, s);
+      if (lane >= s) { x += xo; y += yo; z += zo; }
     }
-    if (kb < nkb) sc.bbase[(size_t)u * sc.nkb_cap + kb] = make_int2(a + x - c.x, b + y - c.y);
+    if (kb < nkb) {
+      sc.bbase[bx] = make_int2(a + x - c.x, b + y - c.y);
+      if (pv.mid_enabled) sc.bbase_m[bx] = m + z - cm;
+    }
     a += __shfl_sync(0xffffffffu, x, 31);
     b += __shfl_sync(0xffffffffu, y, 31);
+    m += __shfl_sync(0xffffffffu, z, 31);
   }
   if (lane == 0) {
     const int gh = (n0 + pv.hi.t - 1) / pv.hi.t + pv.slack;
     const int nhp = (a + pv.hi.t - 1) / pv.hi.t, nlp = (b + pv.lo.t - 1) / pv.lo.t;
-    if (nhp + nlp > gh || nhp + nlp > pv.L) latch_error(pv, DKV_ERR_TABLE_FULL, u);
-    sc.unit_info[u] = make_int4(gh, a, b, max(0, gh - nhp - nlp));
+    const int nmp = pv.mid_enabled ? (m + pv.mid.t - 1) / pv.mid.t : 0;
+    if (nhp + nmp + nlp > gh || nhp + nlp > pv.L || nmp > pv.Lm) latch_error(pv, DKV_ERR_TABLE_FULL, u);
+    sc.unit_info[u] = make_int4(gh, a, b, max(0, gh - nhp - nmp - nlp));
+    if (pv.mid_enabled) sc.unit_mid[u] = m;
   }
 }
 
@@ -171,19 +180,23 @@ __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_commit(PoolView
   const int i = u / pv.hkv, kvh = u % pv.hkv, slot = ca->slots[i];
   const int4 ui = sc.unit_info[u];
   const int gh = ui.x, nhp = (ui.y + pv.hi.t - 1) / pv.hi.t, nlp = (ui.z + pv.lo.t - 1) / pv.lo.t;
+  const int nm = pv.mid_enabled ? sc.unit_mid[u] : 0;
+  const int nmp = pv.mid_enabled ? (nm + pv.mid.t - 1) / pv.mid.t : 0;   // grant pages nhp .. nhp+nmp-1
   const int* gid = sc.grant_ids + (size_t)u * sc.grant_cap;
-  for (int x = nhp + lane; x < gh - nlp; x += 32)
-    pv.list[(end + (unsigned long long)(s_r[u] + x - nhp)) % pv.n_pages] = gid[x];
+  for (int x = nhp + nmp + lane; x < gh - nlp; x += 32)
+    pv.list[(end + (unsigned long long)(s_r[u] + x - nhp - nmp)) % pv.n_pages] = gid[x];
   int* row = pv.row(layer, slot, kvh);
-  for (int e = lane; e < pv.L; e += 32) {
+  for (int e = lane; e < pv.Lrow; e += 32) {
     int v = -1;
     if (e < nhp) v = gid[e];
-    else if (e >= pv.L - nlp) v = gid[gh - 1 - (pv.L - 1 - e)];
+    else if (e < pv.L && e >= pv.L - nlp) v = gid[gh - 1 - (pv.L - 1 - e)];
+    else if (e >= pv.L && e < pv.L + nmp) v = gid[nhp + e - pv.L];   // the one-way mid part
     row[e] = v;
   }
   if (lane == 0) {
     int* cn = pv.cnt(layer, slot, kvh);
     cn[0] = ui.y; cn[1] = ui.z; cn[2] = nhp; cn[3] = nlp;
+    if (pv.mid_enabled) { cn[4] = nm; cn[5] = nmp; }
     if (kvh == 0) {
       int* rq = pv.rq(layer, slot);
       rq[0] = 1; rq[1] = ca->lens[i]; rq[2] = ca->lens[i]; rq[3] = 0;
@@ -193,15 +206,17 @@ __global__ void __launch_bounds__(32 * kPlanWarps) k_prompt_plan_commit(PoolView
 
 // ---------------------------------------------------------------------------
 // Generation-phase coordination: new pages for every head that needs one, by
-// one prefix sum at the list start (per head hi then lo); emptied tail pages
+// one prefix sum at the list start (per head hi, lo, then mid); emptied tail pages
 // (reclaim_in_decode) by one prefix sum at the list end; table rows,
 // counters and the request lengths updated. All checks precede every write.
 // ---------------------------------------------------------------------------
+// MID: a three-tier pool (the two-tier instance compiles the mid tier out)
+template <bool MID>
 __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int layer, Scratch sc,
                                                                  SlotArgs sa) {
   pdl_launch_dependents();        // k_decode_apply may launch; it waits for this grid
   if (pv.noop()) return;
-  extern __shared__ int s_list[];  // [2 n_units] the list entries from the start: the pages a grant can take
+  extern __shared__ int s_list[];  // [k n_units] the list entries from the start: the pages a grant can take
   __shared__ int s_warp[32];
   __shared__ int s_err, s_info;
   const int n_units = sa.n * pv.hkv;
@@ -209,10 +224,11 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
   const int u0 = threadIdx.x * per, u1 = min(n_units, u0 + per);
   if (threadIdx.x == 0) { s_err = 0; s_info = -1; }
   // The list counters and the entries from the start (a head takes at most a
-  // hi and a lo page): only this kernel moves or reads them during a
+  // page of each tier): only this kernel moves or reads them during a
   // generation step, so they load while the plans finish.
   const unsigned long long start = pv.ctl->start, end = pv.ctl->end;
-  for (int x = threadIdx.x; x < 2 * n_units; x += blockDim.x)
+  constexpr int per_head = MID ? 3 : 2;
+  for (int x = threadIdx.x; x < per_head * n_units; x += blockDim.x)
     s_list[x] = pv.list[(start + (unsigned long long)x) % pv.n_pages];
   pdl_wait();                     // the plans of k_decode_plan
   if (pv.noop_after_wait()) return;
@@ -223,8 +239,8 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
     if (p.err != 0) {
       if (atomicCAS(&s_err, 0, p.err) == 0) s_info = u;
     }
-    my_a += p.new_hp + p.new_lp;
-    my_f += p.free_hp + p.free_lp;
+    my_a += p.new_hp + p.new_lp + (MID ? p.new_mp : 0);
+    my_f += p.free_hp + p.free_lp + (MID ? p.free_mp : 0);
   }
   int tot_a, tot_f;
   const int aoff = block_exclusive_scan(my_a, s_warp, &tot_a);
@@ -246,8 +262,10 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
     int* row = pv.row(layer, slot, kvh);
     // the page counts before the step, from the plan (new = old + new - freed)
     const int php0 = p.php - p.new_hp + p.free_hp, plp0 = p.plp - p.new_lp + p.free_lp;
+    const int pmp0 = MID ? p.pmp - p.new_mp + p.free_mp : 0;
     if (p.new_hp) row[php0] = s_list[a++];
     if (p.new_lp) row[pv.L - 1 - plp0] = s_list[a++];
+    if (MID && p.new_mp) row[pv.L + pmp0] = s_list[a++];
     if (p.free_hp) {
       pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[php0 - 1];
       row[php0 - 1] = -1;
@@ -256,7 +274,12 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
       pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[pv.L - plp0];
       row[pv.L - plp0] = -1;
     }
+    if (MID && p.free_mp) {
+      pv.list[(end + (unsigned long long)(f++)) % pv.n_pages] = row[pv.L + pmp0 - 1];
+      row[pv.L + pmp0 - 1] = -1;
+    }
     cn[0] = p.nh; cn[1] = p.nl; cn[2] = p.php; cn[3] = p.plp;
+    if (MID) { cn[4] = p.nm; cn[5] = p.pmp; }
     if (kvh == 0) pv.rq(layer, slot)[2] += 1;
   }
   __syncthreads();
@@ -268,8 +291,9 @@ __global__ void __launch_bounds__(kCoordThreads) k_decode_alloc(PoolView pv, int
 
 // ---------------------------------------------------------------------------
 // Request completion: every page of the request (all layers, all KV heads;
-// within a head hi pages left to right, then lo pages from the outermost in)
-// appended at the list end by one prefix sum; rows and state cleared.
+// within a head hi pages left to right, then lo pages from the outermost in,
+// then mid pages left to right) appended at the list end by one prefix sum;
+// rows and state cleared.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kCoordThreads) k_free_request(PoolView pv, int slot) {
   if (pv.noop()) return;
@@ -278,12 +302,14 @@ __global__ void __launch_bounds__(kCoordThreads) k_free_request(PoolView pv, int
   const int n_units = pv.n_layers * pv.hkv;
   int* s_c = s_dyn;             // pages per (layer, KV head) -> exclusive offsets
   int* s_h = s_dyn + n_units;   // hi pages per (layer, KV head)
+  int* s_l = s_dyn + 2 * n_units;   // lo pages (three-tier pools: mid pages follow them)
   for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
     const int layer = u / pv.hkv, kvh = u % pv.hkv;
     const int* cn = pv.cnt(layer, slot, kvh);
     const bool act = pv.rq(layer, slot)[0] != 0;
-    s_c[u] = act ? cn[2] + cn[3] : 0;
+    s_c[u] = act ? cn[2] + cn[3] + (pv.mid_enabled ? cn[5] : 0) : 0;
     s_h[u] = act ? cn[2] : 0;
+    s_l[u] = act ? cn[3] : 0;
   }
   __syncthreads();
   const int tot = block_scan_array(s_c, n_units, s_warp);
@@ -298,17 +324,18 @@ __global__ void __launch_bounds__(kCoordThreads) k_free_request(PoolView pv, int
       if (s_c[mid] <= x) lo = mid; else hi = mid - 1;
     }
     const int* row = pv.row(lo / pv.hkv, slot, lo % pv.hkv);
-    const int k = x - s_c[lo], nh = s_h[lo];
-    pv.list[(end + (unsigned long long)x) % pv.n_pages] = k < nh ? row[k] : row[pv.L - 1 - (k - nh)];
+    const int k = x - s_c[lo], nh = s_h[lo], nl = s_l[lo];
+    pv.list[(end + (unsigned long long)x) % pv.n_pages] =
+        k < nh ? row[k] : (k < nh + nl ? row[pv.L - 1 - (k - nh)] : row[pv.L + (k - nh - nl)]);
   }
   __syncthreads();
   for (int u = 0; u < n_units; u++) {
     int* row = pv.row(u / pv.hkv, slot, u % pv.hkv);
-    for (int e = threadIdx.x; e < pv.L; e += blockDim.x) row[e] = -1;
+    for (int e = threadIdx.x; e < pv.Lrow; e += blockDim.x) row[e] = -1;
   }
   for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
     int* cn = pv.cnt(u / pv.hkv, slot, u % pv.hkv);
-    cn[0] = cn[1] = cn[2] = cn[3] = 0;
+    for (int x = 0; x < pv.cstride; x++) cn[x] = 0;
   }
   for (int layer = threadIdx.x; layer < pv.n_layers; layer += blockDim.x) {
     int* rq = pv.rq(layer, slot);
@@ -343,7 +370,9 @@ cudaError_t configure_alloc() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_free_request, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_decode_alloc, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  e = cudaFuncSetAttribute(k_decode_alloc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_decode_alloc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
 
 // A programmatic dependent of k_decode_plan. One CTA, a thread per head up to
@@ -353,20 +382,21 @@ cudaError_t launch_decode_alloc(Pool& P, int layer, const SlotArgs& sa, cudaStre
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(1);
   lc.blockDim = dim3(std::min(kCoordThreads, (n_units + 31) / 32 * 32));
-  lc.dynamicSmemBytes = 2 * (size_t)n_units * sizeof(int);   // the list window
+  lc.dynamicSmemBytes = (P.pv.mid_enabled ? 3 : 2) * (size_t)n_units * sizeof(int);   // the list window
   lc.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&lc, k_decode_alloc, P.pv, layer, P.sc, sa);
+  const cudaError_t e = P.pv.mid_enabled ? cudaLaunchKernelEx(&lc, k_decode_alloc<true>, P.pv, layer, P.sc, sa)
+                                         : cudaLaunchKernelEx(&lc, k_decode_alloc<false>, P.pv, layer, P.sc, sa);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_free(Pool& P, int slot, cudaStream_t st) {
-  const int smem = 2 * P.pv.n_layers * P.pv.hkv * (int)sizeof(int);
+  const int smem = 3 * P.pv.n_layers * P.pv.hkv * (int)sizeof(int);
   k_free_request<<<1, kCoordThreads, smem, st>>>(P.pv, slot);
   return cudaGetLastError();
 }

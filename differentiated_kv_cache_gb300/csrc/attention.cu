@@ -26,6 +26,7 @@
 //                  its contiguous K | V | K-meta | V-meta | score prefix;
 //   k_attn_decode  any page geometry: per 16-slot chunk, one copy per page run.
 #include <algorithm>
+#include <vector>
 
 #include "dkv_kernels.cuh"
 
@@ -437,25 +438,32 @@ __device__ __forceinline__ void publish(const PoolView& pv, const AttnArgs& a, A
   }
 }
 
-// Work items of a head with nh hi and nl lo tokens: on the paged path its
-// pages weighted by their cost (wh, wl) after the head's own (hw), on the
-// chunked path its chunks.
-__device__ __forceinline__ int head_items(const PoolView& pv, int nh, int nl, bool paged, int wh, int wl, int hw) {
-  return paged ? (nh + nl > 0 ? hw : 0) + (nh + pv.hi.t - 1) / pv.hi.t * wh + (nl + pv.lo.t - 1) / pv.lo.t * wl
+// Work items of a head with nh hi, nl lo and nm mid tokens: on the paged
+// path its pages weighted by their cost (wh, wl, wm) after the head's own
+// (hw), on the chunked path (two-tier pools only) its chunks.
+__device__ __forceinline__ int head_items(const PoolView& pv, int nh, int nl, int nm, bool paged, int wh, int wl,
+                                          int wm, int hw) {
+  return paged ? (nh + nl + nm > 0 ? hw : 0) + (nh + pv.hi.t - 1) / pv.hi.t * wh +
+                     (nl + pv.lo.t - 1) / pv.lo.t * wl + (nm > 0 ? (nm + pv.mid.t - 1) / pv.mid.t * wm : 0)
                : (nh + kChunk - 1) / kChunk + (nl + kChunk - 1) / kChunk;
 }
 
+// mid tokens of a head (MID: a three-tier pool; 0 in a two-tier pool)
+template <bool MID>
+__device__ __forceinline__ int mid_count(const int* cn) { return MID ? cn[4] : 0; }
+
 // Prefix over the call's heads of their work items (pages or chunks), in
 // shared memory; every CTA computes the same. Returns the total.
-__device__ int item_prefix(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int hw,
-                           int* s_pref, int* s_warp) {
+template <bool MID>
+__device__ int item_prefix(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int wm,
+                           int hw, int* s_pref, int* s_warp) {
   const int n_units = sa.n * pv.hkv;
   const int per = (n_units + blockDim.x - 1) / blockDim.x;
   const int u0 = min(n_units, (int)threadIdx.x * per), u1 = min(n_units, u0 + per);
   int sum = 0;
   for (int u = u0; u < u1; u++) {
     const int* cn = pv.cnt(layer, sa.slots[u / pv.hkv], u % pv.hkv);
-    const int items = head_items(pv, cn[0], cn[1], paged, wh, wl, hw);
+    const int items = head_items(pv, cn[0], cn[1], mid_count<MID>(cn), paged, wh, wl, wm, hw);
     s_pref[u] = items;
     sum += items;
   }
@@ -505,17 +513,20 @@ constexpr float kLazy = 8.0f;         // probabilities stay below 2^kLazy
 
 struct PageCursor {
   int u, begin, end;   // head and its cost range
-  int hp, np;          // hi pages, all pages
+  int hp, mp, np;      // hi pages, mid pages (three-tier pools), all pages
   int nh, nl;
   const int* row;
   int p, off;          // current page and its cost offset
 };
 
+// A head's pages in the order the warps stream them: hi, mid (three-tier
+// pools, MID), then lo.
+template <bool MID>
 struct PagedCtx {
   const PoolView& pv;
   const SlotArgs& sa;
   const int* s_pref;
-  int layer, n_units, wh, wl, hw;
+  int layer, n_units, wh, wl, wm, hw;
 
   __device__ __forceinline__ void at_unit(PageCursor& c, int u) const {
     c.u = u;
@@ -524,8 +535,10 @@ struct PagedCtx {
     const int* cn = pv.cnt(layer, sa.slots[u / pv.hkv], u % pv.hkv);
     c.nh = cn[0];
     c.nl = cn[1];
+    const int nm = mid_count<MID>(cn);
     c.hp = (c.nh + pv.hi.t - 1) / pv.hi.t;
-    c.np = c.hp + (c.nl + pv.lo.t - 1) / pv.lo.t;
+    c.mp = nm > 0 ? (nm + pv.mid.t - 1) / pv.mid.t : 0;
+    c.np = c.hp + c.mp + (c.nl + pv.lo.t - 1) / pv.lo.t;
     c.row = pv.row(layer, sa.slots[u / pv.hkv], u % pv.hkv);
     c.p = 0;
     c.off = c.begin + hw;
@@ -542,9 +555,12 @@ struct PagedCtx {
       if (o <= c.hp * wh) {
         c.p = (o + wh - 1) / wh;
         c.off += c.p * wh;
+      } else if (o <= c.hp * wh + c.mp * wm) {
+        c.p = c.hp + (o - c.hp * wh + wm - 1) / wm;
+        c.off += c.hp * wh + (c.p - c.hp) * wm;
       } else {
-        c.p = c.hp + (o - c.hp * wh + wl - 1) / wl;
-        c.off += c.hp * wh + (c.p - c.hp) * wl;
+        c.p = c.hp + c.mp + (o - c.hp * wh - c.mp * wm + wl - 1) / wl;
+        c.off += c.hp * wh + c.mp * wm + (c.p - c.hp - c.mp) * wl;
       }
     }
     settle(c);
@@ -568,8 +584,9 @@ __device__ __forceinline__ float lo_half(uint32_t w) { return __half2float(__ush
 __device__ __forceinline__ float hi_half(uint32_t w) { return __half2float(__ushort_as_half((uint16_t)(w >> 16))); }
 
 // NC consecutive chunks c0 .. c0+NC-1 of a staged page, one softmax step.
-// FULL: every slot of the chunks is valid (no masking).
-template <bool HI, int NC, bool FULL>
+// FULL: every slot of the chunks is valid (no masking). KB, VB: the tier's
+// key and value bits (hi 8/4, mid 8/2, lo 4/2).
+template <int KB, int VB, int NC, bool FULL>
 __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, const TierGeom& tg, int c0, int count,
                                               const uint32_t (&bq)[8][2], float sq0, float sq1, float* lg, int lrow,
                                               int pid, int G, int g, int t, int jA, int jB) {
@@ -580,7 +597,7 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
   for (int c = 0; c < NC; c++) {
     const int sA = (c0 + c) * kChunk + jA, sB = (c0 + c) * kChunk + jB;
     float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (HI) {
+    if (KB == 8) {
       const uint4* pa = reinterpret_cast<const uint4*>(sb + sA * 128 + 32 * t);
       const uint4* pb = reinterpret_cast<const uint4*>(sb + sB * 128 + 32 * t);
       const uint4 ka0 = pa[0], ka1 = pa[1], kb0 = pb[0], kb1 = pb[1];
@@ -667,8 +684,8 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
       S.o[mt][1] *= f1; S.o[mt][3] *= f1;
     }
   }
-  // v^ = s (c - off) + (z + off s), off = 8 (hi) or 2 (lo)
-  constexpr float voff = HI ? 8.0f : 2.0f;
+  // v^ = s (c - off) + (z + off s), off = 8 (4-bit values) or 2 (2-bit values)
+  constexpr float voff = VB == 4 ? 8.0f : 2.0f;
 #pragma unroll
   for (int c = 0; c < NC; c++) {
     const float p0 = fast_exp2(l2[c][0] - S.m[0]), p1 = fast_exp2(l2[c][1] - S.m[1]);
@@ -695,7 +712,7 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
     const uint32_t pb0 = movmatrix_trans(res ? l0 : h0), pb1 = movmatrix_trans(res ? l1 : h1);
     const uint32_t pr0 = two ? movmatrix_trans(l0) : 0u, pr1 = two ? movmatrix_trans(l1) : 0u;
     // ---- O^T += V^T . P'^T ----
-    if (HI) {
+    if (VB == 4) {
       const uint8_t* v0 = sb + tg.off[1] + ((c0 + c) * 8 + 2 * t) * 128 + 16 * g;
       const uint4 vq0 = *reinterpret_cast<const uint4*>(v0);
       const uint4 vq1 = *reinterpret_cast<const uint4*>(v0 + 128);
@@ -732,22 +749,22 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
 }
 
 // All chunks of one staged page: pairs of chunks share a softmax step.
-template <bool HI>
+template <int KB, int VB>
 __device__ __forceinline__ void attend_page(AttnState& S, const uint8_t* sb, const TierGeom& tg, int nch, int count,
                                             const uint32_t (&bq)[8][2], float sq0, float sq1, float* lg, int lrow,
                                             int pid, int G, int g, int t, int jA, int jB) {
   if (count >= nch * kChunk) {
     int c = 0;
     for (; c + 2 <= nch; c += 2)
-      attend_chunks<HI, 2, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G, g, t,
-                                 jA, jB);
+      attend_chunks<KB, VB, 2, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G,
+                                     g, t, jA, jB);
     if (c < nch)
-      attend_chunks<HI, 1, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G, g, t,
-                                 jA, jB);
+      attend_chunks<KB, VB, 1, true>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G,
+                                     g, t, jA, jB);
   } else {
     for (int c = 0; c * kChunk < count; c++)
-      attend_chunks<HI, 1, false>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G, g, t,
-                                  jA, jB);
+      attend_chunks<KB, VB, 1, false>(S, sb, tg, c, count, bq, sq0, sq1, lg ? lg + c * lrow : nullptr, lrow, pid, G,
+                                      g, t, jA, jB);
   }
 }
 
@@ -760,9 +777,14 @@ __device__ __forceinline__ void count_update(const PoolView& pv, const AttnArgs&
     for (int i = threadIdx.x; i < sa.n; i += blockDim.x) pv.rq(a.layer, sa.slots[i])[3] += 1;
 }
 
+// Tier tag of a page descriptor's count word (bit 31 hi, bit 30 mid).
+constexpr uint32_t kDescHi = 0x80000000u, kDescMid = 0x40000000u;
+
 // W: warps per CTA, 16 (one CTA per SM) or 4 (four CTAs per SM); GT: the
-// group size when fixed at compile time (4, 8), else 0 (pv.G)
-template <int W, int GT>
+// group size when fixed at compile time (4, 8), else 0 (pv.G); MID: a
+// three-tier pool (hi, mid and lo pages; the two-tier instances compile the
+// mid tier out)
+template <int W, int GT, bool MID>
 __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView pv, AttnArgs a, SlotArgs sa) {
   // a programmatic dependent of the kernel before it (counts, pages); the
   // epilogue grid, which reads the counts before its own wait, may launch
@@ -773,21 +795,22 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
   __shared__ int s_warp[W];
   const int n_units = sa.n * pv.hkv;
   const int G = GT > 0 ? GT : pv.G;
-  const int nch_hi = pv.hi.t / kChunk, nch_lo = pv.lo.t / kChunk;
+  const int nch_hi = pv.hi.t / kChunk, nch_lo = pv.lo.t / kChunk, nch_mid = MID ? pv.mid.t / kChunk : 0;
   const int wh = page_cost(G, nch_hi), wl = page_cost(G, nch_lo), hw = head_cost(G);
+  const int wm = MID ? page_cost(G, nch_mid) : 0;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + W * kPageStages * a.stage_bytes);
   int4* s_tab = reinterpret_cast<int4*>(s_bar + W * kPageStages);   // [warp][2][32] page descriptors
   int* s_pref = reinterpret_cast<int*>(s_tab + W * 2 * 32);
-  const int total = item_prefix(pv, sa, a.layer, true, wh, wl, hw, s_pref, s_warp);
+  const int total = item_prefix<MID>(pv, sa, a.layer, true, wh, wl, wm, hw, s_pref, s_warp);
   const int nwarps = gridDim.x * W;
   // at least kMinChunks pages of the heaviest kind per range: a head is then
   // covered by at most (its pages / kMinChunks) + 2 ranges
-  const int C = range_width(total, nwarps, true, wh, wl);
+  const int C = range_width(total, nwarps, true, wh, max(wl, wm));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int gw = blockIdx.x * W + warp;
   const int g0 = gw * C, g1 = min(total, g0 + C);
-  const PagedCtx ctx{pv, sa, s_pref, a.layer, n_units, wh, wl, hw};
+  const PagedCtx<MID> ctx{pv, sa, s_pref, a.layer, n_units, wh, wl, wm, hw};
   PageCursor ci;
   bool active = g0 < g1;
   if (active) {
@@ -807,21 +830,25 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
   // The warp's pages in batches of 32, one page a lane: lane k of batch b
   // walks from the batch's first page (head bu, page bp of the head) k pages
   // on, across heads, and writes table entry (b & 1, k) = {head, page ID,
-  // valid slots from the page start (bit 31: hi tier), the head's chunk index
-  // of the page's first chunk}, or head -1 past the range. The 32 page-ID
-  // loads are in flight together. Entries of batch b are replaced by batch
-  // b + 2 only, after every page of batch b was consumed.
+  // valid slots from the page start (bit 31: hi tier, bit 30: mid tier), the
+  // head's chunk index of the page's first chunk}, or head -1 past the range.
+  // The 32 page-ID loads are in flight together. Entries of batch b are
+  // replaced by batch b + 2 only, after every page of batch b was consumed.
   int bu = ci.u, bp = ci.p;
   auto fill_batch = [&](int b) -> int {
     int u = bu, p = bp + lane;
-    int nh = 0, nl = 0, hp = 0, np = 0;
+    int nh = 0, nl = 0, nm = 0, hp = 0, mp = 0, np = 0;
     bool ok = true;
     for (;;) {
       const int* cn = pv.cnt(a.layer, sa.slots[u / pv.hkv], u % pv.hkv);
       nh = cn[0];
       nl = cn[1];
       hp = pv.hi.div(nh + pv.hi.t - 1);
-      np = hp + pv.lo.div(nl + pv.lo.t - 1);
+      if (MID) {
+        nm = cn[4];
+        mp = nm > 0 ? pv.mid.div(nm + pv.mid.t - 1) : 0;
+      }
+      np = hp + mp + pv.lo.div(nl + pv.lo.t - 1);
       if (p < np) break;
       p -= np;
       if (++u >= n_units) {
@@ -829,15 +856,18 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
         break;
       }
     }
-    const bool hi = p < hp;
-    const int pt = hi ? p : p - hp;
-    if (ok) ok = s_pref[u] + hw + (hi ? pt * wh : hp * wh + pt * wl) < g1;
+    const bool hi = p < hp, mid = MID && !hi && p < hp + mp;
+    const int pt = hi ? p : (mid ? p - hp : p - hp - mp);
+    if (ok) ok = s_pref[u] + hw + (hi ? pt * wh : (mid ? hp * wh + pt * wm : hp * wh + mp * wm + pt * wl)) < g1;
     int4 dsc = make_int4(-1, 0, 0, 0);
     if (ok) {
-      const int count = hi ? nh - pt * pv.hi.t : nl - pt * pv.lo.t;
-      const int chunk0 = hi ? pt * nch_hi : (nh + kChunk - 1) / kChunk + pt * nch_lo;
-      const int pid = __ldg(pv.row(a.layer, sa.slots[u / pv.hkv], u % pv.hkv) + (hi ? pt : pv.L - 1 - pt));
-      dsc = make_int4(u, pid, hi ? (int)(0x80000000u | (uint32_t)count) : count, chunk0);
+      const int count = hi ? nh - pt * pv.hi.t : (mid ? nm - pt * pv.mid.t : nl - pt * pv.lo.t);
+      const int ch_h = (nh + kChunk - 1) / kChunk;
+      const int chunk0 = hi ? pt * nch_hi
+                            : (mid ? ch_h + pt * nch_mid : ch_h + (nm + kChunk - 1) / kChunk + pt * nch_lo);
+      const int pid = __ldg(pv.row(a.layer, sa.slots[u / pv.hkv], u % pv.hkv) +
+                            (hi ? pt : (mid ? pv.L + pt : pv.L - 1 - pt)));
+      dsc = make_int4(u, pid, (int)((hi ? kDescHi : (mid ? kDescMid : 0u)) | (uint32_t)count), chunk0);
     }
     wtab[(b & 1) * 32 + lane] = dsc;
     const unsigned vm = __ballot_sync(0xffffffffu, ok);
@@ -853,7 +883,8 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
       const int4 dsc = wtab[((xi >> 5) & 1) * 32 + (xi & 31)];
       const int st = xi % kPageStages;
       const uint32_t bar = bar0 + 8 * st;
-      const uint32_t bytes = dsc.z < 0 ? pv.hi.off[5] : pv.lo.off[5];
+      const uint32_t bytes =
+          dsc.z < 0 ? pv.hi.off[5] : (MID && (dsc.z & kDescMid) ? pv.mid.off[5] : pv.lo.off[5]);
       mbar_expect_tx(bar, bytes);
       bulk_g2s(smem_u32(wst + st * a.stage_bytes), pv.page(dsc.y), bytes, bar);
     }
@@ -863,10 +894,11 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
   for (int x = 0; x < kPageStages - 1 && x < n_pages; x++) issue(x);
   AttnState S;
   lazy_reset(S);
-  // the first head's queries load while its first pages are in flight
+  // the first head's queries load while its first pages are in flight; the
+  // 8-bit key order serves hi and mid pages, the 4-bit one lo pages
   uint32_t bq[8][2];
   float sq0, sq1;
-  bool q_hi = ci.p < ci.hp;
+  bool q_hi = ci.p < ci.hp + ci.mp;
   int cur_u = ci.u;
   load_q1<GT>(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, q_hi, bq, sq0, sq1);
   const int jA = chunk_slot(g), jB = chunk_slot(g + 8);
@@ -888,25 +920,29 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
       failed = true;
       break;
     }
-    const int4 d = wtab[((x >> 5) & 1) * 32 + (x & 31)];   // head, page ID, valid slots | hi, first chunk
+    const int4 d = wtab[((x >> 5) & 1) * 32 + (x & 31)];   // head, page ID, valid slots | tier, first chunk
     const bool hi = d.z < 0;
-    const int count = d.z & 0x7fffffff;
+    const bool mid = MID && (d.z & kDescMid) != 0;
+    const bool k8 = hi || mid;    // 8-bit keys
+    const int count = d.z & 0x3fffffff;
     if (d.x != cur_u) {           // the range enters the next head
       publish<GT>(pv, a, S, cur_u, ctx.first_owner(cur_u, C), gw, lane);
       cur_u = d.x;
-      q_hi = hi;
-      load_q1<GT>(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
+      q_hi = k8;
+      load_q1<GT>(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, k8, bq, sq0, sq1);
       lazy_reset(S);
-    } else if (hi != q_hi) {      // from the head's hi pages to its lo pages
-      q_hi = hi;
-      load_q1<GT>(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, hi, bq, sq0, sq1);
+    } else if (k8 != q_hi) {      // from the head's 8-bit-key pages to its lo pages
+      q_hi = k8;
+      load_q1<GT>(pv, a, cur_u / pv.hkv, cur_u % pv.hkv, g, t, k8, bq, sq0, sq1);
     }
     const uint8_t* sb = wst + (x % kPageStages) * a.stage_bytes;
     float* lgp = a.update ? a.logit + ((size_t)cur_u * a.max_chunks + d.w) * a.lrow : nullptr;
     if (hi)
-      attend_page<true>(S, sb, pv.hi, nch_hi, count, bq, sq0, sq1, lgp, a.lrow, d.y, G, g, t, jA, jB);
+      attend_page<8, 4>(S, sb, pv.hi, nch_hi, count, bq, sq0, sq1, lgp, a.lrow, d.y, G, g, t, jA, jB);
+    else if (MID && mid)
+      attend_page<8, 2>(S, sb, pv.mid, nch_mid, count, bq, sq0, sq1, lgp, a.lrow, d.y, G, g, t, jA, jB);
     else
-      attend_page<false>(S, sb, pv.lo, nch_lo, count, bq, sq0, sq1, lgp, a.lrow, d.y, G, g, t, jA, jB);
+      attend_page<4, 2>(S, sb, pv.lo, nch_lo, count, bq, sq0, sq1, lgp, a.lrow, d.y, G, g, t, jA, jB);
   }
   if (!failed) publish<GT>(pv, a, S, cur_u, ctx.first_owner(cur_u, C), gw, lane);
 }
@@ -929,7 +965,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps, kWarpsPerSm / kAttnWarps) k_a
   const int G = pv.G;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kAttnWarps * kStages * a.stage_bytes);
   int* s_pref = reinterpret_cast<int*>(s_bar + kAttnWarps * kStages);
-  const int total = item_prefix(pv, sa, a.layer, false, 1, 1, 0, s_pref, s_warp);
+  const int total = item_prefix<false>(pv, sa, a.layer, false, 1, 1, 0, 0, s_pref, s_warp);
   const int nwarps = gridDim.x * kAttnWarps;
   const int C = range_width(total, nwarps, false, 1, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1101,14 +1137,15 @@ struct EpiSmem {
 // cost on the paged path, chunks on the chunked path): the offset of its
 // first item and the total over the call, from one block-wide reduction over
 // the heads' counts.
-__device__ void head_span(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int hw,
-                          int u, int* s_red, int& begin, int& total) {
+template <bool MID>
+__device__ void head_span(const PoolView& pv, const SlotArgs& sa, int layer, bool paged, int wh, int wl, int wm,
+                          int hw, int u, int* s_red, int& begin, int& total) {
   const int n_units = sa.n * pv.hkv;
   int before = 0, all = 0;
   for (int v = threadIdx.x; v < n_units; v += blockDim.x) {
     const int* cn = pv.cnt(layer, sa.slots[v / pv.hkv], v % pv.hkv);
-    const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
-    const int items = head_items(pv, nh, nl, paged, wh, wl, hw);
+    const int nh = __ldcg(cn), nl = __ldcg(cn + 1), nm = MID ? __ldcg(cn + 4) : 0;
+    const int items = head_items(pv, nh, nl, nm, paged, wh, wl, wm, hw);
     all += items;
     if (v < u) before += items;
   }
@@ -1252,12 +1289,46 @@ __device__ __noinline__ void empty_head(float* out, float* lse2, int G) {
 constexpr int kPosRegs = 8;
 static_assert(epi_chunks(1) * kChunk / kEpiThreads <= kPosRegs, "position registers");
 
+// Geometry and table entry of a tier's page (MID: the pool has the mid tier;
+// a two-tier instance chooses between hi and lo only).
+template <bool MID>
+__device__ __forceinline__ const TierGeom& tier_geom(const PoolView& pv, int tier) {
+  return MID ? pv.geom(tier) : (tier == kTierHi ? pv.hi : pv.lo);
+}
+template <bool MID>
+__device__ __forceinline__ int tier_entry(const PoolView& pv, int tier, int k) {
+  return MID ? pv.entry(tier, k) : (tier == kTierHi ? k : pv.L - 1 - k);
+}
+
+// The chunks of a head's epilogue rows: its hi chunks, then its mid chunks
+// (three-tier pools, MID), then its lo chunks.
+template <bool MID>
+struct HeadChunks {
+  int ch_hi, ch_mid, nh, nm, nl;
+  // tier of chunk lc, the tier slot of its first row and the tier's tokens
+  __device__ __forceinline__ int tier(int lc, int& slot0, int& n) const {
+    if (lc < ch_hi) {
+      slot0 = lc * kChunk;
+      n = nh;
+      return kTierHi;
+    }
+    if (MID && lc < ch_hi + ch_mid) {
+      slot0 = (lc - ch_hi) * kChunk;
+      n = nm;
+      return kTierMid;
+    }
+    slot0 = (lc - ch_hi - ch_mid) * kChunk;
+    n = nl;
+    return kTierLo;
+  }
+};
+
 // Positions of this thread's slots in chunk step `step` of the head, in the
 // order the score-update loops visit them (0 where a slot is not stored).
 // Read from the pages through the table, neither of which the call changes.
-template <int EC>
+template <int EC, bool MID>
 __device__ __forceinline__ void load_positions(const PoolView& pv, const int* row_tab, bool paged, int step, int nch,
-                                               int ch_hi, int nh, int nl, int* vp) {
+                                               const HeadChunks<MID>& hc, int* vp) {
   const int c0 = step * EC, c1 = min(nch, c0 + EC);
 #pragma unroll
   for (int e = 0; e < kPosRegs; e++) vp[e] = 0;
@@ -1267,12 +1338,13 @@ __device__ __forceinline__ void load_positions(const PoolView& pv, const int* ro
       const int x = k * kEpiThreads + threadIdx.x;
       const int lc = c0 + (x >> 2), j0 = 4 * (x & 3);
       if (lc >= c1) break;
-      const bool hi_t = lc < ch_hi;
-      const int s0 = (hi_t ? lc : lc - ch_hi) * kChunk + j0;
-      if (s0 >= (hi_t ? nh : nl)) continue;
-      const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+      int s0, n;
+      const int tier = hc.tier(lc, s0, n);
+      s0 += j0;
+      if (s0 >= n) continue;
+      const TierGeom& tg = tier_geom<MID>(pv, tier);
       const int d = tg.div(s0);
-      const int pid = __ldg(row_tab + (hi_t ? d : pv.L - 1 - d));
+      const int pid = __ldg(row_tab + tier_entry<MID>(pv, tier, d));
       const int4 p = __ldcg(reinterpret_cast<const int4*>(pv.page(pid) + tg.off[5]) + ((s0 - d * tg.t) >> 2));
       vp[4 * k] = p.x;
       vp[4 * k + 1] = p.y;
@@ -1285,18 +1357,19 @@ __device__ __forceinline__ void load_positions(const PoolView& pv, const int* ro
       const int x = k * kEpiThreads + threadIdx.x;
       const int lc = c0 + x / kChunk, j = x % kChunk;
       if (lc >= c1) break;
-      const bool hi_t = lc < ch_hi;
-      const int slot = (hi_t ? lc : lc - ch_hi) * kChunk + j;
-      if (slot >= (hi_t ? nh : nl)) continue;
-      const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+      int slot, n;
+      const int tier = hc.tier(lc, slot, n);
+      slot += j;
+      if (slot >= n) continue;
+      const TierGeom& tg = tier_geom<MID>(pv, tier);
       const int d = tg.div(slot);
-      const int pid = __ldg(row_tab + (hi_t ? d : pv.L - 1 - d));
+      const int pid = __ldg(row_tab + tier_entry<MID>(pv, tier, d));
       vp[k] = __ldcg(reinterpret_cast<const int*>(pv.page(pid) + tg.off[5]) + (slot - d * tg.t));
     }
   }
 }
 
-template <int G>
+template <int G, bool MID>
 __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnArgs a, SlotArgs sa) {
   if (pv.noop()) return;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -1307,13 +1380,15 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   const bool paged = a.paged != 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int* cn = pv.cnt(a.layer, sa.slots[i], kvh);
-  const int nh = __ldcg(cn), nl = __ldcg(cn + 1);
-  if (nh + nl == 0) {             // an empty head: zero output, lse2 = -inf
+  const int nh = __ldcg(cn), nl = __ldcg(cn + 1), nm = MID ? __ldcg(cn + 4) : 0;
+  if (nh + nl + nm == 0) {        // an empty head: zero output, lse2 = -inf
     if (xb == 0)
       empty_head(a.out + ((size_t)i * pv.hkv + kvh) * G * kD, a.lse2 + (size_t)u * G, G);
     return;
   }
-  const int ch_hi = (nh + kChunk - 1) / kChunk, nch = ch_hi + (nl + kChunk - 1) / kChunk;
+  const int ch_hi = (nh + kChunk - 1) / kChunk, ch_mid = MID ? (nm + kChunk - 1) / kChunk : 0;
+  const int nch = ch_hi + ch_mid + (nl + kChunk - 1) / kChunk;
+  const HeadChunks<MID> hc{ch_hi, ch_mid, nh, nm, nl};
   // blocks of the head: with score updates one per chunk step of EC chunks
   // up to the grid's width (block x takes steps x, x + nb, ...), else every
   // block
@@ -1323,13 +1398,15 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   // the head's partial count in the attention kernels' range partition
   const int wh = paged ? page_cost(G, pv.hi.t / kChunk) : 1;
   const int wl = paged ? page_cost(G, pv.lo.t / kChunk) : 1;
+  const int wm = MID ? page_cost(G, pv.mid.t / kChunk) : 0;
   const int hw = paged ? head_cost(G) : 0;
   int begin, total;
-  head_span(pv, sa, a.layer, paged, wh, wl, hw, u, s_red, begin, total);
-  const int items = head_items(pv, nh, nl, paged, wh, wl, hw);
-  const int C = range_width(total, a.nwarps, paged, wh, wl);
+  head_span<MID>(pv, sa, a.layer, paged, wh, wl, wm, hw, u, s_red, begin, total);
+  const int items = head_items(pv, nh, nl, nm, paged, wh, wl, wm, hw);
+  const int C = range_width(total, a.nwarps, paged, wh, max(wl, wm));
   const int first = (begin + hw) / C;
-  const int last = paged ? (begin + items - (nl > 0 ? wl : wh)) / C : (begin + items - 1) / C;
+  // the partial of the warp that owns the head's last page (lo, else mid, else hi)
+  const int last = paged ? (begin + items - (nl > 0 ? wl : (nm > 0 ? wm : wh))) / C : (begin + items - 1) / C;
   const int np = last - first + 1;
   const EpiSmem L(G, a.update != 0);
   // With score updates the block also leaves victim keys (pool scratch only);
@@ -1337,12 +1414,12 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   // table and the pages' position segments do not change in this call.
   __shared__ int s_xc, s_last;
   __shared__ float s_ic;
-  __shared__ ArgMin s_amin[2 * kEpiWarps];
+  __shared__ ArgMin s_amin[(MID ? 3 : 2) * kEpiWarps];
   const bool victims = a.update && a.vpart != nullptr && nb <= a.max_vparts;
   const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
   int vp[kPosRegs];
   if (victims) {
-    load_positions<EC>(pv, row_tab, paged, xb, nch, ch_hi, nh, nl, vp);
+    load_positions<EC, MID>(pv, row_tab, paged, xb, nch, hc, vp);
     if (threadIdx.x == 0) s_xc = -1;
   }
   float* s_rows = reinterpret_cast<float*>(smem + L.rows);
@@ -1396,7 +1473,7 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
     vupd = __ldcg(rq + 3);
   }
   const int vpc = vN - pv.window, vwlim = vN + 1 - pv.window;
-  ArgMin bh{~0ull, -1}, bl{~0ull, -1};
+  ArgMin bh{~0ull, -1}, bl{~0ull, -1}, bm{~0ull, -1};
   int xc = -1;
   float ic = 0.0f;
   for (int step = xb, it = 0; step < nsteps; step += nb, it++) {
@@ -1411,7 +1488,7 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
     }
     // the positions of the block's next step, in flight during this one
     int vq[kPosRegs];
-    if (victims && step + nb < nsteps) load_positions<EC>(pv, row_tab, paged, step + nb, nch, ch_hi, nh, nl, vq);
+    if (victims && step + nb < nsteps) load_positions<EC, MID>(pv, row_tab, paged, step + nb, nch, hc, vq);
     // one decision for the block, so that no thread is left at a barrier
     if (__syncthreads_or(!mbar_wait_bounded(bar, it & 1))) {
       if (threadIdx.x == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = u;
@@ -1427,9 +1504,10 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
         const int x = k * kEpiThreads + threadIdx.x;
         const int lc = c0 + (x >> 2), j0 = 4 * (x & 3);
         if (lc >= c1) break;
-        const bool hi_t = lc < ch_hi;
-        const int s0 = (hi_t ? lc : lc - ch_hi) * kChunk + j0;
-        const int n = (hi_t ? nh : nl) - s0;      // valid slots among the four
+        int s0, nt;
+        const int tier = hc.tier(lc, s0, nt);
+        s0 += j0;
+        const int n = nt - s0;                    // valid slots among the four
         if (n <= 0) continue;
         const float* row = s_rows + (size_t)(lc - c0) * a.lrow;
         float4 mx = *reinterpret_cast<const float4*>(row + j0);
@@ -1444,7 +1522,7 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
         }
         const float4 old = *reinterpret_cast<const float4*>(row + G * kChunk + j0);
         const int pid = reinterpret_cast<const int*>(row)[(G + 1) * kChunk];
-        const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+        const TierGeom& tg = tier_geom<MID>(pv, tier);
         float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (s0 - tg.div(s0) * tg.t);
         const float4 nw = make_float4(old.x + fast_exp2(mx.x), old.y + fast_exp2(mx.y), old.z + fast_exp2(mx.z),
                                       old.w + fast_exp2(mx.w));
@@ -1456,10 +1534,10 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
           if (n > 2) sp[2] = nw.z;
         }
         if (victims) {
-          victim_token(nw.x, vp[4 * k], s0, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
-          if (n > 1) victim_token(nw.y, vp[4 * k + 1], s0 + 1, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
-          if (n > 2) victim_token(nw.z, vp[4 * k + 2], s0 + 2, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
-          if (n > 3) victim_token(nw.w, vp[4 * k + 3], s0 + 3, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
+          victim_token(nw.x, vp[4 * k], s0, tier, vn0, vupd, vpc, vwlim, bh, bl, bm, xc, ic);
+          if (n > 1) victim_token(nw.y, vp[4 * k + 1], s0 + 1, tier, vn0, vupd, vpc, vwlim, bh, bl, bm, xc, ic);
+          if (n > 2) victim_token(nw.z, vp[4 * k + 2], s0 + 2, tier, vn0, vupd, vpc, vwlim, bh, bl, bm, xc, ic);
+          if (n > 3) victim_token(nw.w, vp[4 * k + 3], s0 + 3, tier, vn0, vupd, vpc, vwlim, bh, bl, bm, xc, ic);
         }
       }
     } else {
@@ -1468,21 +1546,22 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
         const int x = k * kEpiThreads + threadIdx.x;
         const int lc = c0 + x / kChunk, j = x % kChunk;
         if (lc >= c1) break;
-        const bool hi_t = lc < ch_hi;
-        const int slot = (hi_t ? lc : lc - ch_hi) * kChunk + j;
-        if (slot >= (hi_t ? nh : nl)) continue;
+        int slot, nt;
+        const int tier = hc.tier(lc, slot, nt);
+        slot += j;
+        if (slot >= nt) continue;
         const float* row = s_rows + (size_t)(lc - c0) * a.lrow;
         float pm = 0.0f;
 #pragma unroll
         for (int qh = 0; qh < G; qh++) pm = fmaxf(pm, fast_exp2(row[qh * kChunk + j] - lse[qh]));
         // chunked path: page from the table, old score from the page
-        const TierGeom& tg = hi_t ? pv.hi : pv.lo;
+        const TierGeom& tg = tier_geom<MID>(pv, tier);
         const int d = tg.div(slot);
-        const int pid = __ldcg(row_tab + (hi_t ? d : pv.L - 1 - d));
+        const int pid = __ldcg(row_tab + tier_entry<MID>(pv, tier, d));
         float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (slot - d * tg.t);
         const float ns = __ldcg(sp) + pm;
         *sp = ns;
-        if (victims) victim_token(ns, vp[k], slot, hi_t, vn0, vupd, vpc, vwlim, bh, bl, xc, ic);
+        if (victims) victim_token(ns, vp[k], slot, tier, vn0, vupd, vpc, vwlim, bh, bl, bm, xc, ic);
       }
     }
 #pragma unroll
@@ -1496,13 +1575,16 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
     s_xc = xc;
     s_ic = ic;
   }
-  block_amin2(bh, bl, s_amin);
+  if (MID) block_amin3(bh, bl, bm, s_amin);
+  else block_amin2(bh, bl, s_amin);
   if (threadIdx.x == 0) {
     ScanPart& part = a.vpart[(size_t)u * a.max_vparts + xb];
     part.kh = bh.key;
     part.sh = bh.slot;
     part.kl = bl.key;
     part.sl = bl.slot;
+    part.km = bm.key;
+    part.sm = bm.slot;
     part.xc = s_xc;
     part.ic = s_ic;
     __threadfence();
@@ -1511,13 +1593,14 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   __syncthreads();
   if (!s_last || warp != 0) return;
   __threadfence();
-  ArgMin rh{~0ull, -1}, rl{~0ull, -1};
+  ArgMin rh{~0ull, -1}, rl{~0ull, -1}, rm{~0ull, -1};
   int rx = -1;
   float ri = 0.0f;
   for (int q = lane; q < nb; q += 32) {
     const ScanPart* part = a.vpart + (size_t)u * a.max_vparts + q;
     rh = amin(rh, ArgMin{__ldcg(&part->kh), __ldcg(&part->sh)});
     rl = amin(rl, ArgMin{__ldcg(&part->kl), __ldcg(&part->sl)});
+    if (MID) rm = amin(rm, ArgMin{__ldcg(&part->km), __ldcg(&part->sm)});
     const int pxc = __ldcg(&part->xc);
     if (pxc >= 0) {
       rx = pxc;
@@ -1528,6 +1611,7 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   for (int sft = 16; sft >= 1; sft >>= 1) {
     rh = shfl_amin(rh, sft);
     rl = shfl_amin(rl, sft);
+    if (MID) rm = shfl_amin(rm, sft);
   }
   const unsigned has = __ballot_sync(0xffffffffu, rx >= 0);
   const int src = has ? __ffs(has) - 1 : 0;
@@ -1536,7 +1620,7 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   if (lane == 0) {
     a.varrive[u] = 0;             // ready for the next call
     VictimCache* vc = pv.vc(a.layer, sa.slots[i], kvh);
-    vc->p = ScanPart{rh.key, rl.key, rh.slot, rl.slot, rx, ri};
+    vc->p = ScanPart{rh.key, rl.key, rh.slot, rl.slot, rx, ri, rm.key, rm.slot, 0};
     vc->n_stamp = vN;
     vc->u_stamp = vupd;
   }
@@ -1555,6 +1639,34 @@ static int pages_per_chunk(int t) {
   return m;
 }
 
+// The paged attention kernel for the pool's group size and tier count.
+template <bool MID>
+static cudaError_t launch_paged(Pool& P, const AttnArgs& a, const SlotArgs& sa, int w, dim3 grid, dim3 block,
+                                int smem, cudaStream_t st) {
+  if (w != kWarpsPerSm)
+    return launch_dependent(k_attn_paged<kAttnWarps, 0, MID>, grid, block, (size_t)smem, st, P.pv, a, sa);
+  if (P.pv.G == 4)
+    return launch_dependent(k_attn_paged<kWarpsPerSm, 4, MID>, grid, block, (size_t)smem, st, P.pv, a, sa);
+  if (P.pv.G == 8)
+    return launch_dependent(k_attn_paged<kWarpsPerSm, 8, MID>, grid, block, (size_t)smem, st, P.pv, a, sa);
+  return launch_dependent(k_attn_paged<kWarpsPerSm, 0, MID>, grid, block, (size_t)smem, st, P.pv, a, sa);
+}
+
+// The epilogue for group size G.
+template <bool MID>
+static cudaError_t launch_epi(cudaLaunchConfig_t& lc, int G, Pool& P, const AttnArgs& a, const SlotArgs& sa) {
+  switch (G) {
+    case 1: return cudaLaunchKernelEx(&lc, k_attn_epi<1, MID>, P.pv, a, sa);
+    case 2: return cudaLaunchKernelEx(&lc, k_attn_epi<2, MID>, P.pv, a, sa);
+    case 3: return cudaLaunchKernelEx(&lc, k_attn_epi<3, MID>, P.pv, a, sa);
+    case 4: return cudaLaunchKernelEx(&lc, k_attn_epi<4, MID>, P.pv, a, sa);
+    case 5: return cudaLaunchKernelEx(&lc, k_attn_epi<5, MID>, P.pv, a, sa);
+    case 6: return cudaLaunchKernelEx(&lc, k_attn_epi<6, MID>, P.pv, a, sa);
+    case 7: return cudaLaunchKernelEx(&lc, k_attn_epi<7, MID>, P.pv, a, sa);
+    default: return cudaLaunchKernelEx(&lc, k_attn_epi<8, MID>, P.pv, a, sa);
+  }
+}
+
 // Launch the attention kernel of the pool's page geometry, then the epilogue
 // kernel (merge and score update) as its programmatic dependent, over the
 // scratch that `a` points to.
@@ -1566,6 +1678,7 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
     a.mseg = 0;
     a.maxp = 1;
     a.stage_bytes = std::max(P.pv.hi.off[5], P.pv.lo.off[5]);
+    if (P.pv.mid_enabled) a.stage_bytes = std::max(a.stage_bytes, P.pv.mid.off[5]);
     // per warp its page ring with mbarriers and its descriptor table; the head prefix
     auto need = [&](int warps) { return warps * (kPageStages * (a.stage_bytes + 8) + 64 * 16) + 4 * (n_units + 1); };
     w = need(kWarpsPerSm) <= kMaxAttnSmem ? kWarpsPerSm : kAttnWarps;
@@ -1585,14 +1698,10 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   cudaError_t e;
   if (!paged)
     e = launch_dependent(k_attn_decode, grid, block, (size_t)smem, st, P.pv, a, sa);
-  else if (w != kWarpsPerSm)
-    e = launch_dependent(k_attn_paged<kAttnWarps, 0>, grid, block, (size_t)smem, st, P.pv, a, sa);
-  else if (P.pv.G == 4)
-    e = launch_dependent(k_attn_paged<kWarpsPerSm, 4>, grid, block, (size_t)smem, st, P.pv, a, sa);
-  else if (P.pv.G == 8)
-    e = launch_dependent(k_attn_paged<kWarpsPerSm, 8>, grid, block, (size_t)smem, st, P.pv, a, sa);
+  else if (P.pv.mid_enabled)
+    e = launch_paged<true>(P, a, sa, w, grid, block, smem, st);
   else
-    e = launch_dependent(k_attn_paged<kWarpsPerSm, 0>, grid, block, (size_t)smem, st, P.pv, a, sa);
+    e = launch_paged<false>(P, a, sa, w, grid, block, smem, st);
   if (e != cudaSuccess) return e;
   // epilogue: merge and (with score updates) the new scores
   const int G = P.pv.G;
@@ -1601,7 +1710,7 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   if (a.update) {
     // chunk steps of the call's longest head, at most one wave of blocks
     // (four per SM) over all heads
-    const int call_chunks = (max_tokens + kChunk - 1) / kChunk + 1;
+    const int call_chunks = (max_tokens + kChunk - 1) / kChunk + (P.pv.mid_enabled ? 2 : 1);
     const int steps = (call_chunks + epi_chunks(G) - 1) / epi_chunks(G);
     gx = (unsigned)std::max(1, std::min(steps, 4 * P.sm_count / std::max(1, n_units)));
   } else {
@@ -1617,16 +1726,7 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  switch (G) {
-    case 1: e = cudaLaunchKernelEx(&lc, k_attn_epi<1>, P.pv, a, sa); break;
-    case 2: e = cudaLaunchKernelEx(&lc, k_attn_epi<2>, P.pv, a, sa); break;
-    case 3: e = cudaLaunchKernelEx(&lc, k_attn_epi<3>, P.pv, a, sa); break;
-    case 4: e = cudaLaunchKernelEx(&lc, k_attn_epi<4>, P.pv, a, sa); break;
-    case 5: e = cudaLaunchKernelEx(&lc, k_attn_epi<5>, P.pv, a, sa); break;
-    case 6: e = cudaLaunchKernelEx(&lc, k_attn_epi<6>, P.pv, a, sa); break;
-    case 7: e = cudaLaunchKernelEx(&lc, k_attn_epi<7>, P.pv, a, sa); break;
-    default: e = cudaLaunchKernelEx(&lc, k_attn_epi<8>, P.pv, a, sa); break;
-  }
+  e = P.pv.mid_enabled ? launch_epi<true>(lc, G, P, a, sa) : launch_epi<false>(lc, G, P, a, sa);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1670,9 +1770,10 @@ struct StaticLayout {
   int max_parts, max_chunks;
 };
 
-StaticLayout static_layout(int n_units, int G, int max_tokens, int update_scores) {
+StaticLayout static_layout(int n_units, int G, int max_tokens, int update_scores, bool mid) {
   StaticLayout L;
-  L.max_chunks = (max_tokens + kChunk - 1) / kChunk + 1;
+  // a head's chunks: each tier's tokens rounded up to 16
+  L.max_chunks = (max_tokens + kChunk - 1) / kChunk + (mid ? 2 : 1);
   L.max_parts = L.max_chunks / kMinChunks + 2;   // warps over one head (ranges >= kMinChunks)
   size_t off = 0;
   L.lse2 = off;
@@ -1697,13 +1798,13 @@ cudaError_t static_scratch_address(void** base) {
 }
 
 size_t attention_static_bytes(const Pool& P, int n_units, int max_tokens, int update_scores) {
-  return static_layout(n_units, P.pv.G, max_tokens, update_scores).total;
+  return static_layout(n_units, P.pv.G, max_tokens, update_scores, P.pv.mid_enabled != 0).total;
 }
 
 cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int max_tokens, const __half* q,
                                     float* out, int update_scores, cudaStream_t st) {
   const int n_units = sa.n * P.pv.hkv;
-  const StaticLayout L = static_layout(n_units, P.pv.G, max_tokens, update_scores);
+  const StaticLayout L = static_layout(n_units, P.pv.G, max_tokens, update_scores, P.pv.mid_enabled != 0);
   if (L.total > DKV_ATTN_STATIC_SCRATCH_BYTES) return cudaErrorInvalidValue;
   uint8_t* base = static_cast<uint8_t*>(P.static_base);
   if (base == nullptr) return cudaErrorInvalidSymbol;
@@ -1725,16 +1826,26 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
   return launch_kernels(P, a, sa, max_tokens, st);
 }
 
+template <bool MID>
+static void attention_fns(std::vector<const void*>& fns) {
+  fns.push_back(reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 4, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 8, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 0, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_paged<kAttnWarps, 0, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_epi<1, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_epi<2, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_epi<3, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_epi<4, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_epi<5, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_epi<6, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_epi<7, MID>));
+  fns.push_back(reinterpret_cast<const void*>(k_attn_epi<8, MID>));
+}
+
 cudaError_t configure_attention() {
-  const void* fns[] = {reinterpret_cast<const void*>(k_attn_decode),
-                       reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 4>),
-                       reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 8>),
-                       reinterpret_cast<const void*>(k_attn_paged<kWarpsPerSm, 0>),
-                       reinterpret_cast<const void*>(k_attn_paged<kAttnWarps, 0>),
-                       reinterpret_cast<const void*>(k_attn_epi<1>), reinterpret_cast<const void*>(k_attn_epi<2>),
-                       reinterpret_cast<const void*>(k_attn_epi<3>), reinterpret_cast<const void*>(k_attn_epi<4>),
-                       reinterpret_cast<const void*>(k_attn_epi<5>), reinterpret_cast<const void*>(k_attn_epi<6>),
-                       reinterpret_cast<const void*>(k_attn_epi<7>), reinterpret_cast<const void*>(k_attn_epi<8>)};
+  std::vector<const void*> fns{reinterpret_cast<const void*>(k_attn_decode)};
+  attention_fns<false>(fns);
+  attention_fns<true>(fns);
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxAttnSmem);
     if (e != cudaSuccess) return e;

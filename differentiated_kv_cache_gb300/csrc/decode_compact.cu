@@ -3,9 +3,11 @@
 // workflow). One token per step per head:
 //   1. the newest token enters the recent window, quantized hi;
 //   2. the window's oldest token t_c is classified against alpha_h/N and
-//      alpha_l/N: it stays hi, is re-quantized to lo, or is pruned;
+//      alpha_l/N (and alpha_m/N in a three-tier pool): it stays hi, is
+//      re-quantized to lo (or mid), or is pruned;
 //   3. if t_c was kept, the least important token t_v of its tier (hi: outside
-//      the window) is considered for demotion (hi -> lo) or pruning.
+//      the window) is considered for demotion (to the tier it classifies at)
+//      or pruning.
 // Removal from a tier fills the hole with the tier's last token. The per-head
 // plan is made by k_decode_plan; pages are granted by k_decode_alloc
 // (alloc.cu); k_decode_apply writes the token slots.
@@ -30,57 +32,76 @@ __device__ __forceinline__ float key_importance(unsigned long long key) {
 // and makes the plan.
 constexpr int kScanSlots = kPlanThreads * 8;   // 2048: the pool sizes its scan partials with it
 
-// The plan of one head from the reduced scan (thread 0 of the last CTA).
-__device__ void decide_plan(const PoolView& pv, int layer, int slot, int kvh, int unit, ArgMin bh, ArgMin bl, int xc_in,
-                            float ic_in, DecodePlan* plans) {
+// The plan of one head from the reduced scan (thread 0 of the last CTA):
+// bh / bl / bm the least important hi token outside the window, lo token and
+// mid token (three-tier pools, MID), xc / ic the hi slot and importance of t_c.
+template <bool MID>
+__device__ void decide_plan(const PoolView& pv, int layer, int slot, int kvh, int unit, ArgMin bh, ArgMin bl, ArgMin bm,
+                            int xc_in, float ic_in, DecodePlan* plans) {
   const int* rq = pv.rq(layer, slot);
   const int n = rq[2] + 1;
   const int* cn = pv.cnt(layer, slot, kvh);
   const int nh = cn[0], nl = cn[1], php = cn[2], plp = cn[3];
+  constexpr bool three = MID;
+  const int nm = three ? cn[4] : 0, pmp = three ? cn[5] : 0;
   const int pc = n - pv.window - 1;
   int s_xc = xc_in;
   float s_ic = ic_in;
   const float2 al = pv.thresholds(layer, kvh);   // the head's pair
   const float th_h = __fdiv_rn(al.x, (float)n), th_l = __fdiv_rn(al.y, (float)n);
+  const float th_m = three ? __fdiv_rn(pv.alpha_m[(size_t)layer * pv.hkv + kvh], (float)n) : 0.0f;
+  auto cls = [&](float imp) { return three ? classify3(imp, th_h, th_m, th_l) : classify(imp, th_h, th_l, pv.lo_enabled); };
   DecodePlan p;
   p.err = 0;
   p.n_moves = 0;
-  int nh2 = nh + 1, nl2 = nl;                 // (1) newest token appended at hi slot nh
-  Move newmv{kTierHi, nh, kSrcNew, -1};
+  int nh2 = nh + 1, nl2 = nl, nm2 = nm;       // (1) newest token appended at hi slot nh
+  Move newmv{kTierHi, nh, kSrcNew, -1, kTierHi};
   if (pc >= 0) {
     const int xc = s_xc;
     if (xc < 0) {
       p.err = DKV_ERR_CHECK;
     } else {
-      const int tc = classify(s_ic, th_h, th_l, pv.lo_enabled);
+      const int tc = cls(s_ic);
       if (tc == kTierHi) {
-        // (3) hi victim: least important hi token outside the window (t_c included)
+        // (3) hi victim: least important hi token outside the window (t_c
+        // included); kept unless it classifies lower
         const int xv = bh.slot;
-        const float iv = key_importance(bh.key);
-        const bool keep = pv.lo_enabled ? (iv > th_h) : (iv >= th_l);
-        if (!keep) {
+        const int cv = cls(key_importance(bh.key));
+        if (cv != kTierHi) {
           newmv.dst_slot = xv;                // last (newest) token fills the hole
           nh2 = nh;
-          if (pv.lo_enabled && iv >= th_l) {
-            p.mv[p.n_moves++] = Move{kTierLo, nl, kSrcDemote, xv};
+          if (cv == kTierLo) {
+            p.mv[p.n_moves++] = Move{kTierLo, nl, kSrcDemote, xv, kTierHi};
             nl2 = nl + 1;
+          } else if (cv == kTierMid) {
+            p.mv[p.n_moves++] = Move{kTierMid, nm, kSrcDemote, xv, kTierHi};
+            nm2 = nm + 1;
           }
         }
-      } else if (tc == kTierLo) {
+      } else if (tc == kTierLo || tc == kTierMid) {
         newmv.dst_slot = xc;                  // t_c leaves hi; the newest token fills it
         nh2 = nh;
-        // t_c re-quantized and appended to lo at slot nl; lo victim over lo + t_c
+        // t_c re-quantized and appended to its tier; that tier's victim over
+        // its tokens and t_c
+        const ArgMin bt = tc == kTierLo ? bl : bm;
+        const int nt = tc == kTierLo ? nl : nm;
         const unsigned long long kc = ((unsigned long long)order_key(s_ic) << 32) | (uint32_t)pc;
-        const bool tc_min = (bl.slot < 0) || (kc < bl.key);
-        const float iv = tc_min ? s_ic : key_importance(bl.key);
-        if (iv < th_l) {
-          if (!tc_min) p.mv[p.n_moves++] = Move{kTierLo, bl.slot, kSrcDemote, xc};
-          nl2 = nl;                           // victim pruned (t_c itself, or the victim's
-                                              // slot refilled with t_c)
+        const bool tc_min = (bt.slot < 0) || (kc < bt.key);
+        // t_c as the victim classifies at its own tier and stays
+        const int cv = tc_min ? tc : cls(key_importance(bt.key));
+        int nt2 = nt + 1;
+        if (tier_rank(cv) < tier_rank(tc)) {
+          // the victim leaves the tier; t_c fills its slot
+          p.mv[p.n_moves++] = Move{tc, bt.slot, kSrcDemote, xc, kTierHi};
+          nt2 = nt;
+          if (cv == kTierLo) {                // a mid victim demoted to lo
+            p.mv[p.n_moves++] = Move{kTierLo, nl, kSrcDemote, bt.slot, kTierMid};
+            nl2 = nl + 1;
+          }
         } else {
-          p.mv[p.n_moves++] = Move{kTierLo, nl, kSrcDemote, xc};
-          nl2 = nl + 1;
+          p.mv[p.n_moves++] = Move{tc, nt, kSrcDemote, xc, kTierHi};
         }
+        if (tc == kTierLo) nl2 = nt2; else nm2 = nt2;
       } else {
         newmv.dst_slot = xc;                  // t_c pruned
         nh2 = nh;
@@ -91,24 +112,33 @@ __device__ void decide_plan(const PoolView& pv, int layer, int slot, int kvh, in
   p.mv[p.n_moves++] = newmv;
   p.nh = nh2;
   p.nl = nl2;
+  p.nm = nm2;
   const int need_h = (nh2 + pv.hi.t - 1) / pv.hi.t, need_l = (nl2 + pv.lo.t - 1) / pv.lo.t;
-  p.new_hp = p.new_lp = p.free_hp = p.free_lp = 0;
+  p.new_hp = p.new_lp = p.free_hp = p.free_lp = p.new_mp = p.free_mp = 0;
   p.php = php;
   p.plp = plp;
+  p.pmp = pmp;
   if (need_h > php) { p.new_hp = need_h - php; p.php = need_h; }
   else if (pv.reclaim && need_h < php) { p.free_hp = php - need_h; p.php = need_h; }
   if (need_l > plp) { p.new_lp = need_l - plp; p.plp = need_l; }
   else if (pv.reclaim && need_l < plp) { p.free_lp = plp - need_l; p.plp = need_l; }
-  if (p.err == 0 && p.php + p.plp > pv.L) p.err = DKV_ERR_TABLE_FULL;
+  if (three) {
+    const int need_m = (nm2 + pv.mid.t - 1) / pv.mid.t;
+    if (need_m > pmp) { p.new_mp = need_m - pmp; p.pmp = need_m; }
+    else if (pv.reclaim && need_m < pmp) { p.free_mp = pmp - need_m; p.pmp = need_m; }
+  }
+  if (p.err == 0 && (p.php + p.plp > pv.L || p.pmp > pv.Lm)) p.err = DKV_ERR_TABLE_FULL;
   plans[unit] = p;
 }
 
+// MID: a three-tier pool (the two-tier instance compiles the mid tier out)
+template <bool MID>
 __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int layer, DecodePlan* plans,
                                                                ScanPart* parts, int* arrivals, int max_parts,
                                                                SlotArgs sa) {
   pdl_launch_dependents();        // k_decode_alloc may launch; it waits for this grid
   if (pv.noop()) return;
-  __shared__ ArgMin s_tmp[2 * (kPlanThreads / 32)];
+  __shared__ ArgMin s_tmp[(MID ? 3 : 2) * (kPlanThreads / 32)];
   __shared__ int s_xc, s_last;
   __shared__ float s_ic;
   const int c = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
@@ -117,7 +147,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
   const int* rq = pv.rq(layer, slot);
   const int n0 = rq[1], n = rq[2] + 1, upd = rq[3];
   const int* cn = pv.cnt(layer, slot, kvh);
-  const int nh = cn[0], nl = cn[1];
+  const int nh = cn[0], nl = cn[1], nm = MID ? cn[4] : 0;
   // The victim keys the last decode-attention call's score update left for
   // this head, while the head is as that call left it (same length, same
   // update count): no scan. The condition is the same for every thread.
@@ -125,18 +155,20 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
   if (__ldcg(&vc->n_stamp) == rq[2] && __ldcg(&vc->u_stamp) == upd) {
     if (c == 0 && threadIdx.x == 0) {
       const ArgMin ch{__ldcg(&vc->p.kh), __ldcg(&vc->p.sh)}, cl{__ldcg(&vc->p.kl), __ldcg(&vc->p.sl)};
-      decide_plan(pv, layer, slot, kvh, unit, ch, cl, __ldcg(&vc->p.xc), __ldcg(&vc->p.ic), plans);
+      const ArgMin cm = MID ? ArgMin{__ldcg(&vc->p.km), __ldcg(&vc->p.sm)} : ArgMin{~0ull, -1};
+      decide_plan<MID>(pv, layer, slot, kvh, unit, ch, cl, cm, __ldcg(&vc->p.xc), __ldcg(&vc->p.ic), plans);
     }
     return;
   }
-  const int nparts = max(1, (nh + nl + kScanSlots - 1) / kScanSlots);
+  const int nst = nh + nl + nm;             // slots: hi, then lo, then mid
+  const int nparts = max(1, (nst + kScanSlots - 1) / kScanSlots);
   if (c >= nparts) return;
   const int* row = pv.row(layer, slot, kvh);
   const int pc = n - pv.window - 1;         // position of t_c
   const int wlim = n - pv.window;           // hi victims: position < wlim
   if (threadIdx.x == 0) { s_xc = -1; s_ic = 0.0f; }
   __syncthreads();
-  ArgMin bh{~0ull, -1}, bl{~0ull, -1};
+  ArgMin bh{~0ull, -1}, bl{~0ull, -1}, bm{~0ull, -1};
   // slots c*kScanSlots + k*kPlanThreads + tid: consecutive threads read
   // consecutive score / position entries of a page
   float sc[8];
@@ -147,12 +179,12 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
     sl[k] = -1;
     sc[k] = 0.0f;
     pos[k] = 0;
-    if (x >= nh + nl) continue;
-    const bool hi = x < nh;
-    const int s = hi ? x : x - nh;
-    const TierGeom& tg = hi ? pv.hi : pv.lo;
+    if (x >= nst) continue;
+    const int tier = x < nh ? kTierHi : (!MID || x < nh + nl ? kTierLo : kTierMid);
+    const int s = x < nh ? x : (!MID || x < nh + nl ? x - nh : x - nh - nl);
+    const TierGeom& tg = pv.geom(tier);
     const int d = tg.div(s);
-    const uint8_t* pg = pv.page(__ldg(row + (hi ? d : pv.L - 1 - d)));
+    const uint8_t* pg = pv.page(__ldg(row + pv.entry(tier, d)));
     sc[k] = *reinterpret_cast<const float*>(pg + tg.off[4] + 4 * (s - d * tg.t));
     pos[k] = *reinterpret_cast<const int*>(pg + tg.off[5] + 4 * (s - d * tg.t));
     sl[k] = x;
@@ -165,15 +197,19 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
     if (sl[k] < nh) {
       if (pos[k] == pc) { s_xc = sl[k]; s_ic = imp; }
       if (pos[k] < wlim) bh = amin(bh, ArgMin{key, sl[k]});
-    } else {
+    } else if (!MID || sl[k] < nh + nl) {
       bl = amin(bl, ArgMin{key, sl[k] - nh});
+    } else {
+      bm = amin(bm, ArgMin{key, sl[k] - nh - nl});
     }
   }
-  block_amin2(bh, bl, s_tmp);
+  if (MID) block_amin3(bh, bl, bm, s_tmp);
+  else block_amin2(bh, bl, s_tmp);
   if (threadIdx.x == 0) {
     ScanPart& part = parts[(size_t)unit * max_parts + c];
     part.kh = bh.key; part.sh = bh.slot;
     part.kl = bl.key; part.sl = bl.slot;
+    part.km = bm.key; part.sm = bm.slot;
     part.xc = s_xc; part.ic = s_ic;
     __threadfence();
     s_last = atomicAdd(arrivals + unit, 1) == nparts - 1;
@@ -182,7 +218,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
   if (!s_last || threadIdx.x != 0) return;
   __threadfence();
   arrivals[unit] = 0;                       // ready for the next step
-  ArgMin rh{~0ull, -1}, rl{~0ull, -1};
+  ArgMin rh{~0ull, -1}, rl{~0ull, -1}, rm{~0ull, -1};
   int xc = -1;
   float ic = 0.0f;
   for (int q = 0; q < nparts; q++) {
@@ -190,10 +226,11 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
     const ArgMin ph{__ldcg(&part.kh), __ldcg(&part.sh)}, pl{__ldcg(&part.kl), __ldcg(&part.sl)};
     rh = amin(rh, ph);
     rl = amin(rl, pl);
+    if (MID) rm = amin(rm, ArgMin{__ldcg(&part.km), __ldcg(&part.sm)});
     const int pxc = __ldcg(&part.xc);
     if (pxc >= 0) { xc = pxc; ic = __ldcg(&part.ic); }
   }
-  decide_plan(pv, layer, slot, kvh, unit, rh, rl, xc, ic, plans);
+  decide_plan<MID>(pv, layer, slot, kvh, unit, rh, rl, rm, xc, ic, plans);
 }
 
 // Token record staged in shared memory between the read and write phases.
@@ -225,6 +262,7 @@ __device__ __forceinline__ void warp_quantize(const float* x, int bits, uint8_t*
   if (lane == 0) *meta = (uint32_t)q.sh | ((uint32_t)q.zh << 16);
 }
 
+template <bool MID>
 __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, const DecodePlan* __restrict__ plans,
                                                       const __half* __restrict__ knew,
                                                       const __half* __restrict__ vnew, SlotArgs sa) {
@@ -254,28 +292,36 @@ __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, con
   const int n = pv.rq(layer, slot)[2];       // already advanced by k_decode_alloc
   if (threadIdx.x == 0) { st[2].score = 0.0f; st[2].pos = n - 1; }
   // read phase: warp m stages the source of move m when it is a demotion
+  // (the new token is always the last move, so m < 2)
   if (warp < p.n_moves && p.mv[warp].src != kSrcNew) {
     const Move mv = p.mv[warp];
     TokStage& s = st[warp];
     float kx[4], vx[4];
     {
-      // demote: dequantize the hi slot's codes, quantize again at lo precision
-      const uint8_t* pg = pv.page(row[mv.src_slot / pv.hi.t]);
-      const int ip = mv.src_slot % pv.hi.t;
-      const uint32_t km = *reinterpret_cast<const uint32_t*>(pg + pv.hi.off[2] + 4 * ip);
-      const uint32_t vm = *reinterpret_cast<const uint32_t*>(pg + pv.hi.off[3] + 4 * ip);
-      const uint32_t kw = *reinterpret_cast<const uint32_t*>(pg + pv.hi.off[0] + ip * pv.hi.kbytes + 4 * lane);
-      const uint32_t vw = *reinterpret_cast<const uint32_t*>(pg + pv.hi.off[1] + (ip / 2) * 128 + 4 * lane);
+      // demote: dequantize the source slot's codes (hi K8V4 or mid K8V2),
+      // quantize again at the destination's precision (mid K8V2, lo K4V2)
+      // a two-tier pool demotes hi -> lo only
+      const int src_tier = MID ? mv.src_tier : kTierHi, dst_tier = MID ? mv.dst_tier : kTierLo;
+      const TierGeom& sg = MID ? pv.geom(src_tier) : pv.hi;
+      const int svb = src_tier == kTierHi ? 4 : 2, sgsz = 8 / svb;
+      const int d = sg.div(mv.src_slot);
+      const uint8_t* pg = pv.page(row[MID ? pv.entry(src_tier, d) : d]);
+      const int ip = mv.src_slot - d * sg.t;
+      const uint32_t km = *reinterpret_cast<const uint32_t*>(pg + sg.off[2] + 4 * ip);
+      const uint32_t vm = *reinterpret_cast<const uint32_t*>(pg + sg.off[3] + 4 * ip);
+      const uint32_t kw = *reinterpret_cast<const uint32_t*>(pg + sg.off[0] + ip * sg.kbytes + 4 * lane);
+      const uint32_t vw = *reinterpret_cast<const uint32_t*>(pg + sg.off[1] + (ip / sgsz) * 128 + 4 * lane);
 #pragma unroll
       for (int e = 0; e < 4; e++) {
         kx[e] = dequant((uint16_t)km, (uint16_t)(km >> 16), (kw >> (8 * e)) & 255u);
-        vx[e] = dequant((uint16_t)vm, (uint16_t)(vm >> 16), (vw >> vbit(4, 4 * lane + e, ip & 1)) & 15u);
+        vx[e] = dequant((uint16_t)vm, (uint16_t)(vm >> 16),
+                        (vw >> vbit(svb, 4 * lane + e, ip % sgsz)) & ((1u << svb) - 1u));
       }
-      warp_quantize(kx, 4, s.kc, &s.kmeta);
+      warp_quantize(kx, dst_tier == kTierLo ? 4 : 8, s.kc, &s.kmeta);
       warp_quantize(vx, 2, s.vc, &s.vmeta);
       if (lane == 0) {
-        s.score = *reinterpret_cast<const float*>(pg + pv.hi.off[4] + 4 * ip);
-        s.pos = *reinterpret_cast<const int*>(pg + pv.hi.off[5] + 4 * ip);
+        s.score = *reinterpret_cast<const float*>(pg + sg.off[4] + 4 * ip);
+        s.pos = *reinterpret_cast<const int*>(pg + sg.off[5] + 4 * ip);
       }
     }
   }
@@ -285,20 +331,20 @@ __global__ void __launch_bounds__(64) k_decode_apply(PoolView pv, int layer, con
   for (int m = 0; m < p.n_moves; m++) {
     const Move mv = p.mv[m];
     const TokStage& s = st[mv.src == kSrcNew ? 2 : m];
-    const bool hi = mv.dst_tier == kTierHi;
-    const TierGeom& tg = hi ? pv.hi : pv.lo;
-    const int e_page = hi ? mv.dst_slot / tg.t : pv.L - 1 - mv.dst_slot / tg.t;
-    uint8_t* pg = pv.page(row[e_page]);
-    const int ip = mv.dst_slot % tg.t;
+    const int tier = mv.dst_tier;
+    const TierGeom& tg = MID ? pv.geom(tier) : (tier == kTierHi ? pv.hi : pv.lo);
+    const int d = tg.div(mv.dst_slot);
+    uint8_t* pg = pv.page(row[MID ? pv.entry(tier, d) : (tier == kTierHi ? d : pv.L - 1 - d)]);
+    const int ip = mv.dst_slot - d * tg.t;
     const uint8_t* kc = s.kc + 4 * lane;
-    if (hi) {
+    if (tier != kTierLo) {                    // 8-bit keys (hi, mid)
       *reinterpret_cast<uint32_t*>(pg + tg.off[0] + ip * 128 + 4 * lane) =
           kc[0] | (kc[1] << 8) | (kc[2] << 16) | ((uint32_t)kc[3] << 24);
     } else {
       *reinterpret_cast<uint16_t*>(pg + tg.off[0] + ip * 64 + 2 * lane) =
           (uint16_t)(kc[0] | (kc[1] << 4) | (kc[2] << 8) | (kc[3] << 12));
     }
-    const int vbits = hi ? 4 : 2, gsz = hi ? 2 : 4;
+    const int vbits = tier == kTierHi ? 4 : 2, gsz = tier == kTierHi ? 2 : 4;
     uint32_t* vw = reinterpret_cast<uint32_t*>(pg + tg.off[1] + (ip / gsz) * 128) + lane;
     uint32_t w = *vw;
     const uint32_t lmask = (1u << vbits) - 1u;
@@ -325,11 +371,15 @@ cudaError_t launch_decode(Pool& P, int layer, const SlotArgs& sa, const __half* 
   const dim3 grid(P.pv.hkv, sa.n);
   int max_n = 1;
   for (int i = 0; i < sa.n; i++) max_n = std::max(max_n, P.h_n[(size_t)layer * P.cfg.max_requests + sa.slots[i]]);
-  const int scan_ctas = (max_n + 1 + kScanSlots - 1) / kScanSlots;   // stored tokens <= N + 1
+  const int scan_ctas = (max_n + 1 + kScanSlots - 1) / kScanSlots;   // stored tokens of all tiers <= N + 1
   if (scan_ctas > P.sc.max_scan) return cudaErrorInvalidConfiguration;
   const dim3 gscan(scan_ctas, P.pv.hkv, sa.n);
-  k_decode_plan<<<gscan, kPlanThreads, 0, st>>>(P.pv, layer, P.sc.dplan, P.sc.dscan, P.sc.darrive, P.sc.max_scan,
-                                                 sa);
+  if (P.pv.mid_enabled)
+    k_decode_plan<true><<<gscan, kPlanThreads, 0, st>>>(P.pv, layer, P.sc.dplan, P.sc.dscan, P.sc.darrive,
+                                                        P.sc.max_scan, sa);
+  else
+    k_decode_plan<false><<<gscan, kPlanThreads, 0, st>>>(P.pv, layer, P.sc.dplan, P.sc.dscan, P.sc.darrive,
+                                                         P.sc.max_scan, sa);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = launch_decode_alloc(P, layer, sa, st)) != cudaSuccess) return e;
@@ -343,7 +393,10 @@ cudaError_t launch_decode(Pool& P, int layer, const SlotArgs& sa, const __half* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, k_decode_apply, P.pv, layer, (const DecodePlan*)P.sc.dplan, k, v, sa);
+  if (P.pv.mid_enabled)
+    e = cudaLaunchKernelEx(&lc, k_decode_apply<true>, P.pv, layer, (const DecodePlan*)P.sc.dplan, k, v, sa);
+  else
+    e = cudaLaunchKernelEx(&lc, k_decode_apply<false>, P.pv, layer, (const DecodePlan*)P.sc.dplan, k, v, sa);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -18,7 +18,7 @@ constexpr int kD = 128;            // head_dim
 constexpr int kObs = 32;           // observation queries per prompt
 constexpr int kMaxG = 8;           // query heads per KV head supported by the kernels
 constexpr int kMaxCallReq = 1024;  // requests per call
-constexpr int kTierPrune = 0, kTierLo = 1, kTierHi = 2;
+constexpr int kTierPrune = 0, kTierLo = 1, kTierHi = 2, kTierMid = 3;   // mid: the optional third tier
 
 // Geometry of one tier's unified page.
 struct TierGeom {
@@ -64,6 +64,8 @@ struct ScanPart {
   int sh, sl;
   int xc;
   float ic;
+  unsigned long long km;      // mid tier (three-tier pools): argmin key and slot
+  int sm, pad;
 };
 
 // The victim keys of a head as the next generation step will see them,
@@ -87,15 +89,28 @@ struct PoolView {
   CallArgs* call;
   VictimCache* vcache;  // [layer][slot][kvh]
   float2* alpha;        // [layer][kvh]: the head's (alpha_h, alpha_l)
+  float* alpha_m;       // [layer][kvh]: the head's alpha_m (three-tier pools)
   int n_pages, page_bytes, n_layers, hkv, G, max_req, max_seq, L;
   int lo_enabled, window, slack, reclaim;
-  TierGeom hi, lo;
+  // Three-tier pools: a row is the two-way table (L entries) followed by the
+  // one-way mid table (Lm entries); counters are {hi tok, lo tok, hi pages,
+  // lo pages, mid tok, mid pages, 0, 0}. Two-tier pools: Lm = 0, 4 counters.
+  int mid_enabled, Lm, Lrow, cstride;
+  TierGeom hi, lo, mid;
 
   __device__ __forceinline__ int* row(int layer, int slot, int kvh) const {
-    return table + ((size_t)((size_t)layer * max_req + slot) * hkv + kvh) * L;
+    return table + ((size_t)((size_t)layer * max_req + slot) * hkv + kvh) * Lrow;
   }
   __device__ __forceinline__ int* cnt(int layer, int slot, int kvh) const {
-    return counts + ((size_t)((size_t)layer * max_req + slot) * hkv + kvh) * 4;
+    return counts + ((size_t)((size_t)layer * max_req + slot) * hkv + kvh) * cstride;
+  }
+  // table entry of a tier's page k: hi from the left of the two-way part, lo
+  // from its right, mid in the one-way part after it
+  __device__ __forceinline__ int entry(int tier, int k) const {
+    return tier == kTierHi ? k : (tier == kTierLo ? L - 1 - k : L + k);
+  }
+  __device__ __forceinline__ const TierGeom& geom(int tier) const {
+    return tier == kTierHi ? hi : (tier == kTierLo ? lo : mid);
   }
   __device__ __forceinline__ VictimCache* vc(int layer, int slot, int kvh) const {
     return vcache + ((size_t)layer * max_req + slot) * hkv + kvh;
@@ -137,6 +152,21 @@ __device__ __forceinline__ int classify(float imp, float th_h, float th_l, int l
     return kTierPrune;
   }
   return imp >= th_l ? kTierHi : kTierPrune;
+}
+
+// Four-way decision of a three-tier pool (DiffKV, compaction policy:
+// extensibility to more precision levels): hi above alpha_h/N, mid from
+// alpha_m/N, lo from alpha_l/N, else pruned.
+__device__ __forceinline__ int classify3(float imp, float th_h, float th_m, float th_l) {
+  if (imp > th_h) return kTierHi;
+  if (imp >= th_m) return kTierMid;
+  if (imp >= th_l) return kTierLo;
+  return kTierPrune;
+}
+
+// precision order of the tiers: prune < lo < mid < hi
+__device__ __forceinline__ int tier_rank(int tier) {
+  return tier == kTierHi ? 3 : (tier == kTierMid ? 2 : (tier == kTierLo ? 1 : 0));
 }
 
 // Total order on floats as unsigned keys (for argmin reductions).

@@ -16,9 +16,13 @@ constexpr int kAttnWarps = 4;      // warps per decode-attention CTA
 // update [16 slots] at row G and the chunk's page ID at row G + 1.
 
 // One slot write of a generation-phase step.
+// src: the new token, or a stored token of tier src_tier at slot src_slot,
+// re-quantised when src_tier differs from dst_tier (a demotion) and copied
+// as is otherwise.
 enum MoveSrc { kSrcNew = 0, kSrcDemote = 1 };
 struct Move {
   int dst_tier, dst_slot, src, src_slot;
+  int src_tier;
 };
 // Per-head plan of one generation-phase step (written by k_decode_plan).
 struct DecodePlan {
@@ -26,7 +30,8 @@ struct DecodePlan {
   int php, plp;                        // page counts after the step
   int new_hp, new_lp, free_hp, free_lp;
   int n_moves, err;
-  Move mv[2];
+  Move mv[3];
+  int nm, pmp, new_mp, free_mp;        // the mid tier (three-tier pools), as above
 };
 
 // Argmin over tokens of (importance, position): key = order_key(importance)
@@ -71,23 +76,57 @@ __device__ __forceinline__ void block_amin2(ArgMin& a, ArgMin& b, ArgMin* s_tmp)
   b = s_tmp[nw];
 }
 
+// Block-wide argmin of three keys at once (s_tmp: three entries per warp).
+__device__ __forceinline__ void block_amin3(ArgMin& a, ArgMin& b, ArgMin& c, ArgMin* s_tmp) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    a = shfl_amin(a, s);
+    b = shfl_amin(b, s);
+    c = shfl_amin(c, s);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) {
+    s_tmp[warp] = a;
+    s_tmp[nw + warp] = b;
+    s_tmp[2 * nw + warp] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < nw; w++) {
+      a = amin(a, s_tmp[w]);
+      b = amin(b, s_tmp[nw + w]);
+      c = amin(c, s_tmp[2 * nw + w]);
+    }
+    s_tmp[0] = a;
+    s_tmp[nw] = b;
+    s_tmp[2 * nw] = c;
+  }
+  __syncthreads();
+  a = s_tmp[0];
+  b = s_tmp[nw];
+  c = s_tmp[2 * nw];
+}
+
 // One stored token's part in the victim search of the next generation step
 // (length n = N + 1 after its append, update count upd): its importance
 // S / c and argmin key; hi tokens before wlim = n - W are hi-victim
 // candidates, the hi token at pc = n - W - 1 is t_c, every lo token is a
 // lo-victim candidate.
-__device__ __forceinline__ void victim_token(float score, int pos, int slot, bool hi, int n0, int upd, int pc,
-                                             int wlim, ArgMin& bh, ArgMin& bl, int& xc, float& ic) {
+// In a three-tier pool every mid token is a mid-victim candidate (bm).
+__device__ __forceinline__ void victim_token(float score, int pos, int slot, int tier, int n0, int upd, int pc,
+                                             int wlim, ArgMin& bh, ArgMin& bl, ArgMin& bm, int& xc, float& ic) {
   const float imp = __fdiv_rn(score, (float)score_count(pos, n0, upd));
   const unsigned long long key = ((unsigned long long)order_key(imp) << 32) | (uint32_t)pos;
-  if (hi) {
+  if (tier == kTierHi) {
     if (pos == pc) {
       xc = slot;
       ic = imp;
     }
     if (pos < wlim) bh = amin(bh, ArgMin{key, slot});
-  } else {
+  } else if (tier == kTierLo) {
     bl = amin(bl, ArgMin{key, slot});
+  } else {
+    bm = amin(bm, ArgMin{key, slot});
   }
 }
 
@@ -98,10 +137,13 @@ struct Scratch {
   float* lse2;          // [units][32*G]
   float* score;         // [max_tokens][Hkv]
   uint16_t* tokinfo;    // [max_tokens][Hkv]: rank << 2 | tier
-  int2* bcnt;           // [units][nkb_cap]
-  int2* bbase;          // [units][nkb_cap]
-  int* rank2pos;        // [units][2][max_seq]
-  int4* unit_info;      // [units]: grant pages, hi count, lo count
+  int2* bcnt;           // [units][nkb_cap]: hi and lo tokens of a key block
+  int2* bbase;          // [units][nkb_cap]: their exclusive prefixes over the head's blocks
+  int* bcnt_m;          // [units][nkb_cap]: mid tokens of a key block (three-tier pools)
+  int* bbase_m;         // [units][nkb_cap]: their exclusive prefixes
+  int* rank2pos;        // [units][2 or 3][max_seq]: maps lo, hi (, mid)
+  int4* unit_info;      // [units]: grant pages, hi count, lo count, reclaimed pages
+  int* unit_mid;        // [units]: mid count (three-tier pools)
   int* grant_ids;       // [units][grant_cap]
   unsigned long long* pbase;   // prompt coordination: list start, end and grant total at the call
   // decode compaction

@@ -92,6 +92,7 @@ int validate(const dkv_config* c) {
   if (c->page_bytes < 64 || c->page_bytes % 16) return DKV_ERR_ARG;
   if (c->recent_window < 0 || c->prompt_grant_slack < 0) return DKV_ERR_ARG;
   if (std::isnan(c->alpha_h) || std::isnan(c->alpha_l)) return DKV_ERR_ARG;
+  if (c->mid_enabled && (!c->lo_enabled || std::isnan(c->alpha_m))) return DKV_ERR_ARG;
   if (c->head_dim != kD || c->group_size < 1 || c->group_size > kMaxG || c->obs_window != kObs)
     return DKV_ERR_UNSUPPORTED;
   return DKV_OK;
@@ -128,9 +129,15 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   *out = nullptr;
   int rc = validate(cfg);
   if (rc) return rc;
-  TierGeom hi{}, lo{};
+  TierGeom hi{}, lo{}, mid{};
   if (fit_tier(cfg->page_bytes, 8, 4, cfg->tokens_per_hi_page, &hi) < 0) return DKV_ERR_ARG;
   if (fit_tier(cfg->page_bytes, 4, 2, cfg->tokens_per_lo_page, &lo) < 0) return DKV_ERR_ARG;
+  const bool three = cfg->mid_enabled != 0;
+  if (three) {
+    if (fit_tier(cfg->page_bytes, 8, 2, cfg->tokens_per_mid_page, &mid) < 0) return DKV_ERR_ARG;
+    // the three-tier path runs the page-per-copy attention kernel only
+    if (hi.t % kChunk || lo.t % kChunk || mid.t % kChunk) return DKV_ERR_UNSUPPORTED;
+  }
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || cuda_device < 0 || cuda_device >= ndev) return DKV_ERR_ARG;
   DeviceGuard guard(cuda_device);
@@ -158,6 +165,11 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   v.reclaim = cfg->reclaim_in_decode ? 1 : 0;
   v.hi = hi;
   v.lo = lo;
+  v.mid = mid;
+  v.mid_enabled = three ? 1 : 0;
+  v.Lm = three ? (cfg->max_seq_len + mid.t - 1) / mid.t + 1 : 0;
+  v.Lrow = v.L + v.Lm;
+  v.cstride = three ? 8 : 4;
   Scratch& s = P.sc;
   const size_t heads = (size_t)cfg->n_layers * cfg->max_requests * cfg->n_kv_heads;
   const size_t units = (size_t)cfg->max_requests * cfg->n_kv_heads;
@@ -165,7 +177,8 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   const int G = cfg->group_size;
   s.nkb_cap = (cfg->max_seq_len + kKeyBlock - 1) / kKeyBlock;
   s.grant_cap = (cfg->max_seq_len + hi.t - 1) / hi.t + cfg->prompt_grant_slack;
-  s.max_chunks = (cfg->max_seq_len + kChunk - 1) / kChunk + 1;
+  // chunks of a head: its tiers' token counts rounded up to 16 each
+  s.max_chunks = (cfg->max_seq_len + kChunk - 1) / kChunk + (three ? 2 : 1);
   s.max_splits = s.max_chunks / 8 + 2;   // attention partials per head (>= 8 chunks per warp)
   s.max_scan = (cfg->max_seq_len + 1 + 2047) / 2048;   // generation-phase scan CTAs per head
   s.max_vparts = (s.max_chunks + 63) / 64;              // attention epilogue blocks per head (>= 64 chunks each)
@@ -175,20 +188,24 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   };
   A(&v.pages, (size_t)cfg->n_pages * cfg->page_bytes);
   A(&v.list, (size_t)cfg->n_pages);
-  A(&v.table, heads * v.L);
-  A(&v.counts, heads * 4);
+  A(&v.table, heads * v.Lrow);
+  A(&v.counts, heads * v.cstride);
   A(&v.req, (size_t)cfg->n_layers * cfg->max_requests * 4);
   A(&v.ctl, 1);
   A(&v.call, 1);
   A(&v.vcache, heads);
   A(&v.alpha, (size_t)cfg->n_layers * cfg->n_kv_heads);
+  A(&v.alpha_m, (size_t)cfg->n_layers * cfg->n_kv_heads);
   A(&s.partial, units * s.nkb_cap * kObs * G);
   A(&s.lse2, units * kObs * G);
   A(&s.score, max_tokens * cfg->n_kv_heads);
   A(&s.tokinfo, max_tokens * cfg->n_kv_heads);
   A(&s.bcnt, units * s.nkb_cap);
   A(&s.bbase, units * s.nkb_cap);
-  A(&s.rank2pos, units * 2 * cfg->max_seq_len);
+  A(&s.bcnt_m, units * s.nkb_cap);
+  A(&s.bbase_m, units * s.nkb_cap);
+  A(&s.unit_mid, units);
+  A(&s.rank2pos, units * (three ? 3 : 2) * cfg->max_seq_len);
   A(&s.unit_info, units);
   A(&s.grant_ids, units * s.grant_cap);
   A(&s.pbase, 4);
@@ -205,8 +222,8 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   // stamps -1: no head has victim keys yet
   if (e == cudaSuccess) e = cudaMemset(v.vcache, 0xff, heads * sizeof(VictimCache));
   if (e == cudaSuccess) e = cudaMemset(v.pages, 0, (size_t)cfg->n_pages * cfg->page_bytes);
-  if (e == cudaSuccess) e = cudaMemset(v.table, 0xff, heads * v.L * sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(v.counts, 0, heads * 4 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(v.table, 0xff, heads * v.Lrow * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(v.counts, 0, heads * v.cstride * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v.req, 0, (size_t)cfg->n_layers * cfg->max_requests * 4 * sizeof(int));
   if (e == cudaSuccess) {
     Ctl c{};
@@ -218,6 +235,10 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   if (e == cudaSuccess) {        // every head starts with the configuration's pair
     std::vector<float2> al((size_t)cfg->n_layers * cfg->n_kv_heads, make_float2(cfg->alpha_h, cfg->alpha_l));
     e = cudaMemcpy(v.alpha, al.data(), al.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) {
+    std::vector<float> am((size_t)cfg->n_layers * cfg->n_kv_heads, three ? cfg->alpha_m : 0.0f);
+    e = cudaMemcpy(v.alpha_m, am.data(), am.size() * sizeof(float), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) {
     k_init_list<<<256, 256>>>(v.list, cfg->n_pages);
@@ -261,6 +282,12 @@ int dkv_pool_geometry(const dkv_pool* pool, dkv_geometry* out) {
   TierGeom tmp;
   out->hi_used = layout_tier(v.hi.t, 8, 4, &tmp);
   out->lo_used = layout_tier(v.lo.t, 4, 2, &tmp);
+  out->t_mid = v.mid_enabled ? v.mid.t : 0;
+  out->mid_table_len = v.Lm;
+  out->row_len = v.Lrow;
+  out->count_stride = v.cstride;
+  for (int s = 0; s < 6; s++) out->mid_off[s] = v.mid_enabled ? v.mid.off[s] : 0;
+  out->mid_used = v.mid_enabled ? layout_tier(v.mid.t, 8, 2, &tmp) : 0;
   return DKV_OK;
 }
 
@@ -481,6 +508,23 @@ int dkv_pool_set_thresholds(dkv_pool* pool, int32_t layer, const float* alpha_h,
   return cuda_err(e);
 }
 
+int dkv_pool_set_mid_thresholds(dkv_pool* pool, int32_t layer, const float* alpha_m, void* stream) {
+  if (!pool || !alpha_m) return DKV_ERR_ARG;
+  Pool& P = pool->P;
+  const dkv_config& c = P.cfg;
+  if (layer < 0 || layer >= c.n_layers || !P.pv.mid_enabled) return DKV_ERR_ARG;
+  std::vector<float> am(c.n_kv_heads);
+  for (int h = 0; h < c.n_kv_heads; h++) {
+    if (std::isnan(alpha_m[h])) return DKV_ERR_ARG;
+    am[h] = alpha_m[h];
+  }
+  DeviceGuard guard(P.device);
+  const cudaError_t e = cudaMemcpyAsync(P.pv.alpha_m + (size_t)layer * c.n_kv_heads, am.data(),
+                                        am.size() * sizeof(float), cudaMemcpyHostToDevice,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return cuda_err(e);
+}
+
 int dkv_free_request(dkv_pool* pool, int32_t req_slot, void* stream) {
   if (!pool) return DKV_ERR_ARG;
   Pool& P = pool->P;
@@ -509,7 +553,8 @@ int dkv_pool_status(dkv_pool* pool, dkv_status* out) {
   Ctl c;
   if (cudaMemcpy(&c, P.pv.ctl, sizeof(Ctl), cudaMemcpyDeviceToHost) != cudaSuccess) return DKV_ERR_CUDA;
   const size_t heads = (size_t)P.cfg.n_layers * P.cfg.max_requests * P.cfg.n_kv_heads;
-  std::vector<int> cnt(heads * 4);
+  const int cs = P.pv.cstride;
+  std::vector<int> cnt(heads * cs);
   if (cudaMemcpy(cnt.data(), P.pv.counts, cnt.size() * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return DKV_ERR_CUDA;
   out->error = c.error;
@@ -517,12 +562,16 @@ int dkv_pool_status(dkv_pool* pool, dkv_status* out) {
   out->list_start = (int64_t)c.start;
   out->list_end = (int64_t)c.end;
   out->free_pages = (int64_t)(c.end - c.start);
-  out->hi_tokens = out->lo_tokens = out->hi_pages = out->lo_pages = 0;
+  out->hi_tokens = out->lo_tokens = out->hi_pages = out->lo_pages = out->mid_tokens = out->mid_pages = 0;
   for (size_t h = 0; h < heads; h++) {
-    out->hi_tokens += cnt[4 * h];
-    out->lo_tokens += cnt[4 * h + 1];
-    out->hi_pages += cnt[4 * h + 2];
-    out->lo_pages += cnt[4 * h + 3];
+    out->hi_tokens += cnt[cs * h];
+    out->lo_tokens += cnt[cs * h + 1];
+    out->hi_pages += cnt[cs * h + 2];
+    out->lo_pages += cnt[cs * h + 3];
+    if (cs > 4) {
+      out->mid_tokens += cnt[cs * h + 4];
+      out->mid_pages += cnt[cs * h + 5];
+    }
   }
   return DKV_OK;
 }
@@ -566,8 +615,8 @@ int dkv_pool_export(dkv_pool* pool, dkv_snapshot* out) {
   };
   cp(out->pages, P.pv.pages, (size_t)c.n_pages * c.page_bytes);
   cp(out->free_list, P.pv.list, (size_t)c.n_pages * sizeof(int));
-  cp(out->table, P.pv.table, heads * P.pv.L * sizeof(int));
-  cp(out->head_counts, P.pv.counts, heads * 4 * sizeof(int));
+  cp(out->table, P.pv.table, heads * P.pv.Lrow * sizeof(int));
+  cp(out->head_counts, P.pv.counts, heads * P.pv.cstride * sizeof(int));
   cp(out->req_state, P.pv.req, (size_t)c.n_layers * c.max_requests * 4 * sizeof(int));
   if (out->pointers && e == cudaSuccess) {
     Ctl ctl;

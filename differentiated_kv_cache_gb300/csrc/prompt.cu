@@ -14,9 +14,13 @@
 namespace dkv {
 
 // Tier of one prompt token and its rank among same-tier tokens of the block
-// (block of kKeyBlock consecutive positions handled by 128 threads).
-__device__ __forceinline__ void classify_block(const PoolView& pv, float2 al, int n0, int j, float s, int& tier,
-                                               int& rank, int* s_cnt /*[2*4]*/, int2* bcnt_out) {
+// (block of kKeyBlock consecutive positions handled by 128 threads). A
+// three-tier pool also splits off mid tokens (am: the head's alpha_m) and
+// counts them in *bcm_out (MID).
+template <bool MID>
+__device__ __forceinline__ void classify_block(const PoolView& pv, float2 al, float am, int n0, int j, float s,
+                                               int& tier, int& rank, int* s_cnt /*[3*4]*/, int2* bcnt_out,
+                                               int* bcm_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   tier = kTierPrune;
   if (j < n0) {
@@ -24,28 +28,41 @@ __device__ __forceinline__ void classify_block(const PoolView& pv, float2 al, in
       tier = kTierHi;
     } else {
       const float imp = __fdiv_rn(s, (float)score_count(j, n0, 0));
-      tier = classify(imp, __fdiv_rn(al.x, (float)n0), __fdiv_rn(al.y, (float)n0), pv.lo_enabled);
+      const float th_h = __fdiv_rn(al.x, (float)n0), th_l = __fdiv_rn(al.y, (float)n0);
+      tier = MID ? classify3(imp, th_h, __fdiv_rn(am, (float)n0), th_l) : classify(imp, th_h, th_l, pv.lo_enabled);
     }
   }
   const unsigned bh = __ballot_sync(0xffffffffu, tier == kTierHi);
   const unsigned bl = __ballot_sync(0xffffffffu, tier == kTierLo);
-  if (lane == 0) { s_cnt[warp] = __popc(bh); s_cnt[4 + warp] = __popc(bl); }
+  const unsigned bm = MID ? __ballot_sync(0xffffffffu, tier == kTierMid) : 0u;
+  if (lane == 0) {
+    s_cnt[warp] = __popc(bh);
+    s_cnt[4 + warp] = __popc(bl);
+    if (MID) s_cnt[8 + warp] = __popc(bm);
+  }
   __syncthreads();
-  int bh0 = 0, bl0 = 0;
-  for (int w = 0; w < warp; w++) { bh0 += s_cnt[w]; bl0 += s_cnt[4 + w]; }
+  int bh0 = 0, bl0 = 0, bm0 = 0;
+  for (int w = 0; w < warp; w++) {
+    bh0 += s_cnt[w];
+    bl0 += s_cnt[4 + w];
+    if (MID) bm0 += s_cnt[8 + w];
+  }
   const unsigned below = (1u << lane) - 1u;
-  rank = tier == kTierHi ? bh0 + __popc(bh & below) : (tier == kTierLo ? bl0 + __popc(bl & below) : 0);
+  rank = tier == kTierHi ? bh0 + __popc(bh & below)
+                         : (tier == kTierLo ? bl0 + __popc(bl & below) : (tier == kTierMid ? bm0 + __popc(bm & below) : 0));
   if (tid == 0 && bcnt_out)
     *bcnt_out = make_int2(s_cnt[0] + s_cnt[1] + s_cnt[2] + s_cnt[3], s_cnt[4] + s_cnt[5] + s_cnt[6] + s_cnt[7]);
+  if (MID && tid == 0) *bcm_out = s_cnt[8] + s_cnt[9] + s_cnt[10] + s_cnt[11];
 }
 
 // Tier from caller-given scores (score_in), same rule and ranks, against the
-// thresholds of the token's head.
+// thresholds of the token's head. MID: a three-tier pool.
+template <bool MID>
 __global__ void __launch_bounds__(128) k_prompt_given(PoolView pv, int layer, const float* __restrict__ score_in,
-                                                       float* score_out, uint16_t* tokinfo, int2* bcnt,
+                                                       float* score_out, uint16_t* tokinfo, int2* bcnt, int* bcnt_m,
                                                        int nkb_cap) {
   if (pv.noop()) return;
-  __shared__ int s_cnt[8];
+  __shared__ int s_cnt[12];
   const int kb = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
   const CallArgs* ca = pv.call;
   const int n0 = ca->lens[i];
@@ -55,17 +72,22 @@ __global__ void __launch_bounds__(128) k_prompt_given(PoolView pv, int layer, co
   const size_t tok = (size_t)(ca->tok0[i] + j) * pv.hkv + kvh;
   const float s = j < n0 ? score_in[tok] : 0.0f;
   int tier, rank;
-  classify_block(pv, pv.thresholds(layer, kvh), n0, j, s, tier, rank, s_cnt,
-                 bcnt + ((size_t)i * pv.hkv + kvh) * nkb_cap + kb);
+  const size_t bx = ((size_t)i * pv.hkv + kvh) * nkb_cap + kb;
+  classify_block<MID>(pv, pv.thresholds(layer, kvh), MID ? pv.alpha_m[(size_t)layer * pv.hkv + kvh] : 0.0f, n0, j,
+                      s, tier, rank, s_cnt, bcnt + bx, bcnt_m + bx);
   if (j < n0) {
     if (score_out) score_out[tok] = s;
     tokinfo[tok] = (uint16_t)((rank << 2) | tier);
   }
 }
 
-// rank2pos[unit][tier][rank] = position, rank = block base + in-block rank.
+// rank -> position map of a head's tier: map 0 lo, 1 hi, 2 mid
+__device__ __forceinline__ int tier_map(int tier) { return tier == kTierHi ? 1 : (tier == kTierLo ? 0 : 2); }
+
+// rank2pos[unit][map][rank] = position, rank = block base + in-block rank.
 __global__ void __launch_bounds__(128) k_prompt_scatter(PoolView pv, const uint16_t* __restrict__ tokinfo,
-                                                         const int2* __restrict__ bbase, int* rank2pos,
+                                                         const int2* __restrict__ bbase,
+                                                         const int* __restrict__ bbase_m, int* rank2pos,
                                                          int nkb_cap) {
   if (pv.noop()) return;
   const int kb = blockIdx.x, kvh = blockIdx.y, i = blockIdx.z;
@@ -77,9 +99,15 @@ __global__ void __launch_bounds__(128) k_prompt_scatter(PoolView pv, const uint1
   const uint16_t info = tokinfo[(size_t)(ca->tok0[i] + j) * pv.hkv + kvh];
   const int tier = info & 3;
   if (tier == kTierPrune) return;
-  const int2 base = bbase[unit * nkb_cap + kb];
-  const int rank = (tier == kTierHi ? base.x : base.y) + (info >> 2);
-  rank2pos[(unit * 2 + (tier == kTierHi ? 1 : 0)) * pv.max_seq + rank] = j;
+  int base;
+  if (tier == kTierMid) {
+    base = bbase_m[unit * nkb_cap + kb];
+  } else {
+    const int2 b2 = bbase[unit * nkb_cap + kb];
+    base = tier == kTierHi ? b2.x : b2.y;
+  }
+  const int rank = base + (info >> 2);
+  rank2pos[(unit * (pv.mid_enabled ? 3 : 2) + tier_map(tier)) * pv.max_seq + rank] = j;
 }
 
 // ---------------------------------------------------------------------------
@@ -115,12 +143,16 @@ __device__ __forceinline__ uint32_t pack_sat(int a, int b, uint32_t c) {
 // (e, q) holds token e's K and V features 32q .. 32q+31 in kv (4 uint4 of K,
 // then 4 of V) and its position j (-1 past the tier's count); grant: the
 // head's granted page IDs; s_vw: the warp's [token][value word] scratch.
-template <bool HI>
+// TIER: hi (K8V4, pages from the grant's left), lo (K4V2, from its right) or
+// mid (K8V2, from grant entry mbase on: the pages after the hi ones).
+template <int TIER>
 __device__ __forceinline__ void pack_group(const PoolView& pv, const uint4 (&kv)[8], int j, int r0, int count,
-                                           int gcnt, const int* __restrict__ grant, const float* __restrict__ score,
-                                           size_t tok_base, int kvh, uint32_t (*s_vw)[32]) {
-  constexpr int KB = HI ? 8 : 4, VB = HI ? 4 : 2, GSZ = 8 / VB;   // GSZ: tokens per value row
-  const TierGeom& tg = HI ? pv.hi : pv.lo;
+                                           int gcnt, int mbase, const int* __restrict__ grant,
+                                           const float* __restrict__ score, size_t tok_base, int kvh,
+                                           uint32_t (*s_vw)[32]) {
+  constexpr bool HI = TIER == kTierHi, LOW = TIER == kTierLo;
+  constexpr int KB = LOW ? 4 : 8, VB = HI ? 4 : 2, GSZ = 8 / VB;   // GSZ: tokens per value row
+  const TierGeom& tg = HI ? pv.hi : (LOW ? pv.lo : pv.mid);
   const int lane = threadIdx.x & 31, e = lane >> 2, q = lane & 3;   // token e of the 8, features 32q..32q+31
   // bit offset of this token's slot inside a value word
   const int slot_e = e % GSZ;
@@ -171,12 +203,13 @@ __device__ __forceinline__ void pack_group(const PoolView& pv, const uint4 (&kv)
     s_vw[e][8 * q + w] = valid ? f << eb : 0u;
   }
   if (valid) {
-    // page and slot of rank r: hi from the left of the grant, lo from the right
-    const int pidx = HI ? tg.div(r) : gcnt - 1 - tg.div(r);
+    // page and slot of rank r: hi from the left of the grant, lo from the
+    // right, mid from mbase on
+    const int pidx = HI ? tg.div(r) : (LOW ? gcnt - 1 - tg.div(r) : mbase + tg.div(r));
     const int slot = r - tg.div(r) * tg.t;
     uint8_t* page = pv.page(grant[pidx]);
     uint8_t* krow = page + tg.off[0] + slot * tg.kbytes;
-    if (HI) {
+    if (KB == 8) {
       uint32_t w[8];
 #pragma unroll
       for (int y = 0; y < 8; y++) {             // bytes 4y .. 4y+3
@@ -219,7 +252,7 @@ __device__ __forceinline__ void pack_group(const PoolView& pv, const uint4 (&kv)
   for (int row = 0; row < kPackTok / GSZ; row++) {
     const int rfirst = r0 + row * GSZ;
     if (rfirst >= count) break;
-    const int pidx = HI ? tg.div(rfirst) : gcnt - 1 - tg.div(rfirst);
+    const int pidx = HI ? tg.div(rfirst) : (LOW ? gcnt - 1 - tg.div(rfirst) : mbase + tg.div(rfirst));
     const int slot0 = rfirst - tg.div(rfirst) * tg.t;
     uint8_t* page = pv.page(grant[pidx]);
     uint32_t word = 0;
@@ -235,11 +268,15 @@ __device__ __forceinline__ void pack_group(const PoolView& pv, const uint4 (&kv)
 // that every warp streams one long sequence with its loads ahead of the math:
 // the positions of the group after next and the K/V rows of the next group
 // are in flight while a group is quantized and stored.
+// A three-tier pool's heads (MID) also have mid groups (after their lo
+// groups); unit_mid holds each head's mid token count.
+template <bool MID>
 __global__ void __launch_bounds__(256, 2) k_prompt_pack(PoolView pv, const __half* __restrict__ k,
                                                          const __half* __restrict__ v,
                                                          const float* __restrict__ score,
                                                          const int* __restrict__ rank2pos,
                                                          const int4* __restrict__ unit_info,
+                                                         const int* __restrict__ unit_mid,
                                                          const int* __restrict__ grant_ids, int grant_cap) {
   if (pv.noop()) return;
   extern __shared__ int s_pref[];              // [n_units + 1] first group of each head
@@ -256,6 +293,7 @@ __global__ void __launch_bounds__(256, 2) k_prompt_pack(PoolView pv, const __hal
     for (int u = u0; u < u1; u++) {
       const int4 ui = unit_info[u];
       sum += (ui.y + kPackTok - 1) / kPackTok + (ui.z + kPackTok - 1) / kPackTok;
+      if (MID) sum += (unit_mid[u] + kPackTok - 1) / kPackTok;
     }
     int x = sum;
 #pragma unroll
@@ -271,6 +309,7 @@ __global__ void __launch_bounds__(256, 2) k_prompt_pack(PoolView pv, const __hal
       s_pref[u] = run;
       const int4 ui = unit_info[u];
       run += (ui.y + kPackTok - 1) / kPackTok + (ui.z + kPackTok - 1) / kPackTok;
+      if (MID) run += (unit_mid[u] + kPackTok - 1) / kPackTok;
     }
     if (threadIdx.x == blockDim.x - 1) s_pref[n_units] = run;
     __syncthreads();
@@ -278,9 +317,9 @@ __global__ void __launch_bounds__(256, 2) k_prompt_pack(PoolView pv, const __hal
   const int total = s_pref[n_units];
   const int W = gridDim.x * 8;
   struct Grp {
-    int unit, r0, count, gcnt;
-    bool hi;
+    int unit, r0, count, gcnt, tier, mbase;
   };
+  constexpr int nmaps = MID ? 3 : 2;
   auto describe = [&](int x, Grp& d) {
     if (x >= total) return false;
     int lo = 0, hi = n_units - 1;              // last head with s_pref <= x
@@ -289,18 +328,21 @@ __global__ void __launch_bounds__(256, 2) k_prompt_pack(PoolView pv, const __hal
       if (s_pref[mid] <= x) lo = mid; else hi = mid - 1;
     }
     const int4 ui = unit_info[lo];
-    const int gh = (ui.y + kPackTok - 1) / kPackTok, off = x - s_pref[lo];
+    const int gh = (ui.y + kPackTok - 1) / kPackTok, gl = (ui.z + kPackTok - 1) / kPackTok;
+    const int off = x - s_pref[lo];
     d.unit = lo;
-    d.hi = off < gh;
-    d.r0 = kPackTok * (d.hi ? off : off - gh);
-    d.count = d.hi ? ui.y : ui.z;
+    d.tier = off < gh ? kTierHi : (!MID || off < gh + gl ? kTierLo : kTierMid);
+    d.r0 = kPackTok * (off < gh ? off : (!MID || off < gh + gl ? off - gh : off - gh - gl));
+    d.count = d.tier == kTierHi ? ui.y : (d.tier == kTierLo ? ui.z : unit_mid[lo]);
     d.gcnt = ui.x;
+    d.mbase = MID ? pv.hi.div(ui.y + pv.hi.t - 1) : 0;   // mid pages follow the head's hi pages in its grant
     return true;
   };
   auto pos_of = [&](bool has, const Grp& d) {
     if (!has) return -1;
     const int r = d.r0 + e;
-    return r < d.count ? __ldg(rank2pos + ((size_t)d.unit * 2 + (d.hi ? 1 : 0)) * pv.max_seq + r) : -1;
+    const int map = d.tier == kTierHi ? 1 : (d.tier == kTierLo ? 0 : 2);
+    return r < d.count ? __ldg(rank2pos + ((size_t)d.unit * nmaps + map) * pv.max_seq + r) : -1;
   };
   auto load_kv = [&](const Grp& d, int j, uint4 (&kv)[8]) {
     if (j >= 0) {
@@ -329,10 +371,15 @@ __global__ void __launch_bounds__(256, 2) k_prompt_pack(PoolView pv, const __hal
     const int ja = pos_of(ha, da);
     const int i = dc.unit / hkv, kvh = dc.unit % hkv;
     const int* grant = grant_ids + (size_t)dc.unit * grant_cap;
-    if (dc.hi)
-      pack_group<true>(pv, kvc, jc, dc.r0, dc.count, dc.gcnt, grant, score, (size_t)ca->tok0[i], kvh, s_vw[warp]);
-    else
-      pack_group<false>(pv, kvc, jc, dc.r0, dc.count, dc.gcnt, grant, score, (size_t)ca->tok0[i], kvh, s_vw[warp]);
+    if (dc.tier == kTierHi)
+      pack_group<kTierHi>(pv, kvc, jc, dc.r0, dc.count, dc.gcnt, 0, grant, score, (size_t)ca->tok0[i], kvh,
+                          s_vw[warp]);
+    else if (dc.tier == kTierLo)
+      pack_group<kTierLo>(pv, kvc, jc, dc.r0, dc.count, dc.gcnt, 0, grant, score, (size_t)ca->tok0[i], kvh,
+                          s_vw[warp]);
+    else if (MID)
+      pack_group<kTierMid>(pv, kvc, jc, dc.r0, dc.count, dc.gcnt, dc.mbase, grant, score, (size_t)ca->tok0[i], kvh,
+                           s_vw[warp]);
     dc = dn;
     hc = hn;
     jc = jn;
@@ -360,7 +407,10 @@ cudaError_t configure_kernels() {
   if ((e = configure_alloc()) != cudaSuccess) return e;
   if ((e = configure_prefill()) != cudaSuccess) return e;
   // the pack kernel keeps one int per head of the call in shared memory
-  if ((e = cudaFuncSetAttribute(k_prompt_pack, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) !=
+  if ((e = cudaFuncSetAttribute(k_prompt_pack<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_prompt_pack<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) !=
       cudaSuccess)
     return e;
   return configure_attention();
@@ -375,25 +425,38 @@ cudaError_t launch_prompt(Pool& P, int layer, int n_req, int max_len, long long 
   cudaError_t e = cudaSuccess;
   const float* score_src;
   if (scores_in) {
-    k_prompt_given<<<grid, 128, 0, st>>>(P.pv, layer, scores_in, scores_out, s.tokinfo, s.bcnt, s.nkb_cap);
+    if (P.pv.mid_enabled)
+      k_prompt_given<true><<<grid, 128, 0, st>>>(P.pv, layer, scores_in, scores_out, s.tokinfo, s.bcnt, s.bcnt_m,
+                                                 s.nkb_cap);
+    else
+      k_prompt_given<false><<<grid, 128, 0, st>>>(P.pv, layer, scores_in, scores_out, s.tokinfo, s.bcnt, s.bcnt_m,
+                                                  s.nkb_cap);
     e = cudaGetLastError();
     score_src = scores_in;
   } else {
     float* so = scores_out ? scores_out : s.score;
     e = launch_scoring_tc(P, k, q_obs, lse_obs, n_tok, n_req, so, st);
     if (e == cudaSuccess) {      // tiers and in-block ranks from the scores
-      k_prompt_given<<<grid, 128, 0, st>>>(P.pv, layer, so, nullptr, s.tokinfo, s.bcnt, s.nkb_cap);
+      if (P.pv.mid_enabled)
+        k_prompt_given<true><<<grid, 128, 0, st>>>(P.pv, layer, so, nullptr, s.tokinfo, s.bcnt, s.bcnt_m, s.nkb_cap);
+      else
+        k_prompt_given<false><<<grid, 128, 0, st>>>(P.pv, layer, so, nullptr, s.tokinfo, s.bcnt, s.bcnt_m,
+                                                    s.nkb_cap);
       e = cudaGetLastError();
     }
     score_src = so;
   }
   if (e != cudaSuccess) return e;
   if ((e = launch_prompt_plan(P, layer, n_req, st)) != cudaSuccess) return e;
-  k_prompt_scatter<<<grid, 128, 0, st>>>(P.pv, s.tokinfo, s.bbase, s.rank2pos, s.nkb_cap);
+  k_prompt_scatter<<<grid, 128, 0, st>>>(P.pv, s.tokinfo, s.bbase, s.bbase_m, s.rank2pos, s.nkb_cap);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t pref = sizeof(int) * ((size_t)n_req * P.pv.hkv + 1);
-  k_prompt_pack<<<2 * P.sm_count, 256, pref, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info, s.grant_ids,
-                                                   s.grant_cap);
+  if (P.pv.mid_enabled)
+    k_prompt_pack<true><<<2 * P.sm_count, 256, pref, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info,
+                                                           s.unit_mid, s.grant_ids, s.grant_cap);
+  else
+    k_prompt_pack<false><<<2 * P.sm_count, 256, pref, st>>>(P.pv, k, v, score_src, s.rank2pos, s.unit_info,
+                                                            s.unit_mid, s.grant_ids, s.grant_cap);
   return cudaGetLastError();
 }
 

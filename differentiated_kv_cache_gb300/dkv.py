@@ -23,8 +23,8 @@ DKV_PROMPT, DKV_DECODE = 0, 1
 
 EXPORTED = ("dkv_pool_create", "dkv_pool_destroy", "dkv_pool_geometry", "dkv_compact_step",
             "dkv_decode_attention", "dkv_decode_attention_static", "dkv_free_request", "dkv_pool_status", "dkv_pool_clear_error",
-            "dkv_pool_export", "dkv_pool_set_thresholds", "dkv_prefill_attention", "dkv_compact_step_prefilled",
-            "dkv_strerror")
+            "dkv_pool_export", "dkv_pool_set_thresholds", "dkv_pool_set_mid_thresholds", "dkv_prefill_attention",
+            "dkv_compact_step_prefilled", "dkv_strerror")
 
 
 class dkv_config(C.Structure):
@@ -32,19 +32,23 @@ class dkv_config(C.Structure):
         "n_layers", "n_kv_heads", "group_size", "head_dim", "page_bytes", "n_pages", "max_requests",
         "max_seq_len", "tokens_per_hi_page", "tokens_per_lo_page", "lo_enabled")] + \
         [("alpha_h", C.c_float), ("alpha_l", C.c_float)] + \
-        [(n, C.c_int32) for n in ("recent_window", "obs_window", "prompt_grant_slack", "reclaim_in_decode")]
+        [(n, C.c_int32) for n in ("recent_window", "obs_window", "prompt_grant_slack", "reclaim_in_decode",
+                                  "mid_enabled")] + \
+        [("alpha_m", C.c_float), ("tokens_per_mid_page", C.c_int32)]
 
 
 class dkv_geometry(C.Structure):
     _fields_ = [("t_hi", C.c_int32), ("t_lo", C.c_int32), ("table_len", C.c_int32),
                 ("hi_off", C.c_int32 * 6), ("lo_off", C.c_int32 * 6), ("hi_used", C.c_int32),
-                ("lo_used", C.c_int32)]
+                ("lo_used", C.c_int32), ("t_mid", C.c_int32), ("mid_table_len", C.c_int32),
+                ("row_len", C.c_int32), ("count_stride", C.c_int32), ("mid_off", C.c_int32 * 6),
+                ("mid_used", C.c_int32)]
 
 
 class dkv_status(C.Structure):
     _fields_ = [("error", C.c_int32), ("error_info", C.c_int32)] + \
         [(n, C.c_int64) for n in ("list_start", "list_end", "free_pages", "hi_tokens", "lo_tokens",
-                                  "hi_pages", "lo_pages")]
+                                  "hi_pages", "lo_pages", "mid_tokens", "mid_pages")]
 
 
 class dkv_snapshot(C.Structure):
@@ -82,6 +86,7 @@ def load() -> C.CDLL:
         L.dkv_compact_step_prefilled.argtypes = [P, I, I, P, P, P, P, P, P, P, P]
         L.dkv_free_request.argtypes = [P, I, P]
         L.dkv_pool_set_thresholds.argtypes = [P, I, P, P, P]
+        L.dkv_pool_set_mid_thresholds.argtypes = [P, I, P, P]
         L.dkv_pool_status.argtypes = [P, C.POINTER(dkv_status)]
         L.dkv_pool_clear_error.argtypes = [P]
         L.dkv_pool_export.argtypes = [P, C.POINTER(dkv_snapshot)]
@@ -132,7 +137,7 @@ def make_config(**kw) -> dkv_config:
     c = dkv_config()
     defaults = dict(head_dim=128, page_bytes=4096, tokens_per_hi_page=0, tokens_per_lo_page=0, lo_enabled=1,
                     alpha_h=2.0, alpha_l=0.25, recent_window=64, obs_window=32, prompt_grant_slack=1,
-                    reclaim_in_decode=1)
+                    reclaim_in_decode=1, mid_enabled=0, alpha_m=0.0, tokens_per_mid_page=0)
     defaults.update(kw)
     for name, _ in dkv_config._fields_:
         setattr(c, name, defaults[name])
@@ -155,7 +160,8 @@ def dkv_pool_geometry(pool) -> dict:
     g = dkv_geometry()
     _check(load().dkv_pool_geometry(pool, C.byref(g)), "dkv_pool_geometry")
     return dict(t_hi=g.t_hi, t_lo=g.t_lo, table_len=g.table_len, hi_off=list(g.hi_off), lo_off=list(g.lo_off),
-                hi_used=g.hi_used, lo_used=g.lo_used)
+                hi_used=g.hi_used, lo_used=g.lo_used, t_mid=g.t_mid, mid_table_len=g.mid_table_len,
+                row_len=g.row_len, count_stride=g.count_stride, mid_off=list(g.mid_off), mid_used=g.mid_used)
 
 
 def dkv_compact_step(pool, layer: int, mode: int, req_slots, seq_lens, k, v, q_obs=None, scores_in=None,
@@ -232,6 +238,13 @@ def dkv_pool_set_thresholds(pool, layer: int, alpha_h, alpha_l, stream=None, che
     return _check(rc, "dkv_pool_set_thresholds") if check else rc
 
 
+def dkv_pool_set_mid_thresholds(pool, layer: int, alpha_m, stream=None, check: bool = True) -> int:
+    """Per-KV-head thresholds of the mid tier of one layer (n_kv_heads floats)."""
+    am = np.ascontiguousarray(alpha_m, dtype=np.float32)
+    rc = load().dkv_pool_set_mid_thresholds(pool, int(layer), am.ctypes.data_as(C.c_void_p), _stream(stream))
+    return _check(rc, "dkv_pool_set_mid_thresholds") if check else rc
+
+
 def dkv_free_request(pool, req_slot: int, stream=None, check: bool = True) -> int:
     rc = load().dkv_free_request(pool, int(req_slot), _stream(stream))
     return _check(rc, "dkv_free_request") if check else rc
@@ -247,14 +260,16 @@ def dkv_pool_clear_error(pool) -> None:
     _check(load().dkv_pool_clear_error(pool), "dkv_pool_clear_error")
 
 
-def dkv_pool_export(pool, cfg: dict, table_len: int, pages: bool = True) -> dict:
-    """Host copy of the device state as numpy arrays, shaped like the oracle's."""
+def dkv_pool_export(pool, cfg: dict, table_len: int, pages: bool = True, count_stride: int = 4) -> dict:
+    """Host copy of the device state as numpy arrays, shaped like the oracle's
+    (table_len: entries of a table row, the geometry's row_len; count_stride:
+    ints of a head's counters, 8 with the mid tier)."""
     nl, mr, hk, npg = cfg["n_layers"], cfg["max_requests"], cfg["n_kv_heads"], cfg["n_pages"]
     out = dict(
         pages=np.zeros((npg, cfg["page_bytes"]) if pages else (0,), np.uint8),
         free_list=np.zeros(npg, np.int32),
         table=np.zeros((nl, mr, hk, table_len), np.int32),
-        head_counts=np.zeros((nl, mr, hk, 4), np.int32),
+        head_counts=np.zeros((nl, mr, hk, count_stride), np.int32),
         req_state=np.zeros((nl, mr, 4), np.int32),
         pointers=np.zeros(2, np.int64))
     snap = dkv_snapshot()

@@ -56,11 +56,12 @@
  * Unified page format  [Mem-UP]
  * -----------------------------
  * Two tiers, fixed bit widths: hi = K8V4 (8-bit key codes, 4-bit value
- * codes), lo = K4V2 [Pol-P]. head_dim d = 128. A page holds T tokens of one
- * tier; T is the largest multiple of g = 8/vbits (tokens sharing a value
- * byte: 2 for hi, 4 for lo) whose six segments fit in page_bytes. For
- * page_bytes = 4096: T_hi = 18, T_lo = 36. Segments, in order, each starting
- * on a 16-byte boundary, slot t in [0, T):
+ * codes), lo = K4V2 [Pol-P]; optionally a third, mid = K8V2, between them
+ * [Pol-Ext] (config.mid_enabled). head_dim d = 128. A page holds T tokens of
+ * one tier; T is the largest multiple of g = 8/vbits (tokens sharing a value
+ * byte: 2 for hi, 4 for lo and mid) whose six segments fit in page_bytes.
+ * For page_bytes = 4096: T_hi = 18, T_lo = 36, T_mid = 20. Segments, in
+ * order, each starting on a 16-byte boundary, slot t in [0, T):
  *   1. K codes  T rows of d*kbits/8 bytes (128 B hi, 64 B lo).
  *               8-bit: byte i = code of feature i.
  *               4-bit: byte i bits 0-3 = feature 2i, bits 4-7 = feature 2i+1.
@@ -92,6 +93,21 @@
  * head) of L_e = ceil(max_seq_len / T_hi) + 1 int32 entries: hi page k at
  * entry k, lo page k at entry L_e-1-k, unused entries -1. Hi slot s lives on
  * hi page s / T_hi at slot s % T_hi; lo slot s on lo page s / T_lo.
+ * With the mid tier each row composes that two-way table with a one-way
+ * table of L_m = ceil(max_seq_len / T_mid) + 1 entries after it [Mem-Gen:
+ * further precision levels by combining one-way or two-way page tables]:
+ * mid page k at entry L_e + k; the row then has L_e + L_m entries.
+ *
+ * Three tiers [Pol-Ext]: a token is hi if I > alpha_h/N, else mid if
+ * I >= alpha_m/N, else lo if I >= alpha_l/N, else pruned. The prompt grant
+ * stays ceil(N0/T_hi)+slack pages (slack 2 covers the three partial pages);
+ * mid pages take the grant pages right after the hi ones. In a generation
+ * step the victim is the least important token of the tier t_c ended in (hi:
+ * outside the window; mid and lo: t_c included); it stays if it classifies
+ * at its tier or above, else moves to the end of the tier it classifies at
+ * (re-quantised from its dequantised values) or is pruned. New pages of a
+ * head are taken hi, lo, then mid; request completion returns hi, lo, then
+ * mid pages.
  */
 #ifndef DKV_H
 #define DKV_H
@@ -137,6 +153,10 @@ typedef struct dkv_config {
   int32_t obs_window;          /* observation queries per prompt; must be 32   */
   int32_t prompt_grant_slack;  /* extra pages in each head's all-hi grant, >=0 */
   int32_t reclaim_in_decode;   /* 1: free a tier's emptied tail page in DECODE */
+  int32_t mid_enabled;         /* 1: a third tier mid = K8V2 (needs lo_enabled;
+                                  every tier's T a multiple of 16)            */
+  float   alpha_m;             /* mid threshold alpha_m / N (mid_enabled)      */
+  int32_t tokens_per_mid_page; /* 0 = largest that fits; else a multiple of 4  */
 } dkv_config;
 
 typedef struct dkv_pool dkv_pool;   /* opaque; owns every device structure */
@@ -148,6 +168,12 @@ typedef struct dkv_geometry {
   int32_t hi_off[6];               /* segment byte offsets, hi page        */
   int32_t lo_off[6];               /* segment byte offsets, lo page        */
   int32_t hi_used, lo_used;        /* bytes used by the six segments       */
+  int32_t t_mid;                   /* tokens per mid page (0 without mid)  */
+  int32_t mid_table_len;           /* L_m (0 without mid)                  */
+  int32_t row_len;                 /* table entries per head: L_e + L_m    */
+  int32_t count_stride;            /* head counter ints: 4, or 8 with mid  */
+  int32_t mid_off[6];              /* segment byte offsets, mid page       */
+  int32_t mid_used;                /* bytes used by a mid page's segments  */
 } dkv_geometry;
 
 /* Sticky status and pool-wide counters (host struct). */
@@ -161,13 +187,16 @@ typedef struct dkv_status {
   int64_t lo_tokens;    /* stored lo tokens                                            */
   int64_t hi_pages;     /* pages held as hi                                            */
   int64_t lo_pages;     /* pages held as lo                                            */
+  int64_t mid_tokens;   /* stored mid tokens (0 without mid)                           */
+  int64_t mid_pages;    /* pages held as mid                                           */
 } dkv_status;
 
 /* Host snapshot of the device state; every pointer may be NULL to skip it.
  * Sizes: pages  n_pages*page_bytes bytes; free_list n_pages int32;
- *        table  n_layers*max_requests*n_kv_heads*table_len int32;
- *        head_counts n_layers*max_requests*n_kv_heads*4 int32
- *                    {hi tokens, lo tokens, hi pages, lo pages};
+ *        table  n_layers*max_requests*n_kv_heads*row_len int32;
+ *        head_counts n_layers*max_requests*n_kv_heads*count_stride int32
+ *                    {hi tokens, lo tokens, hi pages, lo pages
+ *                     [, mid tokens, mid pages, 0, 0 with the mid tier]};
  *        req_state   n_layers*max_requests*4 int32 {active, N0, N, updates};
  *        pointers    2 int64 {start, end}. */
 typedef struct dkv_snapshot {
@@ -182,8 +211,10 @@ typedef struct dkv_snapshot {
 /* Create a pool on `cuda_device`: allocates the pages, the free list, page
  * tables, counters, scratch and the status word, all on the device. The
  * pool's memory is fixed for its lifetime. Errors: DKV_ERR_ARG for an invalid
- * config, DKV_ERR_UNSUPPORTED (head_dim != 128, G outside 1..8,
- * obs_window != 32), DKV_ERR_CUDA if an allocation fails (nothing leaks). */
+ * config (mid_enabled without lo_enabled included), DKV_ERR_UNSUPPORTED
+ * (head_dim != 128, G outside 1..8, obs_window != 32, mid_enabled with a
+ * tier whose T is not a multiple of 16), DKV_ERR_CUDA if an allocation fails
+ * (nothing leaks). */
 int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out);
 
 /* Synchronise the device, free everything the pool owns. NULL is a no-op. */
@@ -212,8 +243,9 @@ int dkv_pool_geometry(const dkv_pool* pool, dkv_geometry* out);
  *           the score S of every token (given or computed).
  *   Each head is granted ceil(N0/T_hi)+slack pages by one prefix sum over
  *   the heads (call order, then KV head) at the list start; hi tokens fill
- *   the grant from the left, lo tokens from the right, the unused middle
- *   pages are reclaimed at the list end by a second prefix sum.
+ *   the grant from the left (mid tokens the pages after them), lo tokens
+ *   from the right, the unused middle pages are reclaimed at the list end by
+ *   a second prefix sum.
  *
  * DECODE [Pol-G] [Mem-Gen]: every req_slots[i] must be active in `layer`.
  *   k, v    device fp16 [n_req][n_kv_heads][128]: the new token of each
@@ -267,7 +299,8 @@ int dkv_compact_step_prefilled(dkv_pool* pool, int32_t layer, int32_t n_req, con
 /* Decode attention of one layer over the mixed-precision pages [Impl-Kern]
  * [Bkg-Attn]: for each request i and query head h,
  *   out[i][h] = sum_j softmax_j(q[i][h] . k^_j / sqrt(128)) v^_j
- * over every stored token j of KV head h / G (hi pages, then lo pages), with
+ * over every stored token j of KV head h / G (hi pages, then mid pages, then
+ * lo pages), with
  * k^, v^ the dequantised codes. q: device fp16 [n_req][n_kv_heads*G][128];
  * out: device fp32 [n_req][n_kv_heads*G][128]. If update_scores != 0, each
  * stored token's score gains max over the group's heads of its softmax
@@ -336,10 +369,19 @@ int dkv_decode_attention_static(dkv_pool* pool, int32_t layer, int32_t n_req,
 int dkv_pool_set_thresholds(dkv_pool* pool, int32_t layer, const float* alpha_h, const float* alpha_l,
                             void* stream);
 
+/* The mid tier's threshold for each KV head of one layer [Pol-Ext]: from the
+ * next compaction step of `layer` on (stream order), head h's tokens are mid
+ * when I >= alpha_m[h]/N and not hi. alpha_m: host array of n_kv_heads
+ * floats, copied before the call returns. Until set, every head uses
+ * config.alpha_m. Errors: DKV_ERR_ARG (NULL, layer out of range, NaN, pool
+ * without the mid tier); DKV_ERR_CUDA. */
+int dkv_pool_set_mid_thresholds(dkv_pool* pool, int32_t layer, const float* alpha_m, void* stream);
+
 /* Return every page of request `req_slot` in every layer to the list end
  * (one prefix sum over (layer, KV head); within a head hi pages left to
- * right, then lo pages from the outermost inward) and clear its rows
- * [Mem-Gen]. Errors: DKV_ERR_ARG, DKV_ERR_STATE (slot active in no layer). */
+ * right, then lo pages from the outermost inward, then mid pages left to
+ * right) and clear its rows [Mem-Gen]. Errors: DKV_ERR_ARG, DKV_ERR_STATE
+ * (slot active in no layer). */
 int dkv_free_request(dkv_pool* pool, int32_t req_slot, void* stream);
 
 /* Synchronise the pool's device work and read the sticky status and counters. */

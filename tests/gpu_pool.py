@@ -17,6 +17,9 @@ class GPool:
                                                          if k in dict(dkv.dkv_config._fields_)}), 0)
         self.geom = dkv.dkv_pool_geometry(self.h)
         self.t_hi, self.t_lo, self.table_len = self.geom["t_hi"], self.geom["t_lo"], self.geom["table_len"]
+        # three-tier pools: rows of row_len entries (two-way part, then the
+        # one-way mid part), counters of 8 ints
+        self.t_mid, self.row_len, self.cstride = self.geom["t_mid"], self.geom["row_len"], self.geom["count_stride"]
 
     def close(self):
         if self.h is not None:
@@ -66,7 +69,7 @@ class GPool:
         return rc
 
     def snapshot(self, pages=True):
-        return dkv.dkv_pool_export(self.h, self.cfg, self.table_len, pages=pages)
+        return dkv.dkv_pool_export(self.h, self.cfg, self.row_len, pages=pages, count_stride=self.cstride)
 
     def status(self):
         return dkv.dkv_pool_status(self.h)

@@ -101,6 +101,14 @@ WORKLOADS: dict[str, Workload] = {
 }
 
 
+# The three-tier variant of a workload (its pool configuration only; the
+# inputs are the workload's own): a mid tier K8V2 between hi and lo from
+# alpha_m / N = 1 / N, 16 tokens per mid page (the attention kernel's chunk),
+# two slack pages in the prompt grant for the three partial pages a head can
+# leave.
+THREE_TIER = dict(mid_enabled=1, alpha_m=1.0, tokens_per_mid_page=16, prompt_grant_slack=2)
+
+
 def _rng(name: str, seed: int, role: str, step: int = 0) -> np.random.Generator:
     key = zlib.crc32(f"{name}/{role}".encode())
     return np.random.default_rng([seed, key, step])
