@@ -330,9 +330,10 @@ int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
  * the library's module is loaded. No cudaMalloc, cudaFree or other
  * allocating routine is called.
  *
- * Size limit: with U = n_req * n_kv_heads, C = ceil(max_n / 16) + 1 (max_n =
- * the largest current length N among the call's requests: prompt length
- * plus generated tokens, pruned tokens included, not the stored count) and
+ * Size limit: with U = n_req * n_kv_heads, C = ceil(max_n / 16) + 1, or + 2
+ * in a pool with the mid tier (max_n = the largest current length N among
+ * the call's requests: prompt length plus generated tokens, pruned tokens
+ * included, not the stored count) and
  * r(x) = x rounded up to 256, the call needs r(4UG) + r(4U(C/8 + 2)(128G + 16))
  * bytes, plus 64(G + 2)UC if update_scores != 0. A larger call returns
  * DKV_ERR_SCRATCH and queues nothing.
