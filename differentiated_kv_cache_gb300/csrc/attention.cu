@@ -107,9 +107,8 @@ struct AttnArgs {
   float* logit;       // [unit][max_chunks][lrow]: chunk rows of [query < G][16 slots] log2-domain
                       // logits, then (paged path) the 16 old scores and the page ID
   float* lse2;        // [unit][G]
-  ScanPart* vpart;    // [unit][max_vparts] victim-key partials of the epilogue's blocks, with
-  int* varrive;       // [unit] arrival counters (zero between calls); NULL: no victim keys
-  int max_parts, max_chunks, max_vparts;
+  int victims;        // 1: the score update leaves victim-key partials in the pool
+  int max_parts, max_chunks;
   int lrow;           // floats per chunk row: (G + 2) * 16
   int nwarps;         // warps of the attention grid
   int update;
@@ -1104,6 +1103,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps, kWarpsPerSm / kAttnWarps) k_a
 // ---------------------------------------------------------------------------
 constexpr int kEpiThreads = 256;
 constexpr int kEpiWarps = kEpiThreads / 32;
+static_assert(kEpiWarps == kVictimWarps, "one victim-key partial per epilogue warp");
 constexpr int kSlices = kD / 32;             // merge tasks per query: feature slices of 32
 constexpr int kMergeRegs = 4;                // partials per lane held in registers by a merge task
 
@@ -1412,15 +1412,11 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   // With score updates the block also leaves victim keys (pool scratch only);
   // the positions of its first step's slots load now, before the wait: the
   // table and the pages' position segments do not change in this call.
-  __shared__ int s_xc, s_last;
-  __shared__ float s_ic;
-  __shared__ ArgMin s_amin[(MID ? 3 : 2) * kEpiWarps];
-  const bool victims = a.update && a.vpart != nullptr && nb <= a.max_vparts;
+  const bool victims = a.update && a.victims && nb * kEpiWarps <= pv.max_vp;
   const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
   int vp[kPosRegs];
   if (victims) {
     load_positions<EC, MID>(pv, row_tab, paged, xb, nch, hc, vp);
-    if (threadIdx.x == 0) s_xc = -1;
   }
   float* s_rows = reinterpret_cast<float*>(smem + L.rows);
   float* s_lse = reinterpret_cast<float*>(smem + L.lse);
@@ -1568,62 +1564,23 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
     for (int e = 0; e < kPosRegs; e++) vp[e] = vq[e];
   }
   if (!victims) return;
-  // the block's victim keys, then the head's: the last of its nb blocks to
-  // arrive reduces the partials (warp 0, a partial a lane) and stamps the
-  // head's cache entry
-  if (xc >= 0) {                  // t_c is one slot of the head: at most one thread
-    s_xc = xc;
-    s_ic = ic;
-  }
-  if (MID) block_amin3(bh, bl, bm, s_amin);
-  else block_amin2(bh, bl, s_amin);
-  if (threadIdx.x == 0) {
-    ScanPart& part = a.vpart[(size_t)u * a.max_vparts + xb];
-    part.kh = bh.key;
-    part.sh = bh.slot;
-    part.kl = bl.key;
-    part.sl = bl.slot;
-    part.km = bm.key;
-    part.sm = bm.slot;
-    part.xc = s_xc;
-    part.ic = s_ic;
-    __threadfence();
-    s_last = atomicAdd(a.varrive + u, 1) == nb - 1;
-  }
-  __syncthreads();
-  if (!s_last || warp != 0) return;
-  __threadfence();
-  ArgMin rh{~0ull, -1}, rl{~0ull, -1}, rm{~0ull, -1};
-  int rx = -1;
-  float ri = 0.0f;
-  for (int q = lane; q < nb; q += 32) {
-    const ScanPart* part = a.vpart + (size_t)u * a.max_vparts + q;
-    rh = amin(rh, ArgMin{__ldcg(&part->kh), __ldcg(&part->sh)});
-    rl = amin(rl, ArgMin{__ldcg(&part->kl), __ldcg(&part->sl)});
-    if (MID) rm = amin(rm, ArgMin{__ldcg(&part->km), __ldcg(&part->sm)});
-    const int pxc = __ldcg(&part->xc);
-    if (pxc >= 0) {
-      rx = pxc;
-      ri = __ldcg(&part->ic);
-    }
-  }
+  // each warp leaves its share of the head's victim keys (one partial a
+  // warp, no barrier); the next generation step reduces the head's partials
 #pragma unroll
   for (int sft = 16; sft >= 1; sft >>= 1) {
-    rh = shfl_amin(rh, sft);
-    rl = shfl_amin(rl, sft);
-    if (MID) rm = shfl_amin(rm, sft);
+    bh = shfl_amin(bh, sft);
+    bl = shfl_amin(bl, sft);
+    if (MID) bm = shfl_amin(bm, sft);
   }
-  const unsigned has = __ballot_sync(0xffffffffu, rx >= 0);
+  const unsigned has = __ballot_sync(0xffffffffu, xc >= 0);   // t_c is one slot of the head
   const int src = has ? __ffs(has) - 1 : 0;
-  rx = __shfl_sync(0xffffffffu, rx, src);
-  ri = __shfl_sync(0xffffffffu, ri, src);
-  if (lane == 0) {
-    a.varrive[u] = 0;             // ready for the next call
-    VictimCache* vc = pv.vc(a.layer, sa.slots[i], kvh);
-    vc->p = ScanPart{rh.key, rl.key, rh.slot, rl.slot, rx, ri, rm.key, rm.slot, 0};
-    vc->n_stamp = vN;
-    vc->u_stamp = vupd;
-  }
+  xc = __shfl_sync(0xffffffffu, xc, src);
+  ic = __shfl_sync(0xffffffffu, ic, src);
+  if (lane == 0)
+    pv.vpart(a.layer, sa.slots[i], kvh)[xb * kEpiWarps + warp] =
+        VictimPart{bh.key, bl.key, bm.key, bh.slot, bl.slot, bm.slot, xc, ic, vN, vupd, nb * kEpiWarps};
+  if (xb == 0 && threadIdx.x == 0)         // the head's stamps, in their own array
+    *pv.vst(a.layer, sa.slots[i], kvh) = make_int4(vN, vupd, nb * kEpiWarps, 0);
 }
 
 constexpr int kMaxAttnSmem = 220 * 1024;
@@ -1739,9 +1696,7 @@ cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tok
   a.part = P.sc.apart;
   a.logit = P.sc.alogit;
   a.lse2 = P.sc.alse;
-  a.vpart = P.sc.vpart;
-  a.varrive = P.sc.varrive;
-  a.max_vparts = P.sc.max_vparts;
+  a.victims = 1;
   a.max_parts = P.sc.max_splits;
   a.max_chunks = P.sc.max_chunks;
   a.update = update_scores;
@@ -1816,9 +1771,7 @@ cudaError_t launch_attention_static(Pool& P, int layer, const SlotArgs& sa, int 
   a.logit = reinterpret_cast<float*>(base + L.logit);
   a.max_parts = L.max_parts;
   a.max_chunks = L.max_chunks;
-  a.vpart = nullptr;              // no victim keys: the next generation step scans
-  a.varrive = nullptr;
-  a.max_vparts = 0;
+  a.victims = 0;                  // no victim keys: the next generation step scans
   a.update = update_scores;
   a.layer = layer;
   // Nothing in the array needs clearing: every value a call reads from it

@@ -32,24 +32,41 @@ __device__ __forceinline__ float key_importance(unsigned long long key) {
 // and makes the plan.
 constexpr int kScanSlots = kPlanThreads * 8;   // 2048: the pool sizes its scan partials with it
 
-// The plan of one head from the reduced scan (thread 0 of the last CTA):
-// bh / bl / bm the least important hi token outside the window, lo token and
-// mid token (three-tier pools, MID), xc / ic the hi slot and importance of t_c.
+// What a head's plan needs besides its victim keys, loaded at the plan
+// kernel's start with the request state (one round of loads for both): the
+// length after the append, the tier counts and page counts before the step,
+// and the head's thresholds.
+struct HeadIn {
+  int n, nh, nl, nm, php, plp, pmp;
+  float2 al;
+  float am;
+};
+
 template <bool MID>
-__device__ void decide_plan(const PoolView& pv, int layer, int slot, int kvh, int unit, ArgMin bh, ArgMin bl, ArgMin bm,
-                            int xc_in, float ic_in, DecodePlan* plans) {
-  const int* rq = pv.rq(layer, slot);
-  const int n = rq[2] + 1;
+__device__ __forceinline__ HeadIn load_head(const PoolView& pv, int layer, int slot, int kvh, int n) {
   const int* cn = pv.cnt(layer, slot, kvh);
-  const int nh = cn[0], nl = cn[1], php = cn[2], plp = cn[3];
+  const int4 c4 = *reinterpret_cast<const int4*>(cn);   // counter rows start on 16-byte boundaries
+  const int2 m2 = MID ? *reinterpret_cast<const int2*>(cn + 4) : make_int2(0, 0);
+  return HeadIn{n, c4.x, c4.y, m2.x, c4.z, c4.w, m2.y, pv.thresholds(layer, kvh),
+                MID ? pv.alpha_m[(size_t)layer * pv.hkv + kvh] : 0.0f};
+}
+
+// The plan of one head (one thread): bh / bl / bm the least important hi
+// token outside the window, lo token and mid token (three-tier pools, MID),
+// xc / ic the hi slot and importance of t_c; h the head's state.
+template <bool MID>
+__device__ void decide_plan(const PoolView& pv, const HeadIn& h, int unit, ArgMin bh, ArgMin bl, ArgMin bm,
+                            int xc_in, float ic_in, DecodePlan* plans) {
+  const int n = h.n;
+  const int nh = h.nh, nl = h.nl, php = h.php, plp = h.plp;
   constexpr bool three = MID;
-  const int nm = three ? cn[4] : 0, pmp = three ? cn[5] : 0;
+  const int nm = three ? h.nm : 0, pmp = three ? h.pmp : 0;
   const int pc = n - pv.window - 1;
   int s_xc = xc_in;
   float s_ic = ic_in;
-  const float2 al = pv.thresholds(layer, kvh);   // the head's pair
+  const float2 al = h.al;                        // the head's pair
   const float th_h = __fdiv_rn(al.x, (float)n), th_l = __fdiv_rn(al.y, (float)n);
-  const float th_m = three ? __fdiv_rn(pv.alpha_m[(size_t)layer * pv.hkv + kvh], (float)n) : 0.0f;
+  const float th_m = three ? __fdiv_rn(h.am, (float)n) : 0.0f;
   auto cls = [&](float imp) { return three ? classify3(imp, th_h, th_m, th_l) : classify(imp, th_h, th_l, pv.lo_enabled); };
   DecodePlan p;
   p.err = 0;
@@ -146,18 +163,54 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
   const int unit = i * pv.hkv + kvh;
   const int* rq = pv.rq(layer, slot);
   const int n0 = rq[1], n = rq[2] + 1, upd = rq[3];
-  const int* cn = pv.cnt(layer, slot, kvh);
-  const int nh = cn[0], nl = cn[1], nm = MID ? cn[4] : 0;
-  // The victim keys the last decode-attention call's score update left for
-  // this head, while the head is as that call left it (same length, same
-  // update count): no scan. The condition is the same for every thread.
-  const VictimCache* vc = pv.vc(layer, slot, kvh);
-  if (__ldcg(&vc->n_stamp) == rq[2] && __ldcg(&vc->u_stamp) == upd) {
-    if (c == 0 && threadIdx.x == 0) {
-      const ArgMin ch{__ldcg(&vc->p.kh), __ldcg(&vc->p.sh)}, cl{__ldcg(&vc->p.kl), __ldcg(&vc->p.sl)};
-      const ArgMin cm = MID ? ArgMin{__ldcg(&vc->p.km), __ldcg(&vc->p.sm)} : ArgMin{~0ull, -1};
-      decide_plan<MID>(pv, layer, slot, kvh, unit, ch, cl, cm, __ldcg(&vc->p.xc), __ldcg(&vc->p.ic), plans);
+  // the head's counts and thresholds, loaded in the same round as the
+  // request state and the victim-key stamps below
+  const HeadIn hin = load_head<MID>(pv, layer, slot, kvh, n);
+  const int nh = hin.nh, nl = hin.nl, nm = hin.nm;
+  // The victim-key partials the last decode-attention call's score update
+  // left for this head, while the head is as that call left it (same length,
+  // same update count): the first CTA's first warp reduces them (a partial
+  // a lane), no scan. The condition is the same for every thread of the
+  // head's CTAs.
+  const VictimPart* vps = pv.vpart(layer, slot, kvh);
+  const int4 vs4 = __ldcg(pv.vst(layer, slot, kvh));
+  const int vcount = vs4.z;
+  // The first warp of the head's first CTA loads up to 32 partials before it
+  // knows whether they are valid, so that they arrive with the stamps (one
+  // round of memory latency instead of two).
+  ArgMin ch{~0ull, -1}, cl{~0ull, -1}, cm{~0ull, -1};
+  int xc = -1;
+  float ic = 0.0f;
+  auto take = [&](const VictimPart* vp) {
+    ch = amin(ch, ArgMin{__ldcg(&vp->kh), __ldcg(&vp->sh)});
+    cl = amin(cl, ArgMin{__ldcg(&vp->kl), __ldcg(&vp->sl)});
+    if (MID) cm = amin(cm, ArgMin{__ldcg(&vp->km), __ldcg(&vp->sm)});
+    const int pxc = __ldcg(&vp->xc);
+    const float pic = __ldcg(&vp->ic);
+    if (pxc >= 0) {
+      xc = pxc;
+      ic = pic;
     }
+  };
+  if (c == 0 && threadIdx.x < 32 && threadIdx.x < pv.max_vp) take(vps + threadIdx.x);
+  if (vs4.x == rq[2] && vs4.y == upd && vcount >= 1 && vcount <= pv.max_vp) {
+    if (c != 0 || threadIdx.x >= 32) return;
+    if (threadIdx.x >= vcount) {            // speculative loads past the call's partials
+      ch = cl = cm = ArgMin{~0ull, -1};
+      xc = -1;
+    }
+    for (int q = threadIdx.x + 32; q < vcount; q += 32) take(vps + q);
+#pragma unroll
+    for (int sft = 16; sft >= 1; sft >>= 1) {
+      ch = shfl_amin(ch, sft);
+      cl = shfl_amin(cl, sft);
+      if (MID) cm = shfl_amin(cm, sft);
+    }
+    const unsigned has = __ballot_sync(0xffffffffu, xc >= 0);
+    const int src = has ? __ffs(has) - 1 : 0;
+    xc = __shfl_sync(0xffffffffu, xc, src);
+    ic = __shfl_sync(0xffffffffu, ic, src);
+    if (threadIdx.x == 0) decide_plan<MID>(pv, hin, unit, ch, cl, cm, xc, ic, plans);
     return;
   }
   const int nst = nh + nl + nm;             // slots: hi, then lo, then mid
@@ -219,8 +272,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
   __threadfence();
   arrivals[unit] = 0;                       // ready for the next step
   ArgMin rh{~0ull, -1}, rl{~0ull, -1}, rm{~0ull, -1};
-  int xc = -1;
-  float ic = 0.0f;
+  int rx = -1;
+  float ri = 0.0f;
   for (int q = 0; q < nparts; q++) {
     const ScanPart& part = parts[(size_t)unit * max_parts + q];
     const ArgMin ph{__ldcg(&part.kh), __ldcg(&part.sh)}, pl{__ldcg(&part.kl), __ldcg(&part.sl)};
@@ -228,9 +281,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_decode_plan(PoolView pv, int l
     rl = amin(rl, pl);
     if (MID) rm = amin(rm, ArgMin{__ldcg(&part.km), __ldcg(&part.sm)});
     const int pxc = __ldcg(&part.xc);
-    if (pxc >= 0) { xc = pxc; ic = __ldcg(&part.ic); }
+    const float pic = __ldcg(&part.ic);
+    if (pxc >= 0) { rx = pxc; ri = pic; }
   }
-  decide_plan<MID>(pv, layer, slot, kvh, unit, rh, rl, rm, xc, ic, plans);
+  decide_plan<MID>(pv, hin, unit, rh, rl, rm, rx, ri, plans);
 }
 
 // Token record staged in shared memory between the read and write phases.

@@ -68,14 +68,22 @@ struct ScanPart {
   int sm, pad;
 };
 
-// The victim keys of a head as the next generation step will see them,
-// computed by the score update of a decode-attention call, stamped with the
-// request's length N and update count after that call. A generation step
-// uses them only while both stamps still match the request state, else it
-// scans the head.
-struct VictimCache {
-  ScanPart p;
-  int n_stamp, u_stamp;
+// One warp's share of a head's victim keys as the next generation step will
+// see them, left by the score update of a decode-attention call: the argmin
+// keys and slots of the hi tokens outside the next step's window, of the lo
+// tokens and of the mid tokens among the warp's slots, and the hi slot and
+// importance of t_c if the warp holds it (-1 otherwise). Every partial is
+// stamped with the request's length N and update count after that call and
+// with the number of partials the call left for the head; the head's first
+// block also writes these stamps into a small array of their own (one 16-byte
+// entry per head, read by every CTA of the next step's plan). A generation
+// step reduces a head's partials while its stamps still match the request
+// state, else it scans the head.
+struct VictimPart {
+  unsigned long long kh, kl, km;
+  int sh, sl, sm, xc;
+  float ic;
+  int n_stamp, u_stamp, count;
 };
 
 // Device view of a pool, passed by value to every kernel.
@@ -87,7 +95,8 @@ struct PoolView {
   int* req;          // [layer][slot][4]: active, N0, N, updates
   Ctl* ctl;
   CallArgs* call;
-  VictimCache* vcache;  // [layer][slot][kvh]
+  VictimPart* vparts;   // [layer][slot][kvh][max_vp]
+  int4* vstamp;         // [layer][slot][kvh]: {N, update count, partials, 0} of the call that left them
   float2* alpha;        // [layer][kvh]: the head's (alpha_h, alpha_l)
   float* alpha_m;       // [layer][kvh]: the head's alpha_m (three-tier pools)
   int n_pages, page_bytes, n_layers, hkv, G, max_req, max_seq, L;
@@ -96,6 +105,7 @@ struct PoolView {
   // one-way mid table (Lm entries); counters are {hi tok, lo tok, hi pages,
   // lo pages, mid tok, mid pages, 0, 0}. Two-tier pools: Lm = 0, 4 counters.
   int mid_enabled, Lm, Lrow, cstride;
+  int max_vp;           // victim-key partials per head (epilogue blocks x warps)
   TierGeom hi, lo, mid;
 
   __device__ __forceinline__ int* row(int layer, int slot, int kvh) const {
@@ -112,8 +122,11 @@ struct PoolView {
   __device__ __forceinline__ const TierGeom& geom(int tier) const {
     return tier == kTierHi ? hi : (tier == kTierLo ? lo : mid);
   }
-  __device__ __forceinline__ VictimCache* vc(int layer, int slot, int kvh) const {
-    return vcache + ((size_t)layer * max_req + slot) * hkv + kvh;
+  __device__ __forceinline__ int4* vst(int layer, int slot, int kvh) const {
+    return vstamp + ((size_t)layer * max_req + slot) * hkv + kvh;
+  }
+  __device__ __forceinline__ VictimPart* vpart(int layer, int slot, int kvh) const {
+    return vparts + (((size_t)layer * max_req + slot) * hkv + kvh) * max_vp;
   }
   __device__ __forceinline__ float2 thresholds(int layer, int kvh) const {
     return alpha[(size_t)layer * hkv + kvh];

@@ -11,6 +11,7 @@ namespace dkv {
 constexpr int kKeyBlock = 128;     // prompt tokens per scoring / classification block
 constexpr int kChunk = 16;         // decode-attention tokens per mma chunk
 constexpr int kAttnWarps = 4;      // warps per decode-attention CTA
+constexpr int kVictimWarps = 8;    // warps of an attention epilogue block, each leaving a victim-key partial
 // Decode-attention scratch row per 16-slot chunk (floats): the log2-domain
 // logits [query < G][16 slots], then (paged path) the scores before the
 // update [16 slots] at row G and the chunk's page ID at row G + 1.
@@ -150,14 +151,11 @@ struct Scratch {
   DecodePlan* dplan;    // [units]
   ScanPart* dscan;      // [units][max_scan] partials of the generation-phase scan
   int* darrive;         // [units] scan CTAs arrived (zero between calls)
-  // victim keys from the attention epilogue's score update
-  ScanPart* vpart;      // [units][max_vparts] partials, one per epilogue block of a head
-  int* varrive;         // [units] epilogue blocks arrived (zero between calls)
   // decode attention
   float* apart;         // [units][max_splits][G*(128+2)]
   float* alogit;        // [units][max_chunks][(G + 2) * 16]: per chunk logits, old scores, page ID
   float* alse;          // [units][G]
-  int nkb_cap, grant_cap, max_splits, max_chunks, max_scan, max_vparts;
+  int nkb_cap, grant_cap, max_splits, max_chunks, max_scan;
 };
 
 // Host side of a pool.

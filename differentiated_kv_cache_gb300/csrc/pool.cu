@@ -181,7 +181,9 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   s.max_chunks = (cfg->max_seq_len + kChunk - 1) / kChunk + (three ? 2 : 1);
   s.max_splits = s.max_chunks / 8 + 2;   // attention partials per head (>= 8 chunks per warp)
   s.max_scan = (cfg->max_seq_len + 1 + 2047) / 2048;   // generation-phase scan CTAs per head
-  s.max_vparts = (s.max_chunks + 63) / 64;              // attention epilogue blocks per head (>= 64 chunks each)
+  // victim-key partials per head: a warp of every attention epilogue block
+  // of the head (>= 64 chunks a block)
+  v.max_vp = (s.max_chunks + 63) / 64 * kVictimWarps;
   cudaError_t e = cudaSuccess;
   auto A = [&](auto** ptr, size_t n) {
     if (e == cudaSuccess) e = dev_alloc(P, ptr, n);
@@ -193,7 +195,8 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&v.req, (size_t)cfg->n_layers * cfg->max_requests * 4);
   A(&v.ctl, 1);
   A(&v.call, 1);
-  A(&v.vcache, heads);
+  A(&v.vparts, heads * v.max_vp);
+  A(&v.vstamp, heads);
   A(&v.alpha, (size_t)cfg->n_layers * cfg->n_kv_heads);
   A(&v.alpha_m, (size_t)cfg->n_layers * cfg->n_kv_heads);
   A(&s.partial, units * s.nkb_cap * kObs * G);
@@ -212,15 +215,13 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&s.dplan, units);
   A(&s.dscan, units * s.max_scan);
   A(&s.darrive, units);
-  A(&s.vpart, units * s.max_vparts);
-  A(&s.varrive, units);
   A(&s.apart, units * s.max_splits * (G * kD + 2 * kMaxG));
   A(&s.alogit, units * s.max_chunks * (G + 2) * kChunk);
   A(&s.alse, units * G);
   if (e == cudaSuccess) e = cudaMemset(s.darrive, 0, units * sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(s.varrive, 0, units * sizeof(int));
   // stamps -1: no head has victim keys yet
-  if (e == cudaSuccess) e = cudaMemset(v.vcache, 0xff, heads * sizeof(VictimCache));
+  if (e == cudaSuccess) e = cudaMemset(v.vparts, 0xff, heads * v.max_vp * sizeof(VictimPart));
+  if (e == cudaSuccess) e = cudaMemset(v.vstamp, 0xff, heads * sizeof(int4));
   if (e == cudaSuccess) e = cudaMemset(v.pages, 0, (size_t)cfg->n_pages * cfg->page_bytes);
   if (e == cudaSuccess) e = cudaMemset(v.table, 0xff, heads * v.Lrow * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(v.counts, 0, heads * v.cstride * sizeof(int));
@@ -588,8 +589,6 @@ int dkv_pool_clear_error(dkv_pool* pool) {
   if (cudaMemcpy(P.pv.ctl, &c, sizeof(Ctl), cudaMemcpyHostToDevice) != cudaSuccess) return DKV_ERR_CUDA;
   // a step cut short can leave generation-phase scan or epilogue arrivals behind
   if (cudaMemset(P.sc.darrive, 0, (size_t)P.cfg.max_requests * P.cfg.n_kv_heads * sizeof(int)) != cudaSuccess)
-    return DKV_ERR_CUDA;
-  if (cudaMemset(P.sc.varrive, 0, (size_t)P.cfg.max_requests * P.cfg.n_kv_heads * sizeof(int)) != cudaSuccess)
     return DKV_ERR_CUDA;
   std::vector<int> rq((size_t)P.cfg.n_layers * P.cfg.max_requests * 4);
   if (cudaMemcpy(rq.data(), P.pv.req, rq.size() * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)

@@ -21,6 +21,7 @@ class Churn:
     n_kv_heads: int
     t_hi: int
     slack: int = 1
+    tiers: int = 2                                 # precision tiers of the pool (3 with mid)
     prompt_lens: tuple = (100, 700)
     gen_lens: tuple = (5, 40)
     rate: float = 0.35
@@ -34,7 +35,7 @@ class Churn:
     def _growth_pages(self, gen: int) -> int:
         # pages a request may still take while it generates `gen` tokens:
         # a new page per tier at most every t_hi tokens, plus one each
-        return 2 * self.n_kv_heads * (gen // self.t_hi + 2)
+        return self.tiers * self.n_kv_heads * (gen // self.t_hi + 2)
 
     def tick(self, free_pages: int) -> list:
         """Operations of one tick, in order: ("prompt", slot, n0, seed),

@@ -45,11 +45,16 @@ def step_inputs(n: int, tick: int):
             workloads.random_fp16((n, H * G, 128), 90000 + tick, scale=2.0))
 
 
-@pytest.mark.parametrize("reclaim", [1, 0])
-def test_oracle_churn_invariants(reclaim):
-    cfg = churn_cfg(reclaim_in_decode=reclaim)
+# the three-tier pool (mid tier K8V2; its pages in the one-way part of each row)
+MID = dict(mid_enabled=1, alpha_m=0.8, tokens_per_mid_page=16, prompt_grant_slack=2)
+
+
+@pytest.mark.parametrize("reclaim,mid", [(1, 0), (0, 0), (1, 1)])
+def test_oracle_churn_invariants(reclaim, mid):
+    cfg = churn_cfg(reclaim_in_decode=reclaim, **(MID if mid else {}))
     op = oracle.Pool(cfg)
-    ch = Churn(seed=3 + reclaim, max_requests=cfg["max_requests"], n_kv_heads=H, t_hi=op.t_hi)
+    ch = Churn(seed=3 + reclaim + 5 * mid, max_requests=cfg["max_requests"], n_kv_heads=H, t_hi=op.t_hi,
+               slack=cfg["prompt_grant_slack"], tiers=3 if mid else 2)
     n_ops = 0
     for tick in range(400):
         free = int(op.pointers[1] - op.pointers[0])
@@ -67,7 +72,8 @@ def test_oracle_churn_invariants(reclaim):
             else:
                 assert op.free_request(o[1]) == 0
             n_ops += 1
-            pagefmt.check_invariants(op.snapshot(), op.t_hi, op.t_lo, cfg["n_pages"], reclaim=bool(reclaim))
+            pagefmt.check_invariants(op.snapshot(), op.t_hi, op.t_lo, cfg["n_pages"], reclaim=bool(reclaim),
+                                     table_len=op.table_len, t_mid=op.t_mid)
     start, end = (int(x) for x in op.pointers)
     assert start >= 3 * cfg["n_pages"] and end >= 4 * cfg["n_pages"], (start, end)
     for s in sorted(ch.active):
@@ -79,7 +85,8 @@ def test_oracle_churn_invariants(reclaim):
 
 
 @pytest.mark.gpu
-def test_gpu_churn_bit_exact():
+@pytest.mark.parametrize("mid", [0, 1])
+def test_gpu_churn_bit_exact(mid):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -88,10 +95,11 @@ def test_gpu_churn_bit_exact():
     from tests.gpu_pool import GPool, load_into
     dkv.build.build()
     dkv.load()
-    cfg = churn_cfg()
+    cfg = churn_cfg(**(MID if mid else {}))
     op = oracle.Pool(cfg)
     with GPool(cfg) as gp:
-        ch = Churn(seed=11, max_requests=cfg["max_requests"], n_kv_heads=H, t_hi=gp.t_hi)
+        ch = Churn(seed=11 + mid, max_requests=cfg["max_requests"], n_kv_heads=H, t_hi=gp.t_hi,
+                   slack=cfg["prompt_grant_slack"], tiers=3 if mid else 2)
         q = None
         for tick in range(300):
             free = gp.status()["free_pages"]
@@ -113,7 +121,7 @@ def test_gpu_churn_bit_exact():
                     assert op.free_request(o[1]) == 0
                 assert gp.status()["error"] == 0
                 parity.compare_states(gp.snapshot(), op.snapshot(), gp.t_hi, gp.t_lo, cfg["n_pages"],
-                                      cfg["page_bytes"])
+                                      cfg["page_bytes"], table_len=gp.table_len, t_mid=gp.t_mid)
         st = gp.status()
         assert st["list_start"] >= 3 * cfg["n_pages"], st
         print(f"{ch.n_arrived} requests; list start {st['list_start']} end {st['list_end']}")
