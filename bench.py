@@ -61,23 +61,23 @@ LAUNCHES = {"prompt": 10, "decode": 3, "attention": 2, "free": 1}
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 119_645_952 + 4_707_072 + 30_606_336,
+    "bytes_per_call": 119_689_216 + 4_951_040 + 30_590_976,
     "sources": {
-        "attention.cu": "b0273bced4432a3eca8deb4e5a1f832c3de2fa4a1113c47c78b43f15ecfbc1cd",
-        "dkv_common.cuh": "bcd6734e6c5b4bd5fc941201972200f49e4eed4b73ae8e36152d81d14831054a",
-        "dkv_kernels.cuh": "8b696d22cc7aad5a45af9c7632518d943f3eb86e086728ea9c67a90bc1b2ce06",
+        "attention.cu": "aba0ef560a7264eff077da19b8224b65252213fcf16a88c67763fe03177957ba",
+        "dkv_common.cuh": "ba5510123ecbe1069424c0470463527dccb53b0444f61c6e606f7028ef848f8c",
+        "dkv_kernels.cuh": "55585a4674a5f894f501562c639d98907e2766ec1b961e0a84fd24bc896b76db",
     },
 }
 PROMPT_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 1_018_308_096 + 103_099_648,
+    "bytes_per_call": 1_018_202_624 + 103_041_024,
     "sources": {
-        "prompt.cu": "e7677c71cd5c346b45bb412ebcba1827dc7640e58abe352da3618341f309fde7",
+        "prompt.cu": "112318ce1a431d52729ded02427ab6e7b9e88199071cb46c7cfdd9ec55d07845",
         "prompt_tc.cu": "fa63d0ced7a2f9d8266fe4673083378e67dddf037238d1f050656313a455b8c1",
-        "alloc.cu": "4b1b90d8af16eca24a790b2bfff5e6c9ac5de18f04712cde3b02fdaedde08e40",
+        "alloc.cu": "3cb94c20d08da98fe7db21a35c9243c2b56696d18fe5239f842f1bd8ca6b512a",
         "dkv_tc.cuh": "acb3452effe630c9cbc898bc8a87929dbf4ecd2f43abeb537319b63ad151c2fb",
-        "dkv_common.cuh": "bcd6734e6c5b4bd5fc941201972200f49e4eed4b73ae8e36152d81d14831054a",
-        "dkv_kernels.cuh": "8b696d22cc7aad5a45af9c7632518d943f3eb86e086728ea9c67a90bc1b2ce06",
+        "dkv_common.cuh": "ba5510123ecbe1069424c0470463527dccb53b0444f61c6e606f7028ef848f8c",
+        "dkv_kernels.cuh": "55585a4674a5f894f501562c639d98907e2766ec1b961e0a84fd24bc896b76db",
     },
 }
 L2_FLUSH_BYTES = 256 << 20
