@@ -105,11 +105,11 @@ struct AttnArgs {
   float* part;        // [unit][max_parts][G*128 + 16]: O (G x 128), m (8), l (8); a
                       // multiple of 4 floats so every record is 16-byte aligned
   float* logit;       // [unit][max_chunks][lrow]: chunk rows of [query < G][16 slots] log2-domain
-                      // logits, then (paged path) the 16 old scores and the page ID
+                      // logits
   float* lse2;        // [unit][G]
   int victims;        // 1: the score update leaves victim-key partials in the pool
   int max_parts, max_chunks;
-  int lrow;           // floats per chunk row: (G + 2) * 16
+  int lrow;           // floats per chunk row: G * 16
   int nwarps;         // warps of the attention grid
   int update;
   int layer;
@@ -641,7 +641,7 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
       if (sA >= count) l2[c][0] = l2[c][1] = -INFINITY;
       if (sB >= count) l2[c][2] = l2[c][3] = -INFINITY;
     }
-    if (lg != nullptr) {           // scratch row of the chunk: logits, old scores, page ID
+    if (lg != nullptr) {           // scratch row of the chunk: its logits
       float* lc = lg + c * lrow;
       if (2 * t < G) {
         lc[(2 * t) * kChunk + jA] = l2[c][0];
@@ -650,11 +650,6 @@ __device__ __forceinline__ void attend_chunks(AttnState& S, const uint8_t* sb, c
       if (2 * t + 1 < G) {
         lc[(2 * t + 1) * kChunk + jA] = l2[c][1];
         lc[(2 * t + 1) * kChunk + jB] = l2[c][3];
-      }
-      if (t == 0) {
-        lc[G * kChunk + jA] = *reinterpret_cast<const float*>(sb + tg.off[4] + 4 * sA);
-        lc[G * kChunk + jB] = *reinterpret_cast<const float*>(sb + tg.off[4] + 4 * sB);
-        if (g == 0) reinterpret_cast<int*>(lc)[(G + 1) * kChunk] = pid;
       }
     }
   }
@@ -883,7 +878,7 @@ __global__ void __launch_bounds__(32 * W, kWarpsPerSm / W) k_attn_paged(PoolView
       const int st = xi % kPageStages;
       const uint32_t bar = bar0 + 8 * st;
       const uint32_t bytes =
-          dsc.z < 0 ? pv.hi.off[5] : (MID && (dsc.z & kDescMid) ? pv.mid.off[5] : pv.lo.off[5]);
+          dsc.z < 0 ? pv.hi.off[4] : (MID && (dsc.z & kDescMid) ? pv.mid.off[4] : pv.lo.off[4]);
       mbar_expect_tx(bar, bytes);
       bulk_g2s(smem_u32(wst + st * a.stage_bytes), pv.page(dsc.y), bytes, bar);
     }
@@ -1127,7 +1122,7 @@ struct EpiSmem {
   int rows, lse, misc, total;
   __host__ __device__ EpiSmem(int G, bool update) {
     rows = 0;
-    lse = update ? epi_chunks(G) * (G + 2) * kChunk * 4 : 0;
+    lse = update ? epi_chunks(G) * G * kChunk * 4 : 0;
     misc = lse + 4 * kMaxG;
     total = misc + 16;
   }
@@ -1324,11 +1319,15 @@ struct HeadChunks {
 };
 
 // Positions of this thread's slots in chunk step `step` of the head, in the
-// order the score-update loops visit them (0 where a slot is not stored).
-// Read from the pages through the table, neither of which the call changes.
+// order the score-update loops visit them (0 where a slot is not stored),
+// and on the paged path their scores before the update and each quad's page
+// ID (vs, vd). Read from the pages through the table before the grid-
+// dependency wait: the attention kernel changes neither (the scores are
+// written by this epilogue only), and a page's score and position segments
+// of a chunk share one 128-byte line.
 template <int EC, bool MID>
 __device__ __forceinline__ void load_positions(const PoolView& pv, const int* row_tab, bool paged, int step, int nch,
-                                               const HeadChunks<MID>& hc, int* vp) {
+                                               const HeadChunks<MID>& hc, int* vp, float* vs, int* vd) {
   const int c0 = step * EC, c1 = min(nch, c0 + EC);
 #pragma unroll
   for (int e = 0; e < kPosRegs; e++) vp[e] = 0;
@@ -1346,10 +1345,16 @@ __device__ __forceinline__ void load_positions(const PoolView& pv, const int* ro
       const int d = tg.div(s0);
       const int pid = __ldg(row_tab + tier_entry<MID>(pv, tier, d));
       const int4 p = __ldcg(reinterpret_cast<const int4*>(pv.page(pid) + tg.off[5]) + ((s0 - d * tg.t) >> 2));
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(pv.page(pid) + tg.off[4]) + ((s0 - d * tg.t) >> 2));
       vp[4 * k] = p.x;
       vp[4 * k + 1] = p.y;
       vp[4 * k + 2] = p.z;
       vp[4 * k + 3] = p.w;
+      vs[4 * k] = o.x;
+      vs[4 * k + 1] = o.y;
+      vs[4 * k + 2] = o.z;
+      vs[4 * k + 3] = o.w;
+      vd[k] = pid;
     }
   } else {
 #pragma unroll
@@ -1414,10 +1419,9 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
   // table and the pages' position segments do not change in this call.
   const bool victims = a.update && a.victims && nb * kEpiWarps <= pv.max_vp;
   const int* row_tab = pv.row(a.layer, sa.slots[i], kvh);
-  int vp[kPosRegs];
-  if (victims) {
-    load_positions<EC, MID>(pv, row_tab, paged, xb, nch, hc, vp);
-  }
+  int vp[kPosRegs], vd[kPosRegs / 4];
+  float vs[kPosRegs];
+  if (a.update) load_positions<EC, MID>(pv, row_tab, paged, xb, nch, hc, vp, vs, vd);
   float* s_rows = reinterpret_cast<float*>(smem + L.rows);
   float* s_lse = reinterpret_cast<float*>(smem + L.lse);
   const uint32_t bar = smem_u32(smem + L.misc);
@@ -1483,8 +1487,9 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
       }
     }
     // the positions of the block's next step, in flight during this one
-    int vq[kPosRegs];
-    if (victims && step + nb < nsteps) load_positions<EC, MID>(pv, row_tab, paged, step + nb, nch, hc, vq);
+    int vq[kPosRegs], vdq[kPosRegs / 4];
+    float vsq[kPosRegs];
+    if (step + nb < nsteps) load_positions<EC, MID>(pv, row_tab, paged, step + nb, nch, hc, vq, vsq, vdq);
     // one decision for the block, so that no thread is left at a barrier
     if (__syncthreads_or(!mbar_wait_bounded(bar, it & 1))) {
       if (threadIdx.x == 0 && atomicCAS(&pv.ctl->error, 0, DKV_ERR_TIMEOUT) == 0) pv.ctl->error_info = u;
@@ -1516,8 +1521,8 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
           mx.z = fmaxf(mx.z, v.z - lse[qh]);
           mx.w = fmaxf(mx.w, v.w - lse[qh]);
         }
-        const float4 old = *reinterpret_cast<const float4*>(row + G * kChunk + j0);
-        const int pid = reinterpret_cast<const int*>(row)[(G + 1) * kChunk];
+        const float4 old = make_float4(vs[4 * k], vs[4 * k + 1], vs[4 * k + 2], vs[4 * k + 3]);
+        const int pid = vd[k];
         const TierGeom& tg = tier_geom<MID>(pv, tier);
         float* sp = reinterpret_cast<float*>(pv.page(pid) + tg.off[4]) + (s0 - tg.div(s0) * tg.t);
         const float4 nw = make_float4(old.x + fast_exp2(mx.x), old.y + fast_exp2(mx.y), old.z + fast_exp2(mx.z),
@@ -1561,7 +1566,12 @@ __global__ void __launch_bounds__(kEpiThreads, 4) k_attn_epi(PoolView pv, AttnAr
       }
     }
 #pragma unroll
-    for (int e = 0; e < kPosRegs; e++) vp[e] = vq[e];
+    for (int e = 0; e < kPosRegs; e++) {
+      vp[e] = vq[e];
+      vs[e] = vsq[e];
+    }
+#pragma unroll
+    for (int e = 0; e < kPosRegs / 4; e++) vd[e] = vdq[e];
   }
   if (!victims) return;
   // each warp leaves its share of the head's victim keys (one partial a
@@ -1634,8 +1644,8 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   if (paged) {
     a.mseg = 0;
     a.maxp = 1;
-    a.stage_bytes = std::max(P.pv.hi.off[5], P.pv.lo.off[5]);
-    if (P.pv.mid_enabled) a.stage_bytes = std::max(a.stage_bytes, P.pv.mid.off[5]);
+    a.stage_bytes = std::max(P.pv.hi.off[4], P.pv.lo.off[4]);
+    if (P.pv.mid_enabled) a.stage_bytes = std::max(a.stage_bytes, P.pv.mid.off[4]);
     // per warp its page ring with mbarriers and its descriptor table; the head prefix
     auto need = [&](int warps) { return warps * (kPageStages * (a.stage_bytes + 8) + 64 * 16) + 4 * (n_units + 1); };
     w = need(kWarpsPerSm) <= kMaxAttnSmem ? kWarpsPerSm : kAttnWarps;
@@ -1649,7 +1659,7 @@ static cudaError_t launch_kernels(Pool& P, AttnArgs a, const SlotArgs& sa, int m
   }
   if (smem > kMaxAttnSmem) return cudaErrorInvalidConfiguration;
   a.paged = paged ? 1 : 0;
-  a.lrow = (P.pv.G + 2) * kChunk;
+  a.lrow = P.pv.G * kChunk;
   a.nwarps = P.sm_count * kWarpsPerSm;
   const dim3 grid(P.sm_count * (kWarpsPerSm / w)), block(32 * w);
   cudaError_t e;
@@ -1736,7 +1746,7 @@ StaticLayout static_layout(int n_units, int G, int max_tokens, int update_scores
   L.part = off;
   off = round256(off + (size_t)n_units * L.max_parts * part_stride(G) * sizeof(float));
   L.logit = off;
-  if (update_scores) off += (size_t)n_units * L.max_chunks * (G + 2) * kChunk * sizeof(float);
+  if (update_scores) off += (size_t)n_units * L.max_chunks * G * kChunk * sizeof(float);
   L.total = off;
   return L;
 }

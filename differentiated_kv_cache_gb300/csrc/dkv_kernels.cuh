@@ -13,8 +13,8 @@ constexpr int kChunk = 16;         // decode-attention tokens per mma chunk
 constexpr int kAttnWarps = 4;      // warps per decode-attention CTA
 constexpr int kVictimWarps = 8;    // warps of an attention epilogue block, each leaving a victim-key partial
 // Decode-attention scratch row per 16-slot chunk (floats): the log2-domain
-// logits [query < G][16 slots], then (paged path) the scores before the
-// update [16 slots] at row G and the chunk's page ID at row G + 1.
+// logits [query < G][16 slots]; the epilogue takes the scores before the
+// update and the page IDs from the pages themselves.
 
 // One slot write of a generation-phase step.
 // src: the new token, or a stored token of tier src_tier at slot src_slot,
@@ -153,7 +153,7 @@ struct Scratch {
   int* darrive;         // [units] scan CTAs arrived (zero between calls)
   // decode attention
   float* apart;         // [units][max_splits][G*(128+2)]
-  float* alogit;        // [units][max_chunks][(G + 2) * 16]: per chunk logits, old scores, page ID
+  float* alogit;        // [units][max_chunks][G * 16]: per chunk logits
   float* alse;          // [units][G]
   int nkb_cap, grant_cap, max_splits, max_chunks, max_scan;
 };

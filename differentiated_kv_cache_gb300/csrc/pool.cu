@@ -216,7 +216,7 @@ int dkv_pool_create(const dkv_config* cfg, int cuda_device, dkv_pool** out) {
   A(&s.dscan, units * s.max_scan);
   A(&s.darrive, units);
   A(&s.apart, units * s.max_splits * (G * kD + 2 * kMaxG));
-  A(&s.alogit, units * s.max_chunks * (G + 2) * kChunk);
+  A(&s.alogit, units * s.max_chunks * G * kChunk);
   A(&s.alse, units * G);
   if (e == cudaSuccess) e = cudaMemset(s.darrive, 0, units * sizeof(int));
   // stamps -1: no head has victim keys yet

@@ -335,7 +335,7 @@ int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
  * the call's requests: prompt length plus generated tokens, pruned tokens
  * included, not the stored count) and
  * r(x) = x rounded up to 256, the call needs r(4UG) + r(4U(C/8 + 2)(128G + 16))
- * bytes, plus 64(G + 2)UC if update_scores != 0. A larger call returns
+ * bytes, plus 64GUC if update_scores != 0. A larger call returns
  * DKV_ERR_SCRATCH and queues nothing.
  *
  * Set-up: dkv_pool_create looks up the array's address on the pool's device

@@ -65,7 +65,7 @@ def need_bytes(n_units, G, max_n, update):
     r = lambda x: (x + 255) // 256 * 256
     C = (max_n + 15) // 16 + 1
     b = r(4 * n_units * G) + r(4 * n_units * (C // 8 + 2) * (128 * G + 16))
-    return b + (64 * (G + 2) * n_units * C if update else 0)
+    return b + (64 * G * n_units * C if update else 0)
 
 
 @pytest.mark.parametrize("pb", [4096, 3584, 8192])
