@@ -61,23 +61,23 @@ LAUNCHES = {"prompt": 10, "decode": 3, "attention": 2, "free": 1}
 # makes the bench report null until a new capture replaces the record.
 ATTN_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 119_689_216 + 4_951_040 + 30_590_976,
+    "bytes_per_call": 114_553_600 + 2_715_648 + 26_332_928,
     "sources": {
-        "attention.cu": "aba0ef560a7264eff077da19b8224b65252213fcf16a88c67763fe03177957ba",
+        "attention.cu": "92a66430ffa971dae02789874d67b5aad0a2c7e44241027bbef30153952b3f3a",
         "dkv_common.cuh": "ba5510123ecbe1069424c0470463527dccb53b0444f61c6e606f7028ef848f8c",
-        "dkv_kernels.cuh": "55585a4674a5f894f501562c639d98907e2766ec1b961e0a84fd24bc896b76db",
+        "dkv_kernels.cuh": "ec4d6d05af74cad9f54d34cff8dd36f8a38b036a2e5483df855c71eea66bd45b",
     },
 }
 PROMPT_TRAFFIC = {
     "workload": "llama8b",
-    "bytes_per_call": 1_018_202_624 + 103_041_024,
+    "bytes_per_call": 1_018_318_592 + 103_008_000,
     "sources": {
         "prompt.cu": "112318ce1a431d52729ded02427ab6e7b9e88199071cb46c7cfdd9ec55d07845",
         "prompt_tc.cu": "fa63d0ced7a2f9d8266fe4673083378e67dddf037238d1f050656313a455b8c1",
         "alloc.cu": "3cb94c20d08da98fe7db21a35c9243c2b56696d18fe5239f842f1bd8ca6b512a",
         "dkv_tc.cuh": "acb3452effe630c9cbc898bc8a87929dbf4ecd2f43abeb537319b63ad151c2fb",
         "dkv_common.cuh": "ba5510123ecbe1069424c0470463527dccb53b0444f61c6e606f7028ef848f8c",
-        "dkv_kernels.cuh": "55585a4674a5f894f501562c639d98907e2766ec1b961e0a84fd24bc896b76db",
+        "dkv_kernels.cuh": "ec4d6d05af74cad9f54d34cff8dd36f8a38b036a2e5483df855c71eea66bd45b",
     },
 }
 L2_FLUSH_BYTES = 256 << 20
