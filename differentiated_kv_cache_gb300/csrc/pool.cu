@@ -587,8 +587,13 @@ int dkv_pool_clear_error(dkv_pool* pool) {
   c.error = 0;
   c.error_info = -1;
   if (cudaMemcpy(P.pv.ctl, &c, sizeof(Ctl), cudaMemcpyHostToDevice) != cudaSuccess) return DKV_ERR_CUDA;
-  // a step cut short can leave generation-phase scan or epilogue arrivals behind
+  // a step cut short can leave generation-phase scan arrivals behind, and an
+  // attention call cut short a head's stamps beside partials it did not
+  // finish: the next generation steps scan
   if (cudaMemset(P.sc.darrive, 0, (size_t)P.cfg.max_requests * P.cfg.n_kv_heads * sizeof(int)) != cudaSuccess)
+    return DKV_ERR_CUDA;
+  if (cudaMemset(P.pv.vstamp, 0xff,
+                 (size_t)P.cfg.n_layers * P.cfg.max_requests * P.cfg.n_kv_heads * sizeof(int4)) != cudaSuccess)
     return DKV_ERR_CUDA;
   std::vector<int> rq((size_t)P.cfg.n_layers * P.cfg.max_requests * 4);
   if (cudaMemcpy(rq.data(), P.pv.req, rq.size() * sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)

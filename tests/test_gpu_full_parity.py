@@ -55,7 +55,7 @@ def gpu():
 
 def _compare(gp, op, **kw):
     parity.compare_states(gp.snapshot(), op.snapshot(), gp.t_hi, gp.t_lo, gp.cfg["n_pages"],
-                          gp.cfg["page_bytes"], **kw)
+                          gp.cfg["page_bytes"], table_len=gp.table_len, t_mid=gp.t_mid, **kw)
 
 
 # -------------------------------------------------- prompt, caller scores
@@ -260,15 +260,17 @@ def test_generation_loop_with_score_updates(G, pb):
         _compare(gp, op)
 
 
-def test_benchmark_loop_llama8b():
+@pytest.mark.parametrize("three", [False, True])
+def test_benchmark_loop_llama8b(three):
     """The benchmark's own step on the full llama8b batch: prompt with
     computed scores, then 128 x (compaction, attention with score update).
     At sampled steps the oracle takes over the GPU's state and both run the
-    compaction; the states must be identical."""
+    compaction; the states must be identical. Also with the three-tier pool
+    the benchmark runs as `llama8b+mid` (mid tier K8V2 from 1/N)."""
     name = "llama8b"
     w = workloads.WORKLOADS[name]
     inp = workloads.prompt_inputs(name, 0)
-    cfg = w.pool_config()
+    cfg = w.pool_config(**(workloads.THREE_TIER if three else {}))
     R, H = w.n_requests, w.n_kv_heads
     slots = list(range(R))
     lens = [int(x) for x in inp["lens"]]
@@ -286,7 +288,10 @@ def test_benchmark_loop_llama8b():
         st = gp.status()
         assert st["error"] == 0
         assert int(gp.snapshot(pages=False)["req_state"][0, 0, 3]) == w.decode_steps
-        print(f"llama8b: {len(check)} steps compared; stored hi {st['hi_tokens']} lo {st['lo_tokens']}")
+        print(f"llama8b{'+mid' if three else ''}: {len(check)} steps compared; stored hi {st['hi_tokens']} "
+              f"mid {st['mid_tokens']} lo {st['lo_tokens']}")
+        if three:
+            assert st["mid_tokens"] > 0
 
 
 def test_generation_steps_after_mixed_attention_calls():
