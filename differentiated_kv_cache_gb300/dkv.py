@@ -170,8 +170,8 @@ def dkv_compact_step(pool, layer: int, mode: int, req_slots, seq_lens, k, v, q_o
     slots = _i32(req_slots)
     lens = None if seq_lens is None else _i32(seq_lens)
     rc = load().dkv_compact_step(
-        pool, int(layer), int(mode), int(slots.size), slots.ctypes.data_as(C.c_void_p),
-        None if lens is None else lens.ctypes.data_as(C.c_void_p),
+        pool, int(layer), int(mode), int(slots.size), slots.ctypes.data,
+        None if lens is None else lens.ctypes.data,
         _dptr(k, torch.float16, "k"), _dptr(v, torch.float16, "v"), _dptr(q_obs, torch.float16, "q_obs"),
         _dptr(scores_in, torch.float32, "scores_in"), _dptr(scores_out, torch.float32, "scores_out"),
         _stream(stream))
@@ -185,7 +185,7 @@ def dkv_prefill_attention(pool, seq_lens, q, k, v, out, lse_obs=None, stream=Non
     base-2 log-sum-exps."""
     import torch
     lens = _i32(seq_lens)
-    rc = load().dkv_prefill_attention(pool, int(lens.size), lens.ctypes.data_as(C.c_void_p),
+    rc = load().dkv_prefill_attention(pool, int(lens.size), lens.ctypes.data,
                                       _dptr(q, torch.float16, "q"), _dptr(k, torch.float16, "k"),
                                       _dptr(v, torch.float16, "v"), _dptr(out, torch.float32, "out"),
                                       _dptr(lse_obs, torch.float32, "lse_obs"), _stream(stream))
@@ -200,7 +200,7 @@ def dkv_compact_step_prefilled(pool, layer: int, req_slots, seq_lens, k, v, q_ob
     slots = _i32(req_slots)
     lens = _i32(seq_lens)
     rc = load().dkv_compact_step_prefilled(
-        pool, int(layer), int(slots.size), slots.ctypes.data_as(C.c_void_p), lens.ctypes.data_as(C.c_void_p),
+        pool, int(layer), int(slots.size), slots.ctypes.data, lens.ctypes.data,
         _dptr(k, torch.float16, "k"), _dptr(v, torch.float16, "v"), _dptr(q_obs, torch.float16, "q_obs"),
         _dptr(lse_obs, torch.float32, "lse_obs"), _dptr(scores_out, torch.float32, "scores_out"), _stream(stream))
     return _check(rc, "dkv_compact_step_prefilled") if check else rc
@@ -210,7 +210,7 @@ def dkv_decode_attention(pool, layer: int, req_slots, q, out, update_scores: boo
                          check: bool = True) -> int:
     import torch
     slots = _i32(req_slots)
-    rc = load().dkv_decode_attention(pool, int(layer), int(slots.size), slots.ctypes.data_as(C.c_void_p),
+    rc = load().dkv_decode_attention(pool, int(layer), int(slots.size), slots.ctypes.data,
                                      _dptr(q, torch.float16, "q"), _dptr(out, torch.float32, "out"),
                                      int(bool(update_scores)), _stream(stream))
     return _check(rc, "dkv_decode_attention") if check else rc
@@ -223,7 +223,7 @@ def dkv_decode_attention_static(pool, layer: int, req_slots, q, out, update_scor
     device memory). Calls that overlap on the GPU race on the array."""
     import torch
     slots = _i32(req_slots)
-    rc = load().dkv_decode_attention_static(pool, int(layer), int(slots.size), slots.ctypes.data_as(C.c_void_p),
+    rc = load().dkv_decode_attention_static(pool, int(layer), int(slots.size), slots.ctypes.data,
                                             _dptr(q, torch.float16, "q"), _dptr(out, torch.float32, "out"),
                                             int(bool(update_scores)), _stream(stream))
     return _check(rc, "dkv_decode_attention_static") if check else rc
@@ -233,15 +233,15 @@ def dkv_pool_set_thresholds(pool, layer: int, alpha_h, alpha_l, stream=None, che
     """Per-KV-head thresholds of one layer (host arrays of n_kv_heads floats)."""
     ah = np.ascontiguousarray(alpha_h, dtype=np.float32)
     al = np.ascontiguousarray(alpha_l, dtype=np.float32)
-    rc = load().dkv_pool_set_thresholds(pool, int(layer), ah.ctypes.data_as(C.c_void_p),
-                                        al.ctypes.data_as(C.c_void_p), _stream(stream))
+    rc = load().dkv_pool_set_thresholds(pool, int(layer), ah.ctypes.data,
+                                        al.ctypes.data, _stream(stream))
     return _check(rc, "dkv_pool_set_thresholds") if check else rc
 
 
 def dkv_pool_set_mid_thresholds(pool, layer: int, alpha_m, stream=None, check: bool = True) -> int:
     """Per-KV-head thresholds of the mid tier of one layer (n_kv_heads floats)."""
     am = np.ascontiguousarray(alpha_m, dtype=np.float32)
-    rc = load().dkv_pool_set_mid_thresholds(pool, int(layer), am.ctypes.data_as(C.c_void_p), _stream(stream))
+    rc = load().dkv_pool_set_mid_thresholds(pool, int(layer), am.ctypes.data, _stream(stream))
     return _check(rc, "dkv_pool_set_mid_thresholds") if check else rc
 
 
@@ -274,7 +274,7 @@ def dkv_pool_export(pool, cfg: dict, table_len: int, pages: bool = True, count_s
         pointers=np.zeros(2, np.int64))
     snap = dkv_snapshot()
     for name in ("free_list", "table", "head_counts", "req_state", "pointers"):
-        setattr(snap, name, out[name].ctypes.data_as(C.c_void_p))
-    snap.pages = out["pages"].ctypes.data_as(C.c_void_p) if pages else None
+        setattr(snap, name, out[name].ctypes.data)
+    snap.pages = out["pages"].ctypes.data if pages else None
     _check(load().dkv_pool_export(pool, C.byref(snap)), "dkv_pool_export")
     return out
