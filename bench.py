@@ -63,7 +63,7 @@ ATTN_TRAFFIC = {
     "workload": "llama8b",
     "bytes_per_call": 114_553_600 + 2_715_648 + 26_332_928,
     "sources": {
-        "attention.cu": "92a66430ffa971dae02789874d67b5aad0a2c7e44241027bbef30153952b3f3a",
+        "attention.cu": "4787725370c06619bafc550a320ea946f0b37b4ab4c2c0246628090ae0b54317",
         "dkv_common.cuh": "ba5510123ecbe1069424c0470463527dccb53b0444f61c6e606f7028ef848f8c",
         "dkv_kernels.cuh": "ec4d6d05af74cad9f54d34cff8dd36f8a38b036a2e5483df855c71eea66bd45b",
     },

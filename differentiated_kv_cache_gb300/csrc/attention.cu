@@ -113,7 +113,7 @@ struct AttnArgs {
   int nwarps;         // warps of the attention grid
   int update;
   int layer;
-  int paged;          // 1: logit rows also carry the old scores and the page ID (paged path)
+  int paged;          // 1: pages hold whole 16-slot chunks (k_attn_paged), 0: any geometry (k_attn_decode)
   int mseg;           // chunked: bytes per page meta segment in the stage
   int maxp;           // chunked: pages a chunk can touch
   int stage_bytes;
@@ -1718,9 +1718,9 @@ cudaError_t launch_attention(Pool& P, int layer, const SlotArgs& sa, int max_tok
 // Allocation-free variant (dkv_decode_attention_static). The same kernels
 // work in one fixed device array instead of the pool's scratch: the per-head
 // lse2, the per-warp partials and, with score updates, the per-chunk rows of
-// logits, old scores and page IDs. The array is part of this library's device image; the
-// CUDA driver reserves it when the module is loaded, so no call here
-// allocates. Every call shares it and it keeps the last call's contents.
+// logits. The array is part of this library's device image; the CUDA driver
+// reserves it when the module is loaded, so no call here allocates. Every
+// call shares it and it keeps the last call's contents.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_attn_static_scratch[DKV_ATTN_STATIC_SCRATCH_BYTES];
 

@@ -345,8 +345,8 @@ int dkv_decode_attention(dkv_pool* pool, int32_t layer, int32_t n_req,
  * pools from before a reset are unusable anyway. Every call on a device
  * shares the array and it keeps the last call's contents; nothing in it has
  * to start at zero, because every value a call reads from the array
- * (partials and the per-chunk rows of logits, old scores and page IDs) is
- * written earlier in the same call.
+ * (partials and the per-chunk rows of logits) is written earlier in the
+ * same call.
  * This entry point leaves no victim keys for the next generation step, which
  * then searches the heads itself (same result, more work).
  * Calls that overlap on the GPU (on different streams, or from different
