@@ -364,7 +364,8 @@ class Loop:
              "alone_ms": statistics.mean(ms(rec["attn_alone"]))}
         # in the loop: (compaction + attention) of the odd steps less the
         # compaction alone of the even steps
-        r["loop_ms"] = statistics.mean(ms(rec["pair"])) - r["compact_ms"] if rec["pair"] else r["alone_ms"]
+        r["pair_ms"] = statistics.mean(ms(rec["pair"])) if rec["pair"] else r["compact_ms"] + r["alone_ms"]
+        r["loop_ms"] = r["pair_ms"] - r["compact_ms"] if rec["pair"] else r["alone_ms"]
         r["attn_bytes"] = sum(self.bytes_per_attn) / len(self.bytes_per_attn)
         return r
 
@@ -386,6 +387,9 @@ class Loop:
             "compact_step_prompt_gbs": round(p, 1), "compact_step_prompt_frac": round(p / peak, 4),
             "compact_step_prompt_bytes": int(self.pbytes),
             "compact_step_decode_us_per_layer": round(r["compact_ms"] * 1e3, 2),
+            # one generation step of the decode loop: compaction and the
+            # attention call with score update, timed as one (odd steps)
+            "generation_step_us": round(r["pair_ms"] * 1e3, 2),
             "stored_tokens_after_prompt": {"hi": pc[1], "lo": pc[2], "pruned": self.n_th - pc[1] - pc[2] - pc[3],
                                            **({"mid": pc[3]} if self.mid else {})},
             "kv_bytes_vs_fp16": round((HI_BYTES * pc[1] + LO_BYTES * pc[2] + MID_BYTES * pc[3]) / (self.n_th * 512),
