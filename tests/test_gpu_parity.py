@@ -374,6 +374,135 @@ def test_grant_short_with_zero_slack():
             assert (before[key] == after[key]).all(), key
 
 
+def test_argument_errors_queue_nothing_and_length_limit():
+    """Calls the host refuses (empty calls, a slot given twice or out of
+    range, prompts of 0 tokens or longer than max_seq_len, a layer out of
+    range, a misaligned tensor, arguments of the other mode, inactive slots)
+    return their code at once, change nothing and latch nothing. A request
+    grown to exactly max_seq_len by generation steps matches the oracle bit
+    for bit, its next step is refused on both sides as a whole (the other
+    request of the call does not step either), and attention over it stays
+    within the element-wise bound."""
+    import differentiated_kv_cache_gb300 as dkv
+    L = 300
+    cfg = cfg_of(max_seq_len=L, n_pages=1024)
+    H, G = cfg["n_kv_heads"], cfg["group_size"]
+    lens, slots = [L - 3, 40, L], [5, 0, 3]
+    n = sum(lens)
+    k = workloads.random_fp16((n, H, 128), 31)
+    v = workloads.random_fp16((n, H, 128), 32)
+    S = workloads.given_scores(n, H, seed=33)
+    E_ARG, E_STATE = dkv.DKV_ERR_ARG, dkv.DKV_ERR_STATE
+    P, D = dkv.DKV_PROMPT, dkv.DKV_DECODE
+    gp, op = both(cfg)
+    with gp:
+        kd, vd, sd = gp.dev(k), gp.dev(v), gp.dev(S.astype(np.float32))
+        kn, vn = gp.dev(k[:3]), gp.dev(v[:3])
+        q = gp.dev(workloads.random_fp16((3, H * G, 128), 34))
+        out = torch.zeros((3, H * G, 128), dtype=torch.float32, device="cuda")
+        before = gp.snapshot()
+
+        def refused(rc, want, what):
+            assert rc == want, (what, rc)
+
+        for layer, sl, ln, what in [(0, [], [], "empty call"), (0, [1, 1], [10, 10], "slot twice"),
+                                    (0, [6], [10], "slot = max_requests"), (0, [-1], [10], "negative slot"),
+                                    (0, [1], [0], "empty prompt"), (0, [1], [L + 1], "beyond max_seq_len"),
+                                    (1, [1], [10], "layer out of range")]:
+            refused(dkv.dkv_compact_step(gp.h, layer, P, sl, ln, kd, vd, None, sd, check=False), E_ARG, what)
+        refused(dkv.dkv_compact_step(gp.h, 0, P, [1], [10], kd.reshape(-1)[1:], vd, None, sd, check=False),
+                E_ARG, "keys 2 bytes past a 16-byte boundary")
+        refused(dkv.dkv_compact_step(gp.h, 0, P, [1], [10], kd, vd, None, None, check=False), E_ARG,
+                "prompt without observation queries or scores")
+        refused(dkv.dkv_compact_step(gp.h, 0, 7, [1], [10], kd, vd, None, sd, check=False), E_ARG, "mode 7")
+        refused(dkv.dkv_compact_step(gp.h, 0, D, [1], [10], kn, vn, check=False), E_ARG, "lengths in DECODE")
+        refused(dkv.dkv_compact_step(gp.h, 0, D, [], None, kn, vn, check=False), E_ARG, "empty generation step")
+        refused(dkv.dkv_compact_step(gp.h, 0, D, [1], None, kn, vn, check=False), E_STATE, "inactive slot")
+        refused(dkv.dkv_decode_attention(gp.h, 0, [], q, out, True, check=False), E_ARG, "empty attention call")
+        refused(dkv.dkv_decode_attention(gp.h, 0, [2], q, out, True, check=False), E_STATE, "attention, inactive")
+        refused(dkv.dkv_free_request(gp.h, 6, check=False), E_ARG, "free, slot out of range")
+        refused(dkv.dkv_free_request(gp.h, 2, check=False), E_STATE, "free, inactive slot")
+        torch.cuda.synchronize()
+        after = gp.snapshot()
+        for key in ("free_list", "table", "head_counts", "req_state", "pointers"):
+            assert (before[key] == after[key]).all(), key
+        assert gp.status()["error"] == 0
+
+        # a request at max_seq_len - 3, another at max_seq_len itself
+        gp.prompt(0, slots, lens, k, v, scores_in=S)
+        assert op.prompt(0, slots, lens, k, v, scores_in=S) == 0
+        assert_same(gp, op)
+        assert gp.decode(0, [3], k[:1], v[:1], check=False) == E_ARG
+        assert op.decode(0, [3], k[:1], v[:1]) == E_ARG
+        for step in range(4):
+            kn = workloads.random_fp16((2, H, 128), 40 + step)
+            vn = workloads.random_fp16((2, H, 128), 50 + step)
+            want = 0 if step < 3 else E_ARG
+            assert gp.decode(0, [5, 0], kn, vn, check=False) == want
+            assert op.decode(0, [5, 0], kn, vn) == want
+            assert_same(gp, op)
+        assert gp.status()["error"] == 0
+        qa = workloads.random_fp16((3, H * G, 128), 35, scale=2.0)
+        got = gp.attention(0, slots, qa, update=False)
+        rc, ref = op.attention(0, slots, qa, update_scores=False)
+        assert rc == 0
+        ok, worst = parity.within(got.astype(np.float64), ref, ATT_ATOL, ATT_RTOL)
+        assert ok, worst
+        for s in slots:
+            gp.free(s)
+            assert op.free_request(s) == 0
+        assert_same(gp, op)
+        assert gp.status()["free_pages"] == cfg["n_pages"]
+
+
+def test_largest_call():
+    """The most requests one call takes (1024, so 2048 heads: the single-CTA
+    page allocation of a generation step then holds two heads a thread):
+    prompt, three generation steps and request completion bit-exact, the
+    attention call within the element-wise bound; a call of 1025 requests
+    is refused on the host."""
+    import differentiated_kv_cache_gb300 as dkv
+    R = 1024
+    cfg = cfg_of(max_requests=R, max_seq_len=64, n_pages=12000)
+    H, G = cfg["n_kv_heads"], cfg["group_size"]
+    lens = [int(x) for x in np.random.default_rng(61).integers(1, 49, R)]
+    slots = [int(s) for s in np.random.default_rng(62).permutation(R)]
+    n = sum(lens)
+    k = workloads.random_fp16((n, H, 128), 63)
+    v = workloads.random_fp16((n, H, 128), 64)
+    S = workloads.given_scores(n, H, seed=65)
+    gp, op = both(cfg)
+    with gp:
+        gp.prompt(0, slots, lens, k, v, scores_in=S)
+        assert op.prompt(0, slots, lens, k, v, scores_in=S) == 0
+        assert_same(gp, op)
+        for step in range(3):
+            kn = workloads.random_fp16((R, H, 128), 70 + step)
+            vn = workloads.random_fp16((R, H, 128), 80 + step)
+            gp.decode(0, slots, kn, vn)
+            assert op.decode(0, slots, kn, vn) == 0
+            assert_same(gp, op)
+        q = workloads.random_fp16((R, H * G, 128), 66, scale=2.0)
+        got = gp.attention(0, slots, q, update=False)
+        rc, ref = op.attention(0, slots, q, update_scores=False)
+        assert rc == 0
+        ok, worst = parity.within(got.astype(np.float64), ref, ATT_ATOL, ATT_RTOL)
+        assert ok, worst
+        for s in slots[:R // 2]:
+            gp.free(s)
+            assert op.free_request(s) == 0
+        assert_same(gp, op)
+        assert gp.status()["error"] == 0
+    with GPool(cfg_of(max_requests=R + 1, max_seq_len=64, n_pages=64)) as big:
+        kd = big.dev(workloads.random_fp16((R + 1, H, 128), 67))
+        q = big.dev(workloads.random_fp16((R + 1, H * G, 128), 68))
+        out = torch.zeros((R + 1, H * G, 128), dtype=torch.float32, device="cuda")
+        assert dkv.dkv_compact_step(big.h, 0, dkv.DKV_PROMPT, list(range(R + 1)), [1] * (R + 1), kd, kd, None,
+                                    big.dev(np.ones((R + 1, H), np.float32)), check=False) == dkv.DKV_ERR_ARG
+        assert dkv.dkv_decode_attention(big.h, 0, list(range(R + 1)), q, out, False, check=False) == \
+            dkv.DKV_ERR_ARG
+
+
 def test_attention_on_workload_with_outliers():
     """The tiny workload itself (outlier channels x8, scores computed from the
     observation queries), a few decode steps with score updates: attention
