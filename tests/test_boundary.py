@@ -75,3 +75,14 @@ def test_create_without_gpu_fails_cleanly():
     cfg = dkv.make_config(n_layers=1, n_kv_heads=2, group_size=4, n_pages=16, max_requests=2, max_seq_len=64)
     with pytest.raises(dkv.DkvError):
         dkv.dkv_pool_create(cfg, 0)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library the binding raises; nothing falls back."""
+    monkeypatch.setattr(dkv.build, "LIB", str(tmp_path / "absent" / "libdkv.so"))
+    monkeypatch.setattr(dkv.dkv, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        dkv.load()
+    with pytest.raises(RuntimeError, match="not built"):
+        dkv.dkv_pool_create(dkv.make_config(n_layers=1, n_kv_heads=2, group_size=4, n_pages=16, max_requests=2,
+                                            max_seq_len=64), 0)
