@@ -865,7 +865,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--dry-run", action="store_true", help="rank start-up and reductions only (gloo, no GPU)")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu DRAM bytes per decode_attention launch, when known for this build")
+                    help="ncu DRAM bytes per decode_attention launch, when known for the current kernel sources")
     args = ap.parse_args()
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         sys.exit(launch_ranks(args.gpus))
